@@ -1,0 +1,440 @@
+"""Benchmark of the KV-cache eviction path on one GB300 (or N, one process each).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+
+One step is the whole path over one batch of synthetic input: observation-window
+scoring, HubKV refinement, Top-K and compaction of every (batch row x layer x KV
+head), then the workload's H2O decode steps on the compacted cache.  The default
+workload is the 128K long-context one (1 x 32 layers, 32 query / 8 KV heads,
+d = 128, T = 131072, bf16, 5% budget incl. 64 recent, then 128 decode steps); it
+is the workload that exercises all five operations at full size.
+
+Prints one JSON line (rank 0).  `value` is KV tokens (batch rows x layers x
+prompt tokens) scored + selected + compacted per second over whole steps, summed
+over ranks; `decode` reports H2O decode steps per second; `roofline` is the
+dominant kernel's achieved bandwidth against the measured HBM copy peak;
+`cpu_baseline` times the float64 oracle on a bounded sample on the host cores.
+Under torchrun every rank runs its own full workload (weak scaling, no
+collective on the data path); rank 0 reports the max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KV tokens scored+selected+compacted/s; H2O decode steps/s; % HBM roofline"
+UNIT = "KV tokens/s"
+L2_BYTES = 129 * 2 ** 20
+
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="long-context")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work per step (bytes that any implementation must move)
+# ---------------------------------------------------------------------------
+def algorithmic_bytes(wl):
+    eb = wl.elem_bytes
+    units = wl.units
+    q_bytes = wl.rows * wl.Hq * wl.W * wl.d * eb
+    k_bytes = units * wl.T * wl.d * eb
+    s_bytes = units * wl.T * 4
+    score = q_bytes + k_bytes + s_bytes                    # read Q, K; write s
+    refine = 2 * s_bytes if wl.r is not None else 0        # read s, write z
+    select = s_bytes + units * wl.k * 4                    # read z, write idx
+    row = wl.d * eb
+    compact = units * wl.k * (4 * row + 4 + 4 + 4 + 4)     # K,V rows read+written; idx, s, pos, acc
+    decode_step = units * wl.cap * (2 * row + 4 + 4 + 4) + wl.rows * (wl.Hq * wl.d * (eb + 4)
+                                                                    + 2 * wl.Hkv * row)
+    return {"kv_score_obs": score, "hubkv_refine": refine, "kv_select_topk": select,
+            "kv_compact": compact, "h2o_decode_step": decode_step}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                self.out = ""
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# the GPU path
+# ---------------------------------------------------------------------------
+class Pipeline:
+    """Preallocated buffers for one workload; step() enqueues the whole path."""
+
+    def __init__(self, wl, device):
+        import torch
+
+        from kv_cache_compression_obs_gb300 import api, gen
+
+        self.api, self.wl, self.dev = api, wl, device
+        self.Q, self.K, self.V = gen.prefill_inputs(wl, device=device)
+        units_shape = (wl.rows, wl.Hkv)
+        f32, i32 = torch.float32, torch.int32
+        self.s = torch.empty(*units_shape, wl.T, dtype=f32, device=device)
+        self.z = torch.empty_like(self.s) if wl.r is not None else self.s
+        self.beta = torch.empty(*units_shape, dtype=f32, device=device)
+        self.idx = torch.empty(*units_shape, wl.k, dtype=i32, device=device)
+        dt = self.K.dtype
+        self.Kc = torch.empty(*units_shape, wl.cap, wl.d, dtype=dt, device=device)
+        self.Vc = torch.empty_like(self.Kc)
+        self.pos = torch.empty(*units_shape, wl.cap, dtype=i32, device=device)
+        self.acc = torch.empty(*units_shape, wl.cap, dtype=f32, device=device)
+        self.len = torch.empty(*units_shape, dtype=i32, device=device)
+        self.o = torch.empty(wl.rows, wl.Hq, wl.d, dtype=f32, device=device)
+        self.ev = torch.empty(*units_shape, dtype=i32, device=device)
+        ws = max(api.kv_workspace_size(api.KV_OP_SCORE_OBS, wl.rows, wl.Hq, wl.Hkv, wl.T, wl.d, wl.W),
+                 api.kv_workspace_size(api.KV_OP_HUBKV_REFINE, wl.rows, wl.Hkv, wl.Hkv, wl.T), 256)
+        self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
+        steps = [gen.decode_inputs(wl, t, device=device) for t in range(wl.n_decode)]
+        self.dq = [x[0] for x in steps]
+        self.dk = [x[1] for x in steps]
+        self.dv = [x[2] for x in steps]
+
+    def prefill(self, stream=None):
+        a, wl = self.api, self.wl
+        a.kv_score_obs(self.Q, self.K, wl.scale, out=self.s, workspace=self.ws, stream=stream)
+        if wl.r is not None:
+            a.hubkv_refine(self.s, wl.r, wl.gamma, wl.pool_width, wl.beta_lo, wl.beta_hi,
+                           out=self.z, beta_out=self.beta, workspace=self.ws, stream=stream)
+        a.kv_select_topk(self.z, wl.k, wl.R, out=self.idx, stream=stream)
+        a.kv_compact(self.K, self.V, self.s, self.idx, wl.cap, K_out=self.Kc, V_out=self.Vc,
+                     pos_out=self.pos, acc_out=self.acc, len_out=self.len, stream=stream)
+
+    def decode(self, t, stream=None):
+        wl = self.wl
+        self.api.h2o_decode_step(self.dq[t], self.dk[t], self.dv[t], self.Kc, self.Vc, self.pos,
+                                 self.acc, self.len, wl.R, wl.T + t, wl.scale, o_out=self.o,
+                                 evicted_out=self.ev, stream=stream)
+
+    def step(self, stream=None):
+        self.prefill(stream)
+        for t in range(self.wl.n_decode):
+            self.decode(t, stream)
+
+    def timed_phases(self):
+        """One step with events between the phases: ms per phase."""
+        import torch
+        a, wl = self.api, self.wl
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        ev[0].record()
+        a.kv_score_obs(self.Q, self.K, wl.scale, out=self.s, workspace=self.ws)
+        ev[1].record()
+        if wl.r is not None:
+            a.hubkv_refine(self.s, wl.r, wl.gamma, wl.pool_width, wl.beta_lo, wl.beta_hi,
+                           out=self.z, beta_out=self.beta, workspace=self.ws)
+        ev[2].record()
+        a.kv_select_topk(self.z, wl.k, wl.R, out=self.idx)
+        ev[3].record()
+        a.kv_compact(self.K, self.V, self.s, self.idx, wl.cap, K_out=self.Kc, V_out=self.Vc,
+                     pos_out=self.pos, acc_out=self.acc, len_out=self.len)
+        ev[4].record()
+        for t in range(wl.n_decode):
+            self.decode(t)
+        ev[5].record()
+        torch.cuda.synchronize()
+        names = ["kv_score_obs", "hubkv_refine", "kv_select_topk", "kv_compact", "h2o_decode_step"]
+        ms = {n: ev[i].elapsed_time(ev[i + 1]) for i, n in enumerate(names)}
+        if wl.n_decode:
+            ms["h2o_decode_step"] /= wl.n_decode  # per decode step
+        return ms
+
+
+def launch_count():
+    from kv_cache_compression_obs_gb300 import api
+    return int(api.library_handle().kv_launch_count())
+
+
+def run_e2e(wl, pipe, steps):
+    """Same metric through the public API with pinned host inputs copied in and the
+    kept positions and decode outputs copied back, inside the timed region."""
+    import torch
+    hQ = pipe.Q.cpu().pin_memory()
+    hK = pipe.K.cpu().pin_memory()
+    hV = pipe.V.cpu().pin_memory()
+    hdq = [t.cpu().pin_memory() for t in pipe.dq]
+    hdk = [t.cpu().pin_memory() for t in pipe.dk]
+    hdv = [t.cpu().pin_memory() for t in pipe.dv]
+    out_idx = torch.empty(pipe.idx.shape, dtype=torch.int32).pin_memory()
+    out_o = torch.empty(pipe.o.shape, dtype=torch.float32).pin_memory()
+    out_ev = torch.empty((wl.n_decode,) + tuple(pipe.ev.shape), dtype=torch.int32).pin_memory()
+    h2d = (hQ.numel() * hQ.element_size() + hK.numel() * hK.element_size()
+           + hV.numel() * hV.element_size()
+           + sum(t.numel() * t.element_size() for t in hdq + hdk + hdv))
+    d2h = (out_idx.numel() * 4 + out_o.numel() * 4 + out_ev.numel() * 4)
+
+    def one():
+        pipe.Q.copy_(hQ, non_blocking=True)
+        pipe.K.copy_(hK, non_blocking=True)
+        pipe.V.copy_(hV, non_blocking=True)
+        for t in range(wl.n_decode):
+            pipe.dq[t].copy_(hdq[t], non_blocking=True)
+            pipe.dk[t].copy_(hdk[t], non_blocking=True)
+            pipe.dv[t].copy_(hdv[t], non_blocking=True)
+        pipe.prefill()
+        out_idx.copy_(pipe.idx, non_blocking=True)
+        for t in range(wl.n_decode):
+            pipe.decode(t)
+            out_ev[t].copy_(pipe.ev, non_blocking=True)
+        out_o.copy_(pipe.o, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    dt = (time.perf_counter() - t0) / steps
+    return dt, h2d, d2h
+
+
+def cpu_baseline(wl, pipe, budget_s=20.0):
+    """The float64 oracle as it stands, on one batch row of the workload, on the host cores."""
+    import numpy as np
+
+    import oracle
+    from kv_cache_compression_obs_gb300 import gen
+
+    cores = os.cpu_count() or 1
+    row = slice(0, 1)
+    Qh = gen.to_numpy_bits(pipe.Q[row])
+    Kh = gen.to_numpy_bits(pipe.K[row])
+    Vh = gen.to_numpy_bits(pipe.V[row])
+    t0 = time.perf_counter()
+    s = oracle.score_obs(Qh, Kh, wl.scale)
+    z = oracle.hubkv_refine(s, wl.r, wl.gamma, wl.pool_width, wl.beta_lo, wl.beta_hi)[0] \
+        if wl.r is not None else s
+    idx = oracle.select_topk(z, wl.k, wl.R)
+    Kc, Vc, pos, acc, ln = oracle.compact(Kh, Vh, s, idx, wl.cap)
+    t_prefill = time.perf_counter() - t0
+    n_dec = 0
+    t1 = time.perf_counter()
+    for t in range(wl.n_decode):
+        if time.perf_counter() - t0 > budget_s:
+            break
+        q, kn, vn = (gen.to_numpy_bits(x[row]) for x in (pipe.dq[t], pipe.dk[t], pipe.dv[t]))
+        oracle.decode_step(q, kn, vn, Kc, Vc, pos, acc, ln, wl.R, wl.T + t, wl.scale)
+        n_dec += 1
+    t_dec = time.perf_counter() - t1
+    per_step_dec = t_dec / max(n_dec, 1)
+    # a whole step for this row: prefill + all decode steps (decode time extrapolated per step)
+    t_row = t_prefill + per_step_dec * wl.n_decode
+    tokens = 1 * wl.T
+    return {"value": tokens / t_row, "unit": UNIT, "cores": int(os.environ.get("OMP_NUM_THREADS", cores)),
+            "kind": "oracle",
+            "sample": (f"batch row 0 of {wl.rows} ({wl.Hkv} KV heads, T={wl.T}): score+refine+Top-K+"
+                       f"compact in {t_prefill:.2f} s, {n_dec} of {wl.n_decode} decode steps timed "
+                       f"({per_step_dec * 1e3:.1f} ms each)"),
+            "decode_steps_per_s": 1.0 / per_step_dec if n_dec else None}
+
+
+def run_ours(args, wl, rank, world):
+    import torch
+    import torch.distributed as dist
+
+    local = _env_int("LOCAL_RANK", 0)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pipe = Pipeline(wl, dev)
+    torch.cuda.synchronize()
+    for _ in range(max(args.warmup, 0)):
+        pipe.step()
+    torch.cuda.synchronize()
+    phases = pipe.timed_phases()
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        e0.record()
+        for _ in range(args.steps):
+            pipe.step()
+        e1.record()
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    launches = launch_count() - launches0
+    ms = e0.elapsed_time(e1) / args.steps
+    ms_t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms_max = float(ms_t.item())
+
+    tokens = wl.rows * wl.T
+    value = world * tokens / (ms_max / 1e3)
+    peak, peak_kind = measured_peaks()
+    alg = algorithmic_bytes(wl)
+    per_launch = {k: alg[k] for k in alg}
+    dom = max(phases, key=lambda n: phases[n] * (wl.n_decode if n == "h2o_decode_step" else 1))
+    achieved = per_launch[dom] / (phases[dom] / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": wl.name, "batch": wl.B, "layers": wl.L, "q_heads": wl.Hq,
+                   "kv_heads": wl.Hkv, "d_head": wl.d, "prompt": wl.T, "obs_window": wl.W,
+                   "budget_k": wl.k, "recent": wl.R, "r": wl.r, "gamma": wl.gamma,
+                   "decode_steps": wl.n_decode, "parallelism": f"replica x{world}",
+                   "l2": f"inputs larger than L2 (K+V {2 * wl.units * wl.T * wl.d * wl.elem_bytes / 1e9:.1f} GB)"},
+        "decode": {"steps_per_s": (1e3 / phases["h2o_decode_step"]) if wl.n_decode else None,
+                   "ms_per_decode_step": phases["h2o_decode_step"] if wl.n_decode else None},
+        "phases_ms": phases,
+        "gpu_launches": launches,
+        "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "algorithmic_bytes": per_launch[dom], "traffic": None},
+        "clocks": clk.summary(),
+    }
+    if not args.no_e2e:
+        dt, h2d, d2h = run_e2e(wl, pipe, min(args.steps, 2))
+        line["e2e"] = {"value": world * tokens / dt, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                       "d2h_bytes_per_step": d2h}
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, pipe)
+    return line
+
+
+def run_reference(args, wl):
+    """The oracle as the reference arm: a bounded sample per step on the host cores."""
+    import torch
+
+    from kv_cache_compression_obs_gb300 import gen
+
+    class HostPipe:
+        pass
+
+    p = HostPipe()
+    p.Q, p.K, p.V = gen.prefill_inputs(wl.scaled(B=1, L=1), device="cpu")
+    steps_in = [gen.decode_inputs(wl.scaled(B=1, L=1), t, device="cpu") for t in range(wl.n_decode)]
+    p.dq = [x[0] for x in steps_in]
+    p.dk = [x[1] for x in steps_in]
+    p.dv = [x[2] for x in steps_in]
+    for _ in range(max(args.warmup, 0)):
+        cpu_baseline(wl.scaled(B=1, L=1), p, budget_s=0.0)
+    vals = []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(wl.scaled(B=1, L=1), p, budget_s=10.0))
+    dt = time.perf_counter() - t0
+    v = statistics.median(x["value"] for x in vals)
+    cb = dict(vals[-1])
+    cb["value"] = v
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": wl.name, "batch": wl.B, "layers": wl.L, "q_heads": wl.Hq,
+                       "kv_heads": wl.Hkv, "d_head": wl.d, "prompt": wl.T, "obs_window": wl.W,
+                       "budget_k": wl.k, "recent": wl.R, "decode_steps": wl.n_decode},
+            "cpu_baseline": cb,
+            "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    from kv_cache_compression_obs_gb300 import configs
+
+    wl = configs.BY_NAME[args.config]
+    rank, world = _env_int("RANK", 0), _env_int("WORLD_SIZE", 1)
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, wl)), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(_env_int("LOCAL_RANK", 0))
+        dist.init_process_group("nccl")
+    line = run_ours(args, wl, rank, world)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

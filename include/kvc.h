@@ -1,0 +1,209 @@
+/*
+ * kvc.h -- C ABI of libkvc.so, GB300 (sm_103a) KV-cache token eviction.
+ *
+ * The eviction path has five operations; each is one call here:
+ *   kv_score_obs     observation-window attention mass per cached token
+ *   hubkv_refine     HubKV score refinement before Top-K
+ *   kv_select_topk   budgeted per-head Top-K with a protected recent window
+ *   kv_compact       gather-compaction of the kept K/V rows into a slot cache
+ *   h2o_decode_step  one decode step: attention, score accumulation, <= 1 eviction
+ *
+ * Sources (page title, section):
+ *   [H2O]    "H2O 完全拆解：抓住 KV Cache 里的「重击者」，20% 预算无损生成（NeurIPS 2023）"
+ *   [HubKV]  "HubKV walkthrough"
+ *   [KVblog] the KV-cache survey blog (famous-torrone-8bc255.netlify.app/posts/kv_cache)
+ *
+ * Conventions shared by every call
+ *   - Every pointer argument is DEVICE memory owned by the caller (allocate it
+ *     with cudaMalloc or a framework allocator), 16-byte aligned.  The library
+ *     never allocates, frees or synchronises; it only enqueues kernels on
+ *     `stream` (a cudaStream_t passed as void*, NULL = legacy default stream).
+ *   - Tensors are dense, row-major, the head dimension fastest and the head
+ *     index outside the token index: K is [B][Hkv][T][d], so one head's keys
+ *     are one contiguous T x d block.  Layers are independent: a caller with L
+ *     layers folds them into B.
+ *   - `dtype` is KV_BF16 (bf16 storage, fp32 arithmetic) or KV_F32; it applies
+ *     to Q, K, V, q, k_new, v_new and the caches.  Scores, accumulators and
+ *     attention outputs are always float32.  d (head dimension) is 64 or 128.
+ *   - Inputs must be finite; the kernels do not check (a check would cost a
+ *     full extra pass over K).
+ *   - Return value: KV_OK when the work was enqueued.  Argument errors
+ *     (KV_ERR_INVALID_ARG, KV_ERR_UNSUPPORTED, KV_ERR_WORKSPACE) are returned
+ *     before anything is launched and leave every output untouched.  A launch
+ *     failure returns KV_ERR_CUDA.  Errors raised while kernels run (for example
+ *     a bounded device-side wait that gave up) are written to `dev_status`
+ *     where the call has one, and are visible after the caller synchronises.
+ */
+#ifndef KVC_H
+#define KVC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KVC_API __attribute__((visibility("default")))
+#else
+#define KVC_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KV_OK = 0,
+  KV_ERR_INVALID_ARG = -1, /* a size, pointer, alignment or flag is out of range */
+  KV_ERR_UNSUPPORTED = -2, /* valid, but not a shape this build handles (e.g. d = 96) */
+  KV_ERR_CUDA = -3,        /* the CUDA runtime refused the launch */
+  KV_ERR_TIMEOUT = -4,     /* (device status) a bounded device-side wait gave up */
+  KV_ERR_WORKSPACE = -5    /* workspace missing or smaller than kv_workspace_size() */
+} kv_status;
+
+typedef enum { KV_BF16 = 0, KV_F32 = 1 } kv_dtype;
+
+/* h2o_decode_step flags */
+enum {
+  /* Algorithm 1 of [H2O] 贪心驱逐算法 exactly: the new query attends only to the
+   * cached tokens (not to itself), the new token enters with accumulated score
+   * 0 and competes for eviction at once.  Requires recent == 0. */
+  KV_H2O_ALG1 = 1
+};
+
+/* operation codes for kv_workspace_size */
+enum { KV_OP_SCORE_OBS = 1, KV_OP_HUBKV_REFINE = 2, KV_OP_SELECT_TOPK = 3 };
+
+typedef void *kv_stream_t;
+
+/*
+ * kv_score_obs -- per-head importance score of every prompt token.
+ *
+ * [H2O] 观察二 defines a token's score as the attention probability it has
+ * accumulated; [KVblog] §4.3 (SnapKV) takes it from the prefill attention of an
+ * observation window; [KVblog] §1.1 gives softmax(q.k / sqrt(d_head)).  For unit
+ * (b, h) and each of its G = Hq/Hkv query heads g = h*G .. h*G+G-1 and window row
+ * w (prompt position p = T - W + w):
+ *     P_{g,w}(j) = softmax_j( scale * <Q_obs[b][g][w], K[b][h][j]> ),  j = 0..p
+ *     s[b][h][j] = sum over g, w with p >= j of P_{g,w}(j)
+ * Keys after a row's position get nothing from it (causal).  Hence
+ * sum_j s[b][h][j] = G * W.
+ *
+ *   Q_obs      [B][Hq][W][d]   the last W prompt queries of every query head
+ *   K          [B][Hkv][T][d]
+ *   scale      logit scale, normally 1/sqrt(d)
+ *   s_out      [B][Hkv][T] float32 (written in full)
+ *   workspace  >= kv_workspace_size(KV_OP_SCORE_OBS, ...) bytes of device memory
+ * Preconditions: 1 <= W <= T, Hq % Hkv == 0, d in {64, 128}.
+ */
+KVC_API int kv_score_obs(const void *Q_obs, const void *K, int B, int Hq, int Hkv, int T, int d,
+                 int W, float scale, int dtype, float *s_out, void *workspace,
+                 size_t workspace_bytes, kv_stream_t stream);
+
+/*
+ * hubkv_refine -- HubKV refinement of base scores before Top-K
+ * ([HubKV] Method: 最终算法：四步修正原始分数).
+ *   1. local hubs:  M_i = max_{|j-i| <= pool_width/2} s_j (window cut at the
+ *                   ends); i is a hub iff s_i == M_i;
+ *   2. SMD discount: q_i = s_i for a hub, gamma * s_i otherwise;
+ *   3. head weight: sel_h = 1 - H(s_h / sum s_h) / ln T (normalised entropy,
+ *                   0 ln 0 = 0; T == 1 or an all-zero head gives 0);
+ *                   beta_h = clip(sel_h / mean_{h' in batch row} sel_h', beta_lo,
+ *                   beta_hi), 1 when that mean is 0;
+ *   4. ratio gate:  z_i = s_i + r^2 (beta_h q_i - s_i).
+ * The head mean in step 3 runs over the H heads of one batch row b.
+ *
+ *   s          [B][H][T] float32 base scores (e.g. from kv_score_obs)
+ *   z_out      [B][H][T] float32
+ *   beta_out   [B][H] float32, may be NULL
+ * Preconditions: pool_width odd, beta_lo <= beta_hi.
+ */
+KVC_API int hubkv_refine(const float *s, int B, int H, int T, int pool_width, float gamma, float r,
+                 float beta_lo, float beta_hi, float *z_out, float *beta_out, void *workspace,
+                 size_t workspace_bytes, kv_stream_t stream);
+
+/*
+ * kv_select_topk -- budgeted per-head Top-K with a protected recent window.
+ * [H2O] 双缓冲: the last `recent` positions [T-recent, T) are always kept; the
+ * other k - recent slots go to the best of [0, T-recent) in the order
+ * (z descending, position ascending).  Each head selects on its own
+ * ([H2O] 为什么要按头独立驱逐).  idx_out lists the k kept positions of each
+ * head in ascending order.  The selection is exact: the same z gives the same
+ * idx bit for bit.
+ *
+ *   z          [B][H][T] float32 (finite; -0.0 is treated as +0.0)
+ *   idx_out    [B][H][k] int32
+ * Preconditions: 0 <= recent < k <= T.
+ */
+KVC_API int kv_select_topk(const float *z, int B, int H, int T, int k, int recent, int32_t *idx_out,
+                   void *workspace, size_t workspace_bytes, kv_stream_t stream);
+
+/*
+ * kv_compact -- "real drop" gather-compaction ([H2O] 两套代码) into a
+ * preallocated slot cache ([H2O] FlexGen 改造).  For every head and m < k:
+ *     K_out[m] = K[idx[m]],  V_out[m] = V[idx[m]],  pos_out[m] = idx[m],
+ *     acc_out[m] = s[idx[m]] (the attention mass received so far),
+ * and len_out = k.  Slots k..cap-1 are not touched.  The copy is bit-exact.
+ *
+ *   K, V       [B][H][T][d]
+ *   s          [B][H][T] float32, may be NULL (then acc_out is not written)
+ *   idx        [B][H][k] int32, each in [0, T) (a slot whose index is out of
+ *              range is left untouched)
+ *   K_out, V_out [B][H][cap][d];  pos_out, acc_out [B][H][cap];  len_out [B][H]
+ * Preconditions: k <= T, k <= cap; acc_out may be NULL.
+ */
+KVC_API int kv_compact(const void *K, const void *V, const float *s, const int32_t *idx, int B, int H,
+               int T, int k, int d, int dtype, void *K_out, void *V_out, int cap,
+               int32_t *pos_out, float *acc_out, int32_t *len_out, kv_stream_t stream);
+
+/*
+ * h2o_decode_step -- one decode step of the H2O eviction policy over a slot
+ * cache ([H2O] 问题形式化, 贪心驱逐算法, 双缓冲, FlexGen 改造).
+ * Per unit (b, h): the attended set C is the filled slots 0..len-1 plus the new
+ * token (unless KV_H2O_ALG1).  For each query head g of the group:
+ *     P_g = softmax over C of scale * <q_g, k_j>  (renormalised over kept keys),
+ *     o_out[b][g] = sum_j P_g(j) v_j.
+ * Each cached accumulator gains sum_g P_g(j); the new token starts with its own
+ * sum (0 under KV_H2O_ALG1).  Then:
+ *   len < cap : the new token goes to slot len, len += 1, evicted_pos = -1;
+ *   len == cap: the victim is the smallest (acc, pos) among the slots with
+ *               pos <= new_pos - recent (the new token itself also competes
+ *               when recent == 0); its slot is overwritten in place by the new
+ *               token (K, V, pos, acc) and evicted_pos = the victim's position;
+ *               if the victim is the new token nothing is written and
+ *               evicted_pos = new_pos.
+ * At most one eviction per KV head per step; |cache| stays cap once full.
+ *
+ *   q          [B][Hq][d];  k_new, v_new [B][Hkv][d]
+ *   K_cache, V_cache [B][Hkv][cap][d]   updated in place
+ *   pos [B][Hkv][cap] int32, acc [B][Hkv][cap] float32, len [B][Hkv] int32 (in place)
+ *   o_out [B][Hq][d] float32;  evicted_pos [B][Hkv] int32
+ *   dev_status  device int, may be NULL; set to a kv_status if a device-side
+ *               error occurs, never cleared by the library
+ * Preconditions: 0 <= recent < cap, KV_H2O_ALG1 => recent == 0, new_pos larger
+ * than every cached position, 0 <= len <= cap.
+ */
+KVC_API int h2o_decode_step(const void *q, const void *k_new, const void *v_new, void *K_cache,
+                    void *V_cache, int32_t *pos, float *acc, int32_t *len, int B, int Hq,
+                    int Hkv, int cap, int d, int recent, int32_t new_pos, float scale,
+                    int flags, int dtype, float *o_out, int32_t *evicted_pos, int *dev_status,
+                    kv_stream_t stream);
+
+/* Device workspace (bytes) that `op` needs for these sizes; 0 if none.
+ * Arguments that an op does not use are ignored; for KV_OP_HUBKV_REFINE pass the
+ * refine call's head count H as Hkv.  Returns 0 for invalid sizes. */
+KVC_API size_t kv_workspace_size(int op, int B, int Hq, int Hkv, int T, int d, int W, int k);
+
+/* Static description of a kv_status value. */
+KVC_API const char *kv_status_string(int status);
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+KVC_API int kv_version(void);
+
+/* Number of kernels this library has launched in this process (all devices,
+ * all threads); a diagnostic for counting launches around a timed region. */
+KVC_API unsigned long long kv_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVC_H */

@@ -1,0 +1,211 @@
+"""Python binding of libkvc.so: the same five calls, argument marshalling only.
+
+Every function takes CUDA torch tensors, checks dtype/shape/contiguity, passes
+raw device pointers and the current CUDA stream to the C ABI, and raises
+``KvcError`` on a non-zero status.  All arithmetic runs in the library's CUDA
+kernels; importing this module raises if ``libkvc.so`` has not been built.
+Output tensors may be passed in (``out=...``) to avoid allocation; otherwise they
+are allocated with torch on the input's device.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvc.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build the CUDA library first "
+        "(python -m kv_cache_compression_obs_gb300.build)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+KV_OK, KV_ERR_INVALID_ARG, KV_ERR_UNSUPPORTED, KV_ERR_CUDA, KV_ERR_TIMEOUT, KV_ERR_WORKSPACE = (
+    0, -1, -2, -3, -4, -5)
+KV_BF16, KV_F32 = 0, 1
+KV_H2O_ALG1 = 1
+KV_OP_SCORE_OBS, KV_OP_HUBKV_REFINE, KV_OP_SELECT_TOPK = 1, 2, 3
+
+_P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_lib.kv_score_obs.restype = _I
+_lib.kv_score_obs.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _Z, _P]
+_lib.hubkv_refine.restype = _I
+_lib.hubkv_refine.argtypes = [_P, _I, _I, _I, _I, _F, _F, _F, _F, _P, _P, _P, _Z, _P]
+_lib.kv_select_topk.restype = _I
+_lib.kv_select_topk.argtypes = [_P, _I, _I, _I, _I, _I, _P, _P, _Z, _P]
+_lib.kv_compact.restype = _I
+_lib.kv_compact.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P]
+_lib.h2o_decode_step.restype = _I
+_lib.h2o_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
+                                 _I, _I, _P, _P, _P, _P]
+_lib.kv_workspace_size.restype = _Z
+_lib.kv_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I]
+_lib.kv_status_string.restype = ctypes.c_char_p
+_lib.kv_status_string.argtypes = [_I]
+_lib.kv_version.restype = _I
+
+
+class KvcError(RuntimeError):
+    def __init__(self, call: str, status: int):
+        super().__init__(f"{call}: {_lib.kv_status_string(status).decode()} (status {status})")
+        self.status = status
+
+
+def _check(call: str, status: int) -> None:
+    if status != KV_OK:
+        raise KvcError(call, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return KV_BF16
+    if t.dtype == torch.float32:
+        return KV_F32
+    raise TypeError(f"expected bfloat16 or float32, got {t.dtype}")
+
+
+def _dev(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def kv_workspace_size(op: int, B: int, Hq: int, Hkv: int, T: int, d: int = 128, W: int = 1,
+                      k: int = 1) -> int:
+    return int(_lib.kv_workspace_size(op, B, Hq, Hkv, T, d, W, k))
+
+
+def _workspace(nbytes: int, device, given):
+    if nbytes == 0:
+        return None, 0
+    if given is not None:
+        return given, given.numel() * given.element_size()
+    return torch.empty(nbytes, dtype=torch.uint8, device=device), nbytes
+
+
+def kv_score_obs(Q_obs: torch.Tensor, K: torch.Tensor, scale: float | None = None, out=None,
+                 workspace=None, stream=None) -> torch.Tensor:
+    """Q_obs [B][Hq][W][d], K [B][Hkv][T][d] -> s [B][Hkv][T] float32."""
+    B, Hq, W, d = Q_obs.shape
+    B2, Hkv, T, d2 = K.shape
+    if B2 != B or d2 != d or Q_obs.dtype != K.dtype:
+        raise ValueError("Q_obs and K disagree in batch, head dim or dtype")
+    _dev(Q_obs, K, out)
+    if scale is None:
+        scale = d ** -0.5
+    s = out if out is not None else torch.empty(B, Hkv, T, dtype=torch.float32, device=K.device)
+    ws, nbytes = _workspace(kv_workspace_size(KV_OP_SCORE_OBS, B, Hq, Hkv, T, d, W), K.device,
+                            workspace)
+    _check("kv_score_obs", _lib.kv_score_obs(_ptr(Q_obs), _ptr(K), B, Hq, Hkv, T, d, W,
+                                             float(scale), _dtype_code(K), _ptr(s), _ptr(ws),
+                                             nbytes, _stream(stream)))
+    return s
+
+
+def hubkv_refine(s: torch.Tensor, r: float, gamma: float = 0.5, pool_width: int = 5,
+                 beta_lo: float = 0.8, beta_hi: float = 1.2, out=None, beta_out=None,
+                 workspace=None, stream=None):
+    """s [B][H][T] float32 -> (z [B][H][T], beta [B][H]) float32."""
+    B, H, T = s.shape
+    if s.dtype != torch.float32:
+        raise TypeError("s must be float32")
+    _dev(s, out, beta_out)
+    z = out if out is not None else torch.empty_like(s)
+    beta = beta_out if beta_out is not None else torch.empty(B, H, dtype=torch.float32,
+                                                             device=s.device)
+    ws, nbytes = _workspace(kv_workspace_size(KV_OP_HUBKV_REFINE, B, H, H, T), s.device, workspace)
+    _check("hubkv_refine", _lib.hubkv_refine(_ptr(s), B, H, T, pool_width, float(gamma), float(r),
+                                             float(beta_lo), float(beta_hi), _ptr(z), _ptr(beta),
+                                             _ptr(ws), nbytes, _stream(stream)))
+    return z, beta
+
+
+def kv_select_topk(z: torch.Tensor, k: int, recent: int, out=None, stream=None) -> torch.Tensor:
+    """z [B][H][T] float32 -> idx [B][H][k] int32 (ascending positions)."""
+    B, H, T = z.shape
+    if z.dtype != torch.float32:
+        raise TypeError("z must be float32")
+    _dev(z, out)
+    idx = out if out is not None else torch.empty(B, H, k, dtype=torch.int32, device=z.device)
+    _check("kv_select_topk", _lib.kv_select_topk(_ptr(z), B, H, T, int(k), int(recent), _ptr(idx),
+                                                 None, 0, _stream(stream)))
+    return idx
+
+
+def kv_compact(K: torch.Tensor, V: torch.Tensor, s, idx: torch.Tensor, cap: int | None = None,
+               K_out=None, V_out=None, pos_out=None, acc_out=None, len_out=None, stream=None):
+    """Gather the kept rows into a slot cache; returns (K_out, V_out, pos, acc, len)."""
+    B, H, T, d = K.shape
+    k = idx.shape[-1]
+    cap = k if cap is None else cap
+    if idx.dtype != torch.int32 or V.shape != K.shape or V.dtype != K.dtype:
+        raise ValueError("idx must be int32 and V must match K")
+    _dev(K, V, s, idx, K_out, V_out, pos_out, acc_out, len_out)
+    dev = K.device
+    K_out = K_out if K_out is not None else torch.empty(B, H, cap, d, dtype=K.dtype, device=dev)
+    V_out = V_out if V_out is not None else torch.empty(B, H, cap, d, dtype=K.dtype, device=dev)
+    pos = pos_out if pos_out is not None else torch.zeros(B, H, cap, dtype=torch.int32, device=dev)
+    acc = acc_out if acc_out is not None else torch.zeros(B, H, cap, dtype=torch.float32, device=dev)
+    ln = len_out if len_out is not None else torch.empty(B, H, dtype=torch.int32, device=dev)
+    _check("kv_compact", _lib.kv_compact(_ptr(K), _ptr(V), _ptr(s), _ptr(idx), B, H, T, k, d,
+                                         _dtype_code(K), _ptr(K_out), _ptr(V_out), int(cap),
+                                         _ptr(pos), _ptr(acc if s is not None else None), _ptr(ln),
+                                         _stream(stream)))
+    return K_out, V_out, pos, acc, ln
+
+
+def h2o_decode_step(q, k_new, v_new, K_cache, V_cache, pos, acc, len_, recent: int, new_pos: int,
+                    scale: float | None = None, flags: int = 0, o_out=None, evicted_out=None,
+                    dev_status=None, stream=None):
+    """One decode step, cache state updated in place; returns (o [B][Hq][d] f32, evicted [B][Hkv])."""
+    B, Hq, d = q.shape
+    _, Hkv, cap, _ = K_cache.shape
+    _dev(q, k_new, v_new, K_cache, V_cache, pos, acc, len_, o_out, evicted_out, dev_status)
+    if scale is None:
+        scale = d ** -0.5
+    o = o_out if o_out is not None else torch.empty(B, Hq, d, dtype=torch.float32, device=q.device)
+    ev = evicted_out if evicted_out is not None else torch.empty(B, Hkv, dtype=torch.int32,
+                                                                 device=q.device)
+    _check("h2o_decode_step", _lib.h2o_decode_step(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(K_cache), _ptr(V_cache), _ptr(pos), _ptr(acc),
+        _ptr(len_), B, Hq, Hkv, cap, d, int(recent), int(new_pos), float(scale), int(flags),
+        _dtype_code(q), _ptr(o), _ptr(ev), _ptr(dev_status), _stream(stream)))
+    return o, ev
+
+
+def compress_prefill(Q_obs, K, V, k: int, recent: int, r: float | None, gamma: float = 0.5,
+                     pool_width: int = 5, beta_lo: float = 0.8, beta_hi: float = 1.2,
+                     cap: int | None = None, scale: float | None = None, stream=None):
+    """The prefill eviction chain: score -> (HubKV refine) -> Top-K -> compact.
+
+    Returns a dict with the base scores s, the refined scores z (s itself when
+    r is None), the kept positions idx and the slot cache (K, V, pos, acc, len).
+    """
+    s = kv_score_obs(Q_obs, K, scale, stream=stream)
+    if r is None:
+        z = s
+        beta = None
+    else:
+        z, beta = hubkv_refine(s, r, gamma, pool_width, beta_lo, beta_hi, stream=stream)
+    idx = kv_select_topk(z, k, recent, stream=stream)
+    Kc, Vc, pos, acc, ln = kv_compact(K, V, s, idx, cap, stream=stream)
+    return {"s": s, "z": z, "beta": beta, "idx": idx, "K": Kc, "V": Vc, "pos": pos, "acc": acc,
+            "len": ln}
+
+
+def library_handle():
+    """The loaded ctypes library (for tests that check exported symbols)."""
+    return _lib

@@ -1,0 +1,152 @@
+// hubkv_refine.cu -- HubKV score refinement (HubKV walkthrough, Method: 最终算法).
+//
+//   1. local hubs: M_i = max_{|j-i| <= pool_width/2} s_j, hub iff s_i == M_i;
+//   2. SMD discount: q_i = s_i for hubs, gamma s_i otherwise;
+//   3. head weight: sel_h = 1 - H_h / ln T with H_h the entropy of s_h / sum(s_h);
+//      beta_h = clip(sel_h / mean over the batch row's heads, lo, hi), 1 if mean 0;
+//   4. ratio gate: z_i = s_i + r^2 (beta_h q_i - s_i).
+// Three launches: an entropy reduction per (head, chunk) writing fixed-order
+// partial sums; one block per batch row turning them into beta_h (double
+// precision, fixed order, so the result is reproducible bit for bit); one pass
+// that applies steps 1, 2 and 4 with a shared-memory halo for the pooling window.
+#include <cmath>
+
+#include "kvc_internal.cuh"
+
+namespace kvc {
+namespace {
+
+constexpr int NT = 256;
+constexpr int kChunk = 4096;       // entropy chunk (elements)
+constexpr int kApply = 2048;       // elements per block of the apply pass
+constexpr int kMaxHalo = 64;       // pool_width <= 129
+
+// Neumaier-compensated float sum.
+struct CSum {
+  float s = 0.f, c = 0.f;
+  __device__ __forceinline__ void add(float x) {
+    const float t = s + x;
+    c += (fabsf(s) >= fabsf(x)) ? (s - t) + x : (x - t) + s;
+    s = t;
+  }
+  __device__ __forceinline__ double value() const { return (double)s + (double)c; }
+};
+
+// Per (head, chunk): sum s and sum s ln s (0 ln 0 = 0), reduced in a fixed tree.
+__global__ __launch_bounds__(NT) void refine_entropy_kernel(const float *__restrict__ s, int T,
+                                                            int n_chunks,
+                                                            double2 *__restrict__ part) {
+  const long head = blockIdx.x / n_chunks;
+  const int chunk = blockIdx.x % n_chunks;
+  const float *sv = s + head * (long)T;
+  const int i0 = chunk * kChunk, i1 = min(T, i0 + kChunk);
+  CSum a, c;
+  for (int i = i0 + threadIdx.x; i < i1; i += NT) {
+    const float x = sv[i];
+    a.add(x);
+    if (x > 0.f) c.add(x * logf(x));
+  }
+  __shared__ double ra[NT], rc[NT];
+  ra[threadIdx.x] = a.value();
+  rc[threadIdx.x] = c.value();
+  __syncthreads();
+  for (int w = NT / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) {
+      ra[threadIdx.x] += ra[threadIdx.x + w];
+      rc[threadIdx.x] += rc[threadIdx.x + w];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) part[head * n_chunks + chunk] = make_double2(ra[0], rc[0]);
+}
+
+// One block per batch row: sel_h per head in double (fixed chunk order), the row
+// mean in head order, then beta_h.
+__global__ void refine_beta_kernel(const double2 *__restrict__ part, int H, int T, int n_chunks,
+                                   float beta_lo, float beta_hi, float *__restrict__ beta_ws,
+                                   float *__restrict__ beta_out) {
+  extern __shared__ double sel[];
+  const long b = blockIdx.x;
+  const double lnT = log((double)T);
+  for (int h = threadIdx.x; h < H; h += blockDim.x) {
+    double S = 0.0, C = 0.0;
+    for (int c = 0; c < n_chunks; ++c) {
+      const double2 p = part[(b * H + h) * n_chunks + c];
+      S += p.x;
+      C += p.y;
+    }
+    sel[h] = (T > 1 && S > 0.0) ? 1.0 - (log(S) - C / S) / lnT : 0.0;
+  }
+  __syncthreads();
+  __shared__ double mean;
+  if (threadIdx.x == 0) {
+    double acc = 0.0;
+    for (int h = 0; h < H; ++h) acc += sel[h];
+    mean = acc / H;
+  }
+  __syncthreads();
+  for (int h = threadIdx.x; h < H; h += blockDim.x) {
+    double bt = 1.0;
+    if (mean != 0.0) bt = fmin(fmax(sel[h] / mean, (double)beta_lo), (double)beta_hi);
+    beta_ws[b * H + h] = (float)bt;
+    if (beta_out) beta_out[b * H + h] = (float)bt;
+  }
+}
+
+__global__ __launch_bounds__(NT) void refine_apply_kernel(
+    const float *__restrict__ s, int T, int blocks_per_head, int half, float gamma, float r2,
+    const float *__restrict__ beta_ws, float *__restrict__ z) {
+  extern __shared__ float tile[];
+  const long head = blockIdx.x / blocks_per_head;
+  const int blk = blockIdx.x % blocks_per_head;
+  const float beta = beta_ws[head];
+  const float *sv = s + head * (long)T;
+  float *zv = z + head * (long)T;
+  const int i0 = blk * kApply, i1 = min(T, i0 + kApply);
+  const int lo = i0 - half, n = (i1 - i0) + 2 * half;
+  for (int t = threadIdx.x; t < n; t += NT) {
+    const int i = lo + t;
+    tile[t] = (i >= 0 && i < T) ? sv[i] : -INFINITY;
+  }
+  __syncthreads();
+  for (int i = i0 + threadIdx.x; i < i1; i += NT) {
+    const int t = i - lo;
+    const float si = tile[t];
+    float M = si;
+    for (int o = -half; o <= half; ++o) M = fmaxf(M, tile[t + o]);
+    const float qi = (si == M) ? si : gamma * si;
+    zv[i] = fmaf(r2, fmaf(beta, qi, -si), si);  // s + r^2 (beta q - s)
+  }
+}
+
+}  // namespace
+
+RefinePlan plan_refine(int B, int H, int T) {
+  RefinePlan p{};
+  p.chunk = kChunk;
+  p.n_chunks = (T + kChunk - 1) / kChunk;
+  p.beta_offset = ((size_t)B * H * p.n_chunks * sizeof(double2) + 255) / 256 * 256;
+  p.ws_bytes = p.beta_offset + (size_t)B * H * sizeof(float);
+  return p;
+}
+
+int launch_hubkv_refine(const float *s, int B, int H, int T, int pool_width, float gamma,
+                        float r, float beta_lo, float beta_hi, float *z, float *beta, void *ws,
+                        const RefinePlan &plan, cudaStream_t st) {
+  const long heads = (long)B * H;
+  const int half = pool_width / 2;
+  if (half > kMaxHalo) return KV_ERR_UNSUPPORTED;
+  double2 *part = static_cast<double2 *>(ws);
+  float *beta_ws = reinterpret_cast<float *>(static_cast<char *>(ws) + plan.beta_offset);
+  refine_entropy_kernel<<<(unsigned)(heads * plan.n_chunks), NT, 0, st>>>(s, T, plan.n_chunks, part);
+  const int bt = H < 256 ? ((H + 31) / 32) * 32 : 256;
+  refine_beta_kernel<<<(unsigned)B, bt, (size_t)H * sizeof(double), st>>>(
+      part, H, T, plan.n_chunks, beta_lo, beta_hi, beta_ws, beta);
+  const int bph = (T + kApply - 1) / kApply;
+  const size_t smem = (size_t)(kApply + 2 * half) * sizeof(float);
+  refine_apply_kernel<<<(unsigned)(heads * bph), NT, smem, st>>>(s, T, bph, half, gamma, r * r,
+                                                                beta_ws, z);
+  return launch_status(3);
+}
+
+}  // namespace kvc

@@ -1,0 +1,182 @@
+// kvc_api.cu -- the extern "C" entry points of libkvc.so: argument checks, then
+// one launcher per operation.  Every check runs on the host before anything is
+// enqueued, so a rejected call touches neither the GPU nor any output.
+#include <atomic>
+#include <climits>
+#include <mutex>
+#include <unordered_map>
+
+#include "kvc_internal.cuh"
+
+namespace kvc {
+
+static std::atomic<unsigned long long> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return kNumSmsHint;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return kNumSmsHint;
+  return n;
+}
+
+// Raise a kernel's dynamic shared-memory limit once per (device, kernel).
+int ensure_smem(const void *func, size_t bytes) {
+  static std::mutex mu;
+  static std::unordered_map<const void *, size_t> done[64];
+  if (bytes <= 48 * 1024) return 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = done[dev].find(func);
+  if (it != done[dev].end() && it->second >= bytes) return 0;
+  int optin = 0;
+  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if ((size_t)optin < bytes) return 1;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return 1;
+  }
+  done[dev][func] = bytes;
+  return 0;
+}
+
+}  // namespace kvc
+
+using namespace kvc;
+
+namespace {
+
+bool dtype_ok(int dt) { return dt == KV_BF16 || dt == KV_F32; }
+bool dim_ok(int d) { return d == 64 || d == 128; }
+// product of non-negative ints without overflow of 2^62
+bool fits(long long a, long long b) { return a >= 0 && b >= 0 && (b == 0 || a <= (1LL << 62) / b); }
+
+}  // namespace
+
+extern "C" {
+
+int kv_version(void) { return 100; }
+
+unsigned long long kv_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char *kv_status_string(int status) {
+  switch (status) {
+    case KV_OK: return "ok";
+    case KV_ERR_INVALID_ARG: return "invalid argument";
+    case KV_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case KV_ERR_CUDA: return "CUDA launch error";
+    case KV_ERR_TIMEOUT: return "device-side wait timed out";
+    case KV_ERR_WORKSPACE: return "workspace missing or too small";
+    default: return "unknown status";
+  }
+}
+
+size_t kv_workspace_size(int op, int B, int Hq, int Hkv, int T, int d, int W, int k) {
+  (void)d;
+  (void)k;
+  if (B < 0 || T <= 0) return 0;
+  switch (op) {
+    case KV_OP_SCORE_OBS:
+      if (Hq <= 0 || Hkv <= 0 || Hq % Hkv || W <= 0 || W > T) return 0;
+      return plan_score(B, Hq, Hkv, T, W).ws_bytes;
+    case KV_OP_HUBKV_REFINE:
+      if (Hkv <= 0) return 0;
+      return plan_refine(B, Hkv, T).ws_bytes;  // the refine call's H is passed as Hkv
+    case KV_OP_SELECT_TOPK:
+      return 0;
+    default:
+      return 0;
+  }
+}
+
+int kv_score_obs(const void *Q_obs, const void *K, int B, int Hq, int Hkv, int T, int d, int W,
+                 float scale, int dtype, float *s_out, void *workspace, size_t workspace_bytes,
+                 kv_stream_t stream) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || T <= 0 || W <= 0 || W > T ||
+      !dtype_ok(dtype) || !(scale == scale))
+    return KV_ERR_INVALID_ARG;
+  if (!dim_ok(d)) return KV_ERR_UNSUPPORTED;
+  if (!fits((long long)B * Hkv, (long long)T * d) || !fits((long long)B * Hq, (long long)W * d))
+    return KV_ERR_INVALID_ARG;
+  if (B == 0) return KV_OK;
+  if (!Q_obs || !K || !s_out || !aligned16(Q_obs) || !aligned16(K) || !aligned16(s_out))
+    return KV_ERR_INVALID_ARG;
+  const ScorePlan plan = plan_score(B, Hq, Hkv, T, W);
+  if (!workspace || workspace_bytes < plan.ws_bytes || !aligned16(workspace)) return KV_ERR_WORKSPACE;
+  return launch_score_obs(Q_obs, K, B, Hq, Hkv, T, d, W, scale, dtype, s_out, workspace, plan,
+                          static_cast<cudaStream_t>(stream));
+}
+
+int hubkv_refine(const float *s, int B, int H, int T, int pool_width, float gamma, float r,
+                 float beta_lo, float beta_hi, float *z_out, float *beta_out, void *workspace,
+                 size_t workspace_bytes, kv_stream_t stream) {
+  if (B < 0 || H <= 0 || T <= 0 || pool_width <= 0 || pool_width % 2 == 0 ||
+      !(beta_lo <= beta_hi) || !(gamma == gamma) || !(r == r))
+    return KV_ERR_INVALID_ARG;
+  if (pool_width > 129) return KV_ERR_UNSUPPORTED;
+  if (!fits((long long)B * H, T)) return KV_ERR_INVALID_ARG;
+  if (B == 0) return KV_OK;
+  if (!s || !z_out || !aligned16(s) || !aligned16(z_out)) return KV_ERR_INVALID_ARG;
+  const RefinePlan plan = plan_refine(B, H, T);
+  if (!workspace || workspace_bytes < plan.ws_bytes || !aligned16(workspace)) return KV_ERR_WORKSPACE;
+  return launch_hubkv_refine(s, B, H, T, pool_width, gamma, r, beta_lo, beta_hi, z_out, beta_out,
+                             workspace, plan, static_cast<cudaStream_t>(stream));
+}
+
+int kv_select_topk(const float *z, int B, int H, int T, int k, int recent, int32_t *idx_out,
+                   void *workspace, size_t workspace_bytes, kv_stream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (B < 0 || H <= 0 || T <= 0 || recent < 0 || k <= recent || k > T) return KV_ERR_INVALID_ARG;
+  if (!fits((long long)B * H, T)) return KV_ERR_INVALID_ARG;
+  if (B == 0) return KV_OK;
+  if (!z || !idx_out || !aligned16(z) || !aligned16(idx_out)) return KV_ERR_INVALID_ARG;
+  return launch_select_topk(z, B, H, T, k, recent, idx_out, static_cast<cudaStream_t>(stream));
+}
+
+int kv_compact(const void *K, const void *V, const float *s, const int32_t *idx, int B, int H,
+               int T, int k, int d, int dtype, void *K_out, void *V_out, int cap,
+               int32_t *pos_out, float *acc_out, int32_t *len_out, kv_stream_t stream) {
+  if (B < 0 || H <= 0 || T <= 0 || k <= 0 || k > T || cap < k || !dtype_ok(dtype))
+    return KV_ERR_INVALID_ARG;
+  if (!dim_ok(d)) return KV_ERR_UNSUPPORTED;
+  if (!fits((long long)B * H, (long long)T * d) || !fits((long long)B * H, (long long)cap * d))
+    return KV_ERR_INVALID_ARG;
+  if (B == 0) return KV_OK;
+  if (!K || !V || !idx || !K_out || !V_out || !pos_out || !len_out) return KV_ERR_INVALID_ARG;
+  if (!aligned16(K) || !aligned16(V) || !aligned16(K_out) || !aligned16(V_out) ||
+      (s && !aligned16(s)) || (acc_out && !aligned16(acc_out)))
+    return KV_ERR_INVALID_ARG;
+  return launch_compact(K, V, acc_out ? s : nullptr, idx, B, H, T, k, d, dtype, K_out, V_out,
+                        cap, pos_out, acc_out, len_out, static_cast<cudaStream_t>(stream));
+}
+
+int h2o_decode_step(const void *q, const void *k_new, const void *v_new, void *K_cache,
+                    void *V_cache, int32_t *pos, float *acc, int32_t *len, int B, int Hq,
+                    int Hkv, int cap, int d, int recent, int32_t new_pos, float scale,
+                    int flags, int dtype, float *o_out, int32_t *evicted_pos, int *dev_status,
+                    kv_stream_t stream) {
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || cap <= 0 || recent < 0 ||
+      recent >= cap || new_pos < 0 || !dtype_ok(dtype) || (flags & ~KV_H2O_ALG1) ||
+      ((flags & KV_H2O_ALG1) && recent != 0) || !(scale == scale))
+    return KV_ERR_INVALID_ARG;
+  if (!dim_ok(d)) return KV_ERR_UNSUPPORTED;
+  if (!fits((long long)B * Hkv, (long long)cap * d)) return KV_ERR_INVALID_ARG;
+  if (B == 0) return KV_OK;
+  if (!q || !k_new || !v_new || !K_cache || !V_cache || !pos || !acc || !len || !o_out ||
+      !evicted_pos)
+    return KV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(K_cache) ||
+      !aligned16(V_cache))
+    return KV_ERR_INVALID_ARG;
+  const int G = Hq / Hkv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return KV_ERR_UNSUPPORTED;
+  if (decode_smem_bytes(G, cap, d) > 227 * 1024) return KV_ERR_UNSUPPORTED;
+  return launch_decode_step(q, k_new, v_new, K_cache, V_cache, pos, acc, len, B, Hq, Hkv, cap,
+                            d, recent, new_pos, scale, flags, dtype, o_out, evicted_pos,
+                            dev_status, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

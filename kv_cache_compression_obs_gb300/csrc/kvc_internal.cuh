@@ -1,0 +1,94 @@
+// kvc_internal.cuh -- shared declarations of the CUDA library (not part of the ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "kvc.h"
+
+namespace kvc {
+
+constexpr int kNumSmsHint = 152;  // GB300; the launchers query the real count
+
+int device_sm_count();
+int ensure_smem(const void *func, size_t bytes);  // opt a kernel into > 48 KB of shared memory
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+void count_launches(int n);  // diagnostic counter behind kv_launch_count()
+
+inline int launch_status(int launches = 1) {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return KV_ERR_CUDA;
+  count_launches(launches);
+  return KV_OK;
+}
+
+// ---- element access ---------------------------------------------------------
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// Unpack one 16-byte vector into floats: 8 bf16 or 4 f32.
+template <typename T> struct Vec16;
+template <> struct Vec16<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ __forceinline__ static void unpack(const uint4 &v, float *out) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      out[2 * i] = __uint_as_float(w[i] << 16);
+      out[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+  }
+};
+template <> struct Vec16<float> {
+  static constexpr int N = 4;
+  __device__ __forceinline__ static void unpack(const uint4 &v, float *out) {
+    out[0] = __uint_as_float(v.x);
+    out[1] = __uint_as_float(v.y);
+    out[2] = __uint_as_float(v.z);
+    out[3] = __uint_as_float(v.w);
+  }
+};
+
+// ---- operation plans (shared by the launchers and kv_workspace_size) --------
+struct ScorePlan {
+  int gw;          // query rows per unit = G * W
+  int row_blocks;  // ceil(gw / 64)
+  int n_splits;    // key splits of the statistics pass
+  int split_len;   // keys per split (multiple of 64)
+  size_t ws_bytes;
+};
+ScorePlan plan_score(int B, int Hq, int Hkv, int T, int W);
+
+struct RefinePlan {
+  int chunk;     // elements per entropy chunk
+  int n_chunks;  // chunks per head
+  size_t beta_offset;  // byte offset of the per-head beta array in the workspace
+  size_t ws_bytes;
+};
+RefinePlan plan_refine(int B, int H, int T);
+
+// ---- launchers (validated arguments only) ------------------------------------
+int launch_score_obs(const void *Q, const void *K, int B, int Hq, int Hkv, int T, int d, int W,
+                     float scale, int dtype, float *s, void *ws, const ScorePlan &plan,
+                     cudaStream_t st);
+int launch_hubkv_refine(const float *s, int B, int H, int T, int pool_width, float gamma,
+                        float r, float beta_lo, float beta_hi, float *z, float *beta, void *ws,
+                        const RefinePlan &plan, cudaStream_t st);
+int launch_select_topk(const float *z, int B, int H, int T, int k, int recent, int32_t *idx,
+                       cudaStream_t st);
+int launch_compact(const void *K, const void *V, const float *s, const int32_t *idx, int B,
+                   int H, int T, int k, int d, int dtype, void *K_out, void *V_out, int cap,
+                   int32_t *pos, float *acc, int32_t *len, cudaStream_t st);
+int launch_decode_step(const void *q, const void *k_new, const void *v_new, void *K_cache,
+                       void *V_cache, int32_t *pos, float *acc, int32_t *len, int B, int Hq,
+                       int Hkv, int cap, int d, int recent, int32_t new_pos, float scale,
+                       int flags, int dtype, float *o, int32_t *evicted, int *dev_status,
+                       cudaStream_t st);
+size_t decode_smem_bytes(int G, int cap, int d);
+
+}  // namespace kvc

@@ -97,9 +97,12 @@ def _plant_unit(wl: Workload, unit: int, q: torch.Tensor, k: torch.Tensor, g) ->
             n = len(segs)
             ns = _normalise(torch.randn(n, d, generator=g, device=device))
             us = _normalise(SEGMENT_ALIGN * qhat + math.sqrt(1 - SEGMENT_ALIGN ** 2) * ns)
-            pos = torch.cat([torch.arange(s, s + ln, device=device) for s, ln in segs])
-            sid = torch.cat([torch.full((ln,), i, device=device, dtype=torch.long)
-                             for i, (s, ln) in enumerate(segs)])
+            starts = np.array([s_ for s_, _ in segs], dtype=np.int64)
+            lens = np.array([ln for _, ln in segs], dtype=np.int64)
+            sid_np = np.repeat(np.arange(n, dtype=np.int64), lens)
+            pos_np = starts[sid_np] + (np.arange(lens.sum()) - np.repeat(np.cumsum(lens) - lens, lens))
+            pos = torch.from_numpy(pos_np).to(device)
+            sid = torch.from_numpy(sid_np).to(device)
             u = us[sid]
             e = torch.randn(pos.numel(), d, generator=g, device=device)
             e = _normalise(e - (e * u).sum(-1, keepdim=True) * u)

@@ -1,0 +1,105 @@
+"""The C ABI without a GPU: the library loads, exports every declared symbol, and
+rejects bad arguments on the host before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvc.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from kv_cache_compression_obs_gb300.build import build
+    path = build()
+    lib = ctypes.CDLL(path)
+    P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.kv_score_obs.argtypes = [P, P, I, I, I, I, I, I, F, I, P, P, Z, P]
+    lib.hubkv_refine.argtypes = [P, I, I, I, I, F, F, F, F, P, P, P, Z, P]
+    lib.kv_select_topk.argtypes = [P, I, I, I, I, I, P, P, Z, P]
+    lib.kv_compact.argtypes = [P, P, P, P, I, I, I, I, I, I, P, P, I, P, P, P, P]
+    lib.h2o_decode_step.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, P, P, P, P]
+    lib.kv_workspace_size.restype = Z
+    lib.kv_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
+    lib.kv_status_string.restype = ctypes.c_char_p
+    return lib
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"KVC_API\s+[\w\s\*]+?\b(\w+)\s*\(", text)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert set(names) >= {"kv_score_obs", "hubkv_refine", "kv_select_topk", "kv_compact",
+                          "h2o_decode_step", "kv_workspace_size", "kv_status_string", "kv_version"}
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version(lib):
+    assert lib.kv_status_string(0) == b"ok"
+    assert b"invalid" in lib.kv_status_string(-1)
+    assert lib.kv_status_string(-4) == b"device-side wait timed out"
+    assert lib.kv_version() >= 100
+
+
+def test_workspace_size(lib):
+    assert lib.kv_workspace_size(1, 4, 32, 8, 32768, 128, 64, 3276) > 0
+    assert lib.kv_workspace_size(1, 1, 32, 8, 100, 128, 101, 1) == 0   # W > T: invalid
+    assert lib.kv_workspace_size(2, 4, 8, 8, 32768, 128, 64, 0) > 0
+    assert lib.kv_workspace_size(3, 4, 8, 8, 32768, 128, 64, 100) == 0
+    assert lib.kv_workspace_size(99, 4, 8, 8, 32768, 128, 64, 100) == 0
+
+
+NULL = None
+
+
+def test_host_validation_rejects_before_cuda(lib):
+    # score: W > T, Hq % Hkv, d unsupported, null pointers
+    assert lib.kv_score_obs(NULL, NULL, 1, 4, 2, 10, 64, 11, 0.1, 0, NULL, NULL, 0, NULL) == -1
+    assert lib.kv_score_obs(NULL, NULL, 1, 3, 2, 10, 64, 4, 0.1, 0, NULL, NULL, 0, NULL) == -1
+    assert lib.kv_score_obs(NULL, NULL, 1, 4, 2, 10, 96, 4, 0.1, 0, NULL, NULL, 0, NULL) == -2
+    assert lib.kv_score_obs(NULL, NULL, 1, 4, 2, 10, 64, 4, 0.1, 7, NULL, NULL, 0, NULL) == -1
+    assert lib.kv_score_obs(NULL, NULL, 1, 4, 2, 10, 64, 4, 0.1, 0, NULL, NULL, 0, NULL) == -1
+    # refine: even pool width, bad clip range
+    assert lib.hubkv_refine(NULL, 1, 2, 10, 4, 0.5, 0.1, 0.8, 1.2, NULL, NULL, NULL, 0, NULL) == -1
+    assert lib.hubkv_refine(NULL, 1, 2, 10, 5, 0.5, 0.1, 1.3, 1.2, NULL, NULL, NULL, 0, NULL) == -1
+    # select: k <= recent, k > T
+    assert lib.kv_select_topk(NULL, 1, 2, 10, 3, 3, NULL, NULL, 0, NULL) == -1
+    assert lib.kv_select_topk(NULL, 1, 2, 10, 11, 3, NULL, NULL, 0, NULL) == -1
+    # compact: cap < k
+    assert lib.kv_compact(NULL, NULL, NULL, NULL, 1, 2, 10, 5, 64, 0, NULL, NULL, 4, NULL, NULL,
+                          NULL, NULL) == -1
+    # decode: ALG1 with a recent window, recent >= cap, unsupported group size
+    assert lib.h2o_decode_step(NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 1, 4, 4, 8, 64, 1, 9,
+                               0.1, 1, 0, NULL, NULL, NULL, NULL) == -1
+    assert lib.h2o_decode_step(NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 1, 4, 4, 8, 64, 8, 9,
+                               0.1, 0, 0, NULL, NULL, NULL, NULL) == -1
+    p = ctypes.c_void_p(16)  # a dummy aligned pointer: never dereferenced, the call is rejected first
+    assert lib.h2o_decode_step(p, p, p, p, p, p, p, p, 1, 12, 4, 8, 64, 1, 9, 0.1, 0, 0, p, p, NULL,
+                               NULL) == -2
+
+
+def test_empty_batch_is_a_no_op(lib):
+    assert lib.kv_score_obs(NULL, NULL, 0, 4, 2, 10, 64, 4, 0.1, 0, NULL, NULL, 0, NULL) == 0
+    assert lib.hubkv_refine(NULL, 0, 2, 10, 5, 0.5, 0.1, 0.8, 1.2, NULL, NULL, NULL, 0, NULL) == 0
+    assert lib.kv_select_topk(NULL, 0, 2, 10, 5, 3, NULL, NULL, 0, NULL) == 0
+    assert lib.kv_compact(NULL, NULL, NULL, NULL, 0, 2, 10, 5, 64, 0, NULL, NULL, 5, NULL, NULL,
+                          NULL, NULL) == 0
+    assert lib.h2o_decode_step(NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 0, 4, 4, 8, 64, 1, 9,
+                               0.1, 0, 0, NULL, NULL, NULL, NULL) == 0
+
+
+def test_no_product_module_imports_the_oracle():
+    """The CUDA path and its binding never import or load the oracle."""
+    pkg = os.path.join(ROOT, "kv_cache_compression_obs_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "liboracle" not in text and "kvc_oracle" not in text, f
