@@ -166,11 +166,11 @@ def decode_inputs(wl: Workload, step: int, device="cpu"):
 
 
 def to_numpy_bits(t: torch.Tensor) -> np.ndarray:
-    """Host numpy view of a tensor's bytes: uint16 bit patterns for bf16, float32 otherwise."""
+    """Host numpy copy of a tensor: uint16 bit patterns for bf16, the same dtype otherwise."""
     t = t.detach().contiguous().cpu()
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16)
-    if t.dtype == torch.float32:
+    if t.dtype in (torch.float32, torch.int32):
         return t.numpy()
     raise TypeError(t.dtype)
 
