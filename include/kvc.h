@@ -187,6 +187,33 @@ KVC_API int h2o_decode_step(const void *q, const void *k_new, const void *v_new,
                     int flags, int dtype, float *o_out, int32_t *evicted_pos, int *dev_status,
                     kv_stream_t stream);
 
+/*
+ * kv_score_obs_noalloc -- kv_score_obs without a caller-provided workspace.
+ * (No counterpart in the pages: this is a calling convention, not a step of
+ * the method.)
+ *
+ * For callers that cannot allocate device memory: code embedded in a host
+ * framework that hands it only its input and output buffers, and code that
+ * must not call cudaMalloc because that call can synchronise the device and
+ * stall other streams.  Computes exactly what kv_score_obs computes, with the
+ * same arguments minus the workspace, using scratch space from a fixed array
+ * of KV_SCORE_NOALLOC_SCRATCH_BYTES bytes inside the library's device image;
+ * it allocates nothing.
+ *   - Every GPU that loads the library holds that array until the process exits.
+ *   - Shapes that need more scratch than that (kv_workspace_size(
+ *     KV_OP_SCORE_OBS, ...) > KV_SCORE_NOALLOC_SCRATCH_BYTES) are rejected with
+ *     KV_ERR_WORKSPACE before anything is launched.
+ *   - All calls share the one array: calls that overlap on the GPU (different
+ *     streams, or different host threads) race and corrupt each other's
+ *     results, so serialise them.  The array keeps the last call's contents.
+ *   - The first call on each device looks the array's device address up, with
+ *     that device current; make that first call before any stream capture.
+ */
+#define KV_SCORE_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+KVC_API int kv_score_obs_noalloc(const void *Q_obs, const void *K, int B, int Hq, int Hkv, int T,
+                                 int d, int W, float scale, int dtype, float *s_out,
+                                 kv_stream_t stream);
+
 /* Device workspace (bytes) that `op` needs for these sizes; 0 if none.
  * Arguments that an op does not use are ignored; for KV_OP_HUBKV_REFINE pass the
  * refine call's head count H as Hkv.  Returns 0 for invalid sizes. */

@@ -42,6 +42,8 @@ _lib.kv_compact.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, 
 _lib.h2o_decode_step.restype = _I
 _lib.h2o_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
                                  _I, _I, _P, _P, _P, _P]
+_lib.kv_score_obs_noalloc.restype = _I
+_lib.kv_score_obs_noalloc.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P]
 _lib.kv_workspace_size.restype = _Z
 _lib.kv_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I]
 _lib.kv_status_string.restype = ctypes.c_char_p
@@ -112,6 +114,23 @@ def kv_score_obs(Q_obs: torch.Tensor, K: torch.Tensor, scale: float | None = Non
     _check("kv_score_obs", _lib.kv_score_obs(_ptr(Q_obs), _ptr(K), B, Hq, Hkv, T, d, W,
                                              float(scale), _dtype_code(K), _ptr(s), _ptr(ws),
                                              nbytes, _stream(stream)))
+    return s
+
+
+def kv_score_obs_noalloc(Q_obs: torch.Tensor, K: torch.Tensor, scale: float | None = None,
+                         out=None, stream=None) -> torch.Tensor:
+    """kv_score_obs with the library's built-in scratch array instead of a workspace."""
+    B, Hq, W, d = Q_obs.shape
+    B2, Hkv, T, d2 = K.shape
+    if B2 != B or d2 != d or Q_obs.dtype != K.dtype:
+        raise ValueError("Q_obs and K disagree in batch, head dim or dtype")
+    _dev(Q_obs, K, out)
+    if scale is None:
+        scale = d ** -0.5
+    s = out if out is not None else torch.empty(B, Hkv, T, dtype=torch.float32, device=K.device)
+    _check("kv_score_obs_noalloc", _lib.kv_score_obs_noalloc(
+        _ptr(Q_obs), _ptr(K), B, Hq, Hkv, T, d, W, float(scale), _dtype_code(K), _ptr(s),
+        _stream(stream)))
     return s
 
 
