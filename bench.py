@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", default="long-context")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="override the workload's layer count (smaller profiling cases)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -418,6 +420,8 @@ def main():
     from kv_cache_compression_obs_gb300 import configs
 
     wl = configs.BY_NAME[args.config]
+    if args.layers is not None:
+        wl = wl.scaled(L=args.layers)
     rank, world = _env_int("RANK", 0), _env_int("WORLD_SIZE", 1)
     if args.impl == "reference":
         if rank == 0:

@@ -92,11 +92,15 @@ typedef void *kv_stream_t;
  *   scale      logit scale, normally 1/sqrt(d)
  *   s_out      [B][Hkv][T] float32 (written in full)
  *   workspace  >= kv_workspace_size(KV_OP_SCORE_OBS, ...) bytes of device memory
+ *   dev_status device int, may be NULL; set to KV_ERR_TIMEOUT if a bounded
+ *              device-side wait gave up (s_out is then not valid); never cleared
  * Preconditions: 1 <= W <= T, Hq % Hkv == 0, d in {64, 128}.
+ * bf16 inputs with G*W <= 256 run on the tensor cores (tcgen05, TMA); fp32
+ * inputs and larger windows on the CUDA cores; both give the same quantity.
  */
 KVC_API int kv_score_obs(const void *Q_obs, const void *K, int B, int Hq, int Hkv, int T, int d,
                  int W, float scale, int dtype, float *s_out, void *workspace,
-                 size_t workspace_bytes, kv_stream_t stream);
+                 size_t workspace_bytes, int *dev_status, kv_stream_t stream);
 
 /*
  * hubkv_refine -- HubKV refinement of base scores before Top-K
@@ -212,7 +216,7 @@ KVC_API int h2o_decode_step(const void *q, const void *k_new, const void *v_new,
 #define KV_SCORE_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 KVC_API int kv_score_obs_noalloc(const void *Q_obs, const void *K, int B, int Hq, int Hkv, int T,
                                  int d, int W, float scale, int dtype, float *s_out,
-                                 kv_stream_t stream);
+                                 int *dev_status, kv_stream_t stream);
 
 /* Device workspace (bytes) that `op` needs for these sizes; 0 if none.
  * Arguments that an op does not use are ignored; for KV_OP_HUBKV_REFINE pass the

@@ -32,7 +32,7 @@ KV_OP_SCORE_OBS, KV_OP_HUBKV_REFINE, KV_OP_SELECT_TOPK = 1, 2, 3
 
 _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _lib.kv_score_obs.restype = _I
-_lib.kv_score_obs.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _Z, _P]
+_lib.kv_score_obs.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _Z, _P, _P]
 _lib.hubkv_refine.restype = _I
 _lib.hubkv_refine.argtypes = [_P, _I, _I, _I, _I, _F, _F, _F, _F, _P, _P, _P, _Z, _P]
 _lib.kv_select_topk.restype = _I
@@ -43,7 +43,7 @@ _lib.h2o_decode_step.restype = _I
 _lib.h2o_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
                                  _I, _I, _P, _P, _P, _P]
 _lib.kv_score_obs_noalloc.restype = _I
-_lib.kv_score_obs_noalloc.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P]
+_lib.kv_score_obs_noalloc.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P]
 _lib.kv_workspace_size.restype = _Z
 _lib.kv_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I]
 _lib.kv_status_string.restype = ctypes.c_char_p
@@ -99,7 +99,7 @@ def _workspace(nbytes: int, device, given):
 
 
 def kv_score_obs(Q_obs: torch.Tensor, K: torch.Tensor, scale: float | None = None, out=None,
-                 workspace=None, stream=None) -> torch.Tensor:
+                 workspace=None, dev_status=None, stream=None) -> torch.Tensor:
     """Q_obs [B][Hq][W][d], K [B][Hkv][T][d] -> s [B][Hkv][T] float32."""
     B, Hq, W, d = Q_obs.shape
     B2, Hkv, T, d2 = K.shape
@@ -111,14 +111,15 @@ def kv_score_obs(Q_obs: torch.Tensor, K: torch.Tensor, scale: float | None = Non
     s = out if out is not None else torch.empty(B, Hkv, T, dtype=torch.float32, device=K.device)
     ws, nbytes = _workspace(kv_workspace_size(KV_OP_SCORE_OBS, B, Hq, Hkv, T, d, W), K.device,
                             workspace)
+    _dev(dev_status)
     _check("kv_score_obs", _lib.kv_score_obs(_ptr(Q_obs), _ptr(K), B, Hq, Hkv, T, d, W,
                                              float(scale), _dtype_code(K), _ptr(s), _ptr(ws),
-                                             nbytes, _stream(stream)))
+                                             nbytes, _ptr(dev_status), _stream(stream)))
     return s
 
 
 def kv_score_obs_noalloc(Q_obs: torch.Tensor, K: torch.Tensor, scale: float | None = None,
-                         out=None, stream=None) -> torch.Tensor:
+                         out=None, dev_status=None, stream=None) -> torch.Tensor:
     """kv_score_obs with the library's built-in scratch array instead of a workspace."""
     B, Hq, W, d = Q_obs.shape
     B2, Hkv, T, d2 = K.shape
@@ -130,7 +131,7 @@ def kv_score_obs_noalloc(Q_obs: torch.Tensor, K: torch.Tensor, scale: float | No
     s = out if out is not None else torch.empty(B, Hkv, T, dtype=torch.float32, device=K.device)
     _check("kv_score_obs_noalloc", _lib.kv_score_obs_noalloc(
         _ptr(Q_obs), _ptr(K), B, Hq, Hkv, T, d, W, float(scale), _dtype_code(K), _ptr(s),
-        _stream(stream)))
+        _ptr(dev_status), _stream(stream)))
     return s
 
 

@@ -93,7 +93,7 @@ size_t kv_workspace_size(int op, int B, int Hq, int Hkv, int T, int d, int W, in
 
 int kv_score_obs(const void *Q_obs, const void *K, int B, int Hq, int Hkv, int T, int d, int W,
                  float scale, int dtype, float *s_out, void *workspace, size_t workspace_bytes,
-                 kv_stream_t stream) {
+                 int *dev_status, kv_stream_t stream) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || T <= 0 || W <= 0 || W > T ||
       !dtype_ok(dtype) || !(scale == scale))
     return KV_ERR_INVALID_ARG;
@@ -106,7 +106,7 @@ int kv_score_obs(const void *Q_obs, const void *K, int B, int Hq, int Hkv, int T
   const ScorePlan plan = plan_score(B, Hq, Hkv, T, W);
   if (!workspace || workspace_bytes < plan.ws_bytes || !aligned16(workspace)) return KV_ERR_WORKSPACE;
   return launch_score_obs(Q_obs, K, B, Hq, Hkv, T, d, W, scale, dtype, s_out, workspace, plan,
-                          static_cast<cudaStream_t>(stream));
+                          dev_status, static_cast<cudaStream_t>(stream));
 }
 
 int hubkv_refine(const float *s, int B, int H, int T, int pool_width, float gamma, float r,

@@ -57,10 +57,12 @@ template <> struct Vec16<float> {
 // ---- operation plans (shared by the launchers and kv_workspace_size) --------
 struct ScorePlan {
   int gw;          // query rows per unit = G * W
-  int row_blocks;  // ceil(gw / 64)
-  int n_splits;    // key splits of the statistics pass
-  int split_len;   // keys per split (multiple of 64)
-  size_t ws_bytes;
+  int row_blocks;  // ceil(gw / 64)                          (CUDA-core path)
+  int n_splits;    // key splits of the statistics pass      (CUDA-core path)
+  int split_len;   // keys per split (multiple of 128)       (CUDA-core path)
+  int tc_splits;   // key splits per unit of both passes     (tensor-core path)
+  int tc_split_len;  // keys per split (multiple of 128)     (tensor-core path)
+  size_t ws_bytes;   // enough for either path
 };
 ScorePlan plan_score(int B, int Hq, int Hkv, int T, int W);
 
@@ -75,7 +77,13 @@ RefinePlan plan_refine(int B, int H, int T);
 // ---- launchers (validated arguments only) ------------------------------------
 int launch_score_obs(const void *Q, const void *K, int B, int Hq, int Hkv, int T, int d, int W,
                      float scale, int dtype, float *s, void *ws, const ScorePlan &plan,
-                     cudaStream_t st);
+                     int *status, cudaStream_t st);
+int launch_score_combine(const float2 *part, int n_splits, int gw, long rows, float2 *fin,
+                         cudaStream_t st);
+bool score_tc_eligible(int dtype, int d, int Hq, int Hkv, int W);
+int launch_score_obs_tc(const void *Q, const void *K, int B, int Hq, int Hkv, int T, int d, int W,
+                        float scale, float *s, void *ws, const ScorePlan &plan, int *status,
+                        cudaStream_t st);
 int launch_hubkv_refine(const float *s, int B, int H, int T, int pool_width, float gamma,
                         float r, float beta_lo, float beta_hi, float *z, float *beta, void *ws,
                         const RefinePlan &plan, cudaStream_t st);

@@ -12,7 +12,10 @@
 //   2. combine: per row M = max m and 1/Z with Z = sum Z_s 2^(m_s - M);
 //   3. colsum:  per key block, sum over rows of 2^(x - M) / Z.
 // Logits are computed twice (once per pass) in fp32 FMA with 64x64 shared-memory
-// tiles; the sums are fixed-order, so repeated runs give identical bits.
+// tiles; the sums are fixed-order, so repeated runs give identical bits.  This is
+// the path for fp32 inputs and for more than 256 query rows per unit; bf16
+// inputs with up to 256 rows per unit go to the tensor-core kernels of
+// score_obs_tc.cu, which share the combine step and the workspace layout.
 #include <cmath>
 
 #include "kvc_internal.cuh"
@@ -146,6 +149,8 @@ __global__ __launch_bounds__(NT) void score_stats_kernel(
   }
 }
 
+}  // namespace
+
 __global__ void score_combine_kernel(const float2 *__restrict__ part, int n_splits, int gw,
                                      long total_rows, float2 *__restrict__ fin) {
   const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -161,6 +166,14 @@ __global__ void score_combine_kernel(const float2 *__restrict__ part, int n_spli
   }
   fin[i] = make_float2(M, 1.0f / Z);  // every row sees key 0, so Z >= 1
 }
+
+int launch_score_combine(const float2 *part, int n_splits, int gw, long rows, float2 *fin,
+                         cudaStream_t st) {
+  score_combine_kernel<<<(unsigned)((rows + 255) / 256), 256, 0, st>>>(part, n_splits, gw, rows, fin);
+  return launch_status();
+}
+
+namespace {
 
 template <typename T, int D>
 __global__ __launch_bounds__(NT) void score_colsum_kernel(
@@ -251,26 +264,37 @@ int run_score(const void *Q, const void *K, int B, int Hq, int Hkv, int Tlen, in
 
 }  // namespace
 
+// Split T into n pieces of a multiple of 128 keys, n about `want` (at least 1).
+static void split_keys(int T, long want, int *n, int *len) {
+  const int max_splits = (T + 127) / 128;
+  if (want < 1) want = 1;
+  if (want > max_splits) want = max_splits;
+  const int per = (int)((T + want - 1) / want);
+  *len = ((per + 127) / 128) * 128;
+  *n = (T + *len - 1) / *len;
+}
+
 ScorePlan plan_score(int B, int Hq, int Hkv, int T, int W) {
   ScorePlan p{};
   p.gw = (Hq / Hkv) * W;
   p.row_blocks = (p.gw + RB - 1) / RB;
   const long units = (long)B * Hkv;
   const long base = units * p.row_blocks;
-  const int max_splits = (T + KT - 1) / KT;
-  long want = (kTargetCtas + base - 1) / (base > 0 ? base : 1);
-  if (want < 1) want = 1;
-  if (want > max_splits) want = max_splits;
-  const int per = (int)((T + want - 1) / want);
-  p.split_len = ((per + KT - 1) / KT) * KT;
-  p.n_splits = (T + p.split_len - 1) / p.split_len;
-  p.ws_bytes = (size_t)units * (p.n_splits + 1) * p.gw * sizeof(float2);
+  split_keys(T, (kTargetCtas + base - 1) / (base > 0 ? base : 1), &p.n_splits, &p.split_len);
+  // tensor-core path: persistent CTAs walk (unit, split) items; about 16 items per
+  // SM keeps the round-robin tail short
+  const long u = units > 0 ? units : 1;
+  split_keys(T, (16L * kNumSmsHint + u - 1) / u, &p.tc_splits, &p.tc_split_len);
+  const int most = p.n_splits > p.tc_splits ? p.n_splits : p.tc_splits;
+  p.ws_bytes = (size_t)units * (most + 1) * p.gw * sizeof(float2);
   return p;
 }
 
 int launch_score_obs(const void *Q, const void *K, int B, int Hq, int Hkv, int T, int d, int W,
                      float scale, int dtype, float *s, void *ws, const ScorePlan &plan,
-                     cudaStream_t st) {
+                     int *status, cudaStream_t st) {
+  if (score_tc_eligible(dtype, d, Hq, Hkv, W))
+    return launch_score_obs_tc(Q, K, B, Hq, Hkv, T, d, W, scale, s, ws, plan, status, st);
   if (dtype == KV_BF16) {
     if (d == 128) return run_score<__nv_bfloat16, 128>(Q, K, B, Hq, Hkv, T, W, scale, s, ws, plan, st);
     return run_score<__nv_bfloat16, 64>(Q, K, B, Hq, Hkv, T, W, scale, s, ws, plan, st);

@@ -52,7 +52,7 @@ void *scratch_on(int dev) {
 
 extern "C" int kv_score_obs_noalloc(const void *Q_obs, const void *K, int B, int Hq, int Hkv,
                                     int T, int d, int W, float scale, int dtype, float *s_out,
-                                    kv_stream_t stream) {
+                                    int *dev_status, kv_stream_t stream) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || T <= 0 || W <= 0 || W > T ||
       !(dtype == KV_BF16 || dtype == KV_F32) || !(scale == scale))
     return KV_ERR_INVALID_ARG;
@@ -71,5 +71,5 @@ extern "C" int kv_score_obs_noalloc(const void *Q_obs, const void *K, int B, int
   void *scratch = scratch_on(dev);
   if (!scratch) return KV_ERR_CUDA;
   return kvc::launch_score_obs(Q_obs, K, B, Hq, Hkv, T, d, W, scale, dtype, s_out, scratch, plan,
-                               static_cast<cudaStream_t>(stream));
+                               dev_status, static_cast<cudaStream_t>(stream));
 }

@@ -1,0 +1,532 @@
+// score_obs_tc.cu -- observation-window scoring on the 5th-generation tensor cores.
+//
+// Same quantity as score_obs.cu (the accumulated attention of the H2O page,
+// 观察二, over SnapKV's observation window, KV-cache blog §4.3), for bf16 inputs
+// with G*W <= 256 query rows per unit (every GQA / MHA prefill workload).
+// The logits are produced by tcgen05.mma (bf16 x bf16 -> fp32 in TMEM) from
+// TMA-staged, 128-byte-swizzled shared-memory tiles:
+//
+//   pass 1 (statistics): D[rows x keys] = Q K^T with the query rows on the TMEM
+//     lanes, so every epilogue thread owns one row and keeps its running max and
+//     normaliser in registers (no cross-thread reduction);
+//   combine: per row M = max and 1/Z over the key splits (score_obs.cu);
+//   pass 2 (column mass): D[keys x rows] = K Q^T with the keys on the TMEM lanes,
+//     so every epilogue thread owns one key and sums 2^(x - M_r) / Z_r over the
+//     rows in registers.
+//
+// Both kernels are persistent (one CTA per SM, items assigned round-robin) and
+// warp-specialised: warp 0 issues TMA loads into a 4-stage K ring (the unit's Q
+// block stays resident per item), warp 1 issues the MMAs into two TMEM slots,
+// warps 2..9 (two warpgroups) drain TMEM.  Every mbarrier wait is bounded; a
+// wait that gives up sets a CTA-wide abort flag and the device status
+// KV_ERR_TIMEOUT, the roles leave their loops, outstanding copies and MMAs are
+// waited for (again bounded) and the TMEM is freed before the CTA exits.
+#include <cmath>
+
+#include "kvc_internal.cuh"
+#include "tc_common.cuh"
+
+namespace kvc {
+namespace {
+
+constexpr int NT = 320;        // 10 warps
+constexpr int KT = 128;        // keys per tile (the UMMA M of pass 2, N of pass 1)
+constexpr int QROWS = 256;     // resident query rows per unit
+constexpr int STAGES = 4;      // K ring depth
+constexpr int TMEM_COLS = 512;
+constexpr long long kWaitBudget = 4000000000LL;  // clock cycles (~2 s) before a wait gives up
+constexpr long long kDrainBudget = 200000000LL;  // ~0.1 s for in-flight copies / MMAs at exit
+
+template <int D>
+struct Geo {
+  static constexpr int NKB = D / 64;                  // 128-byte k-blocks per row
+  static constexpr int KBYTES = KT * D * 2;           // one K tile
+  static constexpr int QBYTES = QROWS * D * 2;        // resident Q block
+  static constexpr int KSUB = KT * 128;               // bytes of one k-block of a K tile
+  static constexpr int QSUB = QROWS * 128;            // bytes of one k-block of the Q block
+  static constexpr int BAR_OFF = QBYTES + STAGES * KBYTES;   // 1024-aligned
+  // barriers: full[S], empty[S], qfull, qempty, tfull[2], tempty[2], drain
+  static constexpr int NBARS = 2 * STAGES + 7;
+  static constexpr int MISC_OFF = BAR_OFF + 256;              // TMEM base, abort flag
+  static constexpr int STAT_OFF = BAR_OFF + 512;              // row M, 1/Z, position (16-aligned)
+  static constexpr int RED_OFF = STAT_OFF + QROWS * 12;       // warpgroup exchange
+  // at least 116 KB so that a single CTA fits per SM: each CTA takes all 512 TMEM columns
+  static constexpr int SMEM_NEED = 1024 /*alignment slack*/ + RED_OFF + KT * 4;
+  static constexpr int SMEM = SMEM_NEED > 116 * 1024 ? SMEM_NEED : 116 * 1024;
+  static_assert(NBARS * 8 <= 256, "barrier area");
+};
+
+struct Bars {
+  uint64_t *full, *empty, *qfull, *qempty, *tfull, *tempty, *drain;
+};
+
+__device__ __forceinline__ unsigned char *align1024(unsigned char *p) {
+  return reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+__device__ __forceinline__ Bars carve_bars(unsigned char *base) {
+  uint64_t *b = reinterpret_cast<uint64_t *>(base);
+  return Bars{b, b + STAGES, b + 2 * STAGES, b + 2 * STAGES + 1, b + 2 * STAGES + 2,
+              b + 2 * STAGES + 4, b + 2 * STAGES + 6};
+}
+
+__device__ __forceinline__ void init_bars(const Bars &B) {
+  for (int i = 0; i < STAGES; ++i) {
+    tc::mbar_init(B.full + i, 1);
+    tc::mbar_init(B.empty + i, 1);
+  }
+  tc::mbar_init(B.qfull, 1);
+  tc::mbar_init(B.qempty, 1);
+  for (int i = 0; i < 2; ++i) {
+    tc::mbar_init(B.tfull + i, 1);
+    tc::mbar_init(B.tempty + i, 8);  // one arrival per epilogue warp
+  }
+  tc::mbar_init(B.drain, 1);
+  tc::mbar_fence_init();
+}
+
+// Work decomposition shared by the three roles: item -> (unit, key range).
+struct Item {
+  long unit;
+  int j_begin, j_end;  // keys [j_begin, j_end)
+};
+__device__ __forceinline__ Item item_of(int item, int per_unit, int span, int T) {
+  Item it;
+  it.unit = item / per_unit;
+  const int c = item % per_unit;
+  it.j_begin = c * span;
+  it.j_end = min(T, it.j_begin + span);
+  return it;
+}
+
+__device__ __forceinline__ void set_abort(volatile int *abort_flag, int *status) {
+  *abort_flag = 1;
+  if (status) atomicExch(status, (int)KV_ERR_TIMEOUT);
+}
+
+// ---------------------------------------------------------------------------
+// Producer (warp 0, one lane): Q block per item, K tiles through the ring.
+// ---------------------------------------------------------------------------
+template <int D>
+__device__ void produce(const CUtensorMap *tmQ, const CUtensorMap *tmK, unsigned char *sQ,
+                        unsigned char *sK, const Bars &B, int n_items, int per_unit, int span,
+                        int Hq, int Hkv, int T, int W, volatile int *abort_flag, int *status) {
+  using G = Geo<D>;
+  tc::tma_prefetch_desc(tmQ);
+  tc::tma_prefetch_desc(tmK);
+  const int Gq = Hq / Hkv;
+  uint32_t g = 0;
+  int it = 0;
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
+    const Item w = item_of(item, per_unit, span, T);
+    const long b = w.unit / Hkv;
+    const int h = static_cast<int>(w.unit % Hkv);
+    const int qrow0 = static_cast<int>((b * Hq + (long)h * Gq) * W);
+    if (!tc::mbar_wait(B.qempty, (it & 1) ^ 1, kWaitBudget, abort_flag)) {
+      set_abort(abort_flag, status);
+      break;
+    }
+    tc::mbar_arrive_expect_tx(B.qfull, G::QBYTES);
+    for (int kb = 0; kb < G::NKB; ++kb)
+      for (int half = 0; half < 2; ++half)
+        tc::tma_load_2d(sQ + kb * G::QSUB + half * 128 * 128, tmQ, kb * 64, qrow0 + half * 128, B.qfull);
+    bool ok = true;
+    for (int j0 = w.j_begin; j0 < w.j_end; j0 += KT, ++g) {
+      const int st = g % STAGES;
+      const uint32_t use = g / STAGES;
+      if (!tc::mbar_wait(B.empty + st, (use & 1) ^ 1, kWaitBudget, abort_flag)) {
+        set_abort(abort_flag, status);
+        ok = false;
+        break;
+      }
+      tc::mbar_arrive_expect_tx(B.full + st, G::KBYTES);
+      const int krow = static_cast<int>(w.unit * (long)T + j0);
+      for (int kb = 0; kb < G::NKB; ++kb)
+        tc::tma_load_2d(sK + st * G::KBYTES + kb * G::KSUB, tmK, kb * 64, krow, B.full + st);
+    }
+    if (!ok) break;
+  }
+  // copies still in flight land before the CTA may exit: wait for the last
+  // uses of every stage (bounded; completed phases return at once)
+  for (int k = 1; k <= STAGES && (int)g - k >= 0; ++k) {
+    const uint32_t gg = g - k;
+    tc::mbar_wait(B.full + gg % STAGES, (gg / STAGES) & 1, kDrainBudget, nullptr);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// MMA issuer (warp 1, one lane).  PASS 1: D[row, key] for the one or two
+// 128-row M-tiles of Q.  PASS 2: D[key, row], N = n_cols query rows.
+// ---------------------------------------------------------------------------
+template <int D, int PASS>
+__device__ void issue(uint32_t tmem, unsigned char *sQ, unsigned char *sK, const Bars &B,
+                      int n_items, int per_unit, int span, int T, int n_mt, int n_cols,
+                      volatile int *abort_flag, int *status) {
+  using G = Geo<D>;
+  const uint32_t q_addr = tc::smem_u32(sQ);
+  const uint32_t k_addr = tc::smem_u32(sK);
+  const uint32_t idesc = (PASS == 1) ? tc::idesc_bf16(128, KT) : tc::idesc_bf16(128, n_cols);
+  uint32_t g = 0;
+  int it = 0;
+  bool ok = true;
+  for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++it) {
+    const Item w = item_of(item, per_unit, span, T);
+    if (!tc::mbar_wait(B.qfull, it & 1, kWaitBudget, abort_flag)) {
+      set_abort(abort_flag, status);
+      break;
+    }
+    tc::fence_after_sync();
+    for (int j0 = w.j_begin; j0 < w.j_end; j0 += KT, ++g) {
+      const int st = g % STAGES;
+      const uint32_t use = g / STAGES;
+      const int slot = g & 1;
+      const uint32_t tuse = g >> 1;
+      if (!tc::mbar_wait(B.full + st, use & 1, kWaitBudget, abort_flag) ||
+          !tc::mbar_wait(B.tempty + slot, (tuse & 1) ^ 1, kWaitBudget, abort_flag)) {
+        set_abort(abort_flag, status);
+        ok = false;
+        break;
+      }
+      tc::fence_after_sync();
+      const uint32_t kst = k_addr + st * G::KBYTES;
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t koff = (kk / 4) * G::KSUB + (kk % 4) * 32;
+        const uint32_t qoff = (kk / 4) * G::QSUB + (kk % 4) * 32;
+        if (PASS == 1) {
+          for (int mt = 0; mt < n_mt; ++mt)
+            tc::umma_bf16(tmem + slot * 256 + mt * 128, tc::sdesc_sw128(q_addr + qoff + mt * 128 * 128),
+                          tc::sdesc_sw128(kst + koff), idesc, kk > 0);
+        } else {
+          tc::umma_bf16(tmem + slot * 256, tc::sdesc_sw128(kst + koff), tc::sdesc_sw128(q_addr + qoff),
+                        idesc, kk > 0);
+        }
+      }
+      tc::umma_commit(B.empty + st);
+      tc::umma_commit(B.tfull + slot);
+    }
+    if (ok) tc::umma_commit(B.qempty);
+  }
+  // every MMA issued above completes before TMEM can be released
+  tc::umma_commit(B.drain);
+  tc::mbar_wait(B.drain, 0, kDrainBudget, nullptr);
+}
+
+// ---------------------------------------------------------------------------
+// Pass 1: per-row running max and normaliser over a key split.
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(NT, 1)
+    score_stats_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                          int Hq, int Hkv, int T, int W, int gw, int per_unit, int span, int n_items,
+                          float c_log2, float2 *__restrict__ part, int *__restrict__ status) {
+  using G = Geo<D>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *sm = align1024(smem_raw);
+  unsigned char *sQ = sm;
+  unsigned char *sK = sm + G::QBYTES;
+  const Bars B = carve_bars(sm + G::BAR_OFF);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + G::MISC_OFF);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_mt = gw > 128 ? 2 : 1;
+
+  if (threadIdx.x == 0) {
+    init_bars(B);
+    *abort_flag = 0;
+  }
+  if (warp == 1) tc::tmem_alloc(tmem_slot, TMEM_COLS);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0)
+      produce<D>(&tmQ, &tmK, sQ, sK, B, n_items, per_unit, span, Hq, Hkv, T, W, abort_flag, status);
+  } else if (warp == 1) {
+    if (lane == 0)
+      issue<D, 1>(tmem, sQ, sK, B, n_items, per_unit, span, T, n_mt, 0, abort_flag, status);
+  } else {
+    const int ew = warp - 2;
+    const int mt = ew >> 2;                 // M-tile (rows 0..127 or 128..255)
+    const int quarter = warp & 3;           // TMEM lane quarter this warp may access
+    const int row = mt * 128 + quarter * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    uint32_t g = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      const Item w = item_of(item, per_unit, span, T);
+      const int p_row = T - W + (row % W);
+      const int jlim = min(w.j_end, p_row + 1);  // keys this row may see in the split
+      float m = -INFINITY, z = 0.f;
+      for (int j0 = w.j_begin; j0 < w.j_end; j0 += KT, ++g) {
+        const int slot = g & 1;
+        const uint32_t tuse = g >> 1;
+        if (!tc::mbar_wait(B.tfull + slot, tuse & 1, kWaitBudget, abort_flag)) {
+          set_abort(abort_flag, status);
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        if (mt < n_mt) {
+#pragma unroll 1
+          for (int half = 0; half < 2; ++half) {
+            uint32_t r[4][16];
+            const uint32_t col = tmem + lane_addr + slot * 256 + mt * 128 + half * 64;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tc::tmem_ld16(col + q * 16, r[q]);
+            tc::tmem_ld_wait();
+            const int jb = j0 + half * 64;
+            const bool full = jb + 64 <= jlim;
+            float cm = -INFINITY;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+              for (int c = 0; c < 16; ++c) {
+                const float x = __uint_as_float(r[q][c]);
+                if (full || jb + q * 16 + c < jlim) cm = fmaxf(cm, x);
+              }
+            if (cm != -INFINITY) {
+              const float mnew = fmaxf(m, cm * c_log2);
+              float acc = 0.f;
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                  const float e = tc::ex2(fmaf(__uint_as_float(r[q][c]), c_log2, -mnew));
+                  acc += (full || jb + q * 16 + c < jlim) ? e : 0.f;
+                }
+              z = z * tc::ex2(m - mnew) + acc;
+              m = mnew;
+            }
+          }
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(B.tempty + slot);
+      }
+      if (ok && mt < n_mt && row < gw) {
+        const int split = item % per_unit;
+        part[(w.unit * per_unit + split) * gw + row] = make_float2(m, z);
+      }
+    }
+  }
+  __syncwarp();  // lanes that skipped a single-lane role rejoin their warp
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Pass 2: column mass s_j = sum_r 2^(x_rj - M_r) / Z_r over a key chunk.
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(NT, 1)
+    score_colsum_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                           int Hq, int Hkv, int T, int W, int gw, int n_cols, int per_unit, int span,
+                           int n_items, float c_log2, const float2 *__restrict__ fin,
+                           float *__restrict__ s_out, int *__restrict__ status) {
+  using G = Geo<D>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *sm = align1024(smem_raw);
+  unsigned char *sQ = sm;
+  unsigned char *sK = sm + G::QBYTES;
+  const Bars B = carve_bars(sm + G::BAR_OFF);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + G::MISC_OFF);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  float *sM = reinterpret_cast<float *>(sm + G::STAT_OFF);
+  float *sZ = sM + QROWS;
+  int *sPos = reinterpret_cast<int *>(sZ + QROWS);
+  float *sRed = reinterpret_cast<float *>(sm + G::RED_OFF);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    init_bars(B);
+    *abort_flag = 0;
+  }
+  if (warp == 1) tc::tmem_alloc(tmem_slot, TMEM_COLS);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0)
+      produce<D>(&tmQ, &tmK, sQ, sK, B, n_items, per_unit, span, Hq, Hkv, T, W, abort_flag, status);
+  } else if (warp == 1) {
+    if (lane == 0)
+      issue<D, 2>(tmem, sQ, sK, B, n_items, per_unit, span, T, 0, n_cols, abort_flag, status);
+  } else {
+    const int et = threadIdx.x - 64;        // 0..255
+    const int ew = warp - 2;
+    const int wg = ew >> 2;                 // column half handled by this warpgroup
+    const int quarter = warp & 3;
+    const int key_in_tile = quarter * 32 + lane;
+    const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    const int n_chunks = n_cols / 16;
+    const int first_masked = T - W;         // keys below this are seen by every row
+    uint32_t g = 0;
+    bool ok = true;
+    // A warp that gives up keeps walking the same items and tiles (without
+    // touching TMEM) so that every named barrier below is reached by all 256
+    // epilogue threads.
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+      const Item w = item_of(item, per_unit, span, T);
+      tc::named_bar_sync(1, 256);           // the previous item's readers are done
+      for (int r = et; r < QROWS; r += 256) {
+        if (r < gw) {
+          const float2 f = fin[w.unit * gw + r];
+          sM[r] = f.x;
+          sZ[r] = f.y;
+          sPos[r] = T - W + (r % W);
+        } else {
+          sM[r] = INFINITY;  // padding rows contribute 2^-inf * 0 = 0
+          sZ[r] = 0.f;
+          sPos[r] = -1;
+        }
+      }
+      tc::named_bar_sync(1, 256);
+      for (int j0 = w.j_begin; j0 < w.j_end; j0 += KT, ++g) {
+        const int slot = g & 1;
+        const uint32_t tuse = g >> 1;
+        if (ok && !tc::mbar_wait(B.tfull + slot, tuse & 1, kWaitBudget, abort_flag)) {
+          set_abort(abort_flag, status);
+          ok = false;
+        }
+        const int j = j0 + key_in_tile;
+        float acc = 0.f;
+        if (ok) {
+          tc::fence_after_sync();
+          const bool masked = j0 + KT > first_masked;
+#pragma unroll 1
+          for (int ch = wg; ch < n_chunks; ch += 2) {
+            uint32_t r[16];
+            tc::tmem_ld16(tmem + lane_addr + slot * 256 + ch * 16, r);
+            tc::tmem_ld_wait();
+            const float4 *m4 = reinterpret_cast<const float4 *>(sM + ch * 16);
+            const float4 *z4 = reinterpret_cast<const float4 *>(sZ + ch * 16);
+            const int4 *p4 = reinterpret_cast<const int4 *>(sPos + ch * 16);
+            float blk = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float4 mm = m4[q], zz = z4[q];
+              const float e0 = tc::ex2(fmaf(__uint_as_float(r[4 * q + 0]), c_log2, -mm.x)) * zz.x;
+              const float e1 = tc::ex2(fmaf(__uint_as_float(r[4 * q + 1]), c_log2, -mm.y)) * zz.y;
+              const float e2 = tc::ex2(fmaf(__uint_as_float(r[4 * q + 2]), c_log2, -mm.z)) * zz.z;
+              const float e3 = tc::ex2(fmaf(__uint_as_float(r[4 * q + 3]), c_log2, -mm.w)) * zz.w;
+              if (!masked) {
+                blk += (e0 + e1) + (e2 + e3);
+              } else {
+                const int4 pp = p4[q];
+                blk += ((j <= pp.x ? e0 : 0.f) + (j <= pp.y ? e1 : 0.f)) +
+                       ((j <= pp.z ? e2 : 0.f) + (j <= pp.w ? e3 : 0.f));
+              }
+            }
+            acc += blk;
+          }
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(B.tempty + slot);
+        }
+        // add the two warpgroups' halves and store the key's mass
+        if (wg == 1) sRed[key_in_tile] = acc;
+        tc::named_bar_sync(1, 256);
+        if (ok && wg == 0 && j < w.j_end) s_out[w.unit * (long)T + j] = acc + sRed[key_in_tile];
+        tc::named_bar_sync(1, 256);
+      }
+    }
+  }
+  __syncwarp();  // lanes that skipped a single-lane role rejoin their warp
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+    else
+      cudaGetLastError();
+  }
+  return fn;
+}
+
+// rows x d bf16 matrix, boxes of 64 elements x 128 rows, 128-byte swizzle.
+bool encode_rows(CUtensorMap *map, const void *base, long rows, int d) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int D>
+int run_tc(const void *Q, const void *K, int B, int Hq, int Hkv, int T, int W, float scale,
+           float *s, void *ws, const ScorePlan &plan, int *status, cudaStream_t st) {
+  using G = Geo<D>;
+  const long units = (long)B * Hkv;
+  float2 *part = static_cast<float2 *>(ws);
+  float2 *fin = part + units * plan.tc_splits * plan.gw;
+  CUtensorMap tmQ, tmK;
+  if (!encode_rows(&tmQ, Q, (long)B * Hq * W, D) || !encode_rows(&tmK, K, units * T, D))
+    return KV_ERR_CUDA;
+  if (ensure_smem((const void *)score_stats_tc_kernel<D>, G::SMEM) ||
+      ensure_smem((const void *)score_colsum_tc_kernel<D>, G::SMEM))
+    return KV_ERR_CUDA;
+  const float c_log2 = scale * 1.4426950408889634f;
+  const int sms = device_sm_count();
+  const int n1 = (int)(units * plan.tc_splits);
+  score_stats_tc_kernel<D><<<min(n1, sms), NT, G::SMEM, st>>>(
+      tmQ, tmK, Hq, Hkv, T, W, plan.gw, plan.tc_splits, plan.tc_split_len, n1, c_log2, part, status);
+  int rc = launch_score_combine(part, plan.tc_splits, plan.gw, units * plan.gw, fin, st);
+  if (rc != KV_OK) return rc;
+  const int n2 = (int)(units * plan.tc_splits);
+  const int n_cols = ((plan.gw + 15) / 16) * 16;
+  score_colsum_tc_kernel<D><<<min(n2, sms), NT, G::SMEM, st>>>(
+      tmQ, tmK, Hq, Hkv, T, W, plan.gw, n_cols, plan.tc_splits, plan.tc_split_len, n2, c_log2, fin,
+      s, status);
+  return launch_status(2);
+}
+
+}  // namespace
+
+bool score_tc_eligible(int dtype, int d, int Hq, int Hkv, int W) {
+  const long gw = (long)(Hq / Hkv) * W;
+  return dtype == KV_BF16 && (d == 64 || d == 128) && gw <= QROWS;
+}
+
+int launch_score_obs_tc(const void *Q, const void *K, int B, int Hq, int Hkv, int T, int d, int W,
+                        float scale, float *s, void *ws, const ScorePlan &plan, int *status,
+                        cudaStream_t st) {
+  if (d == 128) return run_tc<128>(Q, K, B, Hq, Hkv, T, W, scale, s, ws, plan, status, st);
+  return run_tc<64>(Q, K, B, Hq, Hkv, T, W, scale, s, ws, plan, status, st);
+}
+
+}  // namespace kvc

@@ -16,7 +16,7 @@ def lib():
     path = build()
     lib = ctypes.CDLL(path)
     P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
-    lib.kv_score_obs.argtypes = [P, P, I, I, I, I, I, I, F, I, P, P, Z, P]
+    lib.kv_score_obs.argtypes = [P, P, I, I, I, I, I, I, F, I, P, P, Z, P, P]
     lib.hubkv_refine.argtypes = [P, I, I, I, I, F, F, F, F, P, P, P, Z, P]
     lib.kv_select_topk.argtypes = [P, I, I, I, I, I, P, P, Z, P]
     lib.kv_compact.argtypes = [P, P, P, P, I, I, I, I, I, I, P, P, I, P, P, P, P]
@@ -60,11 +60,11 @@ NULL = None
 
 def test_host_validation_rejects_before_cuda(lib):
     # score: W > T, Hq % Hkv, d unsupported, null pointers
-    assert lib.kv_score_obs(NULL, NULL, 1, 4, 2, 10, 64, 11, 0.1, 0, NULL, NULL, 0, NULL) == -1
-    assert lib.kv_score_obs(NULL, NULL, 1, 3, 2, 10, 64, 4, 0.1, 0, NULL, NULL, 0, NULL) == -1
-    assert lib.kv_score_obs(NULL, NULL, 1, 4, 2, 10, 96, 4, 0.1, 0, NULL, NULL, 0, NULL) == -2
-    assert lib.kv_score_obs(NULL, NULL, 1, 4, 2, 10, 64, 4, 0.1, 7, NULL, NULL, 0, NULL) == -1
-    assert lib.kv_score_obs(NULL, NULL, 1, 4, 2, 10, 64, 4, 0.1, 0, NULL, NULL, 0, NULL) == -1
+    assert lib.kv_score_obs(NULL, NULL, 1, 4, 2, 10, 64, 11, 0.1, 0, NULL, NULL, 0, NULL, NULL) == -1
+    assert lib.kv_score_obs(NULL, NULL, 1, 3, 2, 10, 64, 4, 0.1, 0, NULL, NULL, 0, NULL, NULL) == -1
+    assert lib.kv_score_obs(NULL, NULL, 1, 4, 2, 10, 96, 4, 0.1, 0, NULL, NULL, 0, NULL, NULL) == -2
+    assert lib.kv_score_obs(NULL, NULL, 1, 4, 2, 10, 64, 4, 0.1, 7, NULL, NULL, 0, NULL, NULL) == -1
+    assert lib.kv_score_obs(NULL, NULL, 1, 4, 2, 10, 64, 4, 0.1, 0, NULL, NULL, 0, NULL, NULL) == -1
     # refine: even pool width, bad clip range
     assert lib.hubkv_refine(NULL, 1, 2, 10, 4, 0.5, 0.1, 0.8, 1.2, NULL, NULL, NULL, 0, NULL) == -1
     assert lib.hubkv_refine(NULL, 1, 2, 10, 5, 0.5, 0.1, 1.3, 1.2, NULL, NULL, NULL, 0, NULL) == -1
@@ -85,7 +85,7 @@ def test_host_validation_rejects_before_cuda(lib):
 
 
 def test_empty_batch_is_a_no_op(lib):
-    assert lib.kv_score_obs(NULL, NULL, 0, 4, 2, 10, 64, 4, 0.1, 0, NULL, NULL, 0, NULL) == 0
+    assert lib.kv_score_obs(NULL, NULL, 0, 4, 2, 10, 64, 4, 0.1, 0, NULL, NULL, 0, NULL, NULL) == 0
     assert lib.hubkv_refine(NULL, 0, 2, 10, 5, 0.5, 0.1, 0.8, 1.2, NULL, NULL, NULL, 0, NULL) == 0
     assert lib.kv_select_topk(NULL, 0, 2, 10, 5, 3, NULL, NULL, 0, NULL) == 0
     assert lib.kv_compact(NULL, NULL, NULL, NULL, 0, 2, 10, 5, 64, 0, NULL, NULL, 5, NULL, NULL,

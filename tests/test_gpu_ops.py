@@ -34,6 +34,13 @@ SCORE_CASES = [
     (3, 2, 2, 130, 1, 64, "f32", {}),                                     # W = 1
     (1, 8, 1, 300, 40, 128, "f32", {}),                                   # MQA-like group of 8
     (1, 32, 32, 4096, 32, 128, "bf16", dict(n_segments=40, R=32)),        # Llama-2-7B layer
+    # tensor-core path boundaries: G*W = 256 (two M-tiles, N = 256), 129 (second
+    # M-tile with one row), 200 (N padded to 208), 128; d = 64; ragged T
+    (2, 8, 2, 5000, 64, 128, "bf16", dict(n_segments=30, n_sinks=4, R=64)),
+    (1, 3, 1, 1000, 43, 128, "bf16", dict(keys="zipf")),
+    (1, 8, 2, 3333, 50, 64, "bf16", dict(n_segments=10, R=50)),
+    (3, 4, 4, 700, 128, 128, "bf16", dict(keys="zipf")),
+    (1, 1, 1, 130, 1, 128, "bf16", {}),
 ]
 
 

@@ -25,13 +25,13 @@ def _c_noalloc(lib, Q, K, s, scale):
     fn = lib.kv_score_obs_noalloc
     P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     fn.restype = I
-    fn.argtypes = [P, P, I, I, I, I, I, I, F, I, P, P]
+    fn.argtypes = [P, P, I, I, I, I, I, I, F, I, P, P, P]
     B, Hq, W, d = Q.shape
     _, Hkv, T, _ = K.shape
     dt = 0 if K.dtype == torch.bfloat16 else 1
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     return fn(ctypes.c_void_p(Q.data_ptr()), ctypes.c_void_p(K.data_ptr()), B, Hq, Hkv, T, d, W,
-              float(scale), dt, ctypes.c_void_p(s.data_ptr()), stream)
+              float(scale), dt, ctypes.c_void_p(s.data_ptr()), None, stream)
 
 
 WORKLOADS = [
