@@ -51,7 +51,7 @@ struct Geo {
   static constexpr int STAT_OFF = BAR_OFF + 512;              // row M, 1/Z, position (16-aligned)
   static constexpr int RED_OFF = STAT_OFF + QROWS * 12;       // warpgroup exchange
   // at least 116 KB so that a single CTA fits per SM: each CTA takes all 512 TMEM columns
-  static constexpr int SMEM_NEED = 1024 /*alignment slack*/ + RED_OFF + KT * 4;
+  static constexpr int SMEM_NEED = 1024 /*alignment slack*/ + RED_OFF + 2 * KT * 4;
   static constexpr int SMEM = SMEM_NEED > 116 * 1024 ? SMEM_NEED : 116 * 1024;
   static_assert(NBARS * 8 <= 256, "barrier area");
 };
@@ -212,6 +212,26 @@ __device__ void issue(uint32_t tmem, unsigned char *sQ, unsigned char *sK, const
   tc::mbar_wait(B.drain, 0, kDrainBudget, nullptr);
 }
 
+// Sums above this force the exact-max path of the statistics epilogue: every
+// term is then at most 2^64, so the running normaliser cannot overflow.
+constexpr float kLazyLimit = 1.8446744e19f;
+
+// sum_c 2^(x_c * c_log2 - m) over 64 logits, two at a time with packed fp32 math.
+__device__ __forceinline__ float chunk_sum(const uint32_t (&r)[64], float c_log2, float m) {
+  const float2 c2 = make_float2(c_log2, c_log2);
+  const float2 nm2 = make_float2(-m, -m);
+  float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int c = 0; c < 64; c += 4) {
+    const float2 x0 = __ffma2_rn(make_float2(__uint_as_float(r[c]), __uint_as_float(r[c + 1])), c2, nm2);
+    const float2 x1 = __ffma2_rn(make_float2(__uint_as_float(r[c + 2]), __uint_as_float(r[c + 3])), c2, nm2);
+    a0 = __fadd2_rn(a0, make_float2(tc::ex2(x0.x), tc::ex2(x0.y)));
+    a1 = __fadd2_rn(a1, make_float2(tc::ex2(x1.x), tc::ex2(x1.y)));
+  }
+  const float2 a = __fadd2_rn(a0, a1);
+  return a.x + a.y;
+}
+
 // ---------------------------------------------------------------------------
 // Pass 1: per-row running max and normaliser over a key split.
 // ---------------------------------------------------------------------------
@@ -272,31 +292,40 @@ __global__ void __launch_bounds__(NT, 1)
         if (mt < n_mt) {
 #pragma unroll 1
           for (int half = 0; half < 2; ++half) {
-            uint32_t r[4][16];
+            uint32_t r[64];
             const uint32_t col = tmem + lane_addr + slot * 256 + mt * 128 + half * 64;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) tc::tmem_ld16(col + q * 16, r[q]);
+            for (int q = 0; q < 4; ++q)
+              tc::tmem_ld16(col + q * 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16 * q]));
             tc::tmem_ld_wait();
             const int jb = j0 + half * 64;
-            const bool full = jb + 64 <= jlim;
-            float cm = -INFINITY;
+            if (jb + 64 <= jlim) {
+              // every key visible: sum against the running reference m; only a
+              // sum large enough to risk overflow (or the first chunk, m = -inf)
+              // takes the exact-max path
+              float sum = chunk_sum(r, c_log2, m);
+              if (!(sum <= kLazyLimit)) {
+                float cm = -INFINITY;
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-#pragma unroll
-              for (int c = 0; c < 16; ++c) {
-                const float x = __uint_as_float(r[q][c]);
-                if (full || jb + q * 16 + c < jlim) cm = fmaxf(cm, x);
+                for (int c = 0; c < 64; ++c) cm = fmaxf(cm, __uint_as_float(r[c]));
+                const float mnew = fmaxf(m, cm * c_log2);
+                sum = chunk_sum(r, c_log2, mnew);
+                z = z * tc::ex2(m - mnew);
+                m = mnew;
               }
-            if (cm != -INFINITY) {
+              z += sum;
+            } else if (jb < jlim) {
+              float cm = -INFINITY;
+#pragma unroll
+              for (int c = 0; c < 64; ++c)
+                if (jb + c < jlim) cm = fmaxf(cm, __uint_as_float(r[c]));
               const float mnew = fmaxf(m, cm * c_log2);
               float acc = 0.f;
 #pragma unroll
-              for (int q = 0; q < 4; ++q)
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                  const float e = tc::ex2(fmaf(__uint_as_float(r[q][c]), c_log2, -mnew));
-                  acc += (full || jb + q * 16 + c < jlim) ? e : 0.f;
-                }
+              for (int c = 0; c < 64; ++c) {
+                const float e = tc::ex2(fmaf(__uint_as_float(r[c]), c_log2, -mnew));
+                acc += (jb + c < jlim) ? e : 0.f;
+              }
               z = z * tc::ex2(m - mnew) + acc;
               m = mnew;
             }
@@ -380,11 +409,11 @@ __global__ void __launch_bounds__(NT, 1)
       for (int r = et; r < QROWS; r += 256) {
         if (r < gw) {
           const float2 f = fin[w.unit * gw + r];
-          sM[r] = f.x;
+          sM[r] = -f.x;  // stored negated: the exponent is one fma, x * c_log2 + (-M)
           sZ[r] = f.y;
           sPos[r] = T - W + (r % W);
         } else {
-          sM[r] = INFINITY;  // padding rows contribute 2^-inf * 0 = 0
+          sM[r] = -INFINITY;  // padding rows contribute 2^-inf * 0 = 0
           sZ[r] = 0.f;
           sPos[r] = -1;
         }
@@ -402,41 +431,54 @@ __global__ void __launch_bounds__(NT, 1)
         if (ok) {
           tc::fence_after_sync();
           const bool masked = j0 + KT > first_masked;
+          float2 acc2 = make_float2(0.f, 0.f);
+          const float2 c2 = make_float2(c_log2, c_log2);
 #pragma unroll 1
-          for (int ch = wg; ch < n_chunks; ch += 2) {
-            uint32_t r[16];
-            tc::tmem_ld16(tmem + lane_addr + slot * 256 + ch * 16, r);
+          for (int ch0 = wg; ch0 < n_chunks; ch0 += 8) {
+            // up to four 16-column loads in flight before one wait
+            uint32_t r[4][16];
+            const int nq = min(4, (n_chunks - ch0 + 1) / 2);
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              if (q < nq) tc::tmem_ld16(tmem + lane_addr + slot * 256 + (ch0 + 2 * q) * 16, r[q]);
             tc::tmem_ld_wait();
-            const float4 *m4 = reinterpret_cast<const float4 *>(sM + ch * 16);
-            const float4 *z4 = reinterpret_cast<const float4 *>(sZ + ch * 16);
-            const int4 *p4 = reinterpret_cast<const int4 *>(sPos + ch * 16);
-            float blk = 0.f;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const float4 mm = m4[q], zz = z4[q];
-              const float e0 = tc::ex2(fmaf(__uint_as_float(r[4 * q + 0]), c_log2, -mm.x)) * zz.x;
-              const float e1 = tc::ex2(fmaf(__uint_as_float(r[4 * q + 1]), c_log2, -mm.y)) * zz.y;
-              const float e2 = tc::ex2(fmaf(__uint_as_float(r[4 * q + 2]), c_log2, -mm.z)) * zz.z;
-              const float e3 = tc::ex2(fmaf(__uint_as_float(r[4 * q + 3]), c_log2, -mm.w)) * zz.w;
-              if (!masked) {
-                blk += (e0 + e1) + (e2 + e3);
-              } else {
-                const int4 pp = p4[q];
-                blk += ((j <= pp.x ? e0 : 0.f) + (j <= pp.y ? e1 : 0.f)) +
-                       ((j <= pp.z ? e2 : 0.f) + (j <= pp.w ? e3 : 0.f));
+              if (q >= nq) break;
+              const int ch = ch0 + 2 * q;
+              const float4 *m4 = reinterpret_cast<const float4 *>(sM + ch * 16);
+              const float4 *z4 = reinterpret_cast<const float4 *>(sZ + ch * 16);
+              const int4 *p4 = reinterpret_cast<const int4 *>(sPos + ch * 16);
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const float4 mm = m4[u], zz = z4[u];
+                const float2 xa = __ffma2_rn(make_float2(__uint_as_float(r[q][4 * u]), __uint_as_float(r[q][4 * u + 1])),
+                                             c2, make_float2(mm.x, mm.y));
+                const float2 xb = __ffma2_rn(make_float2(__uint_as_float(r[q][4 * u + 2]), __uint_as_float(r[q][4 * u + 3])),
+                                             c2, make_float2(mm.z, mm.w));
+                float2 ea = make_float2(tc::ex2(xa.x), tc::ex2(xa.y));
+                float2 eb = make_float2(tc::ex2(xb.x), tc::ex2(xb.y));
+                if (masked) {
+                  const int4 pp = p4[u];
+                  ea = make_float2(j <= pp.x ? ea.x : 0.f, j <= pp.y ? ea.y : 0.f);
+                  eb = make_float2(j <= pp.z ? eb.x : 0.f, j <= pp.w ? eb.y : 0.f);
+                }
+                acc2 = __ffma2_rn(ea, make_float2(zz.x, zz.y), acc2);
+                acc2 = __ffma2_rn(eb, make_float2(zz.z, zz.w), acc2);
               }
             }
-            acc += blk;
           }
+          acc = acc2.x + acc2.y;
           tc::fence_before_sync();
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(B.tempty + slot);
         }
-        // add the two warpgroups' halves and store the key's mass
-        if (wg == 1) sRed[key_in_tile] = acc;
+        // add the two warpgroups' halves and store the key's mass; the exchange
+        // buffer alternates between tiles, so one barrier per tile suffices
+        float *red = sRed + (g & 1) * KT;
+        if (wg == 1) red[key_in_tile] = acc;
         tc::named_bar_sync(1, 256);
-        if (ok && wg == 0 && j < w.j_end) s_out[w.unit * (long)T + j] = acc + sRed[key_in_tile];
-        tc::named_bar_sync(1, 256);
+        if (ok && wg == 0 && j < w.j_end) s_out[w.unit * (long)T + j] = acc + red[key_in_tile];
       }
     }
   }
