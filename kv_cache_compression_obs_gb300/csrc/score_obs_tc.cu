@@ -17,7 +17,8 @@
 // Both kernels are persistent (one CTA per SM, items assigned round-robin) and
 // warp-specialised: warp 0 issues TMA loads into a 4-stage K ring (the unit's Q
 // block stays resident per item), warp 1 issues the MMAs into two TMEM slots,
-// warps 2..9 (two warpgroups) drain TMEM.  Every mbarrier wait is bounded; a
+// warps 2..17 (four warpgroups, each taking a quarter of a tile's TMEM columns)
+// drain TMEM.  Every mbarrier wait is bounded; a
 // wait that gives up sets a CTA-wide abort flag and the device status
 // KV_ERR_TIMEOUT, the roles leave their loops, outstanding copies and MMAs are
 // waited for (again bounded) and the TMEM is freed before the CTA exits.
@@ -29,7 +30,9 @@
 namespace kvc {
 namespace {
 
-constexpr int NT = 320;        // 10 warps
+constexpr int EPI_WARPS = 16;  // TMEM-draining warps (four warpgroups)
+constexpr int EPI_THREADS = EPI_WARPS * 32;
+constexpr int NT = 64 + EPI_THREADS;  // + producer warp + MMA warp
 constexpr int KT = 128;        // keys per tile (the UMMA M of pass 2, N of pass 1)
 constexpr int QROWS = 256;     // resident query rows per unit
 constexpr int STAGES = 4;      // K ring depth
@@ -49,9 +52,9 @@ struct Geo {
   static constexpr int NBARS = 2 * STAGES + 7;
   static constexpr int MISC_OFF = BAR_OFF + 256;              // TMEM base, abort flag
   static constexpr int STAT_OFF = BAR_OFF + 512;              // row M, 1/Z, position (16-aligned)
-  static constexpr int RED_OFF = STAT_OFF + QROWS * 12;       // warpgroup exchange
+  static constexpr int RED_OFF = STAT_OFF + QROWS * 12;       // warpgroup exchange (4 KB)
   // at least 116 KB so that a single CTA fits per SM: each CTA takes all 512 TMEM columns
-  static constexpr int SMEM_NEED = 1024 /*alignment slack*/ + RED_OFF + 2 * KT * 4;
+  static constexpr int SMEM_NEED = 1024 /*alignment slack*/ + RED_OFF + 4096;
   static constexpr int SMEM = SMEM_NEED > 116 * 1024 ? SMEM_NEED : 116 * 1024;
   static_assert(NBARS * 8 <= 256, "barrier area");
 };
@@ -79,7 +82,7 @@ __device__ __forceinline__ void init_bars(const Bars &B) {
   tc::mbar_init(B.qempty, 1);
   for (int i = 0; i < 2; ++i) {
     tc::mbar_init(B.tfull + i, 1);
-    tc::mbar_init(B.tempty + i, 8);  // one arrival per epilogue warp
+    tc::mbar_init(B.tempty + i, EPI_WARPS);  // one arrival per epilogue warp
   }
   tc::mbar_init(B.drain, 1);
   tc::mbar_fence_init();
@@ -268,14 +271,21 @@ __global__ void __launch_bounds__(NT, 1)
     if (lane == 0)
       issue<D, 1>(tmem, sQ, sK, B, n_items, per_unit, span, T, n_mt, 0, abort_flag, status);
   } else {
-    const int ew = warp - 2;
-    const int mt = ew >> 2;                 // M-tile (rows 0..127 or 128..255)
+    const int ew = warp - 2;                // 0 .. EPI_WARPS-1
+    const int wg = ew >> 2;                 // warpgroup 0..3
+    const int mt = wg >> 1;                 // M-tile (rows 0..127 or 128..255)
+    const int chalf = wg & 1;               // which 64 keys of each 128-key tile
     const int quarter = warp & 3;           // TMEM lane quarter this warp may access
-    const int row = mt * 128 + quarter * 32 + lane;
+    const int rit = quarter * 32 + lane;    // row within the M-tile
+    const int row = mt * 128 + rit;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
+    float2 *xch = reinterpret_cast<float2 *>(sm + G::RED_OFF);  // [2 items][2 M-tiles][128]
     uint32_t g = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+    int it = 0;
+    // A warp that gives up keeps walking the same items and tiles (without
+    // touching TMEM) so that every named barrier is reached by all epilogue threads.
+    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++it) {
       const Item w = item_of(item, per_unit, span, T);
       const int p_row = T - W + (row % W);
       const int jlim = min(w.j_end, p_row + 1);  // keys this row may see in the split
@@ -283,61 +293,67 @@ __global__ void __launch_bounds__(NT, 1)
       for (int j0 = w.j_begin; j0 < w.j_end; j0 += KT, ++g) {
         const int slot = g & 1;
         const uint32_t tuse = g >> 1;
-        if (!tc::mbar_wait(B.tfull + slot, tuse & 1, kWaitBudget, abort_flag)) {
+        if (ok && !tc::mbar_wait(B.tfull + slot, tuse & 1, kWaitBudget, abort_flag)) {
           set_abort(abort_flag, status);
           ok = false;
-          break;
         }
+        if (!ok) continue;
         tc::fence_after_sync();
         if (mt < n_mt) {
-#pragma unroll 1
-          for (int half = 0; half < 2; ++half) {
-            uint32_t r[64];
-            const uint32_t col = tmem + lane_addr + slot * 256 + mt * 128 + half * 64;
+          uint32_t r[64];
+          const uint32_t col = tmem + lane_addr + slot * 256 + mt * 128 + chalf * 64;
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              tc::tmem_ld16(col + q * 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16 * q]));
-            tc::tmem_ld_wait();
-            const int jb = j0 + half * 64;
-            if (jb + 64 <= jlim) {
-              // every key visible: sum against the running reference m; only a
-              // sum large enough to risk overflow (or the first chunk, m = -inf)
-              // takes the exact-max path
-              float sum = chunk_sum(r, c_log2, m);
-              if (!(sum <= kLazyLimit)) {
-                float cm = -INFINITY;
-#pragma unroll
-                for (int c = 0; c < 64; ++c) cm = fmaxf(cm, __uint_as_float(r[c]));
-                const float mnew = fmaxf(m, cm * c_log2);
-                sum = chunk_sum(r, c_log2, mnew);
-                z = z * tc::ex2(m - mnew);
-                m = mnew;
-              }
-              z += sum;
-            } else if (jb < jlim) {
+          for (int q = 0; q < 4; ++q)
+            tc::tmem_ld16(col + q * 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16 * q]));
+          tc::tmem_ld_wait();
+          const int jb = j0 + chalf * 64;
+          if (jb + 64 <= jlim) {
+            // every key visible: sum against the running reference m; only a sum
+            // large enough to risk overflow (or the first chunk, m = -inf) takes
+            // the exact-max path
+            float sum = chunk_sum(r, c_log2, m);
+            if (!(sum <= kLazyLimit)) {
               float cm = -INFINITY;
 #pragma unroll
-              for (int c = 0; c < 64; ++c)
-                if (jb + c < jlim) cm = fmaxf(cm, __uint_as_float(r[c]));
+              for (int c = 0; c < 64; ++c) cm = fmaxf(cm, __uint_as_float(r[c]));
               const float mnew = fmaxf(m, cm * c_log2);
-              float acc = 0.f;
-#pragma unroll
-              for (int c = 0; c < 64; ++c) {
-                const float e = tc::ex2(fmaf(__uint_as_float(r[c]), c_log2, -mnew));
-                acc += (jb + c < jlim) ? e : 0.f;
-              }
-              z = z * tc::ex2(m - mnew) + acc;
+              sum = chunk_sum(r, c_log2, mnew);
+              z = z * tc::ex2(m - mnew);
               m = mnew;
             }
+            z += sum;
+          } else if (jb < jlim) {
+            float cm = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (jb + c < jlim) cm = fmaxf(cm, __uint_as_float(r[c]));
+            const float mnew = fmaxf(m, cm * c_log2);
+            float acc = 0.f;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+              const float e = tc::ex2(fmaf(__uint_as_float(r[c]), c_log2, -mnew));
+              acc += (jb + c < jlim) ? e : 0.f;
+            }
+            z = z * tc::ex2(m - mnew) + acc;
+            m = mnew;
           }
         }
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(B.tempty + slot);
       }
-      if (ok && mt < n_mt && row < gw) {
+      // the two 64-key halves of each row meet here (buffer alternates per item)
+      float2 *xb = xch + (it & 1) * 256;
+      if (chalf == 1) xb[mt * 128 + rit] = make_float2(m, z);
+      tc::named_bar_sync(1, EPI_THREADS);
+      if (ok && chalf == 0 && mt < n_mt && row < gw) {
+        const float2 o = xb[mt * 128 + rit];
+        const float M = fmaxf(m, o.x);
+        float Z = 0.f;
+        if (m != -INFINITY) Z += z * tc::ex2(m - M);
+        if (o.x != -INFINITY) Z += o.y * tc::ex2(o.x - M);
         const int split = item % per_unit;
-        part[(w.unit * per_unit + split) * gw + row] = make_float2(m, z);
+        part[(w.unit * per_unit + split) * gw + row] = make_float2(M, Z);
       }
     }
   }
@@ -390,9 +406,9 @@ __global__ void __launch_bounds__(NT, 1)
     if (lane == 0)
       issue<D, 2>(tmem, sQ, sK, B, n_items, per_unit, span, T, 0, n_cols, abort_flag, status);
   } else {
-    const int et = threadIdx.x - 64;        // 0..255
+    const int et = threadIdx.x - 64;        // 0 .. EPI_THREADS-1
     const int ew = warp - 2;
-    const int wg = ew >> 2;                 // column half handled by this warpgroup
+    const int wg = ew >> 2;                 // this warpgroup takes column chunks wg, wg+4, ...
     const int quarter = warp & 3;
     const int key_in_tile = quarter * 32 + lane;
     const uint32_t lane_addr = static_cast<uint32_t>(quarter * 32) << 16;
@@ -405,8 +421,8 @@ __global__ void __launch_bounds__(NT, 1)
     // epilogue threads.
     for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
       const Item w = item_of(item, per_unit, span, T);
-      tc::named_bar_sync(1, 256);           // the previous item's readers are done
-      for (int r = et; r < QROWS; r += 256) {
+      tc::named_bar_sync(1, EPI_THREADS);   // the previous item's readers are done
+      for (int r = et; r < QROWS; r += EPI_THREADS) {
         if (r < gw) {
           const float2 f = fin[w.unit * gw + r];
           sM[r] = -f.x;  // stored negated: the exponent is one fma, x * c_log2 + (-M)
@@ -418,7 +434,7 @@ __global__ void __launch_bounds__(NT, 1)
           sPos[r] = -1;
         }
       }
-      tc::named_bar_sync(1, 256);
+      tc::named_bar_sync(1, EPI_THREADS);
       for (int j0 = w.j_begin; j0 < w.j_end; j0 += KT, ++g) {
         const int slot = g & 1;
         const uint32_t tuse = g >> 1;
@@ -433,19 +449,18 @@ __global__ void __launch_bounds__(NT, 1)
           const bool masked = j0 + KT > first_masked;
           float2 acc2 = make_float2(0.f, 0.f);
           const float2 c2 = make_float2(c_log2, c_log2);
-#pragma unroll 1
-          for (int ch0 = wg; ch0 < n_chunks; ch0 += 8) {
-            // up to four 16-column loads in flight before one wait
+          {
+            // this warpgroup's (at most four) 16-column chunks in flight before one wait
             uint32_t r[4][16];
-            const int nq = min(4, (n_chunks - ch0 + 1) / 2);
+            const int nq = max(0, min(4, (n_chunks - wg + 3) / 4));
 #pragma unroll
             for (int q = 0; q < 4; ++q)
-              if (q < nq) tc::tmem_ld16(tmem + lane_addr + slot * 256 + (ch0 + 2 * q) * 16, r[q]);
-            tc::tmem_ld_wait();
+              if (q < nq) tc::tmem_ld16(tmem + lane_addr + slot * 256 + (wg + 4 * q) * 16, r[q]);
+            if (nq > 0) tc::tmem_ld_wait();
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               if (q >= nq) break;
-              const int ch = ch0 + 2 * q;
+              const int ch = wg + 4 * q;
               const float4 *m4 = reinterpret_cast<const float4 *>(sM + ch * 16);
               const float4 *z4 = reinterpret_cast<const float4 *>(sZ + ch * 16);
               const int4 *p4 = reinterpret_cast<const int4 *>(sPos + ch * 16);
@@ -473,12 +488,14 @@ __global__ void __launch_bounds__(NT, 1)
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(B.tempty + slot);
         }
-        // add the two warpgroups' halves and store the key's mass; the exchange
-        // buffer alternates between tiles, so one barrier per tile suffices
-        float *red = sRed + (g & 1) * KT;
-        if (wg == 1) red[key_in_tile] = acc;
-        tc::named_bar_sync(1, 256);
-        if (ok && wg == 0 && j < w.j_end) s_out[w.unit * (long)T + j] = acc + red[key_in_tile];
+        // add the four warpgroups' shares (fixed order) and store the key's mass;
+        // the exchange buffer alternates between tiles, so one barrier per tile suffices
+        float *red = sRed + (g & 1) * 4 * KT;
+        if (wg > 0) red[wg * KT + key_in_tile] = acc;
+        tc::named_bar_sync(1, EPI_THREADS);
+        if (ok && wg == 0 && j < w.j_end)
+          s_out[w.unit * (long)T + j] =
+              acc + (red[KT + key_in_tile] + red[2 * KT + key_in_tile] + red[3 * KT + key_in_tile]);
       }
     }
   }
