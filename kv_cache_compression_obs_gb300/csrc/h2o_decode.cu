@@ -9,20 +9,17 @@
 // One thread-block cluster of C CTAs per unit (b, KV head); CTA r owns slot
 // range r of the unit (CTA 0 also owns the new token) and serves the G query
 // heads of the group:
-//   1. each warp streams its own 32-row chunks: one row per lane for the logits
-//      l_gj = scale <q_g, k_j> (the row's 16-byte loads all in flight, q read
-//      from shared memory), then the lanes across d for the values, with an
-//      online softmax (running max, rescaled partial normaliser and output), so
-//      the K and V streams run without CTA-wide synchronisation; the logits are
-//      kept in shared memory;
-//   2. the warps' partials combine into the CTA's (m_c, Z_c) and output share;
-//      cluster barrier; every CTA combines the C pairs, read through distributed
-//      shared memory in rank order, into the same (m_g, Z_g) and rescales its share;
-//   3. p_gj = exp(l_gj - m_g) / Z_g from the kept logits; acc_j += sum_g p_gj; the
-//      CTA's (acc, pos)-smallest eviction candidate;
+//   1. logits l_gj = scale <q_g, k_j> over its rows, one thread per K row with the
+//      whole row's 16-byte loads in flight, kept in shared memory;
+//   2. its local max and normaliser per g; cluster barrier; every CTA combines
+//      the C local pairs, read through distributed shared memory in rank order,
+//      into the same global (m_g, Z_g);
+//   3. p_gj = exp(l_gj - m_g) / Z_g; acc_j += sum_g p_gj; its (acc, pos)-smallest
+//      eviction candidate; its share of o_g = sum_j p_gj v_j (V read once, one
+//      row per warp with the lanes across d, sixteen rows per warp in flight);
 //   4. cluster barrier; CTA 0 takes the smallest candidate over the cluster (and
-//      the new token itself when recent == 0), sums the output shares in rank
-//      order, and appends the new token or writes it over the victim's slot;
+//      the new token itself when recent == 0), sums the o shares in rank order,
+//      and appends the new token or writes it over the victim's slot;
 //   5. a last cluster barrier keeps every CTA's shared memory alive until CTA 0
 //      has read it.
 // The cluster barriers are hardware barriers that every CTA reaches
@@ -30,6 +27,7 @@
 #include <cooperative_groups.h>
 
 #include <cmath>
+#include <type_traits>
 
 #include "kvc_internal.cuh"
 
@@ -40,7 +38,7 @@ namespace {
 
 constexpr int NT = 256;
 constexpr int NWARP = NT / 32;
-constexpr int kMaxCluster = 8;
+constexpr int kMaxCluster = 4;
 constexpr int kSlotsPerCta = 512;  // target rows per CTA when choosing the cluster size
 
 __device__ __forceinline__ bool better(float a, int p, float ba, int bp) {
@@ -56,64 +54,63 @@ struct Cand {
 
 template <int G, int D>
 struct Layout {
-  // floats, in order: qs[G*D], opart[G*D], wo[NWARP*G*D], stat[2G], wst[NWARP*2G],
-  // pbuf[NWARP*32*G], cand, wcand[NWARP], misc[8], lg[G*ldl]
+  // floats, in order: qs[G*D], opart[G*D], wred[NWARP*G*D], stat[2G], wstat[NWARP*G], lg[G*ldl]
   static constexpr int QS = 0;
   static constexpr int OPART = QS + G * D;
-  static constexpr int WO = OPART + G * D;
-  static constexpr int STAT = WO + NWARP * G * D;
-  static constexpr int WST = STAT + 2 * G;
-  static constexpr int PBUF = ((WST + NWARP * 2 * G) + 3) / 4 * 4;  // 16-byte aligned
-  static constexpr int CAND = PBUF + NWARP * 32 * G;
-  static constexpr int WCAND = CAND + 4;
-  static constexpr int MISC = WCAND + 4 * NWARP;
+  static constexpr int WRED = OPART + G * D;
+  static constexpr int STAT = WRED + NWARP * G * D;
+  static constexpr int WSTAT = STAT + 2 * G;
+  static constexpr int CAND = WSTAT + NWARP * G;           // Cand (4 words)
+  static constexpr int WCAND = CAND + 4;                   // NWARP x Cand
+  static constexpr int MISC = WCAND + 4 * NWARP;           // acc_new, slot, evicted, ...
   static constexpr int LG = MISC + 8;
   static size_t bytes(int ldl) { return (size_t)(LG + G * ldl) * sizeof(float); }
 };
 
-// EV consecutive elements of a row, as floats (EV * sizeof(T) = 4, 8 or 16 bytes).
+// EV consecutive elements of a row held packed (EV * sizeof(T) = 4, 8 or 16 bytes)
+// until they are used, so that many rows can be in flight per thread.
 template <typename T, int EV>
-__device__ __forceinline__ void load_ev(const T *p, float (&f)[EV]) {
-  if constexpr (sizeof(T) * EV == 16) {
-    Vec16<T>::unpack(__ldg(reinterpret_cast<const uint4 *>(p)), f);
-  } else if constexpr (sizeof(T) * EV == 8) {
-    const uint2 v = __ldg(reinterpret_cast<const uint2 *>(p));
-    if constexpr (sizeof(T) == 2) {
-      f[0] = __uint_as_float(v.x << 16);
-      f[1] = __uint_as_float(v.x & 0xFFFF0000u);
-      f[2] = __uint_as_float(v.y << 16);
-      f[3] = __uint_as_float(v.y & 0xFFFF0000u);
+struct RawV {
+  static constexpr int BYTES = EV * (int)sizeof(T);
+  using Word = typename std::conditional<BYTES == 16, uint4,
+               typename std::conditional<BYTES == 8, uint2, uint32_t>::type>::type;
+  __device__ __forceinline__ static Word load(const T *p) { return __ldg(reinterpret_cast<const Word *>(p)); }
+  __device__ __forceinline__ static void unpack(const Word &w, float (&f)[EV]) {
+    if constexpr (BYTES == 16) {
+      Vec16<T>::unpack(w, f);
+    } else if constexpr (BYTES == 8 && sizeof(T) == 2) {
+      f[0] = __uint_as_float(w.x << 16);
+      f[1] = __uint_as_float(w.x & 0xFFFF0000u);
+      f[2] = __uint_as_float(w.y << 16);
+      f[3] = __uint_as_float(w.y & 0xFFFF0000u);
+    } else if constexpr (BYTES == 8) {
+      f[0] = __uint_as_float(w.x);
+      f[1] = __uint_as_float(w.y);
     } else {
-      f[0] = __uint_as_float(v.x);
-      f[1] = __uint_as_float(v.y);
+      f[0] = __uint_as_float(w << 16);
+      f[1] = __uint_as_float(w & 0xFFFF0000u);
     }
-  } else {
-    const uint32_t v = __ldg(reinterpret_cast<const uint32_t *>(p));
-    f[0] = __uint_as_float(v << 16);
-    f[1] = __uint_as_float(v & 0xFFFF0000u);
   }
-}
+};
 
 template <typename T, int D, int G>
-__global__ __launch_bounds__(NT, 1) void decode_kernel(
+__global__ __launch_bounds__(NT) void decode_kernel(
     const T *__restrict__ q, const T *__restrict__ k_new, const T *__restrict__ v_new,
     T *__restrict__ Kc, T *__restrict__ Vc, int32_t *__restrict__ pos, float *__restrict__ acc,
     int32_t *__restrict__ len, int Hq, int Hkv, int cap, int recent, int new_pos, float scale,
     int alg1, int C, int ldl, float *__restrict__ o_out, int32_t *__restrict__ evicted,
     int *__restrict__ dev_status) {
   using L = Layout<G, D>;
-  constexpr int EPL = Vec16<T>::N;              // elements per 16-byte vector
-  constexpr int VPR = D * (int)sizeof(T) / 16;  // 16-byte vectors per K row
-  constexpr int VB = VPR < 8 ? VPR : 8;         // K vectors per load batch
-  constexpr int EV = D / 32;                    // V elements per lane
-  constexpr int VR = 16;                        // V rows per load batch
+  constexpr int EPL = Vec16<T>::N;  // elements per 16-byte vector
+  constexpr int LPR = D / EPL;      // lanes per row
+  constexpr int RPW = 32 / LPR;     // rows per warp per iteration
+  constexpr int NG = NWARP * RPW;   // row groups per block
   extern __shared__ float sm[];
   float *qs = sm + L::QS;
   float *opart = sm + L::OPART;
-  float *wo = sm + L::WO;
+  float *wred = sm + L::WRED;
   float *stat = sm + L::STAT;
-  float *wst = sm + L::WST;
-  float *pbuf = sm + L::PBUF;
+  float *wstat = sm + L::WSTAT;
   Cand *cand = reinterpret_cast<Cand *>(sm + L::CAND);
   Cand *wcand = reinterpret_cast<Cand *>(sm + L::WCAND);
   float *misc = sm + L::MISC;
@@ -145,129 +142,86 @@ __global__ __launch_bounds__(NT, 1) void decode_kernel(
   const T *Vu = Vc + unit * (long)cap * D;
   const T *kn = k_new + unit * (long)D;
   const T *vn = v_new + unit * (long)D;
+  const int sl = lane % LPR;  // lane within the row group
+  const int rg = lane / LPR;  // row group within the warp
   auto row_ptr = [&](const T *base, const T *fresh, int r) -> const T * {
     return (r < j1 - j0) ? base + (long)(j0 + r) * D : fresh;
   };
 
-  // 1. streaming: each warp on its own takes 32-row chunks (one row per lane for
-  //    the logits, the lanes across d for the values) with an online softmax, so
-  //    no CTA-wide synchronisation interrupts the K and V streams
-  float m_w[G], zl[G], o[G][EV];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    m_w[g] = -INFINITY;
-    zl[g] = 0.f;
-#pragma unroll
-    for (int e = 0; e < EV; ++e) o[g][e] = 0.f;
-  }
-  float *pw = pbuf + warp * 32 * G;
-  for (int c0 = warp * 32; c0 < nl; c0 += NWARP * 32) {
-    const int r = c0 + lane;
-    const bool valid = r < nl;
+  // 1. logits: one thread per row, the whole row requested before use (VPR
+  //    16-byte loads in flight per thread), q read from shared memory (broadcast)
+  constexpr int VPR = D * (int)sizeof(T) / 16;   // 16-byte vectors per row
+  constexpr int VB = VPR < 8 ? VPR : 8;          // vectors per batch
+  for (int r = threadIdx.x; r < nl; r += NT) {
+    const uint4 *row = reinterpret_cast<const uint4 *>(row_ptr(Ku, kn, r));
     float part[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) part[g] = 0.f;
-    if (valid) {
-      const uint4 *row = reinterpret_cast<const uint4 *>(row_ptr(Ku, kn, r));
 #pragma unroll
-      for (int v0 = 0; v0 < VPR; v0 += VB) {
-        uint4 raw[VB];
+    for (int v0 = 0; v0 < VPR; v0 += VB) {
+      uint4 raw[VB];
 #pragma unroll
-        for (int v = 0; v < VB; ++v) raw[v] = __ldg(row + v0 + v);
+      for (int v = 0; v < VB; ++v) raw[v] = __ldg(row + v0 + v);
 #pragma unroll
-        for (int v = 0; v < VB; ++v) {
-          float f[EPL];
-          Vec16<T>::unpack(raw[v], f);
+      for (int v = 0; v < VB; ++v) {
+        float f[EPL];
+        Vec16<T>::unpack(raw[v], f);
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float4 *q4 = reinterpret_cast<const float4 *>(qs + g * D + (v0 + v) * EPL);
+        for (int g = 0; g < G; ++g) {
+          const float4 *q4 = reinterpret_cast<const float4 *>(qs + g * D + (v0 + v) * EPL);
 #pragma unroll
-            for (int e4 = 0; e4 < EPL / 4; ++e4) {
-              const float4 qq = q4[e4];
-              part[g] = fmaf(f[4 * e4 + 0], qq.x, part[g]);
-              part[g] = fmaf(f[4 * e4 + 1], qq.y, part[g]);
-              part[g] = fmaf(f[4 * e4 + 2], qq.z, part[g]);
-              part[g] = fmaf(f[4 * e4 + 3], qq.w, part[g]);
-            }
+          for (int e4 = 0; e4 < EPL / 4; ++e4) {
+            const float4 qq = q4[e4];
+            part[g] = fmaf(f[4 * e4 + 0], qq.x, part[g]);
+            part[g] = fmaf(f[4 * e4 + 1], qq.y, part[g]);
+            part[g] = fmaf(f[4 * e4 + 2], qq.z, part[g]);
+            part[g] = fmaf(f[4 * e4 + 3], qq.w, part[g]);
           }
         }
       }
     }
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float l = valid ? scale * part[g] : -INFINITY;
-      if (valid) lg[g * ldl + r] = l;
-      float cm = l;
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xFFFFFFFFu, cm, off));
-      const float mnew = fmaxf(m_w[g], cm);  // finite: lane 0 of a chunk is always valid
-      const float sc = (m_w[g] == -INFINITY) ? 0.f : expf(m_w[g] - mnew);
-      zl[g] *= sc;
-#pragma unroll
-      for (int e = 0; e < EV; ++e) o[g][e] *= sc;
-      m_w[g] = mnew;
-      const float pt = valid ? expf(l - mnew) : 0.f;
-      zl[g] += pt;
-      pw[lane * G + g] = pt;
-    }
-    __syncwarp();
-    const int nrow = min(32, nl - c0);
-    for (int rr0 = 0; rr0 < nrow; rr0 += VR) {
-      float vv[VR][EV];
-#pragma unroll
-      for (int u = 0; u < VR; ++u)
-        if (rr0 + u < nrow) load_ev<T, EV>(row_ptr(Vu, vn, c0 + rr0 + u) + lane * EV, vv[u]);
-#pragma unroll
-      for (int u = 0; u < VR; ++u) {
-        if (rr0 + u < nrow) {
-#pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float p = pw[(rr0 + u) * G + g];
-#pragma unroll
-            for (int e = 0; e < EV; ++e) o[g][e] = fmaf(p, vv[u][e], o[g][e]);
-          }
-        }
-      }
-    }
-    __syncwarp();
-  }
-  // the warp's totals
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    float z = zl[g];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, off);
-    if (lane == 0) {
-      wst[warp * 2 * G + g] = m_w[g];
-      wst[warp * 2 * G + G + g] = z;
-    }
-#pragma unroll
-    for (int e = 0; e < EV; ++e) wo[(warp * G + g) * D + lane * EV + e] = o[g][e];
+    for (int g = 0; g < G; ++g) lg[g * ldl + r] = scale * part[g];
   }
   __syncthreads();
 
-  // 2. this CTA's pair (m_c, Z_c) and o share (relative to m_c), then the cluster-wide pair
-  if (threadIdx.x < G) {
-    const int g = threadIdx.x;
-    float m = -INFINITY;
-    for (int w = 0; w < NWARP; ++w) m = fmaxf(m, wst[w * 2 * G + g]);
-    float z = 0.f;
-    for (int w = 0; w < NWARP; ++w) {
-      const float mw = wst[w * 2 * G + g];
-      if (mw != -INFINITY) z += wst[w * 2 * G + G + g] * expf(mw - m);
-    }
-    stat[g] = m;
-    stat[G + g] = z;
+  // 2. local max and normaliser per query head, then the cluster-wide pair
+  float mx[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) mx[g] = -INFINITY;
+  for (int r = threadIdx.x; r < nl; r += NT)
+#pragma unroll
+    for (int g = 0; g < G; ++g) mx[g] = fmaxf(mx[g], lg[g * ldl + r]);
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx[g] = fmaxf(mx[g], __shfl_xor_sync(0xFFFFFFFFu, mx[g], off));
+    if (lane == 0) wstat[warp * G + g] = mx[g];
   }
   __syncthreads();
-  for (int t = threadIdx.x; t < G * D; t += NT) {
-    const int g = t / D;
-    float s = 0.f;
-    for (int w = 0; w < NWARP; ++w) {
-      const float mw = wst[w * 2 * G + g];
-      if (mw != -INFINITY) s += wo[w * G * D + t] * expf(mw - stat[g]);
-    }
-    opart[t] = s;
+  if (threadIdx.x < G) {
+    float m = -INFINITY;
+    for (int w = 0; w < NWARP; ++w) m = fmaxf(m, wstat[w * G + threadIdx.x]);
+    stat[threadIdx.x] = m;
+  }
+  __syncthreads();
+  float zs[G];
+#pragma unroll
+  for (int g = 0; g < G; ++g) zs[g] = 0.f;
+  for (int r = threadIdx.x; r < nl; r += NT)
+#pragma unroll
+    for (int g = 0; g < G; ++g) zs[g] += expf(lg[g * ldl + r] - stat[g]);
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) zs[g] += __shfl_xor_sync(0xFFFFFFFFu, zs[g], off);
+    if (lane == 0) wstat[warp * G + g] = zs[g];
+  }
+  __syncthreads();
+  if (threadIdx.x < G) {
+    float z = 0.f;
+    for (int w = 0; w < NWARP; ++w) z += wstat[w * G + threadIdx.x];
+    stat[G + threadIdx.x] = z;  // stat = [m_0..m_G-1, Z_0..Z_G-1] of this CTA
   }
   cluster.sync();  // #1: every CTA's local pair is visible
   __shared__ float gm[8], gz[8];
@@ -284,11 +238,6 @@ __global__ __launch_bounds__(NT, 1) void decode_kernel(
     gz[g] = z;
   }
   __syncthreads();
-  // this CTA's o share, now normalised with the cluster-wide pair
-  for (int t = threadIdx.x; t < G * D; t += NT) {
-    const int g = t / D;
-    opart[t] = (stat[g] == -INFINITY) ? 0.f : opart[t] * (expf(stat[g] - gm[g]) / gz[g]);
-  }
 
   // 3. probabilities, accumulators, this CTA's eviction candidate
   const long lim = (long)new_pos - recent;
@@ -300,7 +249,11 @@ __global__ __launch_bounds__(NT, 1) void decode_kernel(
   for (int r = threadIdx.x; r < nl; r += NT) {
     float P = 0.f;
 #pragma unroll
-    for (int g = 0; g < G; ++g) P += expf(lg[g * ldl + r] - gm[g]) / gz[g];
+    for (int g = 0; g < G; ++g) {
+      const float p = expf(lg[g * ldl + r] - gm[g]) / gz[g];
+      lg[g * ldl + r] = p;
+      P += p;
+    }
     if (r < j1 - j0) {
       const int j = j0 + r;
       const float a = au[j] + P;
@@ -330,16 +283,56 @@ __global__ __launch_bounds__(NT, 1) void decode_kernel(
   }
   if (lane == 0) {
     wcand[warp] = Cand{best_a, best_p, best_j, 0};
-    wst[warp * 2 * G] = acc_self;  // (reuse) per-warp share of the new token's score
+    wstat[warp * G] = acc_self;  // (reuse) per-warp share of the new token's score
   }
   __syncthreads();
+
+  // o share: sum over this CTA's rows of p_gj v_j.  One row per warp at a time,
+  // the lanes across d (EV elements each), 16 rows per warp in flight.
+  constexpr int EV = D / 32;
+  using RV = RawV<T, EV>;
+  constexpr int U = 128 / RV::BYTES;  // 128 bytes of V in flight per lane
+  float op_[G][EV];
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int e = 0; e < EV; ++e) op_[g][e] = 0.f;
+  for (int r0 = warp * U; r0 < nl; r0 += NWARP * U) {
+    typename RV::Word raw[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+      if (r0 + u < nl) raw[u] = RV::load(row_ptr(Vu, vn, r0 + u) + lane * EV);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      if (r0 + u < nl) {
+        float vv[EV];
+        RV::unpack(raw[u], vv);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float p = lg[g * ldl + r0 + u];
+#pragma unroll
+          for (int e = 0; e < EV; ++e) op_[g][e] = fmaf(p, vv[e], op_[g][e]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int e = 0; e < EV; ++e) wred[(warp * G + g) * D + lane * EV + e] = op_[g][e];
+  __syncthreads();
+  for (int t = threadIdx.x; t < G * D; t += NT) {
+    float s = 0.f;
+    for (int w = 0; w < NWARP; ++w) s += wred[w * G * D + t];
+    opart[t] = s;
+  }
   if (threadIdx.x == 0) {
     Cand best{INFINITY, 0x7FFFFFFF, -2, 0};
     float accnew = 0.f;
     for (int w = 0; w < NWARP; ++w) {
       const Cand c = wcand[w];
       if (c.slot != -2 && (best.slot == -2 || better(c.acc, c.pos, best.acc, best.pos))) best = c;
-      accnew += wst[w * 2 * G];
+      accnew += wstat[w * G];
     }
     *cand = best;
     misc[0] = accnew;
@@ -390,7 +383,7 @@ __global__ __launch_bounds__(NT, 1) void decode_kernel(
     if (slot >= 0) {
       uint4 *kd = reinterpret_cast<uint4 *>(Kc + (unit * (long)cap + slot) * D);
       uint4 *vd = reinterpret_cast<uint4 *>(Vc + (unit * (long)cap + slot) * D);
-      for (int t = threadIdx.x; t < VPR; t += NT) {
+      for (int t = threadIdx.x; t < LPR; t += NT) {
         kd[t] = __ldg(reinterpret_cast<const uint4 *>(kn) + t);
         vd[t] = __ldg(reinterpret_cast<const uint4 *>(vn) + t);
       }
@@ -464,8 +457,7 @@ int dispatch_g(int G, const void *q, const void *k_new, const void *v_new, void 
 size_t decode_smem_bytes(int G, int cap, int d) {
   const int C = cluster_size_for(cap);
   const int ldl = ldl_for(cap, C);
-  const size_t wst_end = (size_t)G * d * (2 + NWARP) + 2 * G + NWARP * 2 * G;
-  const size_t fixed = (wst_end + 3) / 4 * 4 + NWARP * 32 * G + 4 + 4 * NWARP + 8;
+  const size_t fixed = (size_t)G * d * (2 + NWARP) + 2 * G + NWARP * G + 4 + 4 * NWARP + 8;
   return (fixed + (size_t)G * ldl) * sizeof(float);
 }
 
