@@ -64,7 +64,8 @@ struct Layout {
   static constexpr int WCAND = CAND + 4;                   // NWARP x Cand
   static constexpr int MISC = WCAND + 4 * NWARP;           // acc_new, slot, evicted, ...
   static constexpr int LG = MISC + 8;
-  static size_t bytes(int ldl) { return (size_t)(LG + G * ldl) * sizeof(float); }
+  // after lg: the rows' accumulators and positions, staged at kernel start
+  static size_t bytes(int ldl) { return (size_t)(LG + G * ldl + 2 * ldl) * sizeof(float); }
 };
 
 // EV consecutive elements of a row held packed (EV * sizeof(T) = 4, 8 or 16 bytes)
@@ -133,6 +134,21 @@ __global__ __launch_bounds__(NT) void decode_kernel(
   const int j1 = min(n, j0 + chunk);
   const int self_here = (with_self && rank == 0) ? 1 : 0;
   const int nl = (j1 - j0) + self_here;  // local rows; row nl-1 is the new token when self_here
+  float *sacc = lg + G * ldl;                             // [ldl] accumulators of rows j0..j1-1
+  int *spos = reinterpret_cast<int *>(sacc + ldl);        // [ldl] their positions
+  float *au = acc + unit * (long)cap;
+  int32_t *pu = pos + unit * (long)cap;
+  // The accumulators and positions are needed only after the K pass: copy them
+  // to shared memory asynchronously now so that their latency hides behind it.
+  for (int r = threadIdx.x; r < j1 - j0; r += NT) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(sacc + r)),
+                 "l"(au + j0 + r)
+                 : "memory");
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(spos + r)),
+                 "l"(pu + j0 + r)
+                 : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
 
   const T *qg = q + (b * Hq + (long)h * G) * D;
   for (int t = threadIdx.x; t < G * D; t += NT) qs[t] = to_f32(qg[t]);
@@ -244,8 +260,8 @@ __global__ __launch_bounds__(NT) void decode_kernel(
   float best_a = INFINITY;
   int best_p = 0x7FFFFFFF, best_j = -2;
   float acc_self = 0.f;
-  float *au = acc + unit * (long)cap;
-  int32_t *pu = pos + unit * (long)cap;
+  asm volatile("cp.async.wait_all;" ::: "memory");
+  __syncthreads();
   for (int r = threadIdx.x; r < nl; r += NT) {
     float P = 0.f;
 #pragma unroll
@@ -256,9 +272,9 @@ __global__ __launch_bounds__(NT) void decode_kernel(
     }
     if (r < j1 - j0) {
       const int j = j0 + r;
-      const float a = au[j] + P;
+      const float a = sacc[r] + P;
       au[j] = a;
-      const int pj = pu[j];
+      const int pj = spos[r];
       if ((long)pj <= lim && better(a, pj, best_a, best_p)) {
         best_a = a;
         best_p = pj;
@@ -458,7 +474,7 @@ size_t decode_smem_bytes(int G, int cap, int d) {
   const int C = cluster_size_for(cap);
   const int ldl = ldl_for(cap, C);
   const size_t fixed = (size_t)G * d * (2 + NWARP) + 2 * G + NWARP * G + 4 + 4 * NWARP + 8;
-  return (fixed + (size_t)G * ldl) * sizeof(float);
+  return (fixed + (size_t)G * ldl + 2 * (size_t)ldl) * sizeof(float);
 }
 
 int launch_decode_step(const void *q, const void *k_new, const void *v_new, void *K_cache,
