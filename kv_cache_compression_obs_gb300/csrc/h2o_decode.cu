@@ -38,8 +38,8 @@ namespace {
 
 constexpr int NT = 256;
 constexpr int NWARP = NT / 32;
-constexpr int kMaxCluster = 4;
-constexpr int kSlotsPerCta = 512;  // target rows per CTA when choosing the cluster size
+constexpr int kMaxCluster = 5;
+constexpr int kSlotsPerCta = 1300;  // target rows per CTA when choosing the cluster size
 
 __device__ __forceinline__ bool better(float a, int p, float ba, int bp) {
   return a < ba || (a == ba && p < bp);
