@@ -169,6 +169,8 @@ class Pipeline:
         ws = max(api.kv_workspace_size(api.KV_OP_SCORE_OBS, wl.rows, wl.Hq, wl.Hkv, wl.T, wl.d, wl.W),
                  api.kv_workspace_size(api.KV_OP_HUBKV_REFINE, wl.rows, wl.Hkv, wl.Hkv, wl.T), 256)
         self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
+        dws = api.kv_workspace_size(api.KV_OP_DECODE, wl.rows, wl.Hq, wl.Hkv, wl.cap, wl.d)
+        self.dws = torch.empty(max(dws, 256), dtype=torch.uint8, device=device)
         steps = [gen.decode_inputs(wl, t, device=device) for t in range(wl.n_decode)]
         self.dq = [x[0] for x in steps]
         self.dk = [x[1] for x in steps]
@@ -188,7 +190,7 @@ class Pipeline:
         wl = self.wl
         self.api.h2o_decode_step(self.dq[t], self.dk[t], self.dv[t], self.Kc, self.Vc, self.pos,
                                  self.acc, self.len, wl.R, wl.T + t, wl.scale, o_out=self.o,
-                                 evicted_out=self.ev, stream=stream)
+                                 evicted_out=self.ev, workspace=self.dws, stream=stream)
 
     def step(self, stream=None):
         self.prefill(stream)

@@ -70,7 +70,7 @@ enum {
 };
 
 /* operation codes for kv_workspace_size */
-enum { KV_OP_SCORE_OBS = 1, KV_OP_HUBKV_REFINE = 2, KV_OP_SELECT_TOPK = 3 };
+enum { KV_OP_SCORE_OBS = 1, KV_OP_HUBKV_REFINE = 2, KV_OP_SELECT_TOPK = 3, KV_OP_DECODE = 4 };
 
 typedef void *kv_stream_t;
 
@@ -180,16 +180,18 @@ KVC_API int kv_compact(const void *K, const void *V, const float *s, const int32
  *   K_cache, V_cache [B][Hkv][cap][d]   updated in place
  *   pos [B][Hkv][cap] int32, acc [B][Hkv][cap] float32, len [B][Hkv] int32 (in place)
  *   o_out [B][Hq][d] float32;  evicted_pos [B][Hkv] int32
+ *   workspace  >= kv_workspace_size(KV_OP_DECODE, B, Hq, Hkv, cap, d, 0, 0) bytes
  *   dev_status  device int, may be NULL; set to a kv_status if a device-side
- *               error occurs, never cleared by the library
+ *               error occurs (e.g. a len outside [0, cap]: that unit is then left
+ *               untouched), never cleared by the library
  * Preconditions: 0 <= recent < cap, KV_H2O_ALG1 => recent == 0, new_pos larger
  * than every cached position, 0 <= len <= cap.
  */
 KVC_API int h2o_decode_step(const void *q, const void *k_new, const void *v_new, void *K_cache,
                     void *V_cache, int32_t *pos, float *acc, int32_t *len, int B, int Hq,
                     int Hkv, int cap, int d, int recent, int32_t new_pos, float scale,
-                    int flags, int dtype, float *o_out, int32_t *evicted_pos, int *dev_status,
-                    kv_stream_t stream);
+                    int flags, int dtype, float *o_out, int32_t *evicted_pos, void *workspace,
+                    size_t workspace_bytes, int *dev_status, kv_stream_t stream);
 
 /*
  * kv_score_obs_noalloc -- kv_score_obs without a caller-provided workspace.
@@ -220,7 +222,8 @@ KVC_API int kv_score_obs_noalloc(const void *Q_obs, const void *K, int B, int Hq
 
 /* Device workspace (bytes) that `op` needs for these sizes; 0 if none.
  * Arguments that an op does not use are ignored; for KV_OP_HUBKV_REFINE pass the
- * refine call's head count H as Hkv.  Returns 0 for invalid sizes. */
+ * refine call's head count H as Hkv; for KV_OP_DECODE pass the slot capacity as T.
+ * Returns 0 for invalid sizes. */
 KVC_API size_t kv_workspace_size(int op, int B, int Hq, int Hkv, int T, int d, int W, int k);
 
 /* Static description of a kv_status value. */

@@ -28,7 +28,7 @@ KV_OK, KV_ERR_INVALID_ARG, KV_ERR_UNSUPPORTED, KV_ERR_CUDA, KV_ERR_TIMEOUT, KV_E
     0, -1, -2, -3, -4, -5)
 KV_BF16, KV_F32 = 0, 1
 KV_H2O_ALG1 = 1
-KV_OP_SCORE_OBS, KV_OP_HUBKV_REFINE, KV_OP_SELECT_TOPK = 1, 2, 3
+KV_OP_SCORE_OBS, KV_OP_HUBKV_REFINE, KV_OP_SELECT_TOPK, KV_OP_DECODE = 1, 2, 3, 4
 
 _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _lib.kv_score_obs.restype = _I
@@ -41,7 +41,7 @@ _lib.kv_compact.restype = _I
 _lib.kv_compact.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P]
 _lib.h2o_decode_step.restype = _I
 _lib.h2o_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
-                                 _I, _I, _P, _P, _P, _P]
+                                 _I, _I, _P, _P, _P, _Z, _P, _P]
 _lib.kv_score_obs_noalloc.restype = _I
 _lib.kv_score_obs_noalloc.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P]
 _lib.kv_workspace_size.restype = _Z
@@ -189,7 +189,7 @@ def kv_compact(K: torch.Tensor, V: torch.Tensor, s, idx: torch.Tensor, cap: int 
 
 def h2o_decode_step(q, k_new, v_new, K_cache, V_cache, pos, acc, len_, recent: int, new_pos: int,
                     scale: float | None = None, flags: int = 0, o_out=None, evicted_out=None,
-                    dev_status=None, stream=None):
+                    workspace=None, dev_status=None, stream=None):
     """One decode step, cache state updated in place; returns (o [B][Hq][d] f32, evicted [B][Hkv])."""
     B, Hq, d = q.shape
     _, Hkv, cap, _ = K_cache.shape
@@ -199,10 +199,11 @@ def h2o_decode_step(q, k_new, v_new, K_cache, V_cache, pos, acc, len_, recent: i
     o = o_out if o_out is not None else torch.empty(B, Hq, d, dtype=torch.float32, device=q.device)
     ev = evicted_out if evicted_out is not None else torch.empty(B, Hkv, dtype=torch.int32,
                                                                  device=q.device)
+    ws, nbytes = _workspace(kv_workspace_size(KV_OP_DECODE, B, Hq, Hkv, cap, d), q.device, workspace)
     _check("h2o_decode_step", _lib.h2o_decode_step(
         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(K_cache), _ptr(V_cache), _ptr(pos), _ptr(acc),
         _ptr(len_), B, Hq, Hkv, cap, d, int(recent), int(new_pos), float(scale), int(flags),
-        _dtype_code(q), _ptr(o), _ptr(ev), _ptr(dev_status), _stream(stream)))
+        _dtype_code(q), _ptr(o), _ptr(ev), _ptr(ws), nbytes, _ptr(dev_status), _stream(stream)))
     return o, ev
 
 

@@ -86,6 +86,9 @@ size_t kv_workspace_size(int op, int B, int Hq, int Hkv, int T, int d, int W, in
       return plan_refine(B, Hkv, T).ws_bytes;  // the refine call's H is passed as Hkv
     case KV_OP_SELECT_TOPK:
       return 0;
+    case KV_OP_DECODE:  // T is the slot capacity
+      if (Hq <= 0 || Hkv <= 0 || Hq % Hkv || !(d == 64 || d == 128)) return 0;
+      return decode_workspace_bytes((long)B * Hkv, Hq / Hkv, T, d);
     default:
       return 0;
   }
@@ -156,8 +159,8 @@ int kv_compact(const void *K, const void *V, const float *s, const int32_t *idx,
 int h2o_decode_step(const void *q, const void *k_new, const void *v_new, void *K_cache,
                     void *V_cache, int32_t *pos, float *acc, int32_t *len, int B, int Hq,
                     int Hkv, int cap, int d, int recent, int32_t new_pos, float scale,
-                    int flags, int dtype, float *o_out, int32_t *evicted_pos, int *dev_status,
-                    kv_stream_t stream) {
+                    int flags, int dtype, float *o_out, int32_t *evicted_pos, void *workspace,
+                    size_t workspace_bytes, int *dev_status, kv_stream_t stream) {
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || cap <= 0 || recent < 0 ||
       recent >= cap || new_pos < 0 || !dtype_ok(dtype) || (flags & ~KV_H2O_ALG1) ||
       ((flags & KV_H2O_ALG1) && recent != 0) || !(scale == scale))
@@ -173,10 +176,12 @@ int h2o_decode_step(const void *q, const void *k_new, const void *v_new, void *K
     return KV_ERR_INVALID_ARG;
   const int G = Hq / Hkv;
   if (G != 1 && G != 2 && G != 4 && G != 8) return KV_ERR_UNSUPPORTED;
-  if (decode_smem_bytes(G, cap, d) > 227 * 1024) return KV_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < decode_workspace_bytes((long)B * Hkv, G, cap, d) ||
+      !aligned16(workspace))
+    return KV_ERR_WORKSPACE;
   return launch_decode_step(q, k_new, v_new, K_cache, V_cache, pos, acc, len, B, Hq, Hkv, cap,
-                            d, recent, new_pos, scale, flags, dtype, o_out, evicted_pos,
-                            dev_status, static_cast<cudaStream_t>(stream));
+                            d, recent, new_pos, scale, flags, dtype, workspace, o_out,
+                            evicted_pos, dev_status, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -95,8 +95,8 @@ int launch_compact(const void *K, const void *V, const float *s, const int32_t *
 int launch_decode_step(const void *q, const void *k_new, const void *v_new, void *K_cache,
                        void *V_cache, int32_t *pos, float *acc, int32_t *len, int B, int Hq,
                        int Hkv, int cap, int d, int recent, int32_t new_pos, float scale,
-                       int flags, int dtype, float *o, int32_t *evicted, int *dev_status,
-                       cudaStream_t st);
-size_t decode_smem_bytes(int G, int cap, int d);
+                       int flags, int dtype, void *workspace, float *o, int32_t *evicted,
+                       int *dev_status, cudaStream_t st);
+size_t decode_workspace_bytes(long units, int G, int cap, int d);
 
 }  // namespace kvc

@@ -20,7 +20,8 @@ def lib():
     lib.hubkv_refine.argtypes = [P, I, I, I, I, F, F, F, F, P, P, P, Z, P]
     lib.kv_select_topk.argtypes = [P, I, I, I, I, I, P, P, Z, P]
     lib.kv_compact.argtypes = [P, P, P, P, I, I, I, I, I, I, P, P, I, P, P, P, P]
-    lib.h2o_decode_step.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, P, P, P, P]
+    lib.h2o_decode_step.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, P, P, P, Z, P,
+                                    P]
     lib.kv_workspace_size.restype = Z
     lib.kv_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
     lib.kv_status_string.restype = ctypes.c_char_p
@@ -53,6 +54,7 @@ def test_workspace_size(lib):
     assert lib.kv_workspace_size(2, 4, 8, 8, 32768, 128, 64, 0) > 0
     assert lib.kv_workspace_size(3, 4, 8, 8, 32768, 128, 64, 100) == 0
     assert lib.kv_workspace_size(99, 4, 8, 8, 32768, 128, 64, 100) == 0
+    assert lib.kv_workspace_size(4, 1, 32, 8, 6553, 128, 0, 0) > 32 * 6554 * 4
 
 
 NULL = None
@@ -76,12 +78,12 @@ def test_host_validation_rejects_before_cuda(lib):
                           NULL, NULL) == -1
     # decode: ALG1 with a recent window, recent >= cap, unsupported group size
     assert lib.h2o_decode_step(NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 1, 4, 4, 8, 64, 1, 9,
-                               0.1, 1, 0, NULL, NULL, NULL, NULL) == -1
+                               0.1, 1, 0, NULL, NULL, NULL, 0, NULL, NULL) == -1
     assert lib.h2o_decode_step(NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 1, 4, 4, 8, 64, 8, 9,
-                               0.1, 0, 0, NULL, NULL, NULL, NULL) == -1
+                               0.1, 0, 0, NULL, NULL, NULL, 0, NULL, NULL) == -1
     p = ctypes.c_void_p(16)  # a dummy aligned pointer: never dereferenced, the call is rejected first
     assert lib.h2o_decode_step(p, p, p, p, p, p, p, p, 1, 12, 4, 8, 64, 1, 9, 0.1, 0, 0, p, p, NULL,
-                               NULL) == -2
+                               0, NULL, NULL) == -2
 
 
 def test_empty_batch_is_a_no_op(lib):
@@ -91,7 +93,7 @@ def test_empty_batch_is_a_no_op(lib):
     assert lib.kv_compact(NULL, NULL, NULL, NULL, 0, 2, 10, 5, 64, 0, NULL, NULL, 5, NULL, NULL,
                           NULL, NULL) == 0
     assert lib.h2o_decode_step(NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 0, 4, 4, 8, 64, 1, 9,
-                               0.1, 0, 0, NULL, NULL, NULL, NULL) == 0
+                               0.1, 0, 0, NULL, NULL, NULL, 0, NULL, NULL) == 0
 
 
 def test_no_product_module_imports_the_oracle():
