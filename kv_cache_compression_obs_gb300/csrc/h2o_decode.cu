@@ -6,57 +6,145 @@
 // is protected), FlexGen 改造 (the evicted slot is overwritten in place; the
 // score vector is updated as a by-product of the attention kernel).
 //
-// Two launches per step:
-//   stream -- one CTA per (unit, chunk of CH rows), where a unit is (b, KV head)
-//             and its rows are the filled slots plus the new token.  The CTA
-//             reads its K rows (one row per thread, the whole row's 16-byte loads
-//             in flight, q from shared memory) into logits l_gj = scale <q_g, k_j>,
-//             which it also writes to the workspace; takes its local max m_c and
-//             normaliser Z_c per query head; and reads its V rows (one row per
-//             warp, the lanes across d, 128 bytes per lane in flight) into its
-//             output share o_c relative to m_c.  No CTA waits for another, so the
-//             K and V streams of many CTAs overlap freely on every SM.
-//   evict  -- one cluster of CE CTAs per unit: combines the chunks' (m_c, Z_c,
-//             o_c) into the step's output; turns the stored logits into
-//             probabilities, adds them to the slots' accumulators and takes each
-//             CTA's (acc, pos)-smallest slot outside the recent window; after a
-//             cluster barrier CTA 0 picks the smallest over the cluster (and the
-//             new token itself when recent == 0) and appends the new token or
-//             writes it over the victim; a last barrier keeps the CTAs' shared
-//             memory alive until CTA 0 has read it.
-// Workspace: the logits [units][G][cap+1], the chunks' (m, Z) [units][NCH][G] and
-// output shares [units][NCH][G][D], all float.
+// A unit is (b, KV head); its attended rows are the filled slots 0..n-1 plus the
+// new token (row n).  Two launches per step:
+//
+//   stream   -- persistent, one CTA per SM.  Every unit is cut into blocks of RB
+//               rows, the blocks of all units are laid end to end and each CTA
+//               takes one contiguous range of them.  A producer warp streams each
+//               block's K rows and V rows into two rings of shared-memory stages
+//               with TMA (128-byte swizzle, L2 evict-first, 8 KB per copy); pairs
+//               of consumer warps take the blocks round-robin, each pair always
+//               the same stages and each warp 32 rows of a block.  K stage: thread
+//               per row, logits l_gj = scale <q_g, k_j> for the G query heads of
+//               the group, with q read from shared memory as broadcasts; the
+//               logits also go to the workspace (kept in L2 for the finalize
+//               kernel, which finds the slots' scores and positions there too),
+//               and the warp's running max and normaliser per head are updated
+//               online.  V stage: one row at a time across the lanes,
+//               o_g += exp(l_gj - m_g) v_j.  When the CTA's part of a unit is done,
+//               its warps' (m, Z, o) are combined into one partial per (unit, CTA).
+//   finalize -- one cluster of CE CTAs per unit: combines the partials into
+//               o_out; turns the stored logits into probabilities, adds them to
+//               the slots' accumulators and takes each CTA's (acc, pos)-smallest
+//               slot outside the recent window; after a cluster barrier CTA 0
+//               picks the smallest over the cluster (and the new token itself
+//               when recent == 0) and appends the new token or writes it over the
+//               victim.  A CTA's slot loads are issued before the partials are
+//               combined; P_j = sum_g exp(l_gj - (M_g + ln Z_g)).
+//
+// Workspace: logits [units][G][cap+1] and the per-(unit, CTA) partials (m, Z)
+// [units][PM][G] and o [units][PM][G][D], all float.
 #include <cmath>
 #include <type_traits>
 
 #include <cooperative_groups.h>
 
 #include "kvc_internal.cuh"
+#include "tc_common.cuh"
 
 namespace cg = cooperative_groups;
 
 namespace kvc {
 namespace {
 
-constexpr int NT = 256;   // stream kernel threads
-constexpr int NWARP = NT / 32;
-constexpr int CH = 512;   // rows per stream CTA
-constexpr int NTE = 256;  // evict kernel threads per CTA
-constexpr int CE = 4;     // evict kernel CTAs per unit (one thread-block cluster)
-constexpr int NWE = NTE / 32;
+constexpr int WPB = 2;       // consumer warps per block
+constexpr int RB = 32 * WPB; // rows per block: one per lane of each of its warps
+constexpr int PER_MIN = 8;   // a CTA takes at least this many blocks (bounds partials per unit)
+constexpr int kSmemBudget = 220 * 1024;
+constexpr int kMaxStages = 16;
+constexpr long long kWaitBudget = 2000000000LL;  // clock cycles (~1 s) before a wait gives up
+constexpr long long kDrainBudget = 200000000LL;  // ~0.1 s for copies in flight at exit
+constexpr int BAR_CONS = 1;  // named barrier of the consumer warps
+constexpr int NTF = 256;     // finalize threads per CTA
+constexpr int CE = 4;        // finalize CTAs per unit (one thread-block cluster)
+constexpr int RU = 8;        // finalize slots per thread in flight
 
 __device__ __forceinline__ bool better(float a, int p, float ba, int bp) {
   return a < ba || (a == ba && p < bp);
 }
 
-// EV consecutive elements of a row held packed (EV * sizeof(T) = 4, 8 or 16 bytes)
-// until they are used, so that many rows can be in flight per thread.
+// Shared-memory layout of the stream kernel for element type T, head dim D,
+// group size G and NCW consumer warps (NCW / WPB pairs, each pair one block).
+template <typename T, int D, int G, int NCW>
+struct DGeo {
+  static constexpr int NP = NCW / WPB;             // warp groups, one block each
+  static constexpr int ROWB = D * (int)sizeof(T);  // bytes per K or V row
+  static constexpr int NKB = ROWB / 128;           // 128-byte column blocks per row
+  static constexpr int STAGE = RB * ROWB;          // one block of K (or V) rows
+  static constexpr int PBW = G * D + 2 * G;        // one partial: o[G][D], m[G], Z[G]
+  static constexpr int QS_BYTES = G * D * 4;       // q of the unit, fp32
+  static constexpr int PW_BYTES = NCW * 32 * G * 4;  // per-warp weights exp(l - m) of its 32 rows
+  static constexpr int PB_BYTES = NP * PBW * 4;    // one partial per warp group
+  static constexpr int SC_BYTES = NP * G * 4;      // combine scales
+  static constexpr int MISC_BYTES = 1024;          // barriers, flags
+  static constexpr int FIXED = QS_BYTES + PW_BYTES + PB_BYTES + SC_BYTES + MISC_BYTES;
+  static constexpr int S_FIT = (kSmemBudget - 1024 - FIXED) / (2 * STAGE);
+  // depth of each ring: a multiple of NP, so that a stage is always consumed by
+  // the same warp group and its phases are waited for in order
+  static constexpr int S = ((S_FIT > kMaxStages ? kMaxStages : S_FIT) / NP) * NP;
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = S * STAGE;
+  static constexpr int QS_OFF = 2 * S * STAGE;  // 1024-aligned: STAGE is a multiple of 8192
+  static constexpr int PW_OFF = QS_OFF + QS_BYTES;
+  static constexpr int PB_OFF = PW_OFF + PW_BYTES;
+  static constexpr int SC_OFF = PB_OFF + PB_BYTES;
+  static constexpr int MISC_OFF = SC_OFF + SC_BYTES;
+  static constexpr int SMEM = 1024 /*alignment slack*/ + MISC_OFF + MISC_BYTES;
+  static_assert(NKB >= 1 && ROWB % 128 == 0, "rows are whole 128-byte blocks");
+  static_assert(NCW % WPB == 0, "whole warp groups");
+  static_assert(4 * kMaxStages * 8 + 64 + 8 * G <= MISC_BYTES, "misc area");
+};
+
+// Consumer warps: the most (of 12, 8, 6, 4) that still give every warp group a
+// stage of each ring.
+template <typename T, int D, int G>
+struct Pick {
+  static constexpr int NCW = DGeo<T, D, G, 12>::S >= 6 ? 12 : DGeo<T, D, G, 8>::S >= 4 ? 8
+                           : DGeo<T, D, G, 6>::S >= 3 ? 6 : 4;
+  using Geo = DGeo<T, D, G, NCW>;
+  static_assert(Geo::S >= Geo::NP && Geo::S % Geo::NP == 0, "ring depth");
+};
+
+struct Cand {
+  float acc;
+  int pos;
+  int slot;       // -2: no candidate
+  float accself;  // the new token's score
+};
+
+struct Ws {      // workspace carve-up
+  float *lgw;    // [units][G][cap+1] logits
+  float2 *pmz;   // [units][PM][G] per-(unit, CTA) max and normaliser
+  float *po;     // [units][PM][G][D] per-(unit, CTA) output shares (relative to the max)
+};
+
+inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+__host__ __device__ inline int blocks_per_unit(int cap) { return (cap + 1 + RB - 1) / RB; }
+// Partials per unit: a unit's NB blocks meet at most ceil(NB / per) + 1 CTA
+// ranges, and every range holds at least PER_MIN blocks unless one CTA runs alone.
+__host__ __device__ inline int partials_per_unit(int cap) {
+  return (blocks_per_unit(cap) + PER_MIN - 1) / PER_MIN + 1;
+}
+
+Ws carve(void *ws, long units, int G, int cap) {
+  const int PM = partials_per_unit(cap);
+  Ws w;
+  char *p = static_cast<char *>(ws);
+  w.lgw = reinterpret_cast<float *>(p);
+  p += align256((size_t)units * G * (cap + 1) * 4);
+  w.pmz = reinterpret_cast<float2 *>(p);
+  p += align256((size_t)units * PM * G * 8);
+  w.po = reinterpret_cast<float *>(p);
+  return w;
+}
+
+// EV consecutive elements of a row (EV * sizeof(T) = 4, 8 or 16 bytes).
 template <typename T, int EV>
-struct RawV {
+struct RowPiece {
   static constexpr int BYTES = EV * (int)sizeof(T);
   using Word = typename std::conditional<BYTES == 16, uint4,
                typename std::conditional<BYTES == 8, uint2, uint32_t>::type>::type;
-  __device__ __forceinline__ static Word load(const T *p) { return __ldg(reinterpret_cast<const Word *>(p)); }
   __device__ __forceinline__ static void unpack(const Word &w, float (&f)[EV]) {
     if constexpr (BYTES == 16) {
       Vec16<T>::unpack(w, f);
@@ -75,223 +163,415 @@ struct RawV {
   }
 };
 
-struct Ws {      // workspace carve-up
-  float *lgw;    // [units][G][cap+1] logits
-  float2 *mz;    // [units][nch][G] chunk max and normaliser
-  float *opart;  // [units][nch][G][D] chunk output shares
-};
-
-__host__ __device__ inline int n_chunks(int cap) { return (cap + 1 + CH - 1) / CH; }
-
-inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
-
-Ws carve(void *ws, long units, int G, int cap) {
-  Ws w;
-  char *p = static_cast<char *>(ws);
-  const size_t lg_bytes = align256((size_t)units * G * (cap + 1) * 4);
-  const size_t mz_bytes = align256((size_t)units * n_chunks(cap) * G * 8);
-  w.lgw = reinterpret_cast<float *>(p);
-  w.mz = reinterpret_cast<float2 *>(p + lg_bytes);
-  w.opart = reinterpret_cast<float *>(p + lg_bytes + mz_bytes);
-  return w;
+// Byte offset of byte `b` of row `r` inside a stage written by the 2-D TMA with
+// the 128-byte swizzle: column block b / 128 holds RB rows of 128 bytes, and the
+// 16-byte chunk c of row r sits at chunk c ^ (r % 8).
+__device__ __forceinline__ int swz(int r, int b) {
+  return (b >> 7) * (RB * 128) + r * 128 + ((((b >> 4) & 7) ^ (r & 7)) << 4) + (b & 15);
 }
 
-template <typename T, int D, int G>
-__global__ __launch_bounds__(NT, 4) void decode_stream_kernel(
+// The CTAs of the stream kernel whose block ranges meet unit u: the first, and how many.
+struct Span {
+  int first, count;
+};
+__device__ __forceinline__ Span unit_span(long u, int NB, long per) {
+  const int first = static_cast<int>((u * NB) / per);
+  const int last = static_cast<int>(((u + 1) * NB - 1) / per);
+  return Span{first, last - first + 1};
+}
+
+__device__ __forceinline__ void fail(volatile int *abort_flag, int *status) {
+  *abort_flag = 1;
+  if (status) atomicExch(status, (int)KV_ERR_TIMEOUT);
+}
+
+template <typename T, int D, int G, int NCW>
+__global__ __launch_bounds__(32 * (NCW + 1), 1) void decode_stream_kernel(
+    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
     const T *__restrict__ q, const T *__restrict__ k_new, const T *__restrict__ v_new,
-    const T *__restrict__ Kc, const T *__restrict__ Vc, const int32_t *__restrict__ len, int Hq,
-    int Hkv, int cap, float scale, int alg1, Ws ws, int *__restrict__ dev_status) {
-  constexpr int EPL = Vec16<T>::N;              // elements per 16-byte vector
-  constexpr int VPR = D * (int)sizeof(T) / 16;  // 16-byte vectors per K row
-  constexpr int VB = VPR < 8 ? VPR : 8;         // K vectors per load batch
-  constexpr int EV = D / 32;                    // V elements per lane
-  using RV = RawV<T, EV>;
-  constexpr int U = 128 / RV::BYTES;            // V rows per warp in flight (128 bytes per lane)
-  __shared__ __align__(16) float qs[G * D];
-  __shared__ float wst[NWARP * G];
-  __shared__ float cst[G];
-  extern __shared__ __align__(16) float dyn[];  // stream_smem_bytes(G, D)
-  float *wred = dyn;                            // [NWARP][G][D]
-  float *lg = dyn + NWARP * G * D;              // [CH][G] logits, then weights exp(l - m_c)
+    const float *__restrict__ acc, const int32_t *__restrict__ pos, const int32_t *__restrict__ len,
+    int Hq, int Hkv, int cap, float scale, int alg1, long total, long per, Ws ws,
+    int *__restrict__ dev_status) {
+  using Geo = DGeo<T, D, G, NCW>;
+  constexpr int S = Geo::S;
+  constexpr int NP = Geo::NP;
+  constexpr int NCT = 32 * NCW;
+  constexpr int EV = D / 32;  // V elements per lane
+  constexpr int PBW = Geo::PBW;
+  constexpr int EPL = Vec16<T>::N;
+  using RP = RowPiece<T, EV>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *sm = reinterpret_cast<unsigned char *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  unsigned char *sK = sm + Geo::K_OFF;
+  unsigned char *sV = sm + Geo::V_OFF;
+  float *qs = reinterpret_cast<float *>(sm + Geo::QS_OFF);
+  float *pw = reinterpret_cast<float *>(sm + Geo::PW_OFF);
+  float *pb = reinterpret_cast<float *>(sm + Geo::PB_OFF);
+  float *sc = reinterpret_cast<float *>(sm + Geo::SC_OFF);
+  uint64_t *kfull = reinterpret_cast<uint64_t *>(sm + Geo::MISC_OFF);
+  uint64_t *kempty = kfull + kMaxStages;
+  uint64_t *vfull = kempty + kMaxStages;
+  uint64_t *vempty = vfull + kMaxStages;
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(vempty + kMaxStages);
+  float *fm = reinterpret_cast<float *>(sm + Geo::MISC_OFF + 4 * kMaxStages * 8 + 64);  // [G] max
+  float *fz = fm + G;                                                                   // [G] normaliser
 
-  const int nch = n_chunks(cap);
-  const long unit = blockIdx.x / nch;
-  const int c = static_cast<int>(blockIdx.x % nch);
-  const long b = unit / Hkv;
-  const int h = static_cast<int>(unit % Hkv);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int n = len[unit];
-  if (n < 0 || n > cap) {
-    if (c == 0 && threadIdx.x == 0 && dev_status) atomicExch(dev_status, (int)KV_ERR_INVALID_ARG);
-    return;
-  }
-  const int nc = n + (alg1 ? 0 : 1);          // attended rows: slots 0..n-1, then the new token
-  const int r0 = c * CH;
-  const int nl = max(0, min(CH, nc - r0));    // this CTA's rows
-  float2 *mz = ws.mz + (unit * nch + c) * G;
-  float *op = ws.opart + (unit * nch + c) * (long)G * D;
-  if (nl == 0) {
-    if (threadIdx.x < G) mz[threadIdx.x] = make_float2(-INFINITY, 0.f);
-    return;
-  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int NB = blocks_per_unit(cap);
+  const int PM = partials_per_unit(cap);
+  const long lo = blockIdx.x * per;
+  const long hi = min(total, lo + per);
 
-  const T *qg = q + (b * Hq + (long)h * G) * D;
-  for (int t = threadIdx.x; t < G * D; t += NT) qs[t] = to_f32(qg[t]);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) {
+      tc::mbar_init(kfull + i, 1);
+      tc::mbar_init(kempty + i, WPB);
+      tc::mbar_init(vfull + i, 1);
+      tc::mbar_init(vempty + i, WPB);
+    }
+    *abort_flag = 0;
+    tc::mbar_fence_init();
+  }
   __syncthreads();
 
-  const T *Ku = Kc + unit * (long)cap * D;
-  const T *Vu = Vc + unit * (long)cap * D;
-  const T *kn = k_new + unit * (long)D;
-  const T *vn = v_new + unit * (long)D;
-  auto row_ptr = [&](const T *base, const T *fresh, int r) -> const T * {
-    const int j = r0 + r;
-    return (j < n) ? base + (long)j * D : fresh;
-  };
-  float *lgu = ws.lgw + unit * (long)G * (cap + 1);
-
-  // 1. logits: one thread per row; two packed partial sums per query head
-  for (int r = threadIdx.x; r < nl; r += NT) {
-    const uint4 *row = reinterpret_cast<const uint4 *>(row_ptr(Ku, kn, r));
-    float2 part[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g) part[g] = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int v0 = 0; v0 < VPR; v0 += VB) {
-      uint4 raw[VB];
-#pragma unroll
-      for (int v = 0; v < VB; ++v) raw[v] = __ldg(row + v0 + v);
-#pragma unroll
-      for (int v = 0; v < VB; ++v) {
-        float f[EPL];
-        Vec16<T>::unpack(raw[v], f);
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float4 *q4 = reinterpret_cast<const float4 *>(qs + g * D + (v0 + v) * EPL);
-#pragma unroll
-          for (int e4 = 0; e4 < EPL / 4; ++e4) {
-            const float4 qq = q4[e4];
-            part[g] = __ffma2_rn(make_float2(f[4 * e4 + 0], f[4 * e4 + 1]), make_float2(qq.x, qq.y), part[g]);
-            part[g] = __ffma2_rn(make_float2(f[4 * e4 + 2], f[4 * e4 + 3]), make_float2(qq.z, qq.w), part[g]);
-          }
+  if (warp == 0) {
+    // ---------------- producer (one lane) ----------------
+    if (lane == 0 && lo < hi) {
+      tc::tma_prefetch_desc(&tmK);
+      tc::tma_prefetch_desc(&tmV);
+      const uint64_t pol = tc::make_policy_evict_first();
+      long cur_u = -1;
+      int n = 0;
+      long i = 0;
+      for (long gb = lo; gb < hi; ++gb, ++i) {
+        const long u = gb / NB;
+        const int jb = static_cast<int>(gb % NB);
+        if (u != cur_u) {
+          cur_u = u;
+          n = len[u];
+          if (n < 0 || n > cap) n = 0;  // reported by the finalize kernel
+        }
+        const int rows = max(0, min(RB, n - jb * RB));  // cached rows in this block
+        const int si = static_cast<int>(i % S);
+        const uint32_t ph = static_cast<uint32_t>((i / S) & 1);
+        const int y = static_cast<int>(u * cap + (long)jb * RB);
+        if (!tc::mbar_wait(kempty + si, ph ^ 1, kWaitBudget, abort_flag)) {
+          fail(abort_flag, dev_status);
+          break;
+        }
+        if (rows > 0) {
+          tc::mbar_arrive_expect_tx(kfull + si, Geo::STAGE);
+          for (int kb = 0; kb < Geo::NKB; ++kb)
+            tc::tma_load_2d_hint(sK + si * Geo::STAGE + kb * RB * 128, &tmK, kb * (128 / (int)sizeof(T)), y,
+                                 kfull + si, pol);
+        } else {
+          tc::mbar_arrive(kfull + si);
+        }
+        if (!tc::mbar_wait(vempty + si, ph ^ 1, kWaitBudget, abort_flag)) {
+          ++i;  // this block's K copy may be in flight
+          fail(abort_flag, dev_status);
+          break;
+        }
+        if (rows > 0) {
+          tc::mbar_arrive_expect_tx(vfull + si, Geo::STAGE);
+          for (int kb = 0; kb < Geo::NKB; ++kb)
+            tc::tma_load_2d_hint(sV + si * Geo::STAGE + kb * RB * 128, &tmV, kb * (128 / (int)sizeof(T)), y,
+                                 vfull + si, pol);
+        } else {
+          tc::mbar_arrive(vfull + si);
+        }
+      }
+      if (*abort_flag) {
+        // copies still in flight land before the CTA may exit (bounded waits)
+        for (long k = 1; k <= S && i - k >= 0; ++k) {
+          const long ii = i - k;
+          tc::mbar_wait(kfull + ii % S, (uint32_t)((ii / S) & 1), kDrainBudget, nullptr);
+          tc::mbar_wait(vfull + ii % S, (uint32_t)((ii / S) & 1), kDrainBudget, nullptr);
         }
       }
     }
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float l = scale * (part[g].x + part[g].y);
-      lg[r * G + g] = l;
-      lgu[(long)g * (cap + 1) + r0 + r] = l;
-    }
-  }
-  __syncthreads();
-
-  // 2. the chunk's max, weights exp(l - m_c) and normaliser
-  float mx[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) mx[g] = -INFINITY;
-  for (int r = threadIdx.x; r < nl; r += NT)
-#pragma unroll
-    for (int g = 0; g < G; ++g) mx[g] = fmaxf(mx[g], lg[r * G + g]);
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx[g] = fmaxf(mx[g], __shfl_xor_sync(0xFFFFFFFFu, mx[g], off));
-    if (lane == 0) wst[warp * G + g] = mx[g];
-  }
-  __syncthreads();
-  if (threadIdx.x < G) {
-    float m = -INFINITY;
-    for (int w = 0; w < NWARP; ++w) m = fmaxf(m, wst[w * G + threadIdx.x]);
-    cst[threadIdx.x] = m;
-  }
-  __syncthreads();
-  float zs[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) zs[g] = 0.f;
-  for (int r = threadIdx.x; r < nl; r += NT)
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float e = expf(lg[r * G + g] - cst[g]);
-      lg[r * G + g] = e;
-      zs[g] += e;
-    }
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) zs[g] += __shfl_xor_sync(0xFFFFFFFFu, zs[g], off);
-  }
-  __syncthreads();  // every thread is done reading wst (the max) before it is reused
-  if (lane == 0) {
-#pragma unroll
-    for (int g = 0; g < G; ++g) wst[warp * G + g] = zs[g];
-  }
-  __syncthreads();
-  if (threadIdx.x < G) {
-    float z = 0.f;
-    for (int w = 0; w < NWARP; ++w) z += wst[w * G + threadIdx.x];
-    mz[threadIdx.x] = make_float2(cst[threadIdx.x], z);
+    __syncwarp();
+    return;
   }
 
-  // 3. the chunk's output share relative to m_c: one V row per warp, lanes across d
-  static_assert(EV % 2 == 0, "V elements per lane come in pairs");
-  float2 o[G][EV / 2];
+  // ---------------- consumers: warp group gp takes blocks gp, gp + NP, ... ----------------
+  const int w = warp - 1;     // 0 .. NCW-1
+  const int gp = w % NP;      // warp group
+  const int hw = w / NP;      // this warp's 32 rows of a block: [32 hw, 32 hw + 32)
+  const int ct = threadIdx.x - 32;
+  float *pww = pw + w * 32 * G;  // this warp's weights [32][G]
+  const uint64_t pol_keep = tc::make_policy_evict_last();
+  // this lane's byte offsets of its V piece in rows 0..7 of a stage (the swizzle repeats every 8 rows)
+  const int vb = lane * EV * (int)sizeof(T);
+  int voff[8];
 #pragma unroll
-  for (int g = 0; g < G; ++g)
+  for (int k = 0; k < 8; ++k) voff[k] = swz(k, vb);
+  bool ok = true;
+  long i = 0;
+  // A warp that gives up keeps walking the same items (without touching the
+  // rings) so that every named barrier is reached by all consumer threads.
+  for (long gb = lo; gb < hi;) {
+    const long u = gb / NB;
+    const long item_end = min(hi, (u + 1) * NB);
+    const long b = u / Hkv;
+    const int h = static_cast<int>(u % Hkv);
+    int n = len[u];
+    const bool valid = n >= 0 && n <= cap;
+    if (!valid) n = 0;
+    const int nc = valid ? n + (alg1 ? 0 : 1) : 0;  // attended rows
+    const T *qg = q + (b * Hq + (long)h * G) * D;
+    tc::named_bar_sync(BAR_CONS, NCT);  // the previous item's shared-memory readers are done
+    for (int t = ct; t < G * D; t += NCT) qs[t] = to_f32(qg[t]);
+    tc::named_bar_sync(BAR_CONS, NCT);
+
+    float m[G], zl[G];
+    float2 o[G][EV / 2];
 #pragma unroll
-    for (int e = 0; e < EV / 2; ++e) o[g][e] = make_float2(0.f, 0.f);
-  for (int rr = warp * U; rr < nl; rr += NWARP * U) {
-    typename RV::Word raw[U];
+    for (int g = 0; g < G; ++g) {
+      m[g] = -INFINITY;
+      zl[g] = 0.f;
 #pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (rr + u < nl) raw[u] = RV::load(row_ptr(Vu, vn, rr + u) + lane * EV);
+      for (int e = 0; e < EV / 2; ++e) o[g][e] = make_float2(0.f, 0.f);
+    }
+    float *lgu = ws.lgw + u * (long)G * (cap + 1);
+    const T *vn = v_new + u * (long)D;
+
+    for (; gb < item_end; ++gb, ++i) {
+      if ((int)(i % NP) != gp || !ok) continue;
+      const int r0 = static_cast<int>(gb % NB) * RB;
+      const int rows = max(0, min(RB, n - r0));                // cached rows of the block
+      const bool has_new = nc > n && n >= r0 && n < r0 + RB;  // the new token is block row `rows`
+      const bool my_new = has_new && (rows >> 5) == hw;        // ... and one of this warp's
+      const int wr0 = 32 * hw;                                 // this warp's first block row
+      const int wrows = max(0, min(32, rows - wr0));           // its cached rows
+      const int wnv = wrows + (my_new ? 1 : 0);
+      const int si = static_cast<int>(i % S);
+      const uint32_t ph = static_cast<uint32_t>((i / S) & 1);
+
+      // the scores and positions of these slots are read again by the finalize kernel
+      if (lane < 2 && wrows > 0) {  // first and last of this warp's slots: every line they span
+        const long e = u * (long)cap + r0 + wr0 + (lane ? wrows - 1 : 0);
+        tc::prefetch_l2_last(acc + e);
+        tc::prefetch_l2_last(pos + e);
+      }
+      // the new token's logits: the lanes across d, then a warp sum
+      float lnew[G];
+      if (my_new) {
+        const typename RP::Word word =
+            __ldg(reinterpret_cast<const typename RP::Word *>(k_new + u * (long)D + lane * EV));
+        float kv[EV];
+        RP::unpack(word, kv);
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      if (rr + u < nl) {
-        float vv[EV];
-        RV::unpack(raw[u], vv);
-        float pg[G];
+        for (int g = 0; g < G; ++g) {
+          float s = 0.f;
 #pragma unroll
-        for (int g = 0; g < G; ++g) pg[g] = lg[(rr + u) * G + g];
+          for (int e = 0; e < EV; ++e) s = fmaf(kv[e], qs[g * D + lane * EV + e], s);
 #pragma unroll
-        for (int g = 0; g < G; ++g)
+          for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
+          lnew[g] = scale * s;
+        }
+      }
+
+      if (!tc::mbar_wait(kfull + si, ph, kWaitBudget, abort_flag)) {
+        fail(abort_flag, dev_status);
+        ok = false;
+        continue;
+      }
+      // K stage: lane owns block row wr0 + lane
+      float l[G];
+      {
+        float2 part[G];
 #pragma unroll
-          for (int e = 0; e < EV / 2; ++e)
-            o[g][e] = __ffma2_rn(make_float2(pg[g], pg[g]), make_float2(vv[2 * e], vv[2 * e + 1]), o[g][e]);
+        for (int g = 0; g < G; ++g) part[g] = make_float2(0.f, 0.f);
+        if (lane < wrows) {
+          const unsigned char *kst = sK + si * Geo::STAGE + (wr0 + lane) * 128;
+#pragma unroll
+          for (int c = 0; c < Geo::ROWB / 16; ++c) {
+            float f[EPL];
+            Vec16<T>::unpack(*reinterpret_cast<const uint4 *>(
+                                 kst + (c >> 3) * (RB * 128) + (((c & 7) ^ (lane & 7)) << 4)),
+                             f);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              const float4 *q4 = reinterpret_cast<const float4 *>(qs + g * D + c * EPL);
+#pragma unroll
+              for (int e4 = 0; e4 < EPL / 4; ++e4) {
+                const float4 qq = q4[e4];
+                part[g] = __ffma2_rn(make_float2(f[4 * e4 + 0], f[4 * e4 + 1]), make_float2(qq.x, qq.y), part[g]);
+                part[g] = __ffma2_rn(make_float2(f[4 * e4 + 2], f[4 * e4 + 3]), make_float2(qq.z, qq.w), part[g]);
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) l[g] = scale * (part[g].x + part[g].y);
+      }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(kempty + si);
+      if (my_new && lane == (rows & 31)) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) l[g] = lnew[g];
+      }
+      if (lane < wnv) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) tc::st_f32_hint(lgu + (long)g * (cap + 1) + r0 + wr0 + lane, l[g], pol_keep);
+      }
+      if (wnv > 0) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float bm = lane < wnv ? l[g] : -INFINITY;
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, off));
+          const float mn = fmaxf(m[g], bm);
+          if (mn != m[g]) {
+            const float s = expf(m[g] - mn);  // 0 while nothing has been seen
+            zl[g] *= s;
+#pragma unroll
+            for (int e = 0; e < EV / 2; ++e) o[g][e] = __fmul2_rn(o[g][e], make_float2(s, s));
+            m[g] = mn;
+          }
+          const float p = lane < wnv ? expf(l[g] - mn) : 0.f;
+          zl[g] += p;
+          pww[lane * G + g] = p;
+        }
+      }
+      __syncwarp();
+
+      // V stage: one row at a time across the lanes
+      if (!tc::mbar_wait(vfull + si, ph, kWaitBudget, abort_flag)) {
+        fail(abort_flag, dev_status);
+        ok = false;
+        continue;
+      }
+      {
+        const unsigned char *vst = sV + si * Geo::STAGE + wr0 * 128;  // wr0 is a multiple of 8
+        auto accum = [&](const typename RP::Word &word, int r) {
+          float vv[EV];
+          RP::unpack(word, vv);
+          float pg[G];
+          if constexpr (G % 4 == 0) {
+#pragma unroll
+            for (int g4 = 0; g4 < G; g4 += 4) {
+              const float4 p4 = *reinterpret_cast<const float4 *>(pww + r * G + g4);
+              pg[g4] = p4.x;
+              pg[g4 + 1] = p4.y;
+              pg[g4 + 2] = p4.z;
+              pg[g4 + 3] = p4.w;
+            }
+          } else {
+#pragma unroll
+            for (int g = 0; g < G; ++g) pg[g] = pww[r * G + g];
+          }
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int e = 0; e < EV / 2; ++e)
+              o[g][e] = __ffma2_rn(make_float2(pg[g], pg[g]), make_float2(vv[2 * e], vv[2 * e + 1]), o[g][e]);
+        };
+        const int full8 = wrows & ~7;
+        for (int r8 = 0; r8 < full8; r8 += 8) {
+          typename RP::Word word[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            word[k] = *reinterpret_cast<const typename RP::Word *>(vst + r8 * 128 + voff[k]);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) accum(word[k], r8 + k);
+        }
+        for (int r = full8; r < wrows; ++r)
+          accum(*reinterpret_cast<const typename RP::Word *>(vst + swz(r, vb)), r);
+        if (my_new) accum(__ldg(reinterpret_cast<const typename RP::Word *>(vn + lane * EV)), wrows);
+      }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(vempty + si);
+    }
+
+    // ---- the unit's range in this CTA is done: combine the warps into one partial ----
+    // (1) every warp reduces its normaliser; the second warp of each group deposits
+    float zw[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float z = zl[g];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, off);
+      zw[g] = z;
+    }
+    float *pbg = pb + gp * PBW;
+    auto deposit = [&]() {
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+#pragma unroll
+        for (int e = 0; e < EV / 2; ++e) {
+          pbg[g * D + lane * EV + 2 * e] = o[g][e].x;
+          pbg[g * D + lane * EV + 2 * e + 1] = o[g][e].y;
+        }
+        if (lane == 0) {
+          pbg[G * D + g] = m[g];
+          pbg[G * D + G + g] = zw[g];
+        }
+      }
+    };
+    static_assert(WPB == 2, "the merge below pairs two warps");
+    if (hw == 1) deposit();
+    tc::named_bar_sync(BAR_CONS, NCT);
+    // (2) the first warp of each group merges its partner's partial into its own
+    if (hw == 0) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float m1 = pbg[G * D + g];
+        const float Mx = fmaxf(m[g], m1);
+        const float s0 = m[g] == -INFINITY ? 0.f : expf(m[g] - Mx);
+        const float s1 = m1 == -INFINITY ? 0.f : expf(m1 - Mx);
+#pragma unroll
+        for (int e = 0; e < EV / 2; ++e) {
+          const float2 o1 = make_float2(pbg[g * D + lane * EV + 2 * e], pbg[g * D + lane * EV + 2 * e + 1]);
+          o[g][e] = __ffma2_rn(o[g][e], make_float2(s0, s0), __fmul2_rn(o1, make_float2(s1, s1)));
+        }
+        zw[g] = zw[g] * s0 + pbg[G * D + G + g] * s1;
+        m[g] = Mx;
       }
     }
-  }
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int e = 0; e < EV / 2; ++e) {
-      wred[(warp * G + g) * D + lane * EV + 2 * e] = o[g][e].x;
-      wred[(warp * G + g) * D + lane * EV + 2 * e + 1] = o[g][e].y;
+    tc::named_bar_sync(BAR_CONS, NCT);
+    if (hw == 0) deposit();
+    tc::named_bar_sync(BAR_CONS, NCT);
+    // (3) the groups' partials -> one partial of this CTA
+    if (ct < G) {
+      float M = -INFINITY;
+      for (int v = 0; v < NP; ++v) M = fmaxf(M, pb[v * PBW + G * D + ct]);
+      float Z = 0.f;
+      for (int v = 0; v < NP; ++v) {
+        const float mv = pb[v * PBW + G * D + ct];
+        const float s = mv == -INFINITY ? 0.f : expf(mv - M);
+        sc[v * G + ct] = s;
+        Z += pb[v * PBW + G * D + G + ct] * s;
+      }
+      fm[ct] = M;
+      fz[ct] = Z;
     }
-  __syncthreads();
-  for (int t = threadIdx.x; t < G * D; t += NT) {
-    float s = 0.f;
-    for (int w = 0; w < NWARP; ++w) s += wred[w * G * D + t];
-    op[t] = s;
+    tc::named_bar_sync(BAR_CONS, NCT);
+    const Span sp = unit_span(u, NB, per);
+    const long slot = u * PM + (static_cast<int>(blockIdx.x) - sp.first);
+    float *pou = ws.po + slot * (long)G * D;
+    for (int t = ct; t < G * D; t += NCT) {
+      const int g = t / D;
+      float s = 0.f;
+      for (int v = 0; v < NP; ++v) s += pb[v * PBW + t] * sc[v * G + g];
+      pou[t] = s;
+    }
+    if (ct < G) ws.pmz[slot * G + ct] = make_float2(fm[ct], fz[ct]);
   }
 }
 
-struct Cand {
-  float acc;
-  int pos;
-  int slot;       // -2: no candidate
-  float accself;  // the new token's score, from the CTA that holds its row
-};
-
-template <int G, int D>
-__global__ __launch_bounds__(NTE) void decode_evict_kernel(
-    int32_t *__restrict__ pos, float *__restrict__ acc, int32_t *__restrict__ len, int Hq,
-    int Hkv, int cap, int recent, int new_pos, int alg1, Ws ws, void *__restrict__ Kc,
-    void *__restrict__ Vc, const void *__restrict__ k_new, const void *__restrict__ v_new,
-    int row_bytes, float *__restrict__ o_out, int32_t *__restrict__ evicted,
-    int *__restrict__ dev_status) {
-  constexpr int RU = 4;  // rows per thread in flight
-  __shared__ float gm[G], gz[G];
-  __shared__ Cand wc[NWE];
+template <typename T, int D, int G>
+__global__ __launch_bounds__(NTF) void decode_finalize_kernel(
+    const T *__restrict__ k_new, const T *__restrict__ v_new, T *__restrict__ Kc, T *__restrict__ Vc,
+    int32_t *__restrict__ pos, float *__restrict__ acc, int32_t *__restrict__ len, int Hq, int Hkv,
+    int cap, int recent, int new_pos, int alg1, long per, Ws ws, float *__restrict__ o_out,
+    int32_t *__restrict__ evicted, int *__restrict__ dev_status) {
+  constexpr int NWF = NTF / 32;
+  constexpr int GD = G * D;
+  __shared__ float gm[G], gz[G], gc[G];
+  __shared__ Cand wc[NWF];
   __shared__ Cand cand;
   __shared__ int sh_slot;
   cg::cluster_group cluster = cg::this_cluster();
@@ -301,75 +581,90 @@ __global__ __launch_bounds__(NTE) void decode_evict_kernel(
   const int h = static_cast<int>(unit % Hkv);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int n = len[unit];
-  if (n < 0 || n > cap) return;  // same n in the whole cluster; reported by the stream kernel
-  const int nch = n_chunks(cap);
+  if (n < 0 || n > cap) {  // same n in the whole cluster: every CTA leaves here
+    if (rank == 0 && threadIdx.x == 0 && dev_status) atomicExch(dev_status, (int)KV_ERR_INVALID_ARG);
+    return;
+  }
+  const int NB = blocks_per_unit(cap);
+  const int PM = partials_per_unit(cap);
+  const Span sp = unit_span(unit, NB, per);
   const int nc = n + (alg1 ? 0 : 1);
-  const float2 *mz = ws.mz + unit * nch * G;
-  const int nuse = (nc + CH - 1) / CH;  // chunks that hold rows
-  if (threadIdx.x < G) {
-    const int g = threadIdx.x;
-    float m = -INFINITY;
-    for (int c = 0; c < nuse; ++c) m = fmaxf(m, mz[c * G + g].x);
-    float z = 0.f;
-    for (int c = 0; c < nuse; ++c) {
-      const float2 p = mz[c * G + g];
-      if (p.x != -INFINITY) z += p.y * expf(p.x - m);
-    }
-    gm[g] = m;
-    gz[g] = z;
-  }
-  __syncthreads();
-  // this CTA's part of the output: o_g = sum_c o_c exp(m_c - m) / Z
-  float *ou = o_out + (b * Hq + (long)h * G) * D;
-  const float *opu = ws.opart + unit * nch * (long)G * D;
-  constexpr int GD = G * D;
-  for (int t = rank * (GD / CE) + threadIdx.x; t < (rank + 1) * (GD / CE); t += NTE) {
-    const int g = t / D;
-    float s = 0.f;
-    for (int c = 0; c < nuse; ++c) {
-      const float mc = mz[c * G + g].x;
-      if (mc != -INFINITY) s += opu[(long)c * GD + t] * expf(mc - gm[g]);
-    }
-    ou[t] = nuse ? s / gz[g] : 0.f;
-  }
-  // this CTA's rows: probabilities -> accumulators, eviction candidate
-  const int per = (nc + CE - 1) / CE;
-  const int j0 = min(nc, rank * per), j1 = min(nc, j0 + per);
+  const float2 *pmz = ws.pmz + unit * PM * G;
+  const float *po = ws.po + unit * PM * (long)GD;
   const float *lgu = ws.lgw + unit * (long)G * (cap + 1);
   float *au = acc + unit * (long)cap;
   int32_t *pu = pos + unit * (long)cap;
+
+  // this CTA's slots: their loads are issued before the partials are combined
+  const int per_cta = (nc + CE - 1) / CE;
+  const int j0 = min(nc, rank * per_cta), j1 = min(nc, j0 + per_cta);
+  float lv[RU][G], av[RU];
+  int pv[RU];
+  auto load_slots = [&](int jb) {
+#pragma unroll
+    for (int k = 0; k < RU; ++k) {
+      const int j = jb + k * NTF;
+      if (j < j1) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) lv[k][g] = lgu[(long)g * (cap + 1) + j];
+        if (j < n) {
+          av[k] = au[j];
+          pv[k] = pu[j];
+        }
+      }
+    }
+  };
+  const int jstart = j0 + threadIdx.x;
+  load_slots(jstart);
+  // the unit's max and normaliser per head over the partials (a partial of an
+  // empty range has m = -inf and Z = 0 and adds nothing)
+  if (threadIdx.x < G) {
+    const int g = threadIdx.x;
+    float M = -INFINITY, Z = 0.f;
+    for (int p = 0; p < sp.count; ++p) {
+      const float2 v = pmz[p * G + g];
+      if (v.x == -INFINITY) continue;
+      const float Mn = fmaxf(M, v.x);
+      Z = Z * expf(M - Mn) + v.y * expf(v.x - Mn);
+      M = Mn;
+    }
+    gm[g] = M;
+    gz[g] = Z;
+    gc[g] = M + logf(Z);  // exp(l - M) / Z = exp(l - gc)
+  }
+  __syncthreads();
+  // this CTA's part of the output: o_g = sum_p o_p exp(m_p - M) / Z
+  float *ou = o_out + (b * Hq + (long)h * G) * D;
+  for (int t = rank * (GD / CE) + threadIdx.x; t < (rank + 1) * (GD / CE); t += NTF) {
+    const int g = t / D;
+    float s = 0.f;
+#pragma unroll 4
+    for (int p = 0; p < sp.count; ++p) {
+      const float mp = pmz[p * G + g].x;  // o_p = 0 where m_p = -inf
+      s += po[(long)p * GD + t] * (mp == -INFINITY ? 0.f : expf(mp - gm[g]));
+    }
+    ou[t] = nc > 0 ? s / gz[g] : 0.f;
+  }
+  // probabilities -> accumulators, eviction candidate
   const long lim = (long)new_pos - recent;
   float best_a = INFINITY;
   int best_p = 0x7FFFFFFF, best_j = -2;
   float acc_self = 0.f;
-  for (int jb = j0 + threadIdx.x; jb < j1; jb += RU * NTE) {
-    float lv[RU][G], av[RU];
-    int pv[RU];
+  for (int jb = jstart; jb < j1; jb += RU * NTF) {
+    if (jb != jstart) load_slots(jb);
 #pragma unroll
-    for (int u = 0; u < RU; ++u) {
-      const int j = jb + u * NTE;
-      if (j < j1) {
-#pragma unroll
-        for (int g = 0; g < G; ++g) lv[u][g] = lgu[(long)g * (cap + 1) + j];
-        if (j < n) {
-          av[u] = au[j];
-          pv[u] = pu[j];
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < RU; ++u) {
-      const int j = jb + u * NTE;
+    for (int k = 0; k < RU; ++k) {
+      const int j = jb + k * NTF;
       if (j >= j1) continue;
       float P = 0.f;
 #pragma unroll
-      for (int g = 0; g < G; ++g) P += expf(lv[u][g] - gm[g]) / gz[g];
+      for (int g = 0; g < G; ++g) P += expf(lv[k][g] - gc[g]);
       if (j < n) {
-        const float a = av[u] + P;
+        const float a = av[k] + P;
         au[j] = a;
-        if ((long)pv[u] <= lim && better(a, pv[u], best_a, best_p)) {
+        if ((long)pv[k] <= lim && better(a, pv[k], best_a, best_p)) {
           best_a = a;
-          best_p = pv[u];
+          best_p = pv[k];
           best_j = j;
         }
       } else {
@@ -394,13 +689,13 @@ __global__ __launch_bounds__(NTE) void decode_evict_kernel(
   __syncthreads();
   if (threadIdx.x == 0) {
     Cand c{INFINITY, 0x7FFFFFFF, -2, 0.f};
-    for (int w = 0; w < NWE; ++w) {
-      if (wc[w].slot != -2 && (c.slot == -2 || better(wc[w].acc, wc[w].pos, c.acc, c.pos))) {
-        c.acc = wc[w].acc;
-        c.pos = wc[w].pos;
-        c.slot = wc[w].slot;
+    for (int v = 0; v < NWF; ++v) {
+      if (wc[v].slot != -2 && (c.slot == -2 || better(wc[v].acc, wc[v].pos, c.acc, c.pos))) {
+        c.acc = wc[v].acc;
+        c.pos = wc[v].pos;
+        c.slot = wc[v].slot;
       }
-      c.accself += wc[w].accself;
+      c.accself += wc[v].accself;
     }
     cand = c;
   }
@@ -443,12 +738,12 @@ __global__ __launch_bounds__(NTE) void decode_evict_kernel(
     __syncthreads();
     const int slot = sh_slot;
     if (slot >= 0) {
-      const int vecs = row_bytes / 16;
-      uint4 *kd = reinterpret_cast<uint4 *>(static_cast<char *>(Kc) + (unit * (long)cap + slot) * row_bytes);
-      uint4 *vd = reinterpret_cast<uint4 *>(static_cast<char *>(Vc) + (unit * (long)cap + slot) * row_bytes);
-      const uint4 *ks = reinterpret_cast<const uint4 *>(static_cast<const char *>(k_new) + unit * (long)row_bytes);
-      const uint4 *vs = reinterpret_cast<const uint4 *>(static_cast<const char *>(v_new) + unit * (long)row_bytes);
-      for (int t = threadIdx.x; t < vecs; t += NTE) {
+      constexpr int VECS = D * (int)sizeof(T) / 16;
+      uint4 *kd = reinterpret_cast<uint4 *>(Kc + (unit * (long)cap + slot) * D);
+      uint4 *vd = reinterpret_cast<uint4 *>(Vc + (unit * (long)cap + slot) * D);
+      const uint4 *ks = reinterpret_cast<const uint4 *>(k_new + unit * (long)D);
+      const uint4 *vs = reinterpret_cast<const uint4 *>(v_new + unit * (long)D);
+      for (int t = threadIdx.x; t < VECS; t += NTF) {
         kd[t] = __ldg(ks + t);
         vd[t] = __ldg(vs + t);
       }
@@ -457,25 +752,33 @@ __global__ __launch_bounds__(NTE) void decode_evict_kernel(
   cluster.sync();  // #2: rank 0 has finished reading the others' shared memory
 }
 
-constexpr size_t stream_smem_bytes(int G, int D) { return (size_t)(NWARP * G * D + G * CH) * sizeof(float); }
-
 template <typename T, int D, int G>
 int run_decode(const void *q, const void *k_new, const void *v_new, void *K_cache, void *V_cache,
                int32_t *pos, float *acc, int32_t *len, int B, int Hq, int Hkv, int cap,
                int recent, int new_pos, float scale, int flags, void *workspace, float *o,
                int32_t *evicted, int *dev_status, cudaStream_t st) {
+  constexpr int NCW = Pick<T, D, G>::NCW;
+  using Geo = typename Pick<T, D, G>::Geo;
   const long units = (long)B * Hkv;
+  if (units * (long)cap >= (1L << 31)) return KV_ERR_UNSUPPORTED;  // TMA row coordinates are int32
   const Ws ws = carve(workspace, units, G, cap);
   const int alg1 = (flags & KV_H2O_ALG1) ? 1 : 0;
-  const size_t smem = stream_smem_bytes(G, D);
-  if (ensure_smem((const void *)decode_stream_kernel<T, D, G>, smem)) return KV_ERR_CUDA;
-  decode_stream_kernel<T, D, G><<<(unsigned)(units * n_chunks(cap)), NT, smem, st>>>(
-      static_cast<const T *>(q), static_cast<const T *>(k_new), static_cast<const T *>(v_new),
-      static_cast<const T *>(K_cache), static_cast<const T *>(V_cache), len, Hq, Hkv, cap, scale,
-      alg1, ws, dev_status);
+  CUtensorMap tmK, tmV;
+  if (!tc::encode_rows_sw128(&tmK, K_cache, units * cap, D, (int)sizeof(T), RB) ||
+      !tc::encode_rows_sw128(&tmV, V_cache, units * cap, D, (int)sizeof(T), RB))
+    return KV_ERR_CUDA;
+  if (ensure_smem((const void *)decode_stream_kernel<T, D, G, NCW>, Geo::SMEM)) return KV_ERR_CUDA;
+  const int NB = blocks_per_unit(cap);
+  const long total = units * NB;
+  const long grid = std::max(1L, std::min((long)device_sm_count(), total / PER_MIN));
+  const long per = (total + grid - 1) / grid;
+  const long ctas = (total + per - 1) / per;
+  decode_stream_kernel<T, D, G, NCW><<<(unsigned)ctas, 32 * (NCW + 1), Geo::SMEM, st>>>(
+      tmK, tmV, static_cast<const T *>(q), static_cast<const T *>(k_new),
+      static_cast<const T *>(v_new), acc, pos, len, Hq, Hkv, cap, scale, alg1, total, per, ws, dev_status);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(units * CE), 1, 1);
-  cfg.blockDim = dim3(NTE, 1, 1);
+  cfg.blockDim = dim3(NTF, 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -485,9 +788,10 @@ int run_decode(const void *q, const void *k_new, const void *v_new, void *K_cach
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, decode_evict_kernel<G, D>, pos, acc, len, Hq, Hkv, cap, recent,
-                         new_pos, alg1, ws, K_cache, V_cache, k_new, v_new, D * (int)sizeof(T), o,
-                         evicted, dev_status) != cudaSuccess) {
+  if (cudaLaunchKernelEx(&cfg, decode_finalize_kernel<T, D, G>, static_cast<const T *>(k_new),
+                         static_cast<const T *>(v_new), static_cast<T *>(K_cache),
+                         static_cast<T *>(V_cache), pos, acc, len, Hq, Hkv, cap, recent, new_pos,
+                         alg1, per, ws, o, evicted, dev_status) != cudaSuccess) {
     cudaGetLastError();
     return KV_ERR_CUDA;
   }
@@ -515,10 +819,9 @@ int dispatch_g(int G, const void *q, const void *k_new, const void *v_new, void 
 }  // namespace
 
 size_t decode_workspace_bytes(long units, int G, int cap, int d) {
-  const size_t lg_bytes = align256((size_t)units * G * (cap + 1) * 4);
-  const size_t mz_bytes = align256((size_t)units * n_chunks(cap) * G * 8);
-  const size_t op_bytes = (size_t)units * n_chunks(cap) * G * d * 4;
-  return lg_bytes + mz_bytes + op_bytes;
+  const int PM = partials_per_unit(cap);
+  return align256((size_t)units * G * (cap + 1) * 4) + align256((size_t)units * PM * G * 8) +
+         (size_t)units * PM * G * d * 4;
 }
 
 int launch_decode_step(const void *q, const void *k_new, const void *v_new, void *K_cache,
