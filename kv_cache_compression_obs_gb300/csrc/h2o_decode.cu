@@ -13,25 +13,27 @@
 //               rows, the blocks of all units are laid end to end and each CTA
 //               takes one contiguous range of them.  A producer warp streams each
 //               block's K rows and V rows into two rings of shared-memory stages
-//               with TMA (128-byte swizzle, L2 evict-first, 8 KB per copy); pairs
-//               of consumer warps take the blocks round-robin, each pair always
-//               the same stages and each warp 32 rows of a block.  K stage: thread
-//               per row, logits l_gj = scale <q_g, k_j> for the G query heads of
-//               the group, with q read from shared memory as broadcasts; the
-//               logits also go to the workspace (kept in L2 for the finalize
-//               kernel, which finds the slots' scores and positions there too),
-//               and the warp's running max and normaliser per head are updated
-//               online.  V stage: one row at a time across the lanes,
-//               o_g += exp(l_gj - m_g) v_j.  When the CTA's part of a unit is done,
-//               its warps' (m, Z, o) are combined into one partial per (unit, CTA).
+//               with bulk copies (exactly the cached rows, L2 evict-first); all
+//               consumer warps share every block, RB / NCW rows each, so that a
+//               stage is held only briefly and most of the rings are in flight.
+//               K stage: 8 lanes per row (q of the lane's eighth of d in
+//               registers, a butterfly across the 8 lanes), logits in log2 units
+//               l_gj = scale log2(e) <q_g, k_j> for the G query heads of the
+//               group, also written to the workspace.  Weights 2^(l_gj - r_g)
+//               against a per-warp reference r_g that moves (rescaling the warp's
+//               sums) only when a block's max passes it by more than kLazyLog2.
+//               V stage: one row at a time across the lanes, o_g += w_gj v_j.
+//               When the CTA's part of a unit is done, its warps' (r, Z, o) are
+//               combined into one partial per (unit, CTA).
 //   finalize -- one cluster of CE CTAs per unit: combines the partials into
-//               o_out; turns the stored logits into probabilities, adds them to
-//               the slots' accumulators and takes each CTA's (acc, pos)-smallest
-//               slot outside the recent window; after a cluster barrier CTA 0
-//               picks the smallest over the cluster (and the new token itself
-//               when recent == 0) and appends the new token or writes it over the
+//               o_out; turns the stored logits into probabilities
+//               P_j = sum_g 2^(l_gj - (M_g + log2 Z_g)), adds them to the slots'
+//               accumulators and takes each CTA's (acc, pos)-smallest slot
+//               outside the recent window; after a cluster barrier CTA 0 picks
+//               the smallest over the cluster (and the new token itself when
+//               recent == 0) and appends the new token or writes it over the
 //               victim.  A CTA's slot loads are issued before the partials are
-//               combined; P_j = sum_g exp(l_gj - (M_g + ln Z_g)).
+//               combined.
 //
 // Workspace: logits [units][G][cap+1] and the per-(unit, CTA) partials (m, Z)
 // [units][PM][G] and o [units][PM][G][D], all float.
@@ -48,8 +50,11 @@ namespace cg = cooperative_groups;
 namespace kvc {
 namespace {
 
-constexpr int WPB = 2;       // consumer warps per block
-constexpr int RB = 32 * WPB; // rows per block: one per lane of each of its warps
+constexpr int RB_MIN = 64;   // rows per block of the widest rows (bounds the partials per unit)
+constexpr int NCW = 8;       // consumer warps: every block is shared by all of them
+constexpr int LPR = 8;       // lanes per row in the K stage
+constexpr int RPI = 32 / LPR;  // rows per K step of a warp
+constexpr float kLazyLog2 = 16.f;  // the weights' reference moves only when passed by more (log2 units)
 constexpr int PER_MIN = 8;   // a CTA takes at least this many blocks (bounds partials per unit)
 constexpr int kSmemBudget = 220 * 1024;
 constexpr int kMaxStages = 16;
@@ -64,46 +69,40 @@ __device__ __forceinline__ bool better(float a, int p, float ba, int bp) {
   return a < ba || (a == ba && p < bp);
 }
 
-// Shared-memory layout of the stream kernel for element type T, head dim D,
-// group size G and NCW consumer warps (NCW / WPB pairs, each pair one block).
-template <typename T, int D, int G, int NCW>
+// Shared-memory layout of the stream kernel for element type T, head dim D and
+// group size G.  Stages hold whole rows, contiguous as in global memory.
+template <typename T, int D, int G>
 struct DGeo {
-  static constexpr int NP = NCW / WPB;             // warp groups, one block each
   static constexpr int ROWB = D * (int)sizeof(T);  // bytes per K or V row
-  static constexpr int NKB = ROWB / 128;           // 128-byte column blocks per row
+  static constexpr int RB = ROWB <= 256 ? 128 : RB_MIN;  // rows per block
+  static constexpr int RPW = RB / NCW;             // rows of a block per consumer warp
+  static constexpr int KIT = RPW / RPI;            // K steps per block
   static constexpr int STAGE = RB * ROWB;          // one block of K (or V) rows
-  static constexpr int PBW = G * D + 2 * G;        // one partial: o[G][D], m[G], Z[G]
+  static constexpr int CPL = ROWB / 16 / LPR;      // 16-byte chunks per lane of a K row
+  static constexpr int HG = G < 4 ? G : 4;         // query heads per K pass
+  static constexpr int NPASS = G / HG;
+  static constexpr int PBW = G * D + 2 * G;        // one warp's partial: o[G][D], m[G], Z[G]
   static constexpr int QS_BYTES = G * D * 4;       // q of the unit, fp32
-  static constexpr int PW_BYTES = NCW * 32 * G * 4;  // per-warp weights exp(l - m) of its 32 rows
-  static constexpr int PB_BYTES = NP * PBW * 4;    // one partial per warp group
-  static constexpr int SC_BYTES = NP * G * 4;      // combine scales
+  static constexpr int PW_BYTES = NCW * RPW * G * 4;  // per-warp weights exp(l - m) of its rows
+  static constexpr int PB_BYTES = NCW * PBW * 4;
+  static constexpr int SC_BYTES = NCW * G * 4;     // combine scales
   static constexpr int MISC_BYTES = 1024;          // barriers, flags
   static constexpr int FIXED = QS_BYTES + PW_BYTES + PB_BYTES + SC_BYTES + MISC_BYTES;
   static constexpr int S_FIT = (kSmemBudget - 1024 - FIXED) / (2 * STAGE);
-  // depth of each ring: a multiple of NP, so that a stage is always consumed by
-  // the same warp group and its phases are waited for in order
-  static constexpr int S = ((S_FIT > kMaxStages ? kMaxStages : S_FIT) / NP) * NP;
+  static constexpr int S = S_FIT > kMaxStages ? kMaxStages : S_FIT;  // depth of each ring
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = S * STAGE;
-  static constexpr int QS_OFF = 2 * S * STAGE;  // 1024-aligned: STAGE is a multiple of 8192
+  static constexpr int QS_OFF = 2 * S * STAGE;
   static constexpr int PW_OFF = QS_OFF + QS_BYTES;
   static constexpr int PB_OFF = PW_OFF + PW_BYTES;
   static constexpr int SC_OFF = PB_OFF + PB_BYTES;
   static constexpr int MISC_OFF = SC_OFF + SC_BYTES;
   static constexpr int SMEM = 1024 /*alignment slack*/ + MISC_OFF + MISC_BYTES;
-  static_assert(NKB >= 1 && ROWB % 128 == 0, "rows are whole 128-byte blocks");
-  static_assert(NCW % WPB == 0, "whole warp groups");
+  static_assert(ROWB % (16 * LPR) == 0 && CPL >= 1, "a K row splits evenly over its lanes");
+  static_assert(G % HG == 0, "whole head passes");
+  static_assert(RPW % RPI == 0 && RPW % 8 == 0, "whole K steps and V batches");
+  static_assert(S >= 2, "ring depth");
   static_assert(4 * kMaxStages * 8 + 64 + 8 * G <= MISC_BYTES, "misc area");
-};
-
-// Consumer warps: the most (of 12, 8, 6, 4) that still give every warp group a
-// stage of each ring.
-template <typename T, int D, int G>
-struct Pick {
-  static constexpr int NCW = DGeo<T, D, G, 12>::S >= 6 ? 12 : DGeo<T, D, G, 8>::S >= 4 ? 8
-                           : DGeo<T, D, G, 6>::S >= 3 ? 6 : 4;
-  using Geo = DGeo<T, D, G, NCW>;
-  static_assert(Geo::S >= Geo::NP && Geo::S % Geo::NP == 0, "ring depth");
 };
 
 struct Cand {
@@ -120,11 +119,12 @@ struct Ws {      // workspace carve-up
 };
 
 inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
-__host__ __device__ inline int blocks_per_unit(int cap) { return (cap + 1 + RB - 1) / RB; }
+__host__ __device__ inline int blocks_per_unit(int cap, int rb) { return (cap + 1 + rb - 1) / rb; }
 // Partials per unit: a unit's NB blocks meet at most ceil(NB / per) + 1 CTA
-// ranges, and every range holds at least PER_MIN blocks unless one CTA runs alone.
+// ranges, and every range holds at least PER_MIN blocks unless one CTA runs
+// alone; blocks are never shorter than RB_MIN rows.
 __host__ __device__ inline int partials_per_unit(int cap) {
-  return (blocks_per_unit(cap) + PER_MIN - 1) / PER_MIN + 1;
+  return (blocks_per_unit(cap, RB_MIN) + PER_MIN - 1) / PER_MIN + 1;
 }
 
 Ws carve(void *ws, long units, int G, int cap) {
@@ -163,13 +163,6 @@ struct RowPiece {
   }
 };
 
-// Byte offset of byte `b` of row `r` inside a stage written by the 2-D TMA with
-// the 128-byte swizzle: column block b / 128 holds RB rows of 128 bytes, and the
-// 16-byte chunk c of row r sits at chunk c ^ (r % 8).
-__device__ __forceinline__ int swz(int r, int b) {
-  return (b >> 7) * (RB * 128) + r * 128 + ((((b >> 4) & 7) ^ (r & 7)) << 4) + (b & 15);
-}
-
 // The CTAs of the stream kernel whose block ranges meet unit u: the first, and how many.
 struct Span {
   int first, count;
@@ -185,20 +178,51 @@ __device__ __forceinline__ void fail(volatile int *abort_flag, int *status) {
   if (status) atomicExch(status, (int)KV_ERR_TIMEOUT);
 }
 
-template <typename T, int D, int G, int NCW>
+// sum over the LPR = 8 lanes of a row of the HG values v[] (lanes 8r .. 8r+7):
+// after the butterfly, lane pp holds the total of value pp / (8 / HG).
+template <int HG>
+__device__ __forceinline__ float row_butterfly(float (&v)[HG], int pp) {
+  if constexpr (HG == 4) {
+    const bool up4 = pp & 4;
+    float a0 = up4 ? v[2] : v[0], a1 = up4 ? v[3] : v[1];
+    const float s0 = up4 ? v[0] : v[2], s1 = up4 ? v[1] : v[3];
+    a0 += __shfl_xor_sync(0xFFFFFFFFu, s0, 4);
+    a1 += __shfl_xor_sync(0xFFFFFFFFu, s1, 4);
+    const bool up2 = pp & 2;
+    float b = up2 ? a1 : a0;
+    b += __shfl_xor_sync(0xFFFFFFFFu, up2 ? a0 : a1, 2);
+    return b + __shfl_xor_sync(0xFFFFFFFFu, b, 1);
+  } else if constexpr (HG == 2) {
+    const bool up4 = pp & 4;
+    float a = up4 ? v[1] : v[0];
+    a += __shfl_xor_sync(0xFFFFFFFFu, up4 ? v[0] : v[1], 4);
+    a += __shfl_xor_sync(0xFFFFFFFFu, a, 2);
+    return a + __shfl_xor_sync(0xFFFFFFFFu, a, 1);
+  } else {
+    float a = v[0];
+    a += __shfl_xor_sync(0xFFFFFFFFu, a, 4);
+    a += __shfl_xor_sync(0xFFFFFFFFu, a, 2);
+    return a + __shfl_xor_sync(0xFFFFFFFFu, a, 1);
+  }
+}
+
+template <typename T, int D, int G>
 __global__ __launch_bounds__(32 * (NCW + 1), 1) void decode_stream_kernel(
-    const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-    const T *__restrict__ q, const T *__restrict__ k_new, const T *__restrict__ v_new,
-    const float *__restrict__ acc, const int32_t *__restrict__ pos, const int32_t *__restrict__ len,
-    int Hq, int Hkv, int cap, float scale, int alg1, long total, long per, Ws ws,
-    int *__restrict__ dev_status) {
-  using Geo = DGeo<T, D, G, NCW>;
+    const T *__restrict__ Kc, const T *__restrict__ Vc, const T *__restrict__ q,
+    const T *__restrict__ k_new, const T *__restrict__ v_new, const int32_t *__restrict__ len, int Hq,
+    int Hkv, int cap, float c_log2, int alg1, long total, long per, Ws ws, int *__restrict__ dev_status) {
+  using Geo = DGeo<T, D, G>;
+  constexpr int RB = Geo::RB;
+  constexpr int RPW = Geo::RPW;
+  constexpr int KIT = Geo::KIT;
   constexpr int S = Geo::S;
-  constexpr int NP = Geo::NP;
   constexpr int NCT = 32 * NCW;
   constexpr int EV = D / 32;  // V elements per lane
   constexpr int PBW = Geo::PBW;
   constexpr int EPL = Vec16<T>::N;
+  constexpr int CPL = Geo::CPL;
+  constexpr int HG = Geo::HG;
+  constexpr int DUP = LPR / HG;  // lanes of a row holding the same head's logit
   using RP = RowPiece<T, EV>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm = reinterpret_cast<unsigned char *>(
@@ -218,7 +242,7 @@ __global__ __launch_bounds__(32 * (NCW + 1), 1) void decode_stream_kernel(
   float *fz = fm + G;                                                                   // [G] normaliser
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int NB = blocks_per_unit(cap);
+  const int NB = blocks_per_unit(cap, RB);
   const int PM = partials_per_unit(cap);
   const long lo = blockIdx.x * per;
   const long hi = min(total, lo + per);
@@ -226,9 +250,9 @@ __global__ __launch_bounds__(32 * (NCW + 1), 1) void decode_stream_kernel(
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       tc::mbar_init(kfull + i, 1);
-      tc::mbar_init(kempty + i, WPB);
+      tc::mbar_init(kempty + i, NCW);
       tc::mbar_init(vfull + i, 1);
-      tc::mbar_init(vempty + i, WPB);
+      tc::mbar_init(vempty + i, NCW);
     }
     *abort_flag = 0;
     tc::mbar_fence_init();
@@ -238,8 +262,6 @@ __global__ __launch_bounds__(32 * (NCW + 1), 1) void decode_stream_kernel(
   if (warp == 0) {
     // ---------------- producer (one lane) ----------------
     if (lane == 0 && lo < hi) {
-      tc::tma_prefetch_desc(&tmK);
-      tc::tma_prefetch_desc(&tmV);
       const uint64_t pol = tc::make_policy_evict_first();
       long cur_u = -1;
       int n = 0;
@@ -253,18 +275,17 @@ __global__ __launch_bounds__(32 * (NCW + 1), 1) void decode_stream_kernel(
           if (n < 0 || n > cap) n = 0;  // reported by the finalize kernel
         }
         const int rows = max(0, min(RB, n - jb * RB));  // cached rows in this block
+        const uint32_t bytes = static_cast<uint32_t>(rows * Geo::ROWB);
+        const long row0 = u * (long)cap + (long)jb * RB;
         const int si = static_cast<int>(i % S);
         const uint32_t ph = static_cast<uint32_t>((i / S) & 1);
-        const int y = static_cast<int>(u * cap + (long)jb * RB);
         if (!tc::mbar_wait(kempty + si, ph ^ 1, kWaitBudget, abort_flag)) {
           fail(abort_flag, dev_status);
           break;
         }
         if (rows > 0) {
-          tc::mbar_arrive_expect_tx(kfull + si, Geo::STAGE);
-          for (int kb = 0; kb < Geo::NKB; ++kb)
-            tc::tma_load_2d_hint(sK + si * Geo::STAGE + kb * RB * 128, &tmK, kb * (128 / (int)sizeof(T)), y,
-                                 kfull + si, pol);
+          tc::mbar_arrive_expect_tx(kfull + si, bytes);
+          tc::bulk_load_hint(sK + si * Geo::STAGE, Kc + row0 * D, bytes, kfull + si, pol);
         } else {
           tc::mbar_arrive(kfull + si);
         }
@@ -274,10 +295,8 @@ __global__ __launch_bounds__(32 * (NCW + 1), 1) void decode_stream_kernel(
           break;
         }
         if (rows > 0) {
-          tc::mbar_arrive_expect_tx(vfull + si, Geo::STAGE);
-          for (int kb = 0; kb < Geo::NKB; ++kb)
-            tc::tma_load_2d_hint(sV + si * Geo::STAGE + kb * RB * 128, &tmV, kb * (128 / (int)sizeof(T)), y,
-                                 vfull + si, pol);
+          tc::mbar_arrive_expect_tx(vfull + si, bytes);
+          tc::bulk_load_hint(sV + si * Geo::STAGE, Vc + row0 * D, bytes, vfull + si, pol);
         } else {
           tc::mbar_arrive(vfull + si);
         }
@@ -295,18 +314,15 @@ __global__ __launch_bounds__(32 * (NCW + 1), 1) void decode_stream_kernel(
     return;
   }
 
-  // ---------------- consumers: warp group gp takes blocks gp, gp + NP, ... ----------------
-  const int w = warp - 1;     // 0 .. NCW-1
-  const int gp = w % NP;      // warp group
-  const int hw = w / NP;      // this warp's 32 rows of a block: [32 hw, 32 hw + 32)
+  // ---------------- consumers: warp w takes rows [RPW w, RPW w + RPW) of every block ----------------
+  const int w = warp - 1;  // 0 .. NCW-1
   const int ct = threadIdx.x - 32;
-  float *pww = pw + w * 32 * G;  // this warp's weights [32][G]
-  const uint64_t pol_keep = tc::make_policy_evict_last();
-  // this lane's byte offsets of its V piece in rows 0..7 of a stage (the swizzle repeats every 8 rows)
-  const int vb = lane * EV * (int)sizeof(T);
-  int voff[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) voff[k] = swz(k, vb);
+  const int rs = lane / LPR;  // row of a K step
+  const int pp = lane % LPR;  // this lane's part of that row
+  const int hd = pp / DUP;    // head (within a pass) whose logit the lane ends with
+  const bool writer = (pp % DUP) == 0;
+  const int wr0 = RPW * w;    // this warp's first row of a block
+  float *pww = pw + w * RPW * G;  // this warp's weights [RPW][G]
   bool ok = true;
   long i = 0;
   // A warp that gives up keeps walking the same items (without touching the
@@ -325,37 +341,45 @@ __global__ __launch_bounds__(32 * (NCW + 1), 1) void decode_stream_kernel(
     for (int t = ct; t < G * D; t += NCT) qs[t] = to_f32(qg[t]);
     tc::named_bar_sync(BAR_CONS, NCT);
 
-    float m[G], zl[G];
+    // q in registers: for every head of a pass, the lane's CPL chunks (chunk pp + 8 j)
+    float qr[Geo::NPASS][HG][CPL * EPL];
+#pragma unroll
+    for (int pa = 0; pa < Geo::NPASS; ++pa)
+#pragma unroll
+      for (int hh = 0; hh < HG; ++hh)
+#pragma unroll
+        for (int j = 0; j < CPL; ++j)
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) qr[pa][hh][j * EPL + e] = qs[(pa * HG + hh) * D + (pp + LPR * j) * EPL + e];
+
+    // per pass: the reference (lazy running max, log2 units) of the lane's head,
+    // and its normaliser (writer lanes)
+    float mh[Geo::NPASS], zl[Geo::NPASS];
     float2 o[G][EV / 2];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      m[g] = -INFINITY;
-      zl[g] = 0.f;
+    for (int g = 0; g < G; ++g)
 #pragma unroll
       for (int e = 0; e < EV / 2; ++e) o[g][e] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int pa = 0; pa < Geo::NPASS; ++pa) {
+      mh[pa] = -INFINITY;
+      zl[pa] = 0.f;
     }
     float *lgu = ws.lgw + u * (long)G * (cap + 1);
     const T *vn = v_new + u * (long)D;
 
     for (; gb < item_end; ++gb, ++i) {
-      if ((int)(i % NP) != gp || !ok) continue;
+      if (!ok) continue;
       const int r0 = static_cast<int>(gb % NB) * RB;
       const int rows = max(0, min(RB, n - r0));                // cached rows of the block
       const bool has_new = nc > n && n >= r0 && n < r0 + RB;  // the new token is block row `rows`
-      const bool my_new = has_new && (rows >> 5) == hw;        // ... and one of this warp's
-      const int wr0 = 32 * hw;                                 // this warp's first block row
-      const int wrows = max(0, min(32, rows - wr0));           // its cached rows
+      const bool my_new = has_new && rows >= wr0 && rows < wr0 + RPW;  // ... and one of this warp's
+      const int wrows = max(0, min(RPW, rows - wr0));          // this warp's cached rows
       const int wnv = wrows + (my_new ? 1 : 0);
       const int si = static_cast<int>(i % S);
       const uint32_t ph = static_cast<uint32_t>((i / S) & 1);
 
-      // the scores and positions of these slots are read again by the finalize kernel
-      if (lane < 2 && wrows > 0) {  // first and last of this warp's slots: every line they span
-        const long e = u * (long)cap + r0 + wr0 + (lane ? wrows - 1 : 0);
-        tc::prefetch_l2_last(acc + e);
-        tc::prefetch_l2_last(pos + e);
-      }
-      // the new token's logits: the lanes across d, then a warp sum
+      // the new token's logits (every head): the lanes across d, then a warp sum
       float lnew[G];
       if (my_new) {
         const typename RP::Word word =
@@ -369,7 +393,7 @@ __global__ __launch_bounds__(32 * (NCW + 1), 1) void decode_stream_kernel(
           for (int e = 0; e < EV; ++e) s = fmaf(kv[e], qs[g * D + lane * EV + e], s);
 #pragma unroll
           for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
-          lnew[g] = scale * s;
+          lnew[g] = c_log2 * s;
         }
       }
 
@@ -378,62 +402,85 @@ __global__ __launch_bounds__(32 * (NCW + 1), 1) void decode_stream_kernel(
         ok = false;
         continue;
       }
-      // K stage: lane owns block row wr0 + lane
-      float l[G];
+      // K stage: LPR lanes per row, RPI rows per step; lane ends with one head's logit
+      float l[Geo::NPASS][KIT];
       {
-        float2 part[G];
+        const unsigned char *kst = sK + si * Geo::STAGE + (wr0 + rs) * Geo::ROWB + pp * 16;
 #pragma unroll
-        for (int g = 0; g < G; ++g) part[g] = make_float2(0.f, 0.f);
-        if (lane < wrows) {
-          const unsigned char *kst = sK + si * Geo::STAGE + (wr0 + lane) * 128;
+        for (int it = 0; it < KIT; ++it) {
+          float f[CPL][EPL];
 #pragma unroll
-          for (int c = 0; c < Geo::ROWB / 16; ++c) {
-            float f[EPL];
-            Vec16<T>::unpack(*reinterpret_cast<const uint4 *>(
-                                 kst + (c >> 3) * (RB * 128) + (((c & 7) ^ (lane & 7)) << 4)),
-                             f);
+          for (int j = 0; j < CPL; ++j)
+            Vec16<T>::unpack(*reinterpret_cast<const uint4 *>(kst + RPI * it * Geo::ROWB + LPR * j * 16), f[j]);
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-              const float4 *q4 = reinterpret_cast<const float4 *>(qs + g * D + c * EPL);
+          for (int pa = 0; pa < Geo::NPASS; ++pa) {
+            float v[HG];
 #pragma unroll
-              for (int e4 = 0; e4 < EPL / 4; ++e4) {
-                const float4 qq = q4[e4];
-                part[g] = __ffma2_rn(make_float2(f[4 * e4 + 0], f[4 * e4 + 1]), make_float2(qq.x, qq.y), part[g]);
-                part[g] = __ffma2_rn(make_float2(f[4 * e4 + 2], f[4 * e4 + 3]), make_float2(qq.z, qq.w), part[g]);
-              }
+            for (int hh = 0; hh < HG; ++hh) {
+              float2 part = make_float2(0.f, 0.f);
+#pragma unroll
+              for (int j = 0; j < CPL; ++j)
+#pragma unroll
+                for (int e = 0; e < EPL; e += 2)
+                  part = __ffma2_rn(make_float2(f[j][e], f[j][e + 1]),
+                                    make_float2(qr[pa][hh][j * EPL + e], qr[pa][hh][j * EPL + e + 1]), part);
+              v[hh] = part.x + part.y;
             }
+            l[pa][it] = c_log2 * row_butterfly<HG>(v, pp);
           }
         }
-#pragma unroll
-        for (int g = 0; g < G; ++g) l[g] = scale * (part[g].x + part[g].y);
       }
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(kempty + si);
-      if (my_new && lane == (rows & 31)) {
+      if (my_new) {
+        const int rn = rows - wr0;  // the new token's row among this warp's
 #pragma unroll
-        for (int g = 0; g < G; ++g) l[g] = lnew[g];
+        for (int it = 0; it < KIT; ++it)
+          if (RPI * it + rs == rn)
+#pragma unroll
+            for (int pa = 0; pa < Geo::NPASS; ++pa)
+#pragma unroll
+              for (int hh = 0; hh < HG; ++hh)
+                if (hh == hd) l[pa][it] = lnew[pa * HG + hh];
       }
-      if (lane < wnv) {
+      // logits to the workspace; per head, weights 2^(l - reference) with a lazy reference
 #pragma unroll
-        for (int g = 0; g < G; ++g) tc::st_f32_hint(lgu + (long)g * (cap + 1) + r0 + wr0 + lane, l[g], pol_keep);
-      }
-      if (wnv > 0) {
+      for (int pa = 0; pa < Geo::NPASS; ++pa) {
+        float bm = -INFINITY;
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float bm = lane < wnv ? l[g] : -INFINITY;
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, off));
-          const float mn = fmaxf(m[g], bm);
-          if (mn != m[g]) {
-            const float s = expf(m[g] - mn);  // 0 while nothing has been seen
-            zl[g] *= s;
-#pragma unroll
-            for (int e = 0; e < EV / 2; ++e) o[g][e] = __fmul2_rn(o[g][e], make_float2(s, s));
-            m[g] = mn;
+        for (int it = 0; it < KIT; ++it) {
+          const int rr = RPI * it + rs;  // row among this warp's
+          if (rr < wnv) {
+            bm = fmaxf(bm, l[pa][it]);
+            if (writer) lgu[(long)(pa * HG + hd) * (cap + 1) + r0 + wr0 + rr] = l[pa][it];
           }
-          const float p = lane < wnv ? expf(l[g] - mn) : 0.f;
-          zl[g] += p;
-          pww[lane * G + g] = p;
+        }
+#pragma unroll
+        for (int off = LPR; off < 32; off <<= 1) bm = fmaxf(bm, __shfl_xor_sync(0xFFFFFFFFu, bm, off));
+        // a new reference only when the block's max passes the old one by more than
+        // kLazyLog2 (or on the first rows): weights stay below 2^kLazyLog2
+        float s = 1.f;
+        if (bm > mh[pa] + kLazyLog2) {
+          s = tc::ex2(mh[pa] - bm);  // 0 while nothing has been seen
+          zl[pa] *= s;
+          mh[pa] = bm;
+        }
+#pragma unroll
+        for (int hh = 0; hh < HG; ++hh) {
+          const float sh = __shfl_sync(0xFFFFFFFFu, s, hh * DUP);  // lane hh * DUP holds head hh
+          if (sh != 1.f) {
+#pragma unroll
+            for (int e = 0; e < EV / 2; ++e) o[pa * HG + hh][e] = __fmul2_rn(o[pa * HG + hh][e], make_float2(sh, sh));
+          }
+        }
+#pragma unroll
+        for (int it = 0; it < KIT; ++it) {
+          const int rr = RPI * it + rs;
+          const float p = rr < wnv ? tc::ex2(l[pa][it] - mh[pa]) : 0.f;
+          if (writer) {
+            zl[pa] += p;
+            pww[rr * G + pa * HG + hd] = p;
+          }
         }
       }
       __syncwarp();
@@ -445,7 +492,7 @@ __global__ __launch_bounds__(32 * (NCW + 1), 1) void decode_stream_kernel(
         continue;
       }
       {
-        const unsigned char *vst = sV + si * Geo::STAGE + wr0 * 128;  // wr0 is a multiple of 8
+        const unsigned char *vst = sV + si * Geo::STAGE + wr0 * Geo::ROWB + lane * EV * (int)sizeof(T);
         auto accum = [&](const typename RP::Word &word, int r) {
           float vv[EV];
           RP::unpack(word, vv);
@@ -469,81 +516,58 @@ __global__ __launch_bounds__(32 * (NCW + 1), 1) void decode_stream_kernel(
             for (int e = 0; e < EV / 2; ++e)
               o[g][e] = __ffma2_rn(make_float2(pg[g], pg[g]), make_float2(vv[2 * e], vv[2 * e + 1]), o[g][e]);
         };
-        const int full8 = wrows & ~7;
-        for (int r8 = 0; r8 < full8; r8 += 8) {
-          typename RP::Word word[8];
+        if (wrows == RPW) {
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            word[k] = *reinterpret_cast<const typename RP::Word *>(vst + r8 * 128 + voff[k]);
+          for (int r8 = 0; r8 < RPW; r8 += 8) {
+            typename RP::Word word[8];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) accum(word[k], r8 + k);
+            for (int k = 0; k < 8; ++k)
+              word[k] = *reinterpret_cast<const typename RP::Word *>(vst + (r8 + k) * Geo::ROWB);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) accum(word[k], r8 + k);
+          }
+        } else {
+          for (int r = 0; r < wrows; ++r) accum(*reinterpret_cast<const typename RP::Word *>(vst + r * Geo::ROWB), r);
         }
-        for (int r = full8; r < wrows; ++r)
-          accum(*reinterpret_cast<const typename RP::Word *>(vst + swz(r, vb)), r);
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(vempty + si);
         if (my_new) accum(__ldg(reinterpret_cast<const typename RP::Word *>(vn + lane * EV)), wrows);
       }
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(vempty + si);
+      __syncwarp();  // pww is rewritten by the next block
     }
 
     // ---- the unit's range in this CTA is done: combine the warps into one partial ----
-    // (1) every warp reduces its normaliser; the second warp of each group deposits
-    float zw[G];
+    float *pbw = pb + w * PBW;
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float z = zl[g];
+    for (int pa = 0; pa < Geo::NPASS; ++pa) {
+      float z = writer ? zl[pa] : 0.f;
+      // lanes with the same head: the same pp / DUP in every row group
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, off);
-      zw[g] = z;
-    }
-    float *pbg = pb + gp * PBW;
-    auto deposit = [&]() {
+      for (int off = LPR; off < 32; off <<= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, off);
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-#pragma unroll
-        for (int e = 0; e < EV / 2; ++e) {
-          pbg[g * D + lane * EV + 2 * e] = o[g][e].x;
-          pbg[g * D + lane * EV + 2 * e + 1] = o[g][e].y;
-        }
-        if (lane == 0) {
-          pbg[G * D + g] = m[g];
-          pbg[G * D + G + g] = zw[g];
-        }
-      }
-    };
-    static_assert(WPB == 2, "the merge below pairs two warps");
-    if (hw == 1) deposit();
-    tc::named_bar_sync(BAR_CONS, NCT);
-    // (2) the first warp of each group merges its partner's partial into its own
-    if (hw == 0) {
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float m1 = pbg[G * D + g];
-        const float Mx = fmaxf(m[g], m1);
-        const float s0 = m[g] == -INFINITY ? 0.f : expf(m[g] - Mx);
-        const float s1 = m1 == -INFINITY ? 0.f : expf(m1 - Mx);
-#pragma unroll
-        for (int e = 0; e < EV / 2; ++e) {
-          const float2 o1 = make_float2(pbg[g * D + lane * EV + 2 * e], pbg[g * D + lane * EV + 2 * e + 1]);
-          o[g][e] = __ffma2_rn(o[g][e], make_float2(s0, s0), __fmul2_rn(o1, make_float2(s1, s1)));
-        }
-        zw[g] = zw[g] * s0 + pbg[G * D + G + g] * s1;
-        m[g] = Mx;
+      for (int off = 1; off < DUP; off <<= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, off);
+      if (lane < LPR && writer) {
+        pbw[G * D + G + pa * HG + hd] = z;
+        pbw[G * D + pa * HG + hd] = mh[pa];
       }
     }
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int e = 0; e < EV / 2; ++e) {
+        pbw[g * D + lane * EV + 2 * e] = o[g][e].x;
+        pbw[g * D + lane * EV + 2 * e + 1] = o[g][e].y;
+      }
     tc::named_bar_sync(BAR_CONS, NCT);
-    if (hw == 0) deposit();
-    tc::named_bar_sync(BAR_CONS, NCT);
-    // (3) the groups' partials -> one partial of this CTA
     if (ct < G) {
       float M = -INFINITY;
-      for (int v = 0; v < NP; ++v) M = fmaxf(M, pb[v * PBW + G * D + ct]);
+      for (int v = 0; v < NCW; ++v) M = fmaxf(M, pb[v * PBW + G * D + ct]);
       float Z = 0.f;
-      for (int v = 0; v < NP; ++v) {
+      for (int v = 0; v < NCW; ++v) {
         const float mv = pb[v * PBW + G * D + ct];
-        const float s = mv == -INFINITY ? 0.f : expf(mv - M);
-        sc[v * G + ct] = s;
-        Z += pb[v * PBW + G * D + G + ct] * s;
+        const float sv = mv == -INFINITY ? 0.f : tc::ex2(mv - M);
+        sc[v * G + ct] = sv;
+        Z += pb[v * PBW + G * D + G + ct] * sv;
       }
       fm[ct] = M;
       fz[ct] = Z;
@@ -555,7 +579,7 @@ __global__ __launch_bounds__(32 * (NCW + 1), 1) void decode_stream_kernel(
     for (int t = ct; t < G * D; t += NCT) {
       const int g = t / D;
       float s = 0.f;
-      for (int v = 0; v < NP; ++v) s += pb[v * PBW + t] * sc[v * G + g];
+      for (int v = 0; v < NCW; ++v) s += pb[v * PBW + t] * sc[v * G + g];
       pou[t] = s;
     }
     if (ct < G) ws.pmz[slot * G + ct] = make_float2(fm[ct], fz[ct]);
@@ -585,7 +609,7 @@ __global__ __launch_bounds__(NTF) void decode_finalize_kernel(
     if (rank == 0 && threadIdx.x == 0 && dev_status) atomicExch(dev_status, (int)KV_ERR_INVALID_ARG);
     return;
   }
-  const int NB = blocks_per_unit(cap);
+  const int NB = blocks_per_unit(cap, DGeo<T, D, G>::RB);
   const int PM = partials_per_unit(cap);
   const Span sp = unit_span(unit, NB, per);
   const int nc = n + (alg1 ? 0 : 1);
@@ -625,12 +649,12 @@ __global__ __launch_bounds__(NTF) void decode_finalize_kernel(
       const float2 v = pmz[p * G + g];
       if (v.x == -INFINITY) continue;
       const float Mn = fmaxf(M, v.x);
-      Z = Z * expf(M - Mn) + v.y * expf(v.x - Mn);
+      Z = Z * tc::ex2(M - Mn) + v.y * tc::ex2(v.x - Mn);
       M = Mn;
     }
     gm[g] = M;
     gz[g] = Z;
-    gc[g] = M + logf(Z);  // exp(l - M) / Z = exp(l - gc)
+    gc[g] = M + log2f(Z);  // 2^(l - M) / Z = 2^(l - gc)
   }
   __syncthreads();
   // this CTA's part of the output: o_g = sum_p o_p exp(m_p - M) / Z
@@ -641,7 +665,7 @@ __global__ __launch_bounds__(NTF) void decode_finalize_kernel(
 #pragma unroll 4
     for (int p = 0; p < sp.count; ++p) {
       const float mp = pmz[p * G + g].x;  // o_p = 0 where m_p = -inf
-      s += po[(long)p * GD + t] * (mp == -INFINITY ? 0.f : expf(mp - gm[g]));
+      s += po[(long)p * GD + t] * (mp == -INFINITY ? 0.f : tc::ex2(mp - gm[g]));
     }
     ou[t] = nc > 0 ? s / gz[g] : 0.f;
   }
@@ -658,7 +682,7 @@ __global__ __launch_bounds__(NTF) void decode_finalize_kernel(
       if (j >= j1) continue;
       float P = 0.f;
 #pragma unroll
-      for (int g = 0; g < G; ++g) P += expf(lv[k][g] - gc[g]);
+      for (int g = 0; g < G; ++g) P += tc::ex2(lv[k][g] - gc[g]);
       if (j < n) {
         const float a = av[k] + P;
         au[j] = a;
@@ -757,25 +781,20 @@ int run_decode(const void *q, const void *k_new, const void *v_new, void *K_cach
                int32_t *pos, float *acc, int32_t *len, int B, int Hq, int Hkv, int cap,
                int recent, int new_pos, float scale, int flags, void *workspace, float *o,
                int32_t *evicted, int *dev_status, cudaStream_t st) {
-  constexpr int NCW = Pick<T, D, G>::NCW;
-  using Geo = typename Pick<T, D, G>::Geo;
+  using Geo = DGeo<T, D, G>;
   const long units = (long)B * Hkv;
-  if (units * (long)cap >= (1L << 31)) return KV_ERR_UNSUPPORTED;  // TMA row coordinates are int32
   const Ws ws = carve(workspace, units, G, cap);
   const int alg1 = (flags & KV_H2O_ALG1) ? 1 : 0;
-  CUtensorMap tmK, tmV;
-  if (!tc::encode_rows_sw128(&tmK, K_cache, units * cap, D, (int)sizeof(T), RB) ||
-      !tc::encode_rows_sw128(&tmV, V_cache, units * cap, D, (int)sizeof(T), RB))
-    return KV_ERR_CUDA;
-  if (ensure_smem((const void *)decode_stream_kernel<T, D, G, NCW>, Geo::SMEM)) return KV_ERR_CUDA;
-  const int NB = blocks_per_unit(cap);
+  if (ensure_smem((const void *)decode_stream_kernel<T, D, G>, Geo::SMEM)) return KV_ERR_CUDA;
+  const int NB = blocks_per_unit(cap, Geo::RB);
   const long total = units * NB;
   const long grid = std::max(1L, std::min((long)device_sm_count(), total / PER_MIN));
   const long per = (total + grid - 1) / grid;
   const long ctas = (total + per - 1) / per;
-  decode_stream_kernel<T, D, G, NCW><<<(unsigned)ctas, 32 * (NCW + 1), Geo::SMEM, st>>>(
-      tmK, tmV, static_cast<const T *>(q), static_cast<const T *>(k_new),
-      static_cast<const T *>(v_new), acc, pos, len, Hq, Hkv, cap, scale, alg1, total, per, ws, dev_status);
+  decode_stream_kernel<T, D, G><<<(unsigned)ctas, 32 * (NCW + 1), Geo::SMEM, st>>>(
+      static_cast<const T *>(K_cache), static_cast<const T *>(V_cache), static_cast<const T *>(q),
+      static_cast<const T *>(k_new), static_cast<const T *>(v_new), len, Hq, Hkv, cap,
+      scale * 1.4426950408889634f /* log2 e */, alg1, total, per, ws, dev_status);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(units * CE), 1, 1);
   cfg.blockDim = dim3(NTF, 1, 1);
