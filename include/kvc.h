@@ -232,6 +232,11 @@ KVC_API const char *kv_status_string(int status);
 /* Library version (major * 10000 + minor * 100 + patch). */
 KVC_API int kv_version(void);
 
+/* Text of the CUDA error behind the calling thread's last KV_ERR_CUDA (the
+ * failing step, the CUDA error string and name), "" before any; the pointer
+ * stays valid in that thread until its next failing call.  Diagnostic only. */
+KVC_API const char *kv_last_error_detail(void);
+
 /* Number of kernels this library has launched in this process (all devices,
  * all threads); a diagnostic for counting launches around a timed region. */
 KVC_API unsigned long long kv_launch_count(void);

@@ -49,11 +49,18 @@ _lib.kv_workspace_size.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I]
 _lib.kv_status_string.restype = ctypes.c_char_p
 _lib.kv_status_string.argtypes = [_I]
 _lib.kv_version.restype = _I
+_lib.kv_last_error_detail.restype = ctypes.c_char_p
+_lib.kv_last_error_detail.argtypes = []
 
 
 class KvcError(RuntimeError):
     def __init__(self, call: str, status: int):
-        super().__init__(f"{call}: {_lib.kv_status_string(status).decode()} (status {status})")
+        msg = f"{call}: {_lib.kv_status_string(status).decode()} (status {status})"
+        if status == KV_ERR_CUDA:
+            detail = _lib.kv_last_error_detail().decode()
+            if detail:
+                msg += f": {detail}"
+        super().__init__(msg)
         self.status = status
 
 

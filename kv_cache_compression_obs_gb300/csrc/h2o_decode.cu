@@ -785,7 +785,8 @@ int run_decode(const void *q, const void *k_new, const void *v_new, void *K_cach
   const long units = (long)B * Hkv;
   const Ws ws = carve(workspace, units, G, cap);
   const int alg1 = (flags & KV_H2O_ALG1) ? 1 : 0;
-  if (ensure_smem((const void *)decode_stream_kernel<T, D, G>, Geo::SMEM)) return KV_ERR_CUDA;
+  if (ensure_smem((const void *)decode_stream_kernel<T, D, G>, Geo::SMEM))
+    return cuda_failure(cudaErrorInvalidValue, "decode stream kernel: shared memory limit");
   const int NB = blocks_per_unit(cap, Geo::RB);
   const long total = units * NB;
   const long grid = std::max(1L, std::min((long)device_sm_count(), total / PER_MIN));
@@ -807,12 +808,17 @@ int run_decode(const void *q, const void *k_new, const void *v_new, void *K_cach
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, decode_finalize_kernel<T, D, G>, static_cast<const T *>(k_new),
-                         static_cast<const T *>(v_new), static_cast<T *>(K_cache),
-                         static_cast<T *>(V_cache), pos, acc, len, Hq, Hkv, cap, recent, new_pos,
-                         alg1, per, ws, o, evicted, dev_status) != cudaSuccess) {
+  {
+    const int rc = launch_status(0);  // the stream kernel's launch
+    if (rc != KV_OK) return rc;
+  }
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_finalize_kernel<T, D, G>, static_cast<const T *>(k_new),
+                                           static_cast<const T *>(v_new), static_cast<T *>(K_cache),
+                                           static_cast<T *>(V_cache), pos, acc, len, Hq, Hkv, cap, recent,
+                                           new_pos, alg1, per, ws, o, evicted, dev_status);
+  if (e != cudaSuccess) {
     cudaGetLastError();
-    return KV_ERR_CUDA;
+    return cuda_failure(e, "decode finalize kernel launch");
   }
   return launch_status(2);
 }

@@ -3,6 +3,7 @@
 // enqueued, so a rejected call touches neither the GPU nor any output.
 #include <atomic>
 #include <climits>
+#include <cstdio>
 #include <mutex>
 #include <unordered_map>
 
@@ -12,6 +13,15 @@ namespace kvc {
 
 static std::atomic<unsigned long long> g_launches{0};
 void count_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+
+namespace {
+thread_local char g_detail[256] = "";
+}
+int cuda_failure(cudaError_t e, const char *where) {
+  snprintf(g_detail, sizeof g_detail, "%s: %s (%s)", where, cudaGetErrorString(e), cudaGetErrorName(e));
+  return KV_ERR_CUDA;
+}
+const char *last_detail() { return g_detail; }
 
 int device_sm_count() {
   int dev = 0, n = 0;
@@ -60,6 +70,8 @@ extern "C" {
 int kv_version(void) { return 100; }
 
 unsigned long long kv_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char *kv_last_error_detail(void) { return kvc::last_detail(); }
 
 const char *kv_status_string(int status) {
   switch (status) {

@@ -19,10 +19,13 @@ int ensure_smem(const void *func, size_t bytes);  // opt a kernel into > 48 KB o
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 void count_launches(int n);  // diagnostic counter behind kv_launch_count()
+// Remember the CUDA error behind a KV_ERR_CUDA (kv_last_error_detail); returns KV_ERR_CUDA.
+int cuda_failure(cudaError_t e, const char *where);
+const char *last_detail();
 
 inline int launch_status(int launches = 1) {
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return KV_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_failure(e, "kernel launch");
   count_launches(launches);
   return KV_OK;
 }

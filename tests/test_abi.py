@@ -25,6 +25,7 @@ def lib():
     lib.kv_workspace_size.restype = Z
     lib.kv_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
     lib.kv_status_string.restype = ctypes.c_char_p
+    lib.kv_last_error_detail.restype = ctypes.c_char_p
     return lib
 
 
@@ -46,6 +47,10 @@ def test_status_strings_and_version(lib):
     assert b"invalid" in lib.kv_status_string(-1)
     assert lib.kv_status_string(-4) == b"device-side wait timed out"
     assert lib.kv_version() >= 100
+
+
+def test_error_detail_is_empty_before_any_cuda_failure(lib):
+    assert lib.kv_last_error_detail() == b""
 
 
 def test_workspace_size(lib):
