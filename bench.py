@@ -77,14 +77,29 @@ def algorithmic_bytes(wl):
             "kv_compact": compact, "h2o_decode_step": decode_step}
 
 
+def score_flops(wl):
+    """Dense multiply-adds of the observation-window contraction, both passes
+    (statistics, then column mass): 2 x 2 x (G W) x T x d per (batch row, KV head)."""
+    return 2 * 2 * (wl.Hq // wl.Hkv) * wl.W * wl.T * wl.d * wl.units
+
+
+# DRAM bytes per decode step (both launches) from `ncu --metrics
+# dram__bytes_read.sum,dram__bytes_write.sum` of the current kernels, per
+# workload; see profiles/decode_long-context.md (captured on 8 of the 32 layers
+# and scaled by 4: the step's traffic is proportional to the units).  None where
+# not captured.
+DECODE_TRAFFIC = {"long-context": 4 * (214883840 + 4654080 + 10577920)}
+
+
 def measured_peaks():
+    """(HBM GB/s, bf16 dense TFLOP/s burst, kind): MEASURED_PEAKS.json, else the fallback."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), "measured"
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
     except Exception:
-        return 6800.0, "fallback"
+        return 6800.0, 1900.0, "fallback"
 
 
 class ClockSampler:
@@ -349,11 +364,13 @@ def run_ours(args, wl, rank, world):
 
     tokens = wl.rows * wl.T
     value = world * tokens / (ms_max / 1e3)
-    peak, peak_kind = measured_peaks()
+    peak, peak_tf, peak_kind = measured_peaks()
     alg = algorithmic_bytes(wl)
     per_launch = {k: alg[k] for k in alg}
     dom = max(phases, key=lambda n: phases[n] * (wl.n_decode if n == "h2o_decode_step" else 1))
     achieved = per_launch[dom] / (phases[dom] / 1e3) / 1e9
+    traffic = DECODE_TRAFFIC.get(wl.name) if dom == "h2o_decode_step" else None
+    score_tf = score_flops(wl) / (phases["kv_score_obs"] / 1e3) / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
@@ -369,7 +386,14 @@ def run_ours(args, wl, rank, world):
         "gpu_launches": launches,
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                     "algorithmic_bytes": per_launch[dom], "traffic": None},
+                     "algorithmic_bytes": per_launch[dom], "traffic": traffic,
+                     "note": ("one decode step = the stream and finalize launches, timed together"
+                              if dom == "h2o_decode_step" else None)},
+        "roofline_score": {"kernel": "kv_score_obs", "bound": "tensor", "achieved": score_tf,
+                           "peak": peak_tf, "peak_kind": peak_kind + " bf16 dense (burst)",
+                           "unit": "TFLOP/s", "frac": score_tf / peak_tf,
+                           "algorithmic_flops": score_flops(wl),
+                           "hbm_gbs": per_launch["kv_score_obs"] / (phases["kv_score_obs"] / 1e3) / 1e9},
         "clocks": clk.summary(),
     }
     if not args.no_e2e:
