@@ -366,8 +366,32 @@ __global__ void __launch_bounds__(NT, 1)
   }
 }
 
+// acc2 += 2^(x_r c_log2 + m_r) over the 16 rows r of one TMEM chunk (m_r =
+// -(M_r + log2 Z_r)); MASKED: only the rows whose position is at least the key's j.
+template <bool MASKED>
+__device__ __forceinline__ float2 colsum_chunk(const uint32_t (&r)[16], const float4 *m4, const int4 *p4, int j,
+                                               float2 c2, float2 acc2) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float4 mm = m4[u];
+    const float2 xa = __ffma2_rn(make_float2(__uint_as_float(r[4 * u]), __uint_as_float(r[4 * u + 1])), c2,
+                                 make_float2(mm.x, mm.y));
+    const float2 xb = __ffma2_rn(make_float2(__uint_as_float(r[4 * u + 2]), __uint_as_float(r[4 * u + 3])), c2,
+                                 make_float2(mm.z, mm.w));
+    float2 ea = make_float2(tc::ex2(xa.x), tc::ex2(xa.y));
+    float2 eb = make_float2(tc::ex2(xb.x), tc::ex2(xb.y));
+    if constexpr (MASKED) {
+      const int4 pp = p4[u];
+      ea = make_float2(j <= pp.x ? ea.x : 0.f, j <= pp.y ? ea.y : 0.f);
+      eb = make_float2(j <= pp.z ? eb.x : 0.f, j <= pp.w ? eb.y : 0.f);
+    }
+    acc2 = __fadd2_rn(acc2, __fadd2_rn(ea, eb));
+  }
+  return acc2;
+}
+
 // ---------------------------------------------------------------------------
-// Pass 2: column mass s_j = sum_r 2^(x_rj - M_r) / Z_r over a key chunk.
+// Pass 2: column mass s_j = sum_r 2^(x_rj - M_r - log2 Z_r) over a key chunk.
 // ---------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(NT, 1)
@@ -424,13 +448,13 @@ __global__ void __launch_bounds__(NT, 1)
       tc::named_bar_sync(1, EPI_THREADS);   // the previous item's readers are done
       for (int r = et; r < QROWS; r += EPI_THREADS) {
         if (r < gw) {
-          const float2 f = fin[w.unit * gw + r];
-          sM[r] = -f.x;  // stored negated: the exponent is one fma, x * c_log2 + (-M)
-          sZ[r] = f.y;
+          const float2 f = fin[w.unit * gw + r];  // (M, 1/Z)
+          // 2^(x c - M) / Z = 2^(x c - (M + log2 Z)); stored negated, so the
+          // exponent is one fma: x * c_log2 + sM
+          sM[r] = log2f(f.y) - f.x;
           sPos[r] = T - W + (r % W);
         } else {
-          sM[r] = -INFINITY;  // padding rows contribute 2^-inf * 0 = 0
-          sZ[r] = 0.f;
+          sM[r] = -INFINITY;  // padding rows contribute 2^-inf = 0
           sPos[r] = -1;
         }
       }
@@ -462,25 +486,9 @@ __global__ void __launch_bounds__(NT, 1)
               if (q >= nq) break;
               const int ch = wg + 4 * q;
               const float4 *m4 = reinterpret_cast<const float4 *>(sM + ch * 16);
-              const float4 *z4 = reinterpret_cast<const float4 *>(sZ + ch * 16);
               const int4 *p4 = reinterpret_cast<const int4 *>(sPos + ch * 16);
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const float4 mm = m4[u], zz = z4[u];
-                const float2 xa = __ffma2_rn(make_float2(__uint_as_float(r[q][4 * u]), __uint_as_float(r[q][4 * u + 1])),
-                                             c2, make_float2(mm.x, mm.y));
-                const float2 xb = __ffma2_rn(make_float2(__uint_as_float(r[q][4 * u + 2]), __uint_as_float(r[q][4 * u + 3])),
-                                             c2, make_float2(mm.z, mm.w));
-                float2 ea = make_float2(tc::ex2(xa.x), tc::ex2(xa.y));
-                float2 eb = make_float2(tc::ex2(xb.x), tc::ex2(xb.y));
-                if (masked) {
-                  const int4 pp = p4[u];
-                  ea = make_float2(j <= pp.x ? ea.x : 0.f, j <= pp.y ? ea.y : 0.f);
-                  eb = make_float2(j <= pp.z ? eb.x : 0.f, j <= pp.w ? eb.y : 0.f);
-                }
-                acc2 = __ffma2_rn(ea, make_float2(zz.x, zz.y), acc2);
-                acc2 = __ffma2_rn(eb, make_float2(zz.z, zz.w), acc2);
-              }
+              acc2 = masked ? colsum_chunk<true>(r[q], m4, p4, j, c2, acc2)
+                            : colsum_chunk<false>(r[q], m4, p4, j, c2, acc2);
             }
           }
           acc = acc2.x + acc2.y;
