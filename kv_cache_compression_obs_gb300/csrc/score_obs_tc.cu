@@ -166,9 +166,14 @@ __device__ void issue(uint32_t tmem, unsigned char *sQ, unsigned char *sK, const
                       int n_items, int per_unit, int span, int T, int n_mt, int n_cols,
                       volatile int *abort_flag, int *status) {
   using G = Geo<D>;
-  const uint32_t q_addr = tc::smem_u32(sQ);
-  const uint32_t k_addr = tc::smem_u32(sK);
+  // Operand descriptors: built once and stepped by constant offsets (the start
+  // address field holds addr >> 4; shared memory stays below 2^18 bytes, so a
+  // step never carries out of it).  The issuing thread shares its SMSP with busy
+  // epilogue warps, so every instruction saved here keeps the tensor pipe fed.
+  const uint64_t qd0 = tc::sdesc_sw128(tc::smem_u32(sQ));
+  const uint64_t kd_base = tc::sdesc_sw128(tc::smem_u32(sK));
   const uint32_t idesc = (PASS == 1) ? tc::idesc_bf16(128, KT) : tc::idesc_bf16(128, n_cols);
+  const bool two_mt = n_mt > 1;
   uint32_t g = 0;
   int it = 0;
   bool ok = true;
@@ -191,18 +196,17 @@ __device__ void issue(uint32_t tmem, unsigned char *sQ, unsigned char *sK, const
         break;
       }
       tc::fence_after_sync();
-      const uint32_t kst = k_addr + st * G::KBYTES;
+      const uint64_t kd0 = kd_base + (uint64_t)((st * G::KBYTES) >> 4);
+      const uint32_t d0 = tmem + slot * 256;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t koff = (kk / 4) * G::KSUB + (kk % 4) * 32;
-        const uint32_t qoff = (kk / 4) * G::QSUB + (kk % 4) * 32;
+        const uint64_t kd = kd0 + (uint64_t)(((kk / 4) * G::KSUB + (kk % 4) * 32) >> 4);
+        const uint64_t qd = qd0 + (uint64_t)(((kk / 4) * G::QSUB + (kk % 4) * 32) >> 4);
         if (PASS == 1) {
-          for (int mt = 0; mt < n_mt; ++mt)
-            tc::umma_bf16(tmem + slot * 256 + mt * 128, tc::sdesc_sw128(q_addr + qoff + mt * 128 * 128),
-                          tc::sdesc_sw128(kst + koff), idesc, kk > 0);
+          tc::umma_bf16(d0, qd, kd, idesc, kk > 0);
+          if (two_mt) tc::umma_bf16(d0 + 128, qd + (uint64_t)((128 * 128) >> 4), kd, idesc, kk > 0);
         } else {
-          tc::umma_bf16(tmem + slot * 256, tc::sdesc_sw128(kst + koff), tc::sdesc_sw128(q_addr + qoff),
-                        idesc, kk > 0);
+          tc::umma_bf16(d0, kd, qd, idesc, kk > 0);
         }
       }
       tc::umma_commit(B.empty + st);
