@@ -44,14 +44,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Like mbar_try_wait, but the thread may stay suspended (until the phase
+// completes, or at most about `hint_ns` nanoseconds) instead of returning at once.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for the phase with parity `parity` of `bar` to complete, giving up after
 // `budget` clock cycles or (when `abort` is not null) as soon as *abort becomes
-// non-zero.  Returns false when it gave up.
+// non-zero.  Returns false when it gave up.  A waiting thread sleeps in the
+// barrier (at most ~20 us per try) instead of spinning on issue slots.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long long budget,
                                           volatile int *abort) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
     if (abort && *abort) return false;
     if (clock64() - t0 > budget) return false;
   }
