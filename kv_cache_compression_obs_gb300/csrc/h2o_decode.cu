@@ -25,14 +25,15 @@
 //               V stage: one row at a time across the lanes, o_g += w_gj v_j.
 //               When the CTA's part of a unit is done, its warps' (r, Z, o) are
 //               combined into one partial per (unit, CTA).
-//   finalize -- one cluster of CE CTAs per unit: combines the partials into
-//               o_out; turns the stored logits into probabilities
-//               P_j = sum_g 2^(l_gj - (M_g + log2 Z_g)), adds them to the slots'
-//               accumulators and takes each CTA's (acc, pos)-smallest slot
-//               outside the recent window; after a cluster barrier CTA 0 picks
-//               the smallest over the cluster (and the new token itself when
+//   finalize -- CE CTAs per unit: combine the partials into o_out; turn the
+//               stored logits into probabilities P_j = sum_g 2^(l_gj - (M_g +
+//               log2 Z_g)), add them to the slots' accumulators and take each
+//               CTA's (acc, pos)-smallest slot outside the recent window.  Each
+//               CTA publishes its candidate and counts itself in on the unit's
+//               arrival counter (zeroed by the stream kernel); the last to
+//               arrive picks the smallest (and the new token itself when
 //               recent == 0) and appends the new token or writes it over the
-//               victim.  A CTA's slot loads are issued before the partials are
+//               victim.  No CTA waits for another.  A CTA's slot loads are issued before the partials are
 //               combined.
 //
 // Workspace: logits [units][G][cap+1] and the per-(unit, CTA) partials (m, Z)
@@ -40,12 +41,8 @@
 #include <cmath>
 #include <type_traits>
 
-#include <cooperative_groups.h>
-
 #include "kvc_internal.cuh"
 #include "tc_common.cuh"
-
-namespace cg = cooperative_groups;
 
 namespace kvc {
 namespace {
@@ -62,7 +59,7 @@ constexpr long long kWaitBudget = 2000000000LL;  // clock cycles (~1 s) before a
 constexpr long long kDrainBudget = 200000000LL;  // ~0.1 s for copies in flight at exit
 constexpr int BAR_CONS = 1;  // named barrier of the consumer warps
 constexpr int NTF = 256;     // finalize threads per CTA
-constexpr int CE = 4;        // finalize CTAs per unit (one thread-block cluster)
+constexpr int CE = 4;        // finalize CTAs per unit
 constexpr int RU = 8;        // finalize slots per thread in flight
 
 __device__ __forceinline__ bool better(float a, int p, float ba, int bp) {
@@ -116,6 +113,8 @@ struct Ws {      // workspace carve-up
   float *lgw;    // [units][G][cap+1] logits
   float2 *pmz;   // [units][PM][G] per-(unit, CTA) max and normaliser
   float *po;     // [units][PM][G][D] per-(unit, CTA) output shares (relative to the max)
+  Cand *cnd;     // [units][CE] the finalize CTAs' eviction candidates
+  int *cnt;      // [units] finalize arrivals (zeroed by the stream kernel of the same step)
 };
 
 inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
@@ -127,7 +126,7 @@ __host__ __device__ inline int partials_per_unit(int cap) {
   return (blocks_per_unit(cap, RB_MIN) + PER_MIN - 1) / PER_MIN + 1;
 }
 
-Ws carve(void *ws, long units, int G, int cap) {
+Ws carve(void *ws, long units, int G, int cap, int d) {
   const int PM = partials_per_unit(cap);
   Ws w;
   char *p = static_cast<char *>(ws);
@@ -136,6 +135,10 @@ Ws carve(void *ws, long units, int G, int cap) {
   w.pmz = reinterpret_cast<float2 *>(p);
   p += align256((size_t)units * PM * G * 8);
   w.po = reinterpret_cast<float *>(p);
+  p += align256((size_t)units * PM * G * d * 4);
+  w.cnd = reinterpret_cast<Cand *>(p);
+  p += align256((size_t)units * CE * sizeof(Cand));
+  w.cnt = reinterpret_cast<int *>(p);
   return w;
 }
 
@@ -247,6 +250,8 @@ __global__ __launch_bounds__(32 * (NCW + 1), 1) void decode_stream_kernel(
   const long lo = blockIdx.x * per;
   const long hi = min(total, lo + per);
 
+  // the finalize kernel's arrival counters: each unit's by the CTA holding its first block
+  for (long u = (lo + NB - 1) / NB + threadIdx.x; u * NB < hi; u += blockDim.x) ws.cnt[u] = 0;
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       tc::mbar_init(kfull + i, 1);
@@ -596,16 +601,14 @@ __global__ __launch_bounds__(NTF) void decode_finalize_kernel(
   constexpr int GD = G * D;
   __shared__ float gm[G], gz[G], gc[G];
   __shared__ Cand wc[NWF];
-  __shared__ Cand cand;
-  __shared__ int sh_slot;
-  cg::cluster_group cluster = cg::this_cluster();
-  const int rank = static_cast<int>(cluster.block_rank());
+  __shared__ int sh_slot, sh_last;
+  const int rank = static_cast<int>(blockIdx.x % CE);
   const long unit = blockIdx.x / CE;
   const long b = unit / Hkv;
   const int h = static_cast<int>(unit % Hkv);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int n = len[unit];
-  if (n < 0 || n > cap) {  // same n in the whole cluster: every CTA leaves here
+  if (n < 0 || n > cap) {  // same n in all the unit's CTAs: every one leaves here
     if (rank == 0 && threadIdx.x == 0 && dev_status) atomicExch(dev_status, (int)KV_ERR_INVALID_ARG);
     return;
   }
@@ -721,59 +724,62 @@ __global__ __launch_bounds__(NTF) void decode_finalize_kernel(
       }
       c.accself += wc[v].accself;
     }
-    cand = c;
+    // publish this CTA's candidate; the unit's last CTA to arrive decides
+    ws.cnd[unit * CE + rank] = c;
+    __threadfence();
+    sh_last = atomicAdd(ws.cnt + unit, 1) == CE - 1;
   }
-  cluster.sync();  // #1: every CTA's candidate is visible
-  if (rank == 0) {
-    if (threadIdx.x == 0) {
-      float ba = INFINITY, accnew = 0.f;
-      int bp = 0x7FFFFFFF, bj = -2;
-      for (int r = 0; r < CE; ++r) {
-        const Cand cc = *cluster.map_shared_rank(&cand, r);
-        if (cc.slot != -2 && (bj == -2 || better(cc.acc, cc.pos, ba, bp))) {
-          ba = cc.acc;
-          bp = cc.pos;
-          bj = cc.slot;
-        }
-        accnew += cc.accself;
+  __syncthreads();
+  if (!sh_last) return;
+  if (threadIdx.x == 0) {
+    __threadfence();
+    float ba = INFINITY, accnew = 0.f;
+    int bp = 0x7FFFFFFF, bj = -2;
+    for (int r = 0; r < CE; ++r) {
+      const float4 raw = __ldcg(reinterpret_cast<const float4 *>(ws.cnd + unit * CE + r));
+      const Cand cc{raw.x, __float_as_int(raw.y), __float_as_int(raw.z), raw.w};
+      if (cc.slot != -2 && (bj == -2 || better(cc.acc, cc.pos, ba, bp))) {
+        ba = cc.acc;
+        bp = cc.pos;
+        bj = cc.slot;
       }
-      int slot = -1, ev = -1;
-      if (n < cap) {
-        slot = n;
-        len[unit] = n + 1;
+      accnew += cc.accself;
+    }
+    int slot = -1, ev = -1;
+    if (n < cap) {
+      slot = n;
+      len[unit] = n + 1;
+    } else {
+      if (recent == 0 && (bj == -2 || better(accnew, new_pos, ba, bp))) bj = -1;  // the new token
+      if (bj == -2) {
+        if (dev_status) atomicExch(dev_status, (int)KV_ERR_INVALID_ARG);
+      } else if (bj == -1) {
+        ev = new_pos;
       } else {
-        if (recent == 0 && (bj == -2 || better(accnew, new_pos, ba, bp))) bj = -1;  // the new token
-        if (bj == -2) {
-          if (dev_status) atomicExch(dev_status, (int)KV_ERR_INVALID_ARG);
-        } else if (bj == -1) {
-          ev = new_pos;
-        } else {
-          slot = bj;
-          ev = bp;
-        }
-      }
-      sh_slot = slot;
-      evicted[unit] = ev;
-      if (slot >= 0) {
-        pu[slot] = new_pos;
-        au[slot] = accnew;
+        slot = bj;
+        ev = bp;
       }
     }
-    __syncthreads();
-    const int slot = sh_slot;
+    sh_slot = slot;
+    evicted[unit] = ev;
     if (slot >= 0) {
-      constexpr int VECS = D * (int)sizeof(T) / 16;
-      uint4 *kd = reinterpret_cast<uint4 *>(Kc + (unit * (long)cap + slot) * D);
-      uint4 *vd = reinterpret_cast<uint4 *>(Vc + (unit * (long)cap + slot) * D);
-      const uint4 *ks = reinterpret_cast<const uint4 *>(k_new + unit * (long)D);
-      const uint4 *vs = reinterpret_cast<const uint4 *>(v_new + unit * (long)D);
-      for (int t = threadIdx.x; t < VECS; t += NTF) {
-        kd[t] = __ldg(ks + t);
-        vd[t] = __ldg(vs + t);
-      }
+      pu[slot] = new_pos;
+      au[slot] = accnew;
     }
   }
-  cluster.sync();  // #2: rank 0 has finished reading the others' shared memory
+  __syncthreads();
+  const int slot = sh_slot;
+  if (slot >= 0) {
+    constexpr int VECS = D * (int)sizeof(T) / 16;
+    uint4 *kd = reinterpret_cast<uint4 *>(Kc + (unit * (long)cap + slot) * D);
+    uint4 *vd = reinterpret_cast<uint4 *>(Vc + (unit * (long)cap + slot) * D);
+    const uint4 *ks = reinterpret_cast<const uint4 *>(k_new + unit * (long)D);
+    const uint4 *vs = reinterpret_cast<const uint4 *>(v_new + unit * (long)D);
+    for (int t = threadIdx.x; t < VECS; t += NTF) {
+      kd[t] = __ldg(ks + t);
+      vd[t] = __ldg(vs + t);
+    }
+  }
 }
 
 template <typename T, int D, int G>
@@ -783,7 +789,7 @@ int run_decode(const void *q, const void *k_new, const void *v_new, void *K_cach
                int32_t *evicted, int *dev_status, cudaStream_t st) {
   using Geo = DGeo<T, D, G>;
   const long units = (long)B * Hkv;
-  const Ws ws = carve(workspace, units, G, cap);
+  const Ws ws = carve(workspace, units, G, cap, D);
   const int alg1 = (flags & KV_H2O_ALG1) ? 1 : 0;
   if (ensure_smem((const void *)decode_stream_kernel<T, D, G>, Geo::SMEM))
     return cuda_failure(cudaErrorInvalidValue, "decode stream kernel: shared memory limit");
@@ -796,30 +802,14 @@ int run_decode(const void *q, const void *k_new, const void *v_new, void *K_cach
       static_cast<const T *>(K_cache), static_cast<const T *>(V_cache), static_cast<const T *>(q),
       static_cast<const T *>(k_new), static_cast<const T *>(v_new), len, Hq, Hkv, cap,
       scale * 1.4426950408889634f /* log2 e */, alg1, total, per, ws, dev_status);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(units * CE), 1, 1);
-  cfg.blockDim = dim3(NTF, 1, 1);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CE;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
   {
     const int rc = launch_status(0);  // the stream kernel's launch
     if (rc != KV_OK) return rc;
   }
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_finalize_kernel<T, D, G>, static_cast<const T *>(k_new),
-                                           static_cast<const T *>(v_new), static_cast<T *>(K_cache),
-                                           static_cast<T *>(V_cache), pos, acc, len, Hq, Hkv, cap, recent,
-                                           new_pos, alg1, per, ws, o, evicted, dev_status);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return cuda_failure(e, "decode finalize kernel launch");
-  }
+  decode_finalize_kernel<T, D, G><<<(unsigned)(units * CE), NTF, 0, st>>>(
+      static_cast<const T *>(k_new), static_cast<const T *>(v_new), static_cast<T *>(K_cache),
+      static_cast<T *>(V_cache), pos, acc, len, Hq, Hkv, cap, recent, new_pos, alg1, per, ws, o, evicted,
+      dev_status);
   return launch_status(2);
 }
 
@@ -846,7 +836,8 @@ int dispatch_g(int G, const void *q, const void *k_new, const void *v_new, void 
 size_t decode_workspace_bytes(long units, int G, int cap, int d) {
   const int PM = partials_per_unit(cap);
   return align256((size_t)units * G * (cap + 1) * 4) + align256((size_t)units * PM * G * 8) +
-         (size_t)units * PM * G * d * 4;
+         align256((size_t)units * PM * G * d * 4) + align256((size_t)units * CE * sizeof(Cand)) +
+         (size_t)units * sizeof(int);
 }
 
 int launch_decode_step(const void *q, const void *k_new, const void *v_new, void *K_cache,
