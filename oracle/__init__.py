@@ -19,6 +19,7 @@ from .build import build_oracle
 
 BF16, F32 = 0, 1
 FLAG_ALG1 = 1
+HUB_AVGPOOL, HUB_FIXED_HEAD = 1, 2
 
 _lib = None
 
@@ -32,14 +33,14 @@ def _load():
         lib.oracle_kv_cache_bytes.argtypes = [LL, LL, LL, LL, LL]
         lib.oracle_score_obs.restype = I
         lib.oracle_score_obs.argtypes = [P, P, I, I, I, I, I, I, D, I, P]
-        lib.oracle_hubkv_refine.restype = I
-        lib.oracle_hubkv_refine.argtypes = [P, I, I, I, I, D, D, D, D, P, P, P]
-        lib.oracle_select_topk.restype = I
-        lib.oracle_select_topk.argtypes = [P, I, I, I, I, I, P]
+        lib.oracle_hubkv_refine_ex.restype = I
+        lib.oracle_hubkv_refine_ex.argtypes = [P, I, I, I, I, D, D, D, D, I, P, P, P]
+        lib.oracle_select_topk_ex.restype = I
+        lib.oracle_select_topk_ex.argtypes = [P, I, I, I, I, I, I, P]
         lib.oracle_compact.restype = I
         lib.oracle_compact.argtypes = [P, P, P, P, I, I, I, I, I, I, P, P, I, P, P, P]
-        lib.oracle_decode_step.restype = I
-        lib.oracle_decode_step.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, D, I, I, P, P]
+        lib.oracle_decode_step_ex.restype = I
+        lib.oracle_decode_step_ex.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, D, I, I, P, P]
         _lib = lib
     return _lib
 
@@ -76,26 +77,31 @@ def score_obs(Q: np.ndarray, K: np.ndarray, scale: float) -> np.ndarray:
 
 
 def hubkv_refine(s: np.ndarray, r: float, gamma: float = 0.5, pool_width: int = 5,
-                 beta_lo: float = 0.8, beta_hi: float = 1.2):
-    """s [B][H][T] (any float dtype, read as float64) -> (z, beta, sel), all float64."""
+                 beta_lo: float = 0.8, beta_hi: float = 1.2, flags: int = 0):
+    """s [B][H][T] (any float dtype, read as float64) -> (z, beta, sel), all float64.
+
+    flags: HUB_AVGPOOL (average-pool smoothing in place of hubs), HUB_FIXED_HEAD (beta = 1)."""
     s = np.ascontiguousarray(s, dtype=np.float64)
     B, H, T = s.shape
     z = np.zeros_like(s)
     beta = np.zeros((B, H), dtype=np.float64)
     sel = np.zeros((B, H), dtype=np.float64)
-    rc = _load().oracle_hubkv_refine(_ptr(s), B, H, T, pool_width, float(gamma), float(r),
-                                     float(beta_lo), float(beta_hi), _ptr(z), _ptr(beta), _ptr(sel))
+    rc = _load().oracle_hubkv_refine_ex(_ptr(s), B, H, T, pool_width, float(gamma), float(r),
+                                        float(beta_lo), float(beta_hi), int(flags), _ptr(z), _ptr(beta),
+                                        _ptr(sel))
     if rc != 0:
         raise ValueError("oracle_hubkv_refine rejected its inputs")
     return z, beta, sel
 
 
-def select_topk(z: np.ndarray, k: int, recent: int) -> np.ndarray:
-    """z [B][H][T] (read as float64) -> idx [B][H][k] int32, ascending per head."""
+def select_topk(z: np.ndarray, k: int, recent: int, sink: int = 0) -> np.ndarray:
+    """z [B][H][T] (read as float64) -> idx [B][H][k] int32, ascending per head.
+
+    sink: the first `sink` positions are always kept (attention sinks)."""
     z = np.ascontiguousarray(z, dtype=np.float64)
     B, H, T = z.shape
     idx = np.zeros((B, H, k), dtype=np.int32)
-    rc = _load().oracle_select_topk(_ptr(z), B, H, T, int(k), int(recent), _ptr(idx))
+    rc = _load().oracle_select_topk_ex(_ptr(z), B, H, T, int(k), int(recent), int(sink), _ptr(idx))
     if rc != 0:
         raise ValueError("oracle_select_topk rejected its inputs")
     return idx
@@ -123,8 +129,9 @@ def compact(K: np.ndarray, V: np.ndarray, s, idx: np.ndarray, cap: int):
 
 
 def decode_step(q, k_new, v_new, K_cache, V_cache, pos, acc, ln, recent: int, new_pos: int,
-                scale: float, flags: int = 0):
+                scale: float, flags: int = 0, sink: int = 0):
     """One decode step; K_cache, V_cache, pos, acc, ln are updated IN PLACE.
+    Positions below `sink` are never evicted.
 
     Returns (o [B][Hq][d] float64, evicted [B][Hkv] int32).
     """
@@ -138,9 +145,10 @@ def decode_step(q, k_new, v_new, K_cache, V_cache, pos, acc, ln, recent: int, ne
     v_new = np.ascontiguousarray(v_new)
     o = np.zeros((B, Hq, d), dtype=np.float64)
     ev = np.zeros((B, Hkv), dtype=np.int32)
-    rc = _load().oracle_decode_step(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(K_cache), _ptr(V_cache),
-                                    _ptr(pos), _ptr(acc), _ptr(ln), B, Hq, Hkv, cap, d, int(recent),
-                                    int(new_pos), float(scale), int(flags), _dtype_code(q), _ptr(o), _ptr(ev))
+    rc = _load().oracle_decode_step_ex(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(K_cache), _ptr(V_cache),
+                                       _ptr(pos), _ptr(acc), _ptr(ln), B, Hq, Hkv, cap, d, int(recent),
+                                       int(sink), int(new_pos), float(scale), int(flags), _dtype_code(q),
+                                       _ptr(o), _ptr(ev))
     if rc != 0:
         raise ValueError("oracle_decode_step rejected its inputs")
     return o, ev

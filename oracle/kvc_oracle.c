@@ -46,6 +46,8 @@
 #define OR_BF16 0
 #define OR_F32 1
 #define OR_FLAG_ALG1 1
+#define OR_HUB_AVGPOOL 1    /* hubkv_refine variant: average-pool smoothing instead of hubs */
+#define OR_HUB_FIXED_HEAD 2 /* hubkv_refine variant: fixed head weight (beta = 1) */
 
 /* Read element i of a bf16 or f32 array as a double. bf16 is the upper half of
  * an IEEE float32, so the value is exact. */
@@ -137,12 +139,17 @@ int oracle_score_obs(const void *Q, const void *K, int B, int Hq, int Hkv, int T
  *      when that mean is 0.  The unit is one batch row: heads b*H .. b*H+H-1;
  *   4. ratio gate: z_i = s_i + r^2 (beta_h q_i - s_i).
  * s, z [B][H][T]; beta, sel [B][H] (either may be NULL).
+ *
+ * Variants the HubKV page reports as weaker (尝试路线：效果一般的可能原因), as
+ * flags: OR_HUB_AVGPOOL replaces steps 1-2 by average-pool smoothing, q_i = the
+ * mean of s over the same window ("CommunitySmooth"); OR_HUB_FIXED_HEAD replaces
+ * step 3 by a fixed head weight, beta_h = 1.
  * ------------------------------------------------------------------------- */
-int oracle_hubkv_refine(const double *s, int B, int H, int T, int pool_width, double gamma,
-                        double r, double beta_lo, double beta_hi, double *z_out,
-                        double *beta_out, double *sel_out) {
+int oracle_hubkv_refine_ex(const double *s, int B, int H, int T, int pool_width, double gamma,
+                           double r, double beta_lo, double beta_hi, int flags, double *z_out,
+                           double *beta_out, double *sel_out) {
   if (B < 0 || H <= 0 || T <= 0 || pool_width <= 0 || pool_width % 2 == 0 ||
-      beta_lo > beta_hi)
+      beta_lo > beta_hi || (flags & ~(OR_HUB_AVGPOOL | OR_HUB_FIXED_HEAD)))
     return -1;
   const int half = pool_width / 2;
   double *sel = (double *)malloc(sizeof(double) * (size_t)(B > 0 ? B : 1) * H);
@@ -168,7 +175,7 @@ int oracle_hubkv_refine(const double *s, int B, int H, int T, int pool_width, do
     for (int h = 0; h < H; ++h) {
       const long long u = (long long)b * H + h;
       double beta = 1.0;
-      if (mean != 0.0) {
+      if (mean != 0.0 && !(flags & OR_HUB_FIXED_HEAD)) {
         beta = sel[u] / mean;
         if (beta < beta_lo) beta = beta_lo;
         if (beta > beta_hi) beta = beta_hi;
@@ -177,10 +184,23 @@ int oracle_hubkv_refine(const double *s, int B, int H, int T, int pool_width, do
       const double *sv = s + u * (long long)T;
       double *zv = z_out + u * (long long)T;
       for (int i = 0; i < T; ++i) {
-        double M = -INFINITY;
-        for (int j = i - half; j <= i + half; ++j)
-          if (j >= 0 && j < T && sv[j] > M) M = sv[j];
-        const double qi = (sv[i] == M) ? sv[i] : gamma * sv[i];
+        double qi;
+        if (flags & OR_HUB_AVGPOOL) {
+          /* the smoothing variant: the mean of s over the window (cut at the ends) */
+          double sum = 0.0;
+          int cnt = 0;
+          for (int j = i - half; j <= i + half; ++j)
+            if (j >= 0 && j < T) {
+              sum += sv[j];
+              ++cnt;
+            }
+          qi = sum / cnt;
+        } else {
+          double M = -INFINITY;
+          for (int j = i - half; j <= i + half; ++j)
+            if (j >= 0 && j < T && sv[j] > M) M = sv[j];
+          qi = (sv[i] == M) ? sv[i] : gamma * sv[i];
+        }
         zv[i] = sv[i] + r * r * (beta * qi - sv[i]);
       }
     }
@@ -189,12 +209,22 @@ int oracle_hubkv_refine(const double *s, int B, int H, int T, int pool_width, do
   return 0;
 }
 
+int oracle_hubkv_refine(const double *s, int B, int H, int T, int pool_width, double gamma,
+                        double r, double beta_lo, double beta_hi, double *z_out,
+                        double *beta_out, double *sel_out) {
+  return oracle_hubkv_refine_ex(s, B, H, T, pool_width, gamma, r, beta_lo, beta_hi, 0, z_out,
+                                beta_out, sel_out);
+}
+
 /* ---------------------------------------------------------------------------
  * Step 3: budgeted per-head Top-K with a protected recent window.
  * Keep the last R positions [T-R, T) unconditionally ([H2O] 双缓冲), and the
  * k-R best of [0, T-R) ordered by (z descending, position ascending).  Output
  * the k kept positions in ascending order.  Each head selects on its own
  * ([H2O] 按头独立驱逐).  z [B][H][T], idx [B][H][k].  Requires 0 <= R < k <= T.
+ * With S sink positions ([KVblog] §4.1-4.2: the first few tokens are kept as
+ * attention sinks) the first S positions are kept too and the heavy part is the
+ * k-R-S best of [S, T-R); requires S + R < k.
  * ------------------------------------------------------------------------- */
 typedef struct {
   double z;
@@ -213,10 +243,11 @@ static int or_cmp_int(const void *a, const void *b) {
   return (x > y) - (x < y);
 }
 
-int oracle_select_topk(const double *z, int B, int H, int T, int k, int recent,
-                       int32_t *idx_out) {
-  if (B < 0 || H <= 0 || T <= 0 || recent < 0 || k <= recent || k > T) return -1;
-  const int n = T - recent, nh = k - recent;
+int oracle_select_topk_ex(const double *z, int B, int H, int T, int k, int recent, int sink,
+                          int32_t *idx_out) {
+  if (B < 0 || H <= 0 || T <= 0 || recent < 0 || sink < 0 || k <= recent + sink || k > T)
+    return -1;
+  const int n = T - recent - sink, nh = k - recent - sink;
   or_cand *c = (or_cand *)malloc(sizeof(or_cand) * (size_t)(n > 0 ? n : 1));
   int *keep = (int *)malloc(sizeof(int) * (size_t)k);
   if (!c || !keep) {
@@ -227,18 +258,24 @@ int oracle_select_topk(const double *z, int B, int H, int T, int k, int recent,
   for (long long u = 0; u < (long long)B * H; ++u) {
     const double *zv = z + u * (long long)T;
     for (int i = 0; i < n; ++i) {
-      c[i].z = zv[i];
-      c[i].pos = i;
+      c[i].z = zv[sink + i];
+      c[i].pos = sink + i;
     }
     qsort(c, (size_t)n, sizeof(or_cand), or_cmp_desc);
     for (int m = 0; m < nh; ++m) keep[m] = c[m].pos;
     for (int m = 0; m < recent; ++m) keep[nh + m] = T - recent + m;
+    for (int m = 0; m < sink; ++m) keep[nh + recent + m] = m;
     qsort(keep, (size_t)k, sizeof(int), or_cmp_int);
     for (int m = 0; m < k; ++m) idx_out[u * (long long)k + m] = keep[m];
   }
   free(c);
   free(keep);
   return 0;
+}
+
+int oracle_select_topk(const double *z, int B, int H, int T, int k, int recent,
+                       int32_t *idx_out) {
+  return oracle_select_topk_ex(z, B, H, T, k, recent, 0, idx_out);
 }
 
 /* ---------------------------------------------------------------------------
@@ -284,18 +321,20 @@ int oracle_compact(const void *K, const void *V, const double *s, const int32_t 
  *               new token (K, V, position, accumulator) and evicted = its
  *               position; if the victim is the new token, nothing is written
  *               and evicted = new_pos.  At most one eviction per head per step.
+ * With S sinks, slots holding positions below S are never victims either
+ * ([KVblog] §4.1-4.2).
  * The accumulators are stored as float32 (their state type) and the argmin is
  * taken on the stored float32 values.
  * q [B][Hq][d]; k_new, v_new [B][Hkv][d]; K_cache, V_cache [B][Hkv][cap][d];
  * pos, acc [B][Hkv][cap]; len, evicted [B][Hkv]; o [B][Hq][d] (double).
  * ------------------------------------------------------------------------- */
-int oracle_decode_step(const void *q, const void *k_new, const void *v_new, void *K_cache,
-                       void *V_cache, int32_t *pos, float *acc, int32_t *len, int B, int Hq,
-                       int Hkv, int cap, int d, int recent, int new_pos, double scale,
-                       int flags, int dtype, double *o_out, int32_t *evicted) {
+int oracle_decode_step_ex(const void *q, const void *k_new, const void *v_new, void *K_cache,
+                          void *V_cache, int32_t *pos, float *acc, int32_t *len, int B, int Hq,
+                          int Hkv, int cap, int d, int recent, int sink, int new_pos, double scale,
+                          int flags, int dtype, double *o_out, int32_t *evicted) {
   const int alg1 = (flags & OR_FLAG_ALG1) != 0;
   if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || cap <= 0 || d <= 0 || recent < 0 ||
-      recent >= cap || (alg1 && recent != 0))
+      sink < 0 || recent >= cap || (alg1 && recent != 0))
     return -1;
   const int G = Hq / Hkv;
   const size_t eb = or_elem_bytes(dtype), row = (size_t)d * eb;
@@ -372,6 +411,7 @@ int oracle_decode_step(const void *q, const void *k_new, const void *v_new, void
       int best_pos = 0;
       for (int j = 0; j < n; ++j) {
         if ((long long)ps[j] > (long long)new_pos - recent) continue;
+        if (ps[j] < sink) continue; /* a protected sink */
         if (victim == -2 || a[j] < best_acc || (a[j] == best_acc && ps[j] < best_pos)) {
           victim = j;
           best_acc = a[j];
@@ -398,4 +438,12 @@ int oracle_decode_step(const void *q, const void *k_new, const void *v_new, void
     free(P);
   }
   return bad ? -1 : 0;
+}
+
+int oracle_decode_step(const void *q, const void *k_new, const void *v_new, void *K_cache,
+                       void *V_cache, int32_t *pos, float *acc, int32_t *len, int B, int Hq,
+                       int Hkv, int cap, int d, int recent, int new_pos, double scale,
+                       int flags, int dtype, double *o_out, int32_t *evicted) {
+  return oracle_decode_step_ex(q, k_new, v_new, K_cache, V_cache, pos, acc, len, B, Hq, Hkv, cap, d,
+                               recent, 0, new_pos, scale, flags, dtype, o_out, evicted);
 }
