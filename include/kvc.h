@@ -69,6 +69,16 @@ enum {
   KV_H2O_ALG1 = 1
 };
 
+/* hubkv_refine_ex flags: the variants [HubKV] 尝试路线：效果一般的可能原因 reports
+ * as weaker than the final method, for comparison runs */
+enum {
+  /* average-pool smoothing ("CommunitySmooth") instead of steps 1-2: q_i = the
+   * mean of s over the same window (cut at the ends) */
+  KV_HUB_AVGPOOL = 1,
+  /* fixed head weight instead of step 3: beta_h = 1 */
+  KV_HUB_FIXED_HEAD = 2
+};
+
 /* operation codes for kv_workspace_size */
 enum { KV_OP_SCORE_OBS = 1, KV_OP_HUBKV_REFINE = 2, KV_OP_SELECT_TOPK = 3, KV_OP_DECODE = 4 };
 
@@ -125,6 +135,16 @@ KVC_API int hubkv_refine(const float *s, int B, int H, int T, int pool_width, fl
                  size_t workspace_bytes, kv_stream_t stream);
 
 /*
+ * hubkv_refine_ex -- hubkv_refine with `flags` (0 or KV_HUB_AVGPOOL |
+ * KV_HUB_FIXED_HEAD) selecting the variants [HubKV] 尝试路线 compares against;
+ * hubkv_refine is hubkv_refine_ex with flags = 0.  Other flag bits are rejected
+ * with KV_ERR_INVALID_ARG.  Same arguments and workspace otherwise.
+ */
+KVC_API int hubkv_refine_ex(const float *s, int B, int H, int T, int pool_width, float gamma,
+                    float r, float beta_lo, float beta_hi, int flags, float *z_out,
+                    float *beta_out, void *workspace, size_t workspace_bytes, kv_stream_t stream);
+
+/*
  * kv_select_topk -- budgeted per-head Top-K with a protected recent window.
  * [H2O] 双缓冲: the last `recent` positions [T-recent, T) are always kept; the
  * other k - recent slots go to the best of [0, T-recent) in the order
@@ -139,6 +159,19 @@ KVC_API int hubkv_refine(const float *s, int B, int H, int T, int pool_width, fl
  */
 KVC_API int kv_select_topk(const float *z, int B, int H, int T, int k, int recent, int32_t *idx_out,
                    void *workspace, size_t workspace_bytes, kv_stream_t stream);
+
+/*
+ * kv_select_topk_ex -- kv_select_topk that also protects `sink` attention-sink
+ * positions ([KVblog] §4.1-4.2: the first few tokens are kept, as StreamingLLM
+ * keeps them with the recent window): [0, sink) and [T-recent, T) are always
+ * kept and the k - recent - sink heavy slots go to the best of
+ * [sink, T-recent) in the order (z descending, position ascending).
+ * kv_select_topk is kv_select_topk_ex with sink = 0.
+ * Preconditions: sink >= 0, 0 <= recent, sink + recent < k <= T.
+ */
+KVC_API int kv_select_topk_ex(const float *z, int B, int H, int T, int k, int recent, int sink,
+                      int32_t *idx_out, void *workspace, size_t workspace_bytes,
+                      kv_stream_t stream);
 
 /*
  * kv_compact -- "real drop" gather-compaction ([H2O] 两套代码) into a
@@ -192,6 +225,20 @@ KVC_API int h2o_decode_step(const void *q, const void *k_new, const void *v_new,
                     int Hkv, int cap, int d, int recent, int32_t new_pos, float scale,
                     int flags, int dtype, float *o_out, int32_t *evicted_pos, void *workspace,
                     size_t workspace_bytes, int *dev_status, kv_stream_t stream);
+
+/*
+ * h2o_decode_step_ex -- h2o_decode_step that also protects attention sinks
+ * ([KVblog] §4.1-4.2): a slot holding a position below `sink` is never a victim
+ * (it keeps accumulating like any other slot).  h2o_decode_step is
+ * h2o_decode_step_ex with sink = 0.  Same arguments and workspace otherwise;
+ * sink < 0 is rejected with KV_ERR_INVALID_ARG.
+ */
+KVC_API int h2o_decode_step_ex(const void *q, const void *k_new, const void *v_new, void *K_cache,
+                       void *V_cache, int32_t *pos, float *acc, int32_t *len, int B, int Hq,
+                       int Hkv, int cap, int d, int recent, int sink, int32_t new_pos,
+                       float scale, int flags, int dtype, float *o_out, int32_t *evicted_pos,
+                       void *workspace, size_t workspace_bytes, int *dev_status,
+                       kv_stream_t stream);
 
 /*
  * kv_score_obs_noalloc -- kv_score_obs without a caller-provided workspace.

@@ -28,6 +28,7 @@ KV_OK, KV_ERR_INVALID_ARG, KV_ERR_UNSUPPORTED, KV_ERR_CUDA, KV_ERR_TIMEOUT, KV_E
     0, -1, -2, -3, -4, -5)
 KV_BF16, KV_F32 = 0, 1
 KV_H2O_ALG1 = 1
+KV_HUB_AVGPOOL, KV_HUB_FIXED_HEAD = 1, 2
 KV_OP_SCORE_OBS, KV_OP_HUBKV_REFINE, KV_OP_SELECT_TOPK, KV_OP_DECODE = 1, 2, 3, 4
 
 _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -35,13 +36,20 @@ _lib.kv_score_obs.restype = _I
 _lib.kv_score_obs.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _Z, _P, _P]
 _lib.hubkv_refine.restype = _I
 _lib.hubkv_refine.argtypes = [_P, _I, _I, _I, _I, _F, _F, _F, _F, _P, _P, _P, _Z, _P]
+_lib.hubkv_refine_ex.restype = _I
+_lib.hubkv_refine_ex.argtypes = [_P, _I, _I, _I, _I, _F, _F, _F, _F, _I, _P, _P, _P, _Z, _P]
 _lib.kv_select_topk.restype = _I
 _lib.kv_select_topk.argtypes = [_P, _I, _I, _I, _I, _I, _P, _P, _Z, _P]
+_lib.kv_select_topk_ex.restype = _I
+_lib.kv_select_topk_ex.argtypes = [_P, _I, _I, _I, _I, _I, _I, _P, _P, _Z, _P]
 _lib.kv_compact.restype = _I
 _lib.kv_compact.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P]
 _lib.h2o_decode_step.restype = _I
 _lib.h2o_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
                                  _I, _I, _P, _P, _P, _Z, _P, _P]
+_lib.h2o_decode_step_ex.restype = _I
+_lib.h2o_decode_step_ex.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
+                                    _F, _I, _I, _P, _P, _P, _Z, _P, _P]
 _lib.kv_score_obs_noalloc.restype = _I
 _lib.kv_score_obs_noalloc.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P]
 _lib.kv_workspace_size.restype = _Z
@@ -144,8 +152,10 @@ def kv_score_obs_noalloc(Q_obs: torch.Tensor, K: torch.Tensor, scale: float | No
 
 def hubkv_refine(s: torch.Tensor, r: float, gamma: float = 0.5, pool_width: int = 5,
                  beta_lo: float = 0.8, beta_hi: float = 1.2, out=None, beta_out=None,
-                 workspace=None, stream=None):
-    """s [B][H][T] float32 -> (z [B][H][T], beta [B][H]) float32."""
+                 workspace=None, stream=None, flags: int = 0):
+    """s [B][H][T] float32 -> (z [B][H][T], beta [B][H]) float32.
+
+    flags: KV_HUB_AVGPOOL and/or KV_HUB_FIXED_HEAD select the comparison variants."""
     B, H, T = s.shape
     if s.dtype != torch.float32:
         raise TypeError("s must be float32")
@@ -154,21 +164,23 @@ def hubkv_refine(s: torch.Tensor, r: float, gamma: float = 0.5, pool_width: int 
     beta = beta_out if beta_out is not None else torch.empty(B, H, dtype=torch.float32,
                                                              device=s.device)
     ws, nbytes = _workspace(kv_workspace_size(KV_OP_HUBKV_REFINE, B, H, H, T), s.device, workspace)
-    _check("hubkv_refine", _lib.hubkv_refine(_ptr(s), B, H, T, pool_width, float(gamma), float(r),
-                                             float(beta_lo), float(beta_hi), _ptr(z), _ptr(beta),
-                                             _ptr(ws), nbytes, _stream(stream)))
+    _check("hubkv_refine", _lib.hubkv_refine_ex(_ptr(s), B, H, T, pool_width, float(gamma), float(r),
+                                                float(beta_lo), float(beta_hi), int(flags), _ptr(z),
+                                                _ptr(beta), _ptr(ws), nbytes, _stream(stream)))
     return z, beta
 
 
-def kv_select_topk(z: torch.Tensor, k: int, recent: int, out=None, stream=None) -> torch.Tensor:
-    """z [B][H][T] float32 -> idx [B][H][k] int32 (ascending positions)."""
+def kv_select_topk(z: torch.Tensor, k: int, recent: int, out=None, stream=None,
+                   sink: int = 0) -> torch.Tensor:
+    """z [B][H][T] float32 -> idx [B][H][k] int32 (ascending positions); the first
+    `sink` positions are kept as attention sinks."""
     B, H, T = z.shape
     if z.dtype != torch.float32:
         raise TypeError("z must be float32")
     _dev(z, out)
     idx = out if out is not None else torch.empty(B, H, k, dtype=torch.int32, device=z.device)
-    _check("kv_select_topk", _lib.kv_select_topk(_ptr(z), B, H, T, int(k), int(recent), _ptr(idx),
-                                                 None, 0, _stream(stream)))
+    _check("kv_select_topk", _lib.kv_select_topk_ex(_ptr(z), B, H, T, int(k), int(recent), int(sink),
+                                                    _ptr(idx), None, 0, _stream(stream)))
     return idx
 
 
@@ -196,8 +208,9 @@ def kv_compact(K: torch.Tensor, V: torch.Tensor, s, idx: torch.Tensor, cap: int 
 
 def h2o_decode_step(q, k_new, v_new, K_cache, V_cache, pos, acc, len_, recent: int, new_pos: int,
                     scale: float | None = None, flags: int = 0, o_out=None, evicted_out=None,
-                    workspace=None, dev_status=None, stream=None):
-    """One decode step, cache state updated in place; returns (o [B][Hq][d] f32, evicted [B][Hkv])."""
+                    workspace=None, dev_status=None, stream=None, sink: int = 0):
+    """One decode step, cache state updated in place; returns (o [B][Hq][d] f32, evicted [B][Hkv]).
+    Positions below `sink` are never evicted (attention sinks)."""
     B, Hq, d = q.shape
     _, Hkv, cap, _ = K_cache.shape
     _dev(q, k_new, v_new, K_cache, V_cache, pos, acc, len_, o_out, evicted_out, dev_status)
@@ -207,9 +220,9 @@ def h2o_decode_step(q, k_new, v_new, K_cache, V_cache, pos, acc, len_, recent: i
     ev = evicted_out if evicted_out is not None else torch.empty(B, Hkv, dtype=torch.int32,
                                                                  device=q.device)
     ws, nbytes = _workspace(kv_workspace_size(KV_OP_DECODE, B, Hq, Hkv, cap, d), q.device, workspace)
-    _check("h2o_decode_step", _lib.h2o_decode_step(
+    _check("h2o_decode_step", _lib.h2o_decode_step_ex(
         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(K_cache), _ptr(V_cache), _ptr(pos), _ptr(acc),
-        _ptr(len_), B, Hq, Hkv, cap, d, int(recent), int(new_pos), float(scale), int(flags),
+        _ptr(len_), B, Hq, Hkv, cap, d, int(recent), int(sink), int(new_pos), float(scale), int(flags),
         _dtype_code(q), _ptr(o), _ptr(ev), _ptr(ws), nbytes, _ptr(dev_status), _stream(stream)))
     return o, ev
 

@@ -28,7 +28,8 @@
 //   finalize -- CE CTAs per unit: combine the partials into o_out; turn the
 //               stored logits into probabilities P_j = sum_g 2^(l_gj - (M_g +
 //               log2 Z_g)), add them to the slots' accumulators and take each
-//               CTA's (acc, pos)-smallest slot outside the recent window.  Each
+//               CTA's (acc, pos)-smallest slot outside the recent window and
+//               outside the first `sink` positions (attention sinks).  Each
 //               CTA publishes its candidate and counts itself in on the unit's
 //               arrival counter (zeroed by the stream kernel); the last to
 //               arrive picks the smallest (and the new token itself when
@@ -595,7 +596,7 @@ template <typename T, int D, int G>
 __global__ __launch_bounds__(NTF) void decode_finalize_kernel(
     const T *__restrict__ k_new, const T *__restrict__ v_new, T *__restrict__ Kc, T *__restrict__ Vc,
     int32_t *__restrict__ pos, float *__restrict__ acc, int32_t *__restrict__ len, int Hq, int Hkv,
-    int cap, int recent, int new_pos, int alg1, long per, Ws ws, float *__restrict__ o_out,
+    int cap, int recent, int sink, int new_pos, int alg1, long per, Ws ws, float *__restrict__ o_out,
     int32_t *__restrict__ evicted, int *__restrict__ dev_status) {
   constexpr int NWF = NTF / 32;
   constexpr int GD = G * D;
@@ -689,7 +690,7 @@ __global__ __launch_bounds__(NTF) void decode_finalize_kernel(
       if (j < n) {
         const float a = av[k] + P;
         au[j] = a;
-        if ((long)pv[k] <= lim && better(a, pv[k], best_a, best_p)) {
+        if ((long)pv[k] <= lim && pv[k] >= sink && better(a, pv[k], best_a, best_p)) {
           best_a = a;
           best_p = pv[k];
           best_j = j;
@@ -785,7 +786,7 @@ __global__ __launch_bounds__(NTF) void decode_finalize_kernel(
 template <typename T, int D, int G>
 int run_decode(const void *q, const void *k_new, const void *v_new, void *K_cache, void *V_cache,
                int32_t *pos, float *acc, int32_t *len, int B, int Hq, int Hkv, int cap,
-               int recent, int new_pos, float scale, int flags, void *workspace, float *o,
+               int recent, int sink, int new_pos, float scale, int flags, void *workspace, float *o,
                int32_t *evicted, int *dev_status, cudaStream_t st) {
   using Geo = DGeo<T, D, G>;
   const long units = (long)B * Hkv;
@@ -808,7 +809,7 @@ int run_decode(const void *q, const void *k_new, const void *v_new, void *K_cach
   }
   decode_finalize_kernel<T, D, G><<<(unsigned)(units * CE), NTF, 0, st>>>(
       static_cast<const T *>(k_new), static_cast<const T *>(v_new), static_cast<T *>(K_cache),
-      static_cast<T *>(V_cache), pos, acc, len, Hq, Hkv, cap, recent, new_pos, alg1, per, ws, o, evicted,
+      static_cast<T *>(V_cache), pos, acc, len, Hq, Hkv, cap, recent, sink, new_pos, alg1, per, ws, o, evicted,
       dev_status);
   return launch_status(2);
 }
@@ -816,12 +817,12 @@ int run_decode(const void *q, const void *k_new, const void *v_new, void *K_cach
 template <typename T, int D>
 int dispatch_g(int G, const void *q, const void *k_new, const void *v_new, void *K_cache,
                void *V_cache, int32_t *pos, float *acc, int32_t *len, int B, int Hq, int Hkv,
-               int cap, int recent, int new_pos, float scale, int flags, void *workspace,
+               int cap, int recent, int sink, int new_pos, float scale, int flags, void *workspace,
                float *o, int32_t *evicted, int *dev_status, cudaStream_t st) {
 #define KVC_DEC(GG)                                                                          \
   if (G == GG)                                                                               \
     return run_decode<T, D, GG>(q, k_new, v_new, K_cache, V_cache, pos, acc, len, B, Hq, Hkv, \
-                                cap, recent, new_pos, scale, flags, workspace, o, evicted,    \
+                                cap, recent, sink, new_pos, scale, flags, workspace, o, evicted,    \
                                 dev_status, st);
   KVC_DEC(1)
   KVC_DEC(2)
@@ -842,25 +843,25 @@ size_t decode_workspace_bytes(long units, int G, int cap, int d) {
 
 int launch_decode_step(const void *q, const void *k_new, const void *v_new, void *K_cache,
                        void *V_cache, int32_t *pos, float *acc, int32_t *len, int B, int Hq,
-                       int Hkv, int cap, int d, int recent, int32_t new_pos, float scale,
+                       int Hkv, int cap, int d, int recent, int sink, int32_t new_pos, float scale,
                        int flags, int dtype, void *workspace, float *o, int32_t *evicted,
                        int *dev_status, cudaStream_t st) {
   const int G = Hq / Hkv;
   if (dtype == KV_BF16) {
     if (d == 128)
       return dispatch_g<__nv_bfloat16, 128>(G, q, k_new, v_new, K_cache, V_cache, pos, acc, len, B, Hq,
-                                            Hkv, cap, recent, new_pos, scale, flags, workspace, o,
+                                            Hkv, cap, recent, sink, new_pos, scale, flags, workspace, o,
                                             evicted, dev_status, st);
     return dispatch_g<__nv_bfloat16, 64>(G, q, k_new, v_new, K_cache, V_cache, pos, acc, len, B, Hq,
-                                         Hkv, cap, recent, new_pos, scale, flags, workspace, o,
+                                         Hkv, cap, recent, sink, new_pos, scale, flags, workspace, o,
                                          evicted, dev_status, st);
   }
   if (d == 128)
     return dispatch_g<float, 128>(G, q, k_new, v_new, K_cache, V_cache, pos, acc, len, B, Hq, Hkv,
-                                  cap, recent, new_pos, scale, flags, workspace, o, evicted,
+                                  cap, recent, sink, new_pos, scale, flags, workspace, o, evicted,
                                   dev_status, st);
   return dispatch_g<float, 64>(G, q, k_new, v_new, K_cache, V_cache, pos, acc, len, B, Hq, Hkv,
-                               cap, recent, new_pos, scale, flags, workspace, o, evicted,
+                               cap, recent, sink, new_pos, scale, flags, workspace, o, evicted,
                                dev_status, st);
 }
 

@@ -63,8 +63,8 @@ __global__ __launch_bounds__(NT) void refine_entropy_kernel(const float *__restr
 // One block per batch row: sel_h per head in double (fixed chunk order), the row
 // mean in head order, then beta_h.
 __global__ void refine_beta_kernel(const double2 *__restrict__ part, int H, int T, int n_chunks,
-                                   float beta_lo, float beta_hi, float *__restrict__ beta_ws,
-                                   float *__restrict__ beta_out) {
+                                   float beta_lo, float beta_hi, int fixed_head,
+                                   float *__restrict__ beta_ws, float *__restrict__ beta_out) {
   extern __shared__ double sel[];
   const long b = blockIdx.x;
   const double lnT = log((double)T);
@@ -86,13 +86,14 @@ __global__ void refine_beta_kernel(const double2 *__restrict__ part, int H, int 
   }
   __syncthreads();
   for (int h = threadIdx.x; h < H; h += blockDim.x) {
-    double bt = 1.0;
-    if (mean != 0.0) bt = fmin(fmax(sel[h] / mean, (double)beta_lo), (double)beta_hi);
+    double bt = 1.0;  // also the fixed head weight of the KV_HUB_FIXED_HEAD variant
+    if (mean != 0.0 && !fixed_head) bt = fmin(fmax(sel[h] / mean, (double)beta_lo), (double)beta_hi);
     beta_ws[b * H + h] = (float)bt;
     if (beta_out) beta_out[b * H + h] = (float)bt;
   }
 }
 
+template <bool AVG>
 __global__ __launch_bounds__(NT) void refine_apply_kernel(
     const float *__restrict__ s, int T, int blocks_per_head, int half, float gamma, float r2,
     const float *__restrict__ beta_ws, float *__restrict__ z) {
@@ -112,9 +113,22 @@ __global__ __launch_bounds__(NT) void refine_apply_kernel(
   for (int i = i0 + threadIdx.x; i < i1; i += NT) {
     const int t = i - lo;
     const float si = tile[t];
-    float M = si;
-    for (int o = -half; o <= half; ++o) M = fmaxf(M, tile[t + o]);
-    const float qi = (si == M) ? si : gamma * si;
+    float qi;
+    if constexpr (AVG) {
+      // KV_HUB_AVGPOOL: the mean over the window cut at the ends, summed in window order
+      float sum = 0.f;
+      int cnt = 0;
+      for (int o = -half; o <= half; ++o)
+        if (i + o >= 0 && i + o < T) {
+          sum += tile[t + o];
+          ++cnt;
+        }
+      qi = sum / (float)cnt;
+    } else {
+      float M = si;
+      for (int o = -half; o <= half; ++o) M = fmaxf(M, tile[t + o]);
+      qi = (si == M) ? si : gamma * si;
+    }
     zv[i] = fmaf(r2, fmaf(beta, qi, -si), si);  // s + r^2 (beta q - s)
   }
 }
@@ -131,8 +145,8 @@ RefinePlan plan_refine(int B, int H, int T) {
 }
 
 int launch_hubkv_refine(const float *s, int B, int H, int T, int pool_width, float gamma,
-                        float r, float beta_lo, float beta_hi, float *z, float *beta, void *ws,
-                        const RefinePlan &plan, cudaStream_t st) {
+                        float r, float beta_lo, float beta_hi, int flags, float *z, float *beta,
+                        void *ws, const RefinePlan &plan, cudaStream_t st) {
   const long heads = (long)B * H;
   const int half = pool_width / 2;
   if (half > kMaxHalo) return KV_ERR_UNSUPPORTED;
@@ -141,11 +155,15 @@ int launch_hubkv_refine(const float *s, int B, int H, int T, int pool_width, flo
   refine_entropy_kernel<<<(unsigned)(heads * plan.n_chunks), NT, 0, st>>>(s, T, plan.n_chunks, part);
   const int bt = H < 256 ? ((H + 31) / 32) * 32 : 256;
   refine_beta_kernel<<<(unsigned)B, bt, (size_t)H * sizeof(double), st>>>(
-      part, H, T, plan.n_chunks, beta_lo, beta_hi, beta_ws, beta);
+      part, H, T, plan.n_chunks, beta_lo, beta_hi, (flags & KV_HUB_FIXED_HEAD) ? 1 : 0, beta_ws, beta);
   const int bph = (T + kApply - 1) / kApply;
   const size_t smem = (size_t)(kApply + 2 * half) * sizeof(float);
-  refine_apply_kernel<<<(unsigned)(heads * bph), NT, smem, st>>>(s, T, bph, half, gamma, r * r,
-                                                                beta_ws, z);
+  if (flags & KV_HUB_AVGPOOL)
+    refine_apply_kernel<true><<<(unsigned)(heads * bph), NT, smem, st>>>(s, T, bph, half, gamma, r * r,
+                                                                      beta_ws, z);
+  else
+    refine_apply_kernel<false><<<(unsigned)(heads * bph), NT, smem, st>>>(s, T, bph, half, gamma, r * r,
+                                                                       beta_ws, z);
   return launch_status(3);
 }
 

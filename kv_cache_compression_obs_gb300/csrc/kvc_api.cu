@@ -124,11 +124,12 @@ int kv_score_obs(const void *Q_obs, const void *K, int B, int Hq, int Hkv, int T
                           dev_status, static_cast<cudaStream_t>(stream));
 }
 
-int hubkv_refine(const float *s, int B, int H, int T, int pool_width, float gamma, float r,
-                 float beta_lo, float beta_hi, float *z_out, float *beta_out, void *workspace,
-                 size_t workspace_bytes, kv_stream_t stream) {
+int hubkv_refine_ex(const float *s, int B, int H, int T, int pool_width, float gamma, float r,
+                    float beta_lo, float beta_hi, int flags, float *z_out, float *beta_out,
+                    void *workspace, size_t workspace_bytes, kv_stream_t stream) {
   if (B < 0 || H <= 0 || T <= 0 || pool_width <= 0 || pool_width % 2 == 0 ||
-      !(beta_lo <= beta_hi) || !(gamma == gamma) || !(r == r))
+      !(beta_lo <= beta_hi) || !(gamma == gamma) || !(r == r) ||
+      (flags & ~(KV_HUB_AVGPOOL | KV_HUB_FIXED_HEAD)))
     return KV_ERR_INVALID_ARG;
   if (pool_width > 129) return KV_ERR_UNSUPPORTED;
   if (!fits((long long)B * H, T)) return KV_ERR_INVALID_ARG;
@@ -136,19 +137,32 @@ int hubkv_refine(const float *s, int B, int H, int T, int pool_width, float gamm
   if (!s || !z_out || !aligned16(s) || !aligned16(z_out)) return KV_ERR_INVALID_ARG;
   const RefinePlan plan = plan_refine(B, H, T);
   if (!workspace || workspace_bytes < plan.ws_bytes || !aligned16(workspace)) return KV_ERR_WORKSPACE;
-  return launch_hubkv_refine(s, B, H, T, pool_width, gamma, r, beta_lo, beta_hi, z_out, beta_out,
-                             workspace, plan, static_cast<cudaStream_t>(stream));
+  return launch_hubkv_refine(s, B, H, T, pool_width, gamma, r, beta_lo, beta_hi, flags, z_out,
+                             beta_out, workspace, plan, static_cast<cudaStream_t>(stream));
+}
+
+int hubkv_refine(const float *s, int B, int H, int T, int pool_width, float gamma, float r,
+                 float beta_lo, float beta_hi, float *z_out, float *beta_out, void *workspace,
+                 size_t workspace_bytes, kv_stream_t stream) {
+  return hubkv_refine_ex(s, B, H, T, pool_width, gamma, r, beta_lo, beta_hi, 0, z_out, beta_out,
+                         workspace, workspace_bytes, stream);
+}
+
+int kv_select_topk_ex(const float *z, int B, int H, int T, int k, int recent, int sink,
+                      int32_t *idx_out, void *workspace, size_t workspace_bytes, kv_stream_t stream) {
+  (void)workspace;
+  (void)workspace_bytes;
+  if (B < 0 || H <= 0 || T <= 0 || recent < 0 || sink < 0 || k <= recent + sink || k > T)
+    return KV_ERR_INVALID_ARG;
+  if (!fits((long long)B * H, T)) return KV_ERR_INVALID_ARG;
+  if (B == 0) return KV_OK;
+  if (!z || !idx_out || !aligned16(z) || !aligned16(idx_out)) return KV_ERR_INVALID_ARG;
+  return launch_select_topk(z, B, H, T, k, recent, sink, idx_out, static_cast<cudaStream_t>(stream));
 }
 
 int kv_select_topk(const float *z, int B, int H, int T, int k, int recent, int32_t *idx_out,
                    void *workspace, size_t workspace_bytes, kv_stream_t stream) {
-  (void)workspace;
-  (void)workspace_bytes;
-  if (B < 0 || H <= 0 || T <= 0 || recent < 0 || k <= recent || k > T) return KV_ERR_INVALID_ARG;
-  if (!fits((long long)B * H, T)) return KV_ERR_INVALID_ARG;
-  if (B == 0) return KV_OK;
-  if (!z || !idx_out || !aligned16(z) || !aligned16(idx_out)) return KV_ERR_INVALID_ARG;
-  return launch_select_topk(z, B, H, T, k, recent, idx_out, static_cast<cudaStream_t>(stream));
+  return kv_select_topk_ex(z, B, H, T, k, recent, 0, idx_out, workspace, workspace_bytes, stream);
 }
 
 int kv_compact(const void *K, const void *V, const float *s, const int32_t *idx, int B, int H,
@@ -168,12 +182,12 @@ int kv_compact(const void *K, const void *V, const float *s, const int32_t *idx,
                         cap, pos_out, acc_out, len_out, static_cast<cudaStream_t>(stream));
 }
 
-int h2o_decode_step(const void *q, const void *k_new, const void *v_new, void *K_cache,
+int h2o_decode_step_ex(const void *q, const void *k_new, const void *v_new, void *K_cache,
                     void *V_cache, int32_t *pos, float *acc, int32_t *len, int B, int Hq,
-                    int Hkv, int cap, int d, int recent, int32_t new_pos, float scale,
+                    int Hkv, int cap, int d, int recent, int sink, int32_t new_pos, float scale,
                     int flags, int dtype, float *o_out, int32_t *evicted_pos, void *workspace,
                     size_t workspace_bytes, int *dev_status, kv_stream_t stream) {
-  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || cap <= 0 || recent < 0 ||
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || cap <= 0 || recent < 0 || sink < 0 ||
       recent >= cap || new_pos < 0 || !dtype_ok(dtype) || (flags & ~KV_H2O_ALG1) ||
       ((flags & KV_H2O_ALG1) && recent != 0) || !(scale == scale))
     return KV_ERR_INVALID_ARG;
@@ -192,8 +206,18 @@ int h2o_decode_step(const void *q, const void *k_new, const void *v_new, void *K
       !aligned16(workspace))
     return KV_ERR_WORKSPACE;
   return launch_decode_step(q, k_new, v_new, K_cache, V_cache, pos, acc, len, B, Hq, Hkv, cap,
-                            d, recent, new_pos, scale, flags, dtype, workspace, o_out,
+                            d, recent, sink, new_pos, scale, flags, dtype, workspace, o_out,
                             evicted_pos, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+int h2o_decode_step(const void *q, const void *k_new, const void *v_new, void *K_cache,
+                    void *V_cache, int32_t *pos, float *acc, int32_t *len, int B, int Hq,
+                    int Hkv, int cap, int d, int recent, int32_t new_pos, float scale,
+                    int flags, int dtype, float *o_out, int32_t *evicted_pos, void *workspace,
+                    size_t workspace_bytes, int *dev_status, kv_stream_t stream) {
+  return h2o_decode_step_ex(q, k_new, v_new, K_cache, V_cache, pos, acc, len, B, Hq, Hkv, cap, d,
+                            recent, 0, new_pos, scale, flags, dtype, o_out, evicted_pos, workspace,
+                            workspace_bytes, dev_status, stream);
 }
 
 }  // extern "C"

@@ -88,16 +88,16 @@ int launch_score_obs_tc(const void *Q, const void *K, int B, int Hq, int Hkv, in
                         float scale, float *s, void *ws, const ScorePlan &plan, int *status,
                         cudaStream_t st);
 int launch_hubkv_refine(const float *s, int B, int H, int T, int pool_width, float gamma,
-                        float r, float beta_lo, float beta_hi, float *z, float *beta, void *ws,
-                        const RefinePlan &plan, cudaStream_t st);
-int launch_select_topk(const float *z, int B, int H, int T, int k, int recent, int32_t *idx,
-                       cudaStream_t st);
+                        float r, float beta_lo, float beta_hi, int flags, float *z, float *beta,
+                        void *ws, const RefinePlan &plan, cudaStream_t st);
+int launch_select_topk(const float *z, int B, int H, int T, int k, int recent, int sink,
+                       int32_t *idx, cudaStream_t st);
 int launch_compact(const void *K, const void *V, const float *s, const int32_t *idx, int B,
                    int H, int T, int k, int d, int dtype, void *K_out, void *V_out, int cap,
                    int32_t *pos, float *acc, int32_t *len, cudaStream_t st);
 int launch_decode_step(const void *q, const void *k_new, const void *v_new, void *K_cache,
                        void *V_cache, int32_t *pos, float *acc, int32_t *len, int B, int Hq,
-                       int Hkv, int cap, int d, int recent, int32_t new_pos, float scale,
+                       int Hkv, int cap, int d, int recent, int sink, int32_t new_pos, float scale,
                        int flags, int dtype, void *workspace, float *o, int32_t *evicted,
                        int *dev_status, cudaStream_t st);
 size_t decode_workspace_bytes(long units, int G, int cap, int d);

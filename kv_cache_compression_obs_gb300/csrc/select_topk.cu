@@ -3,6 +3,8 @@
 // H2O page, 双缓冲 and 为什么要按头独立驱逐: every head keeps the last R
 // positions and the k - R best of [0, T - R) in the order (z descending,
 // position ascending); the kept positions are written in ascending order.
+// With S sinks (KV-cache survey blog §4.1-4.2) the first S positions are kept
+// too and the heavy part is the k - R - S best of [S, T - R).
 //
 // One 1024-thread block per head:
 //   1. exact radix select (4 passes of 8 bits over order-preserving uint32
@@ -56,7 +58,7 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_sums, int *
 }
 
 __global__ __launch_bounds__(NT) void select_topk_kernel(const float *__restrict__ z, int T,
-                                                         int k, int R,
+                                                         int k, int R, int S,
                                                          int32_t *__restrict__ idx_out) {
   __shared__ uint32_t hist[NW][256];
   __shared__ uint32_t tot[256];
@@ -64,16 +66,18 @@ __global__ __launch_bounds__(NT) void select_topk_kernel(const float *__restrict
   __shared__ uint32_t sh_prefix;
   __shared__ int sh_need;
   const long head = blockIdx.x;
-  const float *zv = z + head * (long)T;
+  const float *zv = z + head * (long)T + S;  // candidates [S, T - R), indexed from S
   int32_t *out = idx_out + head * (long)k;
-  const int n = T - R;   // candidates [0, n)
-  const int nh = k - R;  // heavy slots
+  const int n = T - R - S;   // candidates
+  const int nh = k - R - S;  // heavy slots
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 
   if (nh >= n) {  // k == T: everything is kept
     for (int m = threadIdx.x; m < k; m += NT) out[m] = m;
     return;
   }
+  for (int m = threadIdx.x; m < S; m += NT) out[m] = m;  // the sinks, first
+  out += S;
 
   uint32_t prefix = 0, mask = 0;
   int need = nh;
@@ -137,20 +141,20 @@ __global__ __launch_bounds__(NT) void select_topk_kernel(const float *__restrict
     const int eq_rank = carry_eq + block_exclusive_scan(eq, warp_sums, &eq_total);
     const int keep = gt || (eq && eq_rank < need);
     const int slot = carry_keep + block_exclusive_scan(keep, warp_sums, &keep_total);
-    if (keep && slot < nh) out[slot] = i;
+    if (keep && slot < nh) out[slot] = S + i;
     carry_eq += eq_total;
     carry_keep += keep_total;
   }
-  for (int m = threadIdx.x; m < R; m += NT) out[nh + m] = n + m;
+  for (int m = threadIdx.x; m < R; m += NT) out[nh + m] = S + n + m;
   (void)lane;
 }
 
 }  // namespace
 
-int launch_select_topk(const float *z, int B, int H, int T, int k, int recent, int32_t *idx,
-                       cudaStream_t st) {
+int launch_select_topk(const float *z, int B, int H, int T, int k, int recent, int sink,
+                       int32_t *idx, cudaStream_t st) {
   const long heads = (long)B * H;
-  select_topk_kernel<<<(unsigned)heads, NT, 0, st>>>(z, T, k, recent, idx);
+  select_topk_kernel<<<(unsigned)heads, NT, 0, st>>>(z, T, k, recent, sink, idx);
   return launch_status();
 }
 

@@ -73,7 +73,7 @@ def _acc_of(pos_after, acc_after, u, p):
 
 
 def decode_lockstep(kvc, oracle_mod, q, kn, vn, Kc, Vc, pos, acc, ln, R, new_pos, scale, flags=0,
-                    rows=None):
+                    rows=None, sink=0):
     """One GPU decode step over all units and one oracle step over the batch rows
     `rows` (all when None), both from the same state.
 
@@ -87,9 +87,9 @@ def decode_lockstep(kvc, oracle_mod, q, kn, vn, Kc, Vc, pos, acc, ln, R, new_pos
     sel = (lambda t: t) if rows is None else (lambda t: t[rows])
     st = [gen.to_numpy_bits(sel(t)).copy() for t in (Kc, Vc, pos, acc, ln)]
     qs, kns, vns = (gen.to_numpy_bits(sel(t)) for t in (q, kn, vn))
-    o, ev = kvc.h2o_decode_step(q, kn, vn, Kc, Vc, pos, acc, ln, R, new_pos, scale, flags)
+    o, ev = kvc.h2o_decode_step(q, kn, vn, Kc, Vc, pos, acc, ln, R, new_pos, scale, flags, sink=sink)
     torch.cuda.synchronize()
-    o_ref, ev_ref = oracle_mod.decode_step(qs, kns, vns, *st, R, new_pos, scale, flags)
+    o_ref, ev_ref = oracle_mod.decode_step(qs, kns, vns, *st, R, new_pos, scale, flags, sink=sink)
     Kr, Vr, pr, ar, lr = st  # updated in place by the oracle
     assert_close(sel(o).cpu().numpy(), o_ref, rtol=RTOL, atol=1e-6, what="o")
     ev_g = sel(ev).cpu().numpy()

@@ -26,6 +26,10 @@ def lib():
     lib.kv_workspace_size.argtypes = [I, I, I, I, I, I, I, I]
     lib.kv_status_string.restype = ctypes.c_char_p
     lib.kv_last_error_detail.restype = ctypes.c_char_p
+    lib.hubkv_refine_ex.argtypes = [P, I, I, I, I, F, F, F, F, I, P, P, P, Z, P]
+    lib.kv_select_topk_ex.argtypes = [P, I, I, I, I, I, I, P, P, Z, P]
+    lib.h2o_decode_step_ex.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I, P, P,
+                                       P, Z, P, P]
     return lib
 
 
@@ -89,6 +93,20 @@ def test_host_validation_rejects_before_cuda(lib):
     p = ctypes.c_void_p(16)  # a dummy aligned pointer: never dereferenced, the call is rejected first
     assert lib.h2o_decode_step(p, p, p, p, p, p, p, p, 1, 12, 4, 8, 64, 1, 9, 0.1, 0, 0, p, p, NULL,
                                0, NULL, NULL) == -2
+
+
+def test_extended_entry_points_validate_on_the_host(lib):
+    # refine: an unknown variant flag
+    assert lib.hubkv_refine_ex(NULL, 1, 2, 10, 5, 0.5, 0.1, 0.8, 1.2, 4, NULL, NULL, NULL, 0, NULL) == -1
+    # select: negative sink, sinks + recent filling the budget
+    assert lib.kv_select_topk_ex(NULL, 1, 2, 10, 5, 1, -1, NULL, NULL, 0, NULL) == -1
+    assert lib.kv_select_topk_ex(NULL, 1, 2, 10, 5, 2, 3, NULL, NULL, 0, NULL) == -1
+    # decode: negative sink
+    assert lib.h2o_decode_step_ex(NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL, 1, 4, 4, 8, 64, 1, -1,
+                                  9, 0.1, 0, 0, NULL, NULL, NULL, 0, NULL, NULL) == -1
+    # empty batches are no-ops
+    assert lib.hubkv_refine_ex(NULL, 0, 2, 10, 5, 0.5, 0.1, 0.8, 1.2, 3, NULL, NULL, NULL, 0, NULL) == 0
+    assert lib.kv_select_topk_ex(NULL, 0, 2, 10, 5, 1, 2, NULL, NULL, 0, NULL) == 0
 
 
 def test_empty_batch_is_a_no_op(lib):

@@ -1,0 +1,91 @@
+"""GPU parity for the variants beyond the five core steps: attention sinks in
+Top-K and the decode step (KV-cache survey blog §4.1-4.2), and the HubKV
+comparison variants (HubKV walkthrough, 尝试路线：效果一般的可能原因)."""
+import numpy as np
+import pytest
+import torch
+
+from _parity import RTOL, assert_close, decode_lockstep
+from kv_cache_compression_obs_gb300 import gen
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.mark.parametrize("T,k,R,S", [(10, 5, 2, 2), (10, 10, 2, 3), (4096, 409, 32, 4),
+                                     (8192, 1638, 819, 16), (3001, 300, 0, 5), (131072, 6553, 64, 4),
+                                     (777, 100, 1, 98)])
+@pytest.mark.parametrize("ties", [False, True])
+def test_select_topk_sinks_bit_exact(kvc, oracle_mod, T, k, R, S, ties):
+    B, H = 2, 3
+    g = torch.Generator(device=DEV)
+    g.manual_seed(T + k + S)
+    z = torch.rand(B, H, T, generator=g, device=DEV)
+    if ties:
+        z = torch.floor(z * 7) / 7
+        z[0, 0, ::5] = -0.0
+        z[0, 0, 1::5] = 0.0
+    z[..., :S] = -1.0  # sinks the scores alone would drop
+    idx = kvc.kv_select_topk(z, k, R, sink=S)
+    torch.cuda.synchronize()
+    ref = oracle_mod.select_topk(z.cpu().numpy().astype(np.float64), k, R, sink=S)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref)
+    assert (idx[..., :S].cpu() == torch.arange(S, dtype=torch.int32)).all()
+
+
+def _scores(B, H, T, seed):
+    g = torch.Generator(device=DEV)
+    g.manual_seed(seed)
+    s = torch.rand(B, H, T, generator=g, device=DEV) ** 4
+    return (s / s.sum(-1, keepdim=True) * 8).contiguous()
+
+
+@pytest.mark.parametrize("flags", [1, 2, 3])
+@pytest.mark.parametrize("shape", [(1, 1, 1), (1, 2, 3), (2, 8, 32768), (1, 4, 10001)])
+@pytest.mark.parametrize("r", [0.1, 0.9])
+def test_hubkv_variants(kvc, oracle_mod, flags, shape, r):
+    B, H, T = shape
+    s = _scores(B, H, T, seed=T + H + flags)
+    z, beta = kvc.hubkv_refine(s, r, flags=flags)
+    torch.cuda.synchronize()
+    z_ref, beta_ref, _ = oracle_mod.hubkv_refine(s.cpu().numpy().astype(np.float64), r, flags=flags)
+    assert_close(beta.cpu().numpy(), beta_ref, rtol=1e-6, atol=0, what="beta")
+    assert_close(z.cpu().numpy(), z_ref, rtol=RTOL, atol=1e-30, what="z")
+    if flags & kvc.KV_HUB_FIXED_HEAD:
+        assert torch.all(beta == 1.0)
+
+
+def test_hubkv_variant_flags_rejected(kvc):
+    s = _scores(1, 2, 64, seed=1)
+    with pytest.raises(kvc.KvcError):
+        kvc.hubkv_refine(s, 0.5, flags=4)
+
+
+@pytest.mark.parametrize("G,dt,d,R,S", [(4, "bf16", 128, 8, 4), (1, "f32", 64, 0, 2), (8, "bf16", 64, 3, 1),
+                                        (2, "bf16", 128, 0, 6)])
+def test_decode_lockstep_sinks(kvc, oracle_mod, G, dt, d, R, S):
+    B, Hkv, cap, T0, steps = 2, 3, 40, 200, 30
+    Hq = G * Hkv
+    tdt = torch.bfloat16 if dt == "bf16" else torch.float32
+    g = torch.Generator(device=DEV)
+    g.manual_seed(G * 100 + d + R + S)
+    Kc = torch.randn(B, Hkv, cap, d, generator=g, device=DEV).to(tdt)
+    Vc = torch.randn(B, Hkv, cap, d, generator=g, device=DEV).to(tdt)
+    pos = torch.stack([torch.sort(torch.randperm(T0 - S, generator=g, device=DEV)[:cap - S] + S).values
+                       for _ in range(B * Hkv)]).reshape(B, Hkv, cap - S).to(torch.int32)
+    pos = torch.cat([torch.arange(S, dtype=torch.int32, device=DEV).expand(B, Hkv, S), pos], -1).contiguous()
+    acc = (torch.rand(B, Hkv, cap, generator=g, device=DEV) * 2).contiguous()
+    acc[..., :S] = 0.0   # the sinks score lowest: only the protection keeps them
+    ln = torch.full((B, Hkv), cap, dtype=torch.int32, device=DEV)
+    scale = d ** -0.5
+    exact = 0
+    for step in range(steps):
+        q = torch.randn(B, Hq, d, generator=g, device=DEV).to(tdt)
+        kn = torch.randn(B, Hkv, d, generator=g, device=DEV).to(tdt)
+        vn = torch.randn(B, Hkv, d, generator=g, device=DEV).to(tdt)
+        exact += decode_lockstep(kvc, oracle_mod, q, kn, vn, Kc, Vc, pos, acc, ln, R, T0 + step, scale,
+                                 sink=S)
+        for s in range(S):
+            assert bool((pos == s).any(-1).all()), "a sink was evicted"
+    assert exact >= steps - 2
