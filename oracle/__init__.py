@@ -39,6 +39,10 @@ def _load():
         lib.oracle_select_topk_ex.argtypes = [P, I, I, I, I, I, I, P]
         lib.oracle_compact.restype = I
         lib.oracle_compact.argtypes = [P, P, P, P, I, I, I, I, I, I, P, P, I, P, P, P]
+        lib.oracle_select_budget.restype = I
+        lib.oracle_select_budget.argtypes = [P, I, I, I, I, I, I, I, P, P]
+        lib.oracle_compact_ragged.restype = I
+        lib.oracle_compact_ragged.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, P, I, P, P, P]
         lib.oracle_decode_step_ex.restype = I
         lib.oracle_decode_step_ex.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, D, I, I, P, P]
         _lib = lib
@@ -128,6 +132,47 @@ def compact(K: np.ndarray, V: np.ndarray, s, idx: np.ndarray, cap: int):
     return K_out, V_out, pos, acc, ln
 
 
+def select_budget(z: np.ndarray, budget: int, floor: int, recent: int, sink: int = 0):
+    """Layer-level competitive budget: z [B][H][T] (read as float64), one layer per
+    batch row -> (idx [B][budget] int32, off [B][H+1] int32), CSR per head."""
+    z = np.ascontiguousarray(z, dtype=np.float64)
+    B, H, T = z.shape
+    idx = np.zeros((B, budget), dtype=np.int32)
+    off = np.zeros((B, H + 1), dtype=np.int32)
+    rc = _load().oracle_select_budget(_ptr(z), B, H, T, int(budget), int(floor), int(recent),
+                                      int(sink), _ptr(idx), _ptr(off))
+    if rc != 0:
+        raise ValueError("oracle_select_budget rejected its inputs")
+    return idx, off
+
+
+def compact_ragged(K: np.ndarray, V: np.ndarray, s, idx: np.ndarray, off: np.ndarray, cap: int,
+                   out=None):
+    """Gather head h's rows idx[b][off[b][h]:off[b][h+1]] into slots 0..n-1.
+
+    Returns (K_out, V_out, pos, acc, len); `out` (the same five arrays) is written
+    in place when given, so untouched slots keep their contents."""
+    B, H, T, d = K.shape
+    budget = idx.shape[-1]
+    K = np.ascontiguousarray(K)
+    V = np.ascontiguousarray(V)
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    off = np.ascontiguousarray(off, dtype=np.int32)
+    if out is None:
+        out = (np.zeros((B, H, cap, d), dtype=K.dtype), np.zeros((B, H, cap, d), dtype=V.dtype),
+               np.zeros((B, H, cap), dtype=np.int32), np.zeros((B, H, cap), dtype=np.float32),
+               np.zeros((B, H), dtype=np.int32))
+    K_out, V_out, pos, acc, ln = out
+    s_arr = None if s is None else np.ascontiguousarray(s, dtype=np.float64)
+    rc = _load().oracle_compact_ragged(_ptr(K), _ptr(V), None if s_arr is None else _ptr(s_arr),
+                                       _ptr(idx), _ptr(off), B, H, T, budget, d, _dtype_code(K),
+                                       _ptr(K_out), _ptr(V_out), int(cap), _ptr(pos), _ptr(acc),
+                                       _ptr(ln))
+    if rc != 0:
+        raise ValueError("oracle_compact_ragged rejected its inputs")
+    return K_out, V_out, pos, acc, ln
+
+
 def decode_step(q, k_new, v_new, K_cache, V_cache, pos, acc, ln, recent: int, new_pos: int,
                 scale: float, flags: int = 0, sink: int = 0):
     """One decode step; K_cache, V_cache, pos, acc, ln are updated IN PLACE.
@@ -160,7 +205,8 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
 
 
 __all__ = ["BF16", "F32", "FLAG_ALG1", "kv_cache_bytes", "score_obs", "hubkv_refine",
-           "select_topk", "compact", "decode_step", "bf16_bits_to_f64"]
+           "select_topk", "compact", "select_budget", "compact_ragged", "decode_step",
+           "bf16_bits_to_f64"]
 
 from .alg1 import h2o_greedy_literal  # noqa: E402
 

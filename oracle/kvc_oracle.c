@@ -22,7 +22,9 @@
  *            head calibration, ratio gate).
  *   [KVblog] KV-cache survey blog, §1.1 (scaled dot-product attention with
  *            1/sqrt(d_head)), §1.3 (KV-cache size), §3.3 (GQA), §4.3 (SnapKV
- *            prefill observation window).
+ *            prefill observation window), §4.4 (PyramidKV per-layer budgets).
+ *   [NestedKV] "Technische Samenvatting: NestedKV", section 3. Hoofd-gewijze
+ *            Geheugentoewijzing (competitive head-wise budget).
  *
  * Readings taken where the pages are silent (each one is listed in the design
  * notes as well):
@@ -300,6 +302,131 @@ int oracle_compact(const void *K, const void *V, const double *s, const int32_t 
       if (s && acc_out) acc_out[u * (long long)cap + m] = (float)s[u * (long long)T + j];
     }
     len_out[u] = k;
+  }
+  return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Layer-level competitive budget ([NestedKV] 3. Hoofd-gewijze
+ * Geheugentoewijzing: the (token, head) pairs with the highest scores across
+ * the layer win, subject to a per-head minimum; [KVblog] §4.4 PyramidKV: the
+ * budget belongs to the layer rather than to each head).
+ * Batch row b is one layer; its H heads share `budget` kept positions:
+ *   1. every head keeps its sinks [0, sink) and its recent window [T-recent, T);
+ *   2. floor: every head keeps its floor - sink - recent best positions of
+ *      [sink, T-recent) in the order (z descending, position ascending), so that
+ *      each head keeps at least `floor` positions;
+ *   3. competition: the budget - H*floor slots left go to the best of the row's
+ *      (head, position) pairs with position in [sink, T-recent) not kept yet, in
+ *      the order (z descending, head ascending, position ascending).
+ * Output, CSR: head h of row b kept positions idx[b][off[b][h] .. off[b][h+1]-1]
+ * in ascending order; off[b][0] = 0 and off[b][H] = budget.
+ * Steps 2-3 give the largest score sum over all sets that keep the protected
+ * positions, at least `floor` per head and `budget` in all.
+ * z [B][H][T]; idx [B][budget]; off [B][H+1].
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  double z;
+  int head;
+  int pos;
+} or_pair;
+
+static int or_cmp_pair_desc(const void *a, const void *b) {
+  const or_pair *x = (const or_pair *)a, *y = (const or_pair *)b;
+  if (x->z > y->z) return -1;
+  if (x->z < y->z) return 1;
+  if (x->head != y->head) return (x->head > y->head) - (x->head < y->head);
+  return (x->pos > y->pos) - (x->pos < y->pos);
+}
+
+int oracle_select_budget(const double *z, int B, int H, int T, int budget, int floor_k,
+                         int recent, int sink, int32_t *idx_out, int32_t *off_out) {
+  if (B < 0 || H <= 0 || T <= 0 || recent < 0 || sink < 0 || floor_k < 1 ||
+      floor_k < recent + sink || floor_k > T || budget < (long long)H * floor_k ||
+      budget > (long long)H * T)
+    return -1;
+  const int n = T - recent - sink, nf = floor_k - recent - sink;
+  or_cand *c = (or_cand *)malloc(sizeof(or_cand) * (size_t)(n > 0 ? n : 1));
+  or_pair *pool = (or_pair *)malloc(sizeof(or_pair) * (size_t)H * (size_t)(n > 0 ? n : 1));
+  unsigned char *kept = (unsigned char *)malloc((size_t)H * (size_t)T);
+  if (!c || !pool || !kept) {
+    free(c);
+    free(pool);
+    free(kept);
+    return -1;
+  }
+  for (int b = 0; b < B; ++b) {
+    memset(kept, 0, (size_t)H * (size_t)T);
+    long long np = 0;
+    for (int h = 0; h < H; ++h) {
+      const double *zv = z + ((long long)b * H + h) * T;
+      unsigned char *kh = kept + (size_t)h * T;
+      for (int m = 0; m < sink; ++m) kh[m] = 1;                  /* step 1 */
+      for (int m = T - recent; m < T; ++m) kh[m] = 1;
+      for (int i = 0; i < n; ++i) {
+        c[i].z = zv[sink + i];
+        c[i].pos = sink + i;
+      }
+      qsort(c, (size_t)n, sizeof(or_cand), or_cmp_desc);
+      for (int m = 0; m < nf; ++m) kh[c[m].pos] = 1;             /* step 2 */
+      for (int m = nf; m < n; ++m) {
+        pool[np].z = c[m].z;
+        pool[np].head = h;
+        pool[np].pos = c[m].pos;
+        ++np;
+      }
+    }
+    qsort(pool, (size_t)np, sizeof(or_pair), or_cmp_pair_desc);
+    const long long extra = (long long)budget - (long long)H * floor_k;
+    for (long long m = 0; m < extra; ++m)                         /* step 3 */
+      kept[(size_t)pool[m].head * T + pool[m].pos] = 1;
+    int32_t *ib = idx_out + (long long)b * budget;
+    int32_t *ob = off_out + (long long)b * (H + 1);
+    int w = 0;
+    for (int h = 0; h < H; ++h) {
+      ob[h] = w;
+      for (int p = 0; p < T; ++p)
+        if (kept[(size_t)h * T + p]) ib[w++] = p;
+    }
+    ob[H] = w;
+  }
+  free(c);
+  free(pool);
+  free(kept);
+  return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Ragged gather-compaction: Step 4 for the per-head counts that the layer
+ * budget produces.  Head h of row b keeps n = off[b][h+1] - off[b][h] rows:
+ *   K_out[m] = K[idx[off + m]], V_out[m] = V[idx[off + m]], pos[m] = idx[off + m],
+ *   acc[m] = s[idx[off + m]], len = n, for m < n; slots n..cap-1 untouched.
+ * K, V [B][H][T][d]; idx [B][budget]; off [B][H+1]; K_out, V_out [B][H][cap][d];
+ * pos, acc [B][H][cap]; len [B][H].  Returns -1 when an offset or an index is out
+ * of range or a head keeps more than cap rows.
+ * ------------------------------------------------------------------------- */
+int oracle_compact_ragged(const void *K, const void *V, const double *s, const int32_t *idx,
+                          const int32_t *off, int B, int H, int T, int budget, int d, int dtype,
+                          void *K_out, void *V_out, int cap, int32_t *pos_out, float *acc_out,
+                          int32_t *len_out) {
+  if (B < 0 || H <= 0 || T <= 0 || budget < 0 || d <= 0 || cap < 0) return -1;
+  const size_t row = (size_t)d * or_elem_bytes(dtype);
+  for (int b = 0; b < B; ++b) {
+    const int32_t *ob = off + (long long)b * (H + 1);
+    for (int h = 0; h < H; ++h) {
+      const long long u = (long long)b * H + h;
+      const int lo = ob[h], hi = ob[h + 1];
+      if (lo < 0 || hi < lo || hi > budget || hi - lo > cap) return -1;
+      for (int m = 0; m < hi - lo; ++m) {
+        const int j = idx[(long long)b * budget + lo + m];
+        if (j < 0 || j >= T) return -1;
+        memcpy((char *)K_out + ((size_t)u * cap + m) * row, (const char *)K + ((size_t)u * T + j) * row, row);
+        memcpy((char *)V_out + ((size_t)u * cap + m) * row, (const char *)V + ((size_t)u * T + j) * row, row);
+        pos_out[u * cap + m] = j;
+        if (s && acc_out) acc_out[u * cap + m] = (float)s[u * (long long)T + j];
+      }
+      len_out[u] = hi - lo;
+    }
   }
   return 0;
 }
