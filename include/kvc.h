@@ -7,11 +7,15 @@
  *   kv_select_topk   budgeted per-head Top-K with a protected recent window
  *   kv_compact       gather-compaction of the kept K/V rows into a slot cache
  *   h2o_decode_step  one decode step: attention, score accumulation, <= 1 eviction
+ * and, beyond those five, a layer-level budget shared by the heads of a layer
+ * (kv_select_budget, kv_compact_ragged) and the _ex variants (sinks, HubKV
+ * comparison variants).
  *
  * Sources (page title, section):
  *   [H2O]    "H2O 完全拆解：抓住 KV Cache 里的「重击者」，20% 预算无损生成（NeurIPS 2023）"
  *   [HubKV]  "HubKV walkthrough"
  *   [KVblog] the KV-cache survey blog (famous-torrone-8bc255.netlify.app/posts/kv_cache)
+ *   [NestedKV] "Technische Samenvatting: NestedKV" (gist.science summary)
  *
  * Conventions shared by every call
  *   - Every pointer argument is DEVICE memory owned by the caller (allocate it
@@ -190,6 +194,59 @@ KVC_API int kv_select_topk_ex(const float *z, int B, int H, int T, int k, int re
 KVC_API int kv_compact(const void *K, const void *V, const float *s, const int32_t *idx, int B, int H,
                int T, int k, int d, int dtype, void *K_out, void *V_out, int cap,
                int32_t *pos_out, float *acc_out, int32_t *len_out, kv_stream_t stream);
+
+/*
+ * kv_select_budget -- layer-level competitive budget: the heads of one layer
+ * share one budget ([NestedKV] 3. Hoofd-gewijze Geheugentoewijzing: the
+ * (token, head) pairs with the highest scores across the layer win, every head
+ * keeping a minimum; [KVblog] §4.4 PyramidKV: budgets per layer, not per head).
+ * Batch row b is one layer (fold batch x layers into B); its H heads keep
+ * `budget` positions in all:
+ *   1. every head keeps its sinks [0, sink) and its recent window [T-recent, T);
+ *   2. floor: every head keeps its floor_k - sink - recent best positions of
+ *      [sink, T-recent) in the order (z descending, position ascending), so each
+ *      head keeps at least floor_k;
+ *   3. competition: the budget - H*floor_k slots left go to the best of the
+ *      row's (head, position) pairs with position in [sink, T-recent) not kept
+ *      yet, in the order (z descending, head ascending, position ascending).
+ * Steps 2-3 keep the largest score sum among all sets that keep the protected
+ * positions, at least floor_k per head and budget in all.  The result is exact:
+ * the same z gives the same output bit for bit.
+ *
+ *   z          [B][H][T] float32 (finite; -0.0 is treated as +0.0), 16-byte aligned
+ *   idx_out    [B][budget] int32: head h's kept positions, ascending, at
+ *              idx_out[b][off_out[b][h] .. off_out[b][h+1]-1]
+ *   off_out    [B][H+1] int32: off_out[b][0] = 0, off_out[b][H] = budget
+ * Preconditions: 0 <= sink, 0 <= recent, max(1, sink + recent) <= floor_k <= T,
+ * H*floor_k <= budget <= H*T.  H <= 256 and H*T < 2^31 (else KV_ERR_UNSUPPORTED).
+ * No workspace.  Runs one thread-block cluster of min(H, 8) CTAs per row.
+ */
+KVC_API int kv_select_budget(const float *z, int B, int H, int T, int budget, int floor_k,
+                             int recent, int sink, int32_t *idx_out, int32_t *off_out,
+                             kv_stream_t stream);
+
+/*
+ * kv_compact_ragged -- kv_compact for the per-head counts of kv_select_budget.
+ * Head h of row b keeps n = off[b][h+1] - off[b][h] rows: for m < n,
+ *     K_out[m] = K[idx[b][off[b][h] + m]], V_out[m] = V[...], pos_out[m] = that
+ *     index, acc_out[m] = s[that index],
+ * and len_out = n; slots n..cap-1 are not touched.  The copy is bit-exact.
+ *
+ *   K, V       [B][H][T][d];  s [B][H][T] float32, may be NULL (acc_out not written)
+ *   idx        [B][budget] int32;  off [B][H+1] int32 (CSR, as kv_select_budget writes)
+ *   K_out, V_out [B][H][cap][d];  pos_out, acc_out [B][H][cap];  len_out [B][H]
+ *   dev_status device int, may be NULL; set to KV_ERR_INVALID_ARG when a row's
+ *              offsets are not non-decreasing within [0, budget] (that row is left
+ *              untouched) or a head keeps more than cap rows (that head is left
+ *              untouched); never cleared.  An index outside [0, T) leaves its slot
+ *              untouched.
+ * Preconditions: d in {64, 128}, H <= 256; acc_out may be NULL.
+ */
+KVC_API int kv_compact_ragged(const void *K, const void *V, const float *s, const int32_t *idx,
+                              const int32_t *off, int B, int H, int T, int budget, int d,
+                              int dtype, void *K_out, void *V_out, int cap, int32_t *pos_out,
+                              float *acc_out, int32_t *len_out, int *dev_status,
+                              kv_stream_t stream);
 
 /*
  * h2o_decode_step -- one decode step of the H2O eviction policy over a slot

@@ -1,4 +1,4 @@
-"""Python binding of libkvc.so: the same five calls, argument marshalling only.
+"""Python binding of libkvc.so: the same calls, argument marshalling only.
 
 Every function takes CUDA torch tensors, checks dtype/shape/contiguity, passes
 raw device pointers and the current CUDA stream to the C ABI, and raises
@@ -44,6 +44,11 @@ _lib.kv_select_topk_ex.restype = _I
 _lib.kv_select_topk_ex.argtypes = [_P, _I, _I, _I, _I, _I, _I, _P, _P, _Z, _P]
 _lib.kv_compact.restype = _I
 _lib.kv_compact.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P]
+_lib.kv_select_budget.restype = _I
+_lib.kv_select_budget.argtypes = [_P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]
+_lib.kv_compact_ragged.restype = _I
+_lib.kv_compact_ragged.argtypes = [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P,
+                                   _P, _P, _P]
 _lib.h2o_decode_step.restype = _I
 _lib.h2o_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F,
                                  _I, _I, _P, _P, _P, _Z, _P, _P]
@@ -203,6 +208,49 @@ def kv_compact(K: torch.Tensor, V: torch.Tensor, s, idx: torch.Tensor, cap: int 
                                          _dtype_code(K), _ptr(K_out), _ptr(V_out), int(cap),
                                          _ptr(pos), _ptr(acc if s is not None else None), _ptr(ln),
                                          _stream(stream)))
+    return K_out, V_out, pos, acc, ln
+
+
+def kv_select_budget(z: torch.Tensor, budget: int, floor: int, recent: int, sink: int = 0,
+                     idx_out=None, off_out=None, stream=None):
+    """Layer-level competitive budget: z [B][H][T] float32, one layer per batch row
+    -> (idx [B][budget] int32, off [B][H+1] int32): head h's kept positions,
+    ascending, are idx[b][off[b][h]:off[b][h+1]]."""
+    B, H, T = z.shape
+    if z.dtype != torch.float32:
+        raise TypeError("z must be float32")
+    _dev(z, idx_out, off_out)
+    dev = z.device
+    idx = idx_out if idx_out is not None else torch.empty(B, budget, dtype=torch.int32, device=dev)
+    off = off_out if off_out is not None else torch.empty(B, H + 1, dtype=torch.int32, device=dev)
+    _check("kv_select_budget", _lib.kv_select_budget(_ptr(z), B, H, T, int(budget), int(floor),
+                                                     int(recent), int(sink), _ptr(idx), _ptr(off),
+                                                     _stream(stream)))
+    return idx, off
+
+
+def kv_compact_ragged(K: torch.Tensor, V: torch.Tensor, s, idx: torch.Tensor, off: torch.Tensor,
+                      cap: int, K_out=None, V_out=None, pos_out=None, acc_out=None, len_out=None,
+                      dev_status=None, stream=None):
+    """Gather each head's CSR rows (kv_select_budget's output) into its slots
+    0..n-1 of a slot cache; returns (K_out, V_out, pos, acc, len)."""
+    B, H, T, d = K.shape
+    budget = idx.shape[-1]
+    if idx.dtype != torch.int32 or off.dtype != torch.int32 or V.shape != K.shape or V.dtype != K.dtype:
+        raise ValueError("idx and off must be int32 and V must match K")
+    if tuple(off.shape) != (B, H + 1) or idx.shape[0] != B:
+        raise ValueError("idx must be [B][budget] and off [B][H+1]")
+    _dev(K, V, s, idx, off, K_out, V_out, pos_out, acc_out, len_out, dev_status)
+    dev = K.device
+    K_out = K_out if K_out is not None else torch.empty(B, H, cap, d, dtype=K.dtype, device=dev)
+    V_out = V_out if V_out is not None else torch.empty(B, H, cap, d, dtype=K.dtype, device=dev)
+    pos = pos_out if pos_out is not None else torch.zeros(B, H, cap, dtype=torch.int32, device=dev)
+    acc = acc_out if acc_out is not None else torch.zeros(B, H, cap, dtype=torch.float32, device=dev)
+    ln = len_out if len_out is not None else torch.empty(B, H, dtype=torch.int32, device=dev)
+    _check("kv_compact_ragged", _lib.kv_compact_ragged(
+        _ptr(K), _ptr(V), _ptr(s), _ptr(idx), _ptr(off), B, H, T, budget, d, _dtype_code(K),
+        _ptr(K_out), _ptr(V_out), int(cap), _ptr(pos), _ptr(acc if s is not None else None),
+        _ptr(ln), _ptr(dev_status), _stream(stream)))
     return K_out, V_out, pos, acc, ln
 
 

@@ -182,6 +182,44 @@ int kv_compact(const void *K, const void *V, const float *s, const int32_t *idx,
                         cap, pos_out, acc_out, len_out, static_cast<cudaStream_t>(stream));
 }
 
+int kv_select_budget(const float *z, int B, int H, int T, int budget, int floor_k, int recent,
+                     int sink, int32_t *idx_out, int32_t *off_out, kv_stream_t stream) {
+  if (B < 0 || H <= 0 || T <= 0 || recent < 0 || sink < 0 || floor_k < 1 ||
+      floor_k < recent + sink || floor_k > T || (long long)budget < (long long)H * floor_k ||
+      (long long)budget > (long long)H * T)
+    return KV_ERR_INVALID_ARG;
+  if (H > 256 || (long long)H * T > INT_MAX) return KV_ERR_UNSUPPORTED;
+  if (!fits(B, budget)) return KV_ERR_INVALID_ARG;
+  if (B == 0) return KV_OK;
+  if (!z || !idx_out || !off_out || !aligned16(z) || ((uintptr_t)idx_out & 3u) ||
+      ((uintptr_t)off_out & 3u))
+    return KV_ERR_INVALID_ARG;
+  return launch_select_budget(z, B, H, T, budget, floor_k, recent, sink, idx_out, off_out,
+                              static_cast<cudaStream_t>(stream));
+}
+
+int kv_compact_ragged(const void *K, const void *V, const float *s, const int32_t *idx,
+                      const int32_t *off, int B, int H, int T, int budget, int d, int dtype,
+                      void *K_out, void *V_out, int cap, int32_t *pos_out, float *acc_out,
+                      int32_t *len_out, int *dev_status, kv_stream_t stream) {
+  if (B < 0 || H <= 0 || T <= 0 || budget < 0 || cap < 0 || !dtype_ok(dtype))
+    return KV_ERR_INVALID_ARG;
+  if (!dim_ok(d)) return KV_ERR_UNSUPPORTED;
+  if (H > 256) return KV_ERR_UNSUPPORTED;
+  if (!fits((long long)B * H, (long long)T * d) || !fits((long long)B * H, (long long)cap * d) ||
+      !fits(B, budget))
+    return KV_ERR_INVALID_ARG;
+  if (B == 0) return KV_OK;
+  if (!K || !V || !idx || !off || !K_out || !V_out || !pos_out || !len_out)
+    return KV_ERR_INVALID_ARG;
+  if (!aligned16(K) || !aligned16(V) || !aligned16(K_out) || !aligned16(V_out) ||
+      (s && ((uintptr_t)s & 3u)) || (acc_out && ((uintptr_t)acc_out & 3u)))
+    return KV_ERR_INVALID_ARG;
+  return launch_compact_ragged(K, V, acc_out ? s : nullptr, idx, off, B, H, T, budget, d, dtype,
+                               K_out, V_out, cap, pos_out, acc_out, len_out, dev_status,
+                               static_cast<cudaStream_t>(stream));
+}
+
 int h2o_decode_step_ex(const void *q, const void *k_new, const void *v_new, void *K_cache,
                     void *V_cache, int32_t *pos, float *acc, int32_t *len, int B, int Hq,
                     int Hkv, int cap, int d, int recent, int sink, int32_t new_pos, float scale,

@@ -95,6 +95,12 @@ int launch_select_topk(const float *z, int B, int H, int T, int k, int recent, i
 int launch_compact(const void *K, const void *V, const float *s, const int32_t *idx, int B,
                    int H, int T, int k, int d, int dtype, void *K_out, void *V_out, int cap,
                    int32_t *pos, float *acc, int32_t *len, cudaStream_t st);
+int launch_select_budget(const float *z, int B, int H, int T, int budget, int floor_k,
+                         int recent, int sink, int32_t *idx, int32_t *off, cudaStream_t st);
+int launch_compact_ragged(const void *K, const void *V, const float *s, const int32_t *idx,
+                          const int32_t *off, int B, int H, int T, int budget, int d, int dtype,
+                          void *K_out, void *V_out, int cap, int32_t *pos, float *acc,
+                          int32_t *len, int *status, cudaStream_t st);
 int launch_decode_step(const void *q, const void *k_new, const void *v_new, void *K_cache,
                        void *V_cache, int32_t *pos, float *acc, int32_t *len, int B, int Hq,
                        int Hkv, int cap, int d, int recent, int sink, int32_t new_pos, float scale,

@@ -16,46 +16,13 @@
 //   3. the recent window is appended.
 // Integer work only after the key transform: the same z always gives the same idx.
 #include "kvc_internal.cuh"
+#include "select_common.cuh"
 
 namespace kvc {
 namespace {
 
 constexpr int NT = 1024;
 constexpr int NW = NT / 32;
-
-// Monotone map float -> uint32 (larger float, larger key); -0.0 maps like +0.0.
-__device__ __forceinline__ uint32_t order_key(float f) {
-  uint32_t u = __float_as_uint(f);
-  if (u == 0x80000000u) u = 0u;
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-// Exclusive block-wide prefix sum of one int per thread; *total gets the sum.
-__device__ __forceinline__ int block_exclusive_scan(int v, int *warp_sums, int *total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int y = __shfl_up_sync(0xFFFFFFFFu, x, off);
-    if (lane >= off) x += y;
-  }
-  if (lane == 31) warp_sums[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = (lane < NW) ? warp_sums[lane] : 0;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(0xFFFFFFFFu, w, off);
-      if (lane >= off) w += y;
-    }
-    if (lane < NW) warp_sums[lane] = w;  // inclusive over warps
-  }
-  __syncthreads();
-  const int before = (warp > 0) ? warp_sums[warp - 1] : 0;
-  *total = warp_sums[NW - 1];
-  __syncthreads();  // warp_sums is reused by the next call
-  return before + x - v;
-}
 
 __global__ __launch_bounds__(NT) void select_topk_kernel(const float *__restrict__ z, int T,
                                                          int k, int R, int S,
@@ -138,9 +105,9 @@ __global__ __launch_bounds__(NT) void select_topk_kernel(const float *__restrict
     const int gt = (i < n) && (u > ustar);
     const int eq = (i < n) && (u == ustar);
     int eq_total, keep_total;
-    const int eq_rank = carry_eq + block_exclusive_scan(eq, warp_sums, &eq_total);
+    const int eq_rank = carry_eq + block_exclusive_scan<NT>(eq, warp_sums, &eq_total);
     const int keep = gt || (eq && eq_rank < need);
-    const int slot = carry_keep + block_exclusive_scan(keep, warp_sums, &keep_total);
+    const int slot = carry_keep + block_exclusive_scan<NT>(keep, warp_sums, &keep_total);
     if (keep && slot < nh) out[slot] = S + i;
     carry_eq += eq_total;
     carry_keep += keep_total;

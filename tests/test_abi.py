@@ -30,6 +30,8 @@ def lib():
     lib.kv_select_topk_ex.argtypes = [P, I, I, I, I, I, I, P, P, Z, P]
     lib.h2o_decode_step_ex.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I, P, P,
                                        P, Z, P, P]
+    lib.kv_select_budget.argtypes = [P, I, I, I, I, I, I, I, P, P, P]
+    lib.kv_compact_ragged.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, P, I, P, P, P, P, P]
     return lib
 
 
@@ -107,6 +109,28 @@ def test_extended_entry_points_validate_on_the_host(lib):
     # empty batches are no-ops
     assert lib.hubkv_refine_ex(NULL, 0, 2, 10, 5, 0.5, 0.1, 0.8, 1.2, 3, NULL, NULL, NULL, 0, NULL) == 0
     assert lib.kv_select_topk_ex(NULL, 0, 2, 10, 5, 1, 2, NULL, NULL, 0, NULL) == 0
+
+
+def test_layer_budget_entry_points_validate_on_the_host(lib):
+    sel = lambda B, H, T, budget, floor, R, S: lib.kv_select_budget(  # noqa: E731
+        NULL, B, H, T, budget, floor, R, S, NULL, NULL, NULL)
+    assert sel(1, 2, 10, 3, 2, 0, 0) == -1      # budget < H * floor
+    assert sel(1, 2, 10, 21, 2, 0, 0) == -1     # budget > H * T
+    assert sel(1, 2, 10, 10, 2, 2, 1) == -1     # floor < sinks + recent
+    assert sel(1, 2, 10, 10, 0, 0, 0) == -1     # floor < 1
+    assert sel(1, 2, 10, 10, 11, 0, 0) == -1    # floor > T
+    assert sel(1, 2, 10, 10, 3, -1, 0) == -1
+    assert sel(1, 257, 10, 2570, 10, 0, 0) == -2   # more heads than one cluster serves
+    assert sel(1, 2, 10, 10, 3, 1, 0) == -1     # null pointers
+    assert sel(0, 2, 10, 10, 3, 1, 1) == 0      # empty batch
+    rag = lambda B, H, budget, d, cap: lib.kv_compact_ragged(  # noqa: E731
+        NULL, NULL, NULL, NULL, NULL, B, H, 10, budget, d, 0, NULL, NULL, cap, NULL, NULL, NULL,
+        NULL, NULL)
+    assert rag(1, 2, 8, 64, -1) == -1
+    assert rag(1, 2, -1, 64, 4) == -1
+    assert rag(1, 2, 8, 96, 4) == -2
+    assert rag(1, 2, 8, 64, 4) == -1            # null pointers
+    assert rag(0, 2, 8, 64, 4) == 0
 
 
 def test_empty_batch_is_a_no_op(lib):
