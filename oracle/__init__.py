@@ -41,6 +41,8 @@ def _load():
         lib.oracle_compact.argtypes = [P, P, P, P, I, I, I, I, I, I, P, P, I, P, P, P]
         lib.oracle_select_budget.restype = I
         lib.oracle_select_budget.argtypes = [P, I, I, I, I, I, I, I, P, P]
+        lib.oracle_nested_score.restype = I
+        lib.oracle_nested_score.argtypes = [P, I, I, I, I, I, I, I, I, P, D, P, P, P, P]
         lib.oracle_compact_ragged.restype = I
         lib.oracle_compact_ragged.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, P, I, P, P, P]
         lib.oracle_decode_step_ex.restype = I
@@ -173,6 +175,27 @@ def compact_ragged(K: np.ndarray, V: np.ndarray, s, idx: np.ndarray, off: np.nda
     return K_out, V_out, pos, acc, ln
 
 
+def nested_score(K: np.ndarray, n_disc: int, thresh: float, log_prior=(0.0, 0.0, 0.0),
+                 window: int = 64, n_blocks: int = 32):
+    """NestedKV key-only scores: K [B][H][T][d] (bf16 bits or float32) ->
+    dict(score [B][H][T], a [B][H][3][T] (stable, episodic, current),
+    sigma [B][H][T], w [B][H][3]), all float64."""
+    B, H, T, d = K.shape
+    K = np.ascontiguousarray(K)
+    lp = np.ascontiguousarray(log_prior, dtype=np.float64)
+    assert lp.shape == (3,)
+    score = np.zeros((B, H, T), dtype=np.float64)
+    a = np.zeros((B, H, 3, T), dtype=np.float64)
+    sig = np.zeros((B, H, T), dtype=np.float64)
+    w = np.zeros((B, H, 3), dtype=np.float64)
+    rc = _load().oracle_nested_score(_ptr(K), B, H, T, d, _dtype_code(K), int(window), int(n_blocks),
+                                     int(n_disc), _ptr(lp), float(thresh), _ptr(score), _ptr(a),
+                                     _ptr(sig), _ptr(w))
+    if rc != 0:
+        raise ValueError("oracle_nested_score rejected its inputs")
+    return {"score": score, "a": a, "sigma": sig, "w": w}
+
+
 def decode_step(q, k_new, v_new, K_cache, V_cache, pos, acc, ln, recent: int, new_pos: int,
                 scale: float, flags: int = 0, sink: int = 0):
     """One decode step; K_cache, V_cache, pos, acc, ln are updated IN PLACE.
@@ -205,7 +228,7 @@ def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
 
 
 __all__ = ["BF16", "F32", "FLAG_ALG1", "kv_cache_bytes", "score_obs", "hubkv_refine",
-           "select_topk", "compact", "select_budget", "compact_ragged", "decode_step",
+           "select_topk", "compact", "select_budget", "compact_ragged", "nested_score", "decode_step",
            "bf16_bits_to_f64"]
 
 from .alg1 import h2o_greedy_literal  # noqa: E402

@@ -23,8 +23,10 @@
  *   [KVblog] KV-cache survey blog, §1.1 (scaled dot-product attention with
  *            1/sqrt(d_head)), §1.3 (KV-cache size), §3.3 (GQA), §4.3 (SnapKV
  *            prefill observation window), §4.4 (PyramidKV per-layer budgets).
- *   [NestedKV] "Technische Samenvatting: NestedKV", section 3. Hoofd-gewijze
- *            Geheugentoewijzing (competitive head-wise budget).
+ *   [NestedKV] "Technische Samenvatting: NestedKV", sections 1. Continuum
+ *            Geheugentoestand (three key anchors, cosine anomaly scores),
+ *            2. Buitenste Leraar (head-adaptive blending, surprise routing),
+ *            3. Hoofd-gewijze Geheugentoewijzing (competitive head-wise budget).
  *
  * Readings taken where the pages are silent (each one is listed in the design
  * notes as well):
@@ -429,6 +431,145 @@ int oracle_compact_ragged(const void *K, const void *V, const double *s, const i
     }
   }
   return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * NestedKV key-only scoring ([NestedKV] 1. Continuum Geheugentoestand and
+ * 2. Buitenste Leraar).  Per unit (b, h), over the head's T keys:
+ *   normalised keys   kh_i = k_i / |k_i|  (0 for a zero key);
+ *   three anchors     mu_s    = mean of kh over all T keys (stable);
+ *                     mu_e(i) = mean of kh over i's block, blocks of
+ *                               blk = ceil(T / n_blocks) consecutive keys
+ *                               (episodic; the last block may be shorter);
+ *                     mu_c(i) = mean of kh over [max(0, i-window+1), i]
+ *                               (current: causal moving mean, i included);
+ *   anomaly scores    a_k(i) = -cos(kh_i, mu_k(i)), cos = 0 when a norm is 0;
+ *   discriminative power per scale D_k = (mean of the n_disc largest a_k) -
+ *                     (mean of the n_disc smallest a_k), over the head's tokens;
+ *   scale weights     w = softmax over the three scales of D_k + log_prior[k];
+ *   blend             a_blend(i) = sum_k w_k a_k(i);
+ *   surprise          sigma(i) = population standard deviation of the three a_k(i);
+ *   routing           score(i) = max_k a_k(i) if sigma(i) > thresh, else a_blend(i).
+ * K [B][H][T][d]; score [B][H][T]; a_out [B][H][3][T] (s, e, c; may be NULL);
+ * sigma_out [B][H][T] (may be NULL); w_out [B][H][3] (may be NULL).
+ * ------------------------------------------------------------------------- */
+static double or_cos(const double *x, const double *mu, int d) {
+  double dot = 0.0, nx = 0.0, nm = 0.0;
+  for (int f = 0; f < d; ++f) {
+    dot += x[f] * mu[f];
+    nx += x[f] * x[f];
+    nm += mu[f] * mu[f];
+  }
+  if (nx == 0.0 || nm == 0.0) return 0.0;
+  return dot / (sqrt(nx) * sqrt(nm));
+}
+
+static int or_cmp_double(const void *a, const void *b) {
+  const double x = *(const double *)a, y = *(const double *)b;
+  return (x > y) - (x < y);
+}
+
+int oracle_nested_score(const void *K, int B, int H, int T, int d, int dtype, int window,
+                        int n_blocks, int n_disc, const double *log_prior, double thresh,
+                        double *score_out, double *a_out, double *sigma_out, double *w_out) {
+  if (B < 0 || H <= 0 || T <= 0 || d <= 0 || window < 1 || n_blocks < 1 || n_disc < 1 ||
+      n_disc > T || !log_prior || !score_out)
+    return -1;
+  const int blk = (T + n_blocks - 1) / n_blocks;
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (long long u = 0; u < (long long)B * H; ++u) {
+    double *kh = (double *)malloc(sizeof(double) * (size_t)T * d);
+    double *a = (double *)malloc(sizeof(double) * 3 * (size_t)T);
+    double *srt = (double *)malloc(sizeof(double) * (size_t)T);
+    double *mu = (double *)malloc(sizeof(double) * (size_t)d);
+    if (!kh || !a || !srt || !mu) {
+#pragma omp atomic write
+      bad = 1;
+      free(kh); free(a); free(srt); free(mu);
+      continue;
+    }
+    /* normalised keys */
+    for (int i = 0; i < T; ++i) {
+      double nrm = 0.0;
+      for (int f = 0; f < d; ++f) {
+        const double v = or_load(K, ((size_t)u * T + i) * d + f, dtype);
+        if (!or_is_finite(v)) {
+#pragma omp atomic write
+          bad = 1;
+        }
+        kh[(size_t)i * d + f] = v;
+        nrm += v * v;
+      }
+      nrm = sqrt(nrm);
+      for (int f = 0; f < d; ++f) kh[(size_t)i * d + f] = nrm > 0.0 ? kh[(size_t)i * d + f] / nrm : 0.0;
+    }
+    /* stable anchor */
+    for (int f = 0; f < d; ++f) {
+      double sum = 0.0;
+      for (int j = 0; j < T; ++j) sum += kh[(size_t)j * d + f];
+      mu[f] = sum / T;
+    }
+    for (int i = 0; i < T; ++i) a[i] = -or_cos(kh + (size_t)i * d, mu, d);
+    /* episodic anchor, one block at a time */
+    for (int lo = 0; lo < T; lo += blk) {
+      const int hi = lo + blk < T ? lo + blk : T;
+      for (int f = 0; f < d; ++f) {
+        double sum = 0.0;
+        for (int j = lo; j < hi; ++j) sum += kh[(size_t)j * d + f];
+        mu[f] = sum / (hi - lo);
+      }
+      for (int i = lo; i < hi; ++i) a[T + i] = -or_cos(kh + (size_t)i * d, mu, d);
+    }
+    /* current anchor: causal moving mean */
+    for (int i = 0; i < T; ++i) {
+      const int lo = i - window + 1 > 0 ? i - window + 1 : 0;
+      for (int f = 0; f < d; ++f) {
+        double sum = 0.0;
+        for (int j = lo; j <= i; ++j) sum += kh[(size_t)j * d + f];
+        mu[f] = sum / (i - lo + 1);
+      }
+      a[2 * T + i] = -or_cos(kh + (size_t)i * d, mu, d);
+    }
+    /* discriminative power per scale and the softmax weights */
+    double D[3], w[3];
+    for (int k = 0; k < 3; ++k) {
+      memcpy(srt, a + (size_t)k * T, sizeof(double) * (size_t)T);
+      qsort(srt, (size_t)T, sizeof(double), or_cmp_double);
+      double top = 0.0, bot = 0.0;
+      for (int m = 0; m < n_disc; ++m) {
+        bot += srt[m];
+        top += srt[T - 1 - m];
+      }
+      D[k] = (top - bot) / n_disc;
+    }
+    double zmax = D[0] + log_prior[0];
+    for (int k = 1; k < 3; ++k)
+      if (D[k] + log_prior[k] > zmax) zmax = D[k] + log_prior[k];
+    double zsum = 0.0;
+    for (int k = 0; k < 3; ++k) {
+      w[k] = exp(D[k] + log_prior[k] - zmax);
+      zsum += w[k];
+    }
+    for (int k = 0; k < 3; ++k) w[k] /= zsum;
+    /* blend, surprise, routing */
+    for (int i = 0; i < T; ++i) {
+      const double as = a[i], ae = a[T + i], ac = a[2 * T + i];
+      const double blend = w[0] * as + w[1] * ae + w[2] * ac;
+      const double mean = (as + ae + ac) / 3.0;
+      const double sig = sqrt(((as - mean) * (as - mean) + (ae - mean) * (ae - mean) +
+                               (ac - mean) * (ac - mean)) / 3.0);
+      double win = as > ae ? as : ae;
+      if (ac > win) win = ac;
+      score_out[u * T + i] = sig > thresh ? win : blend;
+      if (sigma_out) sigma_out[u * T + i] = sig;
+    }
+    if (a_out) memcpy(a_out + (size_t)u * 3 * T, a, sizeof(double) * 3 * (size_t)T);
+    if (w_out)
+      for (int k = 0; k < 3; ++k) w_out[u * 3 + k] = w[k];
+    free(kh); free(a); free(srt); free(mu);
+  }
+  return bad ? -1 : 0;
 }
 
 /* ---------------------------------------------------------------------------
