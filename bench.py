@@ -13,7 +13,9 @@ Prints one JSON line (rank 0).  `value` is KV tokens (batch rows x layers x
 prompt tokens) scored + selected + compacted per second over whole steps, summed
 over ranks; `decode` reports H2O decode steps per second; `roofline` is the
 dominant kernel's achieved bandwidth against the measured HBM copy peak;
-`cpu_baseline` times the float64 oracle on a bounded sample on the host cores.
+`cpu_baseline` times the float64 oracle on a bounded sample on the host cores;
+`next_rows` times the rows built beyond the five-step path (layer-level budget,
+ragged compaction) on the same workload, outside the timed step.
 Under torchrun every rank runs its own full workload (weak scaling, no
 collective on the data path); rank 0 reports the max time over ranks.
 """
@@ -54,6 +56,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-next-rows", action="store_true",
+                    help="skip the separate timing of the rows beyond the five-step path")
     return ap.parse_args()
 
 
@@ -240,6 +244,75 @@ class Pipeline:
         return ms
 
 
+def budget_floor(wl):
+    """Per-head minimum for the layer-level budget on a workload: the recent window
+    plus a quarter of the head's heavy share, k_heavy = k - R."""
+    return wl.R + (wl.k - wl.R) // 4
+
+
+def time_next_rows(pipe, reps=5, warmup=3):
+    """Event timing of the rows built beyond the five-step path, on the same
+    workload's buffers, outside the timed step: the layer-level budget
+    (kv_select_budget on z with the same total, Hkv x k per layer) and the ragged
+    compaction that follows it.  L2 is flushed before every repetition."""
+    import torch
+    a, wl = pipe.api, pipe.wl
+    dev = pipe.dev
+    budget, floor = wl.Hkv * wl.k, budget_floor(wl)
+    idx = torch.empty(wl.rows, budget, dtype=torch.int32, device=dev)
+    off = torch.empty(wl.rows, wl.Hkv + 1, dtype=torch.int32, device=dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    cap = budget - (wl.Hkv - 1) * floor  # the most one head can keep
+    dt = pipe.K.dtype
+    Kc = torch.empty(wl.rows, wl.Hkv, cap, wl.d, dtype=dt, device=dev)
+    Vc = torch.empty_like(Kc)
+    pos = torch.empty(wl.rows, wl.Hkv, cap, dtype=torch.int32, device=dev)
+    acc = torch.empty(wl.rows, wl.Hkv, cap, dtype=torch.float32, device=dev)
+    ln = torch.empty(wl.rows, wl.Hkv, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def sel():
+        a.kv_select_budget(pipe.z, budget, floor, wl.R, 0, idx_out=idx, off_out=off)
+
+    def comp():
+        a.kv_compact_ragged(pipe.K, pipe.V, pipe.s, idx, off, cap, K_out=Kc, V_out=Vc, pos_out=pos,
+                            acc_out=acc, len_out=ln, dev_status=status)
+
+    def timed(fn):
+        for _ in range(warmup):
+            fn()
+        ts = []
+        for _ in range(reps):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    out = {}
+    peak, _, kind = measured_peaks()
+    ms = timed(sel)
+    counts = (off[:, 1:] - off[:, :-1])
+    nbytes = wl.units * wl.T * 4 + wl.rows * (budget + wl.Hkv + 1) * 4
+    gbs = nbytes / (ms / 1e3) / 1e9
+    out["kv_select_budget"] = {"ms": ms, "budget_per_layer": budget, "floor": floor,
+                               "algorithmic_bytes": nbytes, "achieved_gbs": gbs,
+                               "frac": gbs / peak, "peak_kind": kind,
+                               "per_head_kept": {"min": int(counts.min()), "max": int(counts.max())}}
+    ms = timed(comp)
+    if int(status.item()) != 0:
+        raise RuntimeError("ragged compaction reported a device status")
+    row = wl.d * pipe.K.element_size()
+    nbytes = wl.rows * budget * (4 * row + 4 + 4 + 4 + 4) + wl.rows * (wl.Hkv + 1) * 4
+    gbs = nbytes / (ms / 1e3) / 1e9
+    out["kv_compact_ragged"] = {"ms": ms, "cap": cap, "algorithmic_bytes": nbytes,
+                                "achieved_gbs": gbs, "frac": gbs / peak, "peak_kind": kind}
+    return out
+
+
 def launch_count():
     from kv_cache_compression_obs_gb300 import api
     return int(api.library_handle().kv_launch_count())
@@ -396,6 +469,8 @@ def run_ours(args, wl, rank, world):
                            "hbm_gbs": per_launch["kv_score_obs"] / (phases["kv_score_obs"] / 1e3) / 1e9},
         "clocks": clk.summary(),
     }
+    if not args.no_next_rows:
+        line["next_rows"] = time_next_rows(pipe)
     if not args.no_e2e:
         dt, h2d, d2h = run_e2e(wl, pipe, min(args.steps, 2))
         line["e2e"] = {"value": world * tokens / dt, "unit": UNIT, "h2d_bytes_per_step": h2d,
