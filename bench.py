@@ -15,7 +15,8 @@ over ranks; `decode` reports H2O decode steps per second; `roofline` is the
 dominant kernel's achieved bandwidth against the measured HBM copy peak;
 `cpu_baseline` times the float64 oracle on a bounded sample on the host cores;
 `next_rows` times the rows built beyond the five-step path (layer-level budget,
-ragged compaction) on the same workload, outside the timed step.
+ragged compaction, NestedKV key-only scoring) on the same workload, outside the
+timed step.
 Under torchrun every rank runs its own full workload (weak scaling, no
 collective on the data path); rank 0 reports the max time over ranks.
 """
@@ -244,6 +245,18 @@ class Pipeline:
         return ms
 
 
+NESTED_THRESH = 0.1  # surprise threshold of the NestedKV timing (the pages leave it open)
+
+
+def nested_bytes(wl):
+    """Bytes any NestedKV scorer must move: the keys twice (the stable anchor needs
+    every key before any score, and a head's keys do not fit on chip), the three
+    anomaly scores written once and read twice (the discriminative powers need all
+    of them before the final pass), and the score written."""
+    k_bytes = wl.units * wl.T * wl.d * wl.elem_bytes
+    return 2 * k_bytes + wl.units * wl.T * (12 + 12 + 12 + 4)
+
+
 def budget_floor(wl):
     """Per-head minimum for the layer-level budget on a workload: the recent window
     plus a quarter of the head's heavy share, k_heavy = k - R."""
@@ -310,6 +323,24 @@ def time_next_rows(pipe, reps=5, warmup=3):
     gbs = nbytes / (ms / 1e3) / 1e9
     out["kv_compact_ragged"] = {"ms": ms, "cap": cap, "algorithmic_bytes": nbytes,
                                 "achieved_gbs": gbs, "frac": gbs / peak, "peak_kind": kind}
+    # NestedKV key-only scoring of the same keys
+    n_disc = -(-wl.T // 10)
+    nscore = torch.empty(wl.rows, wl.Hkv, wl.T, dtype=torch.float32, device=dev)
+    nw = torch.empty(wl.rows, wl.Hkv, 3, dtype=torch.float32, device=dev)
+    nws = torch.empty(a.kv_workspace_size(a.KV_OP_SCORE_NESTED, wl.rows, 0, wl.Hkv, wl.T, wl.d, 32),
+                      dtype=torch.uint8, device=dev)
+    launches0 = launch_count()
+    ms = timed(lambda: a.kv_score_nested(pipe.K, n_disc, NESTED_THRESH, (0.0, 0.0, 0.0), 64, 32,
+                                         out=nscore, w_out=nw, workspace=nws))
+    per_call = (launch_count() - launches0) // (warmup + reps)
+    k_bytes = wl.units * wl.T * wl.d * pipe.K.element_size()
+    nbytes = nested_bytes(wl)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    out["kv_score_nested"] = {"ms": ms, "window": 64, "n_blocks": 32, "n_disc": n_disc,
+                              "surprise_thresh": NESTED_THRESH, "launches": per_call,
+                              "algorithmic_bytes": nbytes, "k_bytes": k_bytes,
+                              "achieved_gbs": gbs, "frac": gbs / peak, "peak_kind": kind,
+                              "tokens_per_s": wl.units * wl.T / (ms / 1e3)}
     return out
 
 

@@ -7,9 +7,9 @@
  *   kv_select_topk   budgeted per-head Top-K with a protected recent window
  *   kv_compact       gather-compaction of the kept K/V rows into a slot cache
  *   h2o_decode_step  one decode step: attention, score accumulation, <= 1 eviction
- * and, beyond those five, a layer-level budget shared by the heads of a layer
- * (kv_select_budget, kv_compact_ragged) and the _ex variants (sinks, HubKV
- * comparison variants).
+ * and, beyond those five, NestedKV's key-only scorer (kv_score_nested), a
+ * layer-level budget shared by the heads of a layer (kv_select_budget,
+ * kv_compact_ragged) and the _ex variants (sinks, HubKV comparison variants).
  *
  * Sources (page title, section):
  *   [H2O]    "H2O 完全拆解：抓住 KV Cache 里的「重击者」，20% 预算无损生成（NeurIPS 2023）"
@@ -84,7 +84,13 @@ enum {
 };
 
 /* operation codes for kv_workspace_size */
-enum { KV_OP_SCORE_OBS = 1, KV_OP_HUBKV_REFINE = 2, KV_OP_SELECT_TOPK = 3, KV_OP_DECODE = 4 };
+enum {
+  KV_OP_SCORE_OBS = 1,
+  KV_OP_HUBKV_REFINE = 2,
+  KV_OP_SELECT_TOPK = 3,
+  KV_OP_DECODE = 4,
+  KV_OP_SCORE_NESTED = 5
+};
 
 typedef void *kv_stream_t;
 
@@ -194,6 +200,41 @@ KVC_API int kv_select_topk_ex(const float *z, int B, int H, int T, int k, int re
 KVC_API int kv_compact(const void *K, const void *V, const float *s, const int32_t *idx, int B, int H,
                int T, int k, int d, int dtype, void *K_out, void *V_out, int cap,
                int32_t *pos_out, float *acc_out, int32_t *len_out, kv_stream_t stream);
+
+/*
+ * kv_score_nested -- NestedKV key-only importance scores ([NestedKV]
+ * 1. Continuum Geheugentoestand, 2. Buitenste Leraar).  No queries: for unit
+ * (b, h) over its T keys, with kh_i = k_i / |k_i| (0 for a zero key),
+ *   stable    mu_s    = mean of kh over all T keys;
+ *   episodic  mu_e(i) = mean of kh over i's block, blocks of ceil(T / n_blocks)
+ *                       consecutive keys (the pages: b ~ N/32, so n_blocks = 32);
+ *   current   mu_c(i) = mean of kh over [max(0, i - window + 1), i] (causal
+ *                       moving mean, i included; the pages: window = 64);
+ *   a_k(i)  = -cos(k_i, mu_k(i)), 0 when a norm is 0 (high = anomalous = keep);
+ *   D_k     = mean of the n_disc largest a_k(i) - mean of the n_disc smallest
+ *             (each scale's discriminative power in this head);
+ *   w       = softmax over k of D_k + log_prior_k (the fixed log-prior);
+ *   sigma(i)= population standard deviation of (a_s, a_e, a_c)(i) (surprise);
+ *   score(i)= max_k a_k(i) if sigma(i) > surprise_thresh, else sum_k w_k a_k(i).
+ * The scores rank tokens for kv_select_topk / kv_select_budget.
+ *
+ *   K          [B][H][T][d] (dtype as everywhere; fp32 arithmetic)
+ *   score_out  [B][H][T] float32
+ *   w_out      [B][H][3] float32 (w_s, w_e, w_c), may be NULL
+ *   a_out      [B][H][3][T] float32 (a_s, a_e, a_c), may be NULL; when given it
+ *              also serves as their scratch, so the workspace can be smaller
+ *   workspace  >= kv_workspace_size(KV_OP_SCORE_NESTED, B, 0, H, T, d, n_blocks, 0)
+ *              bytes (that size assumes a_out == NULL)
+ * Preconditions: 1 <= window <= 4096, 1 <= n_blocks <= 65536, 1 <= n_disc <= T,
+ * finite log priors, surprise_thresh not NaN, d in {64, 128}.
+ * Four launches: two key scans (the stable anchor needs every key before any
+ * score), one selection per (unit, scale), one elementwise pass.
+ */
+KVC_API int kv_score_nested(const void *K, int B, int H, int T, int d, int dtype, int window,
+                            int n_blocks, int n_disc, float log_prior_s, float log_prior_e,
+                            float log_prior_c, float surprise_thresh, float *score_out,
+                            float *w_out, float *a_out, void *workspace, size_t workspace_bytes,
+                            kv_stream_t stream);
 
 /*
  * kv_select_budget -- layer-level competitive budget: the heads of one layer
@@ -326,7 +367,8 @@ KVC_API int kv_score_obs_noalloc(const void *Q_obs, const void *K, int B, int Hq
 
 /* Device workspace (bytes) that `op` needs for these sizes; 0 if none.
  * Arguments that an op does not use are ignored; for KV_OP_HUBKV_REFINE pass the
- * refine call's head count H as Hkv; for KV_OP_DECODE pass the slot capacity as T.
+ * refine call's head count H as Hkv; for KV_OP_DECODE pass the slot capacity as T;
+ * for KV_OP_SCORE_NESTED pass H as Hkv and n_blocks as W.
  * Returns 0 for invalid sizes. */
 KVC_API size_t kv_workspace_size(int op, int B, int Hq, int Hkv, int T, int d, int W, int k);
 

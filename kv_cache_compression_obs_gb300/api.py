@@ -29,7 +29,7 @@ KV_OK, KV_ERR_INVALID_ARG, KV_ERR_UNSUPPORTED, KV_ERR_CUDA, KV_ERR_TIMEOUT, KV_E
 KV_BF16, KV_F32 = 0, 1
 KV_H2O_ALG1 = 1
 KV_HUB_AVGPOOL, KV_HUB_FIXED_HEAD = 1, 2
-KV_OP_SCORE_OBS, KV_OP_HUBKV_REFINE, KV_OP_SELECT_TOPK, KV_OP_DECODE = 1, 2, 3, 4
+KV_OP_SCORE_OBS, KV_OP_HUBKV_REFINE, KV_OP_SELECT_TOPK, KV_OP_DECODE, KV_OP_SCORE_NESTED = 1, 2, 3, 4, 5
 
 _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _lib.kv_score_obs.restype = _I
@@ -44,6 +44,9 @@ _lib.kv_select_topk_ex.restype = _I
 _lib.kv_select_topk_ex.argtypes = [_P, _I, _I, _I, _I, _I, _I, _P, _P, _Z, _P]
 _lib.kv_compact.restype = _I
 _lib.kv_compact.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P]
+_lib.kv_score_nested.restype = _I
+_lib.kv_score_nested.argtypes = [_P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _F, _F, _F, _P, _P, _P, _P,
+                                 _Z, _P]
 _lib.kv_select_budget.restype = _I
 _lib.kv_select_budget.argtypes = [_P, _I, _I, _I, _I, _I, _I, _I, _P, _P, _P]
 _lib.kv_compact_ragged.restype = _I
@@ -209,6 +212,25 @@ def kv_compact(K: torch.Tensor, V: torch.Tensor, s, idx: torch.Tensor, cap: int 
                                          _ptr(pos), _ptr(acc if s is not None else None), _ptr(ln),
                                          _stream(stream)))
     return K_out, V_out, pos, acc, ln
+
+
+def kv_score_nested(K: torch.Tensor, n_disc: int, thresh: float, log_prior=(0.0, 0.0, 0.0),
+                    window: int = 64, n_blocks: int = 32, out=None, w_out=None, a_out=None,
+                    workspace=None, stream=None):
+    """NestedKV key-only scores: K [B][H][T][d] -> (score [B][H][T], w [B][H][3]) float32.
+    a_out ([B][H][3][T] float32), when given, receives the three anomaly scores."""
+    B, H, T, d = K.shape
+    _dev(K, out, w_out, a_out)
+    dev = K.device
+    score = out if out is not None else torch.empty(B, H, T, dtype=torch.float32, device=dev)
+    w = w_out if w_out is not None else torch.empty(B, H, 3, dtype=torch.float32, device=dev)
+    ws, nbytes = _workspace(kv_workspace_size(KV_OP_SCORE_NESTED, B, 0, H, T, d, n_blocks), dev,
+                            workspace)
+    lp = [float(x) for x in log_prior]
+    _check("kv_score_nested", _lib.kv_score_nested(
+        _ptr(K), B, H, T, d, _dtype_code(K), int(window), int(n_blocks), int(n_disc), lp[0], lp[1],
+        lp[2], float(thresh), _ptr(score), _ptr(w), _ptr(a_out), _ptr(ws), nbytes, _stream(stream)))
+    return score, w
 
 
 def kv_select_budget(z: torch.Tensor, budget: int, floor: int, recent: int, sink: int = 0,

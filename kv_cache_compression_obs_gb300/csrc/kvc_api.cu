@@ -3,6 +3,7 @@
 // enqueued, so a rejected call touches neither the GPU nor any output.
 #include <atomic>
 #include <climits>
+#include <cmath>
 #include <cstdio>
 #include <mutex>
 #include <unordered_map>
@@ -98,6 +99,9 @@ size_t kv_workspace_size(int op, int B, int Hq, int Hkv, int T, int d, int W, in
       return plan_refine(B, Hkv, T).ws_bytes;  // the refine call's H is passed as Hkv
     case KV_OP_SELECT_TOPK:
       return 0;
+    case KV_OP_SCORE_NESTED:  // Hkv is the head count, W the number of episodic blocks
+      if (Hkv <= 0 || W <= 0 || !(d == 64 || d == 128)) return 0;
+      return nested_workspace_bytes((long)B * Hkv, T, d, W, true);
     case KV_OP_DECODE:  // T is the slot capacity
       if (Hq <= 0 || Hkv <= 0 || Hq % Hkv || !(d == 64 || d == 128)) return 0;
       return decode_workspace_bytes((long)B * Hkv, Hq / Hkv, T, d);
@@ -218,6 +222,30 @@ int kv_compact_ragged(const void *K, const void *V, const float *s, const int32_
   return launch_compact_ragged(K, V, acc_out ? s : nullptr, idx, off, B, H, T, budget, d, dtype,
                                K_out, V_out, cap, pos_out, acc_out, len_out, dev_status,
                                static_cast<cudaStream_t>(stream));
+}
+
+int kv_score_nested(const void *K, int B, int H, int T, int d, int dtype, int window,
+                    int n_blocks, int n_disc, float log_prior_s, float log_prior_e,
+                    float log_prior_c, float surprise_thresh, float *score_out, float *w_out,
+                    float *a_out, void *workspace, size_t workspace_bytes, kv_stream_t stream) {
+  if (B < 0 || H <= 0 || T <= 0 || !dtype_ok(dtype) || window < 1 || n_blocks < 1 ||
+      n_disc < 1 || n_disc > T || !(surprise_thresh == surprise_thresh) ||
+      !std::isfinite(log_prior_s) || !std::isfinite(log_prior_e) || !std::isfinite(log_prior_c))
+    return KV_ERR_INVALID_ARG;
+  if (!dim_ok(d)) return KV_ERR_UNSUPPORTED;
+  if (window > 4096 || n_blocks > 65536) return KV_ERR_UNSUPPORTED;
+  if (!fits((long long)B * H, (long long)T * d) || !fits((long long)B * H, n_blocks) ||
+      (long long)B * H * n_blocks > INT_MAX || (long long)B * H * 3 > INT_MAX)
+    return KV_ERR_INVALID_ARG;
+  if (B == 0) return KV_OK;
+  if (!K || !score_out || !aligned16(K) || ((uintptr_t)score_out & 3u) ||
+      (w_out && ((uintptr_t)w_out & 3u)) || (a_out && ((uintptr_t)a_out & 3u)))
+    return KV_ERR_INVALID_ARG;
+  const size_t need = nested_workspace_bytes((long)B * H, T, d, n_blocks, a_out == nullptr);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return KV_ERR_WORKSPACE;
+  return launch_score_nested(K, B, H, T, d, dtype, window, n_blocks, n_disc, log_prior_s,
+                             log_prior_e, log_prior_c, surprise_thresh, score_out, w_out, a_out,
+                             workspace, static_cast<cudaStream_t>(stream));
 }
 
 int h2o_decode_step_ex(const void *q, const void *k_new, const void *v_new, void *K_cache,

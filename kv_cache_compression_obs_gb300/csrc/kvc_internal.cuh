@@ -101,6 +101,10 @@ int launch_compact_ragged(const void *K, const void *V, const float *s, const in
                           const int32_t *off, int B, int H, int T, int budget, int d, int dtype,
                           void *K_out, void *V_out, int cap, int32_t *pos, float *acc,
                           int32_t *len, int *status, cudaStream_t st);
+size_t nested_workspace_bytes(long units, int T, int d, int n_blocks, bool with_a);
+int launch_score_nested(const void *K, int B, int H, int T, int d, int dtype, int window,
+                        int n_blocks, int n_disc, float lp0, float lp1, float lp2, float thresh,
+                        float *score, float *w_out, float *a_out, void *ws, cudaStream_t st);
 int launch_decode_step(const void *q, const void *k_new, const void *v_new, void *K_cache,
                        void *V_cache, int32_t *pos, float *acc, int32_t *len, int B, int Hq,
                        int Hkv, int cap, int d, int recent, int sink, int32_t new_pos, float scale,

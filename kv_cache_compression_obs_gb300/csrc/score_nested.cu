@@ -1,0 +1,519 @@
+// score_nested.cu -- NestedKV key-only scoring (NestedKV technical summary,
+// 1. Continuum Geheugentoestand and 2. Buitenste Leraar).
+//
+// Per unit (b, h) over its T keys, with kh_i = k_i / |k_i|:
+//   a_s(i) = -cos(k_i, sum_j kh_j)                       stable anchor
+//   a_e(i) = -cos(k_i, sum of kh over i's block)          episodic anchor, blocks of
+//                                                         ceil(T / n_blocks) keys
+//   a_c(i) = -cos(k_i, sum of kh over [i-window+1, i])    current anchor (causal)
+//   D_k    = mean of the n_disc largest a_k - mean of the n_disc smallest
+//   w      = softmax_k(D_k + log_prior_k)
+//   score  = max_k a_k(i) if the std of the three a_k(i) exceeds thresh, else
+//            sum_k w_k a_k(i).
+// (A mean and a sum point the same way, so the anchors are kept as sums.)
+//
+// HBM-bound key scans on the CUDA cores, four launches:
+//   1. anchors_kernel: one CTA per (unit, episodic block); its warps sweep
+//      contiguous token ranges, lanes over features.  Each key is normalised
+//      once; the block sum of kh goes to the workspace; the causal window sum is
+//      kept as P (the current window-aligned chunk's prefix) + Q (the previous
+//      chunk's suffix, its total minus the rows that left the window), so every
+//      running sum restarts each `window` keys and rounding cannot drift; the
+//      rows leaving the window are re-read (L1/L2) and their 1/|k| comes from a
+//      per-warp ring in shared memory.  Writes a_c.
+//   2. global_kernel: same grid; adds the unit's block sums into the stable
+//      anchor, re-reads the block's keys and writes a_s and a_e.
+//   3. disc_kernel: one CTA per (unit, scale): radix select (order-preserving
+//      32-bit keys) of the n_disc-th largest and smallest a_k, then the two sums.
+//   4. final_kernel: elementwise weights, surprise, routing.
+// Per-token cross-lane sums go through batched butterflies: V values of 4 tokens
+// reduce in V-1 + (5 - log2 V) shuffles instead of 5 V.
+#include "kvc_internal.cuh"
+#include "select_common.cuh"
+
+namespace kvc {
+namespace {
+
+constexpr int NWARP = 4;  // warps per CTA of the two key scans
+constexpr int NT_SCAN = NWARP * 32;
+constexpr int NT_DISC = 1024;
+
+// ---- row loads: lane holds features FPL*lane .. FPL*lane+FPL-1 ----------------
+template <typename T, int D> struct Row;
+template <> struct Row<__nv_bfloat16, 128> {
+  static constexpr int FPL = 4;
+  __device__ __forceinline__ static void load(const __nv_bfloat16 *row, int lane, float (&x)[4]) {
+    const uint2 v = __ldg(reinterpret_cast<const uint2 *>(row) + lane);
+    x[0] = __uint_as_float(v.x << 16);
+    x[1] = __uint_as_float(v.x & 0xFFFF0000u);
+    x[2] = __uint_as_float(v.y << 16);
+    x[3] = __uint_as_float(v.y & 0xFFFF0000u);
+  }
+};
+template <> struct Row<__nv_bfloat16, 64> {
+  static constexpr int FPL = 2;
+  __device__ __forceinline__ static void load(const __nv_bfloat16 *row, int lane, float (&x)[2]) {
+    const uint32_t v = __ldg(reinterpret_cast<const uint32_t *>(row) + lane);
+    x[0] = __uint_as_float(v << 16);
+    x[1] = __uint_as_float(v & 0xFFFF0000u);
+  }
+};
+template <> struct Row<float, 128> {
+  static constexpr int FPL = 4;
+  __device__ __forceinline__ static void load(const float *row, int lane, float (&x)[4]) {
+    const float4 v = __ldg(reinterpret_cast<const float4 *>(row) + lane);
+    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+  }
+};
+template <> struct Row<float, 64> {
+  static constexpr int FPL = 2;
+  __device__ __forceinline__ static void load(const float *row, int lane, float (&x)[2]) {
+    const float2 v = __ldg(reinterpret_cast<const float2 *>(row) + lane);
+    x[0] = v.x; x[1] = v.y;
+  }
+};
+
+// Sum V per-lane values over the warp; afterwards lane l holds the total of
+// value l / (32 / V) (V = 4, 8 or 16).
+template <int V>
+__device__ __forceinline__ float reduce_scatter(float (&v)[V], int lane) {
+  int count = V;
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    if (count > 1) {
+      const int half = count >> 1;
+      const bool up = (lane & o) != 0;
+#pragma unroll
+      for (int j = 0; j < V / 2; ++j) {
+        if (j < half) {
+          const float send = up ? v[j] : v[j + half];
+          const float keep = up ? v[j + half] : v[j];
+          v[j] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
+        }
+      }
+      count = half;
+    } else {
+      v[0] += __shfl_xor_sync(0xFFFFFFFFu, v[0], o);
+    }
+  }
+  return v[0];
+}
+
+// -cos between a key (squared norm nk) and an anchor (norm nm), 0 for a zero norm.
+__device__ __forceinline__ float neg_cos(float dot, float nk2, float nm) {
+  const float den = sqrtf(nk2) * nm;
+  return den > 0.f ? -(dot / den) : 0.f;
+}
+
+// Token range of warp w inside [lo, hi): equal spans.
+__device__ __forceinline__ void warp_range(int lo, int hi, int w, int &s, int &e) {
+  const int span = (hi - lo + NWARP - 1) / NWARP;
+  s = min(hi, lo + w * span);
+  e = min(hi, s + span);
+}
+
+// ---- 1. block sums and the current (moving-window) anchor ---------------------
+template <typename T, int D>
+__global__ __launch_bounds__(NT_SCAN) void anchors_kernel(const T *__restrict__ K, int Tn,
+                                                          int blk, int n_blocks, int window,
+                                                          float *__restrict__ esum,
+                                                          float *__restrict__ a) {
+  using R = Row<T, D>;
+  constexpr int F = R::FPL;
+  extern __shared__ float ring_all[];  // [NWARP][window] 1/|k| of the last rows
+  __shared__ float sums[NWARP][D];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long unit = blockIdx.x / n_blocks;
+  const int bj = blockIdx.x % n_blocks;
+  const int lo = min(Tn, bj * blk), hi = min(Tn, lo + blk);
+  const T *Ku = K + unit * (long)Tn * D;
+  float *ring = ring_all + warp * window;
+  float *ac = a + (unit * 3 + 2) * (long)Tn;
+
+  int s, e;
+  warp_range(lo, hi, warp, s, e);
+  float es[F];
+#pragma unroll
+  for (int f = 0; f < F; ++f) es[f] = 0.f;
+
+  if (s < e) {
+    const int c0 = (s / window) * window;  // first chunk start the warp walks from
+    float P[F], Q[F];
+#pragma unroll
+    for (int f = 0; f < F; ++f) P[f] = Q[f] = 0.f;
+    // warm-up: the full chunk before c0 (its total starts Q; its 1/|k| fill the ring)
+    if (c0 > 0) {
+      for (int i0 = c0 - window; i0 < c0; i0 += 4) {
+        float x[4][F], ss[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int i = i0 + t;
+          if (i < c0) R::load(Ku + (long)i * D, lane, x[t]);
+          else {
+#pragma unroll
+            for (int f = 0; f < F; ++f) x[t][f] = 0.f;
+          }
+          ss[t] = 0.f;
+#pragma unroll
+          for (int f = 0; f < F; ++f) ss[t] = fmaf(x[t][f], x[t][f], ss[t]);
+        }
+        const float tot = reduce_scatter<4>(ss, lane);
+        const float my_inv = tot > 0.f ? 1.f / sqrtf(tot) : 0.f;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int i = i0 + t;
+          const float inv = __shfl_sync(0xFFFFFFFFu, my_inv, t * 8);
+          if (i < c0) {
+#pragma unroll
+            for (int f = 0; f < F; ++f) P[f] = fmaf(x[t][f], inv, P[f]);
+            if (lane == 0) ring[i % window] = inv;
+          }
+        }
+      }
+    }
+    __syncwarp();
+    int r = 0;  // i - (chunk start), i.e. i % window, kept as a running counter
+    for (int i0 = c0; i0 < e; i0 += 4) {
+      float x[4][F], y[4][F], ss[4];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int i = i0 + t;
+        if (i < e) R::load(Ku + (long)i * D, lane, x[t]);
+        else {
+#pragma unroll
+          for (int f = 0; f < F; ++f) x[t][f] = 0.f;
+        }
+        if (i < e && i >= window) R::load(Ku + (long)(i - window) * D, lane, y[t]);
+        else {
+#pragma unroll
+          for (int f = 0; f < F; ++f) y[t][f] = 0.f;
+        }
+        ss[t] = 0.f;
+#pragma unroll
+        for (int f = 0; f < F; ++f) ss[t] = fmaf(x[t][f], x[t][f], ss[t]);
+      }
+      const float tot = reduce_scatter<4>(ss, lane);
+      const float my_inv = tot > 0.f ? 1.f / sqrtf(tot) : 0.f;
+      float part[8];
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int i = i0 + t;
+        const float inv = __shfl_sync(0xFFFFFFFFu, my_inv, t * 8);
+        float dot = 0.f, nrm = 0.f;
+        if (i < e) {
+          if (r == 0) {  // a new chunk: the previous chunk's total becomes Q
+#pragma unroll
+            for (int f = 0; f < F; ++f) {
+              Q[f] = P[f];
+              P[f] = 0.f;
+            }
+          }
+          const float inv_old = (i >= window) ? ring[r] : 0.f;  // 1/|k_{i-window}|
+          __syncwarp();
+          if (lane == 0) ring[r] = inv;
+#pragma unroll
+          for (int f = 0; f < F; ++f) {
+            const float kh = x[t][f] * inv;
+            P[f] += kh;
+            Q[f] = fmaf(-y[t][f], inv_old, Q[f]);
+            const float wsum = P[f] + Q[f];
+            dot = fmaf(kh, wsum, dot);
+            nrm = fmaf(wsum, wsum, nrm);
+            if (i >= s) es[f] += kh;
+          }
+          __syncwarp();
+          r = (r + 1 == window) ? 0 : r + 1;
+        }
+        part[2 * t] = dot;
+        part[2 * t + 1] = nrm;
+      }
+      const float v = reduce_scatter<8>(part, lane);
+      // lane l holds value l / 4: even values are dots, odd ones the window's |.|^2
+      const float nrm = __shfl_down_sync(0xFFFFFFFFu, v, 4);
+      const int idx = lane >> 2;
+      if ((lane & 7) == 0) {
+        const int i = i0 + (idx >> 1);
+        // kh has norm 1 (or is zero, and then the dot is 0): cos = dot / |window sum|
+        if (i >= s && i < e) {
+          const float nw = sqrtf(nrm);
+          ac[i] = nw > 0.f ? -(v / nw) : 0.f;
+        }
+      }
+    }
+  }
+  // block sum of kh over the warps
+#pragma unroll
+  for (int f = 0; f < F; ++f) sums[warp][lane * F + f] = es[f];
+  __syncthreads();
+  for (int f = threadIdx.x; f < D; f += NT_SCAN) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < NWARP; ++w) t += sums[w][f];
+    esum[(unit * n_blocks + bj) * (long)D + f] = t;
+  }
+}
+
+// ---- 2. stable and episodic anchors ----------------------------------------------
+template <typename T, int D>
+__global__ __launch_bounds__(NT_SCAN) void global_kernel(const T *__restrict__ K, int Tn, int blk,
+                                                         int n_blocks,
+                                                         const float *__restrict__ esum,
+                                                         float *__restrict__ a) {
+  using R = Row<T, D>;
+  constexpr int F = R::FPL;
+  __shared__ float S[D], E[D];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const long unit = blockIdx.x / n_blocks;
+  const int bj = blockIdx.x % n_blocks;
+  const int lo = min(Tn, bj * blk), hi = min(Tn, lo + blk);
+  const float *eu = esum + unit * (long)n_blocks * D;
+  for (int f = threadIdx.x; f < D; f += NT_SCAN) {
+    float t = 0.f;
+    for (int j = 0; j < n_blocks; ++j) t += eu[(long)j * D + f];
+    S[f] = t;
+    E[f] = eu[(long)bj * D + f];
+  }
+  __syncthreads();
+  // anchor norms (every warp computes both)
+  float ns = 0.f, ne = 0.f;
+  for (int f = lane; f < D; f += 32) {
+    ns = fmaf(S[f], S[f], ns);
+    ne = fmaf(E[f], E[f], ne);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    ns += __shfl_xor_sync(0xFFFFFFFFu, ns, o);
+    ne += __shfl_xor_sync(0xFFFFFFFFu, ne, o);
+  }
+  const float nS = sqrtf(ns), nE = sqrtf(ne);
+  float sl[F], el[F];
+#pragma unroll
+  for (int f = 0; f < F; ++f) {
+    sl[f] = S[lane * F + f];
+    el[f] = E[lane * F + f];
+  }
+  const T *Ku = K + unit * (long)Tn * D;
+  float *as = a + (unit * 3 + 0) * (long)Tn;
+  float *ae = a + (unit * 3 + 1) * (long)Tn;
+  int s, e;
+  warp_range(lo, hi, warp, s, e);
+  for (int i0 = s; i0 < e; i0 += 4) {
+    float part[16];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      float x[F];
+      if (i0 + t < e) R::load(Ku + (long)(i0 + t) * D, lane, x);
+      else {
+#pragma unroll
+        for (int f = 0; f < F; ++f) x[f] = 0.f;
+      }
+      float ds = 0.f, de = 0.f, nk = 0.f;
+#pragma unroll
+      for (int f = 0; f < F; ++f) {
+        ds = fmaf(x[f], sl[f], ds);
+        de = fmaf(x[f], el[f], de);
+        nk = fmaf(x[f], x[f], nk);
+      }
+      part[4 * t] = ds;
+      part[4 * t + 1] = de;
+      part[4 * t + 2] = nk;
+      part[4 * t + 3] = 0.f;
+    }
+    const float v = reduce_scatter<16>(part, lane);
+    // lane l holds value l / 2: (ds, de, nk, 0) of token l / 8
+    const float de = __shfl_down_sync(0xFFFFFFFFu, v, 2);
+    const float nk = __shfl_down_sync(0xFFFFFFFFu, v, 4);
+    if ((lane & 7) == 0) {
+      const int i = i0 + (lane >> 3);
+      if (i < e) {
+        as[i] = neg_cos(v, nk, nS);
+        ae[i] = neg_cos(de, nk, nE);
+      }
+    }
+  }
+}
+
+// ---- 3. discriminative power per (unit, scale) -----------------------------------
+// Sum of the `m` largest values of v[0..n) (DESC) or of the `m` smallest (!DESC):
+// radix select of the m-th key, then the values beyond it plus the right number
+// of copies of the boundary value.  Deterministic block reduction.
+template <bool DESC>
+__device__ float extreme_sum(const float *__restrict__ v, int n, int m, uint32_t *hist,
+                             uint32_t *tot, int *warp_sums, uint32_t *sh) {
+  constexpr int NW = NT_DISC / 32;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  auto key = [](float x) { return DESC ? order_key(x) : ~order_key(x); };
+  uint32_t prefix = 0, mask = 0;
+  int need = m;
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = threadIdx.x; i < NW * 256; i += NT_DISC) hist[i] = 0u;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += NT_DISC) {
+      const uint32_t u = key(v[i]);
+      if ((u & mask) == prefix) atomicAdd(&hist[warp * 256 + ((u >> shift) & 255u)], 1u);
+    }
+    __syncthreads();
+    if (threadIdx.x < 256) {
+      uint32_t t = 0;
+      for (int w = 0; w < NW; ++w) t += hist[w * 256 + threadIdx.x];
+      tot[threadIdx.x] = t;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      uint32_t mine = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mine += tot[255 - 8 * lane - i];
+      uint32_t incl = mine;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      uint32_t above = incl - mine;
+      if (above < (uint32_t)need && (uint32_t)need <= incl) {
+        for (int i = 0; i < 8; ++i) {
+          const int dgt = 255 - 8 * lane - i;
+          if ((uint32_t)need <= above + tot[dgt]) {
+            sh[0] = prefix | ((uint32_t)dgt << shift);
+            sh[1] = (uint32_t)(need - (int)above);
+            break;
+          }
+          above += tot[dgt];
+        }
+      }
+    }
+    __syncthreads();
+    prefix = sh[0];
+    need = (int)sh[1];
+    mask |= 255u << shift;
+    __syncthreads();
+  }
+  // values strictly beyond the boundary key, in a fixed order
+  const uint32_t ustar = prefix;
+  __shared__ float sh_b;  // the boundary value (every value with that key is equal up to sign of 0)
+  float part = 0.f;
+  for (int i = threadIdx.x; i < n; i += NT_DISC) {
+    const float x = v[i];
+    const uint32_t u = key(x);
+    if (u > ustar) part += x;
+    if (u == ustar) sh_b = x;
+  }
+  float x = part;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+  float *fs = reinterpret_cast<float *>(warp_sums);
+  if (lane == 0) fs[warp] = x;
+  __syncthreads();
+  float total = 0.f;
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < NW; ++w) total += fs[w];
+    total += (float)need * sh_b;
+    fs[NW] = total;
+  }
+  __syncthreads();
+  total = fs[NW];
+  __syncthreads();
+  return total;
+}
+
+__global__ __launch_bounds__(NT_DISC, 1) void disc_kernel(const float *__restrict__ a, int Tn,
+                                                       int m, float *__restrict__ D) {
+  __shared__ uint32_t hist[(NT_DISC / 32) * 256];
+  __shared__ uint32_t tot[256];
+  __shared__ int warp_sums[NT_DISC / 32 + 1];
+  __shared__ uint32_t sh[2];
+  const float *v = a + (long)blockIdx.x * Tn;  // blockIdx.x = unit * 3 + scale
+  const float top = extreme_sum<true>(v, Tn, m, hist, tot, warp_sums, sh);
+  const float bot = extreme_sum<false>(v, Tn, m, hist, tot, warp_sums, sh);
+  if (threadIdx.x == 0) D[blockIdx.x] = (top - bot) / (float)m;
+}
+
+// ---- 4. weights, surprise, routing ------------------------------------------------
+__global__ void final_kernel(const float *__restrict__ a, const float *__restrict__ D, int Tn,
+                             long units, float lp0, float lp1, float lp2, float thresh,
+                             float *__restrict__ score, float *__restrict__ w_out) {
+  for (long u = blockIdx.y; u < units; u += gridDim.y) {
+    const float z0 = D[u * 3 + 0] + lp0, z1 = D[u * 3 + 1] + lp1, z2 = D[u * 3 + 2] + lp2;
+    const float zm = fmaxf(z0, fmaxf(z1, z2));
+    const float e0 = expf(z0 - zm), e1 = expf(z1 - zm), e2 = expf(z2 - zm);
+    const float es = e0 + e1 + e2;
+    const float w0 = e0 / es, w1 = e1 / es, w2 = e2 / es;
+    if (w_out && blockIdx.x == 0 && threadIdx.x == 0) {
+      w_out[u * 3 + 0] = w0;
+      w_out[u * 3 + 1] = w1;
+      w_out[u * 3 + 2] = w2;
+    }
+    const float *as = a + (u * 3 + 0) * (long)Tn;
+    const float *ae = as + Tn;
+    const float *ac = ae + Tn;
+    float *su = score + u * (long)Tn;
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < Tn; i += gridDim.x * blockDim.x) {
+      const float x0 = as[i], x1 = ae[i], x2 = ac[i];
+      const float mean = (x0 + x1 + x2) / 3.f;
+      const float var = ((x0 - mean) * (x0 - mean) + (x1 - mean) * (x1 - mean) +
+                         (x2 - mean) * (x2 - mean)) / 3.f;
+      const float sig = sqrtf(var);
+      su[i] = sig > thresh ? fmaxf(x0, fmaxf(x1, x2)) : w0 * x0 + w1 * x1 + w2 * x2;
+    }
+  }
+}
+
+template <typename T, int D>
+int run_nested(const void *K, long units, int Tn, int window, int n_blocks, int n_disc,
+               float lp0, float lp1, float lp2, float thresh, float *score, float *w_out,
+               float *a, void *ws, cudaStream_t st) {
+  const int blk = (Tn + n_blocks - 1) / n_blocks;
+  float *esum = static_cast<float *>(ws);
+  float *Dw = esum + units * (long)n_blocks * D;
+  const unsigned grid = (unsigned)(units * n_blocks);
+  const size_t ring = (size_t)NWARP * window * sizeof(float);
+  if (ensure_smem((const void *)anchors_kernel<T, D>, ring))
+    return cuda_failure(cudaErrorInvalidValue, "nested anchors kernel: shared memory");
+  anchors_kernel<T, D><<<grid, NT_SCAN, ring, st>>>(static_cast<const T *>(K), Tn, blk, n_blocks,
+                                                    window, esum, a);
+  int rc = launch_status();
+  if (rc) return rc;
+  global_kernel<T, D><<<grid, NT_SCAN, 0, st>>>(static_cast<const T *>(K), Tn, blk, n_blocks,
+                                                esum, a);
+  if ((rc = launch_status())) return rc;
+  disc_kernel<<<(unsigned)(units * 3), NT_DISC, 0, st>>>(a, Tn, n_disc, Dw);
+  if ((rc = launch_status())) return rc;
+  const dim3 fgrid((unsigned)min((Tn + 1023) / 1024, 64), (unsigned)min(units, 65535L));
+  final_kernel<<<fgrid, 256, 0, st>>>(a, Dw, Tn, units, lp0, lp1, lp2, thresh, score, w_out);
+  return launch_status();
+}
+
+}  // namespace
+
+size_t nested_workspace_bytes(long units, int T, int d, int n_blocks, bool with_a) {
+  size_t b = (size_t)units * n_blocks * d * sizeof(float) + (size_t)units * 4 * sizeof(float);
+  b = (b + 255) & ~(size_t)255;
+  if (with_a) b += (size_t)units * 3 * T * sizeof(float);
+  return b;
+}
+
+int launch_score_nested(const void *K, int B, int H, int T, int d, int dtype, int window,
+                        int n_blocks, int n_disc, float lp0, float lp1, float lp2, float thresh,
+                        float *score, float *w_out, float *a_out, void *ws, cudaStream_t st) {
+  const long units = (long)B * H;
+  float *a = a_out;
+  if (!a) {
+    const size_t off = nested_workspace_bytes(units, T, d, n_blocks, false);
+    a = reinterpret_cast<float *>(static_cast<char *>(ws) + off);
+  }
+  if (dtype == KV_BF16) {
+    if (d == 128)
+      return run_nested<__nv_bfloat16, 128>(K, units, T, window, n_blocks, n_disc, lp0, lp1, lp2,
+                                            thresh, score, w_out, a, ws, st);
+    return run_nested<__nv_bfloat16, 64>(K, units, T, window, n_blocks, n_disc, lp0, lp1, lp2,
+                                         thresh, score, w_out, a, ws, st);
+  }
+  if (d == 128)
+    return run_nested<float, 128>(K, units, T, window, n_blocks, n_disc, lp0, lp1, lp2, thresh,
+                                  score, w_out, a, ws, st);
+  return run_nested<float, 64>(K, units, T, window, n_blocks, n_disc, lp0, lp1, lp2, thresh, score,
+                               w_out, a, ws, st);
+}
+
+}  // namespace kvc

@@ -31,6 +31,7 @@ def lib():
     lib.h2o_decode_step_ex.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I, P, P,
                                        P, Z, P, P]
     lib.kv_select_budget.argtypes = [P, I, I, I, I, I, I, I, P, P, P]
+    lib.kv_score_nested.argtypes = [P, I, I, I, I, I, I, I, I, F, F, F, F, P, P, P, P, Z, P]
     lib.kv_compact_ragged.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, P, I, P, P, P, P, P]
     return lib
 
@@ -131,6 +132,25 @@ def test_layer_budget_entry_points_validate_on_the_host(lib):
     assert rag(1, 2, 8, 96, 4) == -2
     assert rag(1, 2, 8, 64, 4) == -1            # null pointers
     assert rag(0, 2, 8, 64, 4) == 0
+
+
+def test_nested_scorer_validates_on_the_host(lib):
+    def call(B=1, H=2, T=100, d=128, dt=0, window=64, nb=32, nd=10, lp=(0.0, 0.0, 0.0), th=0.1,
+             ws=NULL, wsb=0):
+        return lib.kv_score_nested(NULL, B, H, T, d, dt, window, nb, nd, lp[0], lp[1], lp[2], th,
+                                   NULL, NULL, NULL, ws, wsb, NULL)
+    assert call(nd=101) == -1                 # n_disc > T
+    assert call(nd=0) == -1
+    assert call(window=0) == -1
+    assert call(nb=0) == -1
+    assert call(th=float("nan")) == -1
+    assert call(lp=(float("inf"), 0.0, 0.0)) == -1
+    assert call(d=96) == -2
+    assert call(window=5000) == -2
+    assert call() == -1                       # null pointers
+    assert call(B=0) == 0
+    assert lib.kv_workspace_size(5, 1, 0, 8, 131072, 128, 32, 0) >= 8 * 3 * 131072 * 4
+    assert lib.kv_workspace_size(5, 1, 0, 8, 131072, 96, 32, 0) == 0
 
 
 def test_empty_batch_is_a_no_op(lib):
