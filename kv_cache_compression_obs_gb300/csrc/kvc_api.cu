@@ -31,11 +31,18 @@ int device_sm_count() {
   return n;
 }
 
-// Raise a kernel's dynamic shared-memory limit once per (device, kernel).
+// Raise a kernel's dynamic shared-memory limit once per (device, kernel) when its
+// static plus dynamic shared memory passes the 48 KB default.
 int ensure_smem(const void *func, size_t bytes) {
   static std::mutex mu;
   static std::unordered_map<const void *, size_t> done[64];
-  if (bytes <= 48 * 1024) return 0;
+  cudaFuncAttributes fa = {};
+  if (cudaFuncGetAttributes(&fa, func) != cudaSuccess) {
+    cudaGetLastError();
+    return 1;
+  }
+  const size_t static_bytes = fa.sharedSizeBytes;
+  if (bytes + static_bytes <= 48 * 1024) return 0;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
   std::lock_guard<std::mutex> lock(mu);
@@ -43,7 +50,7 @@ int ensure_smem(const void *func, size_t bytes) {
   if (it != done[dev].end() && it->second >= bytes) return 0;
   int optin = 0;
   cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  if ((size_t)optin < bytes) return 1;
+  if ((size_t)optin < bytes + static_bytes) return 1;
   if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
       cudaSuccess) {
     cudaGetLastError();

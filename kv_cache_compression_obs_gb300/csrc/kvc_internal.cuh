@@ -14,7 +14,9 @@ namespace kvc {
 constexpr int kNumSmsHint = 152;  // GB300; the launchers query the real count
 
 int device_sm_count();
-int ensure_smem(const void *func, size_t bytes);  // opt a kernel into > 48 KB of shared memory
+// Opt a kernel into `bytes` of dynamic shared memory when that plus its static
+// shared memory passes 48 KB; nonzero if the device cannot give it.
+int ensure_smem(const void *func, size_t bytes);
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

@@ -19,8 +19,11 @@
 //      kept as P (the current window-aligned chunk's prefix) + Q (the previous
 //      chunk's suffix, its total minus the rows that left the window), so every
 //      running sum restarts each `window` keys and rounding cannot drift; the
-//      rows leaving the window are re-read (L1/L2) and their 1/|k| comes from a
-//      per-warp ring in shared memory.  Writes a_c.
+//      rows leaving the window are re-read and their 1/|k| comes from a per-warp
+//      ring in shared memory.  A row's first read marks it evict_last in L2 and
+//      its re-read evict_first: only the rows inside some warp's window (tens of
+//      MB) are protected, so the re-reads hit L2 instead of HBM.  Packed f32x2
+//      arithmetic throughout.  Writes a_c.
 //   2. global_kernel: same grid; adds the unit's block sums into the stable
 //      anchor, re-reads the block's keys and writes a_s and a_e.
 //   3. disc_kernel: one CTA per (unit, scale): radix select (order-preserving
@@ -30,6 +33,7 @@
 // reduce in V-1 + (5 - log2 V) shuffles instead of 5 V.
 #include "kvc_internal.cuh"
 #include "select_common.cuh"
+#include "tc_common.cuh"
 
 namespace kvc {
 namespace {
@@ -38,38 +42,43 @@ constexpr int NWARP = 4;  // warps per CTA of the two key scans
 constexpr int NT_SCAN = NWARP * 32;
 constexpr int NT_DISC = 1024;
 
-// ---- row loads: lane holds features FPL*lane .. FPL*lane+FPL-1 ----------------
-template <typename T, int D> struct Row;
-template <> struct Row<__nv_bfloat16, 128> {
-  static constexpr int FPL = 4;
-  __device__ __forceinline__ static void load(const __nv_bfloat16 *row, int lane, float (&x)[4]) {
-    const uint2 v = __ldg(reinterpret_cast<const uint2 *>(row) + lane);
-    x[0] = __uint_as_float(v.x << 16);
-    x[1] = __uint_as_float(v.x & 0xFFFF0000u);
-    x[2] = __uint_as_float(v.y << 16);
-    x[3] = __uint_as_float(v.y & 0xFFFF0000u);
+// ---- row loads: lane holds features P2*2*lane .. as P2 float2 pairs -----------
+// Loads carry an L2 cache-policy operand (createpolicy): rows that will be read
+// again soon are kept (evict_last), rows read for the last time go first.
+template <int NW32> struct Words;
+template <> struct Words<1> {
+  __device__ __forceinline__ static void load(const void *p, uint64_t pol, uint32_t (&w)[1]) {
+    asm volatile("ld.global.nc.L2::cache_hint.u32 %0, [%1], %2;" : "=r"(w[0]) : "l"(p), "l"(pol));
   }
 };
-template <> struct Row<__nv_bfloat16, 64> {
-  static constexpr int FPL = 2;
-  __device__ __forceinline__ static void load(const __nv_bfloat16 *row, int lane, float (&x)[2]) {
-    const uint32_t v = __ldg(reinterpret_cast<const uint32_t *>(row) + lane);
-    x[0] = __uint_as_float(v << 16);
-    x[1] = __uint_as_float(v & 0xFFFF0000u);
+template <> struct Words<2> {
+  __device__ __forceinline__ static void load(const void *p, uint64_t pol, uint32_t (&w)[2]) {
+    asm volatile("ld.global.nc.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;"
+                 : "=r"(w[0]), "=r"(w[1]) : "l"(p), "l"(pol));
   }
 };
-template <> struct Row<float, 128> {
-  static constexpr int FPL = 4;
-  __device__ __forceinline__ static void load(const float *row, int lane, float (&x)[4]) {
-    const float4 v = __ldg(reinterpret_cast<const float4 *>(row) + lane);
-    x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+template <> struct Words<4> {
+  __device__ __forceinline__ static void load(const void *p, uint64_t pol, uint32_t (&w)[4]) {
+    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "l"(p), "l"(pol));
   }
 };
-template <> struct Row<float, 64> {
-  static constexpr int FPL = 2;
-  __device__ __forceinline__ static void load(const float *row, int lane, float (&x)[2]) {
-    const float2 v = __ldg(reinterpret_cast<const float2 *>(row) + lane);
-    x[0] = v.x; x[1] = v.y;
+
+template <typename T, int D> struct Row {
+  static constexpr int F = D / 32;                          // features per lane
+  static constexpr int P2 = F / 2;                          // float2 pairs per lane
+  static constexpr int NW = F * (int)sizeof(T) / 4;         // 32-bit words per lane
+  __device__ __forceinline__ static void load(const T *row, int lane, uint64_t pol, float2 (&x)[P2]) {
+    uint32_t w[NW];
+    Words<NW>::load(reinterpret_cast<const char *>(row) + lane * NW * 4, pol, w);
+    if constexpr (sizeof(T) == 2) {  // bf16: a word holds two features
+#pragma unroll
+      for (int p = 0; p < P2; ++p)
+        x[p] = make_float2(__uint_as_float(w[p] << 16), __uint_as_float(w[p] & 0xFFFF0000u));
+    } else {
+#pragma unroll
+      for (int p = 0; p < P2; ++p) x[p] = make_float2(__uint_as_float(w[2 * p]), __uint_as_float(w[2 * p + 1]));
+    }
   }
 };
 
@@ -99,11 +108,7 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[V], int lane) {
   return v[0];
 }
 
-// -cos between a key (squared norm nk) and an anchor (norm nm), 0 for a zero norm.
-__device__ __forceinline__ float neg_cos(float dot, float nk2, float nm) {
-  const float den = sqrtf(nk2) * nm;
-  return den > 0.f ? -(dot / den) : 0.f;
-}
+__device__ __forceinline__ float hsum(float2 a) { return a.x + a.y; }
 
 // Token range of warp w inside [lo, hi): equal spans.
 __device__ __forceinline__ void warp_range(int lo, int hi, int w, int &s, int &e) {
@@ -119,131 +124,164 @@ __global__ __launch_bounds__(NT_SCAN) void anchors_kernel(const T *__restrict__ 
                                                           float *__restrict__ esum,
                                                           float *__restrict__ a) {
   using R = Row<T, D>;
-  constexpr int F = R::FPL;
-  extern __shared__ float ring_all[];  // [NWARP][window] 1/|k| of the last rows
+  constexpr int P2 = R::P2;
+  // [NWARP][window + 4]: 1/|k| of row j at slot j % (window + 4).  A batch writes
+  // four distinct slots and never one that it reads (rows i - window < i0 sit at
+  // least window + 1 rows back), so no two lanes touch a slot in the same batch.
+  extern __shared__ float ring_all[];
   __shared__ float sums[NWARP][D];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const long unit = blockIdx.x / n_blocks;
   const int bj = blockIdx.x % n_blocks;
   const int lo = min(Tn, bj * blk), hi = min(Tn, lo + blk);
   const T *Ku = K + unit * (long)Tn * D;
-  float *ring = ring_all + warp * window;
+  const int RW = window + 4;
+  float *ring = ring_all + warp * RW;
   float *ac = a + (unit * 3 + 2) * (long)Tn;
+  const uint64_t keep_pol = tc::make_policy_evict_last();   // read again `window` rows later
+  const uint64_t last_pol = tc::make_policy_evict_first();  // last read
 
   int s, e;
   warp_range(lo, hi, warp, s, e);
-  float es[F];
+  float2 tot[P2], sil[P2];  // sums of kh over [c0, e) and over [c0, s)
 #pragma unroll
-  for (int f = 0; f < F; ++f) es[f] = 0.f;
+  for (int p = 0; p < P2; ++p) tot[p] = sil[p] = make_float2(0.f, 0.f);
 
   if (s < e) {
-    const int c0 = (s / window) * window;  // first chunk start the warp walks from
-    float P[F], Q[F];
+    const int c0 = (s / window) * window;  // the chunk start the warp walks from
+    float2 P[P2], Q[P2];
 #pragma unroll
-    for (int f = 0; f < F; ++f) P[f] = Q[f] = 0.f;
+    for (int p = 0; p < P2; ++p) P[p] = Q[p] = make_float2(0.f, 0.f);
     // warm-up: the full chunk before c0 (its total starts Q; its 1/|k| fill the ring)
     if (c0 > 0) {
       for (int i0 = c0 - window; i0 < c0; i0 += 4) {
-        float x[4][F], ss[4];
+        float2 x[4][P2];
+        float ss[4];
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-          const int i = i0 + t;
-          if (i < c0) R::load(Ku + (long)i * D, lane, x[t]);
+          if (i0 + t < c0) R::load(Ku + (long)(i0 + t) * D, lane, keep_pol, x[t]);
           else {
 #pragma unroll
-            for (int f = 0; f < F; ++f) x[t][f] = 0.f;
+            for (int p = 0; p < P2; ++p) x[t][p] = make_float2(0.f, 0.f);
           }
-          ss[t] = 0.f;
+          float2 q2 = __fmul2_rn(x[t][0], x[t][0]);
 #pragma unroll
-          for (int f = 0; f < F; ++f) ss[t] = fmaf(x[t][f], x[t][f], ss[t]);
+          for (int p = 1; p < P2; ++p) q2 = __ffma2_rn(x[t][p], x[t][p], q2);
+          ss[t] = hsum(q2);
         }
-        const float tot = reduce_scatter<4>(ss, lane);
-        const float my_inv = tot > 0.f ? 1.f / sqrtf(tot) : 0.f;
+        const float tt = reduce_scatter<4>(ss, lane);
+        const float my_inv = tt > 0.f ? rsqrtf(tt) : 0.f;
+        const int mt = lane >> 3;
+        if ((lane & 7) == 0 && i0 + mt < c0) ring[(i0 + mt) % RW] = my_inv;
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
-          const int i = i0 + t;
           const float inv = __shfl_sync(0xFFFFFFFFu, my_inv, t * 8);
-          if (i < c0) {
+          if (i0 + t < c0) {
+            const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
-            for (int f = 0; f < F; ++f) P[f] = fmaf(x[t][f], inv, P[f]);
-            if (lane == 0) ring[i % window] = inv;
+            for (int p = 0; p < P2; ++p) P[p] = __ffma2_rn(x[t][p], inv2, P[p]);
           }
         }
       }
     }
+    // the first chunk reset moves the warm-up total into Q; keep it out of `tot`
+#pragma unroll
+    for (int p = 0; p < P2; ++p) tot[p] = make_float2(-P[p].x, -P[p].y);
     __syncwarp();
     int r = 0;  // i - (chunk start), i.e. i % window, kept as a running counter
     for (int i0 = c0; i0 < e; i0 += 4) {
-      float x[4][F], y[4][F], ss[4];
+      float2 x[4][P2], y[4][P2];
+      float ss[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         const int i = i0 + t;
-        if (i < e) R::load(Ku + (long)i * D, lane, x[t]);
+        if (i < e) R::load(Ku + (long)i * D, lane, keep_pol, x[t]);
         else {
 #pragma unroll
-          for (int f = 0; f < F; ++f) x[t][f] = 0.f;
+          for (int p = 0; p < P2; ++p) x[t][p] = make_float2(0.f, 0.f);
         }
-        if (i < e && i >= window) R::load(Ku + (long)(i - window) * D, lane, y[t]);
+        if (i < e && i >= window) R::load(Ku + (long)(i - window) * D, lane, last_pol, y[t]);
         else {
 #pragma unroll
-          for (int f = 0; f < F; ++f) y[t][f] = 0.f;
+          for (int p = 0; p < P2; ++p) y[t][p] = make_float2(0.f, 0.f);
         }
-        ss[t] = 0.f;
+        float2 q2 = __fmul2_rn(x[t][0], x[t][0]);
 #pragma unroll
-        for (int f = 0; f < F; ++f) ss[t] = fmaf(x[t][f], x[t][f], ss[t]);
+        for (int p = 1; p < P2; ++p) q2 = __ffma2_rn(x[t][p], x[t][p], q2);
+        ss[t] = hsum(q2);
       }
-      const float tot = reduce_scatter<4>(ss, lane);
-      const float my_inv = tot > 0.f ? 1.f / sqrtf(tot) : 0.f;
+      const float tt = reduce_scatter<4>(ss, lane);
+      // lanes 8t own token t: swap its 1/|k| into the ring, take out the leaving row's
+      const float my_inv = tt > 0.f ? rsqrtf(tt) : 0.f;
+      float my_old = 0.f;
+      {
+        const int mt = lane >> 3, i = i0 + mt;
+        if ((lane & 7) == 0 && i < e) {
+          if (i >= window && i - window < i0) my_old = ring[(i - window) % RW];
+          ring[i % RW] = my_inv;
+        }
+      }
       float part[8];
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         const int i = i0 + t;
         const float inv = __shfl_sync(0xFFFFFFFFu, my_inv, t * 8);
+        float old = __shfl_sync(0xFFFFFFFFu, my_old, t * 8);
+        if (window < 4) {  // the leaving row may be in this very batch
+          const float same = __shfl_sync(0xFFFFFFFFu, my_inv, 8 * max(t - window, 0));
+          if (t >= window) old = same;
+        }
         float dot = 0.f, nrm = 0.f;
         if (i < e) {
           if (r == 0) {  // a new chunk: the previous chunk's total becomes Q
 #pragma unroll
-            for (int f = 0; f < F; ++f) {
-              Q[f] = P[f];
-              P[f] = 0.f;
+            for (int p = 0; p < P2; ++p) {
+              tot[p] = __fadd2_rn(tot[p], P[p]);
+              Q[p] = P[p];
+              P[p] = make_float2(0.f, 0.f);
             }
           }
-          const float inv_old = (i >= window) ? ring[r] : 0.f;  // 1/|k_{i-window}|
-          __syncwarp();
-          if (lane == 0) ring[r] = inv;
+          const float2 inv2 = make_float2(inv, inv), nold2 = make_float2(-old, -old);
+          float2 d2 = make_float2(0.f, 0.f), n2 = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int f = 0; f < F; ++f) {
-            const float kh = x[t][f] * inv;
-            P[f] += kh;
-            Q[f] = fmaf(-y[t][f], inv_old, Q[f]);
-            const float wsum = P[f] + Q[f];
-            dot = fmaf(kh, wsum, dot);
-            nrm = fmaf(wsum, wsum, nrm);
-            if (i >= s) es[f] += kh;
+          for (int p = 0; p < P2; ++p) {
+            P[p] = __ffma2_rn(x[t][p], inv2, P[p]);
+            Q[p] = __ffma2_rn(y[t][p], nold2, Q[p]);
+            const float2 w = __fadd2_rn(P[p], Q[p]);
+            d2 = __ffma2_rn(x[t][p], w, d2);
+            n2 = __ffma2_rn(w, w, n2);
           }
-          __syncwarp();
+          dot = hsum(d2);
+          nrm = hsum(n2);
+          if (i == s - 1) {
+#pragma unroll
+            for (int p = 0; p < P2; ++p) sil[p] = P[p];
+          }
           r = (r + 1 == window) ? 0 : r + 1;
         }
         part[2 * t] = dot;
         part[2 * t + 1] = nrm;
       }
       const float v = reduce_scatter<8>(part, lane);
-      // lane l holds value l / 4: even values are dots, odd ones the window's |.|^2
+      // lane 8t holds token t's <k, window sum> and 1/|k|; lane 8t+4 the window's |.|^2
       const float nrm = __shfl_down_sync(0xFFFFFFFFu, v, 4);
-      const int idx = lane >> 2;
       if ((lane & 7) == 0) {
-        const int i = i0 + (idx >> 1);
-        // kh has norm 1 (or is zero, and then the dot is 0): cos = dot / |window sum|
-        if (i >= s && i < e) {
-          const float nw = sqrtf(nrm);
-          ac[i] = nw > 0.f ? -(v / nw) : 0.f;
-        }
+        const int i = i0 + (lane >> 3);
+        // cos(kh_i, window sum) with |kh_i| = 1 (a zero key has dot 0)
+        if (i >= s && i < e) ac[i] = nrm > 0.f ? -(v * my_inv) * rsqrtf(nrm) : 0.f;
       }
+      __syncwarp();  // this batch's ring writes before the next batch's reads
     }
+#pragma unroll
+    for (int p = 0; p < P2; ++p)
+      tot[p] = __fadd2_rn(__fadd2_rn(tot[p], P[p]), make_float2(-sil[p].x, -sil[p].y));
   }
   // block sum of kh over the warps
 #pragma unroll
-  for (int f = 0; f < F; ++f) sums[warp][lane * F + f] = es[f];
+  for (int p = 0; p < P2; ++p) {
+    sums[warp][lane * 2 * P2 + 2 * p] = tot[p].x;
+    sums[warp][lane * 2 * P2 + 2 * p + 1] = tot[p].y;
+  }
   __syncthreads();
   for (int f = threadIdx.x; f < D; f += NT_SCAN) {
     float t = 0.f;
@@ -260,7 +298,7 @@ __global__ __launch_bounds__(NT_SCAN) void global_kernel(const T *__restrict__ K
                                                          const float *__restrict__ esum,
                                                          float *__restrict__ a) {
   using R = Row<T, D>;
-  constexpr int F = R::FPL;
+  constexpr int P2 = R::P2;
   __shared__ float S[D], E[D];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const long unit = blockIdx.x / n_blocks;
@@ -285,38 +323,43 @@ __global__ __launch_bounds__(NT_SCAN) void global_kernel(const T *__restrict__ K
     ns += __shfl_xor_sync(0xFFFFFFFFu, ns, o);
     ne += __shfl_xor_sync(0xFFFFFFFFu, ne, o);
   }
-  const float nS = sqrtf(ns), nE = sqrtf(ne);
-  float sl[F], el[F];
+  const float rS = ns > 0.f ? rsqrtf(ns) : 0.f, rE = ne > 0.f ? rsqrtf(ne) : 0.f;
+  float2 sl[P2], el[P2];
 #pragma unroll
-  for (int f = 0; f < F; ++f) {
-    sl[f] = S[lane * F + f];
-    el[f] = E[lane * F + f];
+  for (int p = 0; p < P2; ++p) {
+    sl[p] = make_float2(S[lane * 2 * P2 + 2 * p], S[lane * 2 * P2 + 2 * p + 1]);
+    el[p] = make_float2(E[lane * 2 * P2 + 2 * p], E[lane * 2 * P2 + 2 * p + 1]);
   }
+  const uint64_t pol = tc::make_policy_evict_first();
   const T *Ku = K + unit * (long)Tn * D;
   float *as = a + (unit * 3 + 0) * (long)Tn;
   float *ae = a + (unit * 3 + 1) * (long)Tn;
   int s, e;
   warp_range(lo, hi, warp, s, e);
   for (int i0 = s; i0 < e; i0 += 4) {
+    float2 x[4][P2];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      if (i0 + t < e) R::load(Ku + (long)(i0 + t) * D, lane, pol, x[t]);
+      else {
+#pragma unroll
+        for (int p = 0; p < P2; ++p) x[t][p] = make_float2(0.f, 0.f);
+      }
+    }
     float part[16];
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      float x[F];
-      if (i0 + t < e) R::load(Ku + (long)(i0 + t) * D, lane, x);
-      else {
+      float2 ds = __fmul2_rn(x[t][0], sl[0]), de = __fmul2_rn(x[t][0], el[0]),
+             nk = __fmul2_rn(x[t][0], x[t][0]);
 #pragma unroll
-        for (int f = 0; f < F; ++f) x[f] = 0.f;
+      for (int p = 1; p < P2; ++p) {
+        ds = __ffma2_rn(x[t][p], sl[p], ds);
+        de = __ffma2_rn(x[t][p], el[p], de);
+        nk = __ffma2_rn(x[t][p], x[t][p], nk);
       }
-      float ds = 0.f, de = 0.f, nk = 0.f;
-#pragma unroll
-      for (int f = 0; f < F; ++f) {
-        ds = fmaf(x[f], sl[f], ds);
-        de = fmaf(x[f], el[f], de);
-        nk = fmaf(x[f], x[f], nk);
-      }
-      part[4 * t] = ds;
-      part[4 * t + 1] = de;
-      part[4 * t + 2] = nk;
+      part[4 * t] = hsum(ds);
+      part[4 * t + 1] = hsum(de);
+      part[4 * t + 2] = hsum(nk);
       part[4 * t + 3] = 0.f;
     }
     const float v = reduce_scatter<16>(part, lane);
@@ -326,8 +369,9 @@ __global__ __launch_bounds__(NT_SCAN) void global_kernel(const T *__restrict__ K
     if ((lane & 7) == 0) {
       const int i = i0 + (lane >> 3);
       if (i < e) {
-        as[i] = neg_cos(v, nk, nS);
-        ae[i] = neg_cos(de, nk, nE);
+        const float rk = nk > 0.f ? rsqrtf(nk) : 0.f;
+        as[i] = -(v * rk) * rS;
+        ae[i] = -(de * rk) * rE;
       }
     }
   }
@@ -467,7 +511,7 @@ int run_nested(const void *K, long units, int Tn, int window, int n_blocks, int 
   float *esum = static_cast<float *>(ws);
   float *Dw = esum + units * (long)n_blocks * D;
   const unsigned grid = (unsigned)(units * n_blocks);
-  const size_t ring = (size_t)NWARP * window * sizeof(float);
+  const size_t ring = (size_t)NWARP * (window + 4) * sizeof(float);
   if (ensure_smem((const void *)anchors_kernel<T, D>, ring))
     return cuda_failure(cudaErrorInvalidValue, "nested anchors kernel: shared memory");
   anchors_kernel<T, D><<<grid, NT_SCAN, ring, st>>>(static_cast<const T *>(K), Tn, blk, n_blocks,

@@ -49,115 +49,59 @@ constexpr int kMaxHeads = 256;
 constexpr int kMaxOwned = kMaxHeads / kMaxCluster;  // heads per CTA when H > 8
 constexpr uint64_t kNone = ~0ull;                   // above every key: selects nothing
 
-__device__ __forceinline__ uint64_t pair_key(float z, uint32_t flat) {
-  return ((uint64_t)order_key(z) << 32) | (uint64_t)(0xFFFFFFFFu - flat);
-}
-
 struct Smem {
-  uint32_t hist[NW][256];
-  uint32_t tot[2][256];         // this CTA's histogram of a pass, read by the cluster
-  uint32_t gsum[256];           // the cluster's histogram of a pass
+  RadixScratch<NT> rx;
   uint64_t theta[kMaxHeads];    // floor thresholds (owned heads' entries only)
   int cnt[kMaxHeads];           // kept positions per head, written by the owners
   int offs[kMaxHeads + 1];
   int wcnt[kMaxOwned][NW];      // kept middle pairs per (owned head, warp range)
-  uint64_t sh_prefix;
-  int sh_need, sh_done;
 };
 
-// Threshold thr such that exactly `need` candidate keys are >= thr, for unique
-// keys and 1 <= need <= number of candidates.  visit(f) calls f(key) for every
-// candidate key this thread owns.  CLUSTER: the candidates are spread over the
-// cluster's CTAs, each histogramming its own; every CTA reads the others'
-// histograms and takes the same decision, so all run the same passes.
-template <bool CLUSTER, typename Visit>
-__device__ uint64_t radix_select(Smem &sm, int need, Visit visit) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  uint64_t prefix = 0, hmask = 0;
-  for (int pass = 0; pass < 8; ++pass) {
-    const int shift = 56 - 8 * pass;
-    const int buf = pass & 1;
-    for (int e = threadIdx.x; e < NW * 256; e += NT) (&sm.hist[0][0])[e] = 0u;
-    __syncthreads();
-    visit([&](uint64_t key) {
-      if ((key & hmask) == prefix) atomicAdd(&sm.hist[warp][(uint32_t)(key >> shift) & 255u], 1u);
-    });
-    __syncthreads();
-    if (threadIdx.x < 256) {
-      uint32_t t = 0;
-#pragma unroll 8
-      for (int w = 0; w < NW; ++w) t += sm.hist[w][threadIdx.x];
-      sm.tot[buf][threadIdx.x] = t;
-    }
-    if constexpr (CLUSTER) {
-      // tot[buf] is rewritten two passes later, after the next cluster barrier,
-      // by which time every CTA has finished reading it.
-      cg::cluster_group cl = cg::this_cluster();
-      cl.sync();
-      if (threadIdx.x < 256) {
-        uint32_t g = 0;
-        for (unsigned r = 0; r < cl.num_blocks(); ++r)
-          g += cl.map_shared_rank(&sm.tot[buf][0], r)[threadIdx.x];
-        sm.gsum[threadIdx.x] = g;
-      }
-    } else {
-      if (threadIdx.x < 256) sm.gsum[threadIdx.x] = sm.tot[buf][threadIdx.x];
-    }
-    __syncthreads();
-    if (warp == 0) {
-      // lane l owns digits 255-8l .. 248-8l (descending)
-      uint32_t mine = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mine += sm.gsum[255 - 8 * lane - i];
-      uint32_t incl = mine;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-        if (lane >= off) incl += y;
-      }
-      uint32_t above = incl - mine;
-      if (above < (uint32_t)need && (uint32_t)need <= incl) {
-#pragma unroll 1
-        for (int i = 0; i < 8; ++i) {
-          const int dgt = 255 - 8 * lane - i;
-          const uint32_t c = sm.gsum[dgt];
-          if ((uint32_t)need <= above + c) {
-            sm.sh_prefix = prefix | ((uint64_t)dgt << shift);
-            sm.sh_need = need - (int)above;
-            sm.sh_done = ((uint32_t)need == above + c);
-            break;
-          }
-          above += c;
-        }
-      }
-    }
-    __syncthreads();
-    prefix = sm.sh_prefix;
-    need = sm.sh_need;
-    const int done = sm.sh_done;
-    hmask |= 255ull << shift;
-    __syncthreads();  // sh_* and gsum are rewritten by the next pass
-    if (done) break;
-  }
-  return prefix;  // at the last digit unique keys fill the boundary bucket exactly
+// A head's middle range [0, n) split for 16-byte loads: `pre` scalars up to the
+// first 16-byte boundary, n4 float4 vectors, then the scalars from `tail` on.
+struct Split {
+  int pre, n4, tail;
+};
+__device__ __forceinline__ Split split_of(const float *zm, int n) {
+  const int mis = (int)((reinterpret_cast<uintptr_t>(zm) >> 2) & 3);
+  Split sp;
+  sp.pre = min(n, (4 - mis) & 3);
+  sp.n4 = (n - sp.pre) >> 2;
+  sp.tail = sp.pre + 4 * sp.n4;
+  return sp;
 }
 
 // Calls f(key) for the middle pairs of one head, positions [S, S + n), with
-// strided coalesced loads, four in flight per thread.
+// strided coalesced 16-byte loads, four in flight per thread (64 KB per CTA:
+// enough to cover the latency of the repeated passes over L2).
 template <typename F>
 __device__ __forceinline__ void for_head(const float *__restrict__ zm, uint32_t flat0, int n, F &&f) {
-  for (int base = threadIdx.x; base < n; base += 4 * NT) {
-    float v[4];
+  const Split sp = split_of(zm, n);
+  const float4 *z4 = reinterpret_cast<const float4 *>(zm + sp.pre);
+  for (int base = threadIdx.x; base < sp.n4; base += 4 * NT) {
+    float4 v[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int i = base + u * NT;
-      v[u] = (i < n) ? __ldg(zm + i) : 0.f;
+      const int j = base + u * NT;
+      v[u] = (j < sp.n4) ? __ldg(z4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const int i = base + u * NT;
-      if (i < n) f(pair_key(v[u], flat0 + (uint32_t)i));
+      const int j = base + u * NT;
+      if (j < sp.n4) {
+        const uint32_t i = flat0 + (uint32_t)(sp.pre + 4 * j);
+        f(pair_key(v[u].x, i));
+        f(pair_key(v[u].y, i + 1));
+        f(pair_key(v[u].z, i + 2));
+        f(pair_key(v[u].w, i + 3));
+      }
     }
+  }
+  const int t = threadIdx.x, nt = n - sp.tail;
+  if (t < sp.pre) f(pair_key(__ldg(zm + t), flat0 + (uint32_t)t));
+  else if (t < sp.pre + nt) {
+    const int i = sp.tail + (t - sp.pre);
+    f(pair_key(__ldg(zm + i), flat0 + (uint32_t)i));
   }
 }
 
@@ -182,7 +126,7 @@ __global__ __launch_bounds__(NT, 1) void select_budget_kernel(
   for (int h = rank; h < H; h += CL) {
     uint64_t th = kNone;
     if (nf > 0)
-      th = radix_select<false>(sm, nf, [&](auto &&f) { for_head(zmid(h), flat0(h), n, f); });
+      th = radix_select_ge<NT, false>(sm.rx, nf, [&](auto &&f) { for_head(zmid(h), flat0(h), n, f); });
     if (threadIdx.x == 0) sm.theta[h] = th;
   }
   __syncthreads();
@@ -190,7 +134,7 @@ __global__ __launch_bounds__(NT, 1) void select_budget_kernel(
   // 2. competition over the middle pairs below their head's floor threshold
   uint64_t tau = kNone;
   if (extra > 0) {
-    tau = radix_select<true>(sm, (int)extra, [&](auto &&f) {
+    tau = radix_select_ge<NT, true>(sm.rx, (int)extra, [&](auto &&f) {
       for (int h = rank; h < H; h += CL) {
         const uint64_t th = sm.theta[h];
         for_head(zmid(h), flat0(h), n, [&](uint64_t key) {
@@ -200,16 +144,28 @@ __global__ __launch_bounds__(NT, 1) void select_budget_kernel(
     });
   }
 
-  // 3. kept middle pairs per owned head and warp range; counts to every CTA
-  const int per = ((n + NW - 1) / NW + 31) & ~31;
-  const int lo = min(n, warp * per), hi = min(n, lo + per);
+  // 3. kept middle pairs per owned head and warp: warp 0 takes the scalars before
+  // the first 16-byte boundary, every warp a contiguous run of float4 vectors,
+  // the last warp the scalar tail; counts to every CTA of the cluster
   for (int h = rank, j = 0; h < H; h += CL, ++j) {
     const uint64_t lam = min(sm.theta[h], tau);
     const float *zm = zmid(h);
     const uint32_t f0 = flat0(h);
+    const Split sp = split_of(zm, n);
+    const float4 *z4 = reinterpret_cast<const float4 *>(zm + sp.pre);
+    const int per4 = (sp.n4 + NW - 1) / NW;
+    const int b0 = min(sp.n4, warp * per4), b1 = min(sp.n4, b0 + per4);
     int c = 0;
+    if (warp == 0 && lane < sp.pre) c += pair_key(__ldg(zm + lane), f0 + (uint32_t)lane) >= lam;
 #pragma unroll 4
-    for (int i = lo + lane; i < hi; i += 32) c += pair_key(__ldg(zm + i), f0 + (uint32_t)i) >= lam;
+    for (int q = b0 + lane; q < b1; q += 32) {
+      const float4 v = __ldg(z4 + q);
+      const uint32_t i = f0 + (uint32_t)(sp.pre + 4 * q);
+      c += (pair_key(v.x, i) >= lam) + (pair_key(v.y, i + 1) >= lam) +
+           (pair_key(v.z, i + 2) >= lam) + (pair_key(v.w, i + 3) >= lam);
+    }
+    if (warp == NW - 1 && lane < n - sp.tail)
+      c += pair_key(__ldg(zm + sp.tail + lane), f0 + (uint32_t)(sp.tail + lane)) >= lam;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
     if (lane == 0) sm.wcnt[j][warp] = c;
@@ -250,13 +206,54 @@ __global__ __launch_bounds__(NT, 1) void select_budget_kernel(
     const uint64_t lam = min(sm.theta[h], tau);
     const float *zm = zmid(h);
     const uint32_t f0 = flat0(h);
+    const Split sp = split_of(zm, n);
+    const float4 *z4 = reinterpret_cast<const float4 *>(zm + sp.pre);
+    const int per4 = (sp.n4 + NW - 1) / NW;
+    const int b0 = min(sp.n4, warp * per4), b1 = min(sp.n4, b0 + per4);
     int32_t *mid = out + S;
-    for (int i0 = lo; i0 < hi; i0 += 32) {
-      const int i = i0 + lane;
-      const bool keep = i < hi && pair_key(__ldg(zm + i), f0 + (uint32_t)i) >= lam;
+    const unsigned below = (1u << lane) - 1u;
+    if (warp == 0) {
+      const bool keep = lane < sp.pre && pair_key(__ldg(zm + lane), f0 + (uint32_t)lane) >= lam;
       const unsigned m = __ballot_sync(0xFFFFFFFFu, keep);
-      if (keep) mid[run + __popc(m & ((1u << lane) - 1u))] = S + i;
+      const int slot = run + __popc(m & below);
+      if (keep && slot < kept_mid) mid[slot] = S + lane;
       run += __popc(m);
+    }
+    for (int q0 = b0; q0 < b1; q0 += 32) {
+      const int q = q0 + lane;
+      bool k0 = false, k1 = false, k2 = false, k3 = false;
+      const int i = sp.pre + 4 * q;
+      if (q < b1) {
+        const float4 v = __ldg(z4 + q);
+        const uint32_t fi = f0 + (uint32_t)i;
+        k0 = pair_key(v.x, fi) >= lam;
+        k1 = pair_key(v.y, fi + 1) >= lam;
+        k2 = pair_key(v.z, fi + 2) >= lam;
+        k3 = pair_key(v.w, fi + 3) >= lam;
+      }
+      const int c = (int)k0 + (int)k1 + (int)k2 + (int)k3;
+      int incl = c;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      int slot = run + incl - c;
+      if (k0 && slot < kept_mid) mid[slot] = S + i;
+      slot += k0;
+      if (k1 && slot < kept_mid) mid[slot] = S + i + 1;
+      slot += k1;
+      if (k2 && slot < kept_mid) mid[slot] = S + i + 2;
+      slot += k2;
+      if (k3 && slot < kept_mid) mid[slot] = S + i + 3;
+      run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    if (warp == NW - 1) {
+      const int i = sp.tail + lane;
+      const bool keep = i < n && pair_key(__ldg(zm + i), f0 + (uint32_t)i) >= lam;
+      const unsigned m = __ballot_sync(0xFFFFFFFFu, keep);
+      const int slot = run + __popc(m & below);
+      if (keep && slot < kept_mid) mid[slot] = S + i;
     }
   }
 }

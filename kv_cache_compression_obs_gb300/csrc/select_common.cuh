@@ -43,3 +43,110 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_sums, int *
 }
 
 }  // namespace kvc
+
+#include <cooperative_groups.h>
+
+namespace kvc {
+
+// Scratch of radix_select_ge for an NT-thread block.
+template <int NT>
+struct RadixScratch {
+  static constexpr int NW = NT / 32;
+  uint32_t hist[NW][256];  // per-warp histograms
+  uint32_t tot[2][256];    // this CTA's histogram of a pass (read by the cluster)
+  uint32_t gsum[256];      // the (cluster's) histogram of a pass
+  uint64_t sh_prefix;
+  int sh_need, sh_done;
+};
+
+// Threshold thr such that exactly `need` candidate keys are >= thr, for unique
+// 64-bit keys and 1 <= need <= number of candidates.  visit(f) calls f(key) for
+// every candidate key this thread owns.  8-bit digits, most significant first;
+// the search stops as soon as the boundary digit's bucket is taken whole (at
+// the last digit unique keys always fill it exactly).  CLUSTER: the candidates
+// are spread over the cluster's CTAs, each histogramming its own and summing
+// all of them through distributed shared memory, so every CTA takes the same
+// decisions and runs the same passes.  Every thread of every CTA must call.
+template <int NT, bool CLUSTER, typename Visit>
+__device__ uint64_t radix_select_ge(RadixScratch<NT> &sm, int need, Visit visit) {
+  constexpr int NW = NT / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint64_t prefix = 0, hmask = 0;
+  for (int pass = 0; pass < 8; ++pass) {
+    const int shift = 56 - 8 * pass;
+    const int buf = pass & 1;
+    for (int e = threadIdx.x; e < NW * 256; e += NT) (&sm.hist[0][0])[e] = 0u;
+    __syncthreads();
+    visit([&](uint64_t key) {
+      if ((key & hmask) == prefix) atomicAdd(&sm.hist[warp][(uint32_t)(key >> shift) & 255u], 1u);
+    });
+    __syncthreads();
+    for (int d = threadIdx.x; d < 256; d += NT) {
+      uint32_t t = 0;
+#pragma unroll 8
+      for (int w = 0; w < NW; ++w) t += sm.hist[w][d];
+      sm.tot[buf][d] = t;
+    }
+    if constexpr (CLUSTER) {
+      // tot[buf] is rewritten two passes later, after the next cluster barrier,
+      // by which time every CTA has finished reading it.
+      cooperative_groups::cluster_group cl = cooperative_groups::this_cluster();
+      cl.sync();
+      for (int d = threadIdx.x; d < 256; d += NT) {
+        uint32_t g = 0;
+        for (unsigned r = 0; r < cl.num_blocks(); ++r) g += cl.map_shared_rank(&sm.tot[buf][0], r)[d];
+        sm.gsum[d] = g;
+      }
+    } else {
+      for (int d = threadIdx.x; d < 256; d += NT) sm.gsum[d] = sm.tot[buf][d];
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l owns digits 255-8l .. 248-8l (descending)
+      uint32_t mine = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mine += sm.gsum[255 - 8 * lane - i];
+      uint32_t incl = mine;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      uint32_t above = incl - mine;
+      if (above < (uint32_t)need && (uint32_t)need <= incl) {
+#pragma unroll 1
+        for (int i = 0; i < 8; ++i) {
+          const int dgt = 255 - 8 * lane - i;
+          const uint32_t c = sm.gsum[dgt];
+          if ((uint32_t)need <= above + c) {
+            sm.sh_prefix = prefix | ((uint64_t)dgt << shift);
+            sm.sh_need = need - (int)above;
+            sm.sh_done = ((uint32_t)need == above + c);
+            break;
+          }
+          above += c;
+        }
+      }
+    }
+    __syncthreads();
+    prefix = sm.sh_prefix;
+    need = sm.sh_need;
+    const int done = sm.sh_done;
+    hmask |= 255ull << shift;
+    __syncthreads();  // sh_* and gsum are rewritten by the next pass
+    if (done) break;
+  }
+  return prefix;
+}
+
+// Unique 64-bit selection key of element `flat`: the order-preserving image of z
+// in the high word, ~flat in the low word, so that descending keys are
+// (z descending, flat ascending).
+__device__ __forceinline__ uint64_t pair_key(float z, uint32_t flat) {
+  return ((uint64_t)order_key(z) << 32) | (uint64_t)(0xFFFFFFFFu - flat);
+}
+__device__ __forceinline__ uint64_t pair_key_u(uint32_t okey, uint32_t flat) {
+  return ((uint64_t)okey << 32) | (uint64_t)(0xFFFFFFFFu - flat);
+}
+
+}  // namespace kvc

@@ -6,7 +6,18 @@
 // With S sinks (KV-cache survey blog §4.1-4.2) the first S positions are kept
 // too and the heavy part is the k - R - S best of [S, T - R).
 //
-// One 1024-thread block per head:
+// Resident kernel (every head with at most 8 x 49152 candidates): one
+// thread-block cluster of CL CTAs per head; CTA c holds its contiguous slice of
+// the head's candidates in shared memory as order-preserving keys, so z is read
+// from HBM exactly once.  Each candidate's 64-bit key (z's key, ~position) is
+// unique and orders exactly as (z descending, position ascending); a radix
+// select over the slices (histograms summed through distributed shared memory)
+// finds the threshold with exactly k - R - S keys at or above it.  Per-warp
+// counts over contiguous ranges, an exclusive sum over the cluster's CTAs, and
+// warp ballots emit the kept positions already ascending.
+//
+// Streaming kernel (longer heads): one 1024-thread block per head re-reads z
+// (from L2) once per radix pass:
 //   1. exact radix select (4 passes of 8 bits over order-preserving uint32
 //      keys, per-warp shared-memory histograms) finds the (k-R)-th largest key u*
 //      and how many of the keys equal to u* must be taken;
@@ -15,8 +26,12 @@
 //      positions come out ascending without a sort;
 //   3. the recent window is appended.
 // Integer work only after the key transform: the same z always gives the same idx.
+#include <cooperative_groups.h>
+
 #include "kvc_internal.cuh"
 #include "select_common.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace kvc {
 namespace {
@@ -116,11 +131,116 @@ __global__ __launch_bounds__(NT) void select_topk_kernel(const float *__restrict
   (void)lane;
 }
 
+constexpr int NTC = 512;            // threads of the resident kernel
+constexpr int NWC = NTC / 32;
+constexpr int kSliceSmall = 16384;  // keys per CTA with two CTAs per SM
+constexpr int kSliceMax = 49152;    // keys per CTA at most (192 KB)
+constexpr int kMaxCl = 8;
+
+struct ResidentSmem {
+  RadixScratch<NTC> rx;
+  int wcnt[NWC];
+  int cnt[kMaxCl];
+};
+
+__global__ __launch_bounds__(NTC) void select_topk_resident_kernel(
+    const float *__restrict__ z, int T, int k, int R, int S, int len,
+    int32_t *__restrict__ idx_out) {
+  extern __shared__ uint32_t keys[];  // this CTA's slice of candidates, as order keys
+  __shared__ ResidentSmem sm;
+  cg::cluster_group cl = cg::this_cluster();
+  const int CL = (int)cl.num_blocks(), rank = (int)cl.block_rank();
+  const long head = blockIdx.x / CL;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int n = T - R - S, nh = k - R - S;
+  const float *zv = z + head * (long)T + S;
+  int32_t *out = idx_out + head * (long)k;
+  const int lo = min(n, rank * len), hi = min(n, lo + len), m = hi - lo;
+
+  for (int base = threadIdx.x; base < m; base += 8 * NTC) {
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = base + u * NTC;
+      v[u] = (i < m) ? __ldg(zv + lo + i) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = base + u * NTC;
+      if (i < m) keys[i] = order_key(v[u]);
+    }
+  }
+  cl.sync();  // slices loaded, and every CTA of the cluster is running
+
+  const uint64_t thr = radix_select_ge<NTC, true>(sm.rx, nh, [&](auto &&f) {
+    for (int i = threadIdx.x; i < m; i += NTC) f(pair_key_u(keys[i], (uint32_t)(lo + i)));
+  });
+
+  // kept candidates per warp range, per CTA, then the CTA's output offset
+  const int per = ((m + NWC - 1) / NWC + 31) & ~31;
+  const int wlo = min(m, warp * per), whi = min(m, wlo + per);
+  int c = 0;
+  for (int i = wlo + lane; i < whi; i += 32) c += pair_key_u(keys[i], (uint32_t)(lo + i)) >= thr;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
+  if (lane == 0) sm.wcnt[warp] = c;
+  __syncthreads();
+  if (threadIdx.x < CL) {
+    int tot = 0;
+    for (int w = 0; w < NWC; ++w) tot += sm.wcnt[w];
+    cl.map_shared_rank(&sm.cnt[0], threadIdx.x)[rank] = tot;
+  }
+  cl.sync();  // the last remote access is above
+  int run = 0;
+  for (int r = 0; r < rank; ++r) run += sm.cnt[r];
+  for (int w = 0; w < warp; ++w) run += sm.wcnt[w];
+  for (int i0 = wlo; i0 < whi; i0 += 32) {
+    const int i = i0 + lane;
+    const bool keep = i < whi && pair_key_u(keys[i], (uint32_t)(lo + i)) >= thr;
+    const unsigned msk = __ballot_sync(0xFFFFFFFFu, keep);
+    const int slot = run + __popc(msk & ((1u << lane) - 1u));
+    if (keep && slot < nh) out[S + slot] = S + lo + i;
+    run += __popc(msk);
+  }
+  if (rank == 0) {
+    for (int mm = threadIdx.x; mm < S; mm += NTC) out[mm] = mm;
+    for (int mm = threadIdx.x; mm < R; mm += NTC) out[S + nh + mm] = S + n + mm;
+  }
+}
+
 }  // namespace
 
 int launch_select_topk(const float *z, int B, int H, int T, int k, int recent, int sink,
                        int32_t *idx, cudaStream_t st) {
   const long heads = (long)B * H;
+  const int n = T - recent - sink, nh = k - recent - sink;
+  int CL = 0, len = 0;
+  if (nh < n) {
+    CL = (n + kSliceSmall - 1) / kSliceSmall;
+    if (CL > kMaxCl && n <= kMaxCl * kSliceMax) CL = kMaxCl;
+    if (CL <= kMaxCl) len = (n + CL - 1) / CL;
+  }
+  if (len > 0 && heads * CL <= 0x7FFFFFFFL) {
+    const size_t smem = (size_t)len * sizeof(uint32_t);
+    if (ensure_smem((const void *)select_topk_resident_kernel, smem))
+      return cuda_failure(cudaErrorInvalidValue, "select kernel: shared memory");
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(heads * CL));
+    cfg.blockDim = dim3(NTC);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)CL;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, select_topk_resident_kernel, z, T, k, recent,
+                                             sink, len, idx);
+    if (e != cudaSuccess) return cuda_failure(e, "select kernel");
+    return launch_status();
+  }
   select_topk_kernel<<<(unsigned)heads, NT, 0, st>>>(z, T, k, recent, sink, idx);
   return launch_status();
 }

@@ -99,7 +99,11 @@ def test_hubkv_gamma_one_identical_heads(kvc):
 
 @pytest.mark.parametrize("T,k,R", [(10, 3, 0), (10, 10, 2), (4096, 409, 32), (8192, 1638, 819),
                                    (32768, 3276, 64), (131072, 6553, 64), (1000, 999, 998),
-                                   (2049, 100, 1)])
+                                   (2049, 100, 1),
+                                   (16385, 1000, 0),      # two CTAs per head, ragged slices
+                                   (50000, 5000, 17),     # a cluster of 4
+                                   (300000, 15000, 64),   # 8 CTAs with large slices
+                                   (400000, 20000, 64)])  # beyond the resident limit: streaming kernel
 @pytest.mark.parametrize("ties", [False, True])
 def test_select_topk_bit_exact(kvc, oracle_mod, T, k, R, ties):
     B, H = 2, 3
