@@ -19,7 +19,8 @@
  *
  * Conventions shared by every call
  *   - Every pointer argument is DEVICE memory owned by the caller (allocate it
- *     with cudaMalloc or a framework allocator), 16-byte aligned.  The library
+ *     with cudaMalloc or a framework allocator), 16-byte aligned; the gather
+ *     sources of the two compactions may also be pinned host memory.  The library
  *     never allocates, frees or synchronises; it only enqueues kernels on
  *     `stream` (a cudaStream_t passed as void*, NULL = legacy default stream).
  *   - Tensors are dense, row-major, the head dimension fastest and the head
@@ -190,7 +191,10 @@ KVC_API int kv_select_topk_ex(const float *z, int B, int H, int T, int k, int re
  *     acc_out[m] = s[idx[m]] (the attention mass received so far),
  * and len_out = k.  Slots k..cap-1 are not touched.  The copy is bit-exact.
  *
- *   K, V       [B][H][T][d]
+ *   K, V       [B][H][T][d]; device memory, or pinned host memory (allocated with
+ *              cudaHostAlloc / cudaMallocHost, addressed through unified virtual
+ *              addressing): the kernel then reads only the kept rows over the host
+ *              link, so V of a host-resident prompt never has to move in full
  *   s          [B][H][T] float32, may be NULL (then acc_out is not written)
  *   idx        [B][H][k] int32, each in [0, T) (a slot whose index is out of
  *              range is left untouched)
@@ -273,7 +277,8 @@ KVC_API int kv_select_budget(const float *z, int B, int H, int T, int budget, in
  *     index, acc_out[m] = s[that index],
  * and len_out = n; slots n..cap-1 are not touched.  The copy is bit-exact.
  *
- *   K, V       [B][H][T][d];  s [B][H][T] float32, may be NULL (acc_out not written)
+ *   K, V       [B][H][T][d], device or pinned host memory (as for kv_compact);
+ *              s [B][H][T] float32, may be NULL (acc_out not written)
  *   idx        [B][budget] int32;  off [B][H+1] int32 (CSR, as kv_select_budget writes)
  *   K_out, V_out [B][H][cap][d];  pos_out, acc_out [B][H][cap];  len_out [B][H]
  *   dev_status device int, may be NULL; set to KV_ERR_INVALID_ARG when a row's

@@ -17,7 +17,8 @@ importing it loads the CUDA library and raises if it is missing.  ``gen`` and
 from .configs import ALL, BY_NAME, Workload  # noqa: F401
 
 _API_NAMES = {"kv_score_obs", "hubkv_refine", "kv_select_topk", "kv_compact",
-              "h2o_decode_step", "kv_workspace_size", "KvcError", "compress_prefill"}
+              "h2o_decode_step", "kv_workspace_size", "KvcError", "compress_prefill",
+              "compress_prefill_host", "kv_select_budget", "kv_compact_ragged", "kv_score_nested"}
 
 
 def __getattr__(name):

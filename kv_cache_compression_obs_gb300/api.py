@@ -108,6 +108,14 @@ def _dev(*ts):
             raise ValueError("tensors must be contiguous CUDA tensors")
 
 
+def _dev_or_pinned(*ts):
+    """Gather sources may also be pinned host tensors (read by the kernel over the
+    host link, only the rows it keeps)."""
+    for t in ts:
+        if t is not None and (not t.is_contiguous() or not (t.is_cuda or t.is_pinned())):
+            raise ValueError("tensors must be contiguous CUDA tensors or pinned host tensors")
+
+
 def kv_workspace_size(op: int, B: int, Hq: int, Hkv: int, T: int, d: int = 128, W: int = 1,
                       k: int = 1) -> int:
     return int(_lib.kv_workspace_size(op, B, Hq, Hkv, T, d, W, k))
@@ -200,8 +208,9 @@ def kv_compact(K: torch.Tensor, V: torch.Tensor, s, idx: torch.Tensor, cap: int 
     cap = k if cap is None else cap
     if idx.dtype != torch.int32 or V.shape != K.shape or V.dtype != K.dtype:
         raise ValueError("idx must be int32 and V must match K")
-    _dev(K, V, s, idx, K_out, V_out, pos_out, acc_out, len_out)
-    dev = K.device
+    _dev(s, idx, K_out, V_out, pos_out, acc_out, len_out)
+    _dev_or_pinned(K, V)
+    dev = idx.device
     K_out = K_out if K_out is not None else torch.empty(B, H, cap, d, dtype=K.dtype, device=dev)
     V_out = V_out if V_out is not None else torch.empty(B, H, cap, d, dtype=K.dtype, device=dev)
     pos = pos_out if pos_out is not None else torch.zeros(B, H, cap, dtype=torch.int32, device=dev)
@@ -262,8 +271,9 @@ def kv_compact_ragged(K: torch.Tensor, V: torch.Tensor, s, idx: torch.Tensor, of
         raise ValueError("idx and off must be int32 and V must match K")
     if tuple(off.shape) != (B, H + 1) or idx.shape[0] != B:
         raise ValueError("idx must be [B][budget] and off [B][H+1]")
-    _dev(K, V, s, idx, off, K_out, V_out, pos_out, acc_out, len_out, dev_status)
-    dev = K.device
+    _dev(s, idx, off, K_out, V_out, pos_out, acc_out, len_out, dev_status)
+    _dev_or_pinned(K, V)
+    dev = idx.device
     K_out = K_out if K_out is not None else torch.empty(B, H, cap, d, dtype=K.dtype, device=dev)
     V_out = V_out if V_out is not None else torch.empty(B, H, cap, d, dtype=K.dtype, device=dev)
     pos = pos_out if pos_out is not None else torch.zeros(B, H, cap, dtype=torch.int32, device=dev)
@@ -315,6 +325,86 @@ def compress_prefill(Q_obs, K, V, k: int, recent: int, r: float | None, gamma: f
     Kc, Vc, pos, acc, ln = kv_compact(K, V, s, idx, cap, stream=stream)
     return {"s": s, "z": z, "beta": beta, "idx": idx, "K": Kc, "V": Vc, "pos": pos, "acc": acc,
             "len": ln}
+
+
+def prefill_host_buffers(hQ: torch.Tensor, hK: torch.Tensor, k: int, r: float | None,
+                         cap: int | None = None, device=None, rows_per_chunk: int = 1):
+    """Device buffers for compress_prefill_host (reusable across calls)."""
+    B, Hq, W, d = hQ.shape
+    _, Hkv, T, _ = hK.shape
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    cap = k if cap is None else cap
+    f32, i32 = torch.float32, torch.int32
+    rc = min(rows_per_chunk, B)
+    ws = max(kv_workspace_size(KV_OP_SCORE_OBS, rc, Hq, Hkv, T, d, W),
+             kv_workspace_size(KV_OP_HUBKV_REFINE, rc, Hkv, Hkv, T), 256)
+    s = torch.empty(B, Hkv, T, dtype=f32, device=dev)
+    return {
+        "Q": torch.empty(hQ.shape, dtype=hQ.dtype, device=dev),
+        "K": torch.empty(hK.shape, dtype=hK.dtype, device=dev),
+        "s": s,
+        "z": torch.empty_like(s) if r is not None else s,
+        "beta": torch.empty(B, Hkv, dtype=f32, device=dev),
+        "idx": torch.empty(B, Hkv, k, dtype=i32, device=dev),
+        "Kc": torch.empty(B, Hkv, cap, d, dtype=hK.dtype, device=dev),
+        "Vc": torch.empty(B, Hkv, cap, d, dtype=hK.dtype, device=dev),
+        "pos": torch.zeros(B, Hkv, cap, dtype=i32, device=dev),
+        "acc": torch.zeros(B, Hkv, cap, dtype=f32, device=dev),
+        "len": torch.empty(B, Hkv, dtype=i32, device=dev),
+        "ws": torch.empty(ws, dtype=torch.uint8, device=dev),
+        "copy_stream": torch.cuda.Stream(device=dev),
+        "rows_per_chunk": rc,
+        "cap": cap,
+    }
+
+
+def compress_prefill_host(hQ: torch.Tensor, hK: torch.Tensor, hV: torch.Tensor, k: int, recent: int,
+                          r: float | None, gamma: float = 0.5, pool_width: int = 5,
+                          beta_lo: float = 0.8, beta_hi: float = 1.2, scale: float | None = None,
+                          buffers=None, stream=None):
+    """The prefill chain of compress_prefill on host-resident inputs.
+
+    hQ [B][Hq][W][d], hK, hV [B][Hkv][T][d]: pinned host tensors.  Q and K move to
+    the device one chunk of batch rows at a time on a copy stream; each chunk's
+    chain (score, refine, Top-K, compact) runs on `stream` as soon as its keys
+    have landed, so the copies of later chunks overlap the work on earlier ones.
+    V never moves in full: the compaction gathers the kept rows straight from the
+    pinned host memory over the host link.  `buffers` comes from
+    prefill_host_buffers; the result dict holds the same entries as
+    compress_prefill's (views of the buffers).  hV must stay alive until the
+    stream has passed the call.
+    """
+    for t in (hQ, hK, hV):
+        if t.is_cuda or not t.is_pinned() or not t.is_contiguous():
+            raise ValueError("host inputs must be contiguous pinned CPU tensors")
+    B = hK.shape[0]
+    bf = buffers if buffers is not None else prefill_host_buffers(hQ, hK, k, r)
+    cs = torch.cuda.current_stream() if stream is None else stream
+    cp = bf["copy_stream"]
+    cp.wait_stream(cs)  # the buffers' previous readers are done
+    with torch.cuda.stream(cp):
+        bf["Q"].copy_(hQ, non_blocking=True)
+    step = bf["rows_per_chunk"]
+    for r0 in range(0, B, step):
+        r1 = min(B, r0 + step)
+        with torch.cuda.stream(cp):
+            bf["K"][r0:r1].copy_(hK[r0:r1], non_blocking=True)
+            landed = torch.cuda.Event()
+            landed.record(cp)
+        cs.wait_event(landed)
+        Q, K, sc = bf["Q"][r0:r1], bf["K"][r0:r1], bf["s"][r0:r1]
+        kv_score_obs(Q, K, scale, out=sc, workspace=bf["ws"], stream=cs)
+        z = sc
+        if r is not None:
+            z, _ = hubkv_refine(sc, r, gamma, pool_width, beta_lo, beta_hi, out=bf["z"][r0:r1],
+                                beta_out=bf["beta"][r0:r1], workspace=bf["ws"], stream=cs)
+        idx = kv_select_topk(z, k, recent, out=bf["idx"][r0:r1], stream=cs)
+        kv_compact(K, hV[r0:r1], sc, idx, bf["cap"], K_out=bf["Kc"][r0:r1], V_out=bf["Vc"][r0:r1],
+                   pos_out=bf["pos"][r0:r1], acc_out=bf["acc"][r0:r1], len_out=bf["len"][r0:r1],
+                   stream=cs)
+    return {"s": bf["s"], "z": bf["z"], "beta": bf["beta"] if r is not None else None,
+            "idx": bf["idx"], "K": bf["Kc"], "V": bf["Vc"], "pos": bf["pos"], "acc": bf["acc"],
+            "len": bf["len"]}
 
 
 def library_handle():

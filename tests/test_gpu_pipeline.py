@@ -138,3 +138,24 @@ def test_h2o_decode_full_size_sampled(kvc, oracle_mod):
             changed = (pos != before).sum(-1)
             assert torch.all(changed == 1)
     assert exact >= 15
+
+
+@pytest.mark.parametrize("wl", [configs.GQA_PREFILL.scaled(B=1, L=3, T=4096, k=409, n_segments=40),
+                                configs.LONG_CONTEXT.scaled(L=2, T=16384, k=819, n_segments=150),
+                                configs.TINY],
+                         ids=lambda w: w.name)
+def test_host_input_prefill_matches_the_device_path(kvc, wl):
+    """compress_prefill_host (keys streamed per batch row on a copy stream, kept V
+    rows gathered from pinned host memory) gives, bit for bit, what
+    compress_prefill gives on the same rows with the inputs already on the GPU."""
+    Q, K, V = gen.prefill_inputs(wl, device=DEV)
+    hQ, hK, hV = (t.cpu().pin_memory() for t in (Q, K, V))
+    got = kvc.compress_prefill_host(hQ, hK, hV, wl.k, wl.R, wl.r, wl.gamma, wl.pool_width,
+                                    wl.beta_lo, wl.beta_hi, wl.scale)
+    torch.cuda.synchronize()
+    for b in range(wl.rows):  # one batch row per call, as the host path chunks it
+        ref = kvc.compress_prefill(Q[b:b + 1], K[b:b + 1], V[b:b + 1], wl.k, wl.R, wl.r, wl.gamma,
+                                   wl.pool_width, wl.beta_lo, wl.beta_hi, scale=wl.scale)
+        torch.cuda.synchronize()
+        for key in ("s", "z", "idx", "K", "V", "pos", "acc", "len"):
+            assert torch.equal(got[key][b:b + 1], ref[key]), (key, b)
