@@ -206,11 +206,14 @@ class Pipeline:
         a.kv_compact(self.K, self.V, self.s, self.idx, wl.cap, K_out=self.Kc, V_out=self.Vc,
                      pos_out=self.pos, acc_out=self.acc, len_out=self.len, stream=stream)
 
-    def decode(self, t, stream=None):
+    def decode(self, t, stream=None, rows=None):
         wl = self.wl
-        self.api.h2o_decode_step(self.dq[t], self.dk[t], self.dv[t], self.Kc, self.Vc, self.pos,
-                                 self.acc, self.len, wl.R, wl.T + t, wl.scale, o_out=self.o,
-                                 evicted_out=self.ev, workspace=self.dws, stream=stream)
+        r0, r1 = (0, wl.rows) if rows is None else rows
+        sl = slice(r0, r1)
+        self.api.h2o_decode_step(self.dq[t][sl], self.dk[t][sl], self.dv[t][sl], self.Kc[sl],
+                                 self.Vc[sl], self.pos[sl], self.acc[sl], self.len[sl], wl.R,
+                                 wl.T + t, wl.scale, o_out=self.o[sl], evicted_out=self.ev[sl],
+                                 workspace=self.dws, stream=stream)
 
     def step(self, stream=None):
         self.prefill(stream)
@@ -349,6 +352,9 @@ def launch_count():
     return int(api.library_handle().kv_launch_count())
 
 
+E2E_GROUPS = 2  # layer-row groups of the end-to-end path (decode of one overlaps the next's keys)
+
+
 def run_e2e(wl, pipe, steps):
     """Same metric through the public API from pinned host inputs, copies inside the
     timed region: compress_prefill_host streams Q and K to the device one layer row
@@ -376,16 +382,24 @@ def run_e2e(wl, pipe, steps):
            + sum(t.numel() * t.element_size() for t in hdq + hdk + hdv))
     d2h = (out_idx.numel() * 4 + out_o.numel() * 4 + out_ev.numel() * 4)
 
+    groups = [(g * wl.rows // E2E_GROUPS, (g + 1) * wl.rows // E2E_GROUPS) for g in range(E2E_GROUPS)]
+    groups = [gr for gr in groups if gr[1] > gr[0]]
+
     def one():
-        a.compress_prefill_host(hQ, hK, hV, wl.k, wl.R, wl.r, wl.gamma, wl.pool_width, wl.beta_lo,
-                                wl.beta_hi, wl.scale, buffers=bufs)
-        out_idx.copy_(pipe.idx, non_blocking=True)
-        for t in range(wl.n_decode):
+        for t in range(wl.n_decode):  # the decode inputs first: small, needed by every group
             pipe.dq[t].copy_(hdq[t], non_blocking=True)
             pipe.dk[t].copy_(hdk[t], non_blocking=True)
             pipe.dv[t].copy_(hdv[t], non_blocking=True)
-            pipe.decode(t)
-            out_ev[t].copy_(pipe.ev, non_blocking=True)
+        # Layer rows are independent through the whole path: a group's decode steps
+        # start once its own prefill is done, while later groups' keys still stream.
+        for gi, (r0, r1) in enumerate(groups):
+            a.compress_prefill_host(hQ, hK, hV, wl.k, wl.R, wl.r, wl.gamma, wl.pool_width,
+                                    wl.beta_lo, wl.beta_hi, wl.scale, buffers=bufs, rows=(r0, r1),
+                                    wait=(gi == 0))
+            out_idx[r0:r1].copy_(pipe.idx[r0:r1], non_blocking=True)
+            for t in range(wl.n_decode):
+                pipe.decode(t, rows=(r0, r1))
+                out_ev[t, r0:r1].copy_(pipe.ev[r0:r1], non_blocking=True)
         out_o.copy_(pipe.o, non_blocking=True)
 
     one()

@@ -361,7 +361,7 @@ def prefill_host_buffers(hQ: torch.Tensor, hK: torch.Tensor, k: int, r: float | 
 def compress_prefill_host(hQ: torch.Tensor, hK: torch.Tensor, hV: torch.Tensor, k: int, recent: int,
                           r: float | None, gamma: float = 0.5, pool_width: int = 5,
                           beta_lo: float = 0.8, beta_hi: float = 1.2, scale: float | None = None,
-                          buffers=None, stream=None):
+                          buffers=None, stream=None, rows=None, wait=True):
     """The prefill chain of compress_prefill on host-resident inputs.
 
     hQ [B][Hq][W][d], hK, hV [B][Hkv][T][d]: pinned host tensors.  Q and K move to
@@ -372,21 +372,26 @@ def compress_prefill_host(hQ: torch.Tensor, hK: torch.Tensor, hV: torch.Tensor, 
     pinned host memory over the host link.  `buffers` comes from
     prefill_host_buffers; the result dict holds the same entries as
     compress_prefill's (views of the buffers).  hV must stay alive until the
-    stream has passed the call.
+    stream has passed the call.  `rows` = (r0, r1) restricts the call to those
+    batch rows (independent of the others); wait=False skips the copy stream's
+    wait for the work already on `stream`, for a caller that knows those rows'
+    buffers are free (e.g. the later row groups of one step).
     """
     for t in (hQ, hK, hV):
         if t.is_cuda or not t.is_pinned() or not t.is_contiguous():
             raise ValueError("host inputs must be contiguous pinned CPU tensors")
     B = hK.shape[0]
+    lo, hi = (0, B) if rows is None else rows
     bf = buffers if buffers is not None else prefill_host_buffers(hQ, hK, k, r)
     cs = torch.cuda.current_stream() if stream is None else stream
     cp = bf["copy_stream"]
-    cp.wait_stream(cs)  # the buffers' previous readers are done
+    if wait:
+        cp.wait_stream(cs)  # the buffers' previous readers are done
     with torch.cuda.stream(cp):
-        bf["Q"].copy_(hQ, non_blocking=True)
+        bf["Q"][lo:hi].copy_(hQ[lo:hi], non_blocking=True)
     step = bf["rows_per_chunk"]
-    for r0 in range(0, B, step):
-        r1 = min(B, r0 + step)
+    for r0 in range(lo, hi, step):
+        r1 = min(hi, r0 + step)
         with torch.cuda.stream(cp):
             bf["K"][r0:r1].copy_(hK[r0:r1], non_blocking=True)
             landed = torch.cuda.Event()
