@@ -48,18 +48,18 @@ constexpr int NT_DISC = 1024;
 template <int NW32> struct Words;
 template <> struct Words<1> {
   __device__ __forceinline__ static void load(const void *p, uint64_t pol, uint32_t (&w)[1]) {
-    asm volatile("ld.global.nc.L2::cache_hint.u32 %0, [%1], %2;" : "=r"(w[0]) : "l"(p), "l"(pol));
+    asm("ld.global.nc.L2::cache_hint.u32 %0, [%1], %2;" : "=r"(w[0]) : "l"(p), "l"(pol));
   }
 };
 template <> struct Words<2> {
   __device__ __forceinline__ static void load(const void *p, uint64_t pol, uint32_t (&w)[2]) {
-    asm volatile("ld.global.nc.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;"
+    asm("ld.global.nc.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;"
                  : "=r"(w[0]), "=r"(w[1]) : "l"(p), "l"(pol));
   }
 };
 template <> struct Words<4> {
   __device__ __forceinline__ static void load(const void *p, uint64_t pol, uint32_t (&w)[4]) {
-    asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+    asm("ld.global.nc.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
                  : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "l"(p), "l"(pol));
   }
 };
@@ -189,22 +189,17 @@ __global__ __launch_bounds__(NT_SCAN) void anchors_kernel(const T *__restrict__ 
     for (int p = 0; p < P2; ++p) tot[p] = make_float2(-P[p].x, -P[p].y);
     __syncwarp();
     int r = 0;  // i - (chunk start), i.e. i % window, kept as a running counter
+    int rs = c0 % RW;  // i0 % RW
     for (int i0 = c0; i0 < e; i0 += 4) {
       float2 x[4][P2], y[4][P2];
       float ss[4];
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
-        const int i = i0 + t;
-        if (i < e) R::load(Ku + (long)i * D, lane, keep_pol, x[t]);
-        else {
-#pragma unroll
-          for (int p = 0; p < P2; ++p) x[t][p] = make_float2(0.f, 0.f);
-        }
-        if (i < e && i >= window) R::load(Ku + (long)(i - window) * D, lane, last_pol, y[t]);
-        else {
-#pragma unroll
-          for (int p = 0; p < P2; ++p) y[t][p] = make_float2(0.f, 0.f);
-        }
+        // rows past e or before 0 load an in-range row instead (no branch): a token
+        // past e is never used, and a leaving row before 0 is scaled by 1/|k| = 0
+        const int i = min(i0 + t, e - 1);
+        R::load(Ku + (long)i * D, lane, keep_pol, x[t]);
+        R::load(Ku + (long)max(i - window, 0) * D, lane, last_pol, y[t]);
         float2 q2 = __fmul2_rn(x[t][0], x[t][0]);
 #pragma unroll
         for (int p = 1; p < P2; ++p) q2 = __ffma2_rn(x[t][p], x[t][p], q2);
@@ -215,12 +210,20 @@ __global__ __launch_bounds__(NT_SCAN) void anchors_kernel(const T *__restrict__ 
       const float my_inv = tt > 0.f ? rsqrtf(tt) : 0.f;
       float my_old = 0.f;
       {
+        // slot of row j is j % RW; rs tracks i0 % RW, and (i - window) % RW is
+        // (i + 4) % RW because RW = window + 4
         const int mt = lane >> 3, i = i0 + mt;
+        int sn = rs + mt;
+        if (sn >= RW) sn -= RW;
+        int so = sn + 4;
+        if (so >= RW) so -= RW;
         if ((lane & 7) == 0 && i < e) {
-          if (i >= window && i - window < i0) my_old = ring[(i - window) % RW];
-          ring[i % RW] = my_inv;
+          if (i >= window && i - window < i0) my_old = ring[so];
+          ring[sn] = my_inv;
         }
       }
+      rs += 4;
+      if (rs >= RW) rs -= RW;
       float part[8];
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
@@ -339,13 +342,8 @@ __global__ __launch_bounds__(NT_SCAN) void global_kernel(const T *__restrict__ K
   for (int i0 = s; i0 < e; i0 += 4) {
     float2 x[4][P2];
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      if (i0 + t < e) R::load(Ku + (long)(i0 + t) * D, lane, pol, x[t]);
-      else {
-#pragma unroll
-        for (int p = 0; p < P2; ++p) x[t][p] = make_float2(0.f, 0.f);
-      }
-    }
+    for (int t = 0; t < 4; ++t)  // past e: an in-range row, never written out
+      R::load(Ku + (long)min(i0 + t, e - 1) * D, lane, pol, x[t]);
     float part[16];
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
