@@ -57,6 +57,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-groups", type=int, default=None,
+                    help="layer-row groups of the end-to-end path (default E2E_GROUPS)")
     ap.add_argument("--no-next-rows", action="store_true",
                     help="skip the separate timing of the rows beyond the five-step path")
     return ap.parse_args()
@@ -184,17 +186,21 @@ class Pipeline:
         self.pos = torch.empty(*units_shape, wl.cap, dtype=i32, device=device)
         self.acc = torch.empty(*units_shape, wl.cap, dtype=f32, device=device)
         self.len = torch.empty(*units_shape, dtype=i32, device=device)
-        self.o = torch.empty(wl.rows, wl.Hq, wl.d, dtype=f32, device=device)
-        self.ev = torch.empty(*units_shape, dtype=i32, device=device)
+        nd = max(wl.n_decode, 1)
+        self.O = torch.empty(nd, wl.rows, wl.Hq, wl.d, dtype=f32, device=device)  # every step's output
+        self.EV = torch.empty(nd, *units_shape, dtype=i32, device=device)
+        self.o, self.ev = self.O[-1], self.EV[-1]
         ws = max(api.kv_workspace_size(api.KV_OP_SCORE_OBS, wl.rows, wl.Hq, wl.Hkv, wl.T, wl.d, wl.W),
                  api.kv_workspace_size(api.KV_OP_HUBKV_REFINE, wl.rows, wl.Hkv, wl.Hkv, wl.T), 256)
         self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
         dws = api.kv_workspace_size(api.KV_OP_DECODE, wl.rows, wl.Hq, wl.Hkv, wl.cap, wl.d)
         self.dws = torch.empty(max(dws, 256), dtype=torch.uint8, device=device)
         steps = [gen.decode_inputs(wl, t, device=device) for t in range(wl.n_decode)]
-        self.dq = [x[0] for x in steps]
-        self.dk = [x[1] for x in steps]
-        self.dv = [x[2] for x in steps]
+        if steps:  # [n_decode][rows][heads][d], one tensor per input
+            self.DQ, self.DK, self.DV = (torch.stack([x[i] for x in steps]) for i in range(3))
+        self.dq = [self.DQ[t] for t in range(wl.n_decode)]
+        self.dk = [self.DK[t] for t in range(wl.n_decode)]
+        self.dv = [self.DV[t] for t in range(wl.n_decode)]
 
     def prefill(self, stream=None):
         a, wl = self.api, self.wl
@@ -206,19 +212,17 @@ class Pipeline:
         a.kv_compact(self.K, self.V, self.s, self.idx, wl.cap, K_out=self.Kc, V_out=self.Vc,
                      pos_out=self.pos, acc_out=self.acc, len_out=self.len, stream=stream)
 
-    def decode(self, t, stream=None, rows=None):
+    def decode_all(self, stream=None):
+        """All the workload's decode steps, one library call."""
         wl = self.wl
-        r0, r1 = (0, wl.rows) if rows is None else rows
-        sl = slice(r0, r1)
-        self.api.h2o_decode_step(self.dq[t][sl], self.dk[t][sl], self.dv[t][sl], self.Kc[sl],
-                                 self.Vc[sl], self.pos[sl], self.acc[sl], self.len[sl], wl.R,
-                                 wl.T + t, wl.scale, o_out=self.o[sl], evicted_out=self.ev[sl],
-                                 workspace=self.dws, stream=stream)
+        if wl.n_decode:
+            self.api.h2o_decode_steps(self.DQ, self.DK, self.DV, self.Kc, self.Vc, self.pos,
+                                      self.acc, self.len, wl.R, wl.T, wl.scale, o_out=self.O,
+                                      evicted_out=self.EV, workspace=self.dws, stream=stream)
 
     def step(self, stream=None):
         self.prefill(stream)
-        for t in range(self.wl.n_decode):
-            self.decode(t, stream)
+        self.decode_all(stream)
 
     def timed_phases(self):
         """One step with events between the phases: ms per phase."""
@@ -237,8 +241,7 @@ class Pipeline:
         a.kv_compact(self.K, self.V, self.s, self.idx, wl.cap, K_out=self.Kc, V_out=self.Vc,
                      pos_out=self.pos, acc_out=self.acc, len_out=self.len)
         ev[4].record()
-        for t in range(wl.n_decode):
-            self.decode(t)
+        self.decode_all()
         ev[5].record()
         torch.cuda.synchronize()
         names = ["kv_score_obs", "hubkv_refine", "kv_select_topk", "kv_compact", "h2o_decode_step"]
@@ -352,55 +355,60 @@ def launch_count():
     return int(api.library_handle().kv_launch_count())
 
 
-E2E_GROUPS = 2  # layer-row groups of the end-to-end path (decode of one overlaps the next's keys)
+E2E_GROUPS = 4  # layer-row groups of the end-to-end path (decode of one overlaps the next's keys)
 
 
-def run_e2e(wl, pipe, steps):
+def run_e2e(wl, pipe, steps, n_groups):
     """Same metric through the public API from pinned host inputs, copies inside the
-    timed region: compress_prefill_host streams Q and K to the device one layer row
-    at a time on a copy stream while the chain runs on the rows already there, and
-    the compaction gathers the kept V rows straight from host memory; then the
-    decode steps, each with its inputs copied in and its evictions copied back,
-    and the last outputs copied back."""
+    timed region.  Layer rows are independent through the whole path, so they run
+    in n_groups groups: compress_prefill_host streams a group's Q and K to the
+    device one layer row at a time on a copy stream (the compaction gathers the
+    kept V rows straight from host memory), then the group's decode steps run as
+    one h2o_decode_steps call while the next group's keys stream.  The kept
+    positions, every step's evictions and the last step's outputs are copied back."""
     import torch
     a = pipe.api
+    groups = [(g * wl.rows // n_groups, (g + 1) * wl.rows // n_groups) for g in range(n_groups)]
+    groups = [gr for gr in groups if gr[1] > gr[0]]
     hQ = pipe.Q.cpu().pin_memory()
     hK = pipe.K.cpu().pin_memory()
     hV = pipe.V.cpu().pin_memory()
-    hdq = [t.cpu().pin_memory() for t in pipe.dq]
-    hdk = [t.cpu().pin_memory() for t in pipe.dk]
-    hdv = [t.cpu().pin_memory() for t in pipe.dv]
+    # decode inputs held group-major on the host, so that each group's are contiguous
+    hD = [[X[:, r0:r1].contiguous().cpu().pin_memory() for X in (pipe.DQ, pipe.DK, pipe.DV)]
+          for r0, r1 in groups] if wl.n_decode else []
+    dD = [[torch.empty_like(h, device=pipe.dev) for h in hg] for hg in hD]
+    dO = [torch.empty(wl.n_decode, r1 - r0, wl.Hq, wl.d, dtype=torch.float32, device=pipe.dev)
+          for r0, r1 in groups]
+    dE = [torch.empty(wl.n_decode, r1 - r0, wl.Hkv, dtype=torch.int32, device=pipe.dev)
+          for r0, r1 in groups]
     out_idx = torch.empty(pipe.idx.shape, dtype=torch.int32).pin_memory()
     out_o = torch.empty(pipe.o.shape, dtype=torch.float32).pin_memory()
-    out_ev = torch.empty((wl.n_decode,) + tuple(pipe.ev.shape), dtype=torch.int32).pin_memory()
+    out_ev = [torch.empty(e.shape, dtype=torch.int32).pin_memory() for e in dE]
     bufs = {"Q": pipe.Q, "K": pipe.K, "s": pipe.s, "z": pipe.z, "beta": pipe.beta, "idx": pipe.idx,
             "Kc": pipe.Kc, "Vc": pipe.Vc, "pos": pipe.pos, "acc": pipe.acc, "len": pipe.len,
             "ws": pipe.ws, "copy_stream": torch.cuda.Stream(), "rows_per_chunk": 1, "cap": wl.cap}
     row = wl.d * wl.elem_bytes
     h2d = (hQ.numel() * hQ.element_size() + hK.numel() * hK.element_size()
            + wl.units * wl.k * row  # the kept V rows, gathered from host memory
-           + sum(t.numel() * t.element_size() for t in hdq + hdk + hdv))
-    d2h = (out_idx.numel() * 4 + out_o.numel() * 4 + out_ev.numel() * 4)
-
-    groups = [(g * wl.rows // E2E_GROUPS, (g + 1) * wl.rows // E2E_GROUPS) for g in range(E2E_GROUPS)]
-    groups = [gr for gr in groups if gr[1] > gr[0]]
+           + sum(h.numel() * h.element_size() for hg in hD for h in hg))
+    d2h = out_idx.numel() * 4 + out_o.numel() * 4 + sum(e.numel() * 4 for e in out_ev)
 
     def one():
-        for t in range(wl.n_decode):  # the decode inputs first: small, needed by every group
-            pipe.dq[t].copy_(hdq[t], non_blocking=True)
-            pipe.dk[t].copy_(hdk[t], non_blocking=True)
-            pipe.dv[t].copy_(hdv[t], non_blocking=True)
-        # Layer rows are independent through the whole path: a group's decode steps
-        # start once its own prefill is done, while later groups' keys still stream.
+        for dg, hg in zip(dD, hD):  # decode inputs first: small
+            for d_, h_ in zip(dg, hg):
+                d_.copy_(h_, non_blocking=True)
         for gi, (r0, r1) in enumerate(groups):
             a.compress_prefill_host(hQ, hK, hV, wl.k, wl.R, wl.r, wl.gamma, wl.pool_width,
                                     wl.beta_lo, wl.beta_hi, wl.scale, buffers=bufs, rows=(r0, r1),
                                     wait=(gi == 0))
             out_idx[r0:r1].copy_(pipe.idx[r0:r1], non_blocking=True)
-            for t in range(wl.n_decode):
-                pipe.decode(t, rows=(r0, r1))
-                out_ev[t, r0:r1].copy_(pipe.ev[r0:r1], non_blocking=True)
-        out_o.copy_(pipe.o, non_blocking=True)
+            if wl.n_decode:
+                sl = slice(r0, r1)
+                a.h2o_decode_steps(*dD[gi], pipe.Kc[sl], pipe.Vc[sl], pipe.pos[sl], pipe.acc[sl],
+                                   pipe.len[sl], wl.R, wl.T, wl.scale, o_out=dO[gi],
+                                   evicted_out=dE[gi], workspace=pipe.dws)
+                out_ev[gi].copy_(dE[gi], non_blocking=True)
+                out_o[r0:r1].copy_(dO[gi][-1], non_blocking=True)
 
     one()
     torch.cuda.synchronize()
@@ -523,7 +531,7 @@ def run_ours(args, wl, rank, world):
     if not args.no_next_rows:
         line["next_rows"] = time_next_rows(pipe)
     if not args.no_e2e:
-        dt, h2d, d2h = run_e2e(wl, pipe, min(args.steps, 2))
+        dt, h2d, d2h = run_e2e(wl, pipe, min(args.steps, 3), args.e2e_groups or E2E_GROUPS)
         line["e2e"] = {"value": world * tokens / dt, "unit": UNIT, "h2d_bytes_per_step": h2d,
                        "d2h_bytes_per_step": d2h}
     if rank == 0 and not args.no_cpu_baseline:

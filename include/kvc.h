@@ -344,6 +344,27 @@ KVC_API int h2o_decode_step_ex(const void *q, const void *k_new, const void *v_n
                        kv_stream_t stream);
 
 /*
+ * h2o_decode_steps -- n_steps consecutive decode steps in one call: step t
+ * (t = 0 .. n_steps-1) is h2o_decode_step_ex with q + t*B*Hq*d, k_new/v_new +
+ * t*B*Hkv*d, new_pos = first_pos + t, o_out + t*B*Hq*d and evicted_pos +
+ * t*B*Hkv.  The steps are enqueued back to back on `stream` (two launches each),
+ * which removes a caller's per-step launch overhead when the queries are known
+ * ahead.  The result is exactly that of the n_steps single calls.
+ *
+ *   q          [n_steps][B][Hq][d];  k_new, v_new [n_steps][B][Hkv][d]
+ *   o_out      [n_steps][B][Hq][d] float32;  evicted_pos [n_steps][B][Hkv] int32
+ *   everything else as for h2o_decode_step_ex (state updated in place)
+ * Preconditions: n_steps >= 0, first_pos + n_steps - 1 fits int32, and those of
+ * h2o_decode_step_ex.
+ */
+KVC_API int h2o_decode_steps(const void *q, const void *k_new, const void *v_new, int n_steps,
+                             void *K_cache, void *V_cache, int32_t *pos, float *acc, int32_t *len,
+                             int B, int Hq, int Hkv, int cap, int d, int recent, int sink,
+                             int32_t first_pos, float scale, int flags, int dtype, float *o_out,
+                             int32_t *evicted_pos, void *workspace, size_t workspace_bytes,
+                             int *dev_status, kv_stream_t stream);
+
+/*
  * kv_score_obs_noalloc -- kv_score_obs without a caller-provided workspace.
  * (No counterpart in the pages: this is a calling convention, not a step of
  * the method.)

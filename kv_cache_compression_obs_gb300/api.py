@@ -58,6 +58,9 @@ _lib.h2o_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I,
 _lib.h2o_decode_step_ex.restype = _I
 _lib.h2o_decode_step_ex.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
                                     _F, _I, _I, _P, _P, _P, _Z, _P, _P]
+_lib.h2o_decode_steps.restype = _I
+_lib.h2o_decode_steps.argtypes = [_P, _P, _P, _I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I,
+                                  _F, _I, _I, _P, _P, _P, _Z, _P, _P]
 _lib.kv_score_obs_noalloc.restype = _I
 _lib.kv_score_obs_noalloc.argtypes = [_P, _P, _I, _I, _I, _I, _I, _I, _F, _I, _P, _P, _P]
 _lib.kv_workspace_size.restype = _Z
@@ -221,6 +224,30 @@ def kv_compact(K: torch.Tensor, V: torch.Tensor, s, idx: torch.Tensor, cap: int 
                                          _ptr(pos), _ptr(acc if s is not None else None), _ptr(ln),
                                          _stream(stream)))
     return K_out, V_out, pos, acc, ln
+
+
+def h2o_decode_steps(q, k_new, v_new, K_cache, V_cache, pos, acc, len_, recent: int,
+                     first_pos: int, scale: float | None = None, flags: int = 0, o_out=None,
+                     evicted_out=None, workspace=None, dev_status=None, stream=None,
+                     sink: int = 0):
+    """n consecutive decode steps in one call: q [n][B][Hq][d], k_new, v_new [n][B][Hkv][d];
+    step t uses position first_pos + t.  Returns (o [n][B][Hq][d] f32, evicted [n][B][Hkv])."""
+    n, B, Hq, d = q.shape
+    _, Hkv, cap, _ = K_cache.shape
+    _dev(q, k_new, v_new, K_cache, V_cache, pos, acc, len_, o_out, evicted_out, dev_status)
+    if scale is None:
+        scale = d ** -0.5
+    o = o_out if o_out is not None else torch.empty(n, B, Hq, d, dtype=torch.float32,
+                                                    device=q.device)
+    ev = evicted_out if evicted_out is not None else torch.empty(n, B, Hkv, dtype=torch.int32,
+                                                                 device=q.device)
+    ws, nbytes = _workspace(kv_workspace_size(KV_OP_DECODE, B, Hq, Hkv, cap, d), q.device, workspace)
+    _check("h2o_decode_steps", _lib.h2o_decode_steps(
+        _ptr(q), _ptr(k_new), _ptr(v_new), int(n), _ptr(K_cache), _ptr(V_cache), _ptr(pos),
+        _ptr(acc), _ptr(len_), B, Hq, Hkv, cap, d, int(recent), int(sink), int(first_pos),
+        float(scale), int(flags), _dtype_code(q), _ptr(o), _ptr(ev), _ptr(ws), nbytes,
+        _ptr(dev_status), _stream(stream)))
+    return o, ev
 
 
 def kv_score_nested(K: torch.Tensor, n_disc: int, thresh: float, log_prior=(0.0, 0.0, 0.0),

@@ -283,6 +283,36 @@ int h2o_decode_step_ex(const void *q, const void *k_new, const void *v_new, void
                             evicted_pos, dev_status, static_cast<cudaStream_t>(stream));
 }
 
+int h2o_decode_steps(const void *q, const void *k_new, const void *v_new, int n_steps,
+                     void *K_cache, void *V_cache, int32_t *pos, float *acc, int32_t *len, int B,
+                     int Hq, int Hkv, int cap, int d, int recent, int sink, int32_t first_pos,
+                     float scale, int flags, int dtype, float *o_out, int32_t *evicted_pos,
+                     void *workspace, size_t workspace_bytes, int *dev_status,
+                     kv_stream_t stream) {
+  if (n_steps < 0 || first_pos < 0 || (long long)first_pos + n_steps - 1 > INT_MAX)
+    return KV_ERR_INVALID_ARG;
+  if (n_steps == 0 || B == 0) {
+    // validate the rest as a single step would, without launching anything
+    return h2o_decode_step_ex(q, k_new, v_new, K_cache, V_cache, pos, acc, len, 0, Hq, Hkv, cap,
+                              d, recent, sink, first_pos, scale, flags, dtype, o_out, evicted_pos,
+                              workspace, workspace_bytes, dev_status, stream);
+  }
+  const size_t eb = dtype == KV_F32 ? 4 : 2;
+  const size_t q_step = (size_t)B * Hq * d, kv_step = (size_t)B * Hkv * d;
+  for (int t = 0; t < n_steps; ++t) {
+    const int rc = h2o_decode_step_ex(
+        q ? static_cast<const char *>(q) + t * q_step * eb : nullptr,
+        k_new ? static_cast<const char *>(k_new) + t * kv_step * eb : nullptr,
+        v_new ? static_cast<const char *>(v_new) + t * kv_step * eb : nullptr, K_cache, V_cache,
+        pos, acc, len, B, Hq, Hkv, cap, d, recent, sink, first_pos + t, scale, flags, dtype,
+        o_out ? o_out + t * q_step : nullptr,
+        evicted_pos ? evicted_pos + (size_t)t * B * Hkv : nullptr, workspace, workspace_bytes,
+        dev_status, stream);
+    if (rc != KV_OK) return rc;
+  }
+  return KV_OK;
+}
+
 int h2o_decode_step(const void *q, const void *k_new, const void *v_new, void *K_cache,
                     void *V_cache, int32_t *pos, float *acc, int32_t *len, int B, int Hq,
                     int Hkv, int cap, int d, int recent, int32_t new_pos, float scale,

@@ -32,6 +32,8 @@ def lib():
                                        P, Z, P, P]
     lib.kv_select_budget.argtypes = [P, I, I, I, I, I, I, I, P, P, P]
     lib.kv_score_nested.argtypes = [P, I, I, I, I, I, I, I, I, F, F, F, F, P, P, P, P, Z, P]
+    lib.h2o_decode_steps.argtypes = [P, P, P, I, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I, P, P,
+                                     P, Z, P, P]
     lib.kv_compact_ragged.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, P, I, P, P, P, P, P]
     return lib
 
@@ -151,6 +153,19 @@ def test_nested_scorer_validates_on_the_host(lib):
     assert call(B=0) == 0
     assert lib.kv_workspace_size(5, 1, 0, 8, 131072, 128, 32, 0) >= 8 * 3 * 131072 * 4
     assert lib.kv_workspace_size(5, 1, 0, 8, 131072, 96, 32, 0) == 0
+
+
+def test_multi_step_decode_validates_on_the_host(lib):
+    def call(n=4, B=1, Hq=4, Hkv=4, cap=8, d=64, R=1, S=0, first=9, flags=0):
+        return lib.h2o_decode_steps(NULL, NULL, NULL, n, NULL, NULL, NULL, NULL, NULL, B, Hq, Hkv, cap,
+                                    d, R, S, first, 0.1, flags, 0, NULL, NULL, NULL, 0, NULL, NULL)
+    assert call(n=-1) == -1
+    assert call(first=2 ** 31 - 2, n=4) == -1   # positions past int32
+    assert call(R=8) == -1                       # recent >= cap, caught on the first step
+    assert call(flags=1) == -1                   # ALG1 with a recent window
+    assert call(d=96) == -2
+    assert call() == -1                          # null pointers
+    assert call(n=0) == 0 and call(B=0) == 0     # nothing to do
 
 
 def test_empty_batch_is_a_no_op(lib):

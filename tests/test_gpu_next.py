@@ -89,3 +89,33 @@ def test_decode_lockstep_sinks(kvc, oracle_mod, G, dt, d, R, S):
         for s in range(S):
             assert bool((pos == s).any(-1).all()), "a sink was evicted"
     assert exact >= steps - 2
+
+
+@pytest.mark.parametrize("G,sink,R,fill", [(4, 0, 16, 1.0), (2, 3, 0, 1.0), (1, 2, 8, 0.6)])
+def test_multi_step_decode_equals_single_steps(kvc, G, sink, R, fill):
+    """h2o_decode_steps is, bit for bit, the same single steps enqueued one by one
+    (full caches evicting, and a partly filled cache appending first)."""
+    g = torch.Generator(device=DEV)
+    g.manual_seed(G * 10 + sink)
+    B, Hkv, cap, d, n = 2, 3, 300, 128, 20
+    Hq = Hkv * G
+    K = torch.randn(B, Hkv, cap, d, generator=g, device=DEV).to(torch.bfloat16)
+    V = torch.randn(B, Hkv, cap, d, generator=g, device=DEV).to(torch.bfloat16)
+    pos = torch.arange(cap, dtype=torch.int32, device=DEV).repeat(B, Hkv, 1).contiguous()
+    acc = torch.rand(B, Hkv, cap, generator=g, device=DEV)
+    ln = torch.full((B, Hkv), int(cap * fill), dtype=torch.int32, device=DEV)
+    q = torch.randn(n, B, Hq, d, generator=g, device=DEV).to(torch.bfloat16)
+    kn = torch.randn(n, B, Hkv, d, generator=g, device=DEV).to(torch.bfloat16)
+    vn = torch.randn(n, B, Hkv, d, generator=g, device=DEV).to(torch.bfloat16)
+    one = [t.clone() for t in (K, V, pos, acc, ln)]
+    many = [t.clone() for t in (K, V, pos, acc, ln)]
+    o1, e1 = [], []
+    for t in range(n):
+        o, ev = kvc.h2o_decode_step(q[t], kn[t], vn[t], *one, R, cap + t, sink=sink)
+        o1.append(o)
+        e1.append(ev)
+    o2, e2 = kvc.h2o_decode_steps(q, kn, vn, *many, R, cap, sink=sink)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.stack(o1), o2) and torch.equal(torch.stack(e1), e2)
+    for a, b in zip(one, many):
+        assert torch.equal(a, b)
