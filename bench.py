@@ -460,6 +460,23 @@ def cpu_baseline(wl, pipe, budget_s=20.0):
             "decode_steps_per_s": 1.0 / per_step_dec if n_dec else None}
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of every rank's x: the job is as slow as its slowest rank."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, seconds: float) -> float:
+    """Units all ranks processed (each rank runs its own full workload) per second
+    of the slowest rank."""
+    return world * units_per_rank / seconds
+
+
 def run_ours(args, wl, rank, world):
     import torch
     import torch.distributed as dist
@@ -489,13 +506,10 @@ def run_ours(args, wl, rank, world):
         dist.barrier()
     launches = launch_count() - launches0
     ms = e0.elapsed_time(e1) / args.steps
-    ms_t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms_max = float(ms_t.item())
+    ms_max = max_over_ranks(ms, world, dev)
 
     tokens = wl.rows * wl.T
-    value = world * tokens / (ms_max / 1e3)
+    value = whole_job_rate(tokens, world, ms_max / 1e3)
     peak, peak_tf, peak_kind = measured_peaks()
     alg = algorithmic_bytes(wl)
     per_launch = {k: alg[k] for k in alg}
@@ -531,9 +545,12 @@ def run_ours(args, wl, rank, world):
     if not args.no_next_rows:
         line["next_rows"] = time_next_rows(pipe)
     if not args.no_e2e:
+        if world > 1:
+            dist.barrier()
         dt, h2d, d2h = run_e2e(wl, pipe, min(args.steps, 3), args.e2e_groups or E2E_GROUPS)
-        line["e2e"] = {"value": world * tokens / dt, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                       "d2h_bytes_per_step": d2h}
+        dt = max_over_ranks(dt, world, dev)
+        line["e2e"] = {"value": whole_job_rate(tokens, world, dt), "unit": UNIT,
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, pipe)
     return line
