@@ -510,6 +510,7 @@ def run_ours(args, wl, rank, world):
 
     tokens = wl.rows * wl.T
     value = whole_job_rate(tokens, world, ms_max / 1e3)
+    prefill_ms = sum(phases[n] for n in ("kv_score_obs", "hubkv_refine", "kv_select_topk", "kv_compact"))
     peak, peak_tf, peak_kind = measured_peaks()
     alg = algorithmic_bytes(wl)
     per_launch = {k: alg[k] for k in alg}
@@ -526,6 +527,9 @@ def run_ours(args, wl, rank, world):
                    "budget_k": wl.k, "recent": wl.R, "r": wl.r, "gamma": wl.gamma,
                    "decode_steps": wl.n_decode, "parallelism": f"replica x{world}",
                    "l2": f"inputs larger than L2 (K+V {2 * wl.units * wl.T * wl.d * wl.elem_bytes / 1e9:.1f} GB)"},
+        "prefill": {"ms": prefill_ms, "tokens_per_s": whole_job_rate(tokens, world, prefill_ms / 1e3),
+                    "head_tokens_per_s": whole_job_rate(tokens * wl.Hkv, world, prefill_ms / 1e3),
+                    "note": "score + refine + Top-K + compaction (one phase-timed step)"},
         "decode": {"steps_per_s": (1e3 / phases["h2o_decode_step"]) if wl.n_decode else None,
                    "ms_per_decode_step": phases["h2o_decode_step"] if wl.n_decode else None},
         "phases_ms": phases,

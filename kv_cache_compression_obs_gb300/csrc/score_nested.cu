@@ -26,11 +26,14 @@
 //      arithmetic throughout.  Writes a_c.
 //   2. global_kernel: same grid; adds the unit's block sums into the stable
 //      anchor, re-reads the block's keys and writes a_s and a_e.
-//   3. disc_kernel: one CTA per (unit, scale): radix select (order-preserving
-//      32-bit keys) of the n_disc-th largest and smallest a_k, then the two sums.
+//   3. disc_kernel: one CTA per (unit, scale): radix selects (order-preserving
+//      32-bit keys) of the n_disc-th largest and smallest a_k sharing every pass,
+//      then the two sums.
 //   4. final_kernel: elementwise weights, surprise, routing.
 // Per-token cross-lane sums go through batched butterflies: V values of 4 tokens
 // reduce in V-1 + (5 - log2 V) shuffles instead of 5 V.
+#include <type_traits>
+
 #include "kvc_internal.cuh"
 #include "select_common.cuh"
 #include "tc_common.cuh"
@@ -190,16 +193,27 @@ __global__ __launch_bounds__(NT_SCAN) void anchors_kernel(const T *__restrict__ 
     __syncwarp();
     int r = 0;  // i - (chunk start), i.e. i % window, kept as a running counter
     int rs = c0 % RW;  // i0 % RW
-    for (int i0 = c0; i0 < e; i0 += 4) {
+    // One batch of 4 tokens.  FAST: the batch lies inside [s, e), its leaving rows
+    // are real rows (i0 >= window) and window % 4 == 0, so no token needs a bounds
+    // check and a chunk can only start at the batch's first token; rows are then
+    // addressed by constant offsets from one pointer.
+    auto batch = [&](const int i0, auto fast_tag) {
+      constexpr bool FAST = decltype(fast_tag)::value;
       float2 x[4][P2], y[4][P2];
       float ss[4];
+      const T *px = Ku + (long)i0 * D;
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
-        // rows past e or before 0 load an in-range row instead (no branch): a token
-        // past e is never used, and a leaving row before 0 is scaled by 1/|k| = 0
-        const int i = min(i0 + t, e - 1);
-        R::load(Ku + (long)i * D, lane, keep_pol, x[t]);
-        R::load(Ku + (long)max(i - window, 0) * D, lane, last_pol, y[t]);
+        if constexpr (FAST) {
+          R::load(px + t * D, lane, keep_pol, x[t]);
+          R::load(px + (t - window) * D, lane, last_pol, y[t]);
+        } else {
+          // rows past e or before 0 load an in-range row instead (no branch): a
+          // token past e is never used, and a leaving row before 0 is scaled by 0
+          const int i = min(i0 + t, e - 1);
+          R::load(Ku + (long)i * D, lane, keep_pol, x[t]);
+          R::load(Ku + (long)max(i - window, 0) * D, lane, last_pol, y[t]);
+        }
         float2 q2 = __fmul2_rn(x[t][0], x[t][0]);
 #pragma unroll
         for (int p = 1; p < P2; ++p) q2 = __ffma2_rn(x[t][p], x[t][p], q2);
@@ -217,8 +231,8 @@ __global__ __launch_bounds__(NT_SCAN) void anchors_kernel(const T *__restrict__ 
         if (sn >= RW) sn -= RW;
         int so = sn + 4;
         if (so >= RW) so -= RW;
-        if ((lane & 7) == 0 && i < e) {
-          if (i >= window && i - window < i0) my_old = ring[so];
+        if ((lane & 7) == 0 && (FAST || i < e)) {
+          if (FAST || (i >= window && i - window < i0)) my_old = ring[so];
           ring[sn] = my_inv;
         }
       }
@@ -230,13 +244,15 @@ __global__ __launch_bounds__(NT_SCAN) void anchors_kernel(const T *__restrict__ 
         const int i = i0 + t;
         const float inv = __shfl_sync(0xFFFFFFFFu, my_inv, t * 8);
         float old = __shfl_sync(0xFFFFFFFFu, my_old, t * 8);
-        if (window < 4) {  // the leaving row may be in this very batch
-          const float same = __shfl_sync(0xFFFFFFFFu, my_inv, 8 * max(t - window, 0));
-          if (t >= window) old = same;
+        if constexpr (!FAST) {
+          if (window < 4) {  // the leaving row may be in this very batch
+            const float same = __shfl_sync(0xFFFFFFFFu, my_inv, 8 * max(t - window, 0));
+            if (t >= window) old = same;
+          }
         }
         float dot = 0.f, nrm = 0.f;
-        if (i < e) {
-          if (r == 0) {  // a new chunk: the previous chunk's total becomes Q
+        if (FAST || i < e) {
+          if ((!FAST || t == 0) && r == 0) {  // a new chunk: the previous total becomes Q
 #pragma unroll
             for (int p = 0; p < P2; ++p) {
               tot[p] = __fadd2_rn(tot[p], P[p]);
@@ -256,14 +272,20 @@ __global__ __launch_bounds__(NT_SCAN) void anchors_kernel(const T *__restrict__ 
           }
           dot = hsum(d2);
           nrm = hsum(n2);
-          if (i == s - 1) {
+          if constexpr (!FAST) {
+            if (i == s - 1) {
 #pragma unroll
-            for (int p = 0; p < P2; ++p) sil[p] = P[p];
+              for (int p = 0; p < P2; ++p) sil[p] = P[p];
+            }
+            r = (r + 1 == window) ? 0 : r + 1;
           }
-          r = (r + 1 == window) ? 0 : r + 1;
         }
         part[2 * t] = dot;
         part[2 * t + 1] = nrm;
+      }
+      if constexpr (FAST) {
+        r += 4;
+        if (r == window) r = 0;
       }
       const float v = reduce_scatter<8>(part, lane);
       // lane 8t holds token t's <k, window sum> and 1/|k|; lane 8t+4 the window's |.|^2
@@ -271,9 +293,16 @@ __global__ __launch_bounds__(NT_SCAN) void anchors_kernel(const T *__restrict__ 
       if ((lane & 7) == 0) {
         const int i = i0 + (lane >> 3);
         // cos(kh_i, window sum) with |kh_i| = 1 (a zero key has dot 0)
-        if (i >= s && i < e) ac[i] = nrm > 0.f ? -(v * my_inv) * rsqrtf(nrm) : 0.f;
+        if (FAST || (i >= s && i < e)) ac[i] = nrm > 0.f ? -(v * my_inv) * rsqrtf(nrm) : 0.f;
       }
       __syncwarp();  // this batch's ring writes before the next batch's reads
+    };
+    const bool can_fast = window % 4 == 0;
+    for (int i0 = c0; i0 < e; i0 += 4) {
+      if (can_fast && i0 >= s && i0 >= window && i0 + 4 <= e)
+        batch(i0, std::integral_constant<bool, true>());
+      else
+        batch(i0, std::integral_constant<bool, false>());
     }
 #pragma unroll
     for (int p = 0; p < P2; ++p)
@@ -339,11 +368,24 @@ __global__ __launch_bounds__(NT_SCAN) void global_kernel(const T *__restrict__ K
   float *ae = a + (unit * 3 + 1) * (long)Tn;
   int s, e;
   warp_range(lo, hi, warp, s, e);
+  // rows past e load an in-range row instead (never written out); the next
+  // batch's rows are loaded before this batch is reduced, so two batches of
+  // loads are in flight per warp
+  float2 xn[4][P2];
+  if (s < e) {
+#pragma unroll
+    for (int t = 0; t < 4; ++t) R::load(Ku + (long)min(s + t, e - 1) * D, lane, pol, xn[t]);
+  }
   for (int i0 = s; i0 < e; i0 += 4) {
     float2 x[4][P2];
 #pragma unroll
-    for (int t = 0; t < 4; ++t)  // past e: an in-range row, never written out
-      R::load(Ku + (long)min(i0 + t, e - 1) * D, lane, pol, x[t]);
+    for (int t = 0; t < 4; ++t)
+#pragma unroll
+      for (int p = 0; p < P2; ++p) x[t][p] = xn[t][p];
+    if (i0 + 4 < e) {
+#pragma unroll
+      for (int t = 0; t < 4; ++t) R::load(Ku + (long)min(i0 + 4 + t, e - 1) * D, lane, pol, xn[t]);
+    }
     float part[16];
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
@@ -376,36 +418,74 @@ __global__ __launch_bounds__(NT_SCAN) void global_kernel(const T *__restrict__ K
 }
 
 // ---- 3. discriminative power per (unit, scale) -----------------------------------
-// Sum of the `m` largest values of v[0..n) (DESC) or of the `m` smallest (!DESC):
-// radix select of the m-th key, then the values beyond it plus the right number
-// of copies of the boundary value.  Deterministic block reduction.
-template <bool DESC>
-__device__ float extreme_sum(const float *__restrict__ v, int n, int m, uint32_t *hist,
-                             uint32_t *tot, int *warp_sums, uint32_t *sh) {
+// Calls f(x) for every value of v[0..n) with 16-byte loads (scalars up to the first
+// 16-byte boundary and after the last), four vectors in flight per thread.
+template <typename F>
+__device__ __forceinline__ void for_values(const float *__restrict__ v, int n, F &&f) {
+  const int mis = (int)((reinterpret_cast<uintptr_t>(v) >> 2) & 3);
+  const int pre = min(n, (4 - mis) & 3), n4 = (n - pre) >> 2, tail = pre + 4 * n4;
+  const float4 *v4 = reinterpret_cast<const float4 *>(v + pre);
+  for (int base = threadIdx.x; base < n4; base += 4 * NT_DISC) {
+    float4 q[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = base + u * NT_DISC;
+      q[u] = j < n4 ? __ldg(v4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (base + u * NT_DISC < n4) {
+        f(q[u].x);
+        f(q[u].y);
+        f(q[u].z);
+        f(q[u].w);
+      }
+  }
+  const int t = threadIdx.x;
+  if (t < pre) f(__ldg(v + t));
+  else if (t < pre + (n - tail)) f(__ldg(v + tail + (t - pre)));
+}
+
+// D = (sum of the m largest of v) / m - (sum of the m smallest) / m.  Both radix
+// selects (order-preserving keys for the largest, their complements for the
+// smallest) share every pass over v: 4 histogram passes of 8 bits and one sum
+// pass.  Each sum is the values strictly beyond the boundary key plus the right
+// number of copies of the boundary value; block reductions in a fixed order.
+__global__ __launch_bounds__(NT_DISC, 1) void disc_kernel(const float *__restrict__ a, int Tn,
+                                                          int m, float *__restrict__ D) {
   constexpr int NW = NT_DISC / 32;
+  extern __shared__ uint32_t hist[];  // [2][NW][256]
+  __shared__ uint32_t tot[2][256];
+  __shared__ uint32_t sh_prefix[2];
+  __shared__ int sh_need[2];
+  __shared__ float sh_b[2], red[2][NW];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  auto key = [](float x) { return DESC ? order_key(x) : ~order_key(x); };
-  uint32_t prefix = 0, mask = 0;
-  int need = m;
+  const float *v = a + (long)blockIdx.x * Tn;  // blockIdx.x = unit * 3 + scale
+  uint32_t prefix[2] = {0u, 0u}, mask = 0u;
+  int need[2] = {m, m};
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
-    for (int i = threadIdx.x; i < NW * 256; i += NT_DISC) hist[i] = 0u;
+    for (int i = threadIdx.x; i < 2 * NW * 256; i += NT_DISC) hist[i] = 0u;
     __syncthreads();
-    for (int i = threadIdx.x; i < n; i += NT_DISC) {
-      const uint32_t u = key(v[i]);
-      if ((u & mask) == prefix) atomicAdd(&hist[warp * 256 + ((u >> shift) & 255u)], 1u);
-    }
+    uint32_t *h0 = hist + warp * 256, *h1 = hist + (NW + warp) * 256;
+    for_values(v, Tn, [&](float x) {
+      const uint32_t u = order_key(x), ub = ~u;
+      if ((u & mask) == prefix[0]) atomicAdd(h0 + ((u >> shift) & 255u), 1u);
+      if ((ub & mask) == prefix[1]) atomicAdd(h1 + ((ub >> shift) & 255u), 1u);
+    });
     __syncthreads();
-    if (threadIdx.x < 256) {
+    for (int i = threadIdx.x; i < 512; i += NT_DISC) {
+      const int k = i >> 8, d = i & 255;
       uint32_t t = 0;
-      for (int w = 0; w < NW; ++w) t += hist[w * 256 + threadIdx.x];
-      tot[threadIdx.x] = t;
+      for (int w = 0; w < NW; ++w) t += hist[(k * NW + w) * 256 + d];
+      tot[k][d] = t;
     }
     __syncthreads();
-    if (warp == 0) {
+    if (warp < 2) {  // warp 0 decides for the largest, warp 1 for the smallest
+      const int k = warp;
       uint32_t mine = 0;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mine += tot[255 - 8 * lane - i];
+      for (int i = 0; i < 8; ++i) mine += tot[k][255 - 8 * lane - i];
       uint32_t incl = mine;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
@@ -413,62 +493,54 @@ __device__ float extreme_sum(const float *__restrict__ v, int n, int m, uint32_t
         if (lane >= off) incl += y;
       }
       uint32_t above = incl - mine;
-      if (above < (uint32_t)need && (uint32_t)need <= incl) {
+      if (above < (uint32_t)need[k] && (uint32_t)need[k] <= incl) {
         for (int i = 0; i < 8; ++i) {
           const int dgt = 255 - 8 * lane - i;
-          if ((uint32_t)need <= above + tot[dgt]) {
-            sh[0] = prefix | ((uint32_t)dgt << shift);
-            sh[1] = (uint32_t)(need - (int)above);
+          if ((uint32_t)need[k] <= above + tot[k][dgt]) {
+            sh_prefix[k] = prefix[k] | ((uint32_t)dgt << shift);
+            sh_need[k] = need[k] - (int)above;
             break;
           }
-          above += tot[dgt];
+          above += tot[k][dgt];
         }
       }
     }
     __syncthreads();
-    prefix = sh[0];
-    need = (int)sh[1];
+    prefix[0] = sh_prefix[0];
+    prefix[1] = sh_prefix[1];
+    need[0] = sh_need[0];
+    need[1] = sh_need[1];
     mask |= 255u << shift;
     __syncthreads();
   }
-  // values strictly beyond the boundary key, in a fixed order
-  const uint32_t ustar = prefix;
-  __shared__ float sh_b;  // the boundary value (every value with that key is equal up to sign of 0)
-  float part = 0.f;
-  for (int i = threadIdx.x; i < n; i += NT_DISC) {
-    const float x = v[i];
-    const uint32_t u = key(x);
-    if (u > ustar) part += x;
-    if (u == ustar) sh_b = x;
-  }
-  float x = part;
+  float ptop = 0.f, pbot = 0.f;
+  for_values(v, Tn, [&](float x) {
+    const uint32_t u = order_key(x), ub = ~u;
+    if (u > prefix[0]) ptop += x;
+    if (u == prefix[0]) sh_b[0] = x;  // every value with the boundary key is equal (up to the sign of 0)
+    if (ub > prefix[1]) pbot += x;
+    if (ub == prefix[1]) sh_b[1] = x;
+  });
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
-  float *fs = reinterpret_cast<float *>(warp_sums);
-  if (lane == 0) fs[warp] = x;
-  __syncthreads();
-  float total = 0.f;
-  if (threadIdx.x == 0) {
-    for (int w = 0; w < NW; ++w) total += fs[w];
-    total += (float)need * sh_b;
-    fs[NW] = total;
+  for (int o = 16; o > 0; o >>= 1) {
+    ptop += __shfl_xor_sync(0xFFFFFFFFu, ptop, o);
+    pbot += __shfl_xor_sync(0xFFFFFFFFu, pbot, o);
+  }
+  if (lane == 0) {
+    red[0][warp] = ptop;
+    red[1][warp] = pbot;
   }
   __syncthreads();
-  total = fs[NW];
-  __syncthreads();
-  return total;
-}
-
-__global__ __launch_bounds__(NT_DISC, 1) void disc_kernel(const float *__restrict__ a, int Tn,
-                                                       int m, float *__restrict__ D) {
-  __shared__ uint32_t hist[(NT_DISC / 32) * 256];
-  __shared__ uint32_t tot[256];
-  __shared__ int warp_sums[NT_DISC / 32 + 1];
-  __shared__ uint32_t sh[2];
-  const float *v = a + (long)blockIdx.x * Tn;  // blockIdx.x = unit * 3 + scale
-  const float top = extreme_sum<true>(v, Tn, m, hist, tot, warp_sums, sh);
-  const float bot = extreme_sum<false>(v, Tn, m, hist, tot, warp_sums, sh);
-  if (threadIdx.x == 0) D[blockIdx.x] = (top - bot) / (float)m;
+  if (threadIdx.x == 0) {
+    float top = 0.f, bot = 0.f;
+    for (int w = 0; w < NW; ++w) {
+      top += red[0][w];
+      bot += red[1][w];
+    }
+    top += (float)need[0] * sh_b[0];
+    bot += (float)need[1] * sh_b[1];
+    D[blockIdx.x] = (top - bot) / (float)m;
+  }
 }
 
 // ---- 4. weights, surprise, routing ------------------------------------------------
@@ -519,7 +591,10 @@ int run_nested(const void *K, long units, int Tn, int window, int n_blocks, int 
   global_kernel<T, D><<<grid, NT_SCAN, 0, st>>>(static_cast<const T *>(K), Tn, blk, n_blocks,
                                                 esum, a);
   if ((rc = launch_status())) return rc;
-  disc_kernel<<<(unsigned)(units * 3), NT_DISC, 0, st>>>(a, Tn, n_disc, Dw);
+  const size_t dsm = (size_t)2 * (NT_DISC / 32) * 256 * sizeof(uint32_t);
+  if (ensure_smem((const void *)disc_kernel, dsm))
+    return cuda_failure(cudaErrorInvalidValue, "nested disc kernel: shared memory");
+  disc_kernel<<<(unsigned)(units * 3), NT_DISC, dsm, st>>>(a, Tn, n_disc, Dw);
   if ((rc = launch_status())) return rc;
   const dim3 fgrid((unsigned)min((Tn + 1023) / 1024, 64), (unsigned)min(units, 65535L));
   final_kernel<<<fgrid, 256, 0, st>>>(a, Dw, Tn, units, lp0, lp1, lp2, thresh, score, w_out);
