@@ -279,7 +279,8 @@ KVC_API int kv_select_budget(const float *z, int B, int H, int T, int budget, in
  *
  *   K, V       [B][H][T][d], device or pinned host memory (as for kv_compact);
  *              s [B][H][T] float32, may be NULL (acc_out not written)
- *   idx        [B][budget] int32;  off [B][H+1] int32 (CSR, as kv_select_budget writes)
+ *   idx        [B][budget] int32 (may be NULL when budget == 0);  off [B][H+1] int32
+ *              (CSR, as kv_select_budget writes)
  *   K_out, V_out [B][H][cap][d];  pos_out, acc_out [B][H][cap];  len_out [B][H]
  *   dev_status device int, may be NULL; set to KV_ERR_INVALID_ARG when a row's
  *              offsets are not non-decreasing within [0, budget] (that row is left

@@ -221,8 +221,8 @@ int kv_compact_ragged(const void *K, const void *V, const float *s, const int32_
       !fits(B, budget))
     return KV_ERR_INVALID_ARG;
   if (B == 0) return KV_OK;
-  if (!K || !V || !idx || !off || !K_out || !V_out || !pos_out || !len_out)
-    return KV_ERR_INVALID_ARG;
+  if (!K || !V || (!idx && budget > 0) || !off || !K_out || !V_out || !pos_out || !len_out)
+    return KV_ERR_INVALID_ARG;  // idx is not read when the budget is 0
   if (!aligned16(K) || !aligned16(V) || !aligned16(K_out) || !aligned16(V_out) ||
       (s && ((uintptr_t)s & 3u)) || (acc_out && ((uintptr_t)acc_out & 3u)))
     return KV_ERR_INVALID_ARG;

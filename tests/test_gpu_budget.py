@@ -158,3 +158,43 @@ def test_budget_chain_then_decode_appends(kvc, oracle_mod):
         decode_lockstep(kvc, oracle_mod, q, kn, vn, Kc, Vc, pos, acc, ln, R, T + step, scale, sink=S)
     torch.cuda.synchronize()
     assert torch.equal(ln.cpu(), torch.clamp(counts + 12, max=cap))
+
+
+def test_select_budget_max_heads(kvc, oracle_mod):
+    """256 heads: 32 heads per CTA of an 8-CTA cluster."""
+    B, H, T = 2, 256, 300
+    z = _z(B, H, T, seed=256, ties=True)
+    budget, floor, R, S = H * 40, 20, 4, 2
+    idx, off = kvc.kv_select_budget(z, budget, floor, R, S)
+    torch.cuda.synchronize()
+    ref_idx, ref_off = oracle_mod.select_budget(z.cpu().numpy().astype(np.float64), budget, floor, R, S)
+    np.testing.assert_array_equal(off.cpu().numpy(), ref_off)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+
+
+def test_compact_ragged_empty_heads_and_zero_budget(kvc, oracle_mod):
+    B, H, T, d, cap = 1, 4, 40, 64, 6
+    K = torch.randn(B, H, T, d, device=DEV)
+    idx = torch.tensor([[3, 9, 1, 0, 5]], dtype=torch.int32, device=DEV)
+    off = torch.tensor([[0, 0, 2, 2, 5]], dtype=torch.int32, device=DEV)  # heads 0 and 2 keep nothing
+    outs = dict(K_out=torch.full((B, H, cap, d), 5.0, device=DEV),
+                V_out=torch.full((B, H, cap, d), 5.0, device=DEV),
+                pos_out=torch.full((B, H, cap), -3, dtype=torch.int32, device=DEV),
+                len_out=torch.full((B, H), -1, dtype=torch.int32, device=DEV))
+    kvc.kv_compact_ragged(K, K, None, idx, off, cap, **outs)
+    torch.cuda.synchronize()
+    ref = oracle_mod.compact_ragged(K.cpu().numpy(), K.cpu().numpy(), None, idx.cpu().numpy(),
+                                    off.cpu().numpy(), cap,
+                                    out=tuple(t.cpu().numpy().copy() for t in (
+                                        outs["K_out"], outs["V_out"], outs["pos_out"],
+                                        torch.zeros(B, H, cap), outs["len_out"])))
+    np.testing.assert_array_equal(outs["len_out"].cpu().numpy(), [[0, 2, 0, 3]])
+    np.testing.assert_array_equal(outs["pos_out"].cpu().numpy(), ref[2])
+    np.testing.assert_array_equal(outs["K_out"].cpu().numpy(), ref[0])
+    # a zero budget writes only the lengths
+    idx0 = torch.zeros(B, 0, dtype=torch.int32, device=DEV)
+    off0 = torch.zeros(B, H + 1, dtype=torch.int32, device=DEV)
+    kvc.kv_compact_ragged(K, K, None, idx0, off0, cap, **outs)
+    torch.cuda.synchronize()
+    assert (outs["len_out"] == 0).all()
+    np.testing.assert_array_equal(outs["pos_out"].cpu().numpy(), ref[2])

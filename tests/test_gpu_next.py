@@ -119,3 +119,45 @@ def test_multi_step_decode_equals_single_steps(kvc, G, sink, R, fill):
     assert torch.equal(torch.stack(o1), o2) and torch.equal(torch.stack(e1), e2)
     for a, b in zip(one, many):
         assert torch.equal(a, b)
+
+
+def test_multi_step_decode_alg1_and_zero_steps(kvc):
+    g = torch.Generator(device=DEV)
+    g.manual_seed(77)
+    B, Hkv, G, cap, d, n = 1, 2, 4, 64, 64, 9
+    K = torch.randn(B, Hkv, cap, d, generator=g, device=DEV)
+    V = torch.randn(B, Hkv, cap, d, generator=g, device=DEV)
+    pos = torch.arange(cap, dtype=torch.int32, device=DEV).repeat(B, Hkv, 1).contiguous()
+    acc = torch.rand(B, Hkv, cap, generator=g, device=DEV)
+    ln = torch.full((B, Hkv), cap, dtype=torch.int32, device=DEV)
+    q = torch.randn(n, B, Hkv * G, d, generator=g, device=DEV)
+    kn = torch.randn(n, B, Hkv, d, generator=g, device=DEV)
+    vn = torch.randn(n, B, Hkv, d, generator=g, device=DEV)
+    one = [t.clone() for t in (K, V, pos, acc, ln)]
+    many = [t.clone() for t in (K, V, pos, acc, ln)]
+    o1, e1 = zip(*[kvc.h2o_decode_step(q[t], kn[t], vn[t], *one, 0, cap + t, flags=kvc.KV_H2O_ALG1)
+                   for t in range(n)])
+    o2, e2 = kvc.h2o_decode_steps(q, kn, vn, *many, 0, cap, flags=kvc.KV_H2O_ALG1)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.stack(o1), o2) and torch.equal(torch.stack(e1), e2)
+    for a, b in zip(one, many):
+        assert torch.equal(a, b)
+    # zero steps: nothing changes
+    before = [t.clone() for t in many]
+    kvc.h2o_decode_steps(q[:0], kn[:0], vn[:0], *many, 0, cap + n, flags=kvc.KV_H2O_ALG1)
+    torch.cuda.synchronize()
+    for a, b in zip(before, many):
+        assert torch.equal(a, b)
+
+
+def test_select_topk_many_heads(kvc, oracle_mod):
+    """Thousands of single-CTA heads and a few 2-CTA clusters in one launch."""
+    g = torch.Generator(device=DEV)
+    g.manual_seed(3001)
+    for B, H, T, k, R in [(3, 1000, 1000, 100, 10), (1, 40, 17000, 1700, 64)]:
+        z = torch.rand(B, H, T, generator=g, device=DEV)
+        z = torch.floor(z * 50) / 50
+        idx = kvc.kv_select_topk(z, k, R)
+        torch.cuda.synchronize()
+        ref = oracle_mod.select_topk(z.cpu().numpy().astype(np.float64), k, R)
+        np.testing.assert_array_equal(idx.cpu().numpy(), ref)
