@@ -323,6 +323,12 @@ KVC_API int kv_compact_ragged(const void *K, const void *V, const float *s, cons
  *               untouched), never cleared by the library
  * Preconditions: 0 <= recent < cap, KV_H2O_ALG1 => recent == 0, new_pos larger
  * than every cached position, 0 <= len <= cap.
+ * With B >= 2 the batch rows run in two halves, [0, B/2) on `stream` and the
+ * rest on a library-owned stream of the current device (created on first use),
+ * forked from and joined back into `stream` with events: the call stays
+ * asynchronous and ordered on `stream` (and can be captured into a graph), and
+ * one half's finalize work overlaps the other half's cache pass.  The
+ * workspace holds both halves' scratch (kv_workspace_size accounts for it).
  */
 KVC_API int h2o_decode_step(const void *q, const void *k_new, const void *v_new, void *K_cache,
                     void *V_cache, int32_t *pos, float *acc, int32_t *len, int B, int Hq,

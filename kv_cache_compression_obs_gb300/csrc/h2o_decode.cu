@@ -59,8 +59,9 @@ constexpr int kMaxStages = 16;
 constexpr long long kWaitBudget = 2000000000LL;  // clock cycles (~1 s) before a wait gives up
 constexpr long long kDrainBudget = 200000000LL;  // ~0.1 s for copies in flight at exit
 constexpr int BAR_CONS = 1;  // named barrier of the consumer warps
-constexpr int NTF = 256;     // finalize threads per CTA
-constexpr int CE = 4;        // finalize CTAs per unit
+constexpr int NTF = 128;     // finalize threads per CTA: small enough (with its registers) to
+                             // share an SM with a stream CTA of the other half of the rows
+constexpr int CE = 8;        // finalize CTAs per unit
 constexpr int RU = 8;        // finalize slots per thread in flight
 
 __device__ __forceinline__ bool better(float a, int p, float ba, int bp) {

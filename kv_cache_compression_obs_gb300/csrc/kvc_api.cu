@@ -71,9 +71,96 @@ bool dim_ok(int d) { return d == 64 || d == 128; }
 // product of non-negative ints without overflow of 2^62
 bool fits(long long a, long long b) { return a >= 0 && b >= 0 && (b == 0 || a <= (1LL << 62) / b); }
 
+
+// A decode call's batch rows run in two halves: rows [0, B/2) on the caller's
+// stream and [B/2, B) on a library-owned side stream (one per device, created on
+// first use), forked from and joined back into the caller's stream with events.
+// The halves are independent units; each half's latency-bound finalize launches
+// run beside the other half's bandwidth-bound stream kernel.  Fewer than 2 rows,
+// or a device whose side stream could not be created, run on the caller's
+// stream alone.
+int split_rows(int B) { return B >= 2 ? B / 2 : B; }
+
+size_t align256h(size_t x) { return (x + 255) & ~(size_t)255; }
+
+size_t decode_ws_split(int B, int Hkv, int G, int cap, int d) {
+  const int Ba = split_rows(B);
+  const size_t a = decode_workspace_bytes((long)Ba * Hkv, G, cap, d);
+  if (Ba == B) return a;
+  return align256h(a) + decode_workspace_bytes((long)(B - Ba) * Hkv, G, cap, d);
+}
+
+struct SideStream {
+  std::mutex mu;
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  bool ready = false, failed = false;
+};
+SideStream g_side[64];
+
+int decode_run(const void *q, const void *k_new, const void *v_new, int n_steps, void *K_cache,
+               void *V_cache, int32_t *pos, float *acc, int32_t *len, int B, int Hq, int Hkv,
+               int cap, int d, int recent, int sink, int32_t first_pos, float scale, int flags,
+               int dtype, float *o_out, int32_t *evicted_pos, void *workspace, int *dev_status,
+               cudaStream_t stream) {
+  const size_t eb = dtype == KV_F32 ? 4 : 2;
+  const int G = Hq / Hkv;
+  // step t of rows [r0, r1)
+  auto step = [&](int t, int r0, int r1, void *ws, cudaStream_t st) {
+    const size_t row_q = (size_t)Hq * d, row_kv = (size_t)Hkv * d, row_c = (size_t)Hkv * cap;
+    const size_t qo = ((size_t)t * B + r0) * row_q, ko = ((size_t)t * B + r0) * row_kv;
+    return launch_decode_step(
+        static_cast<const char *>(q) + qo * eb, static_cast<const char *>(k_new) + ko * eb,
+        static_cast<const char *>(v_new) + ko * eb,
+        static_cast<char *>(K_cache) + (size_t)r0 * row_c * d * eb,
+        static_cast<char *>(V_cache) + (size_t)r0 * row_c * d * eb, pos + (size_t)r0 * row_c,
+        acc + (size_t)r0 * row_c, len + (size_t)r0 * Hkv, r1 - r0, Hq, Hkv, cap, d, recent, sink,
+        first_pos + t, scale, flags, dtype, ws, o_out + qo,
+        evicted_pos + ((size_t)t * B + r0) * Hkv, dev_status, st);
+  };
+  auto single = [&]() {
+    for (int t = 0; t < n_steps; ++t) {
+      const int rc = step(t, 0, B, workspace, stream);
+      if (rc != KV_OK) return rc;
+    }
+    return (int)KV_OK;
+  };
+  const int Ba = split_rows(B);
+  int dev = 0;
+  if (Ba == B || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return single();
+  SideStream &sd = g_side[dev];
+  std::lock_guard<std::mutex> lock(sd.mu);
+  if (!sd.ready && !sd.failed) {
+    if (cudaStreamCreateWithFlags(&sd.s, cudaStreamNonBlocking) == cudaSuccess &&
+        cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming) == cudaSuccess &&
+        cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming) == cudaSuccess) {
+      sd.ready = true;
+    } else {
+      cudaGetLastError();
+      sd.failed = true;  // the whole batch then runs on the caller's stream
+    }
+  }
+  if (!sd.ready) return single();
+  void *ws_b = static_cast<char *>(workspace) +
+               align256h(decode_workspace_bytes((long)Ba * Hkv, G, cap, d));
+  cudaError_t e = cudaEventRecord(sd.fork, stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(sd.s, sd.fork, 0);
+  if (e != cudaSuccess) return cuda_failure(e, "decode: fork to the side stream");
+  int rc = KV_OK;
+  for (int t = 0; t < n_steps && rc == KV_OK; ++t) {  // interleaved, so both streams start at once
+    rc = step(t, 0, Ba, workspace, stream);
+    if (rc == KV_OK) rc = step(t, Ba, B, ws_b, sd.s);
+  }
+  e = cudaEventRecord(sd.join, sd.s);  // joined back even after a failed launch
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, sd.join, 0);
+  if (e != cudaSuccess && rc == KV_OK) rc = cuda_failure(e, "decode: join from the side stream");
+  return rc;
+}
+
 }  // namespace
 
 extern "C" {
+
 
 int kv_version(void) { return 100; }
 
@@ -111,7 +198,7 @@ size_t kv_workspace_size(int op, int B, int Hq, int Hkv, int T, int d, int W, in
       return nested_workspace_bytes((long)B * Hkv, T, d, W, true);
     case KV_OP_DECODE:  // T is the slot capacity
       if (Hq <= 0 || Hkv <= 0 || Hq % Hkv || !(d == 64 || d == 128)) return 0;
-      return decode_workspace_bytes((long)B * Hkv, Hq / Hkv, T, d);
+      return decode_ws_split(B, Hkv, Hq / Hkv, T, d);
     default:
       return 0;
   }
@@ -260,27 +347,9 @@ int h2o_decode_step_ex(const void *q, const void *k_new, const void *v_new, void
                     int Hkv, int cap, int d, int recent, int sink, int32_t new_pos, float scale,
                     int flags, int dtype, float *o_out, int32_t *evicted_pos, void *workspace,
                     size_t workspace_bytes, int *dev_status, kv_stream_t stream) {
-  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || cap <= 0 || recent < 0 || sink < 0 ||
-      recent >= cap || new_pos < 0 || !dtype_ok(dtype) || (flags & ~KV_H2O_ALG1) ||
-      ((flags & KV_H2O_ALG1) && recent != 0) || !(scale == scale))
-    return KV_ERR_INVALID_ARG;
-  if (!dim_ok(d)) return KV_ERR_UNSUPPORTED;
-  if (!fits((long long)B * Hkv, (long long)cap * d)) return KV_ERR_INVALID_ARG;
-  if (B == 0) return KV_OK;
-  if (!q || !k_new || !v_new || !K_cache || !V_cache || !pos || !acc || !len || !o_out ||
-      !evicted_pos)
-    return KV_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(K_cache) ||
-      !aligned16(V_cache))
-    return KV_ERR_INVALID_ARG;
-  const int G = Hq / Hkv;
-  if (G != 1 && G != 2 && G != 4 && G != 8) return KV_ERR_UNSUPPORTED;
-  if (!workspace || workspace_bytes < decode_workspace_bytes((long)B * Hkv, G, cap, d) ||
-      !aligned16(workspace))
-    return KV_ERR_WORKSPACE;
-  return launch_decode_step(q, k_new, v_new, K_cache, V_cache, pos, acc, len, B, Hq, Hkv, cap,
-                            d, recent, sink, new_pos, scale, flags, dtype, workspace, o_out,
-                            evicted_pos, dev_status, static_cast<cudaStream_t>(stream));
+  return h2o_decode_steps(q, k_new, v_new, 1, K_cache, V_cache, pos, acc, len, B, Hq, Hkv, cap, d,
+                          recent, sink, new_pos, scale, flags, dtype, o_out, evicted_pos, workspace,
+                          workspace_bytes, dev_status, stream);
 }
 
 int h2o_decode_steps(const void *q, const void *k_new, const void *v_new, int n_steps,
@@ -291,26 +360,27 @@ int h2o_decode_steps(const void *q, const void *k_new, const void *v_new, int n_
                      kv_stream_t stream) {
   if (n_steps < 0 || first_pos < 0 || (long long)first_pos + n_steps - 1 > INT_MAX)
     return KV_ERR_INVALID_ARG;
-  if (n_steps == 0 || B == 0) {
-    // validate the rest as a single step would, without launching anything
-    return h2o_decode_step_ex(q, k_new, v_new, K_cache, V_cache, pos, acc, len, 0, Hq, Hkv, cap,
-                              d, recent, sink, first_pos, scale, flags, dtype, o_out, evicted_pos,
-                              workspace, workspace_bytes, dev_status, stream);
-  }
-  const size_t eb = dtype == KV_F32 ? 4 : 2;
-  const size_t q_step = (size_t)B * Hq * d, kv_step = (size_t)B * Hkv * d;
-  for (int t = 0; t < n_steps; ++t) {
-    const int rc = h2o_decode_step_ex(
-        q ? static_cast<const char *>(q) + t * q_step * eb : nullptr,
-        k_new ? static_cast<const char *>(k_new) + t * kv_step * eb : nullptr,
-        v_new ? static_cast<const char *>(v_new) + t * kv_step * eb : nullptr, K_cache, V_cache,
-        pos, acc, len, B, Hq, Hkv, cap, d, recent, sink, first_pos + t, scale, flags, dtype,
-        o_out ? o_out + t * q_step : nullptr,
-        evicted_pos ? evicted_pos + (size_t)t * B * Hkv : nullptr, workspace, workspace_bytes,
-        dev_status, stream);
-    if (rc != KV_OK) return rc;
-  }
-  return KV_OK;
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || cap <= 0 || recent < 0 || sink < 0 ||
+      recent >= cap || !dtype_ok(dtype) || (flags & ~KV_H2O_ALG1) ||
+      ((flags & KV_H2O_ALG1) && recent != 0) || !(scale == scale))
+    return KV_ERR_INVALID_ARG;
+  if (!dim_ok(d)) return KV_ERR_UNSUPPORTED;
+  if (!fits((long long)B * Hkv, (long long)cap * d) || !fits((long long)B * Hq, (long long)n_steps * d))
+    return KV_ERR_INVALID_ARG;
+  if (B == 0 || n_steps == 0) return KV_OK;
+  if (!q || !k_new || !v_new || !K_cache || !V_cache || !pos || !acc || !len || !o_out ||
+      !evicted_pos)
+    return KV_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(K_cache) ||
+      !aligned16(V_cache))
+    return KV_ERR_INVALID_ARG;
+  const int G = Hq / Hkv;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return KV_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < decode_ws_split(B, Hkv, G, cap, d) || !aligned16(workspace))
+    return KV_ERR_WORKSPACE;
+  return decode_run(q, k_new, v_new, n_steps, K_cache, V_cache, pos, acc, len, B, Hq, Hkv, cap, d,
+                    recent, sink, first_pos, scale, flags, dtype, o_out, evicted_pos, workspace,
+                    dev_status, static_cast<cudaStream_t>(stream));
 }
 
 int h2o_decode_step(const void *q, const void *k_new, const void *v_new, void *K_cache,
