@@ -90,12 +90,12 @@ def score_flops(wl):
     return 2 * 2 * (wl.Hq // wl.Hkv) * wl.W * wl.T * wl.d * wl.units
 
 
-# DRAM bytes per decode step (both launches) from `ncu --metrics
-# dram__bytes_read.sum,dram__bytes_write.sum` of the current kernels, per
-# workload; see profiles/decode_long-context.md (captured on 8 of the 32 layers
-# and scaled by 4: the step's traffic is proportional to the units).  None where
-# not captured.
-DECODE_TRAFFIC = {"long-context": 4 * (214883840 + 4654080 + 10577920)}
+# DRAM bytes per decode step (all its launches: the two row halves' stream and
+# finalize kernels) from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum`
+# of the current kernels, per workload; see profiles/decode_long-context.md
+# (captured on 8 of the 32 layers, mean over four halves, scaled by 4: the step's
+# traffic is proportional to the units).  None where not captured.
+DECODE_TRAFFIC = {"long-context": 4 * 2 * (107466880 + 864832 + 5462144)}
 
 
 def measured_peaks():
@@ -537,7 +537,7 @@ def run_ours(args, wl, rank, world):
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "algorithmic_bytes": per_launch[dom], "traffic": traffic,
-                     "note": ("one decode step = the stream and finalize launches, timed together"
+                     "note": ("one decode step = its stream and finalize launches (two row halves on two streams), timed together"
                               if dom == "h2o_decode_step" else None)},
         "roofline_score": {"kernel": "kv_score_obs", "bound": "tensor", "achieved": score_tf,
                            "peak": peak_tf, "peak_kind": peak_kind + " bf16 dense (burst)",
