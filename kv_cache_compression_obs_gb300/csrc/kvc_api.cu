@@ -34,29 +34,38 @@ int device_sm_count() {
 // Raise a kernel's dynamic shared-memory limit once per (device, kernel) when its
 // static plus dynamic shared memory passes the 48 KB default.
 int ensure_smem(const void *func, size_t bytes) {
+  struct Entry {
+    size_t static_bytes = 0;  // the kernel's static shared memory
+    size_t granted = 0;       // dynamic bytes it has been opted into
+  };
   static std::mutex mu;
-  static std::unordered_map<const void *, size_t> done[64];
-  cudaFuncAttributes fa = {};
-  if (cudaFuncGetAttributes(&fa, func) != cudaSuccess) {
-    cudaGetLastError();
-    return 1;
-  }
-  const size_t static_bytes = fa.sharedSizeBytes;
-  if (bytes + static_bytes <= 48 * 1024) return 0;
+  static std::unordered_map<const void *, Entry> done[64];
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
   std::lock_guard<std::mutex> lock(mu);
   auto it = done[dev].find(func);
-  if (it != done[dev].end() && it->second >= bytes) return 0;
+  if (it == done[dev].end()) {  // first launch of this kernel on this device
+    cudaFuncAttributes fa = {};
+    if (cudaFuncGetAttributes(&fa, func) != cudaSuccess) {
+      cudaGetLastError();
+      return 1;
+    }
+    Entry e;
+    e.static_bytes = fa.sharedSizeBytes;
+    e.granted = e.static_bytes <= 48 * 1024 ? 48 * 1024 - e.static_bytes : 0;
+    it = done[dev].emplace(func, e).first;
+  }
+  Entry &e = it->second;
+  if (bytes <= e.granted) return 0;
   int optin = 0;
   cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  if ((size_t)optin < bytes + static_bytes) return 1;
+  if ((size_t)optin < bytes + e.static_bytes) return 1;
   if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
       cudaSuccess) {
     cudaGetLastError();
     return 1;
   }
-  done[dev][func] = bytes;
+  e.granted = bytes;
   return 0;
 }
 
