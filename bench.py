@@ -420,6 +420,26 @@ def run_e2e(wl, pipe, steps, n_groups):
     return dt, h2d, d2h
 
 
+def host_cpu_model():
+    """The host CPU's model name (lscpu / /proc/cpuinfo), or the machine type."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return platform.machine()
+
+
 def cpu_baseline(wl, pipe, budget_s=20.0):
     """The float64 oracle as it stands, on one batch row of the workload, on the host cores."""
     import numpy as np
@@ -453,7 +473,7 @@ def cpu_baseline(wl, pipe, budget_s=20.0):
     t_row = t_prefill + per_step_dec * wl.n_decode
     tokens = 1 * wl.T
     return {"value": tokens / t_row, "unit": UNIT, "cores": int(os.environ.get("OMP_NUM_THREADS", cores)),
-            "kind": "oracle",
+            "cpu": host_cpu_model(), "kind": "oracle",
             "sample": (f"batch row 0 of {wl.rows} ({wl.Hkv} KV heads, T={wl.T}): score+refine+Top-K+"
                        f"compact in {t_prefill:.2f} s, {n_dec} of {wl.n_decode} decode steps timed "
                        f"({per_step_dec * 1e3:.1f} ms each)"),
@@ -513,6 +533,7 @@ def run_ours(args, wl, rank, world):
     prefill_ms = sum(phases[n] for n in ("kv_score_obs", "hubkv_refine", "kv_select_topk", "kv_compact"))
     peak, peak_tf, peak_kind = measured_peaks()
     alg = algorithmic_bytes(wl)
+    prefill_bytes = sum(alg[n] for n in ("kv_score_obs", "hubkv_refine", "kv_select_topk", "kv_compact"))
     per_launch = {k: alg[k] for k in alg}
     dom = max(phases, key=lambda n: phases[n] * (wl.n_decode if n == "h2o_decode_step" else 1))
     achieved = per_launch[dom] / (phases[dom] / 1e3) / 1e9
@@ -529,7 +550,10 @@ def run_ours(args, wl, rank, world):
                    "l2": f"inputs larger than L2 (K+V {2 * wl.units * wl.T * wl.d * wl.elem_bytes / 1e9:.1f} GB)"},
         "prefill": {"ms": prefill_ms, "tokens_per_s": whole_job_rate(tokens, world, prefill_ms / 1e3),
                     "head_tokens_per_s": whole_job_rate(tokens * wl.Hkv, world, prefill_ms / 1e3),
-                    "note": "score + refine + Top-K + compaction (one phase-timed step)"},
+                    "algorithmic_bytes": prefill_bytes,
+                    "hbm_frac": prefill_bytes / (prefill_ms / 1e3) / 1e9 / peak,
+                    "note": "score + refine + Top-K + compaction (one phase-timed step); the "
+                            "scoring share is bound by its two MMA + exp passes, see roofline_score"},
         "decode": {"steps_per_s": (1e3 / phases["h2o_decode_step"]) if wl.n_decode else None,
                    "ms_per_decode_step": phases["h2o_decode_step"] if wl.n_decode else None},
         "phases_ms": phases,
