@@ -17,7 +17,7 @@ namespace kvc {
 namespace {
 
 constexpr int NT = 256;
-constexpr int kChunk = 4096;       // entropy chunk (elements)
+constexpr int kChunk = 16384;      // entropy chunk (elements): 64 per thread
 constexpr int kApply = 2048;       // elements per block of the apply pass
 constexpr int kMaxHalo = 64;       // pool_width <= 129
 
@@ -32,7 +32,8 @@ struct CSum {
   __device__ __forceinline__ double value() const { return (double)s + (double)c; }
 };
 
-// Per (head, chunk): sum s and sum s ln s (0 ln 0 = 0), reduced in a fixed tree.
+// Per (head, chunk): sum s and sum s ln s (0 ln 0 = 0), reduced in a fixed order
+// (per thread, then a warp butterfly in double, then the warps in order).
 __global__ __launch_bounds__(NT) void refine_entropy_kernel(const float *__restrict__ s, int T,
                                                             int n_chunks,
                                                             double2 *__restrict__ part) {
@@ -41,23 +42,40 @@ __global__ __launch_bounds__(NT) void refine_entropy_kernel(const float *__restr
   const float *sv = s + head * (long)T;
   const int i0 = chunk * kChunk, i1 = min(T, i0 + kChunk);
   CSum a, c;
-  for (int i = i0 + threadIdx.x; i < i1; i += NT) {
-    const float x = sv[i];
-    a.add(x);
-    if (x > 0.f) c.add(x * logf(x));
-  }
-  __shared__ double ra[NT], rc[NT];
-  ra[threadIdx.x] = a.value();
-  rc[threadIdx.x] = c.value();
-  __syncthreads();
-  for (int w = NT / 2; w > 0; w >>= 1) {
-    if (threadIdx.x < w) {
-      ra[threadIdx.x] += ra[threadIdx.x + w];
-      rc[threadIdx.x] += rc[threadIdx.x + w];
+  for (int base = i0 + threadIdx.x; base < i1; base += 4 * NT) {
+    float x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {  // four loads in flight per thread
+      const int i = base + u * NT;
+      x[u] = i < i1 ? __ldg(sv + i) : 0.f;
     }
-    __syncthreads();
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      a.add(x[u]);
+      if (x[u] > 0.f) c.add(x[u] * logf(x[u]));
+    }
   }
-  if (threadIdx.x == 0) part[head * n_chunks + chunk] = make_double2(ra[0], rc[0]);
+  double ra = a.value(), rc = c.value();
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    ra += __shfl_xor_sync(0xFFFFFFFFu, ra, o);
+    rc += __shfl_xor_sync(0xFFFFFFFFu, rc, o);
+  }
+  __shared__ double wa[NT / 32], wc[NT / 32];
+  const int warp = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    wa[warp] = ra;
+    wc[warp] = rc;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double sa = 0.0, sc = 0.0;
+    for (int w = 0; w < NT / 32; ++w) {
+      sa += wa[w];
+      sc += wc[w];
+    }
+    part[head * n_chunks + chunk] = make_double2(sa, sc);
+  }
 }
 
 // One block per batch row: sel_h per head in double (fixed chunk order), the row
