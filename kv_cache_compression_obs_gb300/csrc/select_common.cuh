@@ -45,6 +45,8 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_sums, int *
 }  // namespace kvc
 
 #include <cooperative_groups.h>
+#include <cstddef>
+#include <type_traits>
 
 namespace kvc {
 
@@ -67,19 +69,39 @@ struct RadixScratch {
 // are spread over the cluster's CTAs, each histogramming its own and summing
 // all of them through distributed shared memory, so every CTA takes the same
 // decisions and runs the same passes.  Every thread of every CTA must call.
-template <int NT, bool CLUSTER, typename Visit>
-__device__ uint64_t radix_select_ge(RadixScratch<NT> &sm, int need, Visit visit) {
+//
+// visit_hi (optional): visit_hi(f) calls f(key >> 32) for every candidate; the
+// four passes over the high word then use 32-bit keys.  pass0_filled: the caller
+// has already histogrammed the top byte (key >> 56) into sm.hist (per warp).
+template <int NT, bool CLUSTER, typename Visit, typename VisitHi = std::nullptr_t>
+__device__ uint64_t radix_select_ge(RadixScratch<NT> &sm, int need, Visit visit,
+                                    VisitHi visit_hi = nullptr, bool pass0_filled = false) {
   constexpr int NW = NT / 32;
+  constexpr bool HI32 = !std::is_same<VisitHi, std::nullptr_t>::value;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint64_t prefix = 0, hmask = 0;
   for (int pass = 0; pass < 8; ++pass) {
     const int shift = 56 - 8 * pass;
     const int buf = pass & 1;
-    for (int e = threadIdx.x; e < NW * 256; e += NT) (&sm.hist[0][0])[e] = 0u;
-    __syncthreads();
-    visit([&](uint64_t key) {
-      if ((key & hmask) == prefix) atomicAdd(&sm.hist[warp][(uint32_t)(key >> shift) & 255u], 1u);
-    });
+    if (!(pass == 0 && pass0_filled)) {
+      for (int e = threadIdx.x; e < NW * 256; e += NT) (&sm.hist[0][0])[e] = 0u;
+      __syncthreads();
+      bool done_hi = false;
+      if constexpr (HI32) {
+        if (shift >= 32) {
+          const uint32_t p32 = (uint32_t)(prefix >> 32), m32 = (uint32_t)(hmask >> 32);
+          const int sh = shift - 32;
+          visit_hi([&](uint32_t k) {
+            if ((k & m32) == p32) atomicAdd(&sm.hist[warp][(k >> sh) & 255u], 1u);
+          });
+          done_hi = true;
+        }
+      }
+      if (!done_hi)
+        visit([&](uint64_t key) {
+          if ((key & hmask) == prefix) atomicAdd(&sm.hist[warp][(uint32_t)(key >> shift) & 255u], 1u);
+        });
+    }
     __syncthreads();
     for (int d = threadIdx.x; d < 256; d += NT) {
       uint32_t t = 0;

@@ -157,6 +157,9 @@ __global__ __launch_bounds__(NTC) void select_topk_resident_kernel(
   int32_t *out = idx_out + head * (long)k;
   const int lo = min(n, rank * len), hi = min(n, lo + len), m = hi - lo;
 
+  // load the slice as order keys; the first radix pass (top byte) is counted here
+  for (int e = threadIdx.x; e < NWC * 256; e += NTC) (&sm.rx.hist[0][0])[e] = 0u;
+  __syncthreads();
   for (int base = threadIdx.x; base < m; base += 8 * NTC) {
     float v[8];
 #pragma unroll
@@ -167,20 +170,36 @@ __global__ __launch_bounds__(NTC) void select_topk_resident_kernel(
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int i = base + u * NTC;
-      if (i < m) keys[i] = order_key(v[u]);
+      if (i < m) {
+        const uint32_t kk = order_key(v[u]);
+        keys[i] = kk;
+        atomicAdd(&sm.rx.hist[warp][kk >> 24], 1u);
+      }
     }
   }
   cl.sync();  // slices loaded, and every CTA of the cluster is running
 
-  const uint64_t thr = radix_select_ge<NTC, true>(sm.rx, nh, [&](auto &&f) {
-    for (int i = threadIdx.x; i < m; i += NTC) f(pair_key_u(keys[i], (uint32_t)(lo + i)));
-  });
+  const uint64_t thr = radix_select_ge<NTC, true>(
+      sm.rx, nh,
+      [&](auto &&f) {
+        for (int i = threadIdx.x; i < m; i += NTC) f(pair_key_u(keys[i], (uint32_t)(lo + i)));
+      },
+      [&](auto &&f) {
+        for (int i = threadIdx.x; i < m; i += NTC) f(keys[i]);
+      },
+      true);
+  // a threshold with a zero low word is decided by the order keys alone
+  const bool thr32 = (uint32_t)thr == 0u;
+  const uint32_t thr_hi = (uint32_t)(thr >> 32);
+  auto kept = [&](int i) {
+    return thr32 ? keys[i] >= thr_hi : pair_key_u(keys[i], (uint32_t)(lo + i)) >= thr;
+  };
 
   // kept candidates per warp range, per CTA, then the CTA's output offset
   const int per = ((m + NWC - 1) / NWC + 31) & ~31;
   const int wlo = min(m, warp * per), whi = min(m, wlo + per);
   int c = 0;
-  for (int i = wlo + lane; i < whi; i += 32) c += pair_key_u(keys[i], (uint32_t)(lo + i)) >= thr;
+  for (int i = wlo + lane; i < whi; i += 32) c += kept(i);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
   if (lane == 0) sm.wcnt[warp] = c;
@@ -196,7 +215,7 @@ __global__ __launch_bounds__(NTC) void select_topk_resident_kernel(
   for (int w = 0; w < warp; ++w) run += sm.wcnt[w];
   for (int i0 = wlo; i0 < whi; i0 += 32) {
     const int i = i0 + lane;
-    const bool keep = i < whi && pair_key_u(keys[i], (uint32_t)(lo + i)) >= thr;
+    const bool keep = i < whi && kept(i);
     const unsigned msk = __ballot_sync(0xFFFFFFFFu, keep);
     const int slot = run + __popc(msk & ((1u << lane) - 1u));
     if (keep && slot < nh) out[S + slot] = S + lo + i;
