@@ -84,8 +84,10 @@ __device__ uint64_t radix_select_ge(RadixScratch<NT> &sm, int need, Visit visit,
     const int shift = 56 - 8 * pass;
     const int buf = pass & 1;
     if (!(pass == 0 && pass0_filled)) {
-      for (int e = threadIdx.x; e < NW * 256; e += NT) (&sm.hist[0][0])[e] = 0u;
-      __syncthreads();
+      if (pass == 0) {  // later passes find the histograms zeroed by the previous reduction
+        for (int e = threadIdx.x; e < NW * 256; e += NT) (&sm.hist[0][0])[e] = 0u;
+        __syncthreads();
+      }
       bool done_hi = false;
       if constexpr (HI32) {
         if (shift >= 32) {
@@ -106,7 +108,10 @@ __device__ uint64_t radix_select_ge(RadixScratch<NT> &sm, int need, Visit visit,
     for (int d = threadIdx.x; d < 256; d += NT) {
       uint32_t t = 0;
 #pragma unroll 8
-      for (int w = 0; w < NW; ++w) t += sm.hist[w][d];
+      for (int w = 0; w < NW; ++w) {
+        t += sm.hist[w][d];
+        sm.hist[w][d] = 0u;  // ready for the next pass (barriers follow before its visit)
+      }
       sm.tot[buf][d] = t;
     }
     if constexpr (CLUSTER) {

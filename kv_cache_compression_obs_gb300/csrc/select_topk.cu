@@ -185,7 +185,16 @@ __global__ __launch_bounds__(NTC) void select_topk_resident_kernel(
         for (int i = threadIdx.x; i < m; i += NTC) f(pair_key_u(keys[i], (uint32_t)(lo + i)));
       },
       [&](auto &&f) {
-        for (int i = threadIdx.x; i < m; i += NTC) f(keys[i]);
+        const int m4 = m >> 2;  // four keys per 16-byte load
+        const uint4 *k4 = reinterpret_cast<const uint4 *>(keys);
+        for (int i = threadIdx.x; i < m4; i += NTC) {
+          const uint4 q = k4[i];
+          f(q.x);
+          f(q.y);
+          f(q.z);
+          f(q.w);
+        }
+        for (int i = 4 * m4 + threadIdx.x; i < m; i += NTC) f(keys[i]);
       },
       true);
   // a threshold with a zero low word is decided by the order keys alone
