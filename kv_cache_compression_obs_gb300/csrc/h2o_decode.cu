@@ -34,8 +34,9 @@
 //               arrival counter (zeroed by the stream kernel); the last to
 //               arrive picks the smallest (and the new token itself when
 //               recent == 0) and appends the new token or writes it over the
-//               victim.  No CTA waits for another.  A CTA's slot loads are issued before the partials are
-//               combined.
+//               victim.  No CTA waits for another.  Every load that does not
+//               depend on the unit's length (its partials, the CTA's slots,
+//               shared out by capacity) is issued before the length arrives.
 //
 // Workspace: logits [units][G][cap+1] and the per-(unit, CTA) partials (m, Z)
 // [units][PM][G] and o [units][PM][G][D], all float.
@@ -61,7 +62,7 @@ constexpr long long kDrainBudget = 200000000LL;  // ~0.1 s for copies in flight 
 constexpr int BAR_CONS = 1;  // named barrier of the consumer warps
 constexpr int NTF = 128;     // finalize threads per CTA: small enough (with its registers) to
                              // share an SM with a stream CTA of the other half of the rows
-constexpr int CE = 8;        // finalize CTAs per unit
+constexpr int CE = 4;        // finalize CTAs per unit
 constexpr int RU = 8;        // finalize slots per thread in flight
 
 __device__ __forceinline__ bool better(float a, int p, float ba, int bp) {
@@ -609,34 +610,48 @@ __global__ __launch_bounds__(NTF) void decode_finalize_kernel(
   const long b = unit / Hkv;
   const int h = static_cast<int>(unit % Hkv);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int n = len[unit];
-  if (n < 0 || n > cap) {  // same n in all the unit's CTAs: every one leaves here
-    if (rank == 0 && threadIdx.x == 0 && dev_status) atomicExch(dev_status, (int)KV_ERR_INVALID_ARG);
-    return;
-  }
   const int NB = blocks_per_unit(cap, DGeo<T, D, G>::RB);
   const int PM = partials_per_unit(cap);
   const Span sp = unit_span(unit, NB, per);
-  const int nc = n + (alg1 ? 0 : 1);
   const float2 *pmz = ws.pmz + unit * PM * G;
   const float *po = ws.po + unit * PM * (long)GD;
   const float *lgu = ws.lgw + unit * (long)G * (cap + 1);
   float *au = acc + unit * (long)cap;
   int32_t *pu = pos + unit * (long)cap;
 
-  // this CTA's slots: their loads are issued before the partials are combined
-  const int per_cta = (nc + CE - 1) / CE;
-  const int j0 = min(nc, rank * per_cta), j1 = min(nc, j0 + per_cta);
+  // Every load that does not depend on the unit's length is issued before it is
+  // known, so that a CTA waits for about one memory round trip, not three: the
+  // length, the partials (m, Z) and this thread's output shares, and this CTA's
+  // slots.  Slots are shared out by capacity (cap + 1 attended rows at most);
+  // rows past the length are loaded (in bounds) and ignored.
+  const int n_raw = len[unit];
+  constexpr int PR = 4;  // partials held in registers; a longer span reads the rest in a loop
+  const int t_out = rank * (GD / CE) + static_cast<int>(threadIdx.x);  // this thread's output
+  const bool has_out = threadIdx.x < GD / CE;
+  const int g_out = t_out / D;
+  float2 mzr[PR];
+  float2 mzo[PR];
+  float por[PR];
+#pragma unroll
+  for (int p = 0; p < PR; ++p) {
+    const bool pin = p < sp.count;
+    mzr[p] = (pin && threadIdx.x < G) ? pmz[p * G + threadIdx.x] : make_float2(-INFINITY, 0.f);
+    mzo[p] = (pin && has_out) ? pmz[p * G + g_out] : make_float2(-INFINITY, 0.f);
+    por[p] = (pin && has_out) ? po[(long)p * GD + t_out] : 0.f;
+  }
+  const int ncap = cap + 1;
+  const int per_cta = (ncap + CE - 1) / CE;
+  const int j0 = min(ncap, rank * per_cta), j1c = min(ncap, j0 + per_cta);
   float lv[RU][G], av[RU];
   int pv[RU];
   auto load_slots = [&](int jb) {
 #pragma unroll
     for (int k = 0; k < RU; ++k) {
       const int j = jb + k * NTF;
-      if (j < j1) {
+      if (j < j1c) {
 #pragma unroll
         for (int g = 0; g < G; ++g) lv[k][g] = lgu[(long)g * (cap + 1) + j];
-        if (j < n) {
+        if (j < cap) {
           av[k] = au[j];
           pv[k] = pu[j];
         }
@@ -645,18 +660,29 @@ __global__ __launch_bounds__(NTF) void decode_finalize_kernel(
   };
   const int jstart = j0 + threadIdx.x;
   load_slots(jstart);
+
+  const int n = n_raw;
+  if (n < 0 || n > cap) {  // same n in all the unit's CTAs: every one leaves here
+    if (rank == 0 && threadIdx.x == 0 && dev_status) atomicExch(dev_status, (int)KV_ERR_INVALID_ARG);
+    return;
+  }
+  const int nc = n + (alg1 ? 0 : 1);
+  const int j1 = min(nc, j1c);
   // the unit's max and normaliser per head over the partials (a partial of an
   // empty range has m = -inf and Z = 0 and adds nothing)
   if (threadIdx.x < G) {
     const int g = threadIdx.x;
     float M = -INFINITY, Z = 0.f;
-    for (int p = 0; p < sp.count; ++p) {
-      const float2 v = pmz[p * G + g];
-      if (v.x == -INFINITY) continue;
+    auto add = [&](float2 v) {
+      if (v.x == -INFINITY) return;
       const float Mn = fmaxf(M, v.x);
       Z = Z * tc::ex2(M - Mn) + v.y * tc::ex2(v.x - Mn);
       M = Mn;
-    }
+    };
+#pragma unroll
+    for (int p = 0; p < PR; ++p)
+      if (p < sp.count) add(mzr[p]);
+    for (int p = PR; p < sp.count; ++p) add(pmz[p * G + g]);
     gm[g] = M;
     gz[g] = Z;
     gc[g] = M + log2f(Z);  // 2^(l - M) / Z = 2^(l - gc)
@@ -664,12 +690,19 @@ __global__ __launch_bounds__(NTF) void decode_finalize_kernel(
   __syncthreads();
   // this CTA's part of the output: o_g = sum_p o_p exp(m_p - M) / Z
   float *ou = o_out + (b * Hq + (long)h * G) * D;
-  for (int t = rank * (GD / CE) + threadIdx.x; t < (rank + 1) * (GD / CE); t += NTF) {
+  // (the thread's first output has its shares in registers; o_p = 0 where m_p = -inf)
+  for (int t = t_out, it = 0; t < (rank + 1) * (GD / CE); t += NTF, ++it) {
     const int g = t / D;
     float s = 0.f;
-#pragma unroll 4
-    for (int p = 0; p < sp.count; ++p) {
-      const float mp = pmz[p * G + g].x;  // o_p = 0 where m_p = -inf
+    int p = 0;
+    if (it == 0) {
+#pragma unroll
+      for (int q = 0; q < PR; ++q)
+        if (q < sp.count) s += por[q] * (mzo[q].x == -INFINITY ? 0.f : tc::ex2(mzo[q].x - gm[g]));
+      p = PR;
+    }
+    for (; p < sp.count; ++p) {
+      const float mp = pmz[p * G + g].x;
       s += po[(long)p * GD + t] * (mp == -INFINITY ? 0.f : tc::ex2(mp - gm[g]));
     }
     ou[t] = nc > 0 ? s / gz[g] : 0.f;
