@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--layers", type=int, default=None,
                     help="override the workload's layer count (smaller profiling cases)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--eager", action="store_true",
+                    help="enqueue every launch from the host in the timed region (no CUDA graphs)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-groups", type=int, default=None,
@@ -221,8 +223,41 @@ class Pipeline:
                                       evicted_out=self.EV, workspace=self.dws, stream=stream)
 
     def step(self, stream=None):
+        if self.graphs is not None:
+            self.graphs[0].replay()
+            self.graphs[1].replay()
+            return
         self.prefill(stream)
         self.decode_all(stream)
+
+    graphs = None  # (prefill, decode) CUDA graphs once captured
+    launches_per_step = None
+
+    def capture(self):
+        """The step as two CUDA graphs (the prefill chain, then every decode step),
+        captured once after warm-up and replayed: the 128 x 4 decode launches then
+        cost no host round trip each.  The library's own side stream joins the
+        capture through its fork / join events."""
+        import torch
+        side = torch.cuda.Stream(device=self.dev)
+        side.wait_stream(torch.cuda.current_stream(self.dev))
+        with torch.cuda.stream(side):  # one eager pass on a non-default stream first
+            self.prefill()
+            self.decode_all()
+        torch.cuda.current_stream(self.dev).wait_stream(side)
+        torch.cuda.synchronize(self.dev)
+        gp, gd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        n0 = launch_count()
+        with torch.cuda.graph(gp):
+            self.prefill()
+        n1 = launch_count()
+        with torch.cuda.graph(gd):
+            self.decode_all()
+        n2 = launch_count()
+        torch.cuda.synchronize(self.dev)
+        self.graphs = (gp, gd)
+        self.launches_per_step = n2 - n0
+        self.launches_decode = n2 - n1
 
     def timed_phases(self):
         """One step with events between the phases: ms per phase."""
@@ -241,7 +276,10 @@ class Pipeline:
         a.kv_compact(self.K, self.V, self.s, self.idx, wl.cap, K_out=self.Kc, V_out=self.Vc,
                      pos_out=self.pos, acc_out=self.acc, len_out=self.len)
         ev[4].record()
-        self.decode_all()
+        if self.graphs is not None:
+            self.graphs[1].replay()
+        else:
+            self.decode_all()
         ev[5].record()
         torch.cuda.synchronize()
         names = ["kv_score_obs", "hubkv_refine", "kv_select_topk", "kv_compact", "h2o_decode_step"]
@@ -509,6 +547,11 @@ def run_ours(args, wl, rank, world):
     for _ in range(max(args.warmup, 0)):
         pipe.step()
     torch.cuda.synchronize()
+    if not args.eager:
+        pipe.capture()
+        for _ in range(2):  # the graphs' own first replays, untimed
+            pipe.step()
+        torch.cuda.synchronize()
     phases = pipe.timed_phases()
 
     if world > 1:
@@ -525,6 +568,8 @@ def run_ours(args, wl, rank, world):
     if world > 1:
         dist.barrier()
     launches = launch_count() - launches0
+    if pipe.graphs is not None:  # replays count no launches on the host: the captured ones, per step
+        launches = pipe.launches_per_step * args.steps
     ms = e0.elapsed_time(e1) / args.steps
     ms_max = max_over_ranks(ms, world, dev)
 
