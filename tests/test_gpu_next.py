@@ -150,6 +150,68 @@ def test_multi_step_decode_alg1_and_zero_steps(kvc):
         assert torch.equal(a, b)
 
 
+def test_decode_and_chain_graph_replay_equal_eager(kvc):
+    """The library is safe to capture in a CUDA graph: the prefill chain and a
+    multi-step decode (two row halves, the second on the library's side stream,
+    joined through events) replayed from a graph give, bit for bit, what the
+    same calls enqueued from the host give."""
+    g = torch.Generator(device=DEV)
+    g.manual_seed(2024)
+    B, Hq, Hkv, T, d, W, k, R, n = 4, 8, 2, 2048, 128, 32, 256, 32, 12
+    cap = k + 8
+    Q = torch.randn(B, Hq, W, d, generator=g, device=DEV).to(torch.bfloat16)
+    K = torch.randn(B, Hkv, T, d, generator=g, device=DEV).to(torch.bfloat16)
+    V = torch.randn(B, Hkv, T, d, generator=g, device=DEV).to(torch.bfloat16)
+    q = torch.randn(n, B, Hq, d, generator=g, device=DEV).to(torch.bfloat16)
+    kn = torch.randn(n, B, Hkv, d, generator=g, device=DEV).to(torch.bfloat16)
+    vn = torch.randn(n, B, Hkv, d, generator=g, device=DEV).to(torch.bfloat16)
+
+    def buffers():
+        f32, i32 = torch.float32, torch.int32
+        return dict(s=torch.empty(B, Hkv, T, dtype=f32, device=DEV),
+                    z=torch.empty(B, Hkv, T, dtype=f32, device=DEV),
+                    idx=torch.empty(B, Hkv, k, dtype=i32, device=DEV),
+                    Kc=torch.empty(B, Hkv, cap, d, dtype=K.dtype, device=DEV),
+                    Vc=torch.empty(B, Hkv, cap, d, dtype=K.dtype, device=DEV),
+                    pos=torch.empty(B, Hkv, cap, dtype=i32, device=DEV),
+                    acc=torch.empty(B, Hkv, cap, dtype=f32, device=DEV),
+                    ln=torch.empty(B, Hkv, dtype=i32, device=DEV),
+                    o=torch.empty(n, B, Hq, d, dtype=f32, device=DEV),
+                    ev=torch.empty(n, B, Hkv, dtype=i32, device=DEV),
+                    ws=torch.empty(max(kvc.kv_workspace_size(kvc.KV_OP_SCORE_OBS, B, Hq, Hkv, T, d, W),
+                                       kvc.kv_workspace_size(kvc.KV_OP_HUBKV_REFINE, B, Hkv, Hkv, T)),
+                                   dtype=torch.uint8, device=DEV),
+                    dws=torch.empty(kvc.kv_workspace_size(kvc.KV_OP_DECODE, B, Hq, Hkv, cap, d),
+                                    dtype=torch.uint8, device=DEV))
+
+    def run(b):
+        kvc.kv_score_obs(Q, K, out=b["s"], workspace=b["ws"])
+        kvc.hubkv_refine(b["s"], 0.1, out=b["z"], workspace=b["ws"])
+        kvc.kv_select_topk(b["z"], k, R, out=b["idx"])
+        kvc.kv_compact(K, V, b["s"], b["idx"], cap, K_out=b["Kc"], V_out=b["Vc"], pos_out=b["pos"],
+                       acc_out=b["acc"], len_out=b["ln"])
+        kvc.h2o_decode_steps(q, kn, vn, b["Kc"], b["Vc"], b["pos"], b["acc"], b["ln"], R, T,
+                             o_out=b["o"], evicted_out=b["ev"], workspace=b["dws"])
+
+    eager, graphed = buffers(), buffers()
+    run(eager)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        run(graphed)  # warm-up on a non-default stream, then capture and replay once
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    for t in graphed.values():
+        t.zero_()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        run(graphed)
+    graph.replay()
+    torch.cuda.synchronize()
+    for name in ("s", "z", "idx", "Kc", "Vc", "pos", "acc", "ln", "o", "ev"):
+        assert torch.equal(eager[name], graphed[name]), name
+
+
 def test_select_topk_many_heads(kvc, oracle_mod):
     """Thousands of single-CTA heads and a few 2-CTA clusters in one launch."""
     g = torch.Generator(device=DEV)
