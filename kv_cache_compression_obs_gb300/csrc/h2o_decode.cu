@@ -213,7 +213,7 @@ __device__ __forceinline__ float row_butterfly(float (&v)[HG], int pp) {
 }
 
 template <typename T, int D, int G>
-__global__ __launch_bounds__(32 * (NCW + 1), 1) void decode_stream_kernel(
+__device__ __forceinline__ void decode_stream_body(
     const T *__restrict__ Kc, const T *__restrict__ Vc, const T *__restrict__ q,
     const T *__restrict__ k_new, const T *__restrict__ v_new, const int32_t *__restrict__ len, int Hq,
     int Hkv, int cap, float c_log2, int alg1, long total, long per, Ws ws, int *__restrict__ dev_status) {
@@ -594,6 +594,29 @@ __global__ __launch_bounds__(32 * (NCW + 1), 1) void decode_stream_kernel(
   }
 }
 
+// Two entry points with one body.  Where it costs no spills (G <= 4) a thread
+// gets at most 136 registers, so that a finalize CTA of the other half of the
+// rows fits on the SM beside a stream CTA: the stream CTA's nine warps put
+// three on one SM sub-partition, whose 16K-register file then keeps room for a
+// 96-register finalize warp (at 168 registers it keeps 256, and the finalize
+// CTAs had to wait for the stream CTAs to leave).  G = 8 keeps the full budget.
+#define KVC_STREAM_PARAMS                                                                          \
+  const T *__restrict__ Kc, const T *__restrict__ Vc, const T *__restrict__ q,                     \
+      const T *__restrict__ k_new, const T *__restrict__ v_new, const int32_t *__restrict__ len,   \
+      int Hq, int Hkv, int cap, float c_log2, int alg1, long total, long per, Ws ws,               \
+      int *__restrict__ dev_status
+#define KVC_STREAM_ARGS Kc, Vc, q, k_new, v_new, len, Hq, Hkv, cap, c_log2, alg1, total, per, ws, dev_status
+template <typename T, int D, int G>
+__global__ __maxnreg__(136) void decode_stream_kernel(KVC_STREAM_PARAMS) {
+  decode_stream_body<T, D, G>(KVC_STREAM_ARGS);
+}
+template <typename T, int D, int G>
+__global__ __launch_bounds__(32 * (NCW + 1), 1) void decode_stream_kernel_wide(KVC_STREAM_PARAMS) {
+  decode_stream_body<T, D, G>(KVC_STREAM_ARGS);
+}
+#undef KVC_STREAM_PARAMS
+#undef KVC_STREAM_ARGS
+
 template <typename T, int D, int G>
 __global__ __launch_bounds__(NTF) void decode_finalize_kernel(
     const T *__restrict__ k_new, const T *__restrict__ v_new, T *__restrict__ Kc, T *__restrict__ Vc,
@@ -826,14 +849,21 @@ int run_decode(const void *q, const void *k_new, const void *v_new, void *K_cach
   const long units = (long)B * Hkv;
   const Ws ws = carve(workspace, units, G, cap, D);
   const int alg1 = (flags & KV_H2O_ALG1) ? 1 : 0;
-  if (ensure_smem((const void *)decode_stream_kernel<T, D, G>, Geo::SMEM))
+  auto stream_kernel = [] {
+    if constexpr (G <= 4) {
+      return decode_stream_kernel<T, D, G>;
+    } else {
+      return decode_stream_kernel_wide<T, D, G>;
+    }
+  }();
+  if (ensure_smem((const void *)stream_kernel, Geo::SMEM))
     return cuda_failure(cudaErrorInvalidValue, "decode stream kernel: shared memory limit");
   const int NB = blocks_per_unit(cap, Geo::RB);
   const long total = units * NB;
   const long grid = std::max(1L, std::min((long)device_sm_count(), total / PER_MIN));
   const long per = (total + grid - 1) / grid;
   const long ctas = (total + per - 1) / per;
-  decode_stream_kernel<T, D, G><<<(unsigned)ctas, 32 * (NCW + 1), Geo::SMEM, st>>>(
+  stream_kernel<<<(unsigned)ctas, 32 * (NCW + 1), Geo::SMEM, st>>>(
       static_cast<const T *>(K_cache), static_cast<const T *>(V_cache), static_cast<const T *>(q),
       static_cast<const T *>(k_new), static_cast<const T *>(v_new), len, Hq, Hkv, cap,
       scale * 1.4426950408889634f /* log2 e */, alg1, total, per, ws, dev_status);
