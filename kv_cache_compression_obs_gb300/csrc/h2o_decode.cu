@@ -594,12 +594,13 @@ __device__ __forceinline__ void decode_stream_body(
   }
 }
 
-// Two entry points with one body.  Where it costs no spills (G <= 4) a thread
-// gets at most 136 registers, so that a finalize CTA of the other half of the
-// rows fits on the SM beside a stream CTA: the stream CTA's nine warps put
-// three on one SM sub-partition, whose 16K-register file then keeps room for a
-// 96-register finalize warp (at 168 registers it keeps 256, and the finalize
-// CTAs had to wait for the stream CTAs to leave).  G = 8 keeps the full budget.
+// Two entry points with one body.  For G <= 4 a stream thread gets at most 144
+// registers and a finalize thread at most 80, so that a finalize CTA of the
+// other half of the rows fits on the SM beside a stream CTA: the stream CTA's
+// nine warps put three on one SM sub-partition, and 3 x 144 + 80 registers a
+// lane fill that sub-partition's 16K-register file exactly (at 168 the stream
+// warps leave 256 registers, and the finalize CTAs had to wait for the stream
+// CTAs to leave).  G = 8 keeps the full budget in both kernels.
 #define KVC_STREAM_PARAMS                                                                          \
   const T *__restrict__ Kc, const T *__restrict__ Vc, const T *__restrict__ q,                     \
       const T *__restrict__ k_new, const T *__restrict__ v_new, const int32_t *__restrict__ len,   \
@@ -607,7 +608,7 @@ __device__ __forceinline__ void decode_stream_body(
       int *__restrict__ dev_status
 #define KVC_STREAM_ARGS Kc, Vc, q, k_new, v_new, len, Hq, Hkv, cap, c_log2, alg1, total, per, ws, dev_status
 template <typename T, int D, int G>
-__global__ __maxnreg__(136) void decode_stream_kernel(KVC_STREAM_PARAMS) {
+__global__ __maxnreg__(144) void decode_stream_kernel(KVC_STREAM_PARAMS) {
   decode_stream_body<T, D, G>(KVC_STREAM_ARGS);
 }
 template <typename T, int D, int G>
@@ -618,7 +619,7 @@ __global__ __launch_bounds__(32 * (NCW + 1), 1) void decode_stream_kernel_wide(K
 #undef KVC_STREAM_ARGS
 
 template <typename T, int D, int G>
-__global__ __launch_bounds__(NTF) void decode_finalize_kernel(
+__device__ __forceinline__ void decode_finalize_body(
     const T *__restrict__ k_new, const T *__restrict__ v_new, T *__restrict__ Kc, T *__restrict__ Vc,
     int32_t *__restrict__ pos, float *__restrict__ acc, int32_t *__restrict__ len, int Hq, int Hkv,
     int cap, int recent, int sink, int new_pos, int alg1, long per, Ws ws, float *__restrict__ o_out,
@@ -840,6 +841,26 @@ __global__ __launch_bounds__(NTF) void decode_finalize_kernel(
   }
 }
 
+#define KVC_FIN_PARAMS                                                                             \
+  const T *__restrict__ k_new, const T *__restrict__ v_new, T *__restrict__ Kc,                    \
+      T *__restrict__ Vc, int32_t *__restrict__ pos, float *__restrict__ acc,                      \
+      int32_t *__restrict__ len, int Hq, int Hkv, int cap, int recent, int sink, int new_pos,      \
+      int alg1, long per, Ws ws, float *__restrict__ o_out, int32_t *__restrict__ evicted,         \
+      int *__restrict__ dev_status
+#define KVC_FIN_ARGS                                                                               \
+  k_new, v_new, Kc, Vc, pos, acc, len, Hq, Hkv, cap, recent, sink, new_pos, alg1, per, ws, o_out,   \
+      evicted, dev_status
+template <typename T, int D, int G>
+__global__ __maxnreg__(80) void decode_finalize_kernel(KVC_FIN_PARAMS) {
+  decode_finalize_body<T, D, G>(KVC_FIN_ARGS);
+}
+template <typename T, int D, int G>
+__global__ __launch_bounds__(NTF) void decode_finalize_kernel_wide(KVC_FIN_PARAMS) {
+  decode_finalize_body<T, D, G>(KVC_FIN_ARGS);
+}
+#undef KVC_FIN_PARAMS
+#undef KVC_FIN_ARGS
+
 template <typename T, int D, int G>
 int run_decode(const void *q, const void *k_new, const void *v_new, void *K_cache, void *V_cache,
                int32_t *pos, float *acc, int32_t *len, int B, int Hq, int Hkv, int cap,
@@ -854,6 +875,13 @@ int run_decode(const void *q, const void *k_new, const void *v_new, void *K_cach
       return decode_stream_kernel<T, D, G>;
     } else {
       return decode_stream_kernel_wide<T, D, G>;
+    }
+  }();
+  auto finalize_kernel = [] {
+    if constexpr (G <= 4) {
+      return decode_finalize_kernel<T, D, G>;
+    } else {
+      return decode_finalize_kernel_wide<T, D, G>;
     }
   }();
   if (ensure_smem((const void *)stream_kernel, Geo::SMEM))
@@ -871,7 +899,7 @@ int run_decode(const void *q, const void *k_new, const void *v_new, void *K_cach
     const int rc = launch_status(0);  // the stream kernel's launch
     if (rc != KV_OK) return rc;
   }
-  decode_finalize_kernel<T, D, G><<<(unsigned)(units * CE), NTF, 0, st>>>(
+  finalize_kernel<<<(unsigned)(units * CE), NTF, 0, st>>>(
       static_cast<const T *>(k_new), static_cast<const T *>(v_new), static_cast<T *>(K_cache),
       static_cast<T *>(V_cache), pos, acc, len, Hq, Hkv, cap, recent, sink, new_pos, alg1, per, ws, o, evicted,
       dev_status);
