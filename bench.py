@@ -97,7 +97,7 @@ def score_flops(wl):
 # of the current kernels, per workload; see profiles/decode_long-context.md
 # (captured on 8 of the 32 layers, mean over four halves, scaled by 4: the step's
 # traffic is proportional to the units).  None where not captured.
-DECODE_TRAFFIC = {"long-context": 4 * 2 * (107468288 + 1081600 + 5464320 + 1536)}
+DECODE_TRAFFIC = {"long-context": 4 * 2 * (107470016 + 897536 + 5472576)}
 
 
 def measured_peaks():
