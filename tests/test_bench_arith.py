@@ -1,0 +1,53 @@
+"""The benchmark's roofline arithmetic on CPU: the algorithmic bytes and flops
+`bench.py` divides by its event times, checked against the per-unit figures
+worked out by hand for the long-context workload (32 layers x 8 KV heads,
+G = 4 query heads per KV head, W = 64, d = 128, T = 131072, k = cap = 6553, bf16)."""
+import bench
+from kv_cache_compression_obs_gb300 import configs
+
+WL = configs.LONG_CONTEXT
+UNITS = 32 * 8          # (layer, KV head) pairs of the one batch row
+G, W, D, T, K = 4, 64, 128, 131072, 6553
+ROW = D * 2             # one bf16 K or V row
+
+
+def test_workload_shape():
+    assert (WL.units, WL.Hq // WL.Hkv, WL.W, WL.d, WL.T, WL.k, WL.cap, WL.elem_bytes) == \
+        (UNITS, G, W, D, T, K, K, 2)
+
+
+def test_prefill_bytes_per_unit():
+    a = bench.algorithmic_bytes(WL)
+    # scoring: the unit's G x W query rows and its T keys read once, the scores written
+    assert a["kv_score_obs"] == UNITS * (G * W * ROW + T * ROW + 4 * T)
+    # refine: scores read, refined scores written
+    assert a["hubkv_refine"] == UNITS * 8 * T
+    # Top-K: refined scores read, k positions written
+    assert a["kv_select_topk"] == UNITS * (4 * T + 4 * K)
+    # compaction: k K rows and k V rows read and written, and per kept slot its
+    # index, score, position and accumulator
+    assert a["kv_compact"] == UNITS * K * (4 * ROW + 16)
+    assert sum(a[n] for n in ("kv_score_obs", "hubkv_refine", "kv_select_topk", "kv_compact")) \
+        == 10_894_963_712
+
+
+def test_decode_bytes_per_step():
+    a = bench.algorithmic_bytes(WL)
+    # every slot's K and V row, accumulator (read + write) and position; per unit
+    # the G query rows (bf16 in, fp32 out) and the new token's K and V rows
+    assert a["h2o_decode_step"] == UNITS * (K * (2 * ROW + 12) + G * D * 6 + 2 * ROW)
+    assert a["h2o_decode_step"] == 879_963_136
+    # the measured DRAM traffic the bench reports beside it is that, plus a few percent
+    traffic = bench.DECODE_TRAFFIC["long-context"]
+    assert 1.0 <= traffic / a["h2o_decode_step"] <= 1.1
+
+
+def test_score_flops_two_passes():
+    # statistics pass and column-mass pass: 2 x (2 G W T d) flops per unit
+    assert bench.score_flops(WL) == 2 * 2 * G * W * T * D * UNITS == 4_398_046_511_104
+
+
+def test_whole_job_rate_counts_every_rank():
+    # value = KV tokens (rows x T) of all ranks over the slowest rank's step time
+    assert bench.whole_job_rate(WL.rows * WL.T, 1, 0.02338) == WL.rows * WL.T / 0.02338
+    assert bench.whole_job_rate(100, 4, 2.0) == 200.0
