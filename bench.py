@@ -86,18 +86,46 @@ def algorithmic_bytes(wl):
             "kv_compact": compact, "h2o_decode_step": decode_step}
 
 
+def score_pairs(wl):
+    """(query row, key) pairs the observation window sees per (batch row, KV head):
+    each of the G query heads' W rows at prompt position p = T - W + w sees the
+    keys 0..p (causal), G * (W (T - W) + W (W + 1) / 2) in all."""
+    G = wl.Hq // wl.Hkv
+    return G * (wl.W * (wl.T - wl.W) + wl.W * (wl.W + 1) // 2)
+
+
 def score_flops(wl):
-    """Dense multiply-adds of the observation-window contraction, both passes
-    (statistics, then column mass): 2 x 2 x (G W) x T x d per (batch row, KV head)."""
-    return 2 * 2 * (wl.Hq // wl.Hkv) * wl.W * wl.T * wl.d * wl.units
+    """Algorithmic flops of the observation-window contraction: one Q K^T over the
+    visible (row, key) pairs, 2 d per pair (multiply + add), for every unit.  The
+    exact column mass needs every row's softmax normaliser first, so the kernels
+    form each logit twice; that recompute is reported as executed work, not
+    counted here."""
+    return 2 * wl.d * score_pairs(wl) * wl.units
+
+
+def score_flops_executed(wl):
+    """Flops the two-pass kernels issue: both passes over every visible pair."""
+    return 2 * score_flops(wl)
 
 
 # DRAM bytes per decode step (all its launches: the two row halves' stream and
-# finalize kernels) from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum`
-# of the current kernels, per workload; see profiles/decode_long-context.md
-# (captured on 8 of the 32 layers, mean over four halves, scaled by 4: the step's
-# traffic is proportional to the units).  None where not captured.
+# finalize kernels) from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum`,
+# captured on 8 of the 32 layers of the long-context workload (mean over four
+# halves, scaled by 4: the step's traffic is proportional to the units), with the
+# SHA-256 of the decode kernel source it was taken on.  When the source has
+# changed since, the figure no longer describes the kernel and is reported as null.
 DECODE_TRAFFIC = {"long-context": 4 * 2 * (107470016 + 897536 + 5472576)}
+DECODE_TRAFFIC_SOURCE = "kv_cache_compression_obs_gb300/csrc/h2o_decode.cu"
+DECODE_TRAFFIC_SOURCE_SHA256 = "20c1313e366e778898cf19320ffdbee6ee33b6b3d030d9bb99bdd90496642201"
+
+
+def _source_sha256(rel):
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            return hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
 
 
 def measured_peaks():
@@ -403,7 +431,8 @@ def run_e2e(wl, pipe, steps, n_groups):
     device one layer row at a time on a copy stream (the compaction gathers the
     kept V rows straight from host memory), then the group's decode steps run as
     one h2o_decode_steps call while the next group's keys stream.  The kept
-    positions, every step's evictions and the last step's outputs are copied back."""
+    positions and every decode step's evictions and attention outputs are copied
+    back."""
     import torch
     a = pipe.api
     groups = [(g * wl.rows // n_groups, (g + 1) * wl.rows // n_groups) for g in range(n_groups)]
@@ -420,7 +449,7 @@ def run_e2e(wl, pipe, steps, n_groups):
     dE = [torch.empty(wl.n_decode, r1 - r0, wl.Hkv, dtype=torch.int32, device=pipe.dev)
           for r0, r1 in groups]
     out_idx = torch.empty(pipe.idx.shape, dtype=torch.int32).pin_memory()
-    out_o = torch.empty(pipe.o.shape, dtype=torch.float32).pin_memory()
+    out_o = [torch.empty(o.shape, dtype=torch.float32).pin_memory() for o in dO]  # every step's
     out_ev = [torch.empty(e.shape, dtype=torch.int32).pin_memory() for e in dE]
     bufs = {"Q": pipe.Q, "K": pipe.K, "s": pipe.s, "z": pipe.z, "beta": pipe.beta, "idx": pipe.idx,
             "Kc": pipe.Kc, "Vc": pipe.Vc, "pos": pipe.pos, "acc": pipe.acc, "len": pipe.len,
@@ -429,7 +458,7 @@ def run_e2e(wl, pipe, steps, n_groups):
     h2d = (hQ.numel() * hQ.element_size() + hK.numel() * hK.element_size()
            + wl.units * wl.k * row  # the kept V rows, gathered from host memory
            + sum(h.numel() * h.element_size() for hg in hD for h in hg))
-    d2h = out_idx.numel() * 4 + out_o.numel() * 4 + sum(e.numel() * 4 for e in out_ev)
+    d2h = out_idx.numel() * 4 + sum(o.numel() * 4 for o in out_o) + sum(e.numel() * 4 for e in out_ev)
 
     def one():
         for dg, hg in zip(dD, hD):  # decode inputs first: small
@@ -446,7 +475,7 @@ def run_e2e(wl, pipe, steps, n_groups):
                                    pipe.len[sl], wl.R, wl.T, wl.scale, o_out=dO[gi],
                                    evicted_out=dE[gi], workspace=pipe.dws)
                 out_ev[gi].copy_(dE[gi], non_blocking=True)
-                out_o[r0:r1].copy_(dO[gi][-1], non_blocking=True)
+                out_o[gi].copy_(dO[gi], non_blocking=True)
 
     one()
     torch.cuda.synchronize()
@@ -582,8 +611,17 @@ def run_ours(args, wl, rank, world):
     per_launch = {k: alg[k] for k in alg}
     dom = max(phases, key=lambda n: phases[n] * (wl.n_decode if n == "h2o_decode_step" else 1))
     achieved = per_launch[dom] / (phases[dom] / 1e3) / 1e9
-    traffic = DECODE_TRAFFIC.get(wl.name) if dom == "h2o_decode_step" else None
-    score_tf = score_flops(wl) / (phases["kv_score_obs"] / 1e3) / 1e12
+    traffic, traffic_source = None, None
+    if dom == "h2o_decode_step" and wl.name in DECODE_TRAFFIC:
+        if _source_sha256(DECODE_TRAFFIC_SOURCE) == DECODE_TRAFFIC_SOURCE_SHA256:
+            traffic = DECODE_TRAFFIC[wl.name]
+            traffic_source = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of the decode "
+                              "launches, taken on this decode source (sha256 "
+                              f"{DECODE_TRAFFIC_SOURCE_SHA256[:12]})")
+        else:
+            traffic_source = "stale: the decode source changed since the ncu capture"
+    score_s = phases["kv_score_obs"] / 1e3
+    score_tf = score_flops(wl) / score_s / 1e12
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
@@ -606,13 +644,19 @@ def run_ours(args, wl, rank, world):
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "algorithmic_bytes": per_launch[dom], "traffic": traffic,
+                     "traffic_source": traffic_source,
                      "note": ("one decode step = its stream and finalize launches (two row halves on two streams), timed together"
                               if dom == "h2o_decode_step" else None)},
         "roofline_score": {"kernel": "kv_score_obs", "bound": "tensor", "achieved": score_tf,
                            "peak": peak_tf, "peak_kind": peak_kind + " bf16 dense (burst)",
                            "unit": "TFLOP/s", "frac": score_tf / peak_tf,
                            "algorithmic_flops": score_flops(wl),
-                           "hbm_gbs": per_launch["kv_score_obs"] / (phases["kv_score_obs"] / 1e3) / 1e9},
+                           "executed_flops": score_flops_executed(wl),
+                           "executed_frac": score_flops_executed(wl) / score_s / 1e12 / peak_tf,
+                           "hbm_gbs": per_launch["kv_score_obs"] / score_s / 1e9,
+                           "hbm_frac": per_launch["kv_score_obs"] / score_s / 1e9 / peak,
+                           "note": "algorithmic = one Q K^T over the causally visible pairs; "
+                                   "executed = both passes (statistics, column mass)"},
         "clocks": clk.summary(),
     }
     if not args.no_next_rows:

@@ -392,6 +392,9 @@ KVC_API int h2o_decode_steps(const void *q, const void *k_new, const void *v_new
  *     results, so serialise them.  The array keeps the last call's contents.
  *   - The first call on each device looks the array's device address up, with
  *     that device current; make that first call before any stream capture.
+ *     The address is kept for the life of the process: it is not valid after
+ *     cudaDeviceReset (or any other teardown of the device's primary context),
+ *     so do not call this entry point again after one.
  */
 #define KV_SCORE_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 KVC_API int kv_score_obs_noalloc(const void *Q_obs, const void *K, int B, int Hq, int Hkv, int T,

@@ -105,18 +105,33 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"expected bfloat16 or float32, got {t.dtype}")
 
 
+def _on_current_device(t):
+    """The library launches on the current CUDA device (and takes its scratch and
+    side stream from it), so a tensor on another device would be handed to the
+    wrong GPU."""
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"tensor on {t.device} but the current CUDA device is "
+                         f"cuda:{torch.cuda.current_device()}: call inside "
+                         f"`with torch.cuda.device({t.device})`")
+
+
 def _dev(*ts):
     for t in ts:
-        if t is not None and (not t.is_cuda or not t.is_contiguous()):
-            raise ValueError("tensors must be contiguous CUDA tensors")
+        if t is not None:
+            if not t.is_cuda or not t.is_contiguous():
+                raise ValueError("tensors must be contiguous CUDA tensors")
+            _on_current_device(t)
 
 
 def _dev_or_pinned(*ts):
     """Gather sources may also be pinned host tensors (read by the kernel over the
     host link, only the rows it keeps)."""
     for t in ts:
-        if t is not None and (not t.is_contiguous() or not (t.is_cuda or t.is_pinned())):
-            raise ValueError("tensors must be contiguous CUDA tensors or pinned host tensors")
+        if t is not None:
+            if not t.is_contiguous() or not (t.is_cuda or t.is_pinned()):
+                raise ValueError("tensors must be contiguous CUDA tensors or pinned host tensors")
+            if t.is_cuda:
+                _on_current_device(t)
 
 
 def kv_workspace_size(op: int, B: int, Hq: int, Hkv: int, T: int, d: int = 128, W: int = 1,
@@ -163,6 +178,7 @@ def kv_score_obs_noalloc(Q_obs: torch.Tensor, K: torch.Tensor, scale: float | No
     if scale is None:
         scale = d ** -0.5
     s = out if out is not None else torch.empty(B, Hkv, T, dtype=torch.float32, device=K.device)
+    _dev(dev_status)
     _check("kv_score_obs_noalloc", _lib.kv_score_obs_noalloc(
         _ptr(Q_obs), _ptr(K), B, Hq, Hkv, T, d, W, float(scale), _dtype_code(K), _ptr(s),
         _ptr(dev_status), _stream(stream)))

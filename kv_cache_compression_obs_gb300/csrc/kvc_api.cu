@@ -69,6 +69,24 @@ int ensure_smem(const void *func, size_t bytes) {
   return 0;
 }
 
+// Argument checks of the scoring entry points (kv_score_obs and its no-alloc
+// variant), in one place so both answer alike.  KV_OK with B == 0 means there is
+// nothing to launch.
+int check_score_args(const void *Q_obs, const void *K, int B, int Hq, int Hkv, int T, int d,
+                     int W, float scale, int dtype, const float *s_out) {
+  auto fits = [](long long a, long long b) { return a >= 0 && b >= 0 && (b == 0 || a <= (1LL << 62) / b); };
+  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || T <= 0 || W <= 0 || W > T ||
+      !(dtype == KV_BF16 || dtype == KV_F32) || !(scale == scale))
+    return KV_ERR_INVALID_ARG;
+  if (!(d == 64 || d == 128)) return KV_ERR_UNSUPPORTED;
+  if (!fits((long long)B * Hkv, (long long)T * d) || !fits((long long)B * Hq, (long long)W * d))
+    return KV_ERR_INVALID_ARG;
+  if (B == 0) return KV_OK;
+  if (!Q_obs || !K || !s_out || !aligned16(Q_obs) || !aligned16(K) || !aligned16(s_out))
+    return KV_ERR_INVALID_ARG;
+  return KV_OK;
+}
+
 }  // namespace kvc
 
 using namespace kvc;
@@ -216,15 +234,8 @@ size_t kv_workspace_size(int op, int B, int Hq, int Hkv, int T, int d, int W, in
 int kv_score_obs(const void *Q_obs, const void *K, int B, int Hq, int Hkv, int T, int d, int W,
                  float scale, int dtype, float *s_out, void *workspace, size_t workspace_bytes,
                  int *dev_status, kv_stream_t stream) {
-  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || T <= 0 || W <= 0 || W > T ||
-      !dtype_ok(dtype) || !(scale == scale))
-    return KV_ERR_INVALID_ARG;
-  if (!dim_ok(d)) return KV_ERR_UNSUPPORTED;
-  if (!fits((long long)B * Hkv, (long long)T * d) || !fits((long long)B * Hq, (long long)W * d))
-    return KV_ERR_INVALID_ARG;
-  if (B == 0) return KV_OK;
-  if (!Q_obs || !K || !s_out || !aligned16(Q_obs) || !aligned16(K) || !aligned16(s_out))
-    return KV_ERR_INVALID_ARG;
+  const int rc = kvc::check_score_args(Q_obs, K, B, Hq, Hkv, T, d, W, scale, dtype, s_out);
+  if (rc != KV_OK || B == 0) return rc;
   const ScorePlan plan = plan_score(B, Hq, Hkv, T, W);
   if (!workspace || workspace_bytes < plan.ws_bytes || !aligned16(workspace)) return KV_ERR_WORKSPACE;
   return launch_score_obs(Q_obs, K, B, Hq, Hkv, T, d, W, scale, dtype, s_out, workspace, plan,

@@ -59,6 +59,11 @@ template <> struct Vec16<float> {
   }
 };
 
+// Host-side argument checks shared by kv_score_obs and kv_score_obs_noalloc:
+// KV_OK (with B == 0: nothing to launch) or the status to return.
+int check_score_args(const void *Q_obs, const void *K, int B, int Hq, int Hkv, int T, int d,
+                     int W, float scale, int dtype, const float *s_out);
+
 // ---- operation plans (shared by the launchers and kv_workspace_size) --------
 struct ScorePlan {
   int gw;          // query rows per unit = G * W

@@ -20,7 +20,9 @@
 //     kernels write every entry they later read, so nothing needs clearing.
 //   * the device address of the array is looked up (cudaGetSymbolAddress) by
 //     the first call on each device, with that device current; make that first
-//     call before any stream capture.
+//     call before any stream capture.  The address is cached for the life of
+//     the process and is stale after cudaDeviceReset (or any teardown of the
+//     primary context): this entry point must not be called after one.
 #include <mutex>
 
 #include "kvc_internal.cuh"
@@ -53,17 +55,8 @@ void *scratch_on(int dev) {
 extern "C" int kv_score_obs_noalloc(const void *Q_obs, const void *K, int B, int Hq, int Hkv,
                                     int T, int d, int W, float scale, int dtype, float *s_out,
                                     int *dev_status, kv_stream_t stream) {
-  if (B < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || T <= 0 || W <= 0 || W > T ||
-      !(dtype == KV_BF16 || dtype == KV_F32) || !(scale == scale))
-    return KV_ERR_INVALID_ARG;
-  if (!(d == 64 || d == 128)) return KV_ERR_UNSUPPORTED;
-  if ((long long)B * Hkv > (1LL << 40) / ((long long)T * d) ||
-      (long long)B * Hq > (1LL << 40) / ((long long)W * d))
-    return KV_ERR_INVALID_ARG;
-  if (B == 0) return KV_OK;
-  if (!Q_obs || !K || !s_out || !kvc::aligned16(Q_obs) || !kvc::aligned16(K) ||
-      !kvc::aligned16(s_out))
-    return KV_ERR_INVALID_ARG;
+  const int rc = kvc::check_score_args(Q_obs, K, B, Hq, Hkv, T, d, W, scale, dtype, s_out);
+  if (rc != KV_OK || B == 0) return rc;
   const kvc::ScorePlan plan = kvc::plan_score(B, Hq, Hkv, T, W);
   if (plan.ws_bytes > KV_SCORE_NOALLOC_SCRATCH_BYTES) return KV_ERR_WORKSPACE;
   int dev = 0;

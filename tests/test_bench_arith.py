@@ -42,9 +42,22 @@ def test_decode_bytes_per_step():
     assert 1.0 <= traffic / a["h2o_decode_step"] <= 1.1
 
 
-def test_score_flops_two_passes():
-    # statistics pass and column-mass pass: 2 x (2 G W T d) flops per unit
-    assert bench.score_flops(WL) == 2 * 2 * G * W * T * D * UNITS == 4_398_046_511_104
+def test_score_flops_one_contraction_over_visible_pairs():
+    # one Q K^T, 2 d flops per (query row, key) pair the window sees: row w of a
+    # query head sits at position T - W + w and sees keys 0 .. T - W + w
+    pairs = G * sum(T - W + w + 1 for w in range(W))
+    assert bench.score_pairs(WL) == pairs == 33_546_368
+    assert bench.score_flops(WL) == 2 * D * pairs * UNITS == 2_198_494_773_248
+    # the two-pass kernels issue twice that (statistics, then column mass)
+    assert bench.score_flops_executed(WL) == 2 * bench.score_flops(WL)
+
+
+def test_score_pairs_full_causal():
+    # every prompt position observed (W = T, the H2O decode workload's scoring):
+    # the causal triangle, T (T + 1) / 2 pairs per query head
+    wl = configs.H2O_DECODE
+    assert wl.W == wl.T and wl.Hq == wl.Hkv
+    assert bench.score_pairs(wl) == wl.T * (wl.T + 1) // 2
 
 
 def test_whole_job_rate_counts_every_rank():

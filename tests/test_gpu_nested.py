@@ -1,11 +1,13 @@
 """GPU parity of the NestedKV key-only scorer (NestedKV technical summary,
 1. Continuum Geheugentoestand, 2. Buitenste Leraar) against the float64 oracle.
 
-Tolerance: the anomaly scores are cosines in [-1, 1], the discriminative powers
-lie in [0, 2] and the weights in [0, 1]; the 1e-5 relative bar is applied
-relative to that unit scale, i.e. |gpu - ref| <= 1e-5.  The routing compares the
-surprise with a threshold: tokens whose float64 surprise lies within 1e-5 of it
-may take either route, and must then match that route's value.
+Tolerance: the 1e-5 relative bar, |gpu - ref| <= 1e-5 (|ref| + FLOOR).  The
+anomaly scores are cosines, each a d-term fp32 dot product of unit vectors, so
+their rounding error is absolute (a few 1e-8, independent of the cosine's size);
+below |ref| = FLOOR a relative bar would measure that cancellation rather than the
+method, and the bar becomes the absolute 1e-5 FLOOR there.  The routing compares
+the surprise with a threshold: tokens whose float64 surprise lies within the bar
+of it may take either route, and must then match that route's value.
 """
 import numpy as np
 import pytest
@@ -18,6 +20,17 @@ pytestmark = pytest.mark.gpu
 
 DEV = "cuda"
 TOL = 1e-5
+FLOOR = 1e-3
+
+
+def _assert_rel(gpu, ref, what):
+    err = np.abs(gpu - ref)
+    bound = TOL * (np.abs(ref) + FLOOR)
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(err / bound), err.shape)
+        raise AssertionError(f"{what}: {int(bad.sum())}/{bad.size} outside 1e-5 (|ref| + {FLOOR}); "
+                             f"worst at {i}: gpu={gpu[i]!r} ref={ref[i]!r}")
 
 
 def _keys(B, H, T, d, dt, recipe, seed):
@@ -33,18 +46,18 @@ def _check(kvc, oracle_mod, K, n_disc, thresh, lp, window, n_blocks):
     score, w = kvc.kv_score_nested(K, n_disc, thresh, lp, window, n_blocks, a_out=a)
     torch.cuda.synchronize()
     ref = oracle_mod.nested_score(gen.to_numpy_bits(K), n_disc, thresh, lp, window, n_blocks)
-    a_g, w_g, s_g = a.cpu().numpy(), w.cpu().numpy(), score.cpu().numpy()
-    err_a = np.abs(a_g - ref["a"]).max()
-    assert err_a <= TOL, f"anomaly scores: max abs error {err_a:.2e}"
-    err_w = np.abs(w_g - ref["w"]).max()
-    assert err_w <= TOL, f"weights: max abs error {err_w:.2e}"
-    near = np.abs(ref["sigma"] - thresh) <= TOL
-    err = np.abs(s_g - ref["score"])
-    assert err[~near].max(initial=0.0) <= TOL, f"score: max abs error {err[~near].max():.2e}"
+    a_g, w_g, s_g = (x.cpu().numpy().astype(np.float64) for x in (a, w, score))
+    _assert_rel(a_g, ref["a"], "anomaly scores")
+    _assert_rel(w_g, ref["w"], "weights")
+    near = np.abs(ref["sigma"] - thresh) <= TOL * (thresh + FLOOR)
+    _assert_rel(s_g[~near], ref["score"][~near], "score")
     if near.any():  # either route, matched to the GPU's own anomaly scores
         A = a_g.transpose(0, 1, 3, 2)[near]
         blend = (A * w_g[:, :, None, :].repeat(T, axis=2)[near]).sum(-1)
-        ok = (np.abs(s_g[near] - A.max(-1)) <= TOL) | (np.abs(s_g[near] - blend) <= TOL)
+
+        def within(x, y):
+            return np.abs(x - y) <= TOL * (np.abs(y) + FLOOR)
+        ok = within(s_g[near], A.max(-1)) | within(s_g[near], blend)
         assert ok.all()
     # deterministic
     score2, _ = kvc.kv_score_nested(K, n_disc, thresh, lp, window, n_blocks)

@@ -6,22 +6,23 @@ device; they cannot provide kv_score_obs's scratch workspace.  The no-alloc
 entry point takes its scratch from a fixed array inside the library instead.
 This test calls it through the C ABI and checks, on two calls in a row with
 different shapes (so the second call runs on the first call's leftovers), that
-it returns what kv_score_obs returns.  The file is named to run last.
+it returns bit for bit what kv_score_obs returns (both run the same kernels with
+the same plan), and that a device status word passed to it stays 0.  The file
+is named so that pytest collects it last: a failure in the shared-array path
+then cannot stop a run with -x before every other test has run.
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
-from _parity import RTOL, assert_close
 from kv_cache_compression_obs_gb300 import gen
 from kv_cache_compression_obs_gb300.configs import Workload
 
 pytestmark = pytest.mark.gpu
 
 
-def _c_noalloc(lib, Q, K, s, scale):
+def _c_noalloc(lib, Q, K, s, scale, status=None):
     fn = lib.kv_score_obs_noalloc
     P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     fn.restype = I
@@ -31,7 +32,8 @@ def _c_noalloc(lib, Q, K, s, scale):
     dt = 0 if K.dtype == torch.bfloat16 else 1
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     return fn(ctypes.c_void_p(Q.data_ptr()), ctypes.c_void_p(K.data_ptr()), B, Hq, Hkv, T, d, W,
-              float(scale), dt, ctypes.c_void_p(s.data_ptr()), None, stream)
+              float(scale), dt, ctypes.c_void_p(s.data_ptr()),
+              None if status is None else ctypes.c_void_p(status.data_ptr()), stream)
 
 
 WORKLOADS = [
@@ -44,14 +46,16 @@ WORKLOADS = [
 
 def test_noalloc_matches_workspace_entry_point(kvc):
     lib = kvc.library_handle()
-    for wl in WORKLOADS:  # two calls in a row, different shapes and dtypes
+    for i, wl in enumerate(WORKLOADS):  # two calls in a row, different shapes and dtypes
         Q, K, _ = gen.prefill_inputs(wl, device="cuda")
         ref = kvc.kv_score_obs(Q, K)
         s = torch.full_like(ref, float("nan"))
-        assert _c_noalloc(lib, Q, K, s, wl.scale) == kvc.KV_OK
+        status = torch.zeros(1, dtype=torch.int32, device="cuda") if i == 0 else None
+        assert _c_noalloc(lib, Q, K, s, wl.scale, status) == kvc.KV_OK
         torch.cuda.synchronize()
-        assert_close(s.cpu().numpy(), ref.cpu().numpy().astype(np.float64), rtol=RTOL,
-                     what=f"noalloc vs workspace ({wl.name})")
+        assert torch.equal(s, ref), f"noalloc vs workspace ({wl.name}): bits differ"
+        if status is not None:
+            assert int(status.item()) == 0  # no device-side wait gave up
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(kvc):
