@@ -63,6 +63,9 @@ def parse():
                     help="layer-row groups of the end-to-end path (default E2E_GROUPS)")
     ap.add_argument("--no-next-rows", action="store_true",
                     help="skip the separate timing of the rows beyond the five-step path")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip the separate timing of the other workloads (single layer, H2O "
+                         "decode, GQA prefill)")
     return ap.parse_args()
 
 
@@ -416,6 +419,76 @@ def time_next_rows(pipe, reps=5, warmup=3):
     return out
 
 
+OTHER_WORKLOADS = ("llama2-7b-layer", "h2o-decode", "gqa-prefill")
+
+
+def time_workload(name, reps=5):
+    """One of the pages' other workloads on its own buffers, outside the timed step:
+    the prefill chain (and the decode steps, where the workload has them) captured
+    as CUDA graphs and replayed, each replay timed with events on the launching
+    stream; L2 is flushed before every replay when the workload's keys fit in it.
+    Per-phase times come from one eager pass with events between the phases."""
+    import torch
+    from kv_cache_compression_obs_gb300 import configs
+
+    wl = configs.BY_NAME[name]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pipe = Pipeline(wl, dev)
+    for _ in range(3):
+        pipe.step()
+    torch.cuda.synchronize()
+    pipe.capture()
+    phases = pipe.timed_phases()
+    gp, gd = pipe.graphs
+    k_bytes = wl.units * wl.T * wl.d * wl.elem_bytes
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev) if k_bytes < L2_BYTES else None
+    tp, td = [], []
+    for _ in range(reps + 1):  # the first replay is untimed
+        if flush is not None:
+            flush.fill_(1.0)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+        e[0].record()
+        gp.replay()
+        e[1].record()
+        if wl.n_decode:
+            gd.replay()
+        e[2].record()
+        torch.cuda.synchronize()
+        tp.append(e[0].elapsed_time(e[1]))
+        td.append(e[1].elapsed_time(e[2]))
+    tp, td = tp[1:], td[1:]
+    peak, peak_tf, kind = measured_peaks()
+    alg = algorithmic_bytes(wl)
+    names = ("kv_score_obs", "hubkv_refine", "kv_select_topk", "kv_compact")
+    pre_bytes = sum(alg[n] for n in names)
+    ms = statistics.median(tp)
+    score_s = phases["kv_score_obs"] / 1e3
+    out = {"workload": wl.name, "units": wl.units, "prompt": wl.T, "obs_window": wl.W,
+           "budget_k": wl.k, "recent": wl.R, "hubkv": wl.r is not None,
+           "l2": "flushed before every replay" if flush is not None else "inputs larger than L2",
+           "prefill": {"ms": ms, "kv_tokens_per_s": wl.rows * wl.T / (ms / 1e3),
+                       "head_tokens_per_s": wl.units * wl.T / (ms / 1e3),
+                       "algorithmic_bytes": pre_bytes,
+                       "hbm_frac": pre_bytes / (ms / 1e3) / 1e9 / peak, "peak_kind": kind,
+                       "graph": "a1-a4 replayed as one CUDA graph"},
+           "phases_ms_eager": phases,
+           "score": {"ms": phases["kv_score_obs"], "algorithmic_flops": score_flops(wl),
+                     "tflops": score_flops(wl) / score_s / 1e12,
+                     "tensor_frac": score_flops(wl) / score_s / 1e12 / peak_tf,
+                     "hbm_frac": alg["kv_score_obs"] / score_s / 1e9 / peak}}
+    if wl.n_decode:
+        step_ms = statistics.median(td) / wl.n_decode
+        out["decode"] = {"steps": wl.n_decode, "ms_per_step": step_ms,
+                         "steps_per_s": 1e3 / step_ms,
+                         "algorithmic_bytes_per_step": alg["h2o_decode_step"],
+                         "hbm_frac": alg["h2o_decode_step"] / (step_ms / 1e3) / 1e9 / peak,
+                         "cap": wl.cap, "kv_heads": wl.units, "group": wl.G}
+    del pipe, flush
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
 def launch_count():
     from kv_cache_compression_obs_gb300 import api
     return int(api.library_handle().kv_launch_count())
@@ -661,6 +734,11 @@ def run_ours(args, wl, rank, world):
     }
     if not args.no_next_rows:
         line["next_rows"] = time_next_rows(pipe)
+    if not args.no_other_workloads and world == 1:
+        # the pages' other workloads, each on its own buffers (about 20 GB beside the
+        # headline workload's, far below the GPU's memory)
+        line["other_workloads"] = {nm: time_workload(nm) for nm in OTHER_WORKLOADS
+                                   if nm != wl.name}
     if not args.no_e2e:
         if world > 1:
             dist.barrier()

@@ -112,12 +112,16 @@ typedef void *kv_stream_t;
  *   K          [B][Hkv][T][d]
  *   scale      logit scale, normally 1/sqrt(d)
  *   s_out      [B][Hkv][T] float32 (written in full)
- *   workspace  >= kv_workspace_size(KV_OP_SCORE_OBS, ...) bytes of device memory
+ *   workspace  >= kv_workspace_size(KV_OP_SCORE_OBS, ...) bytes of device memory;
+ *              its first words are cleared by an asynchronous memset on `stream`
+ *              at the start of every call, the rest is written before it is read
  *   dev_status device int, may be NULL; set to KV_ERR_TIMEOUT if a bounded
  *              device-side wait gave up (s_out is then not valid); never cleared
  * Preconditions: 1 <= W <= T, Hq % Hkv == 0, d in {64, 128}.
- * bf16 inputs with G*W <= 256 run on the tensor cores (tcgen05, TMA); fp32
- * inputs and larger windows on the CUDA cores; both give the same quantity.
+ * bf16 inputs run on the tensor cores (tcgen05, TMA), the G*W query rows of a
+ * unit in blocks of up to 256 (so W = T, every prompt query observed, works
+ * too); fp32 inputs on the CUDA cores; both give the same quantity.  Repeated
+ * calls on the same inputs give identical bits (fixed-order sums).
  */
 KVC_API int kv_score_obs(const void *Q_obs, const void *K, int B, int Hq, int Hkv, int T, int d,
                  int W, float scale, int dtype, float *s_out, void *workspace,
@@ -389,7 +393,9 @@ KVC_API int h2o_decode_steps(const void *q, const void *k_new, const void *v_new
  *     KV_ERR_WORKSPACE before anything is launched.
  *   - All calls share the one array: calls that overlap on the GPU (different
  *     streams, or different host threads) race and corrupt each other's
- *     results, so serialise them.  The array keeps the last call's contents.
+ *     results, so serialise them.  The array keeps the last call's contents;
+ *     each call clears the few words that must start at zero (the kernels'
+ *     work-claim counters) with a memset on `stream` before its kernels run.
  *   - The first call on each device looks the array's device address up, with
  *     that device current; make that first call before any stream capture.
  *     The address is kept for the life of the process: it is not valid after

@@ -70,11 +70,19 @@ struct ScorePlan {
   int row_blocks;  // ceil(gw / 64)                          (CUDA-core path)
   int n_splits;    // key splits of the statistics pass      (CUDA-core path)
   int split_len;   // keys per split (multiple of 128)       (CUDA-core path)
-  int tc_splits;   // key splits per unit of both passes     (tensor-core path)
-  int tc_split_len;  // keys per split (multiple of 128)     (tensor-core path)
   size_t ws_bytes;   // enough for either path
 };
 ScorePlan plan_score(int B, int Hq, int Hkv, int T, int W);
+
+// Workspace layout of the tensor-core scoring path: claim counters (cleared by
+// every call), per-split row statistics, merged row offsets, per-row-block column sums.
+struct TcLayout {
+  int nrb;        // row blocks of up to 256 query rows per unit
+  int ns;         // key splits per row block
+  int split_len;  // keys per split (a multiple of 128)
+  size_t ctrl_off, part_off, fin_off, pcol_off, bytes;
+};
+TcLayout tc_layout(int B, int Hq, int Hkv, int T, int W);
 
 struct RefinePlan {
   int chunk;     // elements per entropy chunk

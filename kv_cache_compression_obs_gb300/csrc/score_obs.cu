@@ -13,9 +13,8 @@
 //   3. colsum:  per key block, sum over rows of 2^(x - M) / Z.
 // Logits are computed twice (once per pass) in fp32 FMA with 64x64 shared-memory
 // tiles; the sums are fixed-order, so repeated runs give identical bits.  This is
-// the path for fp32 inputs and for more than 256 query rows per unit; bf16
-// inputs with up to 256 rows per unit go to the tensor-core kernels of
-// score_obs_tc.cu, which share the combine step and the workspace layout.
+// the path for fp32 inputs; bf16 inputs go to the tensor-core kernel of
+// score_obs_tc.cu.
 #include <cmath>
 
 #include "kvc_internal.cuh"
@@ -281,12 +280,9 @@ ScorePlan plan_score(int B, int Hq, int Hkv, int T, int W) {
   const long units = (long)B * Hkv;
   const long base = units * p.row_blocks;
   split_keys(T, (kTargetCtas + base - 1) / (base > 0 ? base : 1), &p.n_splits, &p.split_len);
-  // tensor-core path: persistent CTAs walk (unit, split) items; about 16 items per
-  // SM keeps the round-robin tail short
-  const long u = units > 0 ? units : 1;
-  split_keys(T, (16L * kNumSmsHint + u - 1) / u, &p.tc_splits, &p.tc_split_len);
-  const int most = p.n_splits > p.tc_splits ? p.n_splits : p.tc_splits;
-  p.ws_bytes = (size_t)units * (most + 1) * p.gw * sizeof(float2);
+  const size_t core = (size_t)units * (p.n_splits + 1) * p.gw * sizeof(float2);
+  const size_t tcb = tc_layout(B, Hq, Hkv, T, W).bytes;
+  p.ws_bytes = core > tcb ? core : tcb;
   return p;
 }
 

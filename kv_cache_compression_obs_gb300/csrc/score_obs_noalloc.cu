@@ -16,8 +16,10 @@
 //     larger are rejected with KV_ERR_WORKSPACE before anything is launched;
 //   * every call shares the one array, so calls that overlap on the GPU (two
 //     streams, or two host threads) race and corrupt each other's results:
-//     serialise them.  The array keeps the last call's contents; the scoring
-//     kernels write every entry they later read, so nothing needs clearing.
+//     serialise them.  The array keeps the last call's contents: every call
+//     zeroes the scoring kernels' work-claim counters at its start (an
+//     asynchronous memset on the caller's stream, not an allocation), and the
+//     kernels write every other entry before they read it.
 //   * the device address of the array is looked up (cudaGetSymbolAddress) by
 //     the first call on each device, with that device current; make that first
 //     call before any stream capture.  The address is cached for the life of
