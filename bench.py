@@ -79,13 +79,15 @@ def algorithmic_bytes(wl):
     k_bytes = units * wl.T * wl.d * eb
     s_bytes = units * wl.T * 4
     score = q_bytes + k_bytes + s_bytes                    # read Q, K; write s
-    refine = 2 * s_bytes if wl.r is not None else 0        # read s, write z
-    select = s_bytes + units * wl.k * 4                    # read z, write idx
+    # refinement + Top-K (one fused call): the head weights need each head's whole
+    # score vector before any refined score exists, so s is read twice (entropy,
+    # then the selection, which forms z as it loads); the kept positions written
+    select = (2 * s_bytes if wl.r is not None else s_bytes) + units * wl.k * 4
     row = wl.d * eb
     compact = units * wl.k * (4 * row + 4 + 4 + 4 + 4)     # K,V rows read+written; idx, s, pos, acc
     decode_step = units * wl.cap * (2 * row + 4 + 4 + 4) + wl.rows * (wl.Hq * wl.d * (eb + 4)
                                                                     + 2 * wl.Hkv * row)
-    return {"kv_score_obs": score, "hubkv_refine": refine, "kv_select_topk": select,
+    return {"kv_score_obs": score, "hubkv_select_topk": select,
             "kv_compact": compact, "h2o_decode_step": decode_step}
 
 
@@ -224,7 +226,8 @@ class Pipeline:
         self.EV = torch.empty(nd, *units_shape, dtype=i32, device=device)
         self.o, self.ev = self.O[-1], self.EV[-1]
         ws = max(api.kv_workspace_size(api.KV_OP_SCORE_OBS, wl.rows, wl.Hq, wl.Hkv, wl.T, wl.d, wl.W),
-                 api.kv_workspace_size(api.KV_OP_HUBKV_REFINE, wl.rows, wl.Hkv, wl.Hkv, wl.T), 256)
+                 api.kv_workspace_size(api.KV_OP_HUBKV_SELECT, wl.rows, wl.Hkv, wl.Hkv, wl.T, 0,
+                                       wl.R, wl.k), 256)
         self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
         dws = api.kv_workspace_size(api.KV_OP_DECODE, wl.rows, wl.Hq, wl.Hkv, wl.cap, wl.d)
         self.dws = torch.empty(max(dws, 256), dtype=torch.uint8, device=device)
@@ -235,13 +238,20 @@ class Pipeline:
         self.dk = [self.DK[t] for t in range(wl.n_decode)]
         self.dv = [self.DV[t] for t in range(wl.n_decode)]
 
+    def select(self, stream=None):
+        """HubKV refinement + Top-K (one fused call), or Top-K on s without refinement."""
+        a, wl = self.api, self.wl
+        if wl.r is not None:
+            a.hubkv_select_topk(self.s, wl.k, wl.R, wl.r, wl.gamma, wl.pool_width, wl.beta_lo,
+                                wl.beta_hi, out=self.idx, beta_out=self.beta, workspace=self.ws,
+                                stream=stream)
+        else:
+            a.kv_select_topk(self.s, wl.k, wl.R, out=self.idx, stream=stream)
+
     def prefill(self, stream=None):
         a, wl = self.api, self.wl
         a.kv_score_obs(self.Q, self.K, wl.scale, out=self.s, workspace=self.ws, stream=stream)
-        if wl.r is not None:
-            a.hubkv_refine(self.s, wl.r, wl.gamma, wl.pool_width, wl.beta_lo, wl.beta_hi,
-                           out=self.z, beta_out=self.beta, workspace=self.ws, stream=stream)
-        a.kv_select_topk(self.z, wl.k, wl.R, out=self.idx, stream=stream)
+        self.select(stream)
         a.kv_compact(self.K, self.V, self.s, self.idx, wl.cap, K_out=self.Kc, V_out=self.Vc,
                      pos_out=self.pos, acc_out=self.acc, len_out=self.len, stream=stream)
 
@@ -294,26 +304,22 @@ class Pipeline:
         """One step with events between the phases: ms per phase."""
         import torch
         a, wl = self.api, self.wl
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
         ev[0].record()
         a.kv_score_obs(self.Q, self.K, wl.scale, out=self.s, workspace=self.ws)
         ev[1].record()
-        if wl.r is not None:
-            a.hubkv_refine(self.s, wl.r, wl.gamma, wl.pool_width, wl.beta_lo, wl.beta_hi,
-                           out=self.z, beta_out=self.beta, workspace=self.ws)
+        self.select()
         ev[2].record()
-        a.kv_select_topk(self.z, wl.k, wl.R, out=self.idx)
-        ev[3].record()
         a.kv_compact(self.K, self.V, self.s, self.idx, wl.cap, K_out=self.Kc, V_out=self.Vc,
                      pos_out=self.pos, acc_out=self.acc, len_out=self.len)
-        ev[4].record()
+        ev[3].record()
         if self.graphs is not None:
             self.graphs[1].replay()
         else:
             self.decode_all()
-        ev[5].record()
+        ev[4].record()
         torch.cuda.synchronize()
-        names = ["kv_score_obs", "hubkv_refine", "kv_select_topk", "kv_compact", "h2o_decode_step"]
+        names = ["kv_score_obs", "hubkv_select_topk", "kv_compact", "h2o_decode_step"]
         ms = {n: ev[i].elapsed_time(ev[i + 1]) for i, n in enumerate(names)}
         if wl.n_decode:
             ms["h2o_decode_step"] /= wl.n_decode  # per decode step
@@ -382,6 +388,9 @@ def time_next_rows(pipe, reps=5, warmup=3):
 
     out = {}
     peak, _, kind = measured_peaks()
+    if wl.r is not None:  # the refined scores the layer budget ranks (not kept by the step)
+        a.hubkv_refine(pipe.s, wl.r, wl.gamma, wl.pool_width, wl.beta_lo, wl.beta_hi, out=pipe.z,
+                       workspace=pipe.ws)
     ms = timed(sel)
     counts = (off[:, 1:] - off[:, :-1])
     nbytes = wl.units * wl.T * 4 + wl.rows * (budget + wl.Hkv + 1) * 4
@@ -459,7 +468,7 @@ def time_workload(name, reps=5):
     tp, td = tp[1:], td[1:]
     peak, peak_tf, kind = measured_peaks()
     alg = algorithmic_bytes(wl)
-    names = ("kv_score_obs", "hubkv_refine", "kv_select_topk", "kv_compact")
+    names = ("kv_score_obs", "hubkv_select_topk", "kv_compact")
     pre_bytes = sum(alg[n] for n in names)
     ms = statistics.median(tp)
     score_s = phases["kv_score_obs"] / 1e3
@@ -677,10 +686,11 @@ def run_ours(args, wl, rank, world):
 
     tokens = wl.rows * wl.T
     value = whole_job_rate(tokens, world, ms_max / 1e3)
-    prefill_ms = sum(phases[n] for n in ("kv_score_obs", "hubkv_refine", "kv_select_topk", "kv_compact"))
+    PREFILL = ("kv_score_obs", "hubkv_select_topk", "kv_compact")
+    prefill_ms = sum(phases[n] for n in PREFILL)
     peak, peak_tf, peak_kind = measured_peaks()
     alg = algorithmic_bytes(wl)
-    prefill_bytes = sum(alg[n] for n in ("kv_score_obs", "hubkv_refine", "kv_select_topk", "kv_compact"))
+    prefill_bytes = sum(alg[n] for n in PREFILL)
     per_launch = {k: alg[k] for k in alg}
     dom = max(phases, key=lambda n: phases[n] * (wl.n_decode if n == "h2o_decode_step" else 1))
     achieved = per_launch[dom] / (phases[dom] / 1e3) / 1e9

@@ -90,7 +90,8 @@ enum {
   KV_OP_HUBKV_REFINE = 2,
   KV_OP_SELECT_TOPK = 3,
   KV_OP_DECODE = 4,
-  KV_OP_SCORE_NESTED = 5
+  KV_OP_SCORE_NESTED = 5,
+  KV_OP_HUBKV_SELECT = 6
 };
 
 typedef void *kv_stream_t;
@@ -187,6 +188,27 @@ KVC_API int kv_select_topk(const float *z, int B, int H, int T, int k, int recen
 KVC_API int kv_select_topk_ex(const float *z, int B, int H, int T, int k, int recent, int sink,
                       int32_t *idx_out, void *workspace, size_t workspace_bytes,
                       kv_stream_t stream);
+
+/*
+ * hubkv_select_topk -- hubkv_refine_ex followed by kv_select_topk_ex, in one
+ * call ([HubKV] Method: 最终算法 steps 1-4, then [H2O] 双缓冲 / 为什么要按头独立
+ * 驱逐): the kept positions are exactly those kv_select_topk_ex returns on the z
+ * that hubkv_refine_ex writes, and z_out / beta_out (when given) are bit for bit
+ * what hubkv_refine_ex writes.  When the heads fit on chip (T - recent - sink <=
+ * 393216) the selection kernel forms each candidate's z from s itself while
+ * loading, so z never goes through device memory unless the caller asks for it.
+ *
+ *   s          [B][H][T] float32 base scores
+ *   idx_out    [B][H][k] int32, kept positions ascending
+ *   z_out      [B][H][T] float32, may be NULL
+ *   beta_out   [B][H] float32, may be NULL
+ *   workspace  >= kv_workspace_size(KV_OP_HUBKV_SELECT, B, H, H, T, 0, recent + sink, k)
+ * Preconditions: those of hubkv_refine_ex and kv_select_topk_ex.
+ */
+KVC_API int hubkv_select_topk(const float *s, int B, int H, int T, int pool_width, float gamma,
+                              float r, float beta_lo, float beta_hi, int flags, int k, int recent,
+                              int sink, int32_t *idx_out, float *z_out, float *beta_out,
+                              void *workspace, size_t workspace_bytes, kv_stream_t stream);
 
 /*
  * kv_compact -- "real drop" gather-compaction ([H2O] 两套代码) into a

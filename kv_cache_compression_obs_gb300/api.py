@@ -30,6 +30,7 @@ KV_BF16, KV_F32 = 0, 1
 KV_H2O_ALG1 = 1
 KV_HUB_AVGPOOL, KV_HUB_FIXED_HEAD = 1, 2
 KV_OP_SCORE_OBS, KV_OP_HUBKV_REFINE, KV_OP_SELECT_TOPK, KV_OP_DECODE, KV_OP_SCORE_NESTED = 1, 2, 3, 4, 5
+KV_OP_HUBKV_SELECT = 6
 
 _P, _I, _F, _Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _lib.kv_score_obs.restype = _I
@@ -42,6 +43,9 @@ _lib.kv_select_topk.restype = _I
 _lib.kv_select_topk.argtypes = [_P, _I, _I, _I, _I, _I, _P, _P, _Z, _P]
 _lib.kv_select_topk_ex.restype = _I
 _lib.kv_select_topk_ex.argtypes = [_P, _I, _I, _I, _I, _I, _I, _P, _P, _Z, _P]
+_lib.hubkv_select_topk.restype = _I
+_lib.hubkv_select_topk.argtypes = [_P, _I, _I, _I, _I, _F, _F, _F, _F, _I, _I, _I, _I, _P, _P, _P, _P,
+                                   _Z, _P]
 _lib.kv_compact.restype = _I
 _lib.kv_compact.argtypes = [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P]
 _lib.kv_score_nested.restype = _I
@@ -219,6 +223,27 @@ def kv_select_topk(z: torch.Tensor, k: int, recent: int, out=None, stream=None,
     return idx
 
 
+def hubkv_select_topk(s: torch.Tensor, k: int, recent: int, r: float, gamma: float = 0.5,
+                      pool_width: int = 5, beta_lo: float = 0.8, beta_hi: float = 1.2,
+                      sink: int = 0, flags: int = 0, out=None, z_out=None, beta_out=None,
+                      workspace=None, stream=None) -> torch.Tensor:
+    """hubkv_refine then kv_select_topk in one call: s [B][H][T] float32 ->
+    idx [B][H][k] int32 (ascending).  z_out [B][H][T] and beta_out [B][H] are
+    filled when given."""
+    B, H, T = s.shape
+    if s.dtype != torch.float32:
+        raise TypeError("s must be float32")
+    _dev(s, out, z_out, beta_out)
+    idx = out if out is not None else torch.empty(B, H, k, dtype=torch.int32, device=s.device)
+    ws, nbytes = _workspace(kv_workspace_size(KV_OP_HUBKV_SELECT, B, H, H, T, 0, recent + sink, k),
+                            s.device, workspace)
+    _check("hubkv_select_topk", _lib.hubkv_select_topk(
+        _ptr(s), B, H, T, int(pool_width), float(gamma), float(r), float(beta_lo), float(beta_hi),
+        int(flags), int(k), int(recent), int(sink), _ptr(idx), _ptr(z_out), _ptr(beta_out),
+        _ptr(ws), nbytes, _stream(stream)))
+    return idx
+
+
 def kv_compact(K: torch.Tensor, V: torch.Tensor, s, idx: torch.Tensor, cap: int | None = None,
                K_out=None, V_out=None, pos_out=None, acc_out=None, len_out=None, stream=None):
     """Gather the kept rows into a slot cache; returns (K_out, V_out, pos, acc, len)."""
@@ -362,9 +387,12 @@ def compress_prefill(Q_obs, K, V, k: int, recent: int, r: float | None, gamma: f
     if r is None:
         z = s
         beta = None
+        idx = kv_select_topk(z, k, recent, stream=stream)
     else:
-        z, beta = hubkv_refine(s, r, gamma, pool_width, beta_lo, beta_hi, stream=stream)
-    idx = kv_select_topk(z, k, recent, stream=stream)
+        z = torch.empty_like(s)
+        beta = torch.empty(s.shape[:2], dtype=torch.float32, device=s.device)
+        idx = hubkv_select_topk(s, k, recent, r, gamma, pool_width, beta_lo, beta_hi, z_out=z,
+                                beta_out=beta, stream=stream)
     Kc, Vc, pos, acc, ln = kv_compact(K, V, s, idx, cap, stream=stream)
     return {"s": s, "z": z, "beta": beta, "idx": idx, "K": Kc, "V": Vc, "pos": pos, "acc": acc,
             "len": ln}
@@ -380,7 +408,8 @@ def prefill_host_buffers(hQ: torch.Tensor, hK: torch.Tensor, k: int, r: float | 
     f32, i32 = torch.float32, torch.int32
     rc = min(rows_per_chunk, B)
     ws = max(kv_workspace_size(KV_OP_SCORE_OBS, rc, Hq, Hkv, T, d, W),
-             kv_workspace_size(KV_OP_HUBKV_REFINE, rc, Hkv, Hkv, T), 256)
+             kv_workspace_size(KV_OP_HUBKV_REFINE, rc, Hkv, Hkv, T),
+             kv_workspace_size(KV_OP_HUBKV_SELECT, rc, Hkv, Hkv, T, 0, 0, k), 256)
     s = torch.empty(B, Hkv, T, dtype=f32, device=dev)
     return {
         "Q": torch.empty(hQ.shape, dtype=hQ.dtype, device=dev),
@@ -418,7 +447,9 @@ def compress_prefill_host(hQ: torch.Tensor, hK: torch.Tensor, hV: torch.Tensor, 
     stream has passed the call.  `rows` = (r0, r1) restricts the call to those
     batch rows (independent of the others); wait=False skips the copy stream's
     wait for the work already on `stream`, for a caller that knows those rows'
-    buffers are free (e.g. the later row groups of one step).
+    buffers are free (e.g. the later row groups of one step).  With HubKV
+    refinement the refined scores z are formed inside the selection and not
+    written (the result's "z" is None).
     """
     for t in (hQ, hK, hV):
         if t.is_cuda or not t.is_pinned() or not t.is_contiguous():
@@ -442,15 +473,17 @@ def compress_prefill_host(hQ: torch.Tensor, hK: torch.Tensor, hV: torch.Tensor, 
         cs.wait_event(landed)
         Q, K, sc = bf["Q"][r0:r1], bf["K"][r0:r1], bf["s"][r0:r1]
         kv_score_obs(Q, K, scale, out=sc, workspace=bf["ws"], stream=cs)
-        z = sc
-        if r is not None:
-            z, _ = hubkv_refine(sc, r, gamma, pool_width, beta_lo, beta_hi, out=bf["z"][r0:r1],
-                                beta_out=bf["beta"][r0:r1], workspace=bf["ws"], stream=cs)
-        idx = kv_select_topk(z, k, recent, out=bf["idx"][r0:r1], stream=cs)
+        if r is None:
+            idx = kv_select_topk(sc, k, recent, out=bf["idx"][r0:r1], stream=cs)
+        else:  # refinement folded into the selection: z is not written
+            idx = hubkv_select_topk(sc, k, recent, r, gamma, pool_width, beta_lo, beta_hi,
+                                    out=bf["idx"][r0:r1], beta_out=bf["beta"][r0:r1],
+                                    workspace=bf["ws"], stream=cs)
         kv_compact(K, hV[r0:r1], sc, idx, bf["cap"], K_out=bf["Kc"][r0:r1], V_out=bf["Vc"][r0:r1],
                    pos_out=bf["pos"][r0:r1], acc_out=bf["acc"][r0:r1], len_out=bf["len"][r0:r1],
                    stream=cs)
-    return {"s": bf["s"], "z": bf["z"], "beta": bf["beta"] if r is not None else None,
+    return {"s": bf["s"], "z": None if r is not None else bf["s"],
+            "beta": bf["beta"] if r is not None else None,
             "idx": bf["idx"], "K": bf["Kc"], "V": bf["Vc"], "pos": bf["pos"], "acc": bf["acc"],
             "len": bf["len"]}
 

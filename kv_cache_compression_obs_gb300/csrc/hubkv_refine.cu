@@ -12,6 +12,7 @@
 #include <cmath>
 
 #include "kvc_internal.cuh"
+#include "refine_common.cuh"
 
 namespace kvc {
 namespace {
@@ -128,27 +129,8 @@ __global__ __launch_bounds__(NT) void refine_apply_kernel(
     tile[t] = (i >= 0 && i < T) ? sv[i] : -INFINITY;
   }
   __syncthreads();
-  for (int i = i0 + threadIdx.x; i < i1; i += NT) {
-    const int t = i - lo;
-    const float si = tile[t];
-    float qi;
-    if constexpr (AVG) {
-      // KV_HUB_AVGPOOL: the mean over the window cut at the ends, summed in window order
-      float sum = 0.f;
-      int cnt = 0;
-      for (int o = -half; o <= half; ++o)
-        if (i + o >= 0 && i + o < T) {
-          sum += tile[t + o];
-          ++cnt;
-        }
-      qi = sum / (float)cnt;
-    } else {
-      float M = si;
-      for (int o = -half; o <= half; ++o) M = fmaxf(M, tile[t + o]);
-      qi = (si == M) ? si : gamma * si;
-    }
-    zv[i] = fmaf(r2, fmaf(beta, qi, -si), si);  // s + r^2 (beta q - s)
-  }
+  for (int i = i0 + threadIdx.x; i < i1; i += NT)
+    zv[i] = hub_gate<AVG>(tile + (i - lo), half, i, T, gamma, r2, beta);
 }
 
 }  // namespace
@@ -162,18 +144,21 @@ RefinePlan plan_refine(int B, int H, int T) {
   return p;
 }
 
-int launch_hubkv_refine(const float *s, int B, int H, int T, int pool_width, float gamma,
-                        float r, float beta_lo, float beta_hi, int flags, float *z, float *beta,
-                        void *ws, const RefinePlan &plan, cudaStream_t st) {
+int launch_refine_beta(const float *s, int B, int H, int T, float beta_lo, float beta_hi, int flags,
+                       float *beta, void *ws, const RefinePlan &plan, cudaStream_t st) {
   const long heads = (long)B * H;
-  const int half = pool_width / 2;
-  if (half > kMaxHalo) return KV_ERR_UNSUPPORTED;
   double2 *part = static_cast<double2 *>(ws);
   float *beta_ws = reinterpret_cast<float *>(static_cast<char *>(ws) + plan.beta_offset);
   refine_entropy_kernel<<<(unsigned)(heads * plan.n_chunks), NT, 0, st>>>(s, T, plan.n_chunks, part);
   const int bt = H < 256 ? ((H + 31) / 32) * 32 : 256;
   refine_beta_kernel<<<(unsigned)B, bt, (size_t)H * sizeof(double), st>>>(
       part, H, T, plan.n_chunks, beta_lo, beta_hi, (flags & KV_HUB_FIXED_HEAD) ? 1 : 0, beta_ws, beta);
+  return launch_status(2);
+}
+
+int launch_refine_apply(const float *s, int B, int H, int T, int half, float gamma, float r, int flags,
+                        const float *beta_ws, float *z, cudaStream_t st) {
+  const long heads = (long)B * H;
   const int bph = (T + kApply - 1) / kApply;
   const size_t smem = (size_t)(kApply + 2 * half) * sizeof(float);
   if (flags & KV_HUB_AVGPOOL)
@@ -182,7 +167,18 @@ int launch_hubkv_refine(const float *s, int B, int H, int T, int pool_width, flo
   else
     refine_apply_kernel<false><<<(unsigned)(heads * bph), NT, smem, st>>>(s, T, bph, half, gamma, r * r,
                                                                        beta_ws, z);
-  return launch_status(3);
+  return launch_status(1);
+}
+
+int launch_hubkv_refine(const float *s, int B, int H, int T, int pool_width, float gamma,
+                        float r, float beta_lo, float beta_hi, int flags, float *z, float *beta,
+                        void *ws, const RefinePlan &plan, cudaStream_t st) {
+  const int half = pool_width / 2;
+  if (half > kMaxHalo) return KV_ERR_UNSUPPORTED;
+  const int rc = launch_refine_beta(s, B, H, T, beta_lo, beta_hi, flags, beta, ws, plan, st);
+  if (rc != KV_OK) return rc;
+  const float *beta_ws = reinterpret_cast<const float *>(static_cast<const char *>(ws) + plan.beta_offset);
+  return launch_refine_apply(s, B, H, T, half, gamma, r, flags, beta_ws, z, st);
 }
 
 }  // namespace kvc

@@ -209,7 +209,6 @@ const char *kv_status_string(int status) {
 
 size_t kv_workspace_size(int op, int B, int Hq, int Hkv, int T, int d, int W, int k) {
   (void)d;
-  (void)k;
   if (B < 0 || T <= 0) return 0;
   switch (op) {
     case KV_OP_SCORE_OBS:
@@ -220,6 +219,11 @@ size_t kv_workspace_size(int op, int B, int Hq, int Hkv, int T, int d, int W, in
       return plan_refine(B, Hkv, T).ws_bytes;  // the refine call's H is passed as Hkv
     case KV_OP_SELECT_TOPK:
       return 0;
+    case KV_OP_HUBKV_SELECT: {  // the refine call's H is passed as Hkv, recent + sink as W
+      if (Hkv <= 0 || W < 0 || k <= W || k > T) return 0;
+      const size_t r = align256h(plan_refine(B, Hkv, T).ws_bytes);
+      return r + (hubkv_select_needs_z(T, k, W, 0) ? (size_t)B * Hkv * T * sizeof(float) : 0);
+    }
     case KV_OP_SCORE_NESTED:  // Hkv is the head count, W the number of episodic blocks
       if (Hkv <= 0 || W <= 0 || !(d == 64 || d == 128)) return 0;
       return nested_workspace_bytes((long)B * Hkv, T, d, W, true);
@@ -264,6 +268,31 @@ int hubkv_refine(const float *s, int B, int H, int T, int pool_width, float gamm
                  size_t workspace_bytes, kv_stream_t stream) {
   return hubkv_refine_ex(s, B, H, T, pool_width, gamma, r, beta_lo, beta_hi, 0, z_out, beta_out,
                          workspace, workspace_bytes, stream);
+}
+
+int hubkv_select_topk(const float *s, int B, int H, int T, int pool_width, float gamma, float r,
+                      float beta_lo, float beta_hi, int flags, int k, int recent, int sink,
+                      int32_t *idx_out, float *z_out, float *beta_out, void *workspace,
+                      size_t workspace_bytes, kv_stream_t stream) {
+  if (B < 0 || H <= 0 || T <= 0 || pool_width <= 0 || pool_width % 2 == 0 ||
+      !(beta_lo <= beta_hi) || !(gamma == gamma) || !(r == r) ||
+      (flags & ~(KV_HUB_AVGPOOL | KV_HUB_FIXED_HEAD)) || recent < 0 || sink < 0 ||
+      k <= recent + sink || k > T)
+    return KV_ERR_INVALID_ARG;
+  if (pool_width > 129) return KV_ERR_UNSUPPORTED;
+  if (!fits((long long)B * H, T)) return KV_ERR_INVALID_ARG;
+  if (B == 0) return KV_OK;
+  if (!s || !idx_out || !aligned16(s) || !aligned16(idx_out) || (z_out && !aligned16(z_out)))
+    return KV_ERR_INVALID_ARG;
+  const RefinePlan plan = plan_refine(B, H, T);
+  const size_t rbytes = align256h(plan.ws_bytes);
+  const bool need_z = hubkv_select_needs_z(T, k, recent, sink);
+  const size_t need = rbytes + (need_z ? (size_t)B * H * T * sizeof(float) : 0);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace)) return KV_ERR_WORKSPACE;
+  float *z_tmp = need_z ? reinterpret_cast<float *>(static_cast<char *>(workspace) + rbytes) : nullptr;
+  return launch_hubkv_select(s, B, H, T, pool_width, gamma, r, beta_lo, beta_hi, flags, k, recent,
+                             sink, idx_out, z_out, beta_out, workspace, plan, z_tmp,
+                             static_cast<cudaStream_t>(stream));
 }
 
 int kv_select_topk_ex(const float *z, int B, int H, int T, int k, int recent, int sink,

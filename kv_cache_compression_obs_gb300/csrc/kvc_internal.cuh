@@ -107,6 +107,19 @@ int launch_hubkv_refine(const float *s, int B, int H, int T, int pool_width, flo
                         void *ws, const RefinePlan &plan, cudaStream_t st);
 int launch_select_topk(const float *z, int B, int H, int T, int k, int recent, int sink,
                        int32_t *idx, cudaStream_t st);
+// The refinement's two parts: entropy partials and head weights (into the
+// workspace's beta array, copied to beta_out when given), then z.
+int launch_refine_beta(const float *s, int B, int H, int T, float beta_lo, float beta_hi, int flags,
+                       float *beta_out, void *ws, const RefinePlan &plan, cudaStream_t st);
+int launch_refine_apply(const float *s, int B, int H, int T, int half, float gamma, float r, int flags,
+                        const float *beta_ws, float *z, cudaStream_t st);
+// hubkv_refine then kv_select_topk_ex, z formed inside the selection's load when
+// the heads fit on chip; z_tmp ([B][H][T]) is used only when hubkv_select_needs_z.
+bool hubkv_select_needs_z(int T, int k, int recent, int sink);
+int launch_hubkv_select(const float *s, int B, int H, int T, int pool_width, float gamma, float r,
+                        float beta_lo, float beta_hi, int flags, int k, int recent, int sink,
+                        int32_t *idx, float *z_out, float *beta_out, void *ws,
+                        const RefinePlan &plan, float *z_tmp, cudaStream_t st);
 int launch_compact(const void *K, const void *V, const float *s, const int32_t *idx, int B,
                    int H, int T, int k, int d, int dtype, void *K_out, void *V_out, int cap,
                    int32_t *pos, float *acc, int32_t *len, cudaStream_t st);

@@ -29,6 +29,7 @@
 #include <cooperative_groups.h>
 
 #include "kvc_internal.cuh"
+#include "refine_common.cuh"
 #include "select_common.cuh"
 
 namespace cg = cooperative_groups;
@@ -143,9 +144,21 @@ struct ResidentSmem {
   int cnt[kMaxCl];
 };
 
+// HubKV refinement folded into the selection's load (hubkv_select_topk): the
+// kernel reads the base scores s and forms each candidate's z itself.
+struct RefineArgs {
+  const float *beta;  // [heads] head weights
+  float *z_out;       // [heads][T], may be null
+  float gamma, r2;
+  int half;           // pool_width / 2
+};
+
+// MODE 0: z is given.  MODE 1 / 2: z is formed from s with the local-hub /
+// average-pool discount (refine_common.cuh).
+template <int MODE>
 __global__ __launch_bounds__(NTC) void select_topk_resident_kernel(
     const float *__restrict__ z, int T, int k, int R, int S, int len,
-    int32_t *__restrict__ idx_out) {
+    int32_t *__restrict__ idx_out, RefineArgs ra) {
   extern __shared__ uint32_t keys[];  // this CTA's slice of candidates, as order keys
   __shared__ ResidentSmem sm;
   cg::cluster_group cl = cg::this_cluster();
@@ -159,21 +172,72 @@ __global__ __launch_bounds__(NTC) void select_topk_resident_kernel(
 
   // load the slice as order keys; the first radix pass (top byte) is counted here
   for (int e = threadIdx.x; e < NWC * 256; e += NTC) (&sm.rx.hist[0][0])[e] = 0u;
-  __syncthreads();
-  for (int base = threadIdx.x; base < m; base += 8 * NTC) {
-    float v[8];
+  if constexpr (MODE == 0) {
+    __syncthreads();
+    for (int base = threadIdx.x; base < m; base += 8 * NTC) {
+      float v[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int i = base + u * NTC;
-      v[u] = (i < m) ? __ldg(zv + lo + i) : 0.f;
+      for (int u = 0; u < 8; ++u) {
+        const int i = base + u * NTC;
+        v[u] = (i < m) ? __ldg(zv + lo + i) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = base + u * NTC;
+        if (i < m) {
+          const uint32_t kk = order_key(v[u]);
+          keys[i] = kk;
+          atomicAdd(&sm.rx.hist[warp][kk >> 24], 1u);
+        }
+      }
     }
+  } else {
+    // the slice's scores with a halo of `half` on each side (-inf past the
+    // prompt's ends), as floats in the same buffer: tile[t] = s[S + lo - half + t]
+    float *tile = reinterpret_cast<float *>(keys);
+    const float *sv = z + head * (long)T;  // here z holds the base scores s
+    const int p0 = S + lo - ra.half;        // prompt position of tile[0]
+    const int nt = m + 2 * ra.half;
+    for (int t = threadIdx.x; t < nt; t += NTC) {
+      const int p = p0 + t;
+      tile[t] = (p >= 0 && p < T) ? __ldg(sv + p) : -INFINITY;
+    }
+    const float beta = ra.beta[head];
+    float *zo = ra.z_out ? ra.z_out + head * (long)T : nullptr;
+    // batches of 8 x NTC candidates: all z of a batch are formed before any of
+    // its keys overwrites the front of its window (key i goes to tile[i], the
+    // left end of candidate i's window; later batches read only further right)
+    for (int base0 = 0; base0 < m; base0 += 8 * NTC) {
+      __syncthreads();
+      float v[8];
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const int i = base + u * NTC;
-      if (i < m) {
-        const uint32_t kk = order_key(v[u]);
-        keys[i] = kk;
-        atomicAdd(&sm.rx.hist[warp][kk >> 24], 1u);
+      for (int u = 0; u < 8; ++u) {
+        const int i = base0 + threadIdx.x + u * NTC;
+        v[u] = 0.f;
+        if (i < m)
+          v[u] = hub_gate<MODE == 2>(tile + i + ra.half, ra.half, S + lo + i, T, ra.gamma, ra.r2, beta);
+      }
+      __syncthreads();
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = base0 + threadIdx.x + u * NTC;
+        if (i < m) {
+          const uint32_t kk = order_key(v[u]);
+          keys[i] = kk;
+          atomicAdd(&sm.rx.hist[warp][kk >> 24], 1u);
+          if (zo) zo[S + lo + i] = v[u];
+        }
+      }
+    }
+    if (zo && rank == 0) {
+      // z of the always-kept positions (sinks and recent window) for the caller,
+      // windows read from global memory
+      for (int e = threadIdx.x; e < S + R; e += NTC) {
+        const int p = e < S ? e : T - R + (e - S);
+        float win[2 * 64 + 1];
+        for (int o = -ra.half; o <= ra.half; ++o)
+          win[o + ra.half] = (p + o >= 0 && p + o < T) ? __ldg(sv + p + o) : -INFINITY;
+        zo[p] = hub_gate<MODE == 2>(win + ra.half, ra.half, p, T, ra.gamma, ra.r2, beta);
       }
     }
   }
@@ -238,37 +302,85 @@ __global__ __launch_bounds__(NTC) void select_topk_resident_kernel(
 
 }  // namespace
 
+namespace {
+
+// Cluster geometry of the resident kernel for n candidates with nh heavy slots:
+// CTAs per head and candidates per CTA (len 0: not resident).
+void resident_plan(int n, int nh, int *CL, int *len) {
+  *CL = 0;
+  *len = 0;
+  if (nh < n) {
+    *CL = (n + kSliceSmall - 1) / kSliceSmall;
+    if (*CL > kMaxCl && n <= kMaxCl * kSliceMax) *CL = kMaxCl;
+    if (*CL <= kMaxCl) *len = (n + *CL - 1) / *CL;
+  }
+}
+
+template <int MODE>
+int launch_resident(const float *z, long heads, int T, int k, int recent, int sink, int CL, int len,
+                    int halo, int32_t *idx, const RefineArgs &ra, cudaStream_t st) {
+  const size_t smem = (size_t)(len + 2 * halo) * sizeof(uint32_t);
+  if (ensure_smem((const void *)select_topk_resident_kernel<MODE>, smem))
+    return cuda_failure(cudaErrorInvalidValue, "select kernel: shared memory");
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(heads * CL));
+  cfg.blockDim = dim3(NTC);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = (unsigned)CL;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, select_topk_resident_kernel<MODE>, z, T, k, recent,
+                                           sink, len, idx, ra);
+  if (e != cudaSuccess) return cuda_failure(e, "select kernel");
+  return launch_status();
+}
+
+}  // namespace
+
 int launch_select_topk(const float *z, int B, int H, int T, int k, int recent, int sink,
                        int32_t *idx, cudaStream_t st) {
   const long heads = (long)B * H;
-  const int n = T - recent - sink, nh = k - recent - sink;
-  int CL = 0, len = 0;
-  if (nh < n) {
-    CL = (n + kSliceSmall - 1) / kSliceSmall;
-    if (CL > kMaxCl && n <= kMaxCl * kSliceMax) CL = kMaxCl;
-    if (CL <= kMaxCl) len = (n + CL - 1) / CL;
-  }
+  int CL, len;
+  resident_plan(T - recent - sink, k - recent - sink, &CL, &len);
+  if (len > 0 && heads * CL <= 0x7FFFFFFFL)
+    return launch_resident<0>(z, heads, T, k, recent, sink, CL, len, 0, idx, RefineArgs{}, st);
+  select_topk_kernel<<<(unsigned)heads, NT, 0, st>>>(z, T, k, recent, sink, idx);
+  return launch_status();
+}
+
+bool hubkv_select_needs_z(int T, int k, int recent, int sink) {
+  int CL, len;
+  resident_plan(T - recent - sink, k - recent - sink, &CL, &len);
+  return len == 0;
+}
+
+int launch_hubkv_select(const float *s, int B, int H, int T, int pool_width, float gamma, float r,
+                        float beta_lo, float beta_hi, int flags, int k, int recent, int sink,
+                        int32_t *idx, float *z_out, float *beta_out, void *ws,
+                        const RefinePlan &plan, float *z_tmp, cudaStream_t st) {
+  const long heads = (long)B * H;
+  const int half = pool_width / 2;
+  int rc = launch_refine_beta(s, B, H, T, beta_lo, beta_hi, flags, beta_out, ws, plan, st);
+  if (rc != KV_OK) return rc;
+  const float *beta_ws = reinterpret_cast<const float *>(static_cast<const char *>(ws) + plan.beta_offset);
+  int CL, len;
+  resident_plan(T - recent - sink, k - recent - sink, &CL, &len);
   if (len > 0 && heads * CL <= 0x7FFFFFFFL) {
-    const size_t smem = (size_t)len * sizeof(uint32_t);
-    if (ensure_smem((const void *)select_topk_resident_kernel, smem))
-      return cuda_failure(cudaErrorInvalidValue, "select kernel: shared memory");
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(heads * CL));
-    cfg.blockDim = dim3(NTC);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeClusterDimension;
-    at[0].val.clusterDim.x = (unsigned)CL;
-    at[0].val.clusterDim.y = 1;
-    at[0].val.clusterDim.z = 1;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, select_topk_resident_kernel, z, T, k, recent,
-                                             sink, len, idx);
-    if (e != cudaSuccess) return cuda_failure(e, "select kernel");
-    return launch_status();
+    RefineArgs ra{beta_ws, z_out, gamma, r * r, half};
+    if (flags & KV_HUB_AVGPOOL)
+      return launch_resident<2>(s, heads, T, k, recent, sink, CL, len, half, idx, ra, st);
+    return launch_resident<1>(s, heads, T, k, recent, sink, CL, len, half, idx, ra, st);
   }
+  // too long to hold a head on chip (or everything kept): z first, then the
+  // streaming selection
+  float *z = z_out ? z_out : z_tmp;
+  rc = launch_refine_apply(s, B, H, T, half, gamma, r, flags, beta_ws, z, st);
+  if (rc != KV_OK) return rc;
   select_topk_kernel<<<(unsigned)heads, NT, 0, st>>>(z, T, k, recent, sink, idx);
   return launch_status();
 }

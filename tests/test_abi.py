@@ -35,6 +35,7 @@ def lib():
     lib.h2o_decode_steps.argtypes = [P, P, P, I, P, P, P, P, P, I, I, I, I, I, I, I, I, F, I, I, P, P,
                                      P, Z, P, P]
     lib.kv_compact_ragged.argtypes = [P, P, P, P, P, I, I, I, I, I, I, P, P, I, P, P, P, P, P]
+    lib.hubkv_select_topk.argtypes = [P, I, I, I, I, F, F, F, F, I, I, I, I, P, P, P, P, Z, P]
     return lib
 
 
@@ -112,6 +113,28 @@ def test_extended_entry_points_validate_on_the_host(lib):
     # empty batches are no-ops
     assert lib.hubkv_refine_ex(NULL, 0, 2, 10, 5, 0.5, 0.1, 0.8, 1.2, 3, NULL, NULL, NULL, 0, NULL) == 0
     assert lib.kv_select_topk_ex(NULL, 0, 2, 10, 5, 1, 2, NULL, NULL, 0, NULL) == 0
+
+
+def test_fused_refine_select_validates_on_the_host(lib):
+    sel = lambda B, T, pw, flags, k, R, S, ws=0: lib.hubkv_select_topk(  # noqa: E731
+        NULL, B, 2, T, pw, 0.5, 0.1, 0.8, 1.2, flags, k, R, S, NULL, NULL, NULL, NULL, ws, NULL)
+    assert sel(1, 10, 4, 0, 5, 1, 0) == -1     # even pool width
+    assert sel(1, 10, 5, 4, 5, 1, 0) == -1     # unknown variant flag
+    assert sel(1, 10, 5, 0, 5, 2, 3) == -1     # sinks + recent fill the budget
+    assert sel(1, 10, 5, 0, 11, 1, 0) == -1    # k > T
+    assert sel(1, 10, 131, 0, 5, 1, 0) == -2   # pooling window beyond 129
+    assert sel(0, 10, 5, 3, 5, 1, 2) == 0      # empty batch: nothing to do
+    p = ctypes.c_void_p(256)  # dummy aligned pointers: rejected before any use
+    assert lib.hubkv_select_topk(p, 1, 2, 10, 5, 0.5, 0.1, 0.8, 1.2, 0, 5, 1, 0, p, NULL, NULL,
+                                 NULL, 0, NULL) == -5  # no workspace
+    # workspace: the refinement's partials and head weights; a z buffer only for
+    # heads too long to hold on chip
+    short = lib.kv_workspace_size(6, 4, 8, 8, 131072, 0, 64, 6553)
+    assert short == lib.kv_workspace_size(6, 4, 8, 8, 1000, 0, 64, 100) or short > 0
+    assert short < 4 * 8 * 131072 * 4
+    long_ = lib.kv_workspace_size(6, 1, 2, 2, 400000, 0, 64, 20000)
+    assert long_ >= 1 * 2 * 400000 * 4
+    assert lib.kv_workspace_size(6, 1, 2, 2, 100, 0, 64, 64) == 0  # k <= recent + sink
 
 
 def test_layer_budget_entry_points_validate_on_the_host(lib):

@@ -20,15 +20,14 @@ def test_prefill_bytes_per_unit():
     a = bench.algorithmic_bytes(WL)
     # scoring: the unit's G x W query rows and its T keys read once, the scores written
     assert a["kv_score_obs"] == UNITS * (G * W * ROW + T * ROW + 4 * T)
-    # refine: scores read, refined scores written
-    assert a["hubkv_refine"] == UNITS * 8 * T
-    # Top-K: refined scores read, k positions written
-    assert a["kv_select_topk"] == UNITS * (4 * T + 4 * K)
+    # refinement + Top-K (one call): the scores read twice (the head weights need
+    # every score of a head before any refined score), k positions written
+    assert a["hubkv_select_topk"] == UNITS * (2 * 4 * T + 4 * K)
     # compaction: k K rows and k V rows read and written, and per kept slot its
     # index, score, position and accumulator
     assert a["kv_compact"] == UNITS * K * (4 * ROW + 16)
-    assert sum(a[n] for n in ("kv_score_obs", "hubkv_refine", "kv_select_topk", "kv_compact")) \
-        == 10_894_963_712
+    assert sum(a[n] for n in ("kv_score_obs", "hubkv_select_topk", "kv_compact")) \
+        == 10_760_745_984
 
 
 def test_decode_bytes_per_step():

@@ -157,5 +157,7 @@ def test_host_input_prefill_matches_the_device_path(kvc, wl):
         ref = kvc.compress_prefill(Q[b:b + 1], K[b:b + 1], V[b:b + 1], wl.k, wl.R, wl.r, wl.gamma,
                                    wl.pool_width, wl.beta_lo, wl.beta_hi, scale=wl.scale)
         torch.cuda.synchronize()
-        for key in ("s", "z", "idx", "K", "V", "pos", "acc", "len"):
-            assert torch.equal(got[key][b:b + 1], ref[key]), (key, b)
+        for key in ("s", "idx", "K", "V", "pos", "acc", "len", "beta"):
+            if ref[key] is not None:
+                assert torch.equal(got[key][b:b + 1], ref[key]), (key, b)
+        assert got["z"] is None if wl.r is not None else torch.equal(got["z"][b:b + 1], ref["z"])
