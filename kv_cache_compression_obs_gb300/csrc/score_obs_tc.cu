@@ -359,47 +359,6 @@ __device__ __forceinline__ float chunk_sum(const uint32_t *r, float c_log2, floa
   return a.x + a.y;
 }
 
-// The rare cases of the statistics fold, out of line so that the common path
-// keeps its registers: a chunk sum that could overflow against the running
-// reference m (or the first chunk, m = -inf) takes the exact maximum, and a
-// chunk that the row sees only in part (the causal edge) masks the keys at or
-// beyond jlim.  r: the chunk's N logits (a copy in local memory).
-template <int N>
-__device__ __noinline__ void stats_fold_slow(const uint32_t *r, int jb, int jlim, float c_log2, float *mz) {
-  float m = mz[0], z = mz[1];
-  const int lim = min(N, jlim - jb);  // keys of the chunk the row sees (> 0)
-  float cm = -INFINITY;
-  for (int c = 0; c < lim; ++c) cm = fmaxf(cm, __uint_as_float(r[c]));
-  const float mnew = fmaxf(m, cm * c_log2);
-  float acc = 0.f;
-  for (int c = 0; c < lim; ++c) acc += tc::ex2(fmaf(__uint_as_float(r[c]), c_log2, -mnew));
-  mz[0] = mnew;
-  mz[1] = z * tc::ex2(m - mnew) + acc;
-}
-
-// Fold the N logits of keys jb .. jb+N-1 (those below jlim are visible to the
-// row) into the row's running reference m and normaliser z.
-template <int N>
-__device__ __forceinline__ void stats_fold(const uint32_t *r, int jb, int jlim, float c_log2, float &m,
-                                           float &z) {
-  if (jb >= jlim) return;
-  if (jb + N <= jlim) {
-    // every key visible: sum against the running reference m
-    const float sum = chunk_sum<N>(r, c_log2, m);
-    if (sum <= kLazyLimit) {
-      z += sum;
-      return;
-    }
-  }
-  uint32_t tmp[N];
-#pragma unroll
-  for (int c = 0; c < N; ++c) tmp[c] = r[c];
-  float mz[2] = {m, z};
-  stats_fold_slow<N>(tmp, jb, jlim, c_log2, mz);
-  m = mz[0];
-  z = mz[1];
-}
-
 // acc2 += 2^(x_r c_log2 + m_r) over the 16 rows r of one TMEM chunk (m_r =
 // -(M_r + log2 Z_r)); MASKED: only the rows whose position is at least the key's j.
 template <bool MASKED>
@@ -525,7 +484,39 @@ __global__ void __launch_bounds__(NT, 1)
           for (int q = 0; q < 4; ++q)
             tc::tmem_ld16(col + q * 16, *reinterpret_cast<uint32_t(*)[16]>(&r[16 * q]));
           tc::tmem_ld_wait();
-          stats_fold<64>(r, j0 + chalf * 64, jlim, S.c_log2, m, z);
+          // fold the 64 logits of keys jb .. jb+63 (those below jlim are visible to
+          // the row) into the row's running reference m and normaliser z
+          const int jb = j0 + chalf * 64;
+          if (jb + 64 <= jlim) {
+            // every key visible: sum against the running reference m; only a sum
+            // large enough to risk overflow (or the first chunk, m = -inf) takes
+            // the exact-max path (inline: out of line measured 8% slower)
+            float sum = chunk_sum<64>(r, S.c_log2, m);
+            if (!(sum <= kLazyLimit)) {
+              float cm = -INFINITY;
+#pragma unroll
+              for (int c = 0; c < 64; ++c) cm = fmaxf(cm, __uint_as_float(r[c]));
+              const float mnew = fmaxf(m, cm * S.c_log2);
+              sum = chunk_sum<64>(r, S.c_log2, mnew);
+              z = z * tc::ex2(m - mnew);
+              m = mnew;
+            }
+            z += sum;
+          } else if (jb < jlim) {
+            float cm = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (jb + c < jlim) cm = fmaxf(cm, __uint_as_float(r[c]));
+            const float mnew = fmaxf(m, cm * S.c_log2);
+            float acc = 0.f;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+              const float e = tc::ex2(fmaf(__uint_as_float(r[c]), S.c_log2, -mnew));
+              acc += (jb + c < jlim) ? e : 0.f;
+            }
+            z = z * tc::ex2(m - mnew) + acc;
+            m = mnew;
+          }
         }
         tc::fence_before_sync();
         __syncwarp();

@@ -18,13 +18,18 @@
 // head h keeps exactly its middle pairs with key >= min(theta_h, tau).
 //
 // One thread-block cluster per row; CTA c of the cluster owns heads c, c+CL, ...
-//   1. floor: a radix select per owned head finds theta_h: 8-bit digits of the
-//      64-bit key, most significant first, stopping as soon as the boundary
-//      digit's bucket is taken whole (unique keys always stop by the 8th pass,
-//      distinct scores by the 4th);
-//   2. competition: the same radix select over the row's pool; each CTA
-//      histograms its own heads and sums the cluster's histograms through
-//      distributed shared memory, so every CTA takes the same decisions;
+//   1. floor: per owned head, a histogram of the keys' top 12 bits (one stream
+//      over the head's scores) finds the bin holding theta_h; a second stream
+//      gathers that bin's keys on chip, and a radix select over them alone
+//      (8-bit digits, most significant first, stopping as soon as the boundary
+//      digit's bucket is taken whole) gives theta_h exactly.  A bin too large
+//      to gather (heavy ties) falls back to the radix select over the streamed
+//      head;
+//   2. competition: the same two streams over the row's pool, the histograms
+//      summed over the cluster through distributed shared memory (every CTA
+//      reads every histogram and takes the same decisions), then the radix
+//      select over the cluster's gathered boundary-bin keys (histograms summed
+//      through distributed shared memory), with the same fallback;
 //   3. each CTA counts its heads' kept middle pairs (per warp, over a contiguous
 //      range per warp) and stores the counts into every CTA of the cluster;
 //      offsets are a prefix sum over heads;
@@ -42,12 +47,15 @@ namespace cg = cooperative_groups;
 namespace kvc {
 namespace {
 
-constexpr int NT = 1024;
+constexpr int NT = 512;
 constexpr int NW = NT / 32;
 constexpr int kMaxCluster = 8;
 constexpr int kMaxHeads = 256;
 constexpr int kMaxOwned = kMaxHeads / kMaxCluster;  // heads per CTA when H > 8
 constexpr uint64_t kNone = ~0ull;                   // above every key: selects nothing
+constexpr int kBins = 4096;                         // first digit: the key's top 12 bits
+constexpr int kBinShift = 64 - 12;
+constexpr int kListCap = 4096;                      // boundary-bin candidates held on chip
 
 struct Smem {
   RadixScratch<NT> rx;
@@ -55,7 +63,17 @@ struct Smem {
   int cnt[kMaxHeads];           // kept positions per head, written by the owners
   int offs[kMaxHeads + 1];
   int wcnt[kMaxOwned][NW];      // kept middle pairs per (owned head, warp range)
+  int wsum[NW];
+  int bin, need, above, list_n, overflow;
 };
+
+// Dynamic shared memory: the first-digit histogram and the boundary bin's
+// candidate keys (the list region also holds the cluster's summed histogram).
+struct Dyn {
+  uint32_t hist[kBins];
+  uint64_t list[kListCap];
+};
+static_assert(sizeof(uint64_t) * kListCap >= sizeof(uint32_t) * kBins, "summed histogram fits the list");
 
 // A head's middle range [0, n) split for 16-byte loads: `pre` scalars up to the
 // first 16-byte boundary, n4 float4 vectors, then the scalars from `tail` on.
@@ -72,8 +90,8 @@ __device__ __forceinline__ Split split_of(const float *zm, int n) {
 }
 
 // Calls f(key) for the middle pairs of one head, positions [S, S + n), with
-// strided coalesced 16-byte loads, four in flight per thread (64 KB per CTA:
-// enough to cover the latency of the repeated passes over L2).
+// strided coalesced 16-byte loads, four in flight per thread (32 KB per CTA,
+// two CTAs per SM).
 template <typename F>
 __device__ __forceinline__ void for_head(const float *__restrict__ zm, uint32_t flat0, int n, F &&f) {
   const Split sp = split_of(zm, n);
@@ -105,10 +123,40 @@ __device__ __forceinline__ void for_head(const float *__restrict__ zm, uint32_t 
   }
 }
 
-__global__ __launch_bounds__(NT, 1) void select_budget_kernel(
+// In a histogram of kBins counts (bins taken from the top), the bin where the
+// count of keys in it or above first reaches `need`: sm.bin, sm.need (how many of
+// that bin's keys are needed) and sm.above.  Every thread of the CTA must call.
+__device__ void find_boundary(const uint32_t *h, int need, Smem &sm) {
+  constexpr int PER = kBins / NT;
+  const int t = threadIdx.x;
+  int mine = 0;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) mine += (int)h[kBins - 1 - PER * t - i];
+  int total;
+  const int before = block_exclusive_scan<NT>(mine, sm.wsum, &total);
+  if (before < need && need <= before + mine) {
+    int acc = before;
+    for (int i = 0; i < PER; ++i) {
+      const int b = kBins - 1 - PER * t - i;
+      const int c = (int)h[b];
+      if (need <= acc + c) {
+        sm.bin = b;
+        sm.need = need - acc;
+        sm.above = acc;
+        break;
+      }
+      acc += c;
+    }
+  }
+  __syncthreads();
+}
+
+__global__ __launch_bounds__(NT, 2) void select_budget_kernel(
     const float *__restrict__ z, int H, int T, int budget, int floor_k, int R, int S,
     int32_t *__restrict__ idx_out, int32_t *__restrict__ off_out) {
   __shared__ Smem sm;
+  extern __shared__ __align__(16) unsigned char dyn_raw[];
+  Dyn &dy = *reinterpret_cast<Dyn *>(dyn_raw);
   cg::cluster_group cl = cg::this_cluster();
   const int CL = (int)cl.num_blocks();
   const int rank = (int)cl.block_rank();
@@ -122,26 +170,96 @@ __global__ __launch_bounds__(NT, 1) void select_budget_kernel(
 
   cl.sync();  // every CTA of the cluster is running before any remote access
 
-  // 1. floor thresholds of the owned heads
+  // 1. floor thresholds of the owned heads.  Two streams over the head: a
+  // histogram of the keys' top 12 bits finds the boundary bin, then the bin's
+  // keys (a few hundred for spread-out scores) are gathered on chip and the
+  // radix select runs over them alone.  A bin too large to gather (heavy ties)
+  // takes the radix select over the streamed head instead.
   for (int h = rank; h < H; h += CL) {
     uint64_t th = kNone;
-    if (nf > 0)
-      th = radix_select_ge<NT, false>(sm.rx, nf, [&](auto &&f) { for_head(zmid(h), flat0(h), n, f); });
+    if (nf > 0) {
+      for (int e = threadIdx.x; e < kBins; e += NT) dy.hist[e] = 0u;
+      __syncthreads();
+      for_head(zmid(h), flat0(h), n, [&](uint64_t key) { atomicAdd(&dy.hist[key >> kBinShift], 1u); });
+      __syncthreads();
+      find_boundary(dy.hist, nf, sm);
+      const int b = sm.bin, need = sm.need;
+      if (dy.hist[b] <= (uint32_t)kListCap) {
+        if (threadIdx.x == 0) sm.list_n = 0;
+        __syncthreads();
+        for_head(zmid(h), flat0(h), n, [&](uint64_t key) {
+          if ((int)(key >> kBinShift) == b) dy.list[atomicAdd(&sm.list_n, 1)] = key;
+        });
+        __syncthreads();
+        const int ln = sm.list_n;
+        th = radix_select_ge<NT, false>(sm.rx, need, [&](auto &&f) {
+          for (int i = threadIdx.x; i < ln; i += NT) f(dy.list[i]);
+        });
+        // the select stops at the first digit that settles the list; the lower
+        // bins' keys must stay below the threshold too
+        th = max(th, (uint64_t)b << kBinShift);
+      } else {
+        th = radix_select_ge<NT, false>(sm.rx, nf, [&](auto &&f) { for_head(zmid(h), flat0(h), n, f); });
+      }
+    }
     if (threadIdx.x == 0) sm.theta[h] = th;
+    __syncthreads();  // the histogram and the list serve the next head
   }
-  __syncthreads();
 
-  // 2. competition over the middle pairs below their head's floor threshold
+  // 2. competition over the middle pairs below their head's floor threshold: the
+  // same two streams, the histograms summed over the cluster (every CTA reads
+  // every CTA's histogram and takes the same decisions); the radix select then
+  // runs over the cluster's gathered boundary-bin keys
   uint64_t tau = kNone;
   if (extra > 0) {
-    tau = radix_select_ge<NT, true>(sm.rx, (int)extra, [&](auto &&f) {
+    for (int e = threadIdx.x; e < kBins; e += NT) dy.hist[e] = 0u;
+    __syncthreads();
+    for (int h = rank; h < H; h += CL) {
+      const uint64_t th = sm.theta[h];
+      for_head(zmid(h), flat0(h), n, [&](uint64_t key) {
+        if (key < th) atomicAdd(&dy.hist[key >> kBinShift], 1u);
+      });
+    }
+    cl.sync();  // every histogram of the cluster is complete
+    uint32_t *gs = reinterpret_cast<uint32_t *>(dy.list);  // the cluster's sum, in the list region
+    for (int e = threadIdx.x; e < kBins; e += NT) {
+      uint32_t g = 0;
+      for (int r = 0; r < CL; ++r) g += cl.map_shared_rank(dy.hist, r)[e];
+      gs[e] = g;
+    }
+    __syncthreads();
+    find_boundary(gs, (int)extra, sm);
+    const int b = sm.bin, need = sm.need;
+    if (threadIdx.x == 0) {
+      int ovf = 0;
+      for (int r = 0; r < CL; ++r) ovf |= cl.map_shared_rank(dy.hist, r)[b] > (uint32_t)kListCap;
+      sm.overflow = ovf;
+      sm.list_n = 0;
+    }
+    __syncthreads();
+    if (!sm.overflow) {
       for (int h = rank; h < H; h += CL) {
         const uint64_t th = sm.theta[h];
         for_head(zmid(h), flat0(h), n, [&](uint64_t key) {
-          if (key < th) f(key);
+          if (key < th && (int)(key >> kBinShift) == b) dy.list[atomicAdd(&sm.list_n, 1)] = key;
         });
       }
-    });
+      __syncthreads();
+      const int ln = sm.list_n;
+      tau = radix_select_ge<NT, true>(sm.rx, need, [&](auto &&f) {
+        for (int i = threadIdx.x; i < ln; i += NT) f(dy.list[i]);
+      });
+      tau = max(tau, (uint64_t)b << kBinShift);  // as for the floor thresholds
+    } else {
+      tau = radix_select_ge<NT, true>(sm.rx, (int)extra, [&](auto &&f) {
+        for (int h = rank; h < H; h += CL) {
+          const uint64_t th = sm.theta[h];
+          for_head(zmid(h), flat0(h), n, [&](uint64_t key) {
+            if (key < th) f(key);
+          });
+        }
+      });
+    }
   }
 
   // 3. kept middle pairs per owned head and warp: warp 0 takes the scalars before
@@ -266,8 +384,10 @@ int launch_select_budget(const float *z, int B, int H, int T, int budget, int fl
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((long)B * CL));
   cfg.blockDim = dim3(NT);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = sizeof(Dyn);
   cfg.stream = st;
+  if (ensure_smem((const void *)select_budget_kernel, sizeof(Dyn)))
+    return cuda_failure(cudaErrorInvalidValue, "budget selection kernel: shared memory");
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = (unsigned)CL;
