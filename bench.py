@@ -266,7 +266,8 @@ class Pipeline:
     def step(self, stream=None):
         if self.graphs is not None:
             self.graphs[0].replay()
-            self.graphs[1].replay()
+            if self.graphs[1] is not None:
+                self.graphs[1].replay()
             return
         self.prefill(stream)
         self.decode_all(stream)
@@ -287,13 +288,15 @@ class Pipeline:
             self.decode_all()
         torch.cuda.current_stream(self.dev).wait_stream(side)
         torch.cuda.synchronize(self.dev)
-        gp, gd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        gp = torch.cuda.CUDAGraph()
+        gd = torch.cuda.CUDAGraph() if self.wl.n_decode else None
         n0 = launch_count()
         with torch.cuda.graph(gp):
             self.prefill()
         n1 = launch_count()
-        with torch.cuda.graph(gd):
-            self.decode_all()
+        if gd is not None:  # a workload without decode steps has no decode graph
+            with torch.cuda.graph(gd):
+                self.decode_all()
         n2 = launch_count()
         torch.cuda.synchronize(self.dev)
         self.graphs = (gp, gd)
@@ -314,7 +317,8 @@ class Pipeline:
                      pos_out=self.pos, acc_out=self.acc, len_out=self.len)
         ev[3].record()
         if self.graphs is not None:
-            self.graphs[1].replay()
+            if self.graphs[1] is not None:
+                self.graphs[1].replay()
         else:
             self.decode_all()
         ev[4].record()
@@ -459,7 +463,7 @@ def time_workload(name, reps=5):
         e[0].record()
         gp.replay()
         e[1].record()
-        if wl.n_decode:
+        if gd is not None:
             gd.replay()
         e[2].record()
         torch.cuda.synchronize()

@@ -198,9 +198,18 @@ __global__ __launch_bounds__(NTC) void select_topk_resident_kernel(
     const float *sv = z + head * (long)T;  // here z holds the base scores s
     const int p0 = S + lo - ra.half;        // prompt position of tile[0]
     const int nt = m + 2 * ra.half;
-    for (int t = threadIdx.x; t < nt; t += NTC) {
-      const int p = p0 + t;
-      tile[t] = (p >= 0 && p < T) ? __ldg(sv + p) : -INFINITY;
+    for (int base = threadIdx.x; base < nt; base += 8 * NTC) {  // eight loads in flight a thread
+      float v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int t = base + u * NTC, p = p0 + t;
+        v[u] = (t < nt && p >= 0 && p < T) ? __ldg(sv + p) : -INFINITY;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int t = base + u * NTC;
+        if (t < nt) tile[t] = v[u];
+      }
     }
     const float beta = ra.beta[head];
     float *zo = ra.z_out ? ra.z_out + head * (long)T : nullptr;
