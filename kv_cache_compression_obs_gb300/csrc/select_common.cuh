@@ -119,9 +119,13 @@ __device__ uint64_t radix_select_ge(RadixScratch<NT> &sm, int need, Visit visit,
       // by which time every CTA has finished reading it.
       cooperative_groups::cluster_group cl = cooperative_groups::this_cluster();
       cl.sync();
+      const unsigned ncl = cl.num_blocks();
       for (int d = threadIdx.x; d < 256; d += NT) {
         uint32_t g = 0;
-        for (unsigned r = 0; r < cl.num_blocks(); ++r) g += cl.map_shared_rank(&sm.tot[buf][0], r)[d];
+#pragma unroll
+        for (unsigned r = 0; r < 8; ++r)  // independent remote loads, all in flight
+          if (r < ncl) g += cl.map_shared_rank(&sm.tot[buf][0], r)[d];
+        for (unsigned r = 8; r < ncl; ++r) g += cl.map_shared_rank(&sm.tot[buf][0], r)[d];
         sm.gsum[d] = g;
       }
     } else {

@@ -159,63 +159,105 @@ template <int MODE>
 __global__ __launch_bounds__(NTC) void select_topk_resident_kernel(
     const float *__restrict__ z, int T, int k, int R, int S, int len,
     int32_t *__restrict__ idx_out, RefineArgs ra) {
-  extern __shared__ uint32_t keys[];  // this CTA's slice of candidates, as order keys
+  extern __shared__ __align__(16) unsigned char slice_raw[];
   __shared__ ResidentSmem sm;
   cg::cluster_group cl = cg::this_cluster();
   const int CL = (int)cl.num_blocks(), rank = (int)cl.block_rank();
   const long head = blockIdx.x / CL;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int n = T - R - S, nh = k - R - S;
-  const float *zv = z + head * (long)T + S;
   int32_t *out = idx_out + head * (long)k;
   const int lo = min(n, rank * len), hi = min(n, lo + len), m = hi - lo;
-
-  // load the slice as order keys; the first radix pass (top byte) is counted here
+  const int half = MODE == 0 ? 0 : ra.half;
+  const float *row = z + head * (long)T;  // z, or the base scores s (MODE 1 / 2)
   for (int e = threadIdx.x; e < NWC * 256; e += NTC) (&sm.rx.hist[0][0])[e] = 0u;
-  if constexpr (MODE == 0) {
-    __syncthreads();
-    for (int base = threadIdx.x; base < m; base += 8 * NTC) {
-      float v[8];
+
+  // The slice with a halo of `half` on each side (-inf past the prompt's ends):
+  // tile[t] = row[p0 + t].  The tile starts `toff` floats into the buffer so
+  // that it has the global addresses' 16-byte phase: the aligned middle moves
+  // as 16-byte vectors, all in flight at once, the ragged ends as scalars.
+  // The keys then replace the tile in place (key i at or left of tile[i]).
+  const int p0 = S + lo - half, nt = m + 2 * half;
+  const int rmis = (int)((reinterpret_cast<uintptr_t>(row) >> 2) & 3);
+  const int toff = (((rmis + p0) % 4) + 4) % 4;
+  float *tile = reinterpret_cast<float *>(slice_raw) + toff;
+  uint32_t *keys = reinterpret_cast<uint32_t *>(slice_raw);
+  {
+    const int c0 = max(p0, 0), c1 = min(p0 + nt, T);
+    const int a0 = min(c1, c0 + (4 - (rmis + c0) % 4) % 4);  // first 16-byte aligned index
+    const int e0 = max(a0, c1 - (rmis + c1) % 4);            // end of the aligned run
+    const int n4 = (e0 - a0) >> 2;
+    const float4 *g4 = reinterpret_cast<const float4 *>(row + a0);
+    float4 *t4 = reinterpret_cast<float4 *>(tile + (a0 - p0));
+    for (int base = threadIdx.x; base < n4; base += 8 * NTC) {
+      float4 v[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int i = base + u * NTC;
-        v[u] = (i < m) ? __ldg(zv + lo + i) : 0.f;
+        const int j = base + u * NTC;
+        v[u] = j < n4 ? __ldg(g4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int i = base + u * NTC;
-        if (i < m) {
-          const uint32_t kk = order_key(v[u]);
-          keys[i] = kk;
-          atomicAdd(&sm.rx.hist[warp][kk >> 24], 1u);
+        const int j = base + u * NTC;
+        if (j < n4) t4[j] = v[u];
+      }
+    }
+    const int front = a0 - p0, back = p0 + nt - e0;  // tile entries before a0, from e0 on
+    for (int t = threadIdx.x; t < front + back; t += NTC) {
+      const int tt = t < front ? t : (e0 - p0) + (t - front);
+      const int p = p0 + tt;
+      tile[tt] = (p >= 0 && p < T) ? __ldg(row + p) : -INFINITY;
+    }
+  }
+
+  // z and the order keys, in batches of 8 x NTC candidates: every z of a batch
+  // is formed before any of its keys lands (later batches read only further
+  // right).  The first radix digit (the top byte) is counted here.
+  const float beta = MODE == 0 ? 0.f : ra.beta[head];
+  float *zo = (MODE != 0 && ra.z_out) ? ra.z_out + head * (long)T : nullptr;
+  auto put = [&](int i, float zi) {
+    const uint32_t kk = order_key(zi);
+    keys[i] = kk;
+    atomicAdd(&sm.rx.hist[warp][kk >> 24], 1u);
+    if (zo) zo[S + lo + i] = zi;
+  };
+  if (MODE == 1 && half == 2) {
+    // local hubs over a window of 5, four consecutive candidates a thread: the
+    // 8 scores around them give the four window maxima from shared pair maxima
+    // (the same values as hub_gate: a maximum does not depend on its order)
+    const float g = ra.gamma, r2 = ra.r2;
+    for (int base0 = 0; base0 < m; base0 += 8 * NTC) {
+      __syncthreads();
+      float v[2][4];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = base0 + 4 * (h * NTC + (int)threadIdx.x);
+        if (c < m) {
+          float w[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) w[q] = tile[c + q];  // s of candidates c-2 .. c+5
+          const float m01 = fmaxf(w[0], w[1]), m23 = fmaxf(w[2], w[3]), m45 = fmaxf(w[4], w[5]),
+                      m67 = fmaxf(w[6], w[7]);
+          const float M[4] = {fmaxf(fmaxf(m01, m23), w[4]), fmaxf(fmaxf(w[1], m23), m45),
+                              fmaxf(fmaxf(m23, m45), w[6]), fmaxf(fmaxf(w[3], m45), m67)};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float si = w[q + 2];
+            const float qi = (si == M[q]) ? si : g * si;
+            v[h][q] = fmaf(r2, fmaf(beta, qi, -si), si);
+          }
         }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = base0 + 4 * (h * NTC + (int)threadIdx.x);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (c + q < m) put(c + q, v[h][q]);
       }
     }
   } else {
-    // the slice's scores with a halo of `half` on each side (-inf past the
-    // prompt's ends), as floats in the same buffer: tile[t] = s[S + lo - half + t]
-    float *tile = reinterpret_cast<float *>(keys);
-    const float *sv = z + head * (long)T;  // here z holds the base scores s
-    const int p0 = S + lo - ra.half;        // prompt position of tile[0]
-    const int nt = m + 2 * ra.half;
-    for (int base = threadIdx.x; base < nt; base += 8 * NTC) {  // eight loads in flight a thread
-      float v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int t = base + u * NTC, p = p0 + t;
-        v[u] = (t < nt && p >= 0 && p < T) ? __ldg(sv + p) : -INFINITY;
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int t = base + u * NTC;
-        if (t < nt) tile[t] = v[u];
-      }
-    }
-    const float beta = ra.beta[head];
-    float *zo = ra.z_out ? ra.z_out + head * (long)T : nullptr;
-    // batches of 8 x NTC candidates: all z of a batch are formed before any of
-    // its keys overwrites the front of its window (key i goes to tile[i], the
-    // left end of candidate i's window; later batches read only further right)
     for (int base0 = 0; base0 < m; base0 += 8 * NTC) {
       __syncthreads();
       float v[8];
@@ -223,31 +265,30 @@ __global__ __launch_bounds__(NTC) void select_topk_resident_kernel(
       for (int u = 0; u < 8; ++u) {
         const int i = base0 + threadIdx.x + u * NTC;
         v[u] = 0.f;
-        if (i < m)
-          v[u] = hub_gate<MODE == 2>(tile + i + ra.half, ra.half, S + lo + i, T, ra.gamma, ra.r2, beta);
+        if (i < m) {
+          if constexpr (MODE == 0)
+            v[u] = tile[i];
+          else
+            v[u] = hub_gate<MODE == 2>(tile + i + half, half, S + lo + i, T, ra.gamma, ra.r2, beta);
+        }
       }
       __syncthreads();
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int i = base0 + threadIdx.x + u * NTC;
-        if (i < m) {
-          const uint32_t kk = order_key(v[u]);
-          keys[i] = kk;
-          atomicAdd(&sm.rx.hist[warp][kk >> 24], 1u);
-          if (zo) zo[S + lo + i] = v[u];
-        }
+        if (i < m) put(i, v[u]);
       }
     }
-    if (zo && rank == 0) {
-      // z of the always-kept positions (sinks and recent window) for the caller,
-      // windows read from global memory
-      for (int e = threadIdx.x; e < S + R; e += NTC) {
-        const int p = e < S ? e : T - R + (e - S);
-        float win[2 * 64 + 1];
-        for (int o = -ra.half; o <= ra.half; ++o)
-          win[o + ra.half] = (p + o >= 0 && p + o < T) ? __ldg(sv + p + o) : -INFINITY;
-        zo[p] = hub_gate<MODE == 2>(win + ra.half, ra.half, p, T, ra.gamma, ra.r2, beta);
-      }
+  }
+  if (zo && rank == 0) {
+    // z of the always-kept positions (sinks and recent window) for the caller,
+    // windows read from global memory
+    for (int e = threadIdx.x; e < S + R; e += NTC) {
+      const int p = e < S ? e : T - R + (e - S);
+      float win[2 * 64 + 1];
+      for (int o = -half; o <= half; ++o)
+        win[o + half] = (p + o >= 0 && p + o < T) ? __ldg(row + p + o) : -INFINITY;
+      zo[p] = hub_gate<MODE == 2>(win + half, half, p, T, ra.gamma, ra.r2, beta);
     }
   }
   cl.sync();  // slices loaded, and every CTA of the cluster is running
@@ -328,7 +369,7 @@ void resident_plan(int n, int nh, int *CL, int *len) {
 template <int MODE>
 int launch_resident(const float *z, long heads, int T, int k, int recent, int sink, int CL, int len,
                     int halo, int32_t *idx, const RefineArgs &ra, cudaStream_t st) {
-  const size_t smem = (size_t)(len + 2 * halo) * sizeof(uint32_t);
+  const size_t smem = ((size_t)(len + 2 * halo + 8) * sizeof(float) + 15) & ~(size_t)15;
   if (ensure_smem((const void *)select_topk_resident_kernel<MODE>, smem))
     return cuda_failure(cudaErrorInvalidValue, "select kernel: shared memory");
   cudaLaunchConfig_t cfg = {};
