@@ -17,25 +17,33 @@
 //             pairs below their head's theta_h,
 // head h keeps exactly its middle pairs with key >= min(theta_h, tau).
 //
+// Scores concentrate: a head's threshold bin of the keys' top 12 bits can hold
+// thousands of pairs and the competition's tens of thousands, so both
+// thresholds are found through a bucket of the keys' top 20 bits (a 12-bit
+// histogram, then an 8-bit one inside the boundary bin), whose pairs (tens to
+// hundreds) are gathered on chip for an exact radix select.
+//
 // One thread-block cluster per row; CTA c of the cluster owns heads c, c+CL, ...
-//   1. floor: per owned head, a histogram of the keys' top 12 bits (one stream
-//      over the head's scores) finds the bin holding theta_h; a second stream
-//      gathers that bin's keys on chip, and a radix select over them alone
-//      (8-bit digits, most significant first, stopping as soon as the boundary
-//      digit's bucket is taken whole) gives theta_h exactly.  A bin too large
-//      to gather (heavy ties) falls back to the radix select over the streamed
-//      head;
-//   2. competition: the same two streams over the row's pool, the histograms
-//      summed over the cluster through distributed shared memory (every CTA
-//      reads every histogram and takes the same decisions), then the radix
-//      select over the cluster's gathered boundary-bin keys (histograms summed
-//      through distributed shared memory), with the same fallback;
-//   3. each CTA counts its heads' kept middle pairs (per warp, over a contiguous
-//      range per warp) and stores the counts into every CTA of the cluster;
-//      offsets are a prefix sum over heads;
+//   1. floor, per owned head, three streams over its scores: the 12-bit
+//      histogram; the 8-bit one inside the boundary bin; the gather of the
+//      boundary bucket's pairs, counting per warp range the pairs above it.
+//      theta_h follows from the bucket's pairs.  The competition's 12-bit
+//      histogram (pairs below theta_h) follows from the same counts without
+//      another stream;
+//   2. competition: the 12-bit histograms summed over the cluster through
+//      distributed shared memory give tau's bin; one stream per owned head
+//      counts that bin's second digits (pairs below theta_h), summed over the
+//      cluster; one more stream gathers the bucket's pairs and counts per warp
+//      range the pairs above it; every CTA selects tau from the cluster's
+//      gathered pairs, read in place through distributed shared memory;
+//   3. the kept middle pairs per (owned head, warp range) follow from the
+//      counts of step 1 (head limited by theta_h) or of step 2 (by tau); they
+//      go to every CTA of the cluster, and offsets are a prefix sum over heads;
 //   4. each owned head writes its sinks, its kept middle positions (warp
 //      ballots over the same ranges keep them ascending) and its recent window
 //      at its offset.
+// A bucket too large to gather (heavy ties) falls back to a radix select over
+// the streamed pairs, and the kept counts to a counting stream.
 // Integer work only after the key transform: the same z gives the same output.
 #include <cooperative_groups.h>
 
@@ -55,25 +63,35 @@ constexpr int kMaxOwned = kMaxHeads / kMaxCluster;  // heads per CTA when H > 8
 constexpr uint64_t kNone = ~0ull;                   // above every key: selects nothing
 constexpr int kBins = 4096;                         // first digit: the key's top 12 bits
 constexpr int kBinShift = 64 - 12;
-constexpr int kListCap = 4096;                      // boundary-bin candidates held on chip
+constexpr int kSubShift = kBinShift - 8;            // second digit; a bucket is the top 20 bits
+constexpr int kListCap = 2048;                      // bucket pairs held on chip per CTA
 
 struct Smem {
   RadixScratch<NT> rx;
-  uint64_t theta[kMaxHeads];    // floor thresholds (owned heads' entries only)
-  int cnt[kMaxHeads];           // kept positions per head, written by the owners
+  uint64_t theta[kMaxHeads];   // floor thresholds of every head of the row (pushed by owners)
+  int cnt[kMaxHeads];          // kept positions per head, written by the owners
   int offs[kMaxHeads + 1];
-  int wcnt[kMaxOwned][NW];      // kept middle pairs per (owned head, warp range)
+  int wcnt[kMaxOwned][NW];     // kept middle pairs per (owned head, warp range)
+  int wth[kMaxOwned][NW];      // middle pairs >= theta_h per (owned head, warp range)
+  int wtau[kMaxOwned][NW];     // middle pairs above tau's bucket per (owned head, warp range)
+  int thok[kMaxOwned];         // wth holds the counts
+  uint32_t h8[256];            // second-digit histogram of one bin
+  uint32_t g8[256];            // the cluster's sum of it (competition)
+  uint32_t h256[256];          // digit histogram of the selects inside a bucket
   int wsum[NW];
-  int bin, need, above, list_n, overflow;
+  int lnr[kMaxCluster];        // competition bucket pairs held per CTA (pushed)
+  int ovr[kMaxCluster];        // competition bucket overflowed per CTA (pushed)
+  int bin, need, above, list_n, red;
 };
 
-// Dynamic shared memory: the first-digit histogram and the boundary bin's
-// candidate keys (the list region also holds the cluster's summed histogram).
+// Dynamic shared memory: the 12-bit histogram (also the cluster's summed
+// competition histogram), the competition's 12-bit histogram of this CTA,
+// and the gathered bucket pairs.
 struct Dyn {
   uint32_t hist[kBins];
+  uint32_t comp[kBins];
   uint64_t list[kListCap];
 };
-static_assert(sizeof(uint64_t) * kListCap >= sizeof(uint32_t) * kBins, "summed histogram fits the list");
 
 // A head's middle range [0, n) split for 16-byte loads: `pre` scalars up to the
 // first 16-byte boundary, n4 float4 vectors, then the scalars from `tail` on.
@@ -89,22 +107,30 @@ __device__ __forceinline__ Split split_of(const float *zm, int n) {
   return sp;
 }
 
+// Warp ranges of a head: warp 0 takes the scalars before the first 16-byte
+// boundary, every warp a contiguous run of per4 float4 vectors, the last warp
+// the scalar tail.  The warp whose range holds middle position i:
+__device__ __forceinline__ int warp_of(int i, const Split &sp, int per4) {
+  if (i < sp.pre) return 0;
+  if (i >= sp.tail) return NW - 1;
+  return ((i - sp.pre) >> 2) / per4;
+}
+
 // Calls f(key) for the middle pairs of one head, positions [S, S + n), with
-// strided coalesced 16-byte loads, four in flight per thread (32 KB per CTA,
-// two CTAs per SM).
+// strided coalesced 16-byte loads, eight in flight per thread.
 template <typename F>
 __device__ __forceinline__ void for_head(const float *__restrict__ zm, uint32_t flat0, int n, F &&f) {
   const Split sp = split_of(zm, n);
   const float4 *z4 = reinterpret_cast<const float4 *>(zm + sp.pre);
-  for (int base = threadIdx.x; base < sp.n4; base += 4 * NT) {
-    float4 v[4];
+  for (int base = threadIdx.x; base < sp.n4; base += 8 * NT) {
+    float4 v[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 8; ++u) {
       const int j = base + u * NT;
       v[u] = (j < sp.n4) ? __ldg(z4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 8; ++u) {
       const int j = base + u * NT;
       if (j < sp.n4) {
         const uint32_t i = flat0 + (uint32_t)(sp.pre + 4 * j);
@@ -121,6 +147,39 @@ __device__ __forceinline__ void for_head(const float *__restrict__ zm, uint32_t 
     const int i = sp.tail + (t - sp.pre);
     f(pair_key(__ldg(zm + i), flat0 + (uint32_t)i));
   }
+}
+
+// Calls f(key) for the middle pairs of this warp's range (see warp_of), four
+// 16-byte loads in flight per lane.
+template <typename F>
+__device__ __forceinline__ void for_warp(const float *__restrict__ zm, uint32_t flat0, int n, F &&f) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Split sp = split_of(zm, n);
+  const float4 *z4 = reinterpret_cast<const float4 *>(zm + sp.pre);
+  const int per4 = (sp.n4 + NW - 1) / NW;
+  const int b0 = min(sp.n4, warp * per4), b1 = min(sp.n4, b0 + per4);
+  if (warp == 0 && lane < sp.pre) f(pair_key(__ldg(zm + lane), flat0 + (uint32_t)lane));
+  for (int q0 = b0 + lane; q0 < b1; q0 += 4 * 32) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int q = q0 + 32 * u;
+      v[u] = q < b1 ? __ldg(z4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int q = q0 + 32 * u;
+      if (q < b1) {
+        const uint32_t i = flat0 + (uint32_t)(sp.pre + 4 * q);
+        f(pair_key(v[u].x, i));
+        f(pair_key(v[u].y, i + 1));
+        f(pair_key(v[u].z, i + 2));
+        f(pair_key(v[u].w, i + 3));
+      }
+    }
+  }
+  if (warp == NW - 1 && lane < n - sp.tail)
+    f(pair_key(__ldg(zm + sp.tail + lane), flat0 + (uint32_t)(sp.tail + lane)));
 }
 
 // In a histogram of kBins counts (bins taken from the top), the bin where the
@@ -151,6 +210,44 @@ __device__ void find_boundary(const uint32_t *h, int need, Smem &sm) {
   __syncthreads();
 }
 
+// Exact threshold inside one bucket (the keys' top 20 bits fixed to those of
+// `prefix`): the key with exactly `need` of the visited bucket keys at or above
+// it.  8-bit digits below the bucket's bits, stopping once a digit's bucket is
+// taken whole; keys are unique, so the last digit always settles it.  visit(f)
+// calls f(key) for every candidate this thread owns (keys outside the bucket
+// are ignored).  Every thread of the CTA must call.
+template <typename Visit>
+__device__ uint64_t select_in_bucket(Smem &sm, uint64_t prefix, int need, Visit visit) {
+  const int warp = threadIdx.x >> 5;
+  uint64_t hmask = ~0ull << kSubShift;
+  for (int shift = kSubShift - 8;; shift -= 8) {
+    const int sh = max(shift, 0);
+    const uint32_t dmask = shift >= 0 ? 255u : (255u >> -shift);
+    for (int d = threadIdx.x; d < 256; d += NT) sm.h256[d] = 0u;
+    __syncthreads();
+    visit([&](uint64_t key) {
+      if ((key & hmask) == prefix) atomicAdd(&sm.h256[(uint32_t)(key >> sh) & dmask], 1u);
+    });
+    __syncthreads();
+    if (warp == 0) digit_boundary<NT>(sm.h256, need, prefix, sh, sm.rx);
+    __syncthreads();
+    prefix = sm.rx.sh_prefix;
+    need = sm.rx.sh_need;
+    hmask |= (uint64_t)dmask << sh;
+    const int done = sm.rx.sh_done;
+    __syncthreads();  // h256 and sh_* are rewritten by the next digit
+    if (done || sh == 0) break;
+  }
+  return prefix;
+}
+
+// Sum over the block of one int per thread (every thread gets it).
+__device__ __forceinline__ int block_sum(int v, Smem &sm) {
+  int total;
+  block_exclusive_scan<NT>(v, sm.wsum, &total);
+  return total;
+}
+
 __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
     const float *__restrict__ z, int H, int T, int budget, int floor_k, int R, int S,
     int32_t *__restrict__ idx_out, int32_t *__restrict__ off_out) {
@@ -167,89 +264,184 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
   const float *zrow = z + row * (long)H * T;
   auto zmid = [&](int h) { return zrow + (long)h * T + S; };
   auto flat0 = [&](int h) { return (uint32_t)h * (uint32_t)T + (uint32_t)S; };
+  // head and middle position of a pair key
+  auto head_of = [&](uint64_t key) { return (int)((0xFFFFFFFFu - (uint32_t)key) / (uint32_t)T); };
+  auto pos_of = [&](uint64_t key) {
+    const uint32_t flat = 0xFFFFFFFFu - (uint32_t)key;
+    return (int)(flat % (uint32_t)T) - S;
+  };
 
+  for (int e = threadIdx.x; e < kBins; e += NT) dy.comp[e] = 0u;
   cl.sync();  // every CTA of the cluster is running before any remote access
 
-  // 1. floor thresholds of the owned heads.  Two streams over the head: a
-  // histogram of the keys' top 12 bits finds the boundary bin, then the bin's
-  // keys (a few hundred for spread-out scores) are gathered on chip and the
-  // radix select runs over them alone.  A bin too large to gather (heavy ties)
-  // takes the radix select over the streamed head instead.
-  for (int h = rank; h < H; h += CL) {
+  // 1. floor thresholds of the owned heads, and the competition's 12-bit counts
+  for (int h = rank, j = 0; h < H; h += CL, ++j) {
+    const float *zm = zmid(h);
+    const uint32_t f0 = flat0(h);
+    const Split sp = split_of(zm, n);
+    const int per4 = max(1, (sp.n4 + NW - 1) / NW);
     uint64_t th = kNone;
+    int ok = 1;  // wth[j] holds the per-warp counts of pairs >= th
+    for (int e = threadIdx.x; e < kBins; e += NT) dy.hist[e] = 0u;
+    if (threadIdx.x < NW) sm.wth[j][threadIdx.x] = 0;
+    __syncthreads();
+    for_head(zm, f0, n, [&](uint64_t key) { atomicAdd(&dy.hist[key >> kBinShift], 1u); });
+    __syncthreads();
+    int b1 = kBins, d2 = 0;  // theta_h's bin and second digit (b1 = kBins: no floor)
+    int below_in_b1 = 0;     // pairs of bin b1 below theta_h
     if (nf > 0) {
-      for (int e = threadIdx.x; e < kBins; e += NT) dy.hist[e] = 0u;
-      __syncthreads();
-      for_head(zmid(h), flat0(h), n, [&](uint64_t key) { atomicAdd(&dy.hist[key >> kBinShift], 1u); });
-      __syncthreads();
       find_boundary(dy.hist, nf, sm);
-      const int b = sm.bin, need = sm.need;
-      if (dy.hist[b] <= (uint32_t)kListCap) {
+      b1 = sm.bin;
+      const int need1 = sm.need;
+      for (int d = threadIdx.x; d < 256; d += NT) sm.h8[d] = 0u;
+      __syncthreads();
+      for_head(zm, f0, n, [&](uint64_t key) {
+        if ((int)(key >> kBinShift) == b1) atomicAdd(&sm.h8[(uint32_t)(key >> kSubShift) & 255u], 1u);
+      });
+      __syncthreads();
+      if (warp == 0) digit_boundary<NT>(sm.h8, need1, (uint64_t)b1 << kBinShift, kSubShift, sm.rx);
+      __syncthreads();
+      const uint64_t pb = sm.rx.sh_prefix;  // the bucket: its top 20 bits, zeros below
+      const int need2 = sm.rx.sh_need;
+      d2 = (int)((pb >> kSubShift) & 255u);
+      const uint32_t p20 = (uint32_t)(pb >> kSubShift);
+      // pairs of the bin below the bucket (all below theta_h)
+      {
+        int c = 0;
+        for (int d = threadIdx.x; d < d2; d += NT) c += (int)sm.h8[d];
+        below_in_b1 = block_sum(c, sm);
+      }
+      if (sm.h8[d2] <= (uint32_t)kListCap) {
         if (threadIdx.x == 0) sm.list_n = 0;
         __syncthreads();
-        for_head(zmid(h), flat0(h), n, [&](uint64_t key) {
-          if ((int)(key >> kBinShift) == b) dy.list[atomicAdd(&sm.list_n, 1)] = key;
+        int c = 0;
+        for_warp(zm, f0, n, [&](uint64_t key) {
+          const uint32_t pk = (uint32_t)(key >> kSubShift);
+          c += pk > p20;
+          if (pk == p20) dy.list[atomicAdd(&sm.list_n, 1)] = key;
         });
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
+        if (lane == 0) sm.wth[j][warp] = c;
         __syncthreads();
         const int ln = sm.list_n;
-        th = radix_select_ge<NT, false>(sm.rx, need, [&](auto &&f) {
+        th = select_in_bucket(sm, pb, need2, [&](auto &&f) {
           for (int i = threadIdx.x; i < ln; i += NT) f(dy.list[i]);
         });
-        // the select stops at the first digit that settles the list; the lower
-        // bins' keys must stay below the threshold too
-        th = max(th, (uint64_t)b << kBinShift);
+        th = max(th, pb);  // the select stops at the first digit that settles the bucket
+        int cb = 0;
+        for (int i = threadIdx.x; i < ln; i += NT) {
+          const uint64_t key = dy.list[i];
+          if (key >= th) atomicAdd(&sm.wth[j][warp_of(pos_of(key), sp, per4)], 1);
+          else ++cb;
+        }
+        below_in_b1 += block_sum(cb, sm);
       } else {
-        th = radix_select_ge<NT, false>(sm.rx, nf, [&](auto &&f) { for_head(zmid(h), flat0(h), n, f); });
+        th = radix_select_ge<NT, false>(sm.rx, nf, [&](auto &&f) { for_head(zm, f0, n, f); });
+        ok = 0;
       }
     }
-    if (threadIdx.x == 0) sm.theta[h] = th;
-    __syncthreads();  // the histogram and the list serve the next head
-  }
-
-  // 2. competition over the middle pairs below their head's floor threshold: the
-  // same two streams, the histograms summed over the cluster (every CTA reads
-  // every CTA's histogram and takes the same decisions); the radix select then
-  // runs over the cluster's gathered boundary-bin keys
-  uint64_t tau = kNone;
-  if (extra > 0) {
-    for (int e = threadIdx.x; e < kBins; e += NT) dy.hist[e] = 0u;
-    __syncthreads();
-    for (int h = rank; h < H; h += CL) {
-      const uint64_t th = sm.theta[h];
-      for_head(zmid(h), flat0(h), n, [&](uint64_t key) {
-        if (key < th) atomicAdd(&dy.hist[key >> kBinShift], 1u);
+    if (threadIdx.x < CL) cl.map_shared_rank(sm.theta, threadIdx.x)[h] = th;
+    if (threadIdx.x == 0) sm.thok[j] = ok;
+    // the competition's 12-bit counts: this head's pairs below theta_h
+    if (ok) {
+      for (int e = threadIdx.x; e < kBins; e += NT)
+        if (e < b1) dy.comp[e] += dy.hist[e];
+        else if (e == b1) dy.comp[e] += (uint32_t)below_in_b1;
+    } else {
+      __syncthreads();  // hist is read above; the streamed count adds to comp
+      for_head(zm, f0, n, [&](uint64_t key) {
+        if (key < th) atomicAdd(&dy.comp[key >> kBinShift], 1u);
       });
     }
-    cl.sync();  // every histogram of the cluster is complete
-    uint32_t *gs = reinterpret_cast<uint32_t *>(dy.list);  // the cluster's sum, in the list region
+    __syncthreads();  // hist, h8 and the list serve the next head
+  }
+  cl.sync();  // every theta and every competition histogram of the cluster complete
+
+  // 2. competition over the middle pairs below their head's floor threshold
+  uint64_t tau = kNone;
+  int tau_ok = 0;  // wtau and the list hold tau's counts
+  if (extra > 0) {
+    uint32_t *gs = dy.hist;  // the cluster's sum
     for (int e = threadIdx.x; e < kBins; e += NT) {
       uint32_t g = 0;
-      for (int r = 0; r < CL; ++r) g += cl.map_shared_rank(dy.hist, r)[e];
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r)
+        if (r < CL) g += cl.map_shared_rank(dy.comp, r)[e];
       gs[e] = g;
     }
     __syncthreads();
     find_boundary(gs, (int)extra, sm);
-    const int b = sm.bin, need = sm.need;
-    if (threadIdx.x == 0) {
-      int ovf = 0;
-      for (int r = 0; r < CL; ++r) ovf |= cl.map_shared_rank(dy.hist, r)[b] > (uint32_t)kListCap;
-      sm.overflow = ovf;
-      sm.list_n = 0;
+    const int bt = sm.bin, needt1 = sm.need;
+    // second digits of tau's bin, pairs below their head's theta
+    for (int d = threadIdx.x; d < 256; d += NT) sm.h8[d] = 0u;
+    __syncthreads();
+    for (int h = rank; h < H; h += CL) {
+      const uint64_t th = sm.theta[h];
+      if (th != kNone && (int)(th >> kBinShift) < bt) continue;  // nothing below theta in that bin
+      for_head(zmid(h), flat0(h), n, [&](uint64_t key) {
+        if ((int)(key >> kBinShift) == bt && key < th)
+          atomicAdd(&sm.h8[(uint32_t)(key >> kSubShift) & 255u], 1u);
+      });
+    }
+    cl.sync();  // every second-digit histogram complete
+    for (int d = threadIdx.x; d < 256; d += NT) {
+      uint32_t g = 0;
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r)
+        if (r < CL) g += cl.map_shared_rank(sm.h8, r)[d];
+      sm.g8[d] = g;
     }
     __syncthreads();
-    if (!sm.overflow) {
-      for (int h = rank; h < H; h += CL) {
-        const uint64_t th = sm.theta[h];
-        for_head(zmid(h), flat0(h), n, [&](uint64_t key) {
-          if (key < th && (int)(key >> kBinShift) == b) dy.list[atomicAdd(&sm.list_n, 1)] = key;
-        });
-      }
-      __syncthreads();
-      const int ln = sm.list_n;
-      tau = radix_select_ge<NT, true>(sm.rx, need, [&](auto &&f) {
-        for (int i = threadIdx.x; i < ln; i += NT) f(dy.list[i]);
+    if (warp == 0) digit_boundary<NT>(sm.g8, needt1, (uint64_t)bt << kBinShift, kSubShift, sm.rx);
+    __syncthreads();
+    const uint64_t pt = sm.rx.sh_prefix;
+    const int needt2 = sm.rx.sh_need;
+    const uint32_t p20 = (uint32_t)(pt >> kSubShift);
+    // every pair of the bucket (kept by its floor or not), and per warp range the
+    // pairs above the bucket
+    if (threadIdx.x == 0) sm.list_n = 0;
+    __syncthreads();
+    for (int h = rank, j = 0; h < H; h += CL, ++j) {
+      int c = 0;
+      for_warp(zmid(h), flat0(h), n, [&](uint64_t key) {
+        const uint32_t pk = (uint32_t)(key >> kSubShift);
+        c += pk > p20;
+        if (pk == p20) {
+          const int slot = atomicAdd(&sm.list_n, 1);
+          if (slot < kListCap) dy.list[slot] = key;
+        }
       });
-      tau = max(tau, (uint64_t)b << kBinShift);  // as for the floor thresholds
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
+      if (lane == 0) sm.wtau[j][warp] = c;
+    }
+    __syncthreads();
+    if (threadIdx.x < CL) {
+      cl.map_shared_rank(sm.lnr, threadIdx.x)[rank] = min(sm.list_n, kListCap);
+      cl.map_shared_rank(sm.ovr, threadIdx.x)[rank] = sm.list_n > kListCap;
+    }
+    cl.sync();  // every bucket list complete
+    int ovf = 0, ltot = 0;
+    for (int r = 0; r < CL; ++r) {
+      ovf |= sm.ovr[r];
+      ltot += sm.lnr[r];
+    }
+    if (!ovf) {
+      // the lists as one sequence, rank by rank, read in place
+      auto list_at = [&](int q) {
+        int r = 0;
+        while (q >= sm.lnr[r]) q -= sm.lnr[r++];
+        return cl.map_shared_rank(dy.list, r)[q];
+      };
+      tau = select_in_bucket(sm, pt, needt2, [&](auto &&f) {
+        for (int q = threadIdx.x; q < ltot; q += NT) {
+          const uint64_t key = list_at(q);
+          if (key < sm.theta[head_of(key)]) f(key);
+        }
+      });
+      tau = max(tau, pt);  // as for the floor thresholds
+      tau_ok = 1;
     } else {
       tau = radix_select_ge<NT, true>(sm.rx, (int)extra, [&](auto &&f) {
         for (int h = rank; h < H; h += CL) {
@@ -262,31 +454,33 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
     }
   }
 
-  // 3. kept middle pairs per owned head and warp: warp 0 takes the scalars before
-  // the first 16-byte boundary, every warp a contiguous run of float4 vectors,
-  // the last warp the scalar tail; counts to every CTA of the cluster
+  // 3. kept middle pairs per owned head and warp range; counts to every CTA
   for (int h = rank, j = 0; h < H; h += CL, ++j) {
-    const uint64_t lam = min(sm.theta[h], tau);
+    const uint64_t th = sm.theta[h];
+    const uint64_t lam = min(th, tau);
     const float *zm = zmid(h);
     const uint32_t f0 = flat0(h);
     const Split sp = split_of(zm, n);
-    const float4 *z4 = reinterpret_cast<const float4 *>(zm + sp.pre);
-    const int per4 = (sp.n4 + NW - 1) / NW;
-    const int b0 = min(sp.n4, warp * per4), b1 = min(sp.n4, b0 + per4);
-    int c = 0;
-    if (warp == 0 && lane < sp.pre) c += pair_key(__ldg(zm + lane), f0 + (uint32_t)lane) >= lam;
-#pragma unroll 4
-    for (int q = b0 + lane; q < b1; q += 32) {
-      const float4 v = __ldg(z4 + q);
-      const uint32_t i = f0 + (uint32_t)(sp.pre + 4 * q);
-      c += (pair_key(v.x, i) >= lam) + (pair_key(v.y, i + 1) >= lam) +
-           (pair_key(v.z, i + 2) >= lam) + (pair_key(v.w, i + 3) >= lam);
-    }
-    if (warp == NW - 1 && lane < n - sp.tail)
-      c += pair_key(__ldg(zm + sp.tail + lane), f0 + (uint32_t)(sp.tail + lane)) >= lam;
+    const int per4 = max(1, (sp.n4 + NW - 1) / NW);
+    if (lam == th && sm.thok[j]) {
+      if (threadIdx.x < NW) sm.wcnt[j][threadIdx.x] = sm.wth[j][threadIdx.x];
+      __syncthreads();
+    } else if (lam == tau && tau_ok) {
+      if (threadIdx.x < NW) sm.wcnt[j][threadIdx.x] = sm.wtau[j][threadIdx.x];
+      __syncthreads();
+      const int ln = min(sm.list_n, kListCap);
+      for (int i = threadIdx.x; i < ln; i += NT) {
+        const uint64_t key = dy.list[i];
+        if (head_of(key) == h && key >= lam) atomicAdd(&sm.wcnt[j][warp_of(pos_of(key), sp, per4)], 1);
+      }
+    } else {
+      // a counting stream over the warp ranges
+      int c = 0;
+      for_warp(zm, f0, n, [&](uint64_t key) { c += key >= lam; });
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
-    if (lane == 0) sm.wcnt[j][warp] = c;
+      for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
+      if (lane == 0) sm.wcnt[j][warp] = c;
+    }
     __syncthreads();
     if (threadIdx.x < CL) {
       int tot = 0;

@@ -61,6 +61,40 @@ struct RadixScratch {
   int sh_need, sh_done;
 };
 
+// Warp 0 of the block: in a 256-digit histogram h taken from the top, the digit
+// where the count at or above it first reaches `need`.  Writes sm.sh_prefix
+// (prefix with that digit at `shift`), sm.sh_need (how many of the digit's keys
+// are needed) and sm.sh_done (whether that is all of them).
+template <int NT>
+__device__ __forceinline__ void digit_boundary(const uint32_t *h, int need, uint64_t prefix, int shift,
+                                               RadixScratch<NT> &sm) {
+  const int lane = threadIdx.x & 31;
+  uint32_t mine = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) mine += h[255 - 8 * lane - i];  // lane l: digits 255-8l .. 248-8l
+  uint32_t incl = mine;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  uint32_t above = incl - mine;
+  if (above < (uint32_t)need && (uint32_t)need <= incl) {
+#pragma unroll 1
+    for (int i = 0; i < 8; ++i) {
+      const int dgt = 255 - 8 * lane - i;
+      const uint32_t c = h[dgt];
+      if ((uint32_t)need <= above + c) {
+        sm.sh_prefix = prefix | ((uint64_t)dgt << shift);
+        sm.sh_need = need - (int)above;
+        sm.sh_done = ((uint32_t)need == above + c);
+        break;
+      }
+      above += c;
+    }
+  }
+}
+
 // Threshold thr such that exactly `need` candidate keys are >= thr, for unique
 // 64-bit keys and 1 <= need <= number of candidates.  visit(f) calls f(key) for
 // every candidate key this thread owns.  8-bit digits, most significant first;
