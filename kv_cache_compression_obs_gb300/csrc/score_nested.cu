@@ -25,7 +25,8 @@
 //      MB) are protected, so the re-reads hit L2 instead of HBM.  Packed f32x2
 //      arithmetic throughout.  Writes a_c.
 //   2. global_kernel: same grid; adds the unit's block sums into the stable
-//      anchor, re-reads the block's keys and writes a_s and a_e.
+//      anchor, re-reads the block's keys (four lanes per key, the anchors'
+//      slices in registers) and writes a_s and a_e.
 //   3. disc_kernel: one CTA per (unit, scale): radix selects (order-preserving
 //      32-bit keys) of the n_disc-th largest and smallest a_k sharing every pass,
 //      then the two sums.
@@ -324,15 +325,25 @@ __global__ __launch_bounds__(NT_SCAN) void anchors_kernel(const T *__restrict__ 
 }
 
 // ---- 2. stable and episodic anchors ----------------------------------------------
+// Four lanes per key: lane q of a group reads the 16-byte pieces q, q+4, q+8, ...
+// of its key (each load of the group covers whole 32-byte sectors of one row),
+// keeps the matching slices of S and E in registers for the whole scan, and the
+// group adds its four partial <k, S>, <k, E> and |k|^2 with two shuffles.  A
+// warp takes 8 keys a step; the next step's loads are issued before this
+// step's arithmetic.
 template <typename T, int D>
 __global__ __launch_bounds__(NT_SCAN) void global_kernel(const T *__restrict__ K, int Tn, int blk,
                                                          int n_blocks,
                                                          const float *__restrict__ esum,
                                                          float *__restrict__ a) {
-  using R = Row<T, D>;
-  constexpr int P2 = R::P2;
+  constexpr int NC = D * (int)sizeof(T) / 64;  // 16-byte pieces per lane
+  constexpr int FC = 16 / (int)sizeof(T);      // features per piece
+  constexpr int FS = 64 / (int)sizeof(T);      // feature stride between a lane's pieces
+  constexpr int FL = NC * FC;                  // features per lane
   __shared__ float S[D], E[D];
+  __shared__ float nrm[2];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int q = lane & 3, g = lane >> 2;
   const long unit = blockIdx.x / n_blocks;
   const int bj = blockIdx.x % n_blocks;
   const int lo = min(Tn, bj * blk), hi = min(Tn, lo + blk);
@@ -344,75 +355,78 @@ __global__ __launch_bounds__(NT_SCAN) void global_kernel(const T *__restrict__ K
     E[f] = eu[(long)bj * D + f];
   }
   __syncthreads();
-  // anchor norms (every warp computes both)
-  float ns = 0.f, ne = 0.f;
-  for (int f = lane; f < D; f += 32) {
-    ns = fmaf(S[f], S[f], ns);
-    ne = fmaf(E[f], E[f], ne);
-  }
+  if (warp == 0) {  // anchor norms
+    float ns = 0.f, ne = 0.f;
+    for (int f = lane; f < D; f += 32) {
+      ns = fmaf(S[f], S[f], ns);
+      ne = fmaf(E[f], E[f], ne);
+    }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    ns += __shfl_xor_sync(0xFFFFFFFFu, ns, o);
-    ne += __shfl_xor_sync(0xFFFFFFFFu, ne, o);
+    for (int o = 16; o > 0; o >>= 1) {
+      ns += __shfl_xor_sync(0xFFFFFFFFu, ns, o);
+      ne += __shfl_xor_sync(0xFFFFFFFFu, ne, o);
+    }
+    if (lane == 0) {
+      nrm[0] = ns > 0.f ? rsqrtf(ns) : 0.f;
+      nrm[1] = ne > 0.f ? rsqrtf(ne) : 0.f;
+    }
   }
-  const float rS = ns > 0.f ? rsqrtf(ns) : 0.f, rE = ne > 0.f ? rsqrtf(ne) : 0.f;
-  float2 sl[P2], el[P2];
+  __syncthreads();
+  const float rS = nrm[0], rE = nrm[1];
+  float2 sv[FL / 2], ev[FL / 2];  // this lane's slices of S and E, as pairs
 #pragma unroll
-  for (int p = 0; p < P2; ++p) {
-    sl[p] = make_float2(S[lane * 2 * P2 + 2 * p], S[lane * 2 * P2 + 2 * p + 1]);
-    el[p] = make_float2(E[lane * 2 * P2 + 2 * p], E[lane * 2 * P2 + 2 * p + 1]);
-  }
-  const uint64_t pol = tc::make_policy_evict_first();
-  const T *Ku = K + unit * (long)Tn * D;
+  for (int c = 0; c < NC; ++c)
+#pragma unroll
+    for (int e = 0; e < FC / 2; ++e) {
+      const int f = c * FS + q * FC + 2 * e;
+      sv[c * (FC / 2) + e] = make_float2(S[f], S[f + 1]);
+      ev[c * (FC / 2) + e] = make_float2(E[f], E[f + 1]);
+    }
+  const char *Ku = reinterpret_cast<const char *>(K + unit * (long)Tn * D);
   float *as = a + (unit * 3 + 0) * (long)Tn;
   float *ae = a + (unit * 3 + 1) * (long)Tn;
-  int s, e;
-  warp_range(lo, hi, warp, s, e);
-  // rows past e load an in-range row instead (never written out); the next
-  // batch's rows are loaded before this batch is reduced, so two batches of
-  // loads are in flight per warp
-  float2 xn[4][P2];
-  if (s < e) {
+  auto load = [&](int t0, uint4 (&w)[NC]) {
+    const uint4 *row = reinterpret_cast<const uint4 *>(Ku + (long)min(t0 + g, hi - 1) * (D * (int)sizeof(T)));
 #pragma unroll
-    for (int t = 0; t < 4; ++t) R::load(Ku + (long)min(s + t, e - 1) * D, lane, pol, xn[t]);
-  }
-  for (int i0 = s; i0 < e; i0 += 4) {
-    float2 x[4][P2];
+    for (int c = 0; c < NC; ++c) w[c] = __ldg(row + 4 * c + q);
+  };
+  const int step = 8 * NWARP;
+  int t0 = lo + 8 * warp;
+  uint4 wn[NC];
+  if (t0 < hi) load(t0, wn);
+  for (; t0 < hi; t0 += step) {
+    uint4 w[NC];
 #pragma unroll
-    for (int t = 0; t < 4; ++t)
+    for (int c = 0; c < NC; ++c) w[c] = wn[c];
+    if (t0 + step < hi) load(t0 + step, wn);
+    float2 ds = make_float2(0.f, 0.f), de = ds, nk = ds;
 #pragma unroll
-      for (int p = 0; p < P2; ++p) x[t][p] = xn[t][p];
-    if (i0 + 4 < e) {
+    for (int c = 0; c < NC; ++c) {
+      const uint32_t u[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
 #pragma unroll
-      for (int t = 0; t < 4; ++t) R::load(Ku + (long)min(i0 + 4 + t, e - 1) * D, lane, pol, xn[t]);
-    }
-    float part[16];
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      float2 ds = __fmul2_rn(x[t][0], sl[0]), de = __fmul2_rn(x[t][0], el[0]),
-             nk = __fmul2_rn(x[t][0], x[t][0]);
-#pragma unroll
-      for (int p = 1; p < P2; ++p) {
-        ds = __ffma2_rn(x[t][p], sl[p], ds);
-        de = __ffma2_rn(x[t][p], el[p], de);
-        nk = __ffma2_rn(x[t][p], x[t][p], nk);
+      for (int e = 0; e < FC / 2; ++e) {
+        float2 x;
+        if constexpr (sizeof(T) == 2)  // bf16: a word holds two features
+          x = make_float2(__uint_as_float(u[e] << 16), __uint_as_float(u[e] & 0xFFFF0000u));
+        else
+          x = make_float2(__uint_as_float(u[2 * e]), __uint_as_float(u[2 * e + 1]));
+        ds = __ffma2_rn(x, sv[c * (FC / 2) + e], ds);
+        de = __ffma2_rn(x, ev[c * (FC / 2) + e], de);
+        nk = __ffma2_rn(x, x, nk);
       }
-      part[4 * t] = hsum(ds);
-      part[4 * t + 1] = hsum(de);
-      part[4 * t + 2] = hsum(nk);
-      part[4 * t + 3] = 0.f;
     }
-    const float v = reduce_scatter<16>(part, lane);
-    // lane l holds value l / 2: (ds, de, nk, 0) of token l / 8
-    const float de = __shfl_down_sync(0xFFFFFFFFu, v, 2);
-    const float nk = __shfl_down_sync(0xFFFFFFFFu, v, 4);
-    if ((lane & 7) == 0) {
-      const int i = i0 + (lane >> 3);
-      if (i < e) {
-        const float rk = nk > 0.f ? rsqrtf(nk) : 0.f;
-        as[i] = -(v * rk) * rS;
-        ae[i] = -(de * rk) * rE;
-      }
+    float v0 = hsum(ds), v1 = hsum(de), v2 = hsum(nk);
+#pragma unroll
+    for (int o = 1; o <= 2; o <<= 1) {
+      v0 += __shfl_xor_sync(0xFFFFFFFFu, v0, o);
+      v1 += __shfl_xor_sync(0xFFFFFFFFu, v1, o);
+      v2 += __shfl_xor_sync(0xFFFFFFFFu, v2, o);
+    }
+    const int i = t0 + g;
+    if (q == 0 && i < hi) {
+      const float rk = v2 > 0.f ? rsqrtf(v2) : 0.f;
+      as[i] = -(v0 * rk) * rS;
+      ae[i] = -(v1 * rk) * rE;
     }
   }
 }
