@@ -13,15 +13,16 @@
 // (A mean and a sum point the same way, so the anchors are kept as sums.)
 //
 // HBM-bound key scans on the CUDA cores, four launches:
-//   1. anchors_kernel: one CTA per (unit, episodic block); its warps sweep
-//      contiguous token ranges, lanes over features.  Each key is normalised
-//      once; the block sum of kh goes to the workspace; the causal window sum is
-//      kept as P (the current window-aligned chunk's prefix) + Q (the previous
-//      chunk's suffix, its total minus the rows that left the window), so every
-//      running sum restarts each `window` keys and rounding cannot drift; the
-//      rows leaving the window are re-read and their 1/|k| comes from a per-warp
-//      ring in shared memory.  A row's first read marks it evict_last in L2 and
-//      its re-read evict_first: only the rows inside some warp's window (tens of
+//   1. anchors_kernel: one CTA per (unit, episodic block); each warp runs two
+//      token streams over contiguous ranges (16 lanes per key, features spread
+//      over the lanes).  Each key is normalised once; the block sum of kh goes
+//      to the workspace; the causal window sum is kept as P (the current
+//      window-aligned chunk's prefix) + Q (the previous chunk's suffix, its
+//      total minus the rows that left the window), so every running sum
+//      restarts each `window` keys and rounding cannot drift; the rows leaving
+//      the window are re-read and their 1/|k| comes from a per-stream ring in
+//      shared memory.  A row's first read marks it evict_last in L2 and its
+//      re-read evict_first: only the rows inside some stream's window (tens of
 //      MB) are protected, so the re-reads hit L2 instead of HBM.  Packed f32x2
 //      arithmetic throughout.  Writes a_c.
 //   2. global_kernel: same grid; adds the unit's block sums into the stable
@@ -31,8 +32,9 @@
 //      32-bit keys) of the n_disc-th largest and smallest a_k sharing every pass,
 //      then the two sums.
 //   4. final_kernel: elementwise weights, surprise, routing.
-// Per-token cross-lane sums go through batched butterflies: V values of 4 tokens
-// reduce in V-1 + (5 - log2 V) shuffles instead of 5 V.
+// The window scan's per-token cross-lane sums go through batched butterflies
+// over a stream's 16 lanes: V values of 4 tokens reduce in V-1 + (4 - log2 V)
+// shuffles instead of 4 V.
 #include <type_traits>
 
 #include "kvc_internal.cuh"
@@ -50,11 +52,6 @@ constexpr int NT_DISC = 1024;
 // Loads carry an L2 cache-policy operand (createpolicy): rows that will be read
 // again soon are kept (evict_last), rows read for the last time go first.
 template <int NW32> struct Words;
-template <> struct Words<1> {
-  __device__ __forceinline__ static void load(const void *p, uint64_t pol, uint32_t (&w)[1]) {
-    asm("ld.global.nc.L2::cache_hint.u32 %0, [%1], %2;" : "=r"(w[0]) : "l"(p), "l"(pol));
-  }
-};
 template <> struct Words<2> {
   __device__ __forceinline__ static void load(const void *p, uint64_t pol, uint32_t (&w)[2]) {
     asm("ld.global.nc.L2::cache_hint.v2.u32 {%0, %1}, [%2], %3;"
@@ -86,16 +83,59 @@ template <typename T, int D> struct Row {
   }
 };
 
-// Sum V per-lane values over the warp; afterwards lane l holds the total of
-// value l / (32 / V) (V = 4, 8 or 16).
+__device__ __forceinline__ float hsum(float2 a) { return a.x + a.y; }
+
+// ---- 1. block sums and the current (moving-window) anchor ---------------------
+// Sixteen lanes per key: a warp runs two independent token streams, lane l of a
+// stream's group holding the features of pieces l, l+16, ... of each row (a
+// group's load covers contiguous bytes of one row), so a token's sums take four
+// shuffle levels instead of five and every shuffle serves two tokens.
+constexpr int GW = 16;                // lanes per stream
+constexpr int NSW = 32 / GW;          // streams per warp
+constexpr int NSTREAM = NWARP * NSW;  // streams per CTA
+constexpr int OWN = GW / 4;           // group lanes holding one token's sums after a 4-value reduction
+
+template <typename T, int D> struct GroupRow {
+  static constexpr int RB = D * (int)sizeof(T);       // bytes per row
+  static constexpr int LB = RB / GW;                  // bytes per lane
+  static constexpr int US = LB < 16 ? LB : 16;        // bytes per load
+  static constexpr int NL = LB / US;                  // loads per lane
+  static constexpr int PPL = US / (2 * (int)sizeof(T));  // float2 pairs per load
+  static constexpr int P2 = NL * PPL;                 // float2 pairs per lane
+  static_assert(RB % GW == 0 && LB % US == 0 && PPL >= 1, "row must split into pieces over the group");
+  // feature of the first element of pair p held by group lane g
+  __device__ __forceinline__ static int feature(int g, int p) {
+    return ((US * GW) * (p / PPL) + US * g) / (int)sizeof(T) + 2 * (p % PPL);
+  }
+  __device__ __forceinline__ static void load(const T *row, int g, uint64_t pol, float2 (&x)[P2]) {
+    const char *base = reinterpret_cast<const char *>(row) + US * g;
+#pragma unroll
+    for (int j = 0; j < NL; ++j) {
+      uint32_t w[US / 4];
+      Words<US / 4>::load(base + (US * GW) * j, pol, w);
+      if constexpr (sizeof(T) == 2) {  // bf16: a word holds two features
+#pragma unroll
+        for (int e = 0; e < PPL; ++e)
+          x[j * PPL + e] = make_float2(__uint_as_float(w[e] << 16), __uint_as_float(w[e] & 0xFFFF0000u));
+      } else {
+#pragma unroll
+        for (int e = 0; e < PPL; ++e)
+          x[j * PPL + e] = make_float2(__uint_as_float(w[2 * e]), __uint_as_float(w[2 * e + 1]));
+      }
+    }
+  }
+};
+
+// reduce_scatter over the GW lanes of a group: afterwards group lane g holds the
+// total of value g / (GW / V) (V = 2, 4 or 8).
 template <int V>
-__device__ __forceinline__ float reduce_scatter(float (&v)[V], int lane) {
+__device__ __forceinline__ float reduce_scatter_group(float (&v)[V], int g) {
   int count = V;
 #pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
+  for (int o = GW / 2; o >= 1; o >>= 1) {
     if (count > 1) {
       const int half = count >> 1;
-      const bool up = (lane & o) != 0;
+      const bool up = (g & o) != 0;
 #pragma unroll
       for (int j = 0; j < V / 2; ++j) {
         if (j < half) {
@@ -112,214 +152,215 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[V], int lane) {
   return v[0];
 }
 
-__device__ __forceinline__ float hsum(float2 a) { return a.x + a.y; }
-
-// Token range of warp w inside [lo, hi): equal spans.
-__device__ __forceinline__ void warp_range(int lo, int hi, int w, int &s, int &e) {
-  const int span = (hi - lo + NWARP - 1) / NWARP;
-  s = min(hi, lo + w * span);
-  e = min(hi, s + span);
-}
-
-// ---- 1. block sums and the current (moving-window) anchor ---------------------
 template <typename T, int D>
 __global__ __launch_bounds__(NT_SCAN) void anchors_kernel(const T *__restrict__ K, int Tn,
                                                           int blk, int n_blocks, int window,
                                                           float *__restrict__ esum,
                                                           float *__restrict__ a) {
-  using R = Row<T, D>;
+  using R = GroupRow<T, D>;
   constexpr int P2 = R::P2;
-  // [NWARP][window + 4]: 1/|k| of row j at slot j % (window + 4).  A batch writes
+  // [NSTREAM][window + 4]: 1/|k| of row j at slot j % (window + 4).  A batch writes
   // four distinct slots and never one that it reads (rows i - window < i0 sit at
   // least window + 1 rows back), so no two lanes touch a slot in the same batch.
   extern __shared__ float ring_all[];
-  __shared__ float sums[NWARP][D];
+  __shared__ float sums[NSTREAM][D];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int g = lane & (GW - 1);     // lane within the stream's group
+  const int gbase = lane & ~(GW - 1);  // the group's first lane
+  const int sid = warp * NSW + lane / GW;
   const long unit = blockIdx.x / n_blocks;
   const int bj = blockIdx.x % n_blocks;
   const int lo = min(Tn, bj * blk), hi = min(Tn, lo + blk);
   const T *Ku = K + unit * (long)Tn * D;
   const int RW = window + 4;
-  float *ring = ring_all + warp * RW;
+  float *ring = ring_all + sid * RW;
   float *ac = a + (unit * 3 + 2) * (long)Tn;
   const uint64_t keep_pol = tc::make_policy_evict_last();   // read again `window` rows later
   const uint64_t last_pol = tc::make_policy_evict_first();  // last read
 
-  int s, e;
-  warp_range(lo, hi, warp, s, e);
+  // The stream's tokens [s, e): spans are whole windows, so every stream of the
+  // CTA has the same phase against the window-aligned chunks and the streams
+  // of a warp take the same branches batch by batch.
+  const int span = ((hi - lo + NSTREAM - 1) / NSTREAM + window - 1) / window * window;
+  const int s = min(hi, lo + sid * span), e = min(hi, s + span);
+  const bool live = s < e;
   float2 tot[P2], sil[P2];  // sums of kh over [c0, e) and over [c0, s)
 #pragma unroll
   for (int p = 0; p < P2; ++p) tot[p] = sil[p] = make_float2(0.f, 0.f);
 
-  if (s < e) {
-    const int c0 = (s / window) * window;  // the chunk start the warp walks from
-    float2 P[P2], Q[P2];
+  const int c0 = (s / window) * window;  // the chunk start the stream walks from
+  float2 P[P2], Q[P2];
 #pragma unroll
-    for (int p = 0; p < P2; ++p) P[p] = Q[p] = make_float2(0.f, 0.f);
-    // warm-up: the full chunk before c0 (its total starts Q; its 1/|k| fill the ring)
-    if (c0 > 0) {
-      for (int i0 = c0 - window; i0 < c0; i0 += 4) {
-        float2 x[4][P2];
-        float ss[4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          if (i0 + t < c0) R::load(Ku + (long)(i0 + t) * D, lane, keep_pol, x[t]);
-          else {
-#pragma unroll
-            for (int p = 0; p < P2; ++p) x[t][p] = make_float2(0.f, 0.f);
-          }
-          float2 q2 = __fmul2_rn(x[t][0], x[t][0]);
-#pragma unroll
-          for (int p = 1; p < P2; ++p) q2 = __ffma2_rn(x[t][p], x[t][p], q2);
-          ss[t] = hsum(q2);
-        }
-        const float tt = reduce_scatter<4>(ss, lane);
-        const float my_inv = tt > 0.f ? rsqrtf(tt) : 0.f;
-        const int mt = lane >> 3;
-        if ((lane & 7) == 0 && i0 + mt < c0) ring[(i0 + mt) % RW] = my_inv;
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const float inv = __shfl_sync(0xFFFFFFFFu, my_inv, t * 8);
-          if (i0 + t < c0) {
-            const float2 inv2 = make_float2(inv, inv);
-#pragma unroll
-            for (int p = 0; p < P2; ++p) P[p] = __ffma2_rn(x[t][p], inv2, P[p]);
-          }
-        }
-      }
-    }
-    // the first chunk reset moves the warm-up total into Q; keep it out of `tot`
-#pragma unroll
-    for (int p = 0; p < P2; ++p) tot[p] = make_float2(-P[p].x, -P[p].y);
-    __syncwarp();
-    int r = 0;  // i - (chunk start), i.e. i % window, kept as a running counter
-    int rs = c0 % RW;  // i0 % RW
-    // One batch of 4 tokens.  FAST: the batch lies inside [s, e), its leaving rows
-    // are real rows (i0 >= window) and window % 4 == 0, so no token needs a bounds
-    // check and a chunk can only start at the batch's first token; rows are then
-    // addressed by constant offsets from one pointer.
-    auto batch = [&](const int i0, auto fast_tag) {
-      constexpr bool FAST = decltype(fast_tag)::value;
-      float2 x[4][P2], y[4][P2];
+  for (int p = 0; p < P2; ++p) P[p] = Q[p] = make_float2(0.f, 0.f);
+  // warm-up: the full chunk before c0 (its total starts Q; its 1/|k| fill the ring)
+  {
+    const bool warm = live && c0 > 0;
+    for (int k0 = 0; k0 < window; k0 += 4) {
+      const int i0 = c0 - window + k0;
+      float2 x[4][P2];
       float ss[4];
-      const T *px = Ku + (long)i0 * D;
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
-        if constexpr (FAST) {
-          R::load(px + t * D, lane, keep_pol, x[t]);
-          R::load(px + (t - window) * D, lane, last_pol, y[t]);
-        } else {
-          // rows past e or before 0 load an in-range row instead (no branch): a
-          // token past e is never used, and a leaving row before 0 is scaled by 0
-          const int i = min(i0 + t, e - 1);
-          R::load(Ku + (long)i * D, lane, keep_pol, x[t]);
-          R::load(Ku + (long)max(i - window, 0) * D, lane, last_pol, y[t]);
-        }
+        const bool use = warm && k0 + t < window;
+        R::load(Ku + (long)(use ? i0 + t : 0) * D, g, keep_pol, x[t]);
         float2 q2 = __fmul2_rn(x[t][0], x[t][0]);
 #pragma unroll
         for (int p = 1; p < P2; ++p) q2 = __ffma2_rn(x[t][p], x[t][p], q2);
-        ss[t] = hsum(q2);
+        ss[t] = use ? hsum(q2) : 0.f;
       }
-      const float tt = reduce_scatter<4>(ss, lane);
-      // lanes 8t own token t: swap its 1/|k| into the ring, take out the leaving row's
+      const float tt = reduce_scatter_group<4>(ss, g);  // group lanes OWN t ..: token t
       const float my_inv = tt > 0.f ? rsqrtf(tt) : 0.f;
-      float my_old = 0.f;
-      {
-        // slot of row j is j % RW; rs tracks i0 % RW, and (i - window) % RW is
-        // (i + 4) % RW because RW = window + 4
-        const int mt = lane >> 3, i = i0 + mt;
-        int sn = rs + mt;
-        if (sn >= RW) sn -= RW;
-        int so = sn + 4;
-        if (so >= RW) so -= RW;
-        if ((lane & 7) == 0 && (FAST || i < e)) {
-          if (FAST || (i >= window && i - window < i0)) my_old = ring[so];
-          ring[sn] = my_inv;
-        }
-      }
-      rs += 4;
-      if (rs >= RW) rs -= RW;
-      float part[8];
+      const int mt = g / OWN;
+      if (warm && g % OWN == 0 && k0 + mt < window) ring[(i0 + mt) % RW] = my_inv;
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
-        const int i = i0 + t;
-        const float inv = __shfl_sync(0xFFFFFFFFu, my_inv, t * 8);
-        float old = __shfl_sync(0xFFFFFFFFu, my_old, t * 8);
-        if constexpr (!FAST) {
-          if (window < 4) {  // the leaving row may be in this very batch
-            const float same = __shfl_sync(0xFFFFFFFFu, my_inv, 8 * max(t - window, 0));
-            if (t >= window) old = same;
-          }
-        }
-        float dot = 0.f, nrm = 0.f;
-        if (FAST || i < e) {
-          if ((!FAST || t == 0) && r == 0) {  // a new chunk: the previous total becomes Q
+        const float inv = __shfl_sync(0xFFFFFFFFu, my_inv, gbase + OWN * t);
+        if (warm && k0 + t < window) {
+          const float2 inv2 = make_float2(inv, inv);
 #pragma unroll
-            for (int p = 0; p < P2; ++p) {
-              tot[p] = __fadd2_rn(tot[p], P[p]);
-              Q[p] = P[p];
-              P[p] = make_float2(0.f, 0.f);
-            }
-          }
-          const float2 inv2 = make_float2(inv, inv), nold2 = make_float2(-old, -old);
-          float2 d2 = make_float2(0.f, 0.f), n2 = make_float2(0.f, 0.f);
+          for (int p = 0; p < P2; ++p) P[p] = __ffma2_rn(x[t][p], inv2, P[p]);
+        }
+      }
+    }
+  }
+  // the first chunk reset moves the warm-up total into Q; keep it out of `tot`
+#pragma unroll
+  for (int p = 0; p < P2; ++p) tot[p] = make_float2(-P[p].x, -P[p].y);
+  __syncwarp();
+  int r = 0;         // i - (chunk start), i.e. i % window, kept as a running counter
+  int rs = c0 % RW;  // i0 % RW
+  // One batch of 4 tokens of every stream of the warp.  FAST (taken only when
+  // it holds for all four streams): the batch lies inside [s, e), its leaving
+  // rows are real rows (i0 >= window) and window % 4 == 0, so no token needs a
+  // bounds check and a chunk can only start at the batch's first token.
+  auto batch = [&](const int i0, auto fast_tag) {
+    constexpr bool FAST = decltype(fast_tag)::value;
+    float2 x[4][P2], y[4][P2];
+    float ss[4];
+    const T *px = Ku + (long)i0 * D;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      if constexpr (FAST) {
+        R::load(px + t * D, g, keep_pol, x[t]);
+        R::load(px + (t - window) * D, g, last_pol, y[t]);
+      } else {
+        // rows past e or before 0 load an in-range row instead (no branch): a
+        // token past e is never used, and a leaving row before 0 is scaled by 0
+        const int i = max(0, min(i0 + t, e - 1));
+        R::load(Ku + (long)i * D, g, keep_pol, x[t]);
+        R::load(Ku + (long)max(i - window, 0) * D, g, last_pol, y[t]);
+      }
+      float2 q2 = __fmul2_rn(x[t][0], x[t][0]);
+#pragma unroll
+      for (int p = 1; p < P2; ++p) q2 = __ffma2_rn(x[t][p], x[t][p], q2);
+      ss[t] = hsum(q2);
+    }
+    const float tt = reduce_scatter_group<4>(ss, g);
+    // group lanes OWN t .. own token t: swap its 1/|k| into the ring, take out the leaving row's
+    const float my_inv = tt > 0.f ? rsqrtf(tt) : 0.f;
+    float my_old = 0.f;
+    {
+      // slot of row j is j % RW; rs tracks i0 % RW, and (i - window) % RW is
+      // (i + 4) % RW because RW = window + 4
+      const int mt = g / OWN, i = i0 + mt;
+      int sn = rs + mt;
+      if (sn >= RW) sn -= RW;
+      int so = sn + 4;
+      if (so >= RW) so -= RW;
+      if (g % OWN == 0 && (FAST || i < e)) {
+        if (FAST || (i >= window && i - window < i0)) my_old = ring[so];
+        ring[sn] = my_inv;
+      }
+    }
+    rs += 4;
+    if (rs >= RW) rs -= RW;
+    float part[8];
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int i = i0 + t;
+      const float inv = __shfl_sync(0xFFFFFFFFu, my_inv, gbase + OWN * t);
+      float old = __shfl_sync(0xFFFFFFFFu, my_old, gbase + OWN * t);
+      if constexpr (!FAST) {
+        if (window < 4) {  // the leaving row may be in this very batch
+          const float same = __shfl_sync(0xFFFFFFFFu, my_inv, gbase + OWN * max(t - window, 0));
+          if (t >= window) old = same;
+        }
+      }
+      float dot = 0.f, nrm = 0.f;
+      if (FAST || i < e) {
+        if ((!FAST || t == 0) && r == 0) {  // a new chunk: the previous total becomes Q
 #pragma unroll
           for (int p = 0; p < P2; ++p) {
-            P[p] = __ffma2_rn(x[t][p], inv2, P[p]);
-            Q[p] = __ffma2_rn(y[t][p], nold2, Q[p]);
-            const float2 w = __fadd2_rn(P[p], Q[p]);
-            d2 = __ffma2_rn(x[t][p], w, d2);
-            n2 = __ffma2_rn(w, w, n2);
-          }
-          dot = hsum(d2);
-          nrm = hsum(n2);
-          if constexpr (!FAST) {
-            if (i == s - 1) {
-#pragma unroll
-              for (int p = 0; p < P2; ++p) sil[p] = P[p];
-            }
-            r = (r + 1 == window) ? 0 : r + 1;
+            tot[p] = __fadd2_rn(tot[p], P[p]);
+            Q[p] = P[p];
+            P[p] = make_float2(0.f, 0.f);
           }
         }
-        part[2 * t] = dot;
-        part[2 * t + 1] = nrm;
+        const float2 inv2 = make_float2(inv, inv), nold2 = make_float2(-old, -old);
+        float2 d2 = make_float2(0.f, 0.f), n2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int p = 0; p < P2; ++p) {
+          P[p] = __ffma2_rn(x[t][p], inv2, P[p]);
+          Q[p] = __ffma2_rn(y[t][p], nold2, Q[p]);
+          const float2 w = __fadd2_rn(P[p], Q[p]);
+          d2 = __ffma2_rn(x[t][p], w, d2);
+          n2 = __ffma2_rn(w, w, n2);
+        }
+        dot = hsum(d2);
+        nrm = hsum(n2);
+        if constexpr (!FAST) {
+          if (i == s - 1) {
+#pragma unroll
+            for (int p = 0; p < P2; ++p) sil[p] = P[p];
+          }
+          r = (r + 1 == window) ? 0 : r + 1;
+        }
       }
-      if constexpr (FAST) {
-        r += 4;
-        if (r == window) r = 0;
-      }
-      const float v = reduce_scatter<8>(part, lane);
-      // lane 8t holds token t's <k, window sum> and 1/|k|; lane 8t+4 the window's |.|^2
-      const float nrm = __shfl_down_sync(0xFFFFFFFFu, v, 4);
-      if ((lane & 7) == 0) {
-        const int i = i0 + (lane >> 3);
-        // cos(kh_i, window sum) with |kh_i| = 1 (a zero key has dot 0)
-        if (FAST || (i >= s && i < e)) ac[i] = nrm > 0.f ? -(v * my_inv) * rsqrtf(nrm) : 0.f;
-      }
-      __syncwarp();  // this batch's ring writes before the next batch's reads
-    };
-    const bool can_fast = window % 4 == 0;
-    for (int i0 = c0; i0 < e; i0 += 4) {
-      if (can_fast && i0 >= s && i0 >= window && i0 + 4 <= e)
-        batch(i0, std::integral_constant<bool, true>());
-      else
-        batch(i0, std::integral_constant<bool, false>());
+      part[2 * t] = dot;
+      part[2 * t + 1] = nrm;
     }
+    if constexpr (FAST) {
+      r += 4;
+      if (r == window) r = 0;
+    }
+    const float v = reduce_scatter_group<8>(part, g);
+    // group lane OWN t holds token t's <k, window sum> (and 1/|k|); lane OWN t + GW/8
+    // the window's |.|^2
+    const float nrm = __shfl_down_sync(0xFFFFFFFFu, v, GW / 8);
+    if (g % OWN == 0) {
+      const int i = i0 + g / OWN;
+      // cos(kh_i, window sum) with |kh_i| = 1 (a zero key has dot 0)
+      if (FAST || (i >= s && i < e)) ac[i] = nrm > 0.f ? -(v * my_inv) * rsqrtf(nrm) : 0.f;
+    }
+    __syncwarp();  // this batch's ring writes before the next batch's reads
+  };
+  const bool can_fast = window % 4 == 0;
+  for (int i0 = c0; __any_sync(0xFFFFFFFFu, live && i0 < e); i0 += 4) {
+    if (__all_sync(0xFFFFFFFFu, can_fast && live && i0 >= s && i0 >= window && i0 + 4 <= e))
+      batch(i0, std::integral_constant<bool, true>());
+    else
+      batch(i0, std::integral_constant<bool, false>());
+  }
+  if (live) {
 #pragma unroll
     for (int p = 0; p < P2; ++p)
       tot[p] = __fadd2_rn(__fadd2_rn(tot[p], P[p]), make_float2(-sil[p].x, -sil[p].y));
+  } else {
+#pragma unroll
+    for (int p = 0; p < P2; ++p) tot[p] = make_float2(0.f, 0.f);
   }
-  // block sum of kh over the warps
+  // block sum of kh over the streams
 #pragma unroll
   for (int p = 0; p < P2; ++p) {
-    sums[warp][lane * 2 * P2 + 2 * p] = tot[p].x;
-    sums[warp][lane * 2 * P2 + 2 * p + 1] = tot[p].y;
+    const int f = R::feature(g, p);
+    sums[sid][f] = tot[p].x;
+    sums[sid][f + 1] = tot[p].y;
   }
   __syncthreads();
   for (int f = threadIdx.x; f < D; f += NT_SCAN) {
     float t = 0.f;
 #pragma unroll
-    for (int w = 0; w < NWARP; ++w) t += sums[w][f];
+    for (int w = 0; w < NSTREAM; ++w) t += sums[w][f];
     esum[(unit * n_blocks + bj) * (long)D + f] = t;
   }
 }
@@ -595,7 +636,7 @@ int run_nested(const void *K, long units, int Tn, int window, int n_blocks, int 
   float *esum = static_cast<float *>(ws);
   float *Dw = esum + units * (long)n_blocks * D;
   const unsigned grid = (unsigned)(units * n_blocks);
-  const size_t ring = (size_t)NWARP * (window + 4) * sizeof(float);
+  const size_t ring = (size_t)NSTREAM * (window + 4) * sizeof(float);
   if (ensure_smem((const void *)anchors_kernel<T, D>, ring))
     return cuda_failure(cudaErrorInvalidValue, "nested anchors kernel: shared memory");
   anchors_kernel<T, D><<<grid, NT_SCAN, ring, st>>>(static_cast<const T *>(K), Tn, blk, n_blocks,
