@@ -370,8 +370,8 @@ __global__ __launch_bounds__(NT_SCAN) void anchors_kernel(const T *__restrict__ 
 // of its key (each load of the group covers whole 32-byte sectors of one row),
 // keeps the matching slices of S and E in registers for the whole scan, and the
 // group adds its four partial <k, S>, <k, E> and |k|^2 with two shuffles.  A
-// warp takes 8 keys a step; the next step's loads are issued before this
-// step's arithmetic.
+// warp takes 8 keys a step; the next two steps' loads are in flight during
+// this step's arithmetic.
 template <typename T, int D>
 __global__ __launch_bounds__(NT_SCAN) void global_kernel(const T *__restrict__ K, int Tn, int blk,
                                                          int n_blocks,
@@ -433,13 +433,17 @@ __global__ __launch_bounds__(NT_SCAN) void global_kernel(const T *__restrict__ K
   };
   const int step = 8 * NWARP;
   int t0 = lo + 8 * warp;
-  uint4 wn[NC];
+  uint4 wn[NC], wnn[NC];  // the next two steps' pieces, in flight
   if (t0 < hi) load(t0, wn);
+  if (t0 + step < hi) load(t0 + step, wnn);
   for (; t0 < hi; t0 += step) {
     uint4 w[NC];
 #pragma unroll
-    for (int c = 0; c < NC; ++c) w[c] = wn[c];
-    if (t0 + step < hi) load(t0 + step, wn);
+    for (int c = 0; c < NC; ++c) {
+      w[c] = wn[c];
+      wn[c] = wnn[c];
+    }
+    if (t0 + 2 * step < hi) load(t0 + 2 * step, wnn);
     float2 ds = make_float2(0.f, 0.f), de = ds, nk = ds;
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
