@@ -13,9 +13,10 @@
 // (A mean and a sum point the same way, so the anchors are kept as sums.)
 //
 // HBM-bound key scans on the CUDA cores, four launches:
-//   1. anchors_kernel: one CTA per (unit, episodic block); each warp runs two
-//      token streams over contiguous ranges (16 lanes per key, features spread
-//      over the lanes).  Each key is normalised once; the block sum of kh goes
+//   1. anchors_kernel: one CTA of two warps per (unit, episodic block); each
+//      warp runs two token streams over contiguous ranges (16 lanes per key,
+//      features spread over the lanes; every stream first re-reads the window
+//      before its range, so fewer, longer streams re-read less).  Each key is normalised once; the block sum of kh goes
 //      to the workspace; the causal window sum is kept as P (the current
 //      window-aligned chunk's prefix) + Q (the previous chunk's suffix, its
 //      total minus the rows that left the window), so every running sum
@@ -44,7 +45,7 @@
 namespace kvc {
 namespace {
 
-constexpr int NWARP = 4;  // warps per CTA of the two key scans
+constexpr int NWARP = 4;  // warps per CTA of the global scan
 constexpr int NT_SCAN = NWARP * 32;
 constexpr int NT_DISC = 1024;
 
@@ -92,7 +93,9 @@ __device__ __forceinline__ float hsum(float2 a) { return a.x + a.y; }
 // shuffle levels instead of five and every shuffle serves two tokens.
 constexpr int GW = 16;                // lanes per stream
 constexpr int NSW = 32 / GW;          // streams per warp
-constexpr int NSTREAM = NWARP * NSW;  // streams per CTA
+constexpr int AWARP = 2;              // warps per CTA of the window scan
+constexpr int NT_ANCH = AWARP * 32;
+constexpr int NSTREAM = AWARP * NSW;  // streams per CTA
 constexpr int OWN = GW / 4;           // group lanes holding one token's sums after a 4-value reduction
 
 template <typename T, int D> struct GroupRow {
@@ -153,7 +156,7 @@ __device__ __forceinline__ float reduce_scatter_group(float (&v)[V], int g) {
 }
 
 template <typename T, int D>
-__global__ __launch_bounds__(NT_SCAN) void anchors_kernel(const T *__restrict__ K, int Tn,
+__global__ __launch_bounds__(NT_ANCH) void anchors_kernel(const T *__restrict__ K, int Tn,
                                                           int blk, int n_blocks, int window,
                                                           float *__restrict__ esum,
                                                           float *__restrict__ a) {
@@ -357,7 +360,7 @@ __global__ __launch_bounds__(NT_SCAN) void anchors_kernel(const T *__restrict__ 
     sums[sid][f + 1] = tot[p].y;
   }
   __syncthreads();
-  for (int f = threadIdx.x; f < D; f += NT_SCAN) {
+  for (int f = threadIdx.x; f < D; f += NT_ANCH) {
     float t = 0.f;
 #pragma unroll
     for (int w = 0; w < NSTREAM; ++w) t += sums[w][f];
@@ -643,7 +646,7 @@ int run_nested(const void *K, long units, int Tn, int window, int n_blocks, int 
   const size_t ring = (size_t)NSTREAM * (window + 4) * sizeof(float);
   if (ensure_smem((const void *)anchors_kernel<T, D>, ring))
     return cuda_failure(cudaErrorInvalidValue, "nested anchors kernel: shared memory");
-  anchors_kernel<T, D><<<grid, NT_SCAN, ring, st>>>(static_cast<const T *>(K), Tn, blk, n_blocks,
+  anchors_kernel<T, D><<<grid, NT_ANCH, ring, st>>>(static_cast<const T *>(K), Tn, blk, n_blocks,
                                                     window, esum, a);
   int rc = launch_status();
   if (rc) return rc;
