@@ -161,3 +161,34 @@ def test_host_input_prefill_matches_the_device_path(kvc, wl):
             if ref[key] is not None:
                 assert torch.equal(got[key][b:b + 1], ref[key]), (key, b)
         assert got["z"] is None if wl.r is not None else torch.equal(got["z"][b:b + 1], ref["z"])
+
+
+def test_host_input_prefill_reuses_buffers_across_steps(kvc):
+    """Two steps over the same buffers in row groups, with different inputs and
+    other work queued on the stream between the calls: every result equals the
+    device path's on that step's inputs (the copies never overwrite rows that an
+    earlier call's chain still reads)."""
+    wl = configs.LONG_CONTEXT.scaled(L=4, T=8192, k=409, n_segments=60)
+    groups = [(0, 2), (2, 4)]
+    steps = []
+    for seed_shift in (0, 1):
+        Q, K, V = gen.prefill_inputs(wl.scaled(seed=wl.seed + seed_shift), device=DEV)
+        steps.append((Q, K, V, *(t.cpu().pin_memory() for t in (Q, K, V))))
+    bufs = kvc.prefill_host_buffers(steps[0][3], steps[0][4], wl.k, wl.r)
+    busy = torch.empty(64 << 20, device=DEV)
+    for Q, K, V, hQ, hK, hV in steps:
+        outs = []
+        for r0, r1 in groups:
+            got = kvc.compress_prefill_host(hQ, hK, hV, wl.k, wl.R, wl.r, wl.gamma, wl.pool_width,
+                                            wl.beta_lo, wl.beta_hi, wl.scale, buffers=bufs,
+                                            rows=(r0, r1))
+            outs.append({key: got[key][r0:r1].clone() for key in ("idx", "K", "V", "len")})
+            for _ in range(20):  # unrelated work queued between the calls
+                busy.mul_(1.0)
+        torch.cuda.synchronize()
+        for (r0, r1), out in zip(groups, outs):
+            ref = kvc.compress_prefill(Q[r0:r1], K[r0:r1], V[r0:r1], wl.k, wl.R, wl.r, wl.gamma,
+                                       wl.pool_width, wl.beta_lo, wl.beta_hi, scale=wl.scale)
+            torch.cuda.synchronize()
+            for key in out:
+                assert torch.equal(out[key], ref[key]), (key, r0)
