@@ -149,7 +149,7 @@ __device__ __forceinline__ void for_head(const float *__restrict__ zm, uint32_t 
   }
 }
 
-// Calls f(key) for the middle pairs of this warp's range (see warp_of), four
+// Calls f(key) for the middle pairs of this warp's range (see warp_of), eight
 // 16-byte loads in flight per lane.
 template <typename F>
 __device__ __forceinline__ void for_warp(const float *__restrict__ zm, uint32_t flat0, int n, F &&f) {
@@ -159,15 +159,15 @@ __device__ __forceinline__ void for_warp(const float *__restrict__ zm, uint32_t 
   const int per4 = (sp.n4 + NW - 1) / NW;
   const int b0 = min(sp.n4, warp * per4), b1 = min(sp.n4, b0 + per4);
   if (warp == 0 && lane < sp.pre) f(pair_key(__ldg(zm + lane), flat0 + (uint32_t)lane));
-  for (int q0 = b0 + lane; q0 < b1; q0 += 4 * 32) {
-    float4 v[4];
+  for (int q0 = b0 + lane; q0 < b1; q0 += 8 * 32) {
+    float4 v[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 8; ++u) {
       const int q = q0 + 32 * u;
       v[u] = q < b1 ? __ldg(z4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 8; ++u) {
       const int q = q0 + 32 * u;
       if (q < b1) {
         const uint32_t i = flat0 + (uint32_t)(sp.pre + 4 * q);
@@ -531,34 +531,43 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
       if (keep && slot < kept_mid) mid[slot] = S + lane;
       run += __popc(m);
     }
-    for (int q0 = b0; q0 < b1; q0 += 32) {
-      const int q = q0 + lane;
-      bool k0 = false, k1 = false, k2 = false, k3 = false;
-      const int i = sp.pre + 4 * q;
-      if (q < b1) {
-        const float4 v = __ldg(z4 + q);
-        const uint32_t fi = f0 + (uint32_t)i;
-        k0 = pair_key(v.x, fi) >= lam;
-        k1 = pair_key(v.y, fi + 1) >= lam;
-        k2 = pair_key(v.z, fi + 2) >= lam;
-        k3 = pair_key(v.w, fi + 3) >= lam;
-      }
-      const int c = (int)k0 + (int)k1 + (int)k2 + (int)k3;
-      int incl = c;
+    for (int q00 = b0; q00 < b1; q00 += 4 * 32) {  // four vectors a lane in flight
+      float4 vv[4];
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-        if (lane >= off) incl += y;
+      for (int u = 0; u < 4; ++u) {
+        const int q = q00 + 32 * u + lane;
+        vv[u] = q < b1 ? __ldg(z4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      int slot = run + incl - c;
-      if (k0 && slot < kept_mid) mid[slot] = S + i;
-      slot += k0;
-      if (k1 && slot < kept_mid) mid[slot] = S + i + 1;
-      slot += k1;
-      if (k2 && slot < kept_mid) mid[slot] = S + i + 2;
-      slot += k2;
-      if (k3 && slot < kept_mid) mid[slot] = S + i + 3;
-      run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int q = q00 + 32 * u + lane;
+        bool k0 = false, k1 = false, k2 = false, k3 = false;
+        const int i = sp.pre + 4 * q;
+        if (q < b1) {
+          const float4 v = vv[u];
+          const uint32_t fi = f0 + (uint32_t)i;
+          k0 = pair_key(v.x, fi) >= lam;
+          k1 = pair_key(v.y, fi + 1) >= lam;
+          k2 = pair_key(v.z, fi + 2) >= lam;
+          k3 = pair_key(v.w, fi + 3) >= lam;
+        }
+        const int c = (int)k0 + (int)k1 + (int)k2 + (int)k3;
+        int incl = c;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+          if (lane >= off) incl += y;
+        }
+        int slot = run + incl - c;
+        if (k0 && slot < kept_mid) mid[slot] = S + i;
+        slot += k0;
+        if (k1 && slot < kept_mid) mid[slot] = S + i + 1;
+        slot += k1;
+        if (k2 && slot < kept_mid) mid[slot] = S + i + 2;
+        slot += k2;
+        if (k3 && slot < kept_mid) mid[slot] = S + i + 3;
+        run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+      }
     }
     if (warp == NW - 1) {
       const int i = sp.tail + lane;
