@@ -64,3 +64,24 @@ def test_fused_equals_separate_calls(kvc, oracle_mod, case):
         z_or, beta_or, _ = oracle_mod.hubkv_refine(s.cpu().numpy().astype(np.float64), r,
                                                     flags=flags)
         assert_close(z.cpu().numpy(), z_or, rtol=1e-5, atol=1e-30, what="z")
+
+
+@pytest.mark.parametrize("pool_width,flags", [(1, 0), (3, 0), (9, 0), (129, 0), (7, 1), (5, 1)])
+def test_fused_pool_widths(kvc, oracle_mod, pool_width, flags):
+    """Pooling windows other than the default 5 (which has its own four-candidate
+    path in the selection kernel) take the generic per-candidate gate: the same
+    bits as the separate refinement, and the oracle's selection on them."""
+    B, H, T, k, R, S, r = 2, 3, 20000, 2000, 32, 2, 0.3
+    s = _scores(B, H, T, seed=pool_width + 17)
+    z = torch.full_like(s, float("nan"))
+    idx = kvc.hubkv_select_topk(s, k, R, r, pool_width=pool_width, sink=S, flags=flags, z_out=z)
+    z_ref, _ = kvc.hubkv_refine(s, r, pool_width=pool_width, flags=flags)
+    idx_ref = kvc.kv_select_topk(z_ref, k, R, sink=S)
+    torch.cuda.synchronize()
+    assert torch.equal(z, z_ref)
+    assert torch.equal(idx, idx_ref)
+    z_np = z.cpu().numpy().astype(np.float64)
+    np.testing.assert_array_equal(idx.cpu().numpy(), oracle_mod.select_topk(z_np, k, R, S))
+    z_or, _, _ = oracle_mod.hubkv_refine(s.cpu().numpy().astype(np.float64), r, pool_width=pool_width,
+                                         flags=flags)
+    assert_close(z.cpu().numpy(), z_or, rtol=1e-5, atol=1e-30, what="z")
