@@ -34,8 +34,8 @@
 //      then the two sums.
 //   4. final_kernel: elementwise weights, surprise, routing.
 // The window scan's per-token cross-lane sums go through batched butterflies
-// over a stream's 16 lanes: V values of 4 tokens reduce in V-1 + (4 - log2 V)
-// shuffles instead of 4 V.
+// over a stream's 16 lanes: V values of a batch's tokens reduce in
+// V-1 + (4 - log2 V) shuffles instead of 4 V.
 #include <type_traits>
 
 #include "kvc_internal.cuh"
@@ -96,7 +96,8 @@ constexpr int NSW = 32 / GW;          // streams per warp
 constexpr int AWARP = 2;              // warps per CTA of the window scan
 constexpr int NT_ANCH = AWARP * 32;
 constexpr int NSTREAM = AWARP * NSW;  // streams per CTA
-constexpr int OWN = GW / 4;           // group lanes holding one token's sums after a 4-value reduction
+constexpr int NB = 4;                 // tokens of a stream per batch
+constexpr int OWN = GW / NB;          // group lanes holding one token's sums after an NB-value reduction
 
 template <typename T, int D> struct GroupRow {
   static constexpr int RB = D * (int)sizeof(T);       // bytes per row
@@ -162,9 +163,10 @@ __global__ __launch_bounds__(NT_ANCH) void anchors_kernel(const T *__restrict__ 
                                                           float *__restrict__ a) {
   using R = GroupRow<T, D>;
   constexpr int P2 = R::P2;
-  // [NSTREAM][window + 4]: 1/|k| of row j at slot j % (window + 4).  A batch writes
-  // four distinct slots and never one that it reads (rows i - window < i0 sit at
-  // least window + 1 rows back), so no two lanes touch a slot in the same batch.
+  // [NSTREAM][window + NB]: 1/|k| of row j at slot j % (window + NB).  A batch
+  // writes NB distinct slots and never one that it reads (rows i - window < i0
+  // sit at least window + 1 rows back), so no two lanes touch a slot in the same
+  // batch.
   extern __shared__ float ring_all[];
   __shared__ float sums[NSTREAM][D];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -175,7 +177,7 @@ __global__ __launch_bounds__(NT_ANCH) void anchors_kernel(const T *__restrict__ 
   const int bj = blockIdx.x % n_blocks;
   const int lo = min(Tn, bj * blk), hi = min(Tn, lo + blk);
   const T *Ku = K + unit * (long)Tn * D;
-  const int RW = window + 4;
+  const int RW = window + NB;
   float *ring = ring_all + sid * RW;
   float *ac = a + (unit * 3 + 2) * (long)Tn;
   const uint64_t keep_pol = tc::make_policy_evict_last();   // read again `window` rows later
@@ -198,12 +200,12 @@ __global__ __launch_bounds__(NT_ANCH) void anchors_kernel(const T *__restrict__ 
   // warm-up: the full chunk before c0 (its total starts Q; its 1/|k| fill the ring)
   {
     const bool warm = live && c0 > 0;
-    for (int k0 = 0; k0 < window; k0 += 4) {
+    for (int k0 = 0; k0 < window; k0 += NB) {
       const int i0 = c0 - window + k0;
-      float2 x[4][P2];
-      float ss[4];
+      float2 x[NB][P2];
+      float ss[NB];
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
+      for (int t = 0; t < NB; ++t) {
         const bool use = warm && k0 + t < window;
         R::load(Ku + (long)(use ? i0 + t : 0) * D, g, keep_pol, x[t]);
         float2 q2 = __fmul2_rn(x[t][0], x[t][0]);
@@ -211,12 +213,12 @@ __global__ __launch_bounds__(NT_ANCH) void anchors_kernel(const T *__restrict__ 
         for (int p = 1; p < P2; ++p) q2 = __ffma2_rn(x[t][p], x[t][p], q2);
         ss[t] = use ? hsum(q2) : 0.f;
       }
-      const float tt = reduce_scatter_group<4>(ss, g);  // group lanes OWN t ..: token t
+      const float tt = reduce_scatter_group<NB>(ss, g);  // group lanes OWN t ..: token t
       const float my_inv = tt > 0.f ? rsqrtf(tt) : 0.f;
       const int mt = g / OWN;
       if (warm && g % OWN == 0 && k0 + mt < window) ring[(i0 + mt) % RW] = my_inv;
 #pragma unroll
-      for (int t = 0; t < 4; ++t) {
+      for (int t = 0; t < NB; ++t) {
         const float inv = __shfl_sync(0xFFFFFFFFu, my_inv, gbase + OWN * t);
         if (warm && k0 + t < window) {
           const float2 inv2 = make_float2(inv, inv);
@@ -232,17 +234,17 @@ __global__ __launch_bounds__(NT_ANCH) void anchors_kernel(const T *__restrict__ 
   __syncwarp();
   int r = 0;         // i - (chunk start), i.e. i % window, kept as a running counter
   int rs = c0 % RW;  // i0 % RW
-  // One batch of 4 tokens of every stream of the warp.  FAST (taken only when
-  // it holds for all four streams): the batch lies inside [s, e), its leaving
-  // rows are real rows (i0 >= window) and window % 4 == 0, so no token needs a
+  // One batch of NB tokens of every stream of the warp.  FAST (taken only when
+  // it holds for both streams): the batch lies inside [s, e), its leaving rows
+  // are real rows (i0 >= window) and window % NB == 0, so no token needs a
   // bounds check and a chunk can only start at the batch's first token.
   auto batch = [&](const int i0, auto fast_tag) {
     constexpr bool FAST = decltype(fast_tag)::value;
-    float2 x[4][P2], y[4][P2];
-    float ss[4];
+    float2 x[NB][P2], y[NB][P2];
+    float ss[NB];
     const T *px = Ku + (long)i0 * D;
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
+    for (int t = 0; t < NB; ++t) {
       if constexpr (FAST) {
         R::load(px + t * D, g, keep_pol, x[t]);
         R::load(px + (t - window) * D, g, last_pol, y[t]);
@@ -258,33 +260,33 @@ __global__ __launch_bounds__(NT_ANCH) void anchors_kernel(const T *__restrict__ 
       for (int p = 1; p < P2; ++p) q2 = __ffma2_rn(x[t][p], x[t][p], q2);
       ss[t] = hsum(q2);
     }
-    const float tt = reduce_scatter_group<4>(ss, g);
+    const float tt = reduce_scatter_group<NB>(ss, g);
     // group lanes OWN t .. own token t: swap its 1/|k| into the ring, take out the leaving row's
     const float my_inv = tt > 0.f ? rsqrtf(tt) : 0.f;
     float my_old = 0.f;
     {
       // slot of row j is j % RW; rs tracks i0 % RW, and (i - window) % RW is
-      // (i + 4) % RW because RW = window + 4
+      // (i + NB) % RW because RW = window + NB
       const int mt = g / OWN, i = i0 + mt;
       int sn = rs + mt;
       if (sn >= RW) sn -= RW;
-      int so = sn + 4;
+      int so = sn + NB;
       if (so >= RW) so -= RW;
       if (g % OWN == 0 && (FAST || i < e)) {
         if (FAST || (i >= window && i - window < i0)) my_old = ring[so];
         ring[sn] = my_inv;
       }
     }
-    rs += 4;
+    rs += NB;
     if (rs >= RW) rs -= RW;
-    float part[8];
+    float part[2 * NB];
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
+    for (int t = 0; t < NB; ++t) {
       const int i = i0 + t;
       const float inv = __shfl_sync(0xFFFFFFFFu, my_inv, gbase + OWN * t);
       float old = __shfl_sync(0xFFFFFFFFu, my_old, gbase + OWN * t);
       if constexpr (!FAST) {
-        if (window < 4) {  // the leaving row may be in this very batch
+        if (window < NB) {  // the leaving row may be in this very batch
           const float same = __shfl_sync(0xFFFFFFFFu, my_inv, gbase + OWN * max(t - window, 0));
           if (t >= window) old = same;
         }
@@ -323,13 +325,13 @@ __global__ __launch_bounds__(NT_ANCH) void anchors_kernel(const T *__restrict__ 
       part[2 * t + 1] = nrm;
     }
     if constexpr (FAST) {
-      r += 4;
+      r += NB;
       if (r == window) r = 0;
     }
-    const float v = reduce_scatter_group<8>(part, g);
-    // group lane OWN t holds token t's <k, window sum> (and 1/|k|); lane OWN t + GW/8
+    const float v = reduce_scatter_group<2 * NB>(part, g);
+    // group lane OWN t holds token t's <k, window sum> (and 1/|k|); lane OWN t + OWN/2
     // the window's |.|^2
-    const float nrm = __shfl_down_sync(0xFFFFFFFFu, v, GW / 8);
+    const float nrm = __shfl_down_sync(0xFFFFFFFFu, v, OWN / 2);
     if (g % OWN == 0) {
       const int i = i0 + g / OWN;
       // cos(kh_i, window sum) with |kh_i| = 1 (a zero key has dot 0)
@@ -337,9 +339,9 @@ __global__ __launch_bounds__(NT_ANCH) void anchors_kernel(const T *__restrict__ 
     }
     __syncwarp();  // this batch's ring writes before the next batch's reads
   };
-  const bool can_fast = window % 4 == 0;
-  for (int i0 = c0; __any_sync(0xFFFFFFFFu, live && i0 < e); i0 += 4) {
-    if (__all_sync(0xFFFFFFFFu, can_fast && live && i0 >= s && i0 >= window && i0 + 4 <= e))
+  const bool can_fast = window % NB == 0;
+  for (int i0 = c0; __any_sync(0xFFFFFFFFu, live && i0 < e); i0 += NB) {
+    if (__all_sync(0xFFFFFFFFu, can_fast && live && i0 >= s && i0 >= window && i0 + NB <= e))
       batch(i0, std::integral_constant<bool, true>());
     else
       batch(i0, std::integral_constant<bool, false>());
@@ -371,8 +373,10 @@ __global__ __launch_bounds__(NT_ANCH) void anchors_kernel(const T *__restrict__ 
 // ---- 2. stable and episodic anchors ----------------------------------------------
 // Four lanes per key: lane q of a group reads the 16-byte pieces q, q+4, q+8, ...
 // of its key (each load of the group covers whole 32-byte sectors of one row),
-// keeps the matching slices of S and E in registers for the whole scan, and the
-// group adds its four partial <k, S>, <k, E> and |k|^2 with two shuffles.  A
+// reads the matching slices of S and E from shared memory (the four lanes of a
+// group read four different addresses, every group the same: no conflicts),
+// and the group adds its four partial <k, S>, <k, E> and |k|^2 with two
+// shuffles.  A
 // warp takes 8 keys a step; the next two steps' loads are in flight during
 // this step's arithmetic.
 template <typename T, int D>
@@ -384,7 +388,7 @@ __global__ __launch_bounds__(NT_SCAN) void global_kernel(const T *__restrict__ K
   constexpr int FC = 16 / (int)sizeof(T);      // features per piece
   constexpr int FS = 64 / (int)sizeof(T);      // feature stride between a lane's pieces
   constexpr int FL = NC * FC;                  // features per lane
-  __shared__ float S[D], E[D];
+  __shared__ __align__(16) float S[D], E[D];
   __shared__ float nrm[2];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int q = lane & 3, g = lane >> 2;
@@ -417,15 +421,6 @@ __global__ __launch_bounds__(NT_SCAN) void global_kernel(const T *__restrict__ K
   }
   __syncthreads();
   const float rS = nrm[0], rE = nrm[1];
-  float2 sv[FL / 2], ev[FL / 2];  // this lane's slices of S and E, as pairs
-#pragma unroll
-  for (int c = 0; c < NC; ++c)
-#pragma unroll
-    for (int e = 0; e < FC / 2; ++e) {
-      const int f = c * FS + q * FC + 2 * e;
-      sv[c * (FC / 2) + e] = make_float2(S[f], S[f + 1]);
-      ev[c * (FC / 2) + e] = make_float2(E[f], E[f + 1]);
-    }
   const char *Ku = reinterpret_cast<const char *>(K + unit * (long)Tn * D);
   float *as = a + (unit * 3 + 0) * (long)Tn;
   float *ae = a + (unit * 3 + 1) * (long)Tn;
@@ -451,6 +446,9 @@ __global__ __launch_bounds__(NT_SCAN) void global_kernel(const T *__restrict__ K
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
       const uint32_t u[4] = {w[c].x, w[c].y, w[c].z, w[c].w};
+      // this lane's features of piece c, and the anchors' values for them
+      const float2 *sv = reinterpret_cast<const float2 *>(S + c * FS + q * FC);
+      const float2 *ev = reinterpret_cast<const float2 *>(E + c * FS + q * FC);
 #pragma unroll
       for (int e = 0; e < FC / 2; ++e) {
         float2 x;
@@ -458,8 +456,8 @@ __global__ __launch_bounds__(NT_SCAN) void global_kernel(const T *__restrict__ K
           x = make_float2(__uint_as_float(u[e] << 16), __uint_as_float(u[e] & 0xFFFF0000u));
         else
           x = make_float2(__uint_as_float(u[2 * e]), __uint_as_float(u[2 * e + 1]));
-        ds = __ffma2_rn(x, sv[c * (FC / 2) + e], ds);
-        de = __ffma2_rn(x, ev[c * (FC / 2) + e], de);
+        ds = __ffma2_rn(x, sv[e], ds);
+        de = __ffma2_rn(x, ev[e], de);
         nk = __ffma2_rn(x, x, nk);
       }
     }
