@@ -238,21 +238,26 @@ __global__ __launch_bounds__(NT_ANCH) void anchors_kernel(const T *__restrict__ 
   // it holds for both streams): the batch lies inside [s, e), its leaving rows
   // are real rows (i0 >= window) and window % NB == 0, so no token needs a
   // bounds check and a chunk can only start at the batch's first token.
+  // x: this batch's new rows; xn: the next batch's, in flight during this batch.
+  // Rows past e or before 0 load an in-range row instead (no branch): a token
+  // past e is never used.
+  float2 x[NB][P2], xn[NB][P2];
+  auto load_next = [&](const int i0) {
+#pragma unroll
+    for (int t = 0; t < NB; ++t) R::load(Ku + (long)max(0, min(i0 + t, e - 1)) * D, g, keep_pol, xn[t]);
+  };
   auto batch = [&](const int i0, auto fast_tag) {
     constexpr bool FAST = decltype(fast_tag)::value;
-    float2 x[NB][P2], y[NB][P2];
+    float2 y[NB][P2];
     float ss[NB];
     const T *px = Ku + (long)i0 * D;
 #pragma unroll
     for (int t = 0; t < NB; ++t) {
       if constexpr (FAST) {
-        R::load(px + t * D, g, keep_pol, x[t]);
         R::load(px + (t - window) * D, g, last_pol, y[t]);
       } else {
-        // rows past e or before 0 load an in-range row instead (no branch): a
-        // token past e is never used, and a leaving row before 0 is scaled by 0
+        // a leaving row before 0 loads row 0 instead and is scaled by 0
         const int i = max(0, min(i0 + t, e - 1));
-        R::load(Ku + (long)i * D, g, keep_pol, x[t]);
         R::load(Ku + (long)max(i - window, 0) * D, g, last_pol, y[t]);
       }
       float2 q2 = __fmul2_rn(x[t][0], x[t][0]);
@@ -340,7 +345,13 @@ __global__ __launch_bounds__(NT_ANCH) void anchors_kernel(const T *__restrict__ 
     __syncwarp();  // this batch's ring writes before the next batch's reads
   };
   const bool can_fast = window % NB == 0;
+  load_next(c0);
   for (int i0 = c0; __any_sync(0xFFFFFFFFu, live && i0 < e); i0 += NB) {
+#pragma unroll
+    for (int t = 0; t < NB; ++t)
+#pragma unroll
+      for (int p = 0; p < P2; ++p) x[t][p] = xn[t][p];
+    load_next(i0 + NB);
     if (__all_sync(0xFFFFFFFFu, can_fast && live && i0 >= s && i0 >= window && i0 + NB <= e))
       batch(i0, std::integral_constant<bool, true>());
     else
