@@ -241,25 +241,21 @@ __global__ __launch_bounds__(NT_ANCH) void anchors_kernel(const T *__restrict__ 
   // x: this batch's new rows; xn: the next batch's, in flight during this batch.
   // Rows past e or before 0 load an in-range row instead (no branch): a token
   // past e is never used.
-  float2 x[NB][P2], xn[NB][P2];
+  float2 x[NB][P2], xn[NB][P2], y[NB][P2], yn[NB][P2];
   auto load_next = [&](const int i0) {
 #pragma unroll
-    for (int t = 0; t < NB; ++t) R::load(Ku + (long)max(0, min(i0 + t, e - 1)) * D, g, keep_pol, xn[t]);
+    for (int t = 0; t < NB; ++t) {
+      const int i = max(0, min(i0 + t, e - 1));
+      R::load(Ku + (long)i * D, g, keep_pol, xn[t]);
+      // the leaving row (a row before 0 loads row 0 instead and is scaled by 0)
+      R::load(Ku + (long)max(i - window, 0) * D, g, last_pol, yn[t]);
+    }
   };
   auto batch = [&](const int i0, auto fast_tag) {
     constexpr bool FAST = decltype(fast_tag)::value;
-    float2 y[NB][P2];
     float ss[NB];
-    const T *px = Ku + (long)i0 * D;
 #pragma unroll
     for (int t = 0; t < NB; ++t) {
-      if constexpr (FAST) {
-        R::load(px + (t - window) * D, g, last_pol, y[t]);
-      } else {
-        // a leaving row before 0 loads row 0 instead and is scaled by 0
-        const int i = max(0, min(i0 + t, e - 1));
-        R::load(Ku + (long)max(i - window, 0) * D, g, last_pol, y[t]);
-      }
       float2 q2 = __fmul2_rn(x[t][0], x[t][0]);
 #pragma unroll
       for (int p = 1; p < P2; ++p) q2 = __ffma2_rn(x[t][p], x[t][p], q2);
@@ -350,7 +346,10 @@ __global__ __launch_bounds__(NT_ANCH) void anchors_kernel(const T *__restrict__ 
 #pragma unroll
     for (int t = 0; t < NB; ++t)
 #pragma unroll
-      for (int p = 0; p < P2; ++p) x[t][p] = xn[t][p];
+      for (int p = 0; p < P2; ++p) {
+        x[t][p] = xn[t][p];
+        y[t][p] = yn[t][p];
+      }
     load_next(i0 + NB);
     if (__all_sync(0xFFFFFFFFu, can_fast && live && i0 >= s && i0 >= window && i0 + NB <= e))
       batch(i0, std::integral_constant<bool, true>());
