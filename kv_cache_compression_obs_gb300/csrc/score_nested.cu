@@ -538,16 +538,24 @@ __global__ __launch_bounds__(NT_DISC, 1) void disc_kernel(const float *__restric
     for (int i = threadIdx.x; i < 2 * NW * 256; i += NT_DISC) hist[i] = 0u;
     __syncthreads();
     uint32_t *h0 = hist + warp * 256, *h1 = hist + (NW + warp) * 256;
-    for_values(v, Tn, [&](float x) {
-      const uint32_t u = order_key(x), ub = ~u;
-      if ((u & mask) == prefix[0]) atomicAdd(h0 + ((u >> shift) & 255u), 1u);
-      if ((ub & mask) == prefix[1]) atomicAdd(h1 + ((ub >> shift) & 255u), 1u);
-    });
+    if (pass == 0) {
+      // the complements' top byte is 255 minus the keys': one histogram serves both
+      for_values(v, Tn, [&](float x) { atomicAdd(h0 + (order_key(x) >> 24), 1u); });
+    } else {
+      for_values(v, Tn, [&](float x) {
+        const uint32_t u = order_key(x), ub = ~u;
+        if ((u & mask) == prefix[0]) atomicAdd(h0 + ((u >> shift) & 255u), 1u);
+        if ((ub & mask) == prefix[1]) atomicAdd(h1 + ((ub >> shift) & 255u), 1u);
+      });
+    }
     __syncthreads();
     for (int i = threadIdx.x; i < 512; i += NT_DISC) {
       const int k = i >> 8, d = i & 255;
       uint32_t t = 0;
-      for (int w = 0; w < NW; ++w) t += hist[(k * NW + w) * 256 + d];
+      if (pass == 0)
+        for (int w = 0; w < NW; ++w) t += hist[w * 256 + (k ? 255 - d : d)];
+      else
+        for (int w = 0; w < NW; ++w) t += hist[(k * NW + w) * 256 + d];
       tot[k][d] = t;
     }
     __syncthreads();
