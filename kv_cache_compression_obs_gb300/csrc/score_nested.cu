@@ -640,14 +640,43 @@ __global__ void final_kernel(const float *__restrict__ a, const float *__restric
     const float *ae = as + Tn;
     const float *ac = ae + Tn;
     float *su = score + u * (long)Tn;
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < Tn; i += gridDim.x * blockDim.x) {
-      const float x0 = as[i], x1 = ae[i], x2 = ac[i];
+    auto route = [&](float x0, float x1, float x2) {
       const float mean = (x0 + x1 + x2) / 3.f;
       const float var = ((x0 - mean) * (x0 - mean) + (x1 - mean) * (x1 - mean) +
                          (x2 - mean) * (x2 - mean)) / 3.f;
       const float sig = sqrtf(var);
-      su[i] = sig > thresh ? fmaxf(x0, fmaxf(x1, x2)) : w0 * x0 + w1 * x1 + w2 * x2;
+      return sig > thresh ? fmaxf(x0, fmaxf(x1, x2)) : w0 * x0 + w1 * x1 + w2 * x2;
+    };
+    const int stride = gridDim.x * blockDim.x;
+    int i0 = 0;  // tokens from here on take the scalar loop
+    if (((reinterpret_cast<uintptr_t>(as) | reinterpret_cast<uintptr_t>(ae) |
+          reinterpret_cast<uintptr_t>(ac) | reinterpret_cast<uintptr_t>(su)) & 15) == 0) {
+      // 16-byte vectors of four tokens, two a thread in flight
+      const int n4 = Tn >> 2;
+      const float4 *as4 = reinterpret_cast<const float4 *>(as), *ae4 = reinterpret_cast<const float4 *>(ae),
+                   *ac4 = reinterpret_cast<const float4 *>(ac);
+      float4 *su4 = reinterpret_cast<float4 *>(su);
+      for (int q0 = blockIdx.x * blockDim.x + threadIdx.x; q0 < n4; q0 += 2 * stride) {
+        float4 x0[2], x1[2], x2[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int q = min(q0 + h * stride, n4 - 1);
+          x0[h] = __ldg(as4 + q);
+          x1[h] = __ldg(ae4 + q);
+          x2[h] = __ldg(ac4 + q);
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int q = q0 + h * stride;
+          if (q < n4)
+            su4[q] = make_float4(route(x0[h].x, x1[h].x, x2[h].x), route(x0[h].y, x1[h].y, x2[h].y),
+                                 route(x0[h].z, x1[h].z, x2[h].z), route(x0[h].w, x1[h].w, x2[h].w));
+        }
+      }
+      i0 = 4 * n4;
     }
+    for (int i = i0 + blockIdx.x * blockDim.x + threadIdx.x; i < Tn; i += stride)
+      su[i] = route(as[i], ae[i], ac[i]);
   }
 }
 
