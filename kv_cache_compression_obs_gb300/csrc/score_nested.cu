@@ -397,7 +397,6 @@ __global__ __launch_bounds__(NT_SCAN) void global_kernel(const T *__restrict__ K
   constexpr int NC = D * (int)sizeof(T) / 64;  // 16-byte pieces per lane
   constexpr int FC = 16 / (int)sizeof(T);      // features per piece
   constexpr int FS = 64 / (int)sizeof(T);      // feature stride between a lane's pieces
-  constexpr int FL = NC * FC;                  // features per lane
   __shared__ __align__(16) float S[D], E[D];
   __shared__ float nrm[2];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
