@@ -612,11 +612,13 @@ __global__ void __launch_bounds__(NT, 1)
           __syncwarp();
           if (lane == 0) tc::mbar_arrive(B.tempty + slot);
         }
-        // add the four warpgroups' shares (fixed order) and store the key's mass;
-        // the exchange buffer alternates between tiles, so one barrier per tile suffices
+        // add the four warpgroups' shares (fixed order) and store the key's mass.
+        // Only the four warps on the same TMEM lane quarter (the same 32 keys)
+        // exchange, so they meet at their quarter's own barrier; the exchange
+        // buffer alternates between tiles, so one barrier per tile suffices
         float *red = sRed + (kt & 1) * 4 * KT;
         if (wg > 0) red[wg * KT + key_in_tile] = acc;
-        tc::named_bar_sync(1, EPI_THREADS);
+        tc::named_bar_sync(2 + quarter, 4 * 32);
         if (ok && wg == 0 && j < w.j1)
           dst[j] = acc + (red[KT + key_in_tile] + red[2 * KT + key_in_tile] + red[3 * KT + key_in_tile]);
       }
