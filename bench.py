@@ -108,6 +108,26 @@ def score_flops(wl):
     return 2 * wl.d * score_pairs(wl) * wl.units
 
 
+# ex2 results per clock per SM of this GPU's special-function units, measured with a
+# register-only probe (a dependent-free stream of ex2.approx.ftz.f32 on every SM)
+SFU_EX2_PER_CLK_SM = 31.4
+
+
+def sfu_fraction(wl, score_s, clocks, sms):
+    """Exponentials per second of the scoring against the SFU rate of `sms` SMs at the
+    sampled SM clock: one exp per visible (row, key) pair algorithmically, two as
+    executed."""
+    mhz = clocks.get("sm_mhz") or clocks.get("sm_max_mhz")
+    if not mhz:
+        return {}
+    peak = SFU_EX2_PER_CLK_SM * sms * mhz * 1e6
+    exps = score_pairs(wl) * wl.units
+    return {"sfu_exp_per_s": exps / score_s, "sfu_peak": peak,
+            "sfu_peak_kind": f"probe-measured {SFU_EX2_PER_CLK_SM} ex2/clock/SM x {sms} SMs x "
+                             f"{mhz:.0f} MHz (sampled)",
+            "sfu_frac": exps / score_s / peak, "sfu_executed_frac": 2 * exps / score_s / peak}
+
+
 def score_flops_executed(wl):
     """Flops the two-pass kernels issue: both passes over every visible pair."""
     return 2 * score_flops(wl)
@@ -435,7 +455,7 @@ def time_next_rows(pipe, reps=5, warmup=3):
 OTHER_WORKLOADS = ("llama2-7b-layer", "h2o-decode", "gqa-prefill")
 
 
-def time_workload(name, reps=5):
+def time_workload(name, reps=5, clocks=None):
     """One of the pages' other workloads on its own buffers, outside the timed step:
     the prefill chain (and the decode steps, where the workload has them) captured
     as CUDA graphs and replayed, each replay timed with events on the launching
@@ -489,6 +509,11 @@ def time_workload(name, reps=5):
                      "tflops": score_flops(wl) / score_s / 1e12,
                      "tensor_frac": score_flops(wl) / score_s / 1e12 / peak_tf,
                      "hbm_frac": alg["kv_score_obs"] / score_s / 1e9 / peak}}
+    sfu = sfu_fraction(wl, score_s, clocks or {},
+                       torch.cuda.get_device_properties(0).multi_processor_count)
+    if sfu:
+        out["score"]["sfu_frac"] = sfu["sfu_frac"]
+        out["score"]["sfu_executed_frac"] = sfu["sfu_executed_frac"]
     if wl.n_decode:
         step_ms = statistics.median(td) / wl.n_decode
         out["decode"] = {"steps": wl.n_decode, "ms_per_step": step_ms,
@@ -746,12 +771,14 @@ def run_ours(args, wl, rank, world):
                                    "executed = both passes (statistics, column mass)"},
         "clocks": clk.summary(),
     }
+    line["roofline_score"].update(sfu_fraction(
+        wl, score_s, line["clocks"], torch.cuda.get_device_properties(dev).multi_processor_count))
     if not args.no_next_rows:
         line["next_rows"] = time_next_rows(pipe)
     if not args.no_other_workloads and world == 1:
         # the pages' other workloads, each on its own buffers (about 20 GB beside the
         # headline workload's, far below the GPU's memory)
-        line["other_workloads"] = {nm: time_workload(nm) for nm in OTHER_WORKLOADS
+        line["other_workloads"] = {nm: time_workload(nm, clocks=line["clocks"]) for nm in OTHER_WORKLOADS
                                    if nm != wl.name}
     if not args.no_e2e:
         if world > 1:

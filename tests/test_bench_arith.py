@@ -2,6 +2,8 @@
 `bench.py` divides by its event times, checked against the per-unit figures
 worked out by hand for the long-context workload (32 layers x 8 KV heads,
 G = 4 query heads per KV head, W = 64, d = 128, T = 131072, k = cap = 6553, bf16)."""
+import pytest
+
 import bench
 from kv_cache_compression_obs_gb300 import configs
 
@@ -63,3 +65,17 @@ def test_whole_job_rate_counts_every_rank():
     # value = KV tokens (rows x T) of all ranks over the slowest rank's step time
     assert bench.whole_job_rate(WL.rows * WL.T, 1, 0.02338) == WL.rows * WL.T / 0.02338
     assert bench.whole_job_rate(100, 4, 2.0) == 200.0
+
+
+def test_sfu_fraction_counts_one_exp_per_visible_pair():
+    """The scoring's SFU fraction: one exponential per causally visible (row, key)
+    pair (two as executed), against ex2/clock/SM x SMs x the sampled clock."""
+    wl = configs.LONG_CONTEXT
+    f = bench.sfu_fraction(wl, 2.0e-3, {"sm_mhz": 2000.0, "sm_max_mhz": 2070.0}, 152)
+    exps = bench.score_pairs(wl) * wl.units
+    peak = bench.SFU_EX2_PER_CLK_SM * 152 * 2000.0e6
+    assert f["sfu_peak"] == pytest.approx(peak)
+    assert f["sfu_exp_per_s"] == pytest.approx(exps / 2.0e-3)
+    assert f["sfu_frac"] == pytest.approx(exps / 2.0e-3 / peak)
+    assert f["sfu_executed_frac"] == pytest.approx(2 * f["sfu_frac"])
+    assert bench.sfu_fraction(wl, 1.0, {}, 152) == {}
