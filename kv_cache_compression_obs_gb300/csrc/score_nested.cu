@@ -157,7 +157,7 @@ __device__ __forceinline__ float reduce_scatter_group(float (&v)[V], int g) {
 }
 
 template <typename T, int D>
-__global__ __launch_bounds__(NT_ANCH) void anchors_kernel(const T *__restrict__ K, int Tn,
+__global__ __launch_bounds__(NT_ANCH, 7) void anchors_kernel(const T *__restrict__ K, int Tn,
                                                           int blk, int n_blocks, int window,
                                                           float *__restrict__ esum,
                                                           float *__restrict__ a) {
@@ -168,7 +168,8 @@ __global__ __launch_bounds__(NT_ANCH) void anchors_kernel(const T *__restrict__ 
   // sit at least window + 1 rows back), so no two lanes touch a slot in the same
   // batch.
   extern __shared__ float ring_all[];
-  __shared__ float sums[NSTREAM][D];
+  __shared__ __align__(16) float sums[NSTREAM][D];  // a stream's sum of kh over [c0, e), then [s, e)
+  __shared__ __align__(16) float sils[NSTREAM][D];  // a stream's sum of kh over [c0, s)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane & (GW - 1);     // lane within the stream's group
   const int gbase = lane & ~(GW - 1);  // the group's first lane
@@ -189,9 +190,12 @@ __global__ __launch_bounds__(NT_ANCH) void anchors_kernel(const T *__restrict__ 
   const int span = ((hi - lo + NSTREAM - 1) / NSTREAM + window - 1) / window * window;
   const int s = min(hi, lo + sid * span), e = min(hi, s + span);
   const bool live = s < e;
-  float2 tot[P2], sil[P2];  // sums of kh over [c0, e) and over [c0, s)
+  // this lane's pairs of the stream's sums (kept in shared memory: they change
+  // once a chunk)
+  auto tot = [&](int p) -> float2 & { return *reinterpret_cast<float2 *>(&sums[sid][R::feature(g, p)]); };
+  auto sil = [&](int p) -> float2 & { return *reinterpret_cast<float2 *>(&sils[sid][R::feature(g, p)]); };
 #pragma unroll
-  for (int p = 0; p < P2; ++p) tot[p] = sil[p] = make_float2(0.f, 0.f);
+  for (int p = 0; p < P2; ++p) sil(p) = make_float2(0.f, 0.f);
 
   const int c0 = (s / window) * window;  // the chunk start the stream walks from
   float2 P[P2], Q[P2];
@@ -230,7 +234,7 @@ __global__ __launch_bounds__(NT_ANCH) void anchors_kernel(const T *__restrict__ 
   }
   // the first chunk reset moves the warm-up total into Q; keep it out of `tot`
 #pragma unroll
-  for (int p = 0; p < P2; ++p) tot[p] = make_float2(-P[p].x, -P[p].y);
+  for (int p = 0; p < P2; ++p) tot(p) = make_float2(-P[p].x, -P[p].y);
   __syncwarp();
   int r = 0;         // i - (chunk start), i.e. i % window, kept as a running counter
   int rs = c0 % RW;  // i0 % RW
@@ -297,7 +301,7 @@ __global__ __launch_bounds__(NT_ANCH) void anchors_kernel(const T *__restrict__ 
         if ((!FAST || t == 0) && r == 0) {  // a new chunk: the previous total becomes Q
 #pragma unroll
           for (int p = 0; p < P2; ++p) {
-            tot[p] = __fadd2_rn(tot[p], P[p]);
+            tot(p) = __fadd2_rn(tot(p), P[p]);
             Q[p] = P[p];
             P[p] = make_float2(0.f, 0.f);
           }
@@ -317,7 +321,7 @@ __global__ __launch_bounds__(NT_ANCH) void anchors_kernel(const T *__restrict__ 
         if constexpr (!FAST) {
           if (i == s - 1) {
 #pragma unroll
-            for (int p = 0; p < P2; ++p) sil[p] = P[p];
+            for (int p = 0; p < P2; ++p) sil(p) = P[p];
           }
           r = (r + 1 == window) ? 0 : r + 1;
         }
@@ -359,18 +363,12 @@ __global__ __launch_bounds__(NT_ANCH) void anchors_kernel(const T *__restrict__ 
   if (live) {
 #pragma unroll
     for (int p = 0; p < P2; ++p)
-      tot[p] = __fadd2_rn(__fadd2_rn(tot[p], P[p]), make_float2(-sil[p].x, -sil[p].y));
+      tot(p) = __fadd2_rn(__fadd2_rn(tot(p), P[p]), make_float2(-sil(p).x, -sil(p).y));
   } else {
 #pragma unroll
-    for (int p = 0; p < P2; ++p) tot[p] = make_float2(0.f, 0.f);
+    for (int p = 0; p < P2; ++p) tot(p) = make_float2(0.f, 0.f);
   }
   // block sum of kh over the streams
-#pragma unroll
-  for (int p = 0; p < P2; ++p) {
-    const int f = R::feature(g, p);
-    sums[sid][f] = tot[p].x;
-    sums[sid][f + 1] = tot[p].y;
-  }
   __syncthreads();
   for (int f = threadIdx.x; f < D; f += NT_ANCH) {
     float t = 0.f;
