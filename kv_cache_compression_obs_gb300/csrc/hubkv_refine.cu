@@ -34,7 +34,11 @@ struct CSum {
 };
 
 // Per (head, chunk): sum s and sum s ln s (0 ln 0 = 0), reduced in a fixed order
-// (per thread, then a warp butterfly in double, then the warps in order).
+// (per thread, then a warp butterfly in double, then the warps in order).  ln s
+// comes from the SFU's base-2 logarithm times ln 2 (relative error about 1e-7
+// for the scores' range, far below what the head weights need).  A chunk's
+// scores move as 16-byte vectors, four a thread in flight, when the head's row
+// is 16-byte aligned; otherwise as scalars.
 __global__ __launch_bounds__(NT) void refine_entropy_kernel(const float *__restrict__ s, int T,
                                                             int n_chunks,
                                                             double2 *__restrict__ part) {
@@ -43,17 +47,39 @@ __global__ __launch_bounds__(NT) void refine_entropy_kernel(const float *__restr
   const float *sv = s + head * (long)T;
   const int i0 = chunk * kChunk, i1 = min(T, i0 + kChunk);
   CSum a, c;
-  for (int base = i0 + threadIdx.x; base < i1; base += 4 * NT) {
-    float x[4];
+  auto add = [&](float x) {
+    a.add(x);
+    if (x > 0.f) c.add(x * (__log2f(x) * 0.69314718f));
+  };
+  if ((reinterpret_cast<uintptr_t>(sv + i0) & 15) == 0) {
+    const int n4 = (i1 - i0) >> 2;
+    const float4 *v4 = reinterpret_cast<const float4 *>(sv + i0);
+    for (int base = threadIdx.x; base < n4; base += 4 * NT) {
+      float4 x[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {  // four loads in flight per thread
-      const int i = base + u * NT;
-      x[u] = i < i1 ? __ldg(sv + i) : 0.f;
+      for (int u = 0; u < 4; ++u) {
+        const int j = base + u * NT;
+        x[u] = j < n4 ? __ldg(v4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        add(x[u].x);
+        add(x[u].y);
+        add(x[u].z);
+        add(x[u].w);
+      }
     }
+    for (int i = i0 + 4 * n4 + threadIdx.x; i < i1; i += NT) add(__ldg(sv + i));
+  } else {
+    for (int base = i0 + threadIdx.x; base < i1; base += 4 * NT) {
+      float x[4];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      a.add(x[u]);
-      if (x[u] > 0.f) c.add(x[u] * logf(x[u]));
+      for (int u = 0; u < 4; ++u) {  // four loads in flight per thread
+        const int i = base + u * NT;
+        x[u] = i < i1 ? __ldg(sv + i) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) add(x[u]);
     }
   }
   double ra = a.value(), rc = c.value();
