@@ -229,7 +229,7 @@ __device__ uint64_t select_in_bucket(Smem &sm, uint64_t prefix, int need, Visit 
       if ((key & hmask) == prefix) atomicAdd(&sm.h256[(uint32_t)(key >> sh) & dmask], 1u);
     });
     __syncthreads();
-    if (warp == 0) digit_boundary<NT>(sm.h256, need, prefix, sh, sm.rx);
+    if (warp == 0) digit_boundary(sm.h256, need, prefix, sh, sm.rx);
     __syncthreads();
     prefix = sm.rx.sh_prefix;
     need = sm.rx.sh_need;
@@ -299,7 +299,7 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
         if ((int)(key >> kBinShift) == b1) atomicAdd(&sm.h8[(uint32_t)(key >> kSubShift) & 255u], 1u);
       });
       __syncthreads();
-      if (warp == 0) digit_boundary<NT>(sm.h8, need1, (uint64_t)b1 << kBinShift, kSubShift, sm.rx);
+      if (warp == 0) digit_boundary(sm.h8, need1, (uint64_t)b1 << kBinShift, kSubShift, sm.rx);
       __syncthreads();
       const uint64_t pb = sm.rx.sh_prefix;  // the bucket: its top 20 bits, zeros below
       const int need2 = sm.rx.sh_need;
@@ -393,7 +393,7 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
       sm.g8[d] = g;
     }
     __syncthreads();
-    if (warp == 0) digit_boundary<NT>(sm.g8, needt1, (uint64_t)bt << kBinShift, kSubShift, sm.rx);
+    if (warp == 0) digit_boundary(sm.g8, needt1, (uint64_t)bt << kBinShift, kSubShift, sm.rx);
     __syncthreads();
     const uint64_t pt = sm.rx.sh_prefix;
     const int needt2 = sm.rx.sh_need;

@@ -50,11 +50,15 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int *warp_sums, int *
 
 namespace kvc {
 
-// Scratch of radix_select_ge for an NT-thread block.
-template <int NT>
+// Scratch of radix_select_ge for an NT-thread block; warp w counts into
+// histogram copy w % HC (HC a power of two dividing the warps: fewer copies, less
+// shared memory, more atomics on one copy).
+template <int NT, int HC = NT / 32>
 struct RadixScratch {
   static constexpr int NW = NT / 32;
-  uint32_t hist[NW][256];  // per-warp histograms
+  static constexpr int NH = HC;
+  static_assert((HC & (HC - 1)) == 0 && NW % HC == 0, "histogram copies must divide the warps");
+  uint32_t hist[HC][256];  // histogram copies
   uint32_t tot[2][256];    // this CTA's histogram of a pass (read by the cluster)
   uint32_t gsum[256];      // the (cluster's) histogram of a pass
   uint64_t sh_prefix;
@@ -65,9 +69,9 @@ struct RadixScratch {
 // where the count at or above it first reaches `need`.  Writes sm.sh_prefix
 // (prefix with that digit at `shift`), sm.sh_need (how many of the digit's keys
 // are needed) and sm.sh_done (whether that is all of them).
-template <int NT>
+template <typename Scratch>
 __device__ __forceinline__ void digit_boundary(const uint32_t *h, int need, uint64_t prefix, int shift,
-                                               RadixScratch<NT> &sm) {
+                                               Scratch &sm) {
   const int lane = threadIdx.x & 31;
   uint32_t mine = 0;
 #pragma unroll
@@ -107,10 +111,10 @@ __device__ __forceinline__ void digit_boundary(const uint32_t *h, int need, uint
 // visit_hi (optional): visit_hi(f) calls f(key >> 32) for every candidate; the
 // four passes over the high word then use 32-bit keys.  pass0_filled: the caller
 // has already histogrammed the top byte (key >> 56) into sm.hist (per warp).
-template <int NT, bool CLUSTER, typename Visit, typename VisitHi = std::nullptr_t>
-__device__ uint64_t radix_select_ge(RadixScratch<NT> &sm, int need, Visit visit,
+template <int NT, bool CLUSTER, typename Visit, typename VisitHi = std::nullptr_t, int HC = NT / 32>
+__device__ uint64_t radix_select_ge(RadixScratch<NT, HC> &sm, int need, Visit visit,
                                     VisitHi visit_hi = nullptr, bool pass0_filled = false) {
-  constexpr int NW = NT / 32;
+  const int hw = (threadIdx.x >> 5) & (HC - 1);  // this warp's histogram copy
   constexpr bool HI32 = !std::is_same<VisitHi, std::nullptr_t>::value;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint64_t prefix = 0, hmask = 0;
@@ -119,7 +123,7 @@ __device__ uint64_t radix_select_ge(RadixScratch<NT> &sm, int need, Visit visit,
     const int buf = pass & 1;
     if (!(pass == 0 && pass0_filled)) {
       if (pass == 0) {  // later passes find the histograms zeroed by the previous reduction
-        for (int e = threadIdx.x; e < NW * 256; e += NT) (&sm.hist[0][0])[e] = 0u;
+        for (int e = threadIdx.x; e < HC * 256; e += NT) (&sm.hist[0][0])[e] = 0u;
         __syncthreads();
       }
       bool done_hi = false;
@@ -128,21 +132,21 @@ __device__ uint64_t radix_select_ge(RadixScratch<NT> &sm, int need, Visit visit,
           const uint32_t p32 = (uint32_t)(prefix >> 32), m32 = (uint32_t)(hmask >> 32);
           const int sh = shift - 32;
           visit_hi([&](uint32_t k) {
-            if ((k & m32) == p32) atomicAdd(&sm.hist[warp][(k >> sh) & 255u], 1u);
+            if ((k & m32) == p32) atomicAdd(&sm.hist[hw][(k >> sh) & 255u], 1u);
           });
           done_hi = true;
         }
       }
       if (!done_hi)
         visit([&](uint64_t key) {
-          if ((key & hmask) == prefix) atomicAdd(&sm.hist[warp][(uint32_t)(key >> shift) & 255u], 1u);
+          if ((key & hmask) == prefix) atomicAdd(&sm.hist[hw][(uint32_t)(key >> shift) & 255u], 1u);
         });
     }
     __syncthreads();
     for (int d = threadIdx.x; d < 256; d += NT) {
       uint32_t t = 0;
 #pragma unroll 8
-      for (int w = 0; w < NW; ++w) {
+      for (int w = 0; w < HC; ++w) {
         t += sm.hist[w][d];
         sm.hist[w][d] = 0u;  // ready for the next pass (barriers follow before its visit)
       }

@@ -137,9 +137,12 @@ constexpr int NWC = NTC / 32;
 constexpr int kSliceSmall = 16384;  // keys per CTA with two CTAs per SM
 constexpr int kSliceMax = 49152;    // keys per CTA at most (192 KB)
 constexpr int kMaxCl = 8;
+// Radix histogram copies of the resident kernel (each shared by four warps): the
+// smaller scratch lets three CTAs share an SM when their registers allow it.
+constexpr int kHistCopies = 4;
 
 struct ResidentSmem {
-  RadixScratch<NTC> rx;
+  RadixScratch<NTC, kHistCopies> rx;
   int wcnt[NWC];
   int cnt[kMaxCl];
 };
@@ -170,7 +173,7 @@ __global__ __launch_bounds__(NTC) void select_topk_resident_kernel(
   const int lo = min(n, rank * len), hi = min(n, lo + len), m = hi - lo;
   const int half = MODE == 0 ? 0 : ra.half;
   const float *row = z + head * (long)T;  // z, or the base scores s (MODE 1 / 2)
-  for (int e = threadIdx.x; e < NWC * 256; e += NTC) (&sm.rx.hist[0][0])[e] = 0u;
+  for (int e = threadIdx.x; e < kHistCopies * 256; e += NTC) (&sm.rx.hist[0][0])[e] = 0u;
 
   // The slice with a halo of `half` on each side (-inf past the prompt's ends):
   // tile[t] = row[p0 + t].  The tile starts `toff` floats into the buffer so
@@ -218,7 +221,7 @@ __global__ __launch_bounds__(NTC) void select_topk_resident_kernel(
   auto put = [&](int i, float zi) {
     const uint32_t kk = order_key(zi);
     keys[i] = kk;
-    atomicAdd(&sm.rx.hist[warp][kk >> 24], 1u);
+    atomicAdd(&sm.rx.hist[warp & (kHistCopies - 1)][kk >> 24], 1u);
     if (zo) zo[S + lo + i] = zi;
   };
   if (MODE == 1 && half == 2) {
