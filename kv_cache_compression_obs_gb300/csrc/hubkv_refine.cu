@@ -142,7 +142,7 @@ template <bool AVG>
 __global__ __launch_bounds__(NT) void refine_apply_kernel(
     const float *__restrict__ s, int T, int blocks_per_head, int half, float gamma, float r2,
     const float *__restrict__ beta_ws, float *__restrict__ z) {
-  extern __shared__ float tile[];
+  extern __shared__ __align__(16) float tile_raw[];
   const long head = blockIdx.x / blocks_per_head;
   const int blk = blockIdx.x % blocks_per_head;
   const float beta = beta_ws[head];
@@ -150,13 +150,61 @@ __global__ __launch_bounds__(NT) void refine_apply_kernel(
   float *zv = z + head * (long)T;
   const int i0 = blk * kApply, i1 = min(T, i0 + kApply);
   const int lo = i0 - half, n = (i1 - i0) + 2 * half;
-  for (int t = threadIdx.x; t < n; t += NT) {
-    const int i = lo + t;
-    tile[t] = (i >= 0 && i < T) ? sv[i] : -INFINITY;
+  // tile[t] = s[lo + t] (-inf past the prompt's ends), placed `toff` floats into
+  // the buffer so that it has the global addresses' 16-byte phase: the aligned
+  // middle moves as 16-byte vectors, the ragged ends as scalars
+  const int rmis = (int)((reinterpret_cast<uintptr_t>(sv) >> 2) & 3);
+  const int toff = (((rmis + lo) % 4) + 4) % 4;
+  float *tile = tile_raw + toff;
+  {
+    const int c0 = max(lo, 0), c1 = min(lo + n, T);
+    const int a0 = min(c1, c0 + (4 - (rmis + c0) % 4) % 4);
+    const int e0 = max(a0, c1 - (rmis + c1) % 4);
+    const int n4 = (e0 - a0) >> 2;
+    const float4 *g4 = reinterpret_cast<const float4 *>(sv + a0);
+    float4 *t4 = reinterpret_cast<float4 *>(tile + (a0 - lo));
+    for (int j = threadIdx.x; j < n4; j += NT) t4[j] = __ldg(g4 + j);
+    const int front = a0 - lo, back = lo + n - e0;
+    for (int t = threadIdx.x; t < front + back; t += NT) {
+      const int tt = t < front ? t : (e0 - lo) + (t - front);
+      const int i = lo + tt;
+      tile[tt] = (i >= 0 && i < T) ? __ldg(sv + i) : -INFINITY;
+    }
   }
   __syncthreads();
-  for (int i = i0 + threadIdx.x; i < i1; i += NT)
-    zv[i] = hub_gate<AVG>(tile + (i - lo), half, i, T, gamma, r2, beta);
+  if (!AVG && half == 2) {
+    // local hubs over a window of 5, four consecutive candidates a thread: the 8
+    // scores around them give the four window maxima from shared pair maxima
+    // (the same values as hub_gate: a maximum does not depend on its order)
+    const bool vec = ((reinterpret_cast<uintptr_t>(zv + i0)) & 15) == 0;
+    for (int c = i0 + 4 * threadIdx.x; c < i1; c += 4 * NT) {
+      const float *w = tile + (c - 2 - lo);  // s of positions c-2 .. c+5
+      float x[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) x[q] = w[q];
+      const float m01 = fmaxf(x[0], x[1]), m23 = fmaxf(x[2], x[3]), m45 = fmaxf(x[4], x[5]),
+                  m67 = fmaxf(x[6], x[7]);
+      const float M[4] = {fmaxf(fmaxf(m01, m23), x[4]), fmaxf(fmaxf(x[1], m23), m45),
+                          fmaxf(fmaxf(m23, m45), x[6]), fmaxf(fmaxf(x[3], m45), m67)};
+      float zq[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float si = x[q + 2];
+        const float qi = (si == M[q]) ? si : gamma * si;
+        zq[q] = fmaf(r2, fmaf(beta, qi, -si), si);
+      }
+      if (vec && c + 4 <= i1) {
+        *reinterpret_cast<float4 *>(zv + c) = make_float4(zq[0], zq[1], zq[2], zq[3]);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (c + q < i1) zv[c + q] = zq[q];
+      }
+    }
+  } else {
+    for (int i = i0 + threadIdx.x; i < i1; i += NT)
+      zv[i] = hub_gate<AVG>(tile + (i - lo), half, i, T, gamma, r2, beta);
+  }
 }
 
 }  // namespace
@@ -186,7 +234,7 @@ int launch_refine_apply(const float *s, int B, int H, int T, int half, float gam
                         const float *beta_ws, float *z, cudaStream_t st) {
   const long heads = (long)B * H;
   const int bph = (T + kApply - 1) / kApply;
-  const size_t smem = (size_t)(kApply + 2 * half) * sizeof(float);
+  const size_t smem = (size_t)(kApply + 2 * half + 16) * sizeof(float);
   if (flags & KV_HUB_AVGPOOL)
     refine_apply_kernel<true><<<(unsigned)(heads * bph), NT, smem, st>>>(s, T, bph, half, gamma, r * r,
                                                                       beta_ws, z);
