@@ -133,13 +133,14 @@ def score_flops_executed(wl):
     return 2 * score_flops(wl)
 
 
-# DRAM bytes per decode step (all its launches: the two row halves' stream and
-# finalize kernels) from `ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum`,
-# captured on 8 of the 32 layers of the long-context workload (mean over four
-# halves, scaled by 4: the step's traffic is proportional to the units), with the
+# DRAM bytes per decode step and unit (all the step's launches: the two row halves'
+# stream and finalize kernels) from `ncu --metrics dram__bytes_read.sum,
+# dram__bytes_write.sum`, captured on 8 of the 32 layers of the long-context
+# workload (mean over four row halves of 32 units each; the traffic is
+# proportional to the units, so a run on fewer layers scales it), with the
 # SHA-256 of the decode kernel source it was taken on.  When the source has
 # changed since, the figure no longer describes the kernel and is reported as null.
-DECODE_TRAFFIC = {"long-context": 4 * 2 * (107470016 + 897536 + 5472576)}
+DECODE_TRAFFIC_PER_UNIT = {"long-context": (107470016 + 897536 + 5472576) / 32}
 DECODE_TRAFFIC_SOURCE = "kv_cache_compression_obs_gb300/csrc/h2o_decode.cu"
 DECODE_TRAFFIC_SOURCE_SHA256 = "20c1313e366e778898cf19320ffdbee6ee33b6b3d030d9bb99bdd90496642201"
 
@@ -724,9 +725,9 @@ def run_ours(args, wl, rank, world):
     dom = max(phases, key=lambda n: phases[n] * (wl.n_decode if n == "h2o_decode_step" else 1))
     achieved = per_launch[dom] / (phases[dom] / 1e3) / 1e9
     traffic, traffic_source = None, None
-    if dom == "h2o_decode_step" and wl.name in DECODE_TRAFFIC:
+    if dom == "h2o_decode_step" and wl.name in DECODE_TRAFFIC_PER_UNIT:
         if _source_sha256(DECODE_TRAFFIC_SOURCE) == DECODE_TRAFFIC_SOURCE_SHA256:
-            traffic = DECODE_TRAFFIC[wl.name]
+            traffic = round(DECODE_TRAFFIC_PER_UNIT[wl.name] * wl.units)
             traffic_source = ("ncu dram__bytes_read.sum + dram__bytes_write.sum of the decode "
                               "launches, taken on this decode source (sha256 "
                               f"{DECODE_TRAFFIC_SOURCE_SHA256[:12]})")
