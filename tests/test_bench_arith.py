@@ -39,8 +39,10 @@ def test_decode_bytes_per_step():
     assert a["h2o_decode_step"] == UNITS * (K * (2 * ROW + 12) + G * D * 6 + 2 * ROW)
     assert a["h2o_decode_step"] == 879_963_136
     # the measured DRAM traffic the bench reports beside it is that, plus a few percent
-    traffic = bench.DECODE_TRAFFIC["long-context"]
+    traffic = bench.DECODE_TRAFFIC_PER_UNIT["long-context"] * WL.units
     assert 1.0 <= traffic / a["h2o_decode_step"] <= 1.1
+    # kept per unit: a run on fewer layers gets the same traffic per unit
+    assert bench.DECODE_TRAFFIC_PER_UNIT["long-context"] * WL.scaled(L=2).units == traffic / 16
 
 
 def test_score_flops_one_contraction_over_visible_pairs():
