@@ -659,6 +659,42 @@ def cpu_baseline(wl, pipe, budget_s=20.0):
             "decode_steps_per_s": 1.0 / per_step_dec if n_dec else None}
 
 
+def oracle_single_thread(names=("tiny", "llama2-7b-layer")):
+    """The oracle's prefill chain (score, refine, Top-K, compaction) on one OpenMP
+    thread, on the small workloads' first batch row: seconds per call and KV
+    tokens/s, beside the multi-core baseline."""
+    import ctypes
+
+    import oracle
+    from kv_cache_compression_obs_gb300 import configs, gen
+
+    try:
+        gomp = ctypes.CDLL("libgomp.so.1")
+    except OSError:
+        return None
+    before = gomp.omp_get_max_threads()
+    out = {}
+    try:
+        gomp.omp_set_num_threads(1)
+        for nm in names:
+            wl = configs.BY_NAME[nm]
+            Q, K, V = gen.prefill_inputs(wl, units=list(range(wl.Hkv)))
+            Qh, Kh, Vh = (gen.to_numpy_bits(x) for x in (Q, K, V))
+            Qh = Qh.reshape(1, wl.Hq, wl.W, wl.d)
+            Kh, Vh = Kh.reshape(1, wl.Hkv, wl.T, wl.d), Vh.reshape(1, wl.Hkv, wl.T, wl.d)
+            t0 = time.perf_counter()
+            s = oracle.score_obs(Qh, Kh, wl.scale)
+            z = oracle.hubkv_refine(s, wl.r, wl.gamma, wl.pool_width, wl.beta_lo, wl.beta_hi)[0] \
+                if wl.r is not None else s
+            idx = oracle.select_topk(z, wl.k, wl.R)
+            oracle.compact(Kh, Vh, s, idx, wl.cap)
+            dt = time.perf_counter() - t0
+            out[nm] = {"s": dt, "kv_tokens_per_s": wl.T / dt, "threads": 1}
+    finally:
+        gomp.omp_set_num_threads(before)
+    return out
+
+
 def max_over_ranks(x: float, world: int, device) -> float:
     """The largest of every rank's x: the job is as slow as its slowest rank."""
     if world <= 1:
@@ -790,6 +826,9 @@ def run_ours(args, wl, rank, world):
                        "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, pipe)
+        st = oracle_single_thread()
+        if st:
+            line["cpu_baseline"]["single_thread_prefill"] = st
     return line
 
 
