@@ -75,23 +75,36 @@ struct Smem {
   int wth[kMaxOwned][NW];      // middle pairs >= theta_h per (owned head, warp range)
   int wtau[kMaxOwned][NW];     // middle pairs above tau's bucket per (owned head, warp range)
   int thok[kMaxOwned];         // wth holds the counts
-  uint32_t h8[256];            // second-digit histogram of one bin
-  uint32_t g8[256];            // the cluster's sum of it (competition)
+  int b1[kMaxOwned];           // theta_h's 12-bit bin (kBins: no floor)
+  int need1[kMaxOwned];        // pairs of that bin at or above theta_h
+  uint32_t p20h[kMaxOwned];    // theta_h's 20-bit bucket (~0u: none gathered)
+  int need2[kMaxOwned];        // pairs of that bucket at or above theta_h
+  int big[kMaxOwned];          // the bucket is too large to gather
+  uint32_t h8[256];            // second-digit histogram of theta_h's bin
+  uint32_t h8c[256];           // this CTA's second digits of tau's bin (competition)
+  uint32_t g8[256];            // the cluster's sum of them
   uint32_t h256[256];          // digit histogram of the selects inside a bucket
   int wsum[NW];
   int lnr[kMaxCluster];        // competition bucket pairs held per CTA (pushed)
   int ovr[kMaxCluster];        // competition bucket overflowed per CTA (pushed)
-  int bin, need, above, list_n, red;
+  int bin, need, above, list_n, tl_n, red;
 };
 
-// Dynamic shared memory: the 12-bit histogram (also the cluster's summed
-// competition histogram), the competition's 12-bit histogram of this CTA,
-// and the gathered bucket pairs.
-struct Dyn {
-  uint32_t hist[kBins];
-  uint32_t comp[kBins];
-  uint64_t list[kListCap];
+// Dynamic shared memory.  Steps 1-2: the 12-bit histogram of one head (then the
+// cluster's summed competition histogram) and the competition's 12-bit
+// histogram of this CTA (read by the cluster).  Step 3 on: the same bytes hold
+// the gathered pairs of one head's floor bucket and of the competition's bucket.
+union Dyn {
+  struct {
+    uint32_t hist[kBins];
+    uint32_t comp[kBins];
+  } h;
+  struct {
+    uint64_t tlist[kListCap];
+    uint64_t clist[kListCap];
+  } l;
 };
+static_assert(sizeof(uint64_t) * kListCap == sizeof(uint32_t) * kBins, "lists overlay the histograms");
 
 // A head's middle range [0, n) split for 16-byte loads: `pre` scalars up to the
 // first 16-byte boundary, n4 float4 vectors, then the scalars from `tail` on.
@@ -116,8 +129,18 @@ __device__ __forceinline__ int warp_of(int i, const Split &sp, int per4) {
   return ((i - sp.pre) >> 2) / per4;
 }
 
-// Calls f(key) for the middle pairs of one head, positions [S, S + n), with
-// strided coalesced 16-byte loads, eight in flight per thread.
+// A pair's order key (the high word of its 64-bit key) and its flat index
+// h*T + position; the streams pass these, and the 64-bit key is formed only
+// where a pair is kept in a list.  Comparisons against a 64-bit threshold:
+__device__ __forceinline__ bool key_ge(uint32_t ok, uint32_t flat, uint64_t thr) {
+  const uint32_t th = (uint32_t)(thr >> 32);
+  return ok > th || (ok == th && 0xFFFFFFFFu - flat >= (uint32_t)thr);
+}
+constexpr int kBinShift32 = kBinShift - 32;  // the bins and buckets on the order key
+constexpr int kSubShift32 = kSubShift - 32;
+
+// Calls f(order key, flat index) for the middle pairs of one head, positions
+// [S, S + n), with strided coalesced 16-byte loads, eight in flight per thread.
 template <typename F>
 __device__ __forceinline__ void for_head(const float *__restrict__ zm, uint32_t flat0, int n, F &&f) {
   const Split sp = split_of(zm, n);
@@ -134,23 +157,23 @@ __device__ __forceinline__ void for_head(const float *__restrict__ zm, uint32_t 
       const int j = base + u * NT;
       if (j < sp.n4) {
         const uint32_t i = flat0 + (uint32_t)(sp.pre + 4 * j);
-        f(pair_key(v[u].x, i));
-        f(pair_key(v[u].y, i + 1));
-        f(pair_key(v[u].z, i + 2));
-        f(pair_key(v[u].w, i + 3));
+        f(order_key(v[u].x), i);
+        f(order_key(v[u].y), i + 1);
+        f(order_key(v[u].z), i + 2);
+        f(order_key(v[u].w), i + 3);
       }
     }
   }
   const int t = threadIdx.x, nt = n - sp.tail;
-  if (t < sp.pre) f(pair_key(__ldg(zm + t), flat0 + (uint32_t)t));
+  if (t < sp.pre) f(order_key(__ldg(zm + t)), flat0 + (uint32_t)t);
   else if (t < sp.pre + nt) {
     const int i = sp.tail + (t - sp.pre);
-    f(pair_key(__ldg(zm + i), flat0 + (uint32_t)i));
+    f(order_key(__ldg(zm + i)), flat0 + (uint32_t)i);
   }
 }
 
-// Calls f(key) for the middle pairs of this warp's range (see warp_of), eight
-// 16-byte loads in flight per lane.
+// Calls f(order key, flat index) for the middle pairs of this warp's range (see
+// warp_of), eight 16-byte loads in flight per lane.
 template <typename F>
 __device__ __forceinline__ void for_warp(const float *__restrict__ zm, uint32_t flat0, int n, F &&f) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -158,7 +181,7 @@ __device__ __forceinline__ void for_warp(const float *__restrict__ zm, uint32_t 
   const float4 *z4 = reinterpret_cast<const float4 *>(zm + sp.pre);
   const int per4 = (sp.n4 + NW - 1) / NW;
   const int b0 = min(sp.n4, warp * per4), b1 = min(sp.n4, b0 + per4);
-  if (warp == 0 && lane < sp.pre) f(pair_key(__ldg(zm + lane), flat0 + (uint32_t)lane));
+  if (warp == 0 && lane < sp.pre) f(order_key(__ldg(zm + lane)), flat0 + (uint32_t)lane);
   for (int q0 = b0 + lane; q0 < b1; q0 += 8 * 32) {
     float4 v[8];
 #pragma unroll
@@ -171,15 +194,15 @@ __device__ __forceinline__ void for_warp(const float *__restrict__ zm, uint32_t 
       const int q = q0 + 32 * u;
       if (q < b1) {
         const uint32_t i = flat0 + (uint32_t)(sp.pre + 4 * q);
-        f(pair_key(v[u].x, i));
-        f(pair_key(v[u].y, i + 1));
-        f(pair_key(v[u].z, i + 2));
-        f(pair_key(v[u].w, i + 3));
+        f(order_key(v[u].x), i);
+        f(order_key(v[u].y), i + 1);
+        f(order_key(v[u].z), i + 2);
+        f(order_key(v[u].w), i + 3);
       }
     }
   }
   if (warp == NW - 1 && lane < n - sp.tail)
-    f(pair_key(__ldg(zm + sp.tail + lane), flat0 + (uint32_t)(sp.tail + lane)));
+    f(order_key(__ldg(zm + sp.tail + lane)), flat0 + (uint32_t)(sp.tail + lane));
 }
 
 // In a histogram of kBins counts (bins taken from the top), the bin where the
@@ -241,13 +264,6 @@ __device__ uint64_t select_in_bucket(Smem &sm, uint64_t prefix, int need, Visit 
   return prefix;
 }
 
-// Sum over the block of one int per thread (every thread gets it).
-__device__ __forceinline__ int block_sum(int v, Smem &sm) {
-  int total;
-  block_exclusive_scan<NT>(v, sm.wsum, &total);
-  return total;
-}
-
 __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
     const float *__restrict__ z, int H, int T, int budget, int floor_k, int R, int S,
     int32_t *__restrict__ idx_out, int32_t *__restrict__ off_out) {
@@ -271,157 +287,179 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
     return (int)(flat % (uint32_t)T) - S;
   };
 
-  for (int e = threadIdx.x; e < kBins; e += NT) dy.comp[e] = 0u;
+  for (int e = threadIdx.x; e < kBins; e += NT) dy.h.comp[e] = 0u;
   cl.sync();  // every CTA of the cluster is running before any remote access
 
-  // 1. floor thresholds of the owned heads, and the competition's 12-bit counts
+  // 1. per owned head, the 12-bit histogram: theta_h's bin, and from the counts
+  //    alone this head's share of the competition's 12-bit histogram (the bins
+  //    below theta_h's whole, theta_h's bin less the need1 pairs at or above it)
   for (int h = rank, j = 0; h < H; h += CL, ++j) {
-    const float *zm = zmid(h);
-    const uint32_t f0 = flat0(h);
-    const Split sp = split_of(zm, n);
-    const int per4 = max(1, (sp.n4 + NW - 1) / NW);
-    uint64_t th = kNone;
-    int ok = 1;  // wth[j] holds the per-warp counts of pairs >= th
-    for (int e = threadIdx.x; e < kBins; e += NT) dy.hist[e] = 0u;
-    if (threadIdx.x < NW) sm.wth[j][threadIdx.x] = 0;
+    for (int e = threadIdx.x; e < kBins; e += NT) dy.h.hist[e] = 0u;
     __syncthreads();
-    for_head(zm, f0, n, [&](uint64_t key) { atomicAdd(&dy.hist[key >> kBinShift], 1u); });
+    for_head(zmid(h), flat0(h), n, [&](uint32_t ok, uint32_t) { atomicAdd(&dy.h.hist[ok >> kBinShift32], 1u); });
     __syncthreads();
-    int b1 = kBins, d2 = 0;  // theta_h's bin and second digit (b1 = kBins: no floor)
-    int below_in_b1 = 0;     // pairs of bin b1 below theta_h
+    int b1 = kBins, need1 = 0;  // b1 = kBins: no floor, every pair below theta_h
     if (nf > 0) {
-      find_boundary(dy.hist, nf, sm);
+      find_boundary(dy.h.hist, nf, sm);
       b1 = sm.bin;
-      const int need1 = sm.need;
-      for (int d = threadIdx.x; d < 256; d += NT) sm.h8[d] = 0u;
-      __syncthreads();
-      for_head(zm, f0, n, [&](uint64_t key) {
-        if ((int)(key >> kBinShift) == b1) atomicAdd(&sm.h8[(uint32_t)(key >> kSubShift) & 255u], 1u);
-      });
-      __syncthreads();
-      if (warp == 0) digit_boundary(sm.h8, need1, (uint64_t)b1 << kBinShift, kSubShift, sm.rx);
-      __syncthreads();
-      const uint64_t pb = sm.rx.sh_prefix;  // the bucket: its top 20 bits, zeros below
-      const int need2 = sm.rx.sh_need;
-      d2 = (int)((pb >> kSubShift) & 255u);
-      const uint32_t p20 = (uint32_t)(pb >> kSubShift);
-      // pairs of the bin below the bucket (all below theta_h)
-      {
-        int c = 0;
-        for (int d = threadIdx.x; d < d2; d += NT) c += (int)sm.h8[d];
-        below_in_b1 = block_sum(c, sm);
-      }
-      if (sm.h8[d2] <= (uint32_t)kListCap) {
-        if (threadIdx.x == 0) sm.list_n = 0;
-        __syncthreads();
-        int c = 0;
-        for_warp(zm, f0, n, [&](uint64_t key) {
-          const uint32_t pk = (uint32_t)(key >> kSubShift);
-          c += pk > p20;
-          if (pk == p20) dy.list[atomicAdd(&sm.list_n, 1)] = key;
-        });
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
-        if (lane == 0) sm.wth[j][warp] = c;
-        __syncthreads();
-        const int ln = sm.list_n;
-        th = select_in_bucket(sm, pb, need2, [&](auto &&f) {
-          for (int i = threadIdx.x; i < ln; i += NT) f(dy.list[i]);
-        });
-        th = max(th, pb);  // the select stops at the first digit that settles the bucket
-        int cb = 0;
-        for (int i = threadIdx.x; i < ln; i += NT) {
-          const uint64_t key = dy.list[i];
-          if (key >= th) atomicAdd(&sm.wth[j][warp_of(pos_of(key), sp, per4)], 1);
-          else ++cb;
-        }
-        below_in_b1 += block_sum(cb, sm);
-      } else {
-        th = radix_select_ge<NT, false>(sm.rx, nf, [&](auto &&f) { for_head(zm, f0, n, f); });
-        ok = 0;
-      }
+      need1 = sm.need;
     }
-    if (threadIdx.x < CL) cl.map_shared_rank(sm.theta, threadIdx.x)[h] = th;
-    if (threadIdx.x == 0) sm.thok[j] = ok;
-    // the competition's 12-bit counts: this head's pairs below theta_h
-    if (ok) {
-      for (int e = threadIdx.x; e < kBins; e += NT)
-        if (e < b1) dy.comp[e] += dy.hist[e];
-        else if (e == b1) dy.comp[e] += (uint32_t)below_in_b1;
-    } else {
-      __syncthreads();  // hist is read above; the streamed count adds to comp
-      for_head(zm, f0, n, [&](uint64_t key) {
-        if (key < th) atomicAdd(&dy.comp[key >> kBinShift], 1u);
-      });
+    if (threadIdx.x == 0) {
+      sm.b1[j] = b1;
+      sm.need1[j] = need1;
+      sm.p20h[j] = ~0u;  // no bucket to gather (set below when there is one)
+      sm.big[j] = 0;
     }
-    __syncthreads();  // hist, h8 and the list serve the next head
+    for (int e = threadIdx.x; e < kBins; e += NT)
+      if (e < b1) dy.h.comp[e] += dy.h.hist[e];
+      else if (e == b1) dy.h.comp[e] += dy.h.hist[e] - (uint32_t)need1;
+    __syncthreads();  // hist serves the next head
   }
-  cl.sync();  // every theta and every competition histogram of the cluster complete
+  cl.sync();  // every competition histogram complete
 
-  // 2. competition over the middle pairs below their head's floor threshold
-  uint64_t tau = kNone;
-  int tau_ok = 0;  // wtau and the list hold tau's counts
+  // 2. tau's bin from the cluster's sum; one stream per owned head takes the
+  //    second digits of theta_h's bin and, where that bin lies above tau's,
+  //    of tau's bin (all of whose pairs are then below theta_h)
+  int bt = -1, needt1 = 0;
   if (extra > 0) {
-    uint32_t *gs = dy.hist;  // the cluster's sum
+    uint32_t *gs = dy.h.hist;  // the cluster's sum
     for (int e = threadIdx.x; e < kBins; e += NT) {
       uint32_t g = 0;
 #pragma unroll
       for (int r = 0; r < kMaxCluster; ++r)
-        if (r < CL) g += cl.map_shared_rank(dy.comp, r)[e];
+        if (r < CL) g += cl.map_shared_rank(dy.h.comp, r)[e];
       gs[e] = g;
     }
     __syncthreads();
     find_boundary(gs, (int)extra, sm);
-    const int bt = sm.bin, needt1 = sm.need;
-    // second digits of tau's bin, pairs below their head's theta
+    bt = sm.bin;
+    needt1 = sm.need;
+  }
+  for (int d = threadIdx.x; d < 256; d += NT) sm.h8c[d] = 0u;
+  for (int h = rank, j = 0; h < H; h += CL, ++j) {
+    const int b1 = sm.b1[j];
+    const int bc = bt < b1 ? bt : -2;  // tau's bin when below theta_h's (-2: no bin)
+    if (b1 == kBins && bc < 0) continue;  // uniform over the CTA: nothing to count
     for (int d = threadIdx.x; d < 256; d += NT) sm.h8[d] = 0u;
     __syncthreads();
-    for (int h = rank; h < H; h += CL) {
-      const uint64_t th = sm.theta[h];
-      if (th != kNone && (int)(th >> kBinShift) < bt) continue;  // nothing below theta in that bin
-      for_head(zmid(h), flat0(h), n, [&](uint64_t key) {
-        if ((int)(key >> kBinShift) == bt && key < th)
-          atomicAdd(&sm.h8[(uint32_t)(key >> kSubShift) & 255u], 1u);
-      });
+    const int b1s = b1 < kBins ? b1 : -1;
+    for_head(zmid(h), flat0(h), n, [&](uint32_t ok, uint32_t) {
+      const int b = (int)(ok >> kBinShift32);
+      if (b == b1s) atomicAdd(&sm.h8[(ok >> kSubShift32) & 255u], 1u);
+      else if (b == bc) atomicAdd(&sm.h8c[(ok >> kSubShift32) & 255u], 1u);
+    });
+    __syncthreads();
+    if (b1 < kBins) {
+      if (warp == 0) digit_boundary(sm.h8, sm.need1[j], (uint64_t)b1 << kBinShift, kSubShift, sm.rx);
+      __syncthreads();
+      const uint64_t pb = sm.rx.sh_prefix;  // theta_h's bucket: its top 20 bits, zeros below
+      const int need2 = sm.rx.sh_need;
+      const int d2 = (int)((pb >> kSubShift) & 255u);
+      if (threadIdx.x == 0) {
+        sm.p20h[j] = (uint32_t)(pb >> kSubShift);
+        sm.need2[j] = need2;
+        sm.big[j] = sm.h8[d2] > (uint32_t)kListCap;
+      }
+      // tau's bin is theta_h's: the competition takes the bin's pairs below theta_h
+      if (b1 == bt)
+        for (int d = threadIdx.x; d < 256; d += NT)
+          sm.h8c[d] += d < d2 ? sm.h8[d] : d == d2 ? sm.h8[d] - (uint32_t)need2 : 0u;
     }
-    cl.sync();  // every second-digit histogram complete
+    __syncthreads();  // h8 and the sh_* fields serve the next head
+  }
+  cl.sync();  // every second-digit histogram complete
+
+  uint64_t pt = 0;
+  uint32_t p20t = ~0u;  // tau's bucket (~0u: no competition)
+  int needt2 = 0;
+  if (extra > 0) {
     for (int d = threadIdx.x; d < 256; d += NT) {
       uint32_t g = 0;
 #pragma unroll
       for (int r = 0; r < kMaxCluster; ++r)
-        if (r < CL) g += cl.map_shared_rank(sm.h8, r)[d];
+        if (r < CL) g += cl.map_shared_rank(sm.h8c, r)[d];
       sm.g8[d] = g;
     }
     __syncthreads();
     if (warp == 0) digit_boundary(sm.g8, needt1, (uint64_t)bt << kBinShift, kSubShift, sm.rx);
     __syncthreads();
-    const uint64_t pt = sm.rx.sh_prefix;
-    const int needt2 = sm.rx.sh_need;
-    const uint32_t p20 = (uint32_t)(pt >> kSubShift);
-    // every pair of the bucket (kept by its floor or not), and per warp range the
-    // pairs above the bucket
-    if (threadIdx.x == 0) sm.list_n = 0;
+    pt = sm.rx.sh_prefix;
+    needt2 = sm.rx.sh_need;
+    p20t = (uint32_t)(pt >> kSubShift);
+    __syncthreads();  // the sh_* fields are rewritten by the selects below
+  }
+
+  // 3. per owned head, one stream gathers theta_h's bucket and tau's (every pair
+  //    of it, kept by its floor or not) and counts per warp range the pairs above
+  //    each; theta_h follows from its bucket's pairs at once
+  if (threadIdx.x == 0) sm.list_n = 0;
+  for (int h = rank, j = 0; h < H; h += CL, ++j) {
+    const float *zm = zmid(h);
+    const uint32_t f0 = flat0(h);
+    const Split sp = split_of(zm, n);
+    const int per4 = max(1, (sp.n4 + NW - 1) / NW);
+    const int big = sm.big[j];
+    const uint32_t ph = big ? ~0u : sm.p20h[j];  // ~0u: matches no pair
+    if (threadIdx.x == 0) sm.tl_n = 0;
     __syncthreads();
-    for (int h = rank, j = 0; h < H; h += CL, ++j) {
-      int c = 0;
-      for_warp(zmid(h), flat0(h), n, [&](uint64_t key) {
-        const uint32_t pk = (uint32_t)(key >> kSubShift);
-        c += pk > p20;
-        if (pk == p20) {
+    int c1 = 0, c2 = 0;
+    if (ph != ~0u || p20t != ~0u) {
+      for_warp(zm, f0, n, [&](uint32_t ok, uint32_t fl) {
+        const uint32_t pk = ok >> kSubShift32;
+        c1 += pk > ph;
+        c2 += pk > p20t;
+        if (pk == ph) dy.l.tlist[atomicAdd(&sm.tl_n, 1)] = pair_key_u(ok, fl);  // <= kListCap pairs
+        if (pk == p20t) {
           const int slot = atomicAdd(&sm.list_n, 1);
-          if (slot < kListCap) dy.list[slot] = key;
+          if (slot < kListCap) dy.l.clist[slot] = pair_key_u(ok, fl);
         }
       });
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
-      if (lane == 0) sm.wtau[j][warp] = c;
+      for (int off = 16; off > 0; off >>= 1) {
+        c1 += __shfl_xor_sync(0xFFFFFFFFu, c1, off);
+        c2 += __shfl_xor_sync(0xFFFFFFFFu, c2, off);
+      }
+    }
+    if (lane == 0) {
+      sm.wth[j][warp] = c1;
+      sm.wtau[j][warp] = c2;
     }
     __syncthreads();
-    if (threadIdx.x < CL) {
-      cl.map_shared_rank(sm.lnr, threadIdx.x)[rank] = min(sm.list_n, kListCap);
-      cl.map_shared_rank(sm.ovr, threadIdx.x)[rank] = sm.list_n > kListCap;
+    uint64_t th = kNone;
+    int ok = 1;  // wth[j] holds the per-warp counts of pairs >= th
+    if (sm.b1[j] < kBins) {
+      if (!big) {
+        const int ln = sm.tl_n;
+        const uint64_t pb = (uint64_t)ph << kSubShift;
+        th = select_in_bucket(sm, pb, sm.need2[j], [&](auto &&f) {
+          for (int i = threadIdx.x; i < ln; i += NT) f(dy.l.tlist[i]);
+        });
+        th = max(th, pb);  // the select stops at the first digit that settles the bucket
+        for (int i = threadIdx.x; i < ln; i += NT) {
+          const uint64_t key = dy.l.tlist[i];
+          if (key >= th) atomicAdd(&sm.wth[j][warp_of(pos_of(key), sp, per4)], 1);
+        }
+      } else {
+        th = radix_select_ge<NT, false>(sm.rx, nf, [&](auto &&f) {
+          for_head(zm, f0, n, [&](uint32_t ok, uint32_t fl) { f(pair_key_u(ok, fl)); });
+        });
+        ok = 0;
+      }
     }
-    cl.sync();  // every bucket list complete
+    if (threadIdx.x < CL) cl.map_shared_rank(sm.theta, threadIdx.x)[h] = th;
+    if (threadIdx.x == 0) sm.thok[j] = ok;
+    __syncthreads();  // the theta list serves the next head
+  }
+
+  // tau from the cluster's gathered pairs below their head's theta
+  uint64_t tau = kNone;
+  int tau_ok = 0;  // wtau and the list hold tau's counts
+  if (threadIdx.x < CL) {
+    cl.map_shared_rank(sm.lnr, threadIdx.x)[rank] = min(sm.list_n, kListCap);
+    cl.map_shared_rank(sm.ovr, threadIdx.x)[rank] = sm.list_n > kListCap;
+  }
+  cl.sync();  // every theta and every bucket list complete
+  if (extra > 0) {
     int ovf = 0, ltot = 0;
     for (int r = 0; r < CL; ++r) {
       ovf |= sm.ovr[r];
@@ -432,7 +470,7 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
       auto list_at = [&](int q) {
         int r = 0;
         while (q >= sm.lnr[r]) q -= sm.lnr[r++];
-        return cl.map_shared_rank(dy.list, r)[q];
+        return cl.map_shared_rank(dy.l.clist, r)[q];
       };
       tau = select_in_bucket(sm, pt, needt2, [&](auto &&f) {
         for (int q = threadIdx.x; q < ltot; q += NT) {
@@ -446,8 +484,8 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
       tau = radix_select_ge<NT, true>(sm.rx, (int)extra, [&](auto &&f) {
         for (int h = rank; h < H; h += CL) {
           const uint64_t th = sm.theta[h];
-          for_head(zmid(h), flat0(h), n, [&](uint64_t key) {
-            if (key < th) f(key);
+          for_head(zmid(h), flat0(h), n, [&](uint32_t ok, uint32_t fl) {
+            if (!key_ge(ok, fl, th)) f(pair_key_u(ok, fl));
           });
         }
       });
@@ -470,13 +508,13 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
       __syncthreads();
       const int ln = min(sm.list_n, kListCap);
       for (int i = threadIdx.x; i < ln; i += NT) {
-        const uint64_t key = dy.list[i];
+        const uint64_t key = dy.l.clist[i];
         if (head_of(key) == h && key >= lam) atomicAdd(&sm.wcnt[j][warp_of(pos_of(key), sp, per4)], 1);
       }
     } else {
       // a counting stream over the warp ranges
       int c = 0;
-      for_warp(zm, f0, n, [&](uint64_t key) { c += key >= lam; });
+      for_warp(zm, f0, n, [&](uint32_t ok, uint32_t fl) { c += key_ge(ok, fl, lam); });
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
       if (lane == 0) sm.wcnt[j][warp] = c;
@@ -525,7 +563,7 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
     int32_t *mid = out + S;
     const unsigned below = (1u << lane) - 1u;
     if (warp == 0) {
-      const bool keep = lane < sp.pre && pair_key(__ldg(zm + lane), f0 + (uint32_t)lane) >= lam;
+      const bool keep = lane < sp.pre && key_ge(order_key(__ldg(zm + lane)), f0 + (uint32_t)lane, lam);
       const unsigned m = __ballot_sync(0xFFFFFFFFu, keep);
       const int slot = run + __popc(m & below);
       if (keep && slot < kept_mid) mid[slot] = S + lane;
@@ -546,10 +584,10 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
         if (q < b1) {
           const float4 v = vv[u];
           const uint32_t fi = f0 + (uint32_t)i;
-          k0 = pair_key(v.x, fi) >= lam;
-          k1 = pair_key(v.y, fi + 1) >= lam;
-          k2 = pair_key(v.z, fi + 2) >= lam;
-          k3 = pair_key(v.w, fi + 3) >= lam;
+          k0 = key_ge(order_key(v.x), fi, lam);
+          k1 = key_ge(order_key(v.y), fi + 1, lam);
+          k2 = key_ge(order_key(v.z), fi + 2, lam);
+          k3 = key_ge(order_key(v.w), fi + 3, lam);
         }
         const int c = (int)k0 + (int)k1 + (int)k2 + (int)k3;
         int incl = c;
@@ -571,7 +609,7 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
     }
     if (warp == NW - 1) {
       const int i = sp.tail + lane;
-      const bool keep = i < n && pair_key(__ldg(zm + i), f0 + (uint32_t)i) >= lam;
+      const bool keep = i < n && key_ge(order_key(__ldg(zm + i)), f0 + (uint32_t)i, lam);
       const unsigned m = __ballot_sync(0xFFFFFFFFu, keep);
       const int slot = run + __popc(m & below);
       if (keep && slot < kept_mid) mid[slot] = S + i;
