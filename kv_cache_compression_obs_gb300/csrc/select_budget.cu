@@ -24,24 +24,23 @@
 // hundreds) are gathered on chip for an exact radix select.
 //
 // One thread-block cluster per row; CTA c of the cluster owns heads c, c+CL, ...
-//   1. floor, per owned head, three streams over its scores: the 12-bit
-//      histogram; the 8-bit one inside the boundary bin; the gather of the
-//      boundary bucket's pairs, counting per warp range the pairs above it.
-//      theta_h follows from the bucket's pairs.  The competition's 12-bit
-//      histogram (pairs below theta_h) follows from the same counts without
-//      another stream;
-//   2. competition: the 12-bit histograms summed over the cluster through
-//      distributed shared memory give tau's bin; one stream per owned head
-//      counts that bin's second digits (pairs below theta_h), summed over the
-//      cluster; one more stream gathers the bucket's pairs and counts per warp
-//      range the pairs above it; every CTA selects tau from the cluster's
-//      gathered pairs, read in place through distributed shared memory;
-//   3. the kept middle pairs per (owned head, warp range) follow from the
-//      counts of step 1 (head limited by theta_h) or of step 2 (by tau); they
-//      go to every CTA of the cluster, and offsets are a prefix sum over heads;
-//   4. each owned head writes its sinks, its kept middle positions (warp
-//      ballots over the same ranges keep them ascending) and its recent window
-//      at its offset.
+// Four streams over each owned head's scores:
+//   1. the 12-bit histogram: theta_h's bin and how many of its pairs reach
+//      theta_h.  The competition's 12-bit histogram (pairs below theta_h)
+//      follows from these counts alone; summed over the cluster through
+//      distributed shared memory it gives tau's bin;
+//   2. the second digits of theta_h's bin, and of tau's bin where that lies
+//      below theta_h's (where the two bins are one, the competition's digits
+//      follow from theta_h's); summed over the cluster they give tau's bucket;
+//   3. the gather of theta_h's bucket and of tau's bucket, counting per warp
+//      range the pairs above each; theta_h follows from its bucket's pairs, then
+//      tau from the cluster's gathered pairs below their head's theta, read in
+//      place through distributed shared memory.  The kept middle pairs per
+//      (owned head, warp range) follow from the counts (head limited by theta_h,
+//      or by tau); they go to every CTA, and offsets are a prefix sum over heads;
+//   4. output: each owned head writes its sinks, its kept middle positions
+//      (warp ballots over the same ranges keep them ascending) and its recent
+//      window at its offset.
 // A bucket too large to gather (heavy ties) falls back to a radix select over
 // the streamed pairs, and the kept counts to a counting stream.
 // Integer work only after the key transform: the same z gives the same output.
@@ -492,7 +491,7 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
     }
   }
 
-  // 3. kept middle pairs per owned head and warp range; counts to every CTA
+  // kept middle pairs per owned head and warp range; counts to every CTA
   for (int h = rank, j = 0; h < H; h += CL, ++j) {
     const uint64_t th = sm.theta[h];
     const uint64_t lam = min(th, tau);
