@@ -79,8 +79,8 @@ struct Smem {
   uint32_t p20h[kMaxOwned];    // theta_h's 20-bit bucket (~0u: none gathered)
   int need2[kMaxOwned];        // pairs of that bucket at or above theta_h
   int big[kMaxOwned];          // the bucket is too large to gather
-  uint32_t h8[256];            // second-digit histogram of theta_h's bin
-  uint32_t h8c[256];           // this CTA's second digits of tau's bin (competition)
+  uint32_t h8[512];            // second digits: of theta_h's bin [0, 256), and this
+                               // CTA's of tau's bin (competition) [256, 512)
   uint32_t g8[256];            // the cluster's sum of them
   uint32_t h256[256];          // digit histogram of the selects inside a bucket
   int wsum[NW];
@@ -334,7 +334,8 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
     bt = sm.bin;
     needt1 = sm.need;
   }
-  for (int d = threadIdx.x; d < 256; d += NT) sm.h8c[d] = 0u;
+  uint32_t *const h8c = sm.h8 + 256;
+  for (int d = threadIdx.x; d < 256; d += NT) h8c[d] = 0u;
   for (int h = rank, j = 0; h < H; h += CL, ++j) {
     const int b1 = sm.b1[j];
     const int bc = bt < b1 ? bt : -2;  // tau's bin when below theta_h's (-2: no bin)
@@ -344,8 +345,8 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
     const int b1s = b1 < kBins ? b1 : -1;
     for_head(zmid(h), flat0(h), n, [&](uint32_t ok, uint32_t) {
       const int b = (int)(ok >> kBinShift32);
-      if (b == b1s) atomicAdd(&sm.h8[(ok >> kSubShift32) & 255u], 1u);
-      else if (b == bc) atomicAdd(&sm.h8c[(ok >> kSubShift32) & 255u], 1u);
+      const bool in1 = b == b1s;
+      if (in1 || b == bc) atomicAdd(&sm.h8[(in1 ? 0u : 256u) + ((ok >> kSubShift32) & 255u)], 1u);
     });
     __syncthreads();
     if (b1 < kBins) {
@@ -362,7 +363,7 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
       // tau's bin is theta_h's: the competition takes the bin's pairs below theta_h
       if (b1 == bt)
         for (int d = threadIdx.x; d < 256; d += NT)
-          sm.h8c[d] += d < d2 ? sm.h8[d] : d == d2 ? sm.h8[d] - (uint32_t)need2 : 0u;
+          h8c[d] += d < d2 ? sm.h8[d] : d == d2 ? sm.h8[d] - (uint32_t)need2 : 0u;
     }
     __syncthreads();  // h8 and the sh_* fields serve the next head
   }
@@ -376,7 +377,7 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
       uint32_t g = 0;
 #pragma unroll
       for (int r = 0; r < kMaxCluster; ++r)
-        if (r < CL) g += cl.map_shared_rank(sm.h8c, r)[d];
+        if (r < CL) g += cl.map_shared_rank(h8c, r)[d];
       sm.g8[d] = g;
     }
     __syncthreads();
@@ -407,10 +408,12 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
         const uint32_t pk = ok >> kSubShift32;
         c1 += pk > ph;
         c2 += pk > p20t;
-        if (pk == ph) dy.l.tlist[atomicAdd(&sm.tl_n, 1)] = pair_key_u(ok, fl);  // <= kListCap pairs
-        if (pk == p20t) {
-          const int slot = atomicAdd(&sm.list_n, 1);
-          if (slot < kListCap) dy.l.clist[slot] = pair_key_u(ok, fl);
+        if (pk == ph || pk == p20t) {  // rare
+          if (pk == ph) dy.l.tlist[atomicAdd(&sm.tl_n, 1)] = pair_key_u(ok, fl);  // <= kListCap pairs
+          if (pk == p20t) {
+            const int slot = atomicAdd(&sm.list_n, 1);
+            if (slot < kListCap) dy.l.clist[slot] = pair_key_u(ok, fl);
+          }
         }
       });
 #pragma unroll
@@ -561,58 +564,72 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
     const int b0 = min(sp.n4, warp * per4), b1 = min(sp.n4, b0 + per4);
     int32_t *mid = out + S;
     const unsigned below = (1u << lane) - 1u;
-    if (warp == 0) {
-      const bool keep = lane < sp.pre && key_ge(order_key(__ldg(zm + lane)), f0 + (uint32_t)lane, lam);
-      const unsigned m = __ballot_sync(0xFFFFFFFFu, keep);
-      const int slot = run + __popc(m & below);
-      if (keep && slot < kept_mid) mid[slot] = S + lane;
-      run += __popc(m);
-    }
-    for (int q00 = b0; q00 < b1; q00 += 4 * 32) {  // four vectors a lane in flight
-      float4 vv[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int q = q00 + 32 * u + lane;
-        vv[u] = q < b1 ? __ldg(z4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const uint32_t lam_hi = (uint32_t)(lam >> 32);
+    // L0: the threshold's low word is zero, so the order key alone decides
+    auto emit = [&](auto low0) {
+      constexpr bool L0 = decltype(low0)::value;
+      auto ge = [&](uint32_t ok, uint32_t fl) { return L0 ? ok >= lam_hi : key_ge(ok, fl, lam); };
+      if (warp == 0) {
+        const bool keep = lane < sp.pre && ge(order_key(__ldg(zm + lane)), f0 + (uint32_t)lane);
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, keep);
+        const int slot = run + __popc(m & below);
+        if (keep && slot < kept_mid) mid[slot] = S + lane;
+        run += __popc(m);
       }
+      for (int q00 = b0; q00 < b1; q00 += 4 * 32) {  // four vectors a lane in flight
+        float4 vv[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const int q = q00 + 32 * u + lane;
-        bool k0 = false, k1 = false, k2 = false, k3 = false;
-        const int i = sp.pre + 4 * q;
-        if (q < b1) {
-          const float4 v = vv[u];
-          const uint32_t fi = f0 + (uint32_t)i;
-          k0 = key_ge(order_key(v.x), fi, lam);
-          k1 = key_ge(order_key(v.y), fi + 1, lam);
-          k2 = key_ge(order_key(v.z), fi + 2, lam);
-          k3 = key_ge(order_key(v.w), fi + 3, lam);
+        for (int u = 0; u < 4; ++u) {
+          const int q = q00 + 32 * u + lane;
+          vv[u] = q < b1 ? __ldg(z4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        const int c = (int)k0 + (int)k1 + (int)k2 + (int)k3;
-        int incl = c;
+        // keep bits of each vector, and their counts packed one byte per vector
+        // (at most 4 x 32 = 128 a byte, so one scan serves all four)
+        uint32_t kb[4], packed = 0u;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int q = q00 + 32 * u + lane;
+          uint32_t bits = 0u;
+          if (q < b1) {
+            const float4 v = vv[u];
+            const uint32_t fi = f0 + (uint32_t)(sp.pre + 4 * q);
+            bits = (uint32_t)ge(order_key(v.x), fi) | (uint32_t)ge(order_key(v.y), fi + 1) << 1 |
+                   (uint32_t)ge(order_key(v.z), fi + 2) << 2 | (uint32_t)ge(order_key(v.w), fi + 3) << 3;
+          }
+          kb[u] = bits;
+          packed |= (uint32_t)__popc(bits) << (8 * u);
+        }
+        uint32_t incl = packed;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
-          const int y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+          const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
           if (lane >= off) incl += y;
         }
-        int slot = run + incl - c;
-        if (k0 && slot < kept_mid) mid[slot] = S + i;
-        slot += k0;
-        if (k1 && slot < kept_mid) mid[slot] = S + i + 1;
-        slot += k1;
-        if (k2 && slot < kept_mid) mid[slot] = S + i + 2;
-        slot += k2;
-        if (k3 && slot < kept_mid) mid[slot] = S + i + 3;
-        run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+        const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        const uint32_t excl = incl - packed;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          int slot = run + (int)((excl >> (8 * u)) & 255u);
+          const int i = sp.pre + 4 * (q00 + 32 * u + lane);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if ((kb[u] >> c) & 1u) {
+              if (slot < kept_mid) mid[slot] = S + i + c;
+              ++slot;
+            }
+          run += (int)((tot >> (8 * u)) & 255u);
+        }
       }
-    }
-    if (warp == NW - 1) {
-      const int i = sp.tail + lane;
-      const bool keep = i < n && key_ge(order_key(__ldg(zm + i)), f0 + (uint32_t)i, lam);
-      const unsigned m = __ballot_sync(0xFFFFFFFFu, keep);
-      const int slot = run + __popc(m & below);
-      if (keep && slot < kept_mid) mid[slot] = S + i;
-    }
+      if (warp == NW - 1) {
+        const int i = sp.tail + lane;
+        const bool keep = i < n && ge(order_key(__ldg(zm + i)), f0 + (uint32_t)i);
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, keep);
+        const int slot = run + __popc(m & below);
+        if (keep && slot < kept_mid) mid[slot] = S + i;
+      }
+    };
+    if ((uint32_t)lam == 0u) emit(std::true_type{});
+    else emit(std::false_type{});
   }
 }
 

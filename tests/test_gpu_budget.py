@@ -78,6 +78,29 @@ def test_select_budget_many_rows(kvc, oracle_mod):
     np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
 
 
+@pytest.mark.parametrize("levels", [0, 40, 3000])
+@pytest.mark.parametrize("case", [(2, 4, 700, 4 * 120, 40, 8, 4), (1, 8, 4096, 8 * 400, 150, 32, 4),
+                                  (1, 12, 3001, 12 * 300, 100, 16, 0)],
+                         ids=lambda c: "B{}H{}T{}b{}f{}R{}S{}".format(*c))
+def test_select_budget_thresholds_share_a_bin(kvc, oracle_mod, case, levels):
+    """Scores in [1, 1.12): every pair has the same top 12 key bits, so each
+    head's floor threshold and the competition's lie in one bin, the
+    competition's second digits come from the floor's, and with few distinct
+    values (`levels`) the two thresholds often share one 20-bit bucket too."""
+    B, H, T, budget, floor, R, S = case
+    g = torch.Generator(device=DEV)
+    g.manual_seed(levels + T)
+    u = torch.rand(B, H, T, generator=g, device=DEV)
+    if levels:
+        u = torch.floor(u * levels) / levels
+    z = (1.0 + 0.12 * u).contiguous()
+    idx, off = kvc.kv_select_budget(z, budget, floor, R, S)
+    torch.cuda.synchronize()
+    ref_idx, ref_off = oracle_mod.select_budget(z.cpu().numpy().astype(np.float64), budget, floor, R, S)
+    np.testing.assert_array_equal(off.cpu().numpy(), ref_off)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+
+
 # ---------------------------------------------------------------- ragged compaction
 @pytest.mark.parametrize("dt,d", [("bf16", 128), ("f32", 64), ("bf16", 64)])
 def test_compact_ragged_bit_exact(kvc, oracle_mod, dt, d):
