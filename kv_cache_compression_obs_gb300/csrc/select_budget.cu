@@ -64,6 +64,8 @@ constexpr int kBins = 4096;                         // first digit: the key's to
 constexpr int kBinShift = 64 - 12;
 constexpr int kSubShift = kBinShift - 8;            // second digit; a bucket is the top 20 bits
 constexpr int kListCap = 2048;                      // bucket pairs held on chip per CTA
+constexpr int kBmWords = 8200;                      // kept-pair bitmasks of the owned heads
+                                                    // (a 128K-position head takes 4098 words)
 
 struct Smem {
   RadixScratch<NT> rx;
@@ -79,6 +81,7 @@ struct Smem {
   uint32_t p20h[kMaxOwned];    // theta_h's 20-bit bucket (~0u: none gathered)
   int need2[kMaxOwned];        // pairs of that bucket at or above theta_h
   int big[kMaxOwned];          // the bucket is too large to gather
+  int bmok[kMaxOwned];         // the head's kept pairs are in its bitmask
   uint32_t h8[512];            // second digits: of theta_h's bin [0, 256), and this
                                // CTA's of tau's bin (competition) [256, 512)
   uint32_t g8[256];            // the cluster's sum of them
@@ -204,6 +207,79 @@ __device__ __forceinline__ void for_warp(const float *__restrict__ zm, uint32_t 
     f(order_key(__ldg(zm + sp.tail + lane)), flat0 + (uint32_t)(sp.tail + lane));
 }
 
+// Bitmask of a head's kept middle pairs, laid out by the warp ranges of
+// for_warp: warp w, round s (its vectors b0 + 256 s + [0, 256)) and lane l own
+// one word whose nibble u holds the four pairs of vector b0 + 256 s + 32 u + l;
+// two more words hold the leading and the trailing scalars.  nrw: rounds per
+// warp range; a head takes bm_words(nrw) words.
+__host__ __device__ __forceinline__ int bm_words(int nrw) { return NW * nrw * 32 + 2; }
+// rounds for any head with n middle pairs (a head has at most n/4 vectors)
+__host__ __device__ __forceinline__ int bm_rounds(int n) { return (((n >> 2) + NW - 1) / NW + 255) / 256; }
+// Sets the bit of middle position i (shared-memory atomics: the word's other
+// bits may be set at the same time).
+__device__ __forceinline__ void bm_set(uint32_t *bm, int nrw, const Split &sp, int i) {
+  if (i < sp.pre) {
+    atomicOr(&bm[NW * nrw * 32], 1u << i);
+  } else if (i >= sp.tail) {
+    atomicOr(&bm[NW * nrw * 32 + 1], 1u << (i - sp.tail));
+  } else {
+    const int per4 = (sp.n4 + NW - 1) / NW;
+    const int q = (i - sp.pre) >> 2, c = (i - sp.pre) & 3;
+    const int w = q / per4, off = q - w * per4;
+    atomicOr(&bm[(w * nrw + (off >> 8)) * 32 + (off & 31)], 1u << (4 * ((off >> 5) & 7) + c));
+  }
+}
+
+// Step 3's stream over this warp's range (the ranges of for_warp, eight 16-byte
+// loads in flight per lane): visit(order key, flat index) for every middle pair,
+// returning whether the pair is kept for sure; with bm those answers go to the
+// head's bitmask (every word of this warp's rounds is written).
+template <typename V>
+__device__ __forceinline__ void gather_stream(const float *__restrict__ zm, uint32_t flat0, int n,
+                                              uint32_t *bm, int nrw, V &&visit) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Split sp = split_of(zm, n);
+  const float4 *z4 = reinterpret_cast<const float4 *>(zm + sp.pre);
+  const int per4 = (sp.n4 + NW - 1) / NW;
+  const int b0 = min(sp.n4, warp * per4), b1 = min(sp.n4, b0 + per4);
+  if (warp == 0) {
+    bool k = false;
+    if (lane < sp.pre) k = visit(order_key(__ldg(zm + lane)), flat0 + (uint32_t)lane);
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, k);
+    if (bm && lane == 0) bm[NW * nrw * 32] = m;
+  }
+  const int nit = (b1 - b0 + 255) / 256;
+  for (int r = 0; r < nit; ++r) {
+    const int q0 = b0 + 256 * r + lane;
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int q = q0 + 32 * u;
+      v[u] = q < b1 ? __ldg(z4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    uint32_t word = 0u;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int q = q0 + 32 * u;
+      if (q < b1) {
+        const uint32_t i = flat0 + (uint32_t)(sp.pre + 4 * q);
+        uint32_t bits = visit(order_key(v[u].x), i) ? 1u : 0u;
+        bits |= visit(order_key(v[u].y), i + 1) ? 2u : 0u;
+        bits |= visit(order_key(v[u].z), i + 2) ? 4u : 0u;
+        bits |= visit(order_key(v[u].w), i + 3) ? 8u : 0u;
+        word |= bits << (4 * u);
+      }
+    }
+    if (bm) bm[(warp * nrw + r) * 32 + lane] = word;
+  }
+  if (warp == NW - 1) {
+    bool k = false;
+    if (lane < n - sp.tail) k = visit(order_key(__ldg(zm + sp.tail + lane)), flat0 + (uint32_t)(sp.tail + lane));
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, k);
+    if (bm && lane == 0) bm[NW * nrw * 32 + 1] = m;
+  }
+}
+
 // In a histogram of kBins counts (bins taken from the top), the bin where the
 // count of keys in it or above first reaches `need`: sm.bin, sm.need (how many of
 // that bin's keys are needed) and sm.above.  Every thread of the CTA must call.
@@ -269,6 +345,7 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
   __shared__ Smem sm;
   extern __shared__ __align__(16) unsigned char dyn_raw[];
   Dyn &dy = *reinterpret_cast<Dyn *>(dyn_raw);
+  uint32_t *const bm_all = reinterpret_cast<uint32_t *>(dyn_raw + sizeof(Dyn));  // [kBmWords]
   cg::cluster_group cl = cg::this_cluster();
   const int CL = (int)cl.num_blocks();
   const int rank = (int)cl.block_rank();
@@ -392,6 +469,7 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
   // 3. per owned head, one stream gathers theta_h's bucket and tau's (every pair
   //    of it, kept by its floor or not) and counts per warp range the pairs above
   //    each; theta_h follows from its bucket's pairs at once
+  const int nrw = bm_rounds(n), bm_stride = bm_words(nrw);
   if (threadIdx.x == 0) sm.list_n = 0;
   for (int h = rank, j = 0; h < H; h += CL, ++j) {
     const float *zm = zmid(h);
@@ -400,11 +478,20 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
     const int per4 = max(1, (sp.n4 + NW - 1) / NW);
     const int big = sm.big[j];
     const uint32_t ph = big ? ~0u : sm.p20h[j];  // ~0u: matches no pair
-    if (threadIdx.x == 0) sm.tl_n = 0;
+    // The head's threshold min(theta_h, tau) lies in the lower of the two
+    // buckets: the pairs of higher buckets are kept for sure (the bitmask), those
+    // of that bucket are taken from its list once the thresholds are known.
+    const uint32_t pl = min(ph, p20t);
+    const bool use_bm = !big && (ph != ~0u || p20t != ~0u) && (j + 1) * bm_stride <= kBmWords;
+    uint32_t *const bmh = use_bm ? bm_all + j * bm_stride : nullptr;
+    if (threadIdx.x == 0) {
+      sm.tl_n = 0;
+      sm.bmok[j] = use_bm;
+    }
     __syncthreads();
     int c1 = 0, c2 = 0;
     if (ph != ~0u || p20t != ~0u) {
-      for_warp(zm, f0, n, [&](uint32_t ok, uint32_t fl) {
+      gather_stream(zm, f0, n, bmh, nrw, [&](uint32_t ok, uint32_t fl) {
         const uint32_t pk = ok >> kSubShift32;
         c1 += pk > ph;
         c2 += pk > p20t;
@@ -415,6 +502,7 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
             if (slot < kListCap) dy.l.clist[slot] = pair_key_u(ok, fl);
           }
         }
+        return pk > pl;
       });
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
@@ -437,9 +525,14 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
           for (int i = threadIdx.x; i < ln; i += NT) f(dy.l.tlist[i]);
         });
         th = max(th, pb);  // the select stops at the first digit that settles the bucket
+        // theta_h's bucket below tau's: the head's threshold is theta_h
+        const bool mark = use_bm && ph < p20t;
         for (int i = threadIdx.x; i < ln; i += NT) {
           const uint64_t key = dy.l.tlist[i];
-          if (key >= th) atomicAdd(&sm.wth[j][warp_of(pos_of(key), sp, per4)], 1);
+          if (key >= th) {
+            atomicAdd(&sm.wth[j][warp_of(pos_of(key), sp, per4)], 1);
+            if (mark) bm_set(bmh, nrw, sp, pos_of(key));
+          }
         }
       } else {
         th = radix_select_ge<NT, false>(sm.rx, nf, [&](auto &&f) {
@@ -521,7 +614,22 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
       for (int off = 16; off > 0; off >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, off);
       if (lane == 0) sm.wcnt[j][warp] = c;
     }
+    // tau's bucket at or below theta_h's: the head's kept pairs of that bucket
+    // are marked from the competition's list (no list, no bitmask)
+    bool bm_use = sm.bmok[j];
+    if (bm_use && p20t <= (sm.big[j] ? ~0u : sm.p20h[j])) {
+      if (tau_ok) {
+        const int ln = min(sm.list_n, kListCap);
+        for (int i = threadIdx.x; i < ln; i += NT) {
+          const uint64_t key = dy.l.clist[i];
+          if (head_of(key) == h && key >= lam) bm_set(bm_all + j * bm_stride, nrw, sp, pos_of(key));
+        }
+      } else {
+        bm_use = false;
+      }
+    }
     __syncthreads();
+    if (threadIdx.x == 0) sm.bmok[j] = bm_use;
     if (threadIdx.x < CL) {
       int tot = 0;
       for (int w = 0; w < NW; ++w) tot += sm.wcnt[j][w];
@@ -628,8 +736,57 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
         if (keep && slot < kept_mid) mid[slot] = S + i;
       }
     };
-    if ((uint32_t)lam == 0u) emit(std::true_type{});
-    else emit(std::false_type{});
+    if (sm.bmok[j]) {
+      // from the head's bitmask: nibble u of lane l's word of round r holds
+      // vector b0 + 256 r + 32 u + l; the eight vectors' counts packed one byte
+      // each (at most 128) share one scan
+      const uint32_t *bmh = bm_all + j * bm_stride;
+      if (warp == 0) {
+        const unsigned m = bmh[NW * nrw * 32];
+        const int slot = run + __popc(m & below);
+        if (((m >> lane) & 1u) && slot < kept_mid) mid[slot] = S + lane;
+        run += __popc(m);
+      }
+      const int nit = (b1 - b0 + 255) / 256;
+      for (int r = 0; r < nit; ++r) {
+        const uint32_t word = bmh[(warp * nrw + r) * 32 + lane];
+        uint64_t packed = 0u;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) packed |= (uint64_t)__popc((word >> (4 * u)) & 15u) << (8 * u);
+        uint64_t incl = packed;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const uint64_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+          if (lane >= off) incl += y;
+        }
+        const uint64_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        const uint64_t excl = incl - packed;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t nib = (word >> (4 * u)) & 15u;
+          if (nib) {
+            int slot = run + (int)((excl >> (8 * u)) & 255u);
+            const int i = sp.pre + 4 * (b0 + 256 * r + 32 * u + lane);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              if ((nib >> c) & 1u) {
+                if (slot < kept_mid) mid[slot] = S + i + c;
+                ++slot;
+              }
+          }
+          run += (int)((tot >> (8 * u)) & 255u);
+        }
+      }
+      if (warp == NW - 1) {
+        const unsigned m = bmh[NW * nrw * 32 + 1];
+        const int slot = run + __popc(m & below);
+        if (((m >> lane) & 1u) && slot < kept_mid) mid[slot] = S + sp.tail + lane;
+      }
+    } else if ((uint32_t)lam == 0u) {
+      emit(std::true_type{});
+    } else {
+      emit(std::false_type{});
+    }
   }
 }
 
@@ -641,9 +798,10 @@ int launch_select_budget(const float *z, int B, int H, int T, int budget, int fl
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((long)B * CL));
   cfg.blockDim = dim3(NT);
-  cfg.dynamicSmemBytes = sizeof(Dyn);
+  const size_t dyn = sizeof(Dyn) + sizeof(uint32_t) * kBmWords;
+  cfg.dynamicSmemBytes = dyn;
   cfg.stream = st;
-  if (ensure_smem((const void *)select_budget_kernel, sizeof(Dyn)))
+  if (ensure_smem((const void *)select_budget_kernel, dyn))
     return cuda_failure(cudaErrorInvalidValue, "budget selection kernel: shared memory");
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
