@@ -82,6 +82,7 @@ struct Smem {
   int need2[kMaxOwned];        // pairs of that bucket at or above theta_h
   int big[kMaxOwned];          // the bucket is too large to gather
   int bmok[kMaxOwned];         // the head's kept pairs are in its bitmask
+  int nonneg[kMaxOwned];       // the head holds no negative score
   uint32_t h8[512];            // second digits: of theta_h's bin [0, 256), and this
                                // CTA's of tau's bin (competition) [256, 512)
   uint32_t g8[256];            // the cluster's sum of them
@@ -131,6 +132,13 @@ __device__ __forceinline__ int warp_of(int i, const Split &sp, int per4) {
   return ((i - sp.pre) >> 2) / per4;
 }
 
+// The order key; NONNEG: the head holds no negative score (-0 aside), so the
+// key is the bit pattern with the sign bit set (the same value, one instruction).
+template <bool NONNEG>
+__device__ __forceinline__ uint32_t okey(float f) {
+  return NONNEG ? (__float_as_uint(f) | 0x80000000u) : order_key(f);
+}
+
 // A pair's order key (the high word of its 64-bit key) and its flat index
 // h*T + position; the streams pass these, and the 64-bit key is formed only
 // where a pair is kept in a list.  Comparisons against a 64-bit threshold:
@@ -143,7 +151,7 @@ constexpr int kSubShift32 = kSubShift - 32;
 
 // Calls f(order key, flat index) for the middle pairs of one head, positions
 // [S, S + n), with strided coalesced 16-byte loads, eight in flight per thread.
-template <typename F>
+template <bool NONNEG = false, typename F>
 __device__ __forceinline__ void for_head(const float *__restrict__ zm, uint32_t flat0, int n, F &&f) {
   const Split sp = split_of(zm, n);
   const float4 *z4 = reinterpret_cast<const float4 *>(zm + sp.pre);
@@ -159,18 +167,18 @@ __device__ __forceinline__ void for_head(const float *__restrict__ zm, uint32_t 
       const int j = base + u * NT;
       if (j < sp.n4) {
         const uint32_t i = flat0 + (uint32_t)(sp.pre + 4 * j);
-        f(order_key(v[u].x), i);
-        f(order_key(v[u].y), i + 1);
-        f(order_key(v[u].z), i + 2);
-        f(order_key(v[u].w), i + 3);
+        f(okey<NONNEG>(v[u].x), i);
+        f(okey<NONNEG>(v[u].y), i + 1);
+        f(okey<NONNEG>(v[u].z), i + 2);
+        f(okey<NONNEG>(v[u].w), i + 3);
       }
     }
   }
   const int t = threadIdx.x, nt = n - sp.tail;
-  if (t < sp.pre) f(order_key(__ldg(zm + t)), flat0 + (uint32_t)t);
+  if (t < sp.pre) f(okey<NONNEG>(__ldg(zm + t)), flat0 + (uint32_t)t);
   else if (t < sp.pre + nt) {
     const int i = sp.tail + (t - sp.pre);
-    f(order_key(__ldg(zm + i)), flat0 + (uint32_t)i);
+    f(okey<NONNEG>(__ldg(zm + i)), flat0 + (uint32_t)i);
   }
 }
 
@@ -234,7 +242,7 @@ __device__ __forceinline__ void bm_set(uint32_t *bm, int nrw, const Split &sp, i
 // loads in flight per lane): visit(order key, flat index) for every middle pair,
 // returning whether the pair is kept for sure; with bm those answers go to the
 // head's bitmask (every word of this warp's rounds is written).
-template <typename V>
+template <bool NONNEG, typename V>
 __device__ __forceinline__ void gather_stream(const float *__restrict__ zm, uint32_t flat0, int n,
                                               uint32_t *bm, int nrw, V &&visit) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -244,7 +252,7 @@ __device__ __forceinline__ void gather_stream(const float *__restrict__ zm, uint
   const int b0 = min(sp.n4, warp * per4), b1 = min(sp.n4, b0 + per4);
   if (warp == 0) {
     bool k = false;
-    if (lane < sp.pre) k = visit(order_key(__ldg(zm + lane)), flat0 + (uint32_t)lane);
+    if (lane < sp.pre) k = visit(okey<NONNEG>(__ldg(zm + lane)), flat0 + (uint32_t)lane);
     const unsigned m = __ballot_sync(0xFFFFFFFFu, k);
     if (bm && lane == 0) bm[NW * nrw * 32] = m;
   }
@@ -263,10 +271,10 @@ __device__ __forceinline__ void gather_stream(const float *__restrict__ zm, uint
       const int q = q0 + 32 * u;
       if (q < b1) {
         const uint32_t i = flat0 + (uint32_t)(sp.pre + 4 * q);
-        uint32_t bits = visit(order_key(v[u].x), i) ? 1u : 0u;
-        bits |= visit(order_key(v[u].y), i + 1) ? 2u : 0u;
-        bits |= visit(order_key(v[u].z), i + 2) ? 4u : 0u;
-        bits |= visit(order_key(v[u].w), i + 3) ? 8u : 0u;
+        uint32_t bits = visit(okey<NONNEG>(v[u].x), i) ? 1u : 0u;
+        bits |= visit(okey<NONNEG>(v[u].y), i + 1) ? 2u : 0u;
+        bits |= visit(okey<NONNEG>(v[u].z), i + 2) ? 4u : 0u;
+        bits |= visit(okey<NONNEG>(v[u].w), i + 3) ? 8u : 0u;
         word |= bits << (4 * u);
       }
     }
@@ -274,7 +282,7 @@ __device__ __forceinline__ void gather_stream(const float *__restrict__ zm, uint
   }
   if (warp == NW - 1) {
     bool k = false;
-    if (lane < n - sp.tail) k = visit(order_key(__ldg(zm + sp.tail + lane)), flat0 + (uint32_t)(sp.tail + lane));
+    if (lane < n - sp.tail) k = visit(okey<NONNEG>(__ldg(zm + sp.tail + lane)), flat0 + (uint32_t)(sp.tail + lane));
     const unsigned m = __ballot_sync(0xFFFFFFFFu, k);
     if (bm && lane == 0) bm[NW * nrw * 32 + 1] = m;
   }
@@ -374,6 +382,13 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
     __syncthreads();
     for_head(zmid(h), flat0(h), n, [&](uint32_t ok, uint32_t) { atomicAdd(&dy.h.hist[ok >> kBinShift32], 1u); });
     __syncthreads();
+    {
+      // negative scores have keys below 2^31: bins [0, kBins / 2)
+      uint32_t negs = 0u;
+      for (int e = threadIdx.x; e < kBins / 2; e += NT) negs |= dy.h.hist[e];
+      const int nonneg = !__syncthreads_or(negs != 0u);
+      if (threadIdx.x == 0) sm.nonneg[j] = nonneg;
+    }
     int b1 = kBins, need1 = 0;  // b1 = kBins: no floor, every pair below theta_h
     if (nf > 0) {
       find_boundary(dy.h.hist, nf, sm);
@@ -398,13 +413,19 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
   //    of tau's bin (all of whose pairs are then below theta_h)
   int bt = -1, needt1 = 0;
   if (extra > 0) {
-    uint32_t *gs = dy.h.hist;  // the cluster's sum
-    for (int e = threadIdx.x; e < kBins; e += NT) {
-      uint32_t g = 0;
+    uint32_t *gs = dy.h.hist;  // the cluster's sum, four bins a thread at a time
+    static_assert(kBins % (4 * NT) == 0, "bins per sweep");
+    for (int e = threadIdx.x; e < kBins; e += 4 * NT) {
+      uint32_t g[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
       for (int r = 0; r < kMaxCluster; ++r)
-        if (r < CL) g += cl.map_shared_rank(dy.h.comp, r)[e];
-      gs[e] = g;
+        if (r < CL) {
+          const uint32_t *c = cl.map_shared_rank(dy.h.comp, r);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) g[q] += c[e + q * NT];
+        }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) gs[e + q * NT] = g[q];
     }
     __syncthreads();
     find_boundary(gs, (int)extra, sm);
@@ -420,11 +441,13 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
     for (int d = threadIdx.x; d < 256; d += NT) sm.h8[d] = 0u;
     __syncthreads();
     const int b1s = b1 < kBins ? b1 : -1;
-    for_head(zmid(h), flat0(h), n, [&](uint32_t ok, uint32_t) {
+    auto digits = [&](uint32_t ok, uint32_t) {
       const int b = (int)(ok >> kBinShift32);
       const bool in1 = b == b1s;
       if (in1 || b == bc) atomicAdd(&sm.h8[(in1 ? 0u : 256u) + ((ok >> kSubShift32) & 255u)], 1u);
-    });
+    };
+    if (sm.nonneg[j]) for_head<true>(zmid(h), flat0(h), n, digits);
+    else for_head<false>(zmid(h), flat0(h), n, digits);
     __syncthreads();
     if (b1 < kBins) {
       if (warp == 0) digit_boundary(sm.h8, sm.need1[j], (uint64_t)b1 << kBinShift, kSubShift, sm.rx);
@@ -491,7 +514,7 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
     __syncthreads();
     int c1 = 0, c2 = 0;
     if (ph != ~0u || p20t != ~0u) {
-      gather_stream(zm, f0, n, bmh, nrw, [&](uint32_t ok, uint32_t fl) {
+      auto visit = [&](uint32_t ok, uint32_t fl) {
         const uint32_t pk = ok >> kSubShift32;
         c1 += pk > ph;
         c2 += pk > p20t;
@@ -503,7 +526,9 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
           }
         }
         return pk > pl;
-      });
+      };
+      if (sm.nonneg[j]) gather_stream<true>(zm, f0, n, bmh, nrw, visit);
+      else gather_stream<false>(zm, f0, n, bmh, nrw, visit);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
         c1 += __shfl_xor_sync(0xFFFFFFFFu, c1, off);

@@ -101,6 +101,31 @@ def test_select_budget_thresholds_share_a_bin(kvc, oracle_mod, case, levels):
     np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
 
 
+@pytest.mark.parametrize("which", ["all", "one_head"])
+@pytest.mark.parametrize("case", [(2, 4, 700, 4 * 120, 40, 8, 4), (1, 8, 4096, 8 * 400, 150, 32, 4),
+                                  (1, 12, 3001, 12 * 300, 100, 16, 0)],
+                         ids=lambda c: "B{}H{}T{}b{}f{}R{}S{}".format(*c))
+def test_select_budget_signed_scores(kvc, oracle_mod, case, which):
+    """Negative scores (every head, or one head of each row beside non-negative
+    ones, with -0.0 and +0.0 among them): the order keys of signed floats."""
+    B, H, T, budget, floor, R, S = case
+    g = torch.Generator(device=DEV)
+    g.manual_seed(T + len(which))
+    if which == "all":
+        z = torch.randn(B, H, T, generator=g, device=DEV)
+    else:
+        z = torch.rand(B, H, T, generator=g, device=DEV) ** 2
+        z[:, 1] -= 0.5
+    z[:, :, 5::11] = -0.0
+    z[:, :, 7::13] = 0.0
+    z = z.contiguous()
+    idx, off = kvc.kv_select_budget(z, budget, floor, R, S)
+    torch.cuda.synchronize()
+    ref_idx, ref_off = oracle_mod.select_budget(z.cpu().numpy().astype(np.float64), budget, floor, R, S)
+    np.testing.assert_array_equal(off.cpu().numpy(), ref_off)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+
+
 # ---------------------------------------------------------------- ragged compaction
 @pytest.mark.parametrize("dt,d", [("bf16", 128), ("f32", 64), ("bf16", 64)])
 def test_compact_ragged_bit_exact(kvc, oracle_mod, dt, d):
