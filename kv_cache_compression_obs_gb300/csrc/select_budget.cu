@@ -24,7 +24,7 @@
 // hundreds) are gathered on chip for an exact radix select.
 //
 // One thread-block cluster per row; CTA c of the cluster owns heads c, c+CL, ...
-// Four streams over each owned head's scores:
+// Three streams over each owned head's scores, then the output:
 //   1. the 12-bit histogram: theta_h's bin and how many of its pairs reach
 //      theta_h.  The competition's 12-bit histogram (pairs below theta_h)
 //      follows from these counts alone; summed over the cluster through
@@ -33,16 +33,20 @@
 //      below theta_h's (where the two bins are one, the competition's digits
 //      follow from theta_h's); summed over the cluster they give tau's bucket;
 //   3. the gather of theta_h's bucket and of tau's bucket, counting per warp
-//      range the pairs above each; theta_h follows from its bucket's pairs, then
-//      tau from the cluster's gathered pairs below their head's theta, read in
-//      place through distributed shared memory.  The kept middle pairs per
-//      (owned head, warp range) follow from the counts (head limited by theta_h,
-//      or by tau); they go to every CTA, and offsets are a prefix sum over heads;
+//      range the pairs above each and recording in a shared-memory bitmask the
+//      pairs above the lower of the two buckets (kept whatever the thresholds);
+//      theta_h follows from its bucket's pairs, then tau from the cluster's
+//      gathered pairs below their head's theta, read in place through
+//      distributed shared memory.  The kept middle pairs per (owned head, warp
+//      range) follow from the counts (head limited by theta_h, or by tau); they
+//      go to every CTA, and offsets are a prefix sum over heads; the kept pairs
+//      of the threshold's own bucket are marked in the bitmask from its list;
 //   4. output: each owned head writes its sinks, its kept middle positions
-//      (warp ballots over the same ranges keep them ascending) and its recent
+//      (from the bitmask, ascending over the same warp ranges) and its recent
 //      window at its offset.
 // A bucket too large to gather (heavy ties) falls back to a radix select over
-// the streamed pairs, and the kept counts to a counting stream.
+// the streamed pairs, the kept counts to a counting stream and the output to a
+// stream with warp ballots.
 // Integer work only after the key transform: the same z gives the same output.
 #include <cooperative_groups.h>
 
