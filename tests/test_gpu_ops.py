@@ -104,13 +104,18 @@ def test_hubkv_gamma_one_identical_heads(kvc):
                                    (50000, 5000, 17),     # a cluster of 4
                                    (300000, 15000, 64),   # 8 CTAs with large slices
                                    (400000, 20000, 64)])  # beyond the resident limit: streaming kernel
-@pytest.mark.parametrize("ties", [False, True])
+@pytest.mark.parametrize("ties", [False, True, "signed"])
 def test_select_topk_bit_exact(kvc, oracle_mod, T, k, R, ties):
     B, H = 2, 3
     g = torch.Generator(device=DEV)
     g.manual_seed(T + k)
     z = torch.rand(B, H, T, generator=g, device=DEV)
-    if ties:
+    if ties == "signed":                  # negative scores beside positive ones
+        z = torch.randn(B, H, T, generator=g, device=DEV)
+        z[1, 2] = -z[1, 2].abs()          # a head with no positive score
+        z[0, 1, ::9] = -0.0
+        z[0, 1, 4::9] = 0.0
+    elif ties:
         z = torch.floor(z * 7) / 7        # heavy ties: the position rule decides
         z[0, 0, ::5] = -0.0               # signed zeros compare equal
         z[0, 0, 1::5] = 0.0

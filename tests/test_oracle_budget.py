@@ -66,6 +66,26 @@ def test_budget_matches_brute_force_on_tiny_rows(oracle_mod, seed):
     assert cases > 300
 
 
+def test_budget_matches_brute_force_with_signed_scores(oracle_mod):
+    """Negative scores, and -0.0 beside +0.0 (equal scores: the tie goes to the
+    lower head, then the lower position)."""
+    rng = np.random.default_rng(321)
+    values = np.array([-2.0, -1.0, -0.0, 0.0, 1.0])
+    cases = 0
+    for H in (1, 2, 3):
+        for T in range(1, 5):
+            for S in range(0, T + 1):
+                for R in range(0, T + 1 - S):
+                    for floor in range(max(1, S + R), T + 1):
+                        for budget in range(H * floor, H * T + 1):
+                            z = values[rng.integers(0, len(values), size=(H, T))]
+                            idx, off = oracle_mod.select_budget(z[None], budget, floor, R, S)
+                            got = _split(idx[0], off[0])
+                            assert got == _brute_budget(z, budget, floor, R, S), (H, T, S, R, floor, budget, z)
+                            cases += 1
+    assert cases > 200
+
+
 def _check_exchange_optimal(z, kept, floor, R, S):
     """No feasible swap of a kept middle pair x for a dropped middle pair y
     raises the sum: within a head always feasible, across heads when x's head

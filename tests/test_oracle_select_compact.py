@@ -34,6 +34,18 @@ def test_exhaustive_small(oracle_mod, seed):
                 assert list(idx) == _brute_best(list(z), k, R), (T, k, R, z)
 
 
+def test_exhaustive_small_signed_scores(oracle_mod):
+    """Negative scores and -0.0 beside +0.0 (equal: the lower position wins)."""
+    rng = np.random.default_rng(99)
+    values = np.array([-3.0, -1.0, -0.0, 0.0, 2.0])
+    for T in range(1, 9):
+        for k in range(1, T + 1):
+            for R in range(0, k):
+                z = values[rng.integers(0, len(values), size=T)]
+                idx = oracle_mod.select_topk(z[None, None], k, R)[0, 0]
+                assert list(idx) == _brute_best(list(z), k, R), (T, k, R, z)
+
+
 def test_order_characterisation_and_library_sort(oracle_mod):
     rng = np.random.default_rng(20)
     B, H, T, k, R = 2, 3, 500, 60, 17
