@@ -68,6 +68,7 @@ constexpr int kBins = 4096;                         // first digit: the key's to
 constexpr int kBinShift = 64 - 12;
 constexpr int kSubShift = kBinShift - 8;            // second digit; a bucket is the top 20 bits
 constexpr int kListCap = 2048;                      // bucket pairs held on chip per CTA
+constexpr int kGroups = 64;                         // groups of kBins / kGroups bins (tau's bin)
 constexpr int kBmWords = 8200;                      // kept-pair bitmasks of the owned heads
                                                     // (a 128K-position head takes 4098 words)
 
@@ -91,6 +92,7 @@ struct Smem {
                                // CTA's of tau's bin (competition) [256, 512)
   uint32_t g8[256];            // the cluster's sum of them
   uint32_t h256[256];          // digit histogram of the selects inside a bucket
+  uint32_t ccoarse[kGroups];   // this CTA's competition counts per group of bins (read by the cluster)
   int wsum[NW];
   int lnr[kMaxCluster];        // competition bucket pairs held per CTA (pushed)
   int ovr[kMaxCluster];        // competition bucket overflowed per CTA (pushed)
@@ -410,6 +412,18 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
       else if (e == b1) dy.h.comp[e] += dy.h.hist[e] - (uint32_t)need1;
     __syncthreads();  // hist serves the next head
   }
+  {
+    // per group of 64 bins, this CTA's competition counts (8 threads a group)
+    static_assert(kGroups * 8 == NT && kBins == kGroups * 64, "group layout");
+    const int g = threadIdx.x >> 3, part = threadIdx.x & 7;
+    uint32_t c = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c += dy.h.comp[g * 64 + part * 8 + i];
+    c += __shfl_xor_sync(0xFFFFFFFFu, c, 1);
+    c += __shfl_xor_sync(0xFFFFFFFFu, c, 2);
+    c += __shfl_xor_sync(0xFFFFFFFFu, c, 4);
+    if (part == 0) sm.ccoarse[g] = c;
+  }
   cl.sync();  // every competition histogram complete
 
   // 2. tau's bin from the cluster's sum; one stream per owned head takes the
@@ -417,22 +431,65 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
   //    of tau's bin (all of whose pairs are then below theta_h)
   int bt = -1, needt1 = 0;
   if (extra > 0) {
-    uint32_t *gs = dy.h.hist;  // the cluster's sum, four bins a thread at a time
-    static_assert(kBins % (4 * NT) == 0, "bins per sweep");
-    for (int e = threadIdx.x; e < kBins; e += 4 * NT) {
-      uint32_t g[4] = {0u, 0u, 0u, 0u};
+    // warp 0, from the cluster's sums taken from the top: the group of bins
+    // where the count reaches `extra`, then the bin inside it (4 KB of remote
+    // reads instead of every rank's 4096 bins)
+    if (warp == 0) {
+      const uint32_t need = (uint32_t)extra;
+      uint32_t c0 = 0, c1 = 0;  // lane l: groups 63 - 2l and 62 - 2l
 #pragma unroll
       for (int r = 0; r < kMaxCluster; ++r)
         if (r < CL) {
-          const uint32_t *c = cl.map_shared_rank(dy.h.comp, r);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) g[q] += c[e + q * NT];
+          const uint32_t *cc = cl.map_shared_rank(sm.ccoarse, r);
+          c0 += cc[kGroups - 1 - 2 * lane];
+          c1 += cc[kGroups - 2 - 2 * lane];
         }
+      uint32_t incl = c0 + c1;
 #pragma unroll
-      for (int q = 0; q < 4; ++q) gs[e + q * NT] = g[q];
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      uint32_t above = incl - (c0 + c1);
+      bool has = above < need && need <= incl;
+      int G = 0;
+      uint32_t aboveG = 0;
+      if (has) {
+        if (need <= above + c0) {
+          G = kGroups - 1 - 2 * lane;
+          aboveG = above;
+        } else {
+          G = kGroups - 2 - 2 * lane;
+          aboveG = above + c0;
+        }
+      }
+      const int src = (__ffs(__ballot_sync(0xFFFFFFFFu, has)) - 1) & 31;
+      G = __shfl_sync(0xFFFFFFFFu, G, src);
+      aboveG = __shfl_sync(0xFFFFFFFFu, aboveG, src);
+      uint32_t f0 = 0, f1 = 0;  // lane l: bins 64G + 63 - 2l and 64G + 62 - 2l
+      const int e0 = G * 64 + 63 - 2 * lane;
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r)
+        if (r < CL) {
+          const uint32_t *cc = cl.map_shared_rank(dy.h.comp, r);
+          f0 += cc[e0];
+          f1 += cc[e0 - 1];
+        }
+      incl = f0 + f1;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      above = aboveG + incl - (f0 + f1);
+      has = above < need && need <= aboveG + incl;
+      if (has) {
+        const bool first = need <= above + f0;
+        sm.bin = first ? e0 : e0 - 1;
+        sm.need = (int)(need - (first ? above : above + f0));
+      }
     }
     __syncthreads();
-    find_boundary(gs, (int)extra, sm);
     bt = sm.bin;
     needt1 = sm.need;
   }
