@@ -847,21 +847,24 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
         }
         const uint64_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
         const uint64_t excl = incl - packed;
+        // the round's kept pairs before vector u, as 16-bit fields (at most 1024)
+        uint64_t cum_lo = 0u, cum_hi = 0u;
+        uint32_t acc = 0u;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const uint32_t nib = (word >> (4 * u)) & 15u;
-          if (nib) {
-            int slot = run + (int)((excl >> (8 * u)) & 255u);
-            const int i = sp.pre + 4 * (b0 + 256 * r + 32 * u + lane);
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-              if ((nib >> c) & 1u) {
-                if (slot < kept_mid) mid[slot] = S + i + c;
-                ++slot;
-              }
-          }
-          run += (int)((tot >> (8 * u)) & 255u);
+          if (u < 4) cum_lo |= (uint64_t)acc << (16 * u);
+          else cum_hi |= (uint64_t)acc << (16 * (u - 4));
+          acc += (uint32_t)(tot >> (8 * u)) & 255u;
         }
+        // only the set bits (a head keeps a few percent of its middle pairs)
+        for (uint32_t w = word; w; w &= w - 1u) {
+          const int b = __ffs(w) - 1, u = b >> 2, c = b & 3;
+          const uint64_t cum = u < 4 ? cum_lo : cum_hi;
+          const int slot = run + (int)((cum >> (16 * (u & 3))) & 0xFFFFu) +
+                           (int)((excl >> (8 * u)) & 255u) + __popc((word >> (4 * u)) & ((1u << c) - 1u));
+          if (slot < kept_mid) mid[slot] = S + sp.pre + 4 * (b0 + 256 * r + 32 * u + lane) + c;
+        }
+        run += (int)acc;
       }
       if (warp == NW - 1) {
         const unsigned m = bmh[NW * nrw * 32 + 1];
