@@ -40,6 +40,7 @@ CASES = [
     (2, 8, 131072, 8 * 6553, 1638, 64, 4),  # long-context layers
     (1, 5, 1, 5, 1, 0, 0),             # T = 1
     (1, 2, 2048, 2 * 2048 - 1, 2000, 16, 0),  # all but one kept
+    (1, 4, 300000, 4 * 15000, 4000, 64, 4),   # heads too long for the on-chip bitmask
 ]
 
 
