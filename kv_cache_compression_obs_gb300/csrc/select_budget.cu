@@ -93,6 +93,7 @@ struct Smem {
   uint32_t g8[256];            // the cluster's sum of them
   uint32_t h256[256];          // digit histogram of the selects inside a bucket
   uint32_t ccoarse[kGroups];   // this CTA's competition counts per group of bins (read by the cluster)
+  uint32_t wsub[6][256];       // second digits of the predicted bins, taken by the first stream
   int wsum[NW];
   int lnr[kMaxCluster];        // competition bucket pairs held per CTA (pushed)
   int ovr[kMaxCluster];        // competition bucket overflowed per CTA (pushed)
@@ -294,6 +295,110 @@ __device__ __forceinline__ void gather_stream(const float *__restrict__ zm, uint
   }
 }
 
+// Calls f(order key) for the pairs of every 16th vector of one head's middle
+// range (a sample of about n/16 pairs); returns the sample's size.
+template <typename F>
+__device__ __forceinline__ int for_sample(const float *__restrict__ zm, int n, F &&f) {
+  const Split sp = split_of(zm, n);
+  const float4 *z4 = reinterpret_cast<const float4 *>(zm + sp.pre);
+  const int ns4 = (sp.n4 + 15) / 16;
+  for (int base = threadIdx.x; base < ns4; base += 4 * NT) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = base + u * NT;
+      v[u] = j < ns4 ? __ldg(z4 + 16 * j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (base + u * NT < ns4) {
+        f(order_key(v[u].x));
+        f(order_key(v[u].y));
+        f(order_key(v[u].z));
+        f(order_key(v[u].w));
+      }
+  }
+  return 4 * ns4;
+}
+
+// gs[g] = the counts of bins [64 g, 64 g + 64) of a kBins histogram (8 threads a
+// group).  Every thread of the CTA must call; the caller synchronises after.
+__device__ __forceinline__ void group_sums(const uint32_t *h, uint32_t *gs) {
+  static_assert(kGroups * 8 == NT && kBins == kGroups * 64, "group layout");
+  const int g = threadIdx.x >> 3, part = threadIdx.x & 7;
+  uint32_t c = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) c += h[g * 64 + part * 8 + i];
+  c += __shfl_xor_sync(0xFFFFFFFFu, c, 1);
+  c += __shfl_xor_sync(0xFFFFFFFFu, c, 2);
+  c += __shfl_xor_sync(0xFFFFFFFFu, c, 4);
+  if (part == 0) gs[g] = c;
+}
+
+// Warp 0: in the sum over the cluster's ranks of the kBins histograms h (with
+// their group sums gs, both at the same shared-memory offsets in every rank),
+// taken from the top, the bin where the count first reaches `need`: sm.bin and
+// sm.need (sm.bin = -1 when the counts never reach it).  Reads the 64 group
+// sums and then one group's 64 bins of every rank.
+__device__ void cluster_boundary(cg::cluster_group &cl, int CL, const uint32_t *h,
+                                 const uint32_t *gs, uint32_t need, Smem &sm) {
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) sm.bin = -1;
+  __syncwarp();
+  uint32_t c0 = 0, c1 = 0;  // lane l: groups 63 - 2l and 62 - 2l
+#pragma unroll
+  for (int r = 0; r < kMaxCluster; ++r)
+    if (r < CL) {
+      const uint32_t *cc = cl.map_shared_rank(gs, r);
+      c0 += cc[kGroups - 1 - 2 * lane];
+      c1 += cc[kGroups - 2 - 2 * lane];
+    }
+  uint32_t incl = c0 + c1;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  uint32_t above = incl - (c0 + c1);
+  bool has = above < need && need <= incl;
+  int G = 0;
+  uint32_t aboveG = 0;
+  if (has) {
+    if (need <= above + c0) {
+      G = kGroups - 1 - 2 * lane;
+      aboveG = above;
+    } else {
+      G = kGroups - 2 - 2 * lane;
+      aboveG = above + c0;
+    }
+  }
+  const int src = (__ffs(__ballot_sync(0xFFFFFFFFu, has)) - 1) & 31;
+  G = __shfl_sync(0xFFFFFFFFu, G, src);
+  aboveG = __shfl_sync(0xFFFFFFFFu, aboveG, src);
+  uint32_t f0 = 0, f1 = 0;  // lane l: bins 64G + 63 - 2l and 64G + 62 - 2l
+  const int e0 = G * 64 + 63 - 2 * lane;
+#pragma unroll
+  for (int r = 0; r < kMaxCluster; ++r)
+    if (r < CL) {
+      const uint32_t *cc = cl.map_shared_rank(h, r);
+      f0 += cc[e0];
+      f1 += cc[e0 - 1];
+    }
+  incl = f0 + f1;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  above = aboveG + incl - (f0 + f1);
+  has = above < need && need <= aboveG + incl;
+  if (has) {
+    const bool first = need <= above + f0;
+    sm.bin = first ? e0 : e0 - 1;
+    sm.need = (int)(need - (first ? above : above + f0));
+  }
+}
+
 // In a histogram of kBins counts (bins taken from the top), the bin where the
 // count of keys in it or above first reaches `need`: sm.bin, sm.need (how many of
 // that bin's keys are needed) and sm.above.  Every thread of the CTA must call.
@@ -378,7 +483,51 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
   };
 
   for (int e = threadIdx.x; e < kBins; e += NT) dy.h.comp[e] = 0u;
-  cl.sync();  // every CTA of the cluster is running before any remote access
+
+  // 0. With one head per CTA (H <= 8), the bins of theta_h and of tau are
+  //    predicted from a sample of every 16th vector, so that the first stream
+  //    can also take the second digits of three bins around each prediction
+  //    and the digit stream is needed only where a prediction missed.  The
+  //    sample's competition counts go to the bitmask area, which is not written
+  //    before step 3, so the ranks can read them without another barrier.
+  const bool pred = H <= kMaxCluster;
+  int w1 = -8, wt = -8;  // first bin of each three-bin window (-8: none)
+  if (pred) {
+    const int h = rank;
+    uint32_t *const scomp = bm_all;           // [kBins] the sample's competition counts
+    uint32_t *const sgrp = bm_all + kBins;    // [kGroups] their group sums
+    for (int e = threadIdx.x; e < kBins; e += NT) dy.h.hist[e] = 0u;
+    for (int e = threadIdx.x; e < 6 * 256; e += NT) (&sm.wsub[0][0])[e] = 0u;
+    __syncthreads();
+    const int ns = for_sample(zmid(h), n, [&](uint32_t ok) { atomicAdd(&dy.h.hist[ok >> kBinShift32], 1u); });
+    __syncthreads();
+    int b1e = kBins, need1e = 0;
+    if (nf > 0 && ns > 0) {
+      const int nfs = (int)min((long long)ns, max(1LL, ((long long)nf * ns + n / 2) / n));
+      find_boundary(dy.h.hist, nfs, sm);
+      b1e = sm.bin;
+      need1e = sm.need;
+      w1 = b1e - 1;
+    }
+    for (int e = threadIdx.x; e < kBins; e += NT)
+      scomp[e] = e < b1e ? dy.h.hist[e] : e == b1e ? dy.h.hist[e] - (uint32_t)need1e : 0u;
+    __syncthreads();
+    group_sums(scomp, sgrp);
+    cl.sync();  // every CTA of the cluster is running, and every sample's counts are complete
+    if (extra > 0 && ns > 0) {
+      const uint32_t es = (uint32_t)max(1LL, ((long long)extra * ns + n / 2) / n);
+      if (warp == 0) cluster_boundary(cl, CL, scomp, sgrp, es, sm);
+      __syncthreads();
+      if (sm.bin >= 0) wt = sm.bin - 1;
+    }
+  } else {
+    cl.sync();  // every CTA of the cluster is running before any remote access
+  }
+  // the window slot of bin b (0..2 theta's, 3..5 tau's), -1 outside both
+  auto wslot = [&](int b) {
+    const uint32_t d1 = (uint32_t)(b - w1), dt = (uint32_t)(b - wt);
+    return d1 < 3u ? (int)d1 : dt < 3u ? 3 + (int)dt : -1;
+  };
 
   // 1. per owned head, the 12-bit histogram: theta_h's bin, and from the counts
   //    alone this head's share of the competition's 12-bit histogram (the bins
@@ -386,7 +535,16 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
   for (int h = rank, j = 0; h < H; h += CL, ++j) {
     for (int e = threadIdx.x; e < kBins; e += NT) dy.h.hist[e] = 0u;
     __syncthreads();
-    for_head(zmid(h), flat0(h), n, [&](uint32_t ok, uint32_t) { atomicAdd(&dy.h.hist[ok >> kBinShift32], 1u); });
+    if (pred) {
+      for_head(zmid(h), flat0(h), n, [&](uint32_t ok, uint32_t) {
+        const int b = (int)(ok >> kBinShift32);
+        atomicAdd(&dy.h.hist[b], 1u);
+        const int sl = wslot(b);
+        if (sl >= 0) atomicAdd(&sm.wsub[sl][(ok >> kSubShift32) & 255u], 1u);
+      });
+    } else {
+      for_head(zmid(h), flat0(h), n, [&](uint32_t ok, uint32_t) { atomicAdd(&dy.h.hist[ok >> kBinShift32], 1u); });
+    }
     __syncthreads();
     {
       // negative scores have keys below 2^31: bins [0, kBins / 2)
@@ -412,18 +570,7 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
       else if (e == b1) dy.h.comp[e] += dy.h.hist[e] - (uint32_t)need1;
     __syncthreads();  // hist serves the next head
   }
-  {
-    // per group of 64 bins, this CTA's competition counts (8 threads a group)
-    static_assert(kGroups * 8 == NT && kBins == kGroups * 64, "group layout");
-    const int g = threadIdx.x >> 3, part = threadIdx.x & 7;
-    uint32_t c = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) c += dy.h.comp[g * 64 + part * 8 + i];
-    c += __shfl_xor_sync(0xFFFFFFFFu, c, 1);
-    c += __shfl_xor_sync(0xFFFFFFFFu, c, 2);
-    c += __shfl_xor_sync(0xFFFFFFFFu, c, 4);
-    if (part == 0) sm.ccoarse[g] = c;
-  }
+  group_sums(dy.h.comp, sm.ccoarse);  // this CTA's competition counts per group
   cl.sync();  // every competition histogram complete
 
   // 2. tau's bin from the cluster's sum; one stream per owned head takes the
@@ -431,64 +578,10 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
   //    of tau's bin (all of whose pairs are then below theta_h)
   int bt = -1, needt1 = 0;
   if (extra > 0) {
-    // warp 0, from the cluster's sums taken from the top: the group of bins
-    // where the count reaches `extra`, then the bin inside it (4 KB of remote
-    // reads instead of every rank's 4096 bins)
-    if (warp == 0) {
-      const uint32_t need = (uint32_t)extra;
-      uint32_t c0 = 0, c1 = 0;  // lane l: groups 63 - 2l and 62 - 2l
-#pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r)
-        if (r < CL) {
-          const uint32_t *cc = cl.map_shared_rank(sm.ccoarse, r);
-          c0 += cc[kGroups - 1 - 2 * lane];
-          c1 += cc[kGroups - 2 - 2 * lane];
-        }
-      uint32_t incl = c0 + c1;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-        if (lane >= off) incl += y;
-      }
-      uint32_t above = incl - (c0 + c1);
-      bool has = above < need && need <= incl;
-      int G = 0;
-      uint32_t aboveG = 0;
-      if (has) {
-        if (need <= above + c0) {
-          G = kGroups - 1 - 2 * lane;
-          aboveG = above;
-        } else {
-          G = kGroups - 2 - 2 * lane;
-          aboveG = above + c0;
-        }
-      }
-      const int src = (__ffs(__ballot_sync(0xFFFFFFFFu, has)) - 1) & 31;
-      G = __shfl_sync(0xFFFFFFFFu, G, src);
-      aboveG = __shfl_sync(0xFFFFFFFFu, aboveG, src);
-      uint32_t f0 = 0, f1 = 0;  // lane l: bins 64G + 63 - 2l and 64G + 62 - 2l
-      const int e0 = G * 64 + 63 - 2 * lane;
-#pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r)
-        if (r < CL) {
-          const uint32_t *cc = cl.map_shared_rank(dy.h.comp, r);
-          f0 += cc[e0];
-          f1 += cc[e0 - 1];
-        }
-      incl = f0 + f1;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-        if (lane >= off) incl += y;
-      }
-      above = aboveG + incl - (f0 + f1);
-      has = above < need && need <= aboveG + incl;
-      if (has) {
-        const bool first = need <= above + f0;
-        sm.bin = first ? e0 : e0 - 1;
-        sm.need = (int)(need - (first ? above : above + f0));
-      }
-    }
+    // from the cluster's sums taken from the top: the group of bins where the
+    // count reaches `extra`, then the bin inside it (4 KB of remote reads
+    // instead of every rank's 4096 bins)
+    if (warp == 0) cluster_boundary(cl, CL, dy.h.comp, sm.ccoarse, (uint32_t)extra, sm);
     __syncthreads();
     bt = sm.bin;
     needt1 = sm.need;
@@ -499,17 +592,25 @@ __global__ __launch_bounds__(NT, 2) void select_budget_kernel(
     const int b1 = sm.b1[j];
     const int bc = bt < b1 ? bt : -2;  // tau's bin when below theta_h's (-2: no bin)
     if (b1 == kBins && bc < 0) continue;  // uniform over the CTA: nothing to count
-    for (int d = threadIdx.x; d < 256; d += NT) sm.h8[d] = 0u;
+    // digits the first stream took (predicted bins); the stream takes the rest
+    const int s1 = pred && b1 < kBins ? wslot(b1) : -1;
+    const int sc = pred && bc >= 0 ? wslot(bc) : -1;
+    const int b1s = b1 < kBins && s1 < 0 ? b1 : -1;
+    const int bcs = bc >= 0 && sc < 0 ? bc : -2;
+    for (int d = threadIdx.x; d < 256; d += NT) sm.h8[d] = s1 >= 0 ? sm.wsub[s1][d] : 0u;
+    if (sc >= 0)
+      for (int d = threadIdx.x; d < 256; d += NT) h8c[d] += sm.wsub[sc][d];
     __syncthreads();
-    const int b1s = b1 < kBins ? b1 : -1;
-    auto digits = [&](uint32_t ok, uint32_t) {
-      const int b = (int)(ok >> kBinShift32);
-      const bool in1 = b == b1s;
-      if (in1 || b == bc) atomicAdd(&sm.h8[(in1 ? 0u : 256u) + ((ok >> kSubShift32) & 255u)], 1u);
-    };
-    if (sm.nonneg[j]) for_head<true>(zmid(h), flat0(h), n, digits);
-    else for_head<false>(zmid(h), flat0(h), n, digits);
-    __syncthreads();
+    if (b1s >= 0 || bcs >= 0) {
+      auto digits = [&](uint32_t ok, uint32_t) {
+        const int b = (int)(ok >> kBinShift32);
+        const bool in1 = b == b1s;
+        if (in1 || b == bcs) atomicAdd(&sm.h8[(in1 ? 0u : 256u) + ((ok >> kSubShift32) & 255u)], 1u);
+      };
+      if (sm.nonneg[j]) for_head<true>(zmid(h), flat0(h), n, digits);
+      else for_head<false>(zmid(h), flat0(h), n, digits);
+      __syncthreads();
+    }
     if (b1 < kBins) {
       if (warp == 0) digit_boundary(sm.h8, sm.need1[j], (uint64_t)b1 << kBinShift, kSubShift, sm.rx);
       __syncthreads();
