@@ -24,14 +24,18 @@
 // hundreds) are gathered on chip for an exact radix select.
 //
 // One thread-block cluster per row; CTA c of the cluster owns heads c, c+CL, ...
-// Three streams over each owned head's scores, then the output:
-//   1. the 12-bit histogram: theta_h's bin and how many of its pairs reach
-//      theta_h.  The competition's 12-bit histogram (pairs below theta_h)
-//      follows from these counts alone; summed over the cluster through
-//      distributed shared memory it gives tau's bin;
+// Up to three streams over each owned head's scores, then the output:
+//   0. (one head per CTA) a sample of every 16th vector predicts theta_h's bin
+//      and, summed over the cluster, tau's bin;
+//   1. the 12-bit histogram (and the second digits of the predicted bins):
+//      theta_h's bin and how many of its pairs reach theta_h.  The
+//      competition's 12-bit histogram (pairs below theta_h) follows from these
+//      counts alone; summed over the cluster through distributed shared memory
+//      it gives tau's bin;
 //   2. the second digits of theta_h's bin, and of tau's bin where that lies
 //      below theta_h's (where the two bins are one, the competition's digits
-//      follow from theta_h's); summed over the cluster they give tau's bucket;
+//      follow from theta_h's), streamed only where step 1 did not take them;
+//      summed over the cluster they give tau's bucket;
 //   3. the gather of theta_h's bucket and of tau's bucket, counting per warp
 //      range the pairs above each and recording in a shared-memory bitmask the
 //      pairs above the lower of the two buckets (kept whatever the thresholds);
