@@ -214,3 +214,39 @@ def test_compact_ragged_leaves_spare_slots_and_rejects_overfull_heads(oracle_mod
         oracle_mod.compact_ragged(K, K, None, idx, off, 4)           # head 1 keeps 5 > cap
     with pytest.raises(ValueError):
         oracle_mod.compact_ragged(K, K, None, idx, np.array([[0, 5, 3]], np.int32), 6)
+
+
+@pytest.mark.parametrize("H,T,budget,floor,R,S,signed", [
+    (8, 300, 8 * 40, 20, 8, 4, False),
+    (8, 300, 8 * 40, 12, 8, 4, True),
+    (5, 97, 5 * 30, 29, 0, 0, False),
+    (3, 64, 3 * 64, 10, 2, 1, True),      # everything kept
+    (4, 200, 4 * 30, 30, 5, 3, False),    # budget = H * floor: no competition
+])
+def test_threshold_decomposition_equals_the_oracle(oracle_mod, H, T, budget, floor, R, S, signed):
+    """The identity the GPU kernel is built on, checked against the oracle's own
+    selection: with the order (z desc, head asc, position asc) over a row's
+    middle pairs, theta_h the (floor-S-R)-th best pair of head h and tau the
+    (budget - H*floor)-th best pair among those below their head's theta_h,
+    head h keeps exactly its middle pairs at or above min(theta_h, tau)."""
+    rng = np.random.default_rng(H * T + budget)
+    z = rng.standard_normal((H, T)) if signed else np.round(rng.random((H, T)) * 40) / 40
+    n, nf = T - R - S, floor - R - S
+    extra = budget - H * floor
+    # rank of every middle pair in the row order (0 = best)
+    hs, ps = np.meshgrid(np.arange(H), np.arange(S, T - R), indexing="ij")
+    hs, ps = hs.ravel(), ps.ravel()
+    order = np.lexsort((ps, hs, -z[hs, ps]))
+    rank = np.empty(len(order), dtype=np.int64)
+    rank[order] = np.arange(len(order))
+    rank = rank.reshape(H, n)
+    # -1: no floor / no competition ("selects nothing": no rank is <= -1)
+    theta = np.array([np.sort(rank[h])[nf - 1] if nf > 0 else -1 for h in range(H)])
+    below = np.concatenate([rank[h][rank[h] > theta[h]] for h in range(H)])
+    tau = np.sort(below)[extra - 1] if extra > 0 else -1
+    idx, off = oracle_mod.select_budget(z[None], budget, floor, R, S)
+    for h in range(H):
+        lam = max(theta[h], tau)  # ranks: smaller is better, so min over keys is max over ranks
+        mid = [S + i for i in range(n) if rank[h, i] <= lam]
+        want = list(range(S)) + mid + list(range(T - R, T))
+        assert list(idx[0, off[0, h]:off[0, h + 1]]) == want, h
